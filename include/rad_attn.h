@@ -1,0 +1,175 @@
+/*
+ * rad_attn.h -- C ABI of the paged-KV attention library (GB300, sm_103a).
+ *
+ * One operation: attention of a batch of query rows against a paged KV cache,
+ * the `attn_paged` op of "Radiance architecture plugins -- declaring a model"
+ * (section "Declare: the metadata", RadBuildCtx `attn_prefill_fp8`: "pass as
+ * attn_paged's prefill_fp8").  The call shapes are those of "kern manifest v7",
+ * $defs.Batch: a decode step (`groups` sequences x `rows` = 1), a speculative
+ * verify round (`rows` = 8, causal within the round) and a prefill chunk
+ * (`groups` = 1, `rows` = the chunk's tokens, over the cached context).
+ *
+ * Definition (for each group g, row r < rows, query head h < n_head):
+ *   kv    = h / (n_head / n_head_kv)                 (grouped-query heads)
+ *   n     = seq_lens[g] - rows + r + 1               (keys row r may see)
+ *   key j < n is token slot j % page_size of physical page
+ *           page_table[g * pages_per_seq + j / page_size]
+ *   out[g][r][h][:] = sum_j softmax_j(scale * q[g][r][h][:] . K_j) * V_j
+ * with K_j = K[page][slot][kv][:] (times k_scales[page] for fp8) and likewise
+ * V.  seq_lens is "each sequence's length after this call (rows already in the
+ * state plus this call's)" (kern manifest v7, $defs.Fill `seq_len`), so the
+ * K/V rows of this call's own tokens must already be in the pool: writing
+ * them (the `slot` fill of $defs.Fill) is the caller's job.
+ *
+ * Layouts (all row-major, innermost dimension contiguous):
+ *   q, out      bf16 [groups][rows][n_head][head_dim]
+ *   k_pool      [num_pages][page_size][n_head_kv][head_dim], bf16 or e4m3
+ *   v_pool      same layout and dtype as k_pool
+ *   page_table  int32 [groups][pages_per_seq]; entries past a sequence's
+ *               last page are never read
+ *   seq_lens    int32 [groups]
+ *   k_scales, v_scales  fp32 [num_pages], fp8 pools only: element value =
+ *               e4m3 code * scale of its physical page (one scale per page
+ *               and pool, shared by every slot and KV head of the page)
+ * The pool layout is the host-allocated paged state of kern manifest v7
+ * ($defs.HostTensor / $defs.State `host`: a strided tensor whose outermost
+ * extent is the host's page count), with the page table as the input whose
+ * domain indexes it with `stride` = page_size token slots per entry
+ * ($defs.Domain).
+ *
+ * Ownership: every pointer is caller-owned device memory (except where a
+ * comment says otherwise).  The library allocates nothing, keeps no per-call
+ * state, never synchronises the stream and never reads seq_lens or the page
+ * table on the host, so a call can be captured in a CUDA graph (kern
+ * manifest v7, $defs.Program `graph`: decode and verify programs are
+ * replayed from a captured graph).  Work is ordered on `stream`.
+ *
+ * Row invariance: each output row is a function of its own sequence's data,
+ * seq_len and the call's shape scalars (rows, head counts, head_dim,
+ * page_size, kv dtype) only -- never of `groups`, of the other sequences or of
+ * their order ("Adding a model", step 4: every verified row must equal the
+ * decode step's row bit for bit, or speculation is not lossless).
+ */
+#ifndef RAD_ATTN_H
+#define RAD_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA runtime's cudaStream_t is `struct CUstream_st *`; NULL is the
+ * legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st* rad_stream_t;
+
+/* Synchronous status codes.  On any nonzero code nothing was written and
+ * nothing was launched, except RAD_E_CUDA (a launch was attempted and the
+ * runtime refused it). */
+enum {
+    RAD_OK = 0,
+    RAD_E_SHAPE = 1,     /* groups or rows == 0 ("zero rows is not a call":
+                            Radiance architecture plugins, section "Step:
+                            issuing the graph"); n_head not a multiple of
+                            n_head_kv; a size < 1; num_pages*page_size
+                            beyond 2^31-1 */
+    RAD_E_DTYPE = 2,     /* head_dim not 128/256, page_size not 16/32, or an
+                            unknown kv_dtype: refused by name, never
+                            substituted (Radiance architecture plugins,
+                            section "Probe": a switch that cannot be honoured
+                            is an error, never a silent substitution) */
+    RAD_E_ARG = 3,       /* a required pointer is NULL, a pool, q or out
+                            pointer is not 16-byte aligned, or fp8 without
+                            scale arrays */
+    RAD_E_WORKSPACE = 4, /* workspace NULL or smaller than
+                            rad_attn_paged_workspace_bytes() */
+    RAD_E_CUDA = 5,      /* the CUDA runtime refused a launch or a query */
+    RAD_E_DEVICE = 6     /* the current device is not sm_103 (GB300) */
+};
+
+/* KV cache element types ("kern manifest v7", $defs.DType: bf16, fp8e4m3). */
+enum { RAD_KV_BF16 = 0, RAD_KV_FP8_E4M3 = 1 };
+
+/* Device-side error bits, OR-ed into *err_word by the kernel ("kern manifest
+ * v7", $defs.Fill `error`: a one-word error flag read after every call;
+ * nonzero is a failed step).  A group that raises RAD_ERRW_SEQLEN or
+ * RAD_ERRW_PAGE gets all-zero output rows; the other groups are unaffected.
+ * No out-of-bounds access happens in either case. */
+enum {
+    RAD_ERRW_SEQLEN = 1u,  /* seq_lens[g] < rows or > pages_per_seq*page_size */
+    RAD_ERRW_PAGE = 2u,    /* a page id the group needs is outside [0, num_pages) */
+    RAD_ERRW_QRANGE = 4u,  /* fp8 pools: a q element beyond the f16 range
+                              (|q| > 65504) -- that row's output is not
+                              meaningful */
+    RAD_ERRW_TIMEOUT = 8u  /* an internal wait ran past its time limit; the
+                              affected outputs are not meaningful */
+};
+
+/*
+ * Bytes of scratch memory `rad_attn_paged` needs for a call of this shape
+ * (0 is possible).  A pure function of its arguments; no device access.
+ * Returns 0 as well for shapes rad_attn_paged would refuse.  The workspace
+ * holds per-split partial results ("kern manifest v7", $defs.Impl `scratch`:
+ * implementation-private buffers) and is dead between calls; calls that may
+ * run concurrently need separate workspaces.
+ */
+size_t rad_attn_paged_workspace_bytes(int32_t groups, int32_t rows, int32_t n_head,
+                                      int32_t n_head_kv, int32_t head_dim, int32_t page_size,
+                                      int32_t pages_per_seq, int32_t kv_dtype);
+
+/*
+ * Launches the op on `stream`.  Arguments:
+ *   q, k_pool, v_pool, page_table, seq_lens, out: device pointers, layouts above
+ *   groups        sequences in the call (>= 1)
+ *   rows          query rows per sequence (>= 1): 1 decode, 8 verify, the
+ *                 chunk length for a prefill
+ *   n_head, n_head_kv  query and KV heads (n_head % n_head_kv == 0)
+ *   head_dim      128 or 256, as read from the model metadata -- never derived
+ *                 from hidden size / heads (Radiance architecture plugins,
+ *                 section "Declare: the metadata")
+ *   page_size     token slots per page: 16 or 32
+ *   pages_per_seq page-table row stride (entries per sequence, >= 1)
+ *   num_pages     pages in each pool (bounds for page ids)
+ *   scale         logit scale (usually 1/sqrt(head_dim))
+ *   kv_dtype      RAD_KV_BF16 or RAD_KV_FP8_E4M3
+ *   k_scales, v_scales  fp8: device fp32 [num_pages]; bf16: ignored (may be NULL)
+ *   workspace, workspace_bytes  device scratch of at least
+ *                 rad_attn_paged_workspace_bytes(...) bytes (may be NULL when
+ *                 that is 0); its contents need no initialisation
+ *   err_word      optional device uint32 the kernel ORs RAD_ERRW_* bits into
+ *                 (the caller zeroes it); NULL disables reporting
+ *   stream        CUDA stream (cudaStream_t)
+ * Returns RAD_OK or a status code above.
+ */
+int rad_attn_paged(const void* q, const void* k_pool, const void* v_pool,
+                   const int32_t* page_table, const int32_t* seq_lens, int32_t groups,
+                   int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_dim,
+                   int32_t page_size, int32_t pages_per_seq, int32_t num_pages, float scale,
+                   int32_t kv_dtype, const float* k_scales, const float* v_scales, void* out,
+                   void* workspace, size_t workspace_bytes, uint32_t* err_word,
+                   rad_stream_t stream);
+
+/*
+ * Writes a one-line, NUL-terminated description of the kernel a call of this
+ * shape would launch (family, tile, split length, stages) into buf (host
+ * memory, buf_len bytes) -- the pattern of "Radiance architecture plugins",
+ * section "Verifying a new plugin" (`--debug-graph`: every op, its resolved
+ * kernel, and why).  Returns the same status a call of this shape would get
+ * from its scalar checks.  No device access.
+ */
+int rad_attn_paged_describe(int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_dim,
+                            int32_t page_size, int32_t kv_dtype, char* buf, size_t buf_len);
+
+/* Static, NUL-terminated name of a status code ("RAD_E_SHAPE", ...). */
+const char* rad_attn_status_string(int status);
+
+/* Static, NUL-terminated library version string. */
+const char* rad_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RAD_ATTN_H */

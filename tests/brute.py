@@ -1,0 +1,48 @@
+"""Brute-force attention with Python lists and math.exp (test helper).
+
+An independent second route to the op's result, used only to pin the oracle
+on tiny inputs.  It takes the K/V rows of one sequence already gathered into
+contiguous lists (no page table) and plain Python floats, and writes out the
+definition with explicit positions:
+
+    row r of a call with R rows over a sequence of final length L sits at
+    position L - R + r and sees keys 0 .. L - R + r (kern manifest v7,
+    $defs.Fill `seq_len`); query head h reads KV head h // (H / Hkv).
+"""
+import math
+
+
+def attend_sequence(q_rows, keys, values, scale, n_head_kv):
+    """q_rows: [R][H][D] floats; keys/values: [L][Hkv][D] floats.
+
+    Returns out [R][H][D] as floats.
+    """
+    R = len(q_rows)
+    H = len(q_rows[0])
+    L = len(keys)
+    group = H // n_head_kv
+    out = []
+    for r in range(R):
+        position = L - R + r
+        row_out = []
+        for h in range(H):
+            kvh = h // group
+            logits = []
+            for j in range(position + 1):
+                acc = 0.0
+                for a, b in zip(q_rows[r][h], keys[j][kvh]):
+                    acc += a * b
+                logits.append(scale * acc)
+            top = max(logits)
+            ex = [math.exp(x - top) for x in logits]
+            total = sum(ex)
+            D = len(values[0][kvh])
+            vec = [0.0] * D
+            for j, e in enumerate(ex):
+                wgt = e / total
+                vj = values[j][kvh]
+                for d in range(D):
+                    vec[d] += wgt * vj[d]
+            row_out.append(vec)
+        out.append(row_out)
+    return out
