@@ -1,0 +1,403 @@
+#!/usr/bin/env python
+"""Benchmark of paged-KV attention on one GB300 per process.
+
+Workload (default): the batched decode step -- 256 sequences x rows=1,
+n_head=32, n_head_kv=8, head_dim=128, page_size=16, context lengths uniform in
+[512, 8192], bf16 KV ~ N(0,1), random-permutation page table (seeded).  A step
+is one rad_attn_paged call over the whole batch (split kernel + in-kernel
+combine), replayed from a CUDA graph as a decode program is.
+
+Metric: KV bytes read per second (GB/s), the algorithmic bytes of one call --
+every visible key's K and V rows for every KV head, plus page-table entries
+(and per-page scales for fp8) -- divided by the device time of a call.  Also
+reported: context tokens attended per second, rows per second, and the
+fraction of the measured HBM copy bandwidth.
+
+Under torchrun (N > 1) every rank runs its own independent batch (its own
+seed): the op shards by sequence with no data-path exchange, so scaling is
+weak; `value` is the sum of all ranks' bytes over the slowest rank's time.
+
+--impl reference times the fp64 CPU oracle (the only other implementation of
+the op there is) on a bounded sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from dataclasses import replace
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_attention_02_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "paged-decode KV GB/s and seq-tokens/s (fraction of GB300 HBM peak) at 1 GPU"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM traffic per launch from the committed ncu capture (profiles/), valid only
+# while the kernel sources hash to `src_sha256`.
+NCU_TRAFFIC: dict[str, dict] = {}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "paged_kv_attention_02_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="batched_decode", choices=sorted(wl.CONFIGS))
+    ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of graph replay")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- distributed plumbing
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def rank_config(name: str, rank: int) -> wl.Config:
+    """Each rank draws its own batch (weak scaling): rank r uses seed + 1000 r."""
+    cfg = wl.CONFIGS[name]
+    return cfg if rank == 0 else replace(cfg, seed=cfg.seed + 1000 * rank)
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int, period_ms: int = 50):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 f"-lms={period_ms}", f"-i={device_index}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        win = [p for (t, p) in self.samples if t0 <= t <= t1]
+        if not win and self.samples:   # a very short window: the nearest samples
+            win = [min(self.samples, key=lambda s: abs(s[0] - (t0 + t1) / 2))[1]]
+        mhz = [num(p[1]) for p in win if num(p[1]) is not None]
+        mx = [num(p[2]) for p in win if num(p[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in win:
+            for i, n in enumerate(names):
+                if p[5 + i].lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(win)}
+
+
+# ---------------------------------------------------------------- peaks
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------- oracle timing (CPU)
+def time_oracle(w: wl.Workload, groups_idx) -> tuple[float, int]:
+    import oracle
+    sub = w.select_groups(groups_idx)
+    t0 = time.perf_counter()
+    oracle.attn_paged_rows(sub.q, sub.k_pool, sub.v_pool, sub.page_table, sub.seq_lens,
+                           k_scales=sub.k_scales, v_scales=sub.v_scales, **sub.call_args())
+    return time.perf_counter() - t0, wl.kv_bytes(sub)
+
+
+def cpu_baseline(w: wl.Workload, budget_s: float) -> dict:
+    import oracle
+    oracle.build()
+    t1, _ = time_oracle(w, [0])
+    n = int(max(1, min(w.groups, budget_s / max(t1, 1e-3))))
+    idx = list(range(n))
+    dt, nbytes = time_oracle(w, idx)
+    return {"value": nbytes / dt / 1e9, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{n} of {w.groups} sequences (all rows and heads), one oracle call, fp64",
+            "seconds": round(dt, 3)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = wl.make_workload(rank_config(args.workload, 0))
+    t1, _ = time_oracle(w, [0])
+    per_step = max(0.2, min(3.0, 150.0 / max(1, args.steps + args.warmup)))
+    n = int(max(1, min(w.groups, per_step / max(t1, 1e-3))))
+    rng = np.random.default_rng(12345)
+    for _ in range(args.warmup):
+        time_oracle(w, rng.choice(w.groups, n, replace=False))
+    total_t, total_b = 0.0, 0
+    for _ in range(args.steps):
+        dt, nb = time_oracle(w, rng.choice(w.groups, n, replace=False))
+        total_t += dt
+        total_b += nb
+    value = total_b / total_t / 1e9
+    cores = oracle.max_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{n} random sequences of {w.groups} per step, all rows and heads"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+def workload_config(w: wl.Workload) -> dict:
+    c = w.cfg
+    return {"workload": f"{c.name}: {w.groups} seqs x rows={c.rows}, n_head={c.n_head}, "
+                        f"n_head_kv={c.n_head_kv}, head_dim={c.head_dim}, page_size={c.page_size}, "
+                        f"ctx {c.lens}, {'fp8-e4m3' if c.kv_dtype else 'bf16'} KV, seed {c.seed}",
+            "groups": w.groups, "rows": c.rows, "n_head": c.n_head, "n_head_kv": c.n_head_kv,
+            "head_dim": c.head_dim, "page_size": c.page_size, "num_pages": w.num_pages,
+            "kv_pool_bytes": int(w.k_pool.nbytes + w.v_pool.nbytes),
+            "l2": "inputs larger than L2 (no flush): the KV pools exceed the 129 MB L2"}
+
+
+def run_ours(args, rank, world, local):
+    from paged_kv_attention_02_gb300 import binding as b
+    from paged_kv_attention_02_gb300.build import build_library
+
+    build_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = wl.make_workload(rank_config(args.workload, rank))
+    c = w.cfg
+    fp8 = c.kv_dtype == wl.KV_FP8_E4M3
+
+    def to_dev(a, as_bf16=False):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if as_bf16:
+            t = t.view(torch.int16).view(torch.bfloat16)
+        return t.to(dev)
+
+    q = to_dev(w.q.view(np.int16), True)
+    k = to_dev(w.k_pool) if fp8 else to_dev(w.k_pool.view(np.int16), True)
+    v = to_dev(w.v_pool) if fp8 else to_dev(w.v_pool.view(np.int16), True)
+    ks = to_dev(w.k_scales) if fp8 else None
+    vs = to_dev(w.v_scales) if fp8 else None
+    table = to_dev(w.page_table)
+    lens = to_dev(w.seq_lens)
+    out = torch.empty((w.groups, c.rows, c.n_head, c.head_dim), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(1, b.workspace_bytes(w.groups, c.rows, c.n_head, c.n_head_kv, c.head_dim,
+                                               c.page_size, w.pages_per_seq, c.kv_dtype)),
+                     dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def call(qq=q, tt=table, ll=lens, oo=out):
+        b.attn_paged(qq, k, v, tt, ll, rows=c.rows, n_head=c.n_head, n_head_kv=c.n_head_kv,
+                     head_dim=c.head_dim, page_size=c.page_size, scale=c.scale, kv_dtype=c.kv_dtype,
+                     k_scales=ks, v_scales=vs, out=oo, workspace=ws, err_word=err, stream=stream)
+
+    with torch.cuda.stream(stream):
+        call()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, f"error word {int(err.item())}"
+
+    step = call
+    if not args.no_graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            call()
+        step = g.replay
+
+    sampler = ClockSampler(local)
+    # ---- device-resident timing
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    torch.cuda.synchronize()
+    barrier(world)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    barrier(world)
+    ms = ev0.elapsed_time(ev1) / args.steps
+    clocks = sampler.summary(wall0, wall1)
+    sampler.stop()
+    assert int(err.item()) == 0
+
+    # ---- end to end: per-step inputs from pinned host memory, result back to host
+    q_h = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16).pin_memory()
+    t_h = torch.from_numpy(w.page_table).pin_memory()
+    l_h = torch.from_numpy(w.seq_lens).pin_memory()
+    o_h = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+    q_d, t_d, l_d = torch.empty_like(q), torch.empty_like(table), torch.empty_like(lens)
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        t_d.copy_(t_h, non_blocking=True)
+        l_d.copy_(l_h, non_blocking=True)
+        call(q_d, t_d, l_d, out)
+        o_h.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    h2d = q_h.numel() * 2 + t_h.numel() * 4 + l_h.numel() * 4
+    d2h = o_h.numel() * 2
+
+    nbytes = wl.kv_bytes(w)
+    tokens = int(w.seq_lens.astype(np.int64).sum())
+    ms_max = reduce_max(ms, world)
+    e2e_max = reduce_max(e2e_ms, world)
+    tot_bytes = reduce_sum(float(nbytes), world)
+    tot_tokens = reduce_sum(float(tokens), world)
+    tot_rows = reduce_sum(float(w.groups * c.rows), world)
+    if rank != 0:
+        return
+    value = tot_bytes / (ms_max * 1e-3) / 1e9
+    peak, peak_src = hbm_peak()
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    tr = NCU_TRAFFIC.get(c.name)
+    traffic = tr["bytes_per_launch"] if tr and tr.get("src_sha256") == kernel_source_hash() else None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8e4m3" if fp8 else "bf16", "data": "synthetic",
+        "config": dict(workload_config(w), graph=not args.no_graph),
+        "seq_tokens_per_s": tot_tokens / (ms_max * 1e-3),
+        "rows_per_s": tot_rows / (ms_max * 1e-3),
+        "hbm_frac": value / world / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": nbytes},
+        "clocks": clocks,
+        "e2e": {"value": tot_bytes / (e2e_max * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": e2e_max,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "KV pools resident (persistent state); q, page table, seq_lens in and out back per step"},
+        "gpu_launches": args.steps,
+        "kernel": b.describe(c.rows, c.n_head, c.n_head_kv, c.head_dim, c.page_size, c.kv_dtype),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,142 @@
+"""Python binding of the C ABI in include/rad_attn.h (argument marshalling only).
+
+Every step of the op runs in the CUDA library ``_lib/librad_attn.so``; this
+module only turns torch tensors into pointers, sizes and a stream, and turns
+status codes into exceptions.  If the library is missing it raises -- there is
+no fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB_PATH
+
+RAD_OK = 0
+RAD_E_SHAPE = 1
+RAD_E_DTYPE = 2
+RAD_E_ARG = 3
+RAD_E_WORKSPACE = 4
+RAD_E_CUDA = 5
+RAD_E_DEVICE = 6
+
+RAD_KV_BF16 = 0
+RAD_KV_FP8_E4M3 = 1
+
+RAD_ERRW_SEQLEN = 1
+RAD_ERRW_PAGE = 2
+RAD_ERRW_QRANGE = 4
+RAD_ERRW_TIMEOUT = 8
+
+EXPORTS = ("rad_attn_paged", "rad_attn_paged_workspace_bytes", "rad_attn_paged_describe",
+           "rad_attn_status_string", "rad_attn_version")
+
+_lib = None
+
+
+class RadAttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+        self.status = status
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Loads the library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built: {path} is missing (run __graft_entry__.build())")
+    lib = ctypes.CDLL(path)
+    i32, p, sz = ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t
+    lib.rad_attn_paged.restype = ctypes.c_int
+    lib.rad_attn_paged.argtypes = [p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, i32,
+                                   ctypes.c_float, i32, p, p, p, p, sz, p, p]
+    lib.rad_attn_paged_workspace_bytes.restype = sz
+    lib.rad_attn_paged_workspace_bytes.argtypes = [i32] * 8
+    lib.rad_attn_paged_describe.restype = ctypes.c_int
+    lib.rad_attn_paged_describe.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.c_char_p, sz]
+    lib.rad_attn_status_string.restype = ctypes.c_char_p
+    lib.rad_attn_status_string.argtypes = [ctypes.c_int]
+    lib.rad_attn_version.restype = ctypes.c_char_p
+    lib.rad_attn_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().rad_attn_status_string(int(status)).decode()
+
+
+def version() -> str:
+    return load().rad_attn_version().decode()
+
+
+def workspace_bytes(groups, rows, n_head, n_head_kv, head_dim, page_size, pages_per_seq,
+                    kv_dtype=RAD_KV_BF16) -> int:
+    return int(load().rad_attn_paged_workspace_bytes(groups, rows, n_head, n_head_kv, head_dim,
+                                                      page_size, pages_per_seq, kv_dtype))
+
+
+def describe(rows, n_head, n_head_kv, head_dim, page_size, kv_dtype=RAD_KV_BF16) -> str:
+    buf = ctypes.create_string_buffer(512)
+    rc = load().rad_attn_paged_describe(rows, n_head, n_head_kv, head_dim, page_size, kv_dtype, buf,
+                                        len(buf))
+    if rc != RAD_OK:
+        raise RadAttnError(rc, "rad_attn_paged_describe")
+    return buf.value.decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def attn_paged(q, k_pool, v_pool, page_table, seq_lens, *, rows, n_head, n_head_kv, head_dim,
+               page_size, scale, kv_dtype=RAD_KV_BF16, k_scales=None, v_scales=None, out=None,
+               workspace=None, err_word=None, stream=None):
+    """Launches rad_attn_paged on `stream` (default: torch's current stream).
+
+    q: bf16 [groups, rows, n_head, head_dim]; k_pool / v_pool: bf16 or uint8 (e4m3
+    codes) [num_pages, page_size, n_head_kv, head_dim]; page_table: int32
+    [groups, pages_per_seq]; seq_lens: int32 [groups]; k_scales / v_scales:
+    float32 [num_pages] for fp8.  Returns `out` (bf16, allocated if None).
+    A workspace is allocated with torch when none is given.
+    """
+    groups = int(seq_lens.shape[0])
+    pages_per_seq = int(page_table.shape[1])
+    num_pages = int(k_pool.shape[0])
+    if out is None:
+        out = torch.empty((groups, rows, n_head, head_dim), dtype=torch.bfloat16, device=q.device)
+    need = workspace_bytes(groups, rows, n_head, n_head_kv, head_dim, page_size, pages_per_seq, kv_dtype)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().rad_attn_paged(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(seq_lens), groups, rows, n_head,
+        n_head_kv, head_dim, page_size, pages_per_seq, num_pages, float(scale), kv_dtype,
+        _ptr(k_scales), _ptr(v_scales), _ptr(out), _ptr(workspace), ws_bytes, _ptr(err_word),
+        _stream_handle(stream))
+    if rc != RAD_OK:
+        raise RadAttnError(rc, "rad_attn_paged")
+    return out
+
+
+def call_raw(q_ptr, k_ptr, v_ptr, table_ptr, lens_ptr, groups, rows, n_head, n_head_kv, head_dim,
+             page_size, pages_per_seq, num_pages, scale, kv_dtype, ks_ptr, vs_ptr, out_ptr, ws_ptr,
+             ws_bytes, err_ptr, stream_ptr) -> int:
+    """The C call with raw integer pointers (for boundary tests); returns the status."""
+    def vp(x):
+        return ctypes.c_void_p(x) if x else None
+    return int(load().rad_attn_paged(
+        vp(q_ptr), vp(k_ptr), vp(v_ptr), vp(table_ptr), vp(lens_ptr), groups, rows, n_head, n_head_kv,
+        head_dim, page_size, pages_per_seq, num_pages, float(scale), kv_dtype, vp(ks_ptr), vp(vs_ptr),
+        vp(out_ptr), vp(ws_ptr), ws_bytes, vp(err_ptr), vp(stream_ptr)))

@@ -1,0 +1,707 @@
+// Paged-KV attention tile kernel (sm_103a).
+//
+// One CTA is persistent and walks a list of work items.  A work item is
+// (split s, sequence g, KV head kvh, query tile qt): the query rows of one KV
+// head -- the `rows` rows times the n_head/n_head_kv query heads that share it
+// ("Radiance architecture plugins", section "Declare: the metadata": n_head over
+// n_head_kv) -- against one contiguous range of the sequence's keys.
+//
+// Warp roles.  The last warp is the producer: it reads page ids from the page
+// table ("kern manifest v7", $defs.Domain: `stride` token slots per entry) and
+// issues one TMA load per (page, pool) into a ring of shared-memory stages,
+// plus bulk copies of the item's query rows.  The other warps consume stages:
+//
+//   S^T[key][q] = K[key][:] . Q[q][:]          mma.m16n8k16, keys as M, query
+//                                              rows as N (8 per n-tile)
+//   online softmax over keys, per query row    fp32, exp2, warp shuffles
+//   O^T[d][q]  += V^T[d][key] P^T[key][q]      mma.m16n8k16, P^T re-laid out
+//                                              from the S^T accumulator with
+//                                              movmatrix
+//
+// Keys as the M dimension keeps a decode step (a handful of query rows per KV
+// head) at no worse than half-used n-tiles.
+//
+// Splits.  With split_len > 0 a sequence's keys are cut into ceil(L/split_len)
+// ranges whose count and boundaries depend only on L.  Each range writes a
+// partial (running max, sum, unnormalised accumulator) to the workspace; the
+// CTA that finishes a (g, kvh, qt) last -- found with an atomic ticket, no
+// waiting -- merges the partials in split order 0..n-1.  Every output row is
+// therefore the same function of its own sequence whatever else is in the
+// call ("Adding a model", step 4: verified rows must equal decode rows bit
+// for bit).
+//
+// fp8 pools (e4m3 codes, one fp32 scale per page and pool): codes are turned
+// into f16 pairs with cvt.rn.f16x2.e4m3x2 (exact), Q is rounded bf16->f16
+// (exact inside the f16 range; elements past it raise RAD_ERRW_QRANGE), the
+// page's K scale multiplies the logits and its V scale multiplies P before
+// P is rounded to f16 for the PV product.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math_constants.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace rad {
+
+// Device error bits (mirror of RAD_ERRW_* in include/rad_attn.h).
+constexpr uint32_t kErrSeqLen = 1u;
+constexpr uint32_t kErrPage = 2u;
+constexpr uint32_t kErrQRange = 4u;
+constexpr uint32_t kErrTimeout = 8u;
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+
+struct AttnParams {
+    const __nv_bfloat16* q;
+    const int32_t* page_table;
+    const int32_t* seq_lens;
+    const float* k_scales;
+    const float* v_scales;
+    __nv_bfloat16* out;
+    float* part_acc;       // [slots][qtv][D]
+    float* part_ml;        // [slots][qtv][2]  (max in log2 units, sum)
+    uint32_t* part_flag;   // [slots]         page-id error seen by the split
+    uint32_t* counters;    // [groups * n_head_kv * n_qtiles]; zero at launch
+    uint32_t* err_word;    // optional
+    int groups, rows, n_head, n_head_kv, ratio, page_size, pages_per_seq, num_pages;
+    int M;                 // rows * ratio: query rows per KV head
+    int n_qtiles;          // ceil(M / QT)
+    int qtv;               // query rows stored per partial slot: min(M, QT)
+    int max_splits;        // 1 without splitting
+    int split_len;         // keys per split; 0 = one range over the whole context
+    long long n_items;     // max_splits * groups * n_head_kv * n_qtiles
+    float scale_log2;      // scale * log2(e)
+};
+
+template <int D_, bool FP8_, int WQ_, int NQW_, int WK_, int KS_, int NS_>
+struct TileCfg {
+    static constexpr int D = D_;
+    static constexpr bool FP8 = FP8_;
+    static constexpr int WQ = WQ_;      // consumer warps along query rows
+    static constexpr int NQW = NQW_;    // 8-row query n-tiles per warp
+    static constexpr int WK = WK_;      // consumer warps along keys
+    static constexpr int KS = KS_;      // keys per stage
+    static constexpr int NS = NS_;      // stages
+    static constexpr int E = FP8 ? 1 : 2;
+    static constexpr int QT = WQ * NQW * 8;
+    static constexpr int NCW = WQ * WK;
+    static constexpr int NCT = NCW * 32;
+    static constexpr int NTHREADS = NCT + 32;
+    static constexpr int SUBS = KS / 16;
+    static constexpr int ROW_BYTES = D * E;
+    static constexpr int TILE_BYTES = KS * ROW_BYTES;
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+    static constexpr int MAX_PAGES_STAGE = KS / 16;
+    static constexpr int Q_SLOT_BYTES = QT * D * 2;
+    static constexpr int MSTRIDE = D + 4;   // floats per merge row (bank spread)
+    static constexpr int OFF_Q = NS * STAGE_BYTES;
+    static constexpr int OFF_MERGE = OFF_Q + 2 * Q_SLOT_BYTES;
+    static constexpr int OFF_ML = OFF_MERGE + WK * QT * MSTRIDE * 4;
+    static constexpr int OFF_META = OFF_ML + WK * QT * 2 * 4;
+    static constexpr int META_STRIDE = 64;  // ks[4], vs[4], bad, pad
+    static constexpr int OFF_BARS = OFF_META + NS * META_STRIDE;
+    static constexpr int OFF_MISC = OFF_BARS + (2 * NS + 4) * 8;
+    static constexpr int SMEM_USED = OFF_MISC + 16;
+    static constexpr int SMEM_BYTES = SMEM_USED + 1024;   // base alignment slack
+    static_assert(KS % 16 == 0 && SUBS % WK == 0, "stage keys must split evenly over key warps");
+    static_assert(MAX_PAGES_STAGE <= 4, "stage meta holds 4 pages");
+    static_assert(D % 32 == 0, "head_dim multiple of 32");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+struct ItemPlan {
+    int s, g, kvh, qt;
+    int L;
+    bool seq_ok;
+    bool active;
+    int n_splits;
+    int k0, k1;        // key range of the item
+    int m0, m_end;     // query rows [m0, m_end) of the KV head
+    int n_stages;
+};
+
+template <class C>
+__device__ __forceinline__ ItemPlan plan_item(long long item, const AttnParams& p) {
+    ItemPlan it;
+    const long long per_split = (long long)p.groups * p.n_head_kv * p.n_qtiles;
+    it.s = (int)(item / per_split);
+    long long rem = item - (long long)it.s * per_split;
+    const int per_g = p.n_head_kv * p.n_qtiles;
+    it.g = (int)(rem / per_g);
+    int rem2 = (int)(rem - (long long)it.g * per_g);
+    it.kvh = rem2 / p.n_qtiles;
+    it.qt = rem2 - it.kvh * p.n_qtiles;
+    if (p.split_len == 0) it.qt = p.n_qtiles - 1 - it.qt;   // causal: later tiles see more keys
+    it.L = __ldg(p.seq_lens + it.g);
+    it.seq_ok = it.L >= p.rows && (long long)it.L <= (long long)p.pages_per_seq * p.page_size;
+    it.m0 = it.qt * C::QT;
+    it.m_end = min(p.M, it.m0 + C::QT);
+    it.k0 = it.k1 = 0;
+    it.n_stages = 0;
+    it.n_splits = 1;
+    if (!it.seq_ok) {
+        it.active = (it.s == 0);
+        return it;
+    }
+    const int r_last = (it.m_end - 1) / p.ratio;
+    const int kmax = it.L - p.rows + r_last + 1;
+    if (p.split_len > 0) {
+        it.n_splits = (it.L + p.split_len - 1) / p.split_len;
+        it.active = it.s < it.n_splits;
+        it.k0 = it.s * p.split_len;
+        it.k1 = min(it.k0 + p.split_len, kmax);
+    } else {
+        it.active = (it.s == 0);
+        it.k0 = 0;
+        it.k1 = kmax;
+    }
+    if (it.k1 < it.k0) it.k1 = it.k0;
+    it.n_stages = (it.k1 - it.k0 + C::KS - 1) / C::KS;
+    return it;
+}
+
+// Column (query row index within the KV head) held by this lane.
+template <class C>
+__device__ __forceinline__ int lane_col(int wq, int j, int t4, int c) {
+    return (wq * C::NQW + j) * 8 + 2 * t4 + c;
+}
+
+// Head-dim index of accumulator row `row16` (0..15) of d-tile `mt`.
+template <class C>
+__device__ __forceinline__ int d_of(int mt, int row16) {
+    if constexpr (C::FP8) {
+        // fp8 V fragments are built so that m-tile 2b+hb, row g holds
+        // d = 32b + 4g + 2hb and row g+8 holds d = 32b + 4g + 2hb + 1.
+        const int b = mt >> 1, hb = mt & 1;
+        const int g = row16 & 7, hi = row16 >> 3;
+        return 32 * b + 4 * g + 2 * hb + hi;
+    } else {
+        return 16 * mt + row16;
+    }
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::NTHREADS, 1)
+    attn_tile_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ AttnParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (base - raw_addr);
+
+    const uint32_t bar_full = base + C::OFF_BARS;
+    const uint32_t bar_empty = bar_full + 8 * C::NS;
+    const uint32_t bar_qfull = bar_empty + 8 * C::NS;
+    const uint32_t bar_qempty = bar_qfull + 16;
+    volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::NS; ++i) {
+            mbar_init(bar_full + 8 * i, 1);
+            mbar_init(bar_empty + 8 * i, C::NCW);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_qfull + 8 * i, 1);
+            mbar_init(bar_qempty + 8 * i, C::NCW);
+        }
+        misc[0] = 0;  // abort flag (set by any warp that timed out)
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+
+    if (warp == C::NCW) {
+        // ===================================================== producer warp
+        if (lane == 0) {
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+        }
+        const uint64_t pol_kv = policy_evict_first();
+        uint32_t scount = 0, qcount = 0;
+        bool abort = false;
+        for (long long item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
+            const ItemPlan it = plan_item<C>(item, p);
+            if (!it.active || !it.seq_ok) continue;
+            // ---- query rows of the item
+            {
+                const uint32_t slot = qcount & 1u, use = qcount >> 1;
+                if (use >= 1 && !mbar_wait_bounded(bar_qempty + 8 * slot, (use - 1) & 1u, kWaitLimitNs)) {
+                    abort = true;
+                    break;
+                }
+                const int nrows = it.m_end - it.m0;
+                if (lane == 0) mbar_arrive_expect_tx(bar_qfull + 8 * slot, (uint32_t)(nrows * C::D * 2));
+                __syncwarp();
+                const uint32_t qdst = base + C::OFF_Q + slot * C::Q_SLOT_BYTES;
+                for (int i = lane; i < nrows; i += 32) {
+                    const int m = it.m0 + i;
+                    const int r = m / p.ratio, hl = m - r * p.ratio;
+                    const __nv_bfloat16* src =
+                        p.q + (((long long)it.g * p.rows + r) * p.n_head + it.kvh * p.ratio + hl) * C::D;
+                    bulk_load(qdst + i * C::D * 2, src, C::D * 2, bar_qfull + 8 * slot);
+                }
+                ++qcount;
+            }
+            // ---- KV pages of the item, batched 32 page ids at a time
+            const int P = p.page_size;
+            const int page_hi = (it.k1 + P - 1) / P;   // exclusive
+            const int32_t* trow = p.page_table + (long long)it.g * p.pages_per_seq;
+            int batch0 = -1 << 30;
+            int my_pg = 0;
+            float my_ks = 1.f, my_vs = 1.f;
+            bool my_bad = false;
+            for (int st = 0; st < it.n_stages; ++st) {
+                const int key0 = it.k0 + st * C::KS;
+                const int pstart = key0 / P;
+                const int npages = min(C::KS / P, page_hi - pstart);
+                if (pstart + npages > batch0 + 32) {
+                    batch0 = pstart;
+                    const int pi = batch0 + lane;
+                    my_bad = false;
+                    my_pg = 0;
+                    if (pi < page_hi) {
+                        const int pg = __ldg(trow + pi);
+                        my_bad = (pg < 0 || pg >= p.num_pages);
+                        my_pg = my_bad ? 0 : pg;
+                        if constexpr (C::FP8) {
+                            my_ks = __ldg(p.k_scales + my_pg);
+                            my_vs = __ldg(p.v_scales + my_pg);
+                        }
+                    }
+                }
+                const uint32_t slot = scount % C::NS, use = scount / C::NS;
+                if (use >= 1 && !mbar_wait_bounded(bar_empty + 8 * slot, (use - 1) & 1u, kWaitLimitNs)) {
+                    abort = true;
+                    break;
+                }
+                uint32_t bad_any = 0;
+                int pgs[C::MAX_PAGES_STAGE];
+                float kss[C::MAX_PAGES_STAGE], vss[C::MAX_PAGES_STAGE];
+#pragma unroll
+                for (int i = 0; i < C::MAX_PAGES_STAGE; ++i) {
+                    const int src = (pstart - batch0 + i) & 31;
+                    pgs[i] = __shfl_sync(0xffffffffu, my_pg, src);
+                    kss[i] = __shfl_sync(0xffffffffu, my_ks, src);
+                    vss[i] = __shfl_sync(0xffffffffu, my_vs, src);
+                    const uint32_t b = __shfl_sync(0xffffffffu, (uint32_t)my_bad, src);
+                    if (i < npages) bad_any |= b;
+                }
+                if (lane == 0) {
+                    float* meta = reinterpret_cast<float*>(smem + C::OFF_META + slot * C::META_STRIDE);
+#pragma unroll
+                    for (int i = 0; i < C::MAX_PAGES_STAGE; ++i) {
+                        meta[i] = kss[i];
+                        meta[4 + i] = vss[i];
+                    }
+                    reinterpret_cast<uint32_t*>(meta)[8] = bad_any;
+                    const uint32_t page_bytes = (uint32_t)(P * C::ROW_BYTES);
+                    mbar_arrive_expect_tx(bar_full + 8 * slot, 2u * page_bytes * (uint32_t)npages);
+                    const uint32_t kdst = base + slot * C::STAGE_BYTES;
+                    const uint32_t vdst = kdst + C::TILE_BYTES;
+                    for (int i = 0; i < npages; ++i) {
+                        const int tok = pgs[i] * P;
+                        tma_load_4d(kdst + i * page_bytes, &tm_k, bar_full + 8 * slot, 0, 0, it.kvh, tok, pol_kv);
+                        tma_load_4d(vdst + i * page_bytes, &tm_v, bar_full + 8 * slot, 0, 0, it.kvh, tok, pol_kv);
+                    }
+                }
+                __syncwarp();
+                ++scount;
+            }
+            if (misc[0]) abort = true;
+        }
+        if (abort) {
+            misc[0] = 1;
+            if (lane == 0 && p.err_word) atomicOr(p.err_word, kErrTimeout);
+        }
+        // Drain: make sure no copy into shared memory is still in flight.
+        if (lane == 0) {
+            const uint32_t first = scount > (uint32_t)C::NS ? scount - C::NS : 0u;
+            for (uint32_t c = first; c < scount; ++c)
+                mbar_wait_bounded(bar_full + 8 * (c % C::NS), (c / C::NS) & 1u, kWaitLimitNs);
+            const uint32_t qfirst = qcount > 2u ? qcount - 2u : 0u;
+            for (uint32_t c = qfirst; c < qcount; ++c)
+                mbar_wait_bounded(bar_qfull + 8 * (c & 1u), (c >> 1) & 1u, kWaitLimitNs);
+        }
+        return;
+    }
+
+    // ========================================================= consumer warps
+    const int wq = warp / C::WK;
+    const int wk = warp - wq * C::WK;
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const int tid = threadIdx.x;   // 0 .. NCT-1
+    uint32_t scount = 0, qcount = 0;
+    bool abort = false;
+
+    for (long long item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
+        const ItemPlan it = plan_item<C>(item, p);
+        if (!it.active) continue;
+        if (!it.seq_ok) {
+            // Invalid length: this group's rows become zeros (the split-0 items
+            // of every query tile write them).
+            for (int idx = tid; idx < (it.m_end - it.m0) * C::D; idx += C::NCT) {
+                const int m = it.m0 + idx / C::D, d = idx % C::D;
+                const int r = m / p.ratio, hl = m - r * p.ratio;
+                p.out[(((long long)it.g * p.rows + r) * p.n_head + it.kvh * p.ratio + hl) * C::D + d] =
+                    __float2bfloat16_rn(0.f);
+            }
+            if (tid == 0 && p.err_word) atomicOr(p.err_word, kErrSeqLen);
+            continue;
+        }
+
+        // ---- query fragments (B operand of S^T = K Q^T), one per n-tile and k-step
+        uint32_t qb[C::NQW][C::D / 16][2];
+        int nk[C::NQW][2];
+        {
+            const uint32_t slot = qcount & 1u, use = qcount >> 1;
+            if (!mbar_wait_bounded(bar_qfull + 8 * slot, use & 1u, kWaitLimitNs)) abort = true;
+            const uint8_t* qs = smem + C::OFF_Q + slot * C::Q_SLOT_BYTES;
+            bool qrange_bad = false;
+#pragma unroll
+            for (int j = 0; j < C::NQW; ++j) {
+                const int colb = (wq * C::NQW + j) * 8 + g8;      // this lane's B column
+                const bool valid = it.m0 + colb < it.m_end;
+                const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qs + colb * C::D * 2);
+#pragma unroll
+                for (int ks = 0; ks < C::D / 16; ++ks) {
+                    uint32_t b0 = 0, b1 = 0;
+                    if (valid) {
+                        if constexpr (C::FP8) {
+                            const int b = ks >> 1, hh = ks & 1;
+                            const int d0 = 32 * b + 8 * t4 + 4 * hh;
+                            const uint32_t x0 = qrow[d0 / 2], x1 = qrow[d0 / 2 + 1];
+                            const float f0 = bf16_lo(x0), f1 = bf16_hi(x0), f2 = bf16_lo(x1), f3 = bf16_hi(x1);
+                            qrange_bad |= fabsf(f0) > 65504.f || fabsf(f1) > 65504.f ||
+                                          fabsf(f2) > 65504.f || fabsf(f3) > 65504.f;
+                            b0 = pack_f16x2(f0, f1);
+                            b1 = pack_f16x2(f2, f3);
+                        } else {
+                            b0 = qrow[(16 * ks + 2 * t4) / 2];
+                            b1 = qrow[(16 * ks + 8 + 2 * t4) / 2];
+                        }
+                    }
+                    qb[j][ks][0] = b0;
+                    qb[j][ks][1] = b1;
+                }
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int m = it.m0 + lane_col<C>(wq, j, t4, c);
+                    nk[j][c] = (m < it.m_end) ? it.L - p.rows + m / p.ratio + 1 : 0;
+                }
+            }
+            if (C::FP8 && qrange_bad && p.err_word) atomicOr(p.err_word, kErrQRange);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_qempty + 8 * slot);
+            ++qcount;
+        }
+
+        float m_run[C::NQW][2], l_run[C::NQW][2];
+        float oacc[C::NQW][C::D / 16][4];
+#pragma unroll
+        for (int j = 0; j < C::NQW; ++j) {
+            m_run[j][0] = m_run[j][1] = -CUDART_INF_F;
+            l_run[j][0] = l_run[j][1] = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < C::D / 16; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) oacc[j][mt][e] = 0.f;
+        }
+        uint32_t bad = 0;
+        const int P = p.page_size;
+
+        for (int st = 0; st < it.n_stages && !abort; ++st) {
+            const uint32_t slot = scount % C::NS, use = scount / C::NS;
+            if (!mbar_wait_bounded(bar_full + 8 * slot, use & 1u, kWaitLimitNs)) {
+                abort = true;
+                break;
+            }
+            const uint32_t kbase = base + slot * C::STAGE_BYTES;
+            const uint32_t vbase = kbase + C::TILE_BYTES;
+            const float* meta = reinterpret_cast<const float*>(smem + C::OFF_META + slot * C::META_STRIDE);
+            bad |= reinterpret_cast<const uint32_t*>(meta)[8];
+            const int skey0 = it.k0 + st * C::KS;
+
+#pragma unroll 1
+            for (int kt = wk; kt < C::SUBS; kt += C::WK) {
+                const int key0 = skey0 + kt * 16;
+                if (key0 >= it.k1) break;
+                float kfac = p.scale_log2, vfac = 1.f;
+                if constexpr (C::FP8) {
+                    const int pi = (kt * 16) / P;   // page of this 16-key sub-tile within the stage
+                    kfac *= meta[pi];
+                    vfac = meta[4 + pi];
+                }
+                // ---------------- S^T = K Q^T
+                float sacc[C::NQW][4];
+#pragma unroll
+                for (int j = 0; j < C::NQW; ++j)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sacc[j][e] = 0.f;
+                if constexpr (!C::FP8) {
+                    const int mi = lane >> 3, ri = lane & 7;
+                    const uint32_t row = kt * 16 + ri + 8 * (mi & 1);
+#pragma unroll
+                    for (int ks = 0; ks < C::D / 16; ++ks) {
+                        const uint32_t off = row * C::ROW_BYTES + (16 * ks + 8 * (mi >> 1)) * 2;
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4(kbase + swz128(off), a0, a1, a2, a3);
+#pragma unroll
+                        for (int j = 0; j < C::NQW; ++j) mma_bf16(sacc[j], a0, a1, a2, a3, qb[j][ks][0], qb[j][ks][1]);
+                    }
+                } else {
+                    const uint32_t rlo = (kt * 16 + g8) * C::ROW_BYTES;
+                    const uint32_t rhi = rlo + 8 * C::ROW_BYTES;
+#pragma unroll
+                    for (int b = 0; b < C::D / 32; ++b) {
+                        const uint32_t col = 32 * b + 8 * t4;
+                        uint32_t lo0, lo1, hi0, hi1;
+                        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(lo0), "=r"(lo1) : "r"(kbase + swz128(rlo + col)));
+                        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(hi0), "=r"(hi1) : "r"(kbase + swz128(rhi + col)));
+                        // k-step 2b: bytes 0..3 ; k-step 2b+1: bytes 4..7
+                        const uint32_t a0 = e4m3x2_to_f16x2((uint16_t)(lo0 & 0xFFFF));
+                        const uint32_t a1 = e4m3x2_to_f16x2((uint16_t)(hi0 & 0xFFFF));
+                        const uint32_t a2 = e4m3x2_to_f16x2((uint16_t)(lo0 >> 16));
+                        const uint32_t a3 = e4m3x2_to_f16x2((uint16_t)(hi0 >> 16));
+                        const uint32_t c0 = e4m3x2_to_f16x2((uint16_t)(lo1 & 0xFFFF));
+                        const uint32_t c1 = e4m3x2_to_f16x2((uint16_t)(hi1 & 0xFFFF));
+                        const uint32_t c2 = e4m3x2_to_f16x2((uint16_t)(lo1 >> 16));
+                        const uint32_t c3 = e4m3x2_to_f16x2((uint16_t)(hi1 >> 16));
+#pragma unroll
+                        for (int j = 0; j < C::NQW; ++j) {
+                            mma_f16(sacc[j], a0, a1, a2, a3, qb[j][2 * b][0], qb[j][2 * b][1]);
+                            mma_f16(sacc[j], c0, c1, c2, c3, qb[j][2 * b + 1][0], qb[j][2 * b + 1][1]);
+                        }
+                    }
+                }
+                // ---------------- mask, online softmax
+                uint32_t pb[C::NQW][2];
+#pragma unroll
+                for (int j = 0; j < C::NQW; ++j) {
+                    float x[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int key = key0 + g8 + ((e >> 1) << 3);
+                        x[e] = (key < nk[j][e & 1]) ? sacc[j][e] * kfac : -CUDART_INF_F;
+                    }
+                    float alpha[2];
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        float mx = fmaxf(x[c], x[c + 2]);
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                        const float m_new = fmaxf(m_run[j][c], mx);
+                        const float m_use = (m_new == -CUDART_INF_F) ? 0.f : m_new;
+                        alpha[c] = exp2f(m_run[j][c] - m_use);
+                        m_run[j][c] = m_new;
+                        x[c] = exp2f(x[c] - m_use);
+                        x[c + 2] = exp2f(x[c + 2] - m_use);
+                        l_run[j][c] = l_run[j][c] * alpha[c] + (x[c] + x[c + 2]);
+                    }
+#pragma unroll
+                    for (int mt = 0; mt < C::D / 16; ++mt) {
+                        oacc[j][mt][0] *= alpha[0];
+                        oacc[j][mt][1] *= alpha[1];
+                        oacc[j][mt][2] *= alpha[0];
+                        oacc[j][mt][3] *= alpha[1];
+                    }
+                    if constexpr (C::FP8) {
+                        pb[j][0] = movmatrix_trans(pack_f16x2(x[0] * vfac, x[1] * vfac));
+                        pb[j][1] = movmatrix_trans(pack_f16x2(x[2] * vfac, x[3] * vfac));
+                    } else {
+                        pb[j][0] = movmatrix_trans(pack_bf16x2(x[0], x[1]));
+                        pb[j][1] = movmatrix_trans(pack_bf16x2(x[2], x[3]));
+                    }
+                }
+                // ---------------- O^T += V^T P^T
+                const bool edge = key0 + 16 > it.k1;   // keys past the item's range are zeroed in V
+                if constexpr (!C::FP8) {
+                    const int mi = lane >> 3, ri = lane & 7;
+                    const uint32_t row = kt * 16 + ri + 8 * (mi >> 1);
+                    const int ke = key0 + 2 * t4;
+                    const uint32_t m_lo = (edge ? ((ke < it.k1 ? 0x0000FFFFu : 0u) | (ke + 1 < it.k1 ? 0xFFFF0000u : 0u)) : 0xFFFFFFFFu);
+                    const uint32_t m_hi = (edge ? ((ke + 8 < it.k1 ? 0x0000FFFFu : 0u) | (ke + 9 < it.k1 ? 0xFFFF0000u : 0u)) : 0xFFFFFFFFu);
+#pragma unroll
+                    for (int dt = 0; dt < C::D / 16; ++dt) {
+                        const uint32_t off = row * C::ROW_BYTES + (16 * dt + 8 * (mi & 1)) * 2;
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4_trans(vbase + swz128(off), a0, a1, a2, a3);
+                        a0 &= m_lo;
+                        a1 &= m_lo;
+                        a2 &= m_hi;
+                        a3 &= m_hi;
+#pragma unroll
+                        for (int j = 0; j < C::NQW; ++j) mma_bf16(oacc[j][dt], a0, a1, a2, a3, pb[j][0], pb[j][1]);
+                    }
+                } else {
+                    const int kr = kt * 16 + 2 * t4;
+                    const int ke = key0 + 2 * t4;
+                    const bool z0 = edge && ke >= it.k1, z1 = edge && ke + 1 >= it.k1;
+                    const bool z2 = edge && ke + 8 >= it.k1, z3 = edge && ke + 9 >= it.k1;
+#pragma unroll
+                    for (int b = 0; b < C::D / 32; ++b) {
+                        const uint32_t col = 32 * b + 4 * g8;
+                        uint32_t w0, w1, w2, w3;
+                        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w0) : "r"(vbase + swz128(kr * C::ROW_BYTES + col)));
+                        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w1) : "r"(vbase + swz128((kr + 1) * C::ROW_BYTES + col)));
+                        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w2) : "r"(vbase + swz128((kr + 8) * C::ROW_BYTES + col)));
+                        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w3) : "r"(vbase + swz128((kr + 9) * C::ROW_BYTES + col)));
+                        if (z0) w0 = 0;
+                        if (z1) w1 = 0;
+                        if (z2) w2 = 0;
+                        if (z3) w3 = 0;
+                        // pairs (key 2t, key 2t+1) and (key 2t+8, key 2t+9) at one d
+                        const uint32_t p01_lo = __byte_perm(w0, w1, 0x5140);   // d+0 | d+1
+                        const uint32_t p01_hi = __byte_perm(w0, w1, 0x7362);   // d+2 | d+3
+                        const uint32_t p89_lo = __byte_perm(w2, w3, 0x5140);
+                        const uint32_t p89_hi = __byte_perm(w2, w3, 0x7362);
+                        // m-tile 2b: rows g (d+0), g+8 (d+1); m-tile 2b+1: rows g (d+2), g+8 (d+3)
+                        const uint32_t e0 = e4m3x2_to_f16x2((uint16_t)(p01_lo & 0xFFFF));
+                        const uint32_t e1 = e4m3x2_to_f16x2((uint16_t)(p01_lo >> 16));
+                        const uint32_t e2 = e4m3x2_to_f16x2((uint16_t)(p89_lo & 0xFFFF));
+                        const uint32_t e3 = e4m3x2_to_f16x2((uint16_t)(p89_lo >> 16));
+                        const uint32_t f0 = e4m3x2_to_f16x2((uint16_t)(p01_hi & 0xFFFF));
+                        const uint32_t f1 = e4m3x2_to_f16x2((uint16_t)(p01_hi >> 16));
+                        const uint32_t f2 = e4m3x2_to_f16x2((uint16_t)(p89_hi & 0xFFFF));
+                        const uint32_t f3 = e4m3x2_to_f16x2((uint16_t)(p89_hi >> 16));
+#pragma unroll
+                        for (int j = 0; j < C::NQW; ++j) {
+                            mma_f16(oacc[j][2 * b], e0, e1, e2, e3, pb[j][0], pb[j][1]);
+                            mma_f16(oacc[j][2 * b + 1], f0, f1, f2, f3, pb[j][0], pb[j][1]);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+            ++scount;
+            if (misc[0]) abort = true;
+        }
+        // Every consumer warp reaches this barrier once per item, whatever
+        // happened above, so a time-out never strands the others.
+        if (named_barrier_or(1, C::NCT, abort)) {
+            abort = true;
+            break;
+        }
+
+        // ---------------- per-warp sums over the 8 key lanes
+#pragma unroll
+        for (int j = 0; j < C::NQW; ++j)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float l = l_run[j][c];
+                l += __shfl_xor_sync(0xffffffffu, l, 4);
+                l += __shfl_xor_sync(0xffffffffu, l, 8);
+                l += __shfl_xor_sync(0xffffffffu, l, 16);
+                l_run[j][c] = l;
+            }
+        // ---------------- stage this warp's state in shared memory
+        float* mrg = reinterpret_cast<float*>(smem + C::OFF_MERGE) + wk * C::QT * C::MSTRIDE;
+        float* mml = reinterpret_cast<float*>(smem + C::OFF_ML) + wk * C::QT * 2;
+#pragma unroll
+        for (int j = 0; j < C::NQW; ++j) {
+#pragma unroll
+            for (int mt = 0; mt < C::D / 16; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int col = lane_col<C>(wq, j, t4, e & 1);
+                    mrg[col * C::MSTRIDE + d_of<C>(mt, g8 + ((e >> 1) << 3))] = oacc[j][mt][e];
+                }
+            if (g8 == 0)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int col = lane_col<C>(wq, j, t4, c);
+                    mml[col * 2 + 0] = m_run[j][c];
+                    mml[col * 2 + 1] = l_run[j][c];
+                }
+        }
+        // Stage-meta `bad` words were OR-ed per warp; make them CTA-wide.
+        const bool item_bad = named_barrier_or(1, C::NCT, bad != 0);
+
+        const bool final_write = (p.split_len == 0) || it.n_splits == 1;
+        const long long gq = ((long long)it.g * p.n_head_kv + it.kvh) * p.n_qtiles + it.qt;
+        const long long slot_idx = gq * p.max_splits + it.s;
+        float* pacc = p.part_acc + slot_idx * p.qtv * C::D;
+        float* pml = p.part_ml + slot_idx * p.qtv * 2;
+        const float* mrg0 = reinterpret_cast<const float*>(smem + C::OFF_MERGE);
+        const float* mml0 = reinterpret_cast<const float*>(smem + C::OFF_ML);
+        for (int idx = tid; idx < (it.m_end - it.m0) * C::D; idx += C::NCT) {
+            const int col = idx / C::D, d = idx - col * C::D;
+            float mw = -CUDART_INF_F;
+#pragma unroll
+            for (int w = 0; w < C::WK; ++w) mw = fmaxf(mw, mml0[(w * C::QT + col) * 2]);
+            const float m_use = (mw == -CUDART_INF_F) ? 0.f : mw;
+            float acc = 0.f, l = 0.f;
+#pragma unroll
+            for (int w = 0; w < C::WK; ++w) {
+                const float f = exp2f(mml0[(w * C::QT + col) * 2] - m_use);
+                acc += f * mrg0[(w * C::QT + col) * C::MSTRIDE + d];
+                l += f * mml0[(w * C::QT + col) * 2 + 1];
+            }
+            if (final_write) {
+                const int m = it.m0 + col;
+                const int r = m / p.ratio, hl = m - r * p.ratio;
+                const float o = item_bad ? 0.f : acc / l;
+                p.out[(((long long)it.g * p.rows + r) * p.n_head + it.kvh * p.ratio + hl) * C::D + d] =
+                    __float2bfloat16_rn(o);
+            } else {
+                __stcg(pacc + col * C::D + d, acc);
+                if (d == 0) {
+                    __stcg(pml + col * 2, mw);
+                    __stcg(pml + col * 2 + 1, l);
+                }
+            }
+        }
+        if (final_write) {
+            if (item_bad && tid == 0 && p.err_word) atomicOr(p.err_word, kErrPage);
+            // the merge buffers are rewritten by the next item
+            named_barrier_sync(1, C::NCT);
+            continue;
+        }
+        // ---------------- ticket: the last split of (g, kvh, qt) merges all of them
+        if (tid == 0) __stcg(p.part_flag + slot_idx, item_bad ? 1u : 0u);
+        __threadfence();
+        named_barrier_sync(1, C::NCT);
+        bool last = false;
+        if (tid == 0) last = atomicAdd(p.counters + gq, 1u) == (uint32_t)(it.n_splits - 1);
+        if (named_barrier_or(1, C::NCT, last)) {
+            __threadfence();
+            const long long slot0 = gq * p.max_splits;
+            uint32_t any_bad = 0;
+            for (int s = 0; s < it.n_splits; ++s) any_bad |= __ldcg(p.part_flag + slot0 + s);
+            for (int idx = tid; idx < (it.m_end - it.m0) * C::D; idx += C::NCT) {
+                const int col = idx / C::D, d = idx - col * C::D;
+                float mx = -CUDART_INF_F;
+                for (int s = 0; s < it.n_splits; ++s)
+                    mx = fmaxf(mx, __ldcg(p.part_ml + (slot0 + s) * p.qtv * 2 + col * 2));
+                const float m_use = (mx == -CUDART_INF_F) ? 0.f : mx;
+                float acc = 0.f, l = 0.f;
+                for (int s = 0; s < it.n_splits; ++s) {
+                    const float* ml = p.part_ml + (slot0 + s) * p.qtv * 2 + col * 2;
+                    const float f = exp2f(__ldcg(ml) - m_use);
+                    l += f * __ldcg(ml + 1);
+                    acc += f * __ldcg(p.part_acc + (slot0 + s) * p.qtv * C::D + col * C::D + d);
+                }
+                const int m = it.m0 + col;
+                const int r = m / p.ratio, hl = m - r * p.ratio;
+                const float o = any_bad ? 0.f : acc / l;
+                p.out[(((long long)it.g * p.rows + r) * p.n_head + it.kvh * p.ratio + hl) * C::D + d] =
+                    __float2bfloat16_rn(o);
+            }
+            if (any_bad && tid == 0 && p.err_word) atomicOr(p.err_word, kErrPage);
+        }
+        named_barrier_sync(1, C::NCT);
+    }
+    if (abort) {
+        misc[0] = 1;
+        if (lane == 0 && p.err_word) atomicOr(p.err_word, kErrTimeout);
+    }
+}
+
+}  // namespace rad

@@ -1,0 +1,273 @@
+// Host side of the C ABI declared in include/rad_attn.h: argument checks, the
+// kernel choice, workspace layout, TMA descriptors and the launch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+
+#include "rad_attn.h"
+#include "tile_configs.cuh"
+
+namespace {
+
+using rad::AttnParams;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    std::atomic<int> ready{0};
+    int sms = 0;
+    int cc_major = 0, cc_minor = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::atomic<int> g_encode_ready{0};
+
+bool is_aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ------------------------------------------------------------------ call plan
+struct Plan {
+    int family;
+    int split_len;
+    int ratio, M, n_qtiles, qtv, max_splits;
+    rad::TileInfo tile;
+    long long n_items;
+    size_t counters_bytes, flags_bytes, ml_bytes, acc_bytes, total_bytes;
+};
+
+int check_scalars(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_dim,
+                  int32_t page_size, int32_t pages_per_seq, int32_t kv_dtype) {
+    if (groups <= 0 || rows <= 0) return RAD_E_SHAPE;
+    if (n_head <= 0 || n_head_kv <= 0 || n_head % n_head_kv != 0) return RAD_E_SHAPE;
+    if (pages_per_seq <= 0) return RAD_E_SHAPE;
+    if (head_dim != 128 && head_dim != 256) return RAD_E_DTYPE;
+    if (page_size != 16 && page_size != 32) return RAD_E_DTYPE;
+    if (kv_dtype != RAD_KV_BF16 && kv_dtype != RAD_KV_FP8_E4M3) return RAD_E_DTYPE;
+    const long long M = (long long)rows * (n_head / n_head_kv);
+    if (M > (1ll << 30) || (long long)groups * rows * n_head > (1ll << 40)) return RAD_E_SHAPE;
+    return RAD_OK;
+}
+
+rad::TileInfo tile_for(int head_dim, int kv_dtype, int family) {
+    const bool fp8 = kv_dtype == RAD_KV_FP8_E4M3;
+    if (head_dim == 128) return fp8 ? rad::tile_info<128, true>(family) : rad::tile_info<128, false>(family);
+    return fp8 ? rad::tile_info<256, true>(family) : rad::tile_info<256, false>(family);
+}
+
+Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_dim,
+               int32_t page_size, int32_t pages_per_seq, int32_t kv_dtype) {
+    Plan pl{};
+    pl.ratio = n_head / n_head_kv;
+    pl.M = rows * pl.ratio;
+    pl.family = pl.M <= 8 ? rad::kFamDecode : (pl.M <= 32 ? rad::kFamVerify : rad::kFamWide);
+    pl.split_len = rows <= rad::kSplitMaxRows ? rad::kSplitLen : 0;
+    pl.tile = tile_for(head_dim, kv_dtype, pl.family);
+    pl.n_qtiles = (pl.M + pl.tile.QT - 1) / pl.tile.QT;
+    pl.qtv = pl.M < pl.tile.QT ? pl.M : pl.tile.QT;
+    const long long cap_keys = (long long)pages_per_seq * page_size;
+    pl.max_splits = pl.split_len > 0 ? (int)((cap_keys + pl.split_len - 1) / pl.split_len) : 1;
+    const long long n_gq = (long long)groups * n_head_kv * pl.n_qtiles;
+    pl.n_items = n_gq * pl.max_splits;
+    if (pl.split_len > 0) {
+        const long long slots = n_gq * pl.max_splits;
+        pl.counters_bytes = round_up((size_t)n_gq * 4, 256);
+        pl.flags_bytes = round_up((size_t)slots * 4, 256);
+        pl.ml_bytes = round_up((size_t)slots * pl.qtv * 2 * 4, 256);
+        pl.acc_bytes = round_up((size_t)slots * pl.qtv * head_dim * 4, 256);
+    }
+    pl.total_bytes = pl.counters_bytes + pl.flags_bytes + pl.ml_bytes + pl.acc_bytes;
+    return pl;
+}
+
+const char* family_name(int f) {
+    return f == rad::kFamDecode ? "decode" : (f == rad::kFamVerify ? "verify" : "wide");
+}
+
+// ------------------------------------------------------------------ device facts
+int device_info(int* dev_out, int* sms_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return RAD_E_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return RAD_E_DEVICE;
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready.load(std::memory_order_acquire)) {
+        int sms = 0, ma = 0, mi = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&ma, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&mi, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return RAD_E_CUDA;
+        d.sms = sms;
+        d.cc_major = ma;
+        d.cc_minor = mi;
+        d.ready.store(1, std::memory_order_release);
+    }
+    if (d.cc_major != 10 || d.cc_minor != 3) return RAD_E_DEVICE;
+    *dev_out = dev;
+    *sms_out = d.sms;
+    return RAD_OK;
+}
+
+int get_encoder() {
+    if (g_encode_ready.load(std::memory_order_acquire)) return RAD_OK;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return RAD_E_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    g_encode_ready.store(1, std::memory_order_release);
+    return RAD_OK;
+}
+
+// 4-D view of a pool [num_pages*page_size tokens][n_head_kv][head_dim] whose
+// innermost dimension is cut into 128-byte rows, so that one box is one page of
+// one KV head and the tile lands in shared memory with 128-byte swizzling.
+int encode_pool_map(CUtensorMap* m, const void* pool, int kv_dtype, int head_dim, int n_head_kv,
+                    int page_size, int num_pages) {
+    const int e = kv_dtype == RAD_KV_FP8_E4M3 ? 1 : 2;
+    const int boxw = 128 / e;
+    cuuint64_t dims[4] = {(cuuint64_t)boxw, (cuuint64_t)(head_dim / boxw), (cuuint64_t)n_head_kv,
+                          (cuuint64_t)num_pages * (cuuint64_t)page_size};
+    cuuint64_t strides[3] = {128, (cuuint64_t)head_dim * e, (cuuint64_t)n_head_kv * head_dim * e};
+    cuuint32_t box[4] = {(cuuint32_t)boxw, (cuuint32_t)(head_dim / boxw), 1, (cuuint32_t)page_size};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(m,
+                          e == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                          const_cast<void*>(pool), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? RAD_OK : RAD_E_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t rad_attn_paged_workspace_bytes(int32_t groups, int32_t rows, int32_t n_head,
+                                      int32_t n_head_kv, int32_t head_dim, int32_t page_size,
+                                      int32_t pages_per_seq, int32_t kv_dtype) {
+    if (check_scalars(groups, rows, n_head, n_head_kv, head_dim, page_size, pages_per_seq, kv_dtype) !=
+        RAD_OK)
+        return 0;
+    return make_plan(groups, rows, n_head, n_head_kv, head_dim, page_size, pages_per_seq, kv_dtype)
+        .total_bytes;
+}
+
+int rad_attn_paged(const void* q, const void* k_pool, const void* v_pool, const int32_t* page_table,
+                   const int32_t* seq_lens, int32_t groups, int32_t rows, int32_t n_head,
+                   int32_t n_head_kv, int32_t head_dim, int32_t page_size, int32_t pages_per_seq,
+                   int32_t num_pages, float scale, int32_t kv_dtype, const float* k_scales,
+                   const float* v_scales, void* out, void* workspace, size_t workspace_bytes,
+                   uint32_t* err_word, rad_stream_t stream) {
+    int rc = check_scalars(groups, rows, n_head, n_head_kv, head_dim, page_size, pages_per_seq, kv_dtype);
+    if (rc != RAD_OK) return rc;
+    if (num_pages <= 0 || (long long)num_pages * page_size > 0x7FFFFFFFll) return RAD_E_SHAPE;
+    if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !out) return RAD_E_ARG;
+    if (!is_aligned(q, 16) || !is_aligned(k_pool, 16) || !is_aligned(v_pool, 16) || !is_aligned(out, 2) ||
+        !is_aligned(page_table, 4) || !is_aligned(seq_lens, 4) || !is_aligned(err_word, 4))
+        return RAD_E_ARG;
+    const bool fp8 = kv_dtype == RAD_KV_FP8_E4M3;
+    if (fp8 && (!k_scales || !v_scales || !is_aligned(k_scales, 4) || !is_aligned(v_scales, 4)))
+        return RAD_E_ARG;
+    if (!std::isfinite(scale)) return RAD_E_ARG;
+    const Plan pl = make_plan(groups, rows, n_head, n_head_kv, head_dim, page_size, pages_per_seq, kv_dtype);
+    if (pl.total_bytes > 0 && (!workspace || workspace_bytes < pl.total_bytes || !is_aligned(workspace, 256)))
+        return RAD_E_WORKSPACE;
+
+    int dev = 0, sms = 0;
+    rc = device_info(&dev, &sms);
+    if (rc != RAD_OK) return rc;
+    rc = get_encoder();
+    if (rc != RAD_OK) return rc;
+
+    CUtensorMap tk, tv;
+    if (encode_pool_map(&tk, k_pool, kv_dtype, head_dim, n_head_kv, page_size, num_pages) != RAD_OK ||
+        encode_pool_map(&tv, v_pool, kv_dtype, head_dim, n_head_kv, page_size, num_pages) != RAD_OK)
+        return RAD_E_CUDA;
+
+    AttnParams p{};
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.page_table = page_table;
+    p.seq_lens = seq_lens;
+    p.k_scales = fp8 ? k_scales : nullptr;
+    p.v_scales = fp8 ? v_scales : nullptr;
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.err_word = err_word;
+    p.groups = groups;
+    p.rows = rows;
+    p.n_head = n_head;
+    p.n_head_kv = n_head_kv;
+    p.ratio = pl.ratio;
+    p.page_size = page_size;
+    p.pages_per_seq = pages_per_seq;
+    p.num_pages = num_pages;
+    p.M = pl.M;
+    p.n_qtiles = pl.n_qtiles;
+    p.qtv = pl.qtv;
+    p.max_splits = pl.max_splits;
+    p.split_len = pl.split_len;
+    p.n_items = pl.n_items;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (pl.total_bytes > 0) {
+        char* ws = static_cast<char*>(workspace);
+        p.counters = reinterpret_cast<uint32_t*>(ws);
+        p.part_flag = reinterpret_cast<uint32_t*>(ws + pl.counters_bytes);
+        p.part_ml = reinterpret_cast<float*>(ws + pl.counters_bytes + pl.flags_bytes);
+        p.part_acc = reinterpret_cast<float*>(ws + pl.counters_bytes + pl.flags_bytes + pl.ml_bytes);
+        if (cudaMemsetAsync(p.counters, 0, pl.counters_bytes, st) != cudaSuccess) return RAD_E_CUDA;
+    }
+    const long long grid = pl.n_items < (long long)sms ? pl.n_items : (long long)sms;
+    cudaError_t e;
+    if (head_dim == 128)
+        e = fp8 ? rad::launch_d128_fp8(pl.family, tk, tv, p, (int)grid, st)
+                : rad::launch_d128_bf16(pl.family, tk, tv, p, (int)grid, st);
+    else
+        e = fp8 ? rad::launch_d256_fp8(pl.family, tk, tv, p, (int)grid, st)
+                : rad::launch_d256_bf16(pl.family, tk, tv, p, (int)grid, st);
+    return e == cudaSuccess ? RAD_OK : RAD_E_CUDA;
+}
+
+int rad_attn_paged_describe(int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_dim,
+                            int32_t page_size, int32_t kv_dtype, char* buf, size_t buf_len) {
+    const int rc = check_scalars(1, rows, n_head, n_head_kv, head_dim, page_size, 1, kv_dtype);
+    if (!buf || buf_len == 0) return rc != RAD_OK ? rc : RAD_E_ARG;
+    if (rc != RAD_OK) {
+        snprintf(buf, buf_len, "refused: %s", rad_attn_status_string(rc));
+        return rc;
+    }
+    const Plan pl = make_plan(1, rows, n_head, n_head_kv, head_dim, page_size, 1, kv_dtype);
+    const rad::TileInfo& t = pl.tile;
+    snprintf(buf, buf_len,
+             "attn_tile family=%s head_dim=%d kv=%s query_rows_per_kv_head=%d tile_rows=%d "
+             "warps(q=%d,k=%d)+producer n_tiles_per_warp=%d keys_per_stage=%d stages=%d split_len=%d "
+             "threads=%d smem=%d mma=m16n8k16.%s",
+             family_name(pl.family), head_dim, kv_dtype == RAD_KV_FP8_E4M3 ? "fp8e4m3" : "bf16", pl.M,
+             t.QT, t.WQ, t.WK, t.NQW, t.KS, t.NS, pl.split_len, t.threads, t.smem,
+             kv_dtype == RAD_KV_FP8_E4M3 ? "f16" : "bf16");
+    return RAD_OK;
+}
+
+const char* rad_attn_status_string(int status) {
+    switch (status) {
+        case RAD_OK: return "RAD_OK";
+        case RAD_E_SHAPE: return "RAD_E_SHAPE";
+        case RAD_E_DTYPE: return "RAD_E_DTYPE";
+        case RAD_E_ARG: return "RAD_E_ARG";
+        case RAD_E_WORKSPACE: return "RAD_E_WORKSPACE";
+        case RAD_E_CUDA: return "RAD_E_CUDA";
+        case RAD_E_DEVICE: return "RAD_E_DEVICE";
+        default: return "RAD_E_UNKNOWN";
+    }
+}
+
+const char* rad_attn_version(void) { return "rad_attn 0.1.0 sm_103a"; }
+
+}  // extern "C"

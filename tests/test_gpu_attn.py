@@ -1,0 +1,246 @@
+"""GPU parity, row invariance and error-contract tests, through the C ABI.
+
+Every expected value comes from the fp64 oracle (oracle/) on the same seeded
+inputs; the CUDA path never produces a reference."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import DevWorkload, as_f64, assert_parity, bits, oracle_rows
+from paged_kv_attention_02_gb300 import binding as b
+from paged_kv_attention_02_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+# Mid-size cases: several stages, several splits, ragged last pages, every
+# call family, both head dims and both pool types, unused slots NaN-poisoned.
+MID = {
+    "dec128": wl.Config("dec128", 9, 1, 32, 8, 128, 16, wl.KV_BF16, 101,
+                        "fixed:1,15,16,17,511,512,513,1500,3001", pages_per_seq=200),
+    "dec256": wl.Config("dec256", 5, 1, 16, 2, 256, 32, wl.KV_BF16, 102, "fixed:1,33,700,1025,2500",
+                        pages_per_seq=100, meta=dict(head_dim=256, n_embd=3408)),
+    "dec_fp8_ratio1": wl.Config("dec_fp8_ratio1", 6, 1, 8, 8, 128, 16, wl.KV_FP8_E4M3, 103,
+                                "fixed:3,64,700,1023,1024,1025", pages_per_seq=70),
+    "dec_fp8_d256": wl.Config("dec_fp8_d256", 3, 1, 16, 2, 256, 32, wl.KV_FP8_E4M3, 104,
+                              "fixed:40,900,1700", pages_per_seq=60),
+    "ver_fp8": wl.Config("ver_fp8", 5, 8, 32, 8, 128, 16, wl.KV_FP8_E4M3, 105, "fixed:8,9,520,1000,2050",
+                         pages_per_seq=130),
+    "ver_bf16": wl.Config("ver_bf16", 4, 8, 8, 2, 128, 16, wl.KV_BF16, 106, "fixed:8,100,513,1100",
+                          pages_per_seq=70),
+    "ver_wide_d256": wl.Config("ver_wide_d256", 3, 8, 16, 2, 256, 32, wl.KV_BF16, 107, "fixed:8,600,1500",
+                               pages_per_seq=50),
+    "ratio16": wl.Config("ratio16", 3, 1, 16, 1, 128, 16, wl.KV_BF16, 108, "fixed:5,600,1200",
+                         pages_per_seq=80),
+    "chunk_split": wl.Config("chunk_split", 2, 40, 8, 2, 128, 16, wl.KV_BF16, 109, "fixed:40,1500",
+                             pages_per_seq=100),
+    "prefill": wl.Config("prefill", 2, 300, 8, 2, 128, 16, wl.KV_BF16, 110, "fixed:300,1000",
+                         pages_per_seq=64),
+    "prefill_fp8_d256": wl.Config("prefill_fp8_d256", 1, 260, 4, 1, 256, 32, wl.KV_FP8_E4M3, 111,
+                                  "fixed:900", pages_per_seq=30),
+}
+
+
+@pytest.fixture(scope="module")
+def mid():
+    cache = {}
+
+    def get(name):
+        if name not in cache:
+            w = wl.make_workload(MID[name], poison=True)
+            cache[name] = (w, DevWorkload(w))
+        return cache[name]
+    return get
+
+
+@pytest.mark.parametrize("name", list(MID))
+def test_mid_size_matches_oracle_everywhere(mid, name):
+    w, dw = mid(name)
+    out, err = dw.run()
+    assert err == 0
+    ref = oracle_rows(w)
+    assert ref.err_word == 0
+    assert_parity(as_f64(out), ref.out, dw.fp8, name)
+
+
+def test_tiny_decode_matches_oracle_everywhere():
+    w = wl.make_workload("tiny_decode", poison=True)
+    out, err = DevWorkload(w).run()
+    assert err == 0
+    assert_parity(as_f64(out), oracle_rows(w).out, False, "tiny_decode")
+
+
+# ------------------------------------------------------------------ full-size configurations
+
+@pytest.fixture(scope="module")
+def full():
+    cache = {}
+
+    def get(name):
+        if name not in cache:
+            cache.clear()
+            torch.cuda.empty_cache()
+            w = wl.make_workload(name)
+            cache[name] = (w, DevWorkload(w))
+        return cache[name]
+    return get
+
+
+FULL = ["batched_decode", "hybrid_decode", "spec_verify", "prefill_chunk"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_rows_match_oracle(full, name):
+    w, dw = full(name)
+    out, err = dw.run()
+    assert err == 0
+    o = as_f64(out)
+    assert np.all(np.isfinite(o))
+    c = w.cfg
+    rng = np.random.default_rng(7)
+    n = 48
+    sel = np.stack([rng.integers(0, w.groups, n), rng.integers(0, c.rows, n),
+                    rng.integers(0, c.n_head, n)], axis=1)
+    sel[0] = (int(np.argmax(w.seq_lens)), c.rows - 1, c.n_head - 1)     # the longest row
+    sel[1] = (int(np.argmin(w.seq_lens)), 0, 0)                         # the shortest
+    ref = oracle_rows(w, sel)
+    got = o[sel[:, 0], sel[:, 1], sel[:, 2]]
+    assert_parity(got, ref.out, dw.fp8, name)
+
+
+@pytest.mark.parametrize("name", ["batched_decode", "spec_verify"])
+def test_full_size_rows_are_bit_identical_across_batch_compositions(full, name):
+    w, dw = full(name)
+    out, _ = dw.run()
+    base = bits(out)
+    rng = np.random.default_rng(3)
+    pick = rng.choice(w.groups, size=5, replace=False)
+    # each sequence alone
+    for g in pick[:3]:
+        sub = w.select_groups([g])
+        o, err = dw.run(q=dw.q[g:g + 1], table=dw.table[g:g + 1], lens=dw.lens[g:g + 1])
+        assert err == 0
+        assert np.array_equal(bits(o)[0], base[g]), f"group {g} alone"
+        del sub
+    # a shuffled subset padded with dummy sequences (seq_len = rows on page 0)
+    order = np.concatenate([pick[::-1], [-1, -1, -1]])
+    q = torch.cat([dw.q[g:g + 1] if g >= 0 else torch.zeros_like(dw.q[:1]) for g in order])
+    table = torch.cat([dw.table[g:g + 1] if g >= 0 else torch.zeros_like(dw.table[:1]) for g in order])
+    lens = torch.tensor([int(w.seq_lens[g]) if g >= 0 else w.cfg.rows for g in order], dtype=torch.int32,
+                        device="cuda")
+    o, err = dw.run(q=q, table=table, lens=lens)
+    assert err == 0
+    ob = bits(o)
+    for i, g in enumerate(order):
+        if g >= 0:
+            assert np.array_equal(ob[i], base[g]), f"group {g} in a shuffled padded batch"
+
+
+def test_prefill_rows_bit_identical_alone_and_batched(mid):
+    w, dw = mid("prefill")
+    out, _ = dw.run()
+    o1, _ = dw.run(q=dw.q[1:2], table=dw.table[1:2], lens=dw.lens[1:2])
+    assert np.array_equal(bits(o1)[0], bits(out)[1])
+
+
+def test_repeated_calls_are_bit_identical(mid):
+    w, dw = mid("dec128")
+    a, _ = dw.run()
+    for _ in range(3):
+        c, _ = dw.run()
+        assert np.array_equal(bits(a), bits(c))
+
+
+# ------------------------------------------------------------------ errors never fault
+
+def test_bad_inputs_flag_errors_and_zero_only_their_group(mid):
+    w, dw = mid("dec128")
+    good, _ = dw.run()
+    gb = bits(good)
+    # a page id past the pool in group 8 (3001 keys: several splits)
+    table = dw.table.clone()
+    table[8, 100] = w.num_pages + 5
+    o, err = dw.run(table=table)
+    assert err == b.RAD_ERRW_PAGE
+    ob = bits(o)
+    assert np.all(ob[8] == 0) and np.array_equal(ob[:8], gb[:8])
+    # negative page id in group 3 (17 keys: one split)
+    table = dw.table.clone()
+    table[3, 1] = -1
+    o, err = dw.run(table=table)
+    assert err == b.RAD_ERRW_PAGE
+    ob = bits(o)
+    assert np.all(ob[3] == 0) and np.array_equal(np.delete(ob, 3, 0), np.delete(gb, 3, 0))
+    # seq_len 0 (< rows) and seq_len past the page table's capacity
+    lens = dw.lens.clone()
+    lens[0] = 0
+    lens[5] = 200 * 16 + 1
+    o, err = dw.run(lens=lens)
+    assert err == b.RAD_ERRW_SEQLEN
+    ob = bits(o)
+    assert np.all(ob[0] == 0) and np.all(ob[5] == 0)
+    keep = [1, 2, 3, 4, 6, 7, 8]
+    assert np.array_equal(ob[keep], gb[keep])
+
+
+def test_verify_bad_page_in_a_late_split_zeroes_every_row(mid):
+    w, dw = mid("ver_fp8")
+    good, _ = dw.run()
+    table = dw.table.clone()
+    table[4, 120] = 1 << 30
+    o, err = dw.run(table=table)
+    assert err == b.RAD_ERRW_PAGE
+    ob, gb = bits(o), bits(good)
+    assert np.all(ob[4] == 0) and np.array_equal(ob[:4], gb[:4])
+
+
+def test_refused_shapes_write_nothing(mid):
+    w, dw = mid("dec128")
+    canary = torch.full((w.groups, 1, 32, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    for kw, code in ((dict(head_dim=96), b.RAD_E_DTYPE), (dict(page_size=24), b.RAD_E_DTYPE),
+                     (dict(rows=0), b.RAD_E_SHAPE)):
+        args = dict(rows=1, n_head=32, n_head_kv=8, head_dim=128, page_size=16, scale=0.08,
+                    kv_dtype=b.RAD_KV_BF16)
+        args.update(kw)
+        with pytest.raises(b.RadAttnError) as e:
+            b.attn_paged(dw.q, dw.k, dw.v, dw.table, dw.lens, out=canary, **args)
+        assert e.value.status == code
+    torch.cuda.synchronize()
+    assert torch.all(canary == 7.0)
+
+
+def test_head_dim_is_read_from_metadata_not_derived(mid):
+    w, dw = mid("dec256")
+    meta = w.cfg.meta
+    derived = meta["n_embd"] // w.cfg.n_head      # 213 on the hybrid
+    assert derived != meta["head_dim"]
+    with pytest.raises(b.RadAttnError) as e:
+        b.attn_paged(dw.q, dw.k, dw.v, dw.table, dw.lens, rows=1, n_head=16, n_head_kv=2,
+                     head_dim=derived, page_size=32, scale=0.06)
+    assert e.value.status == b.RAD_E_DTYPE
+
+
+# ------------------------------------------------------------------ streams and graphs
+
+def test_side_stream_and_cuda_graph_replay_are_bit_identical(mid):
+    w, dw = mid("ver_fp8")
+    eager, _ = dw.run()
+    c = w.cfg
+    out = torch.empty_like(eager)
+    ws = torch.empty(b.workspace_bytes(w.groups, c.rows, c.n_head, c.n_head_kv, c.head_dim, c.page_size,
+                                       w.pages_per_seq, c.kv_dtype), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        dw.run(out=out, workspace=ws, stream=s)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(out), bits(eager))
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        b.attn_paged(dw.q, dw.k, dw.v, dw.table, dw.lens, rows=c.rows, n_head=c.n_head,
+                     n_head_kv=c.n_head_kv, head_dim=c.head_dim, page_size=c.page_size, scale=c.scale,
+                     kv_dtype=c.kv_dtype, k_scales=dw.ks, v_scales=dw.vs, out=out, workspace=ws)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(out), bits(eager))

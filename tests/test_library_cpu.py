@@ -1,0 +1,96 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every function
+include/rad_attn.h declares, and its host-side checks return the documented
+status codes before touching any device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_attention_02_gb300 import binding as b
+from paged_kv_attention_02_gb300.build import build_library
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "rad_attn.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    build_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rad_attn\w*)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function():
+    names = declared_functions()
+    assert set(names) == set(b.EXPORTS)
+    lib = ctypes.CDLL(b.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version():
+    assert b.status_string(b.RAD_OK) == "RAD_OK"
+    assert b.status_string(b.RAD_E_DTYPE) == "RAD_E_DTYPE"
+    assert "sm_103a" in b.version()
+
+
+def good_args(**over):
+    a = dict(q_ptr=4096, k_ptr=8192, v_ptr=12288, table_ptr=16384, lens_ptr=20480, groups=4, rows=1,
+             n_head=8, n_head_kv=2, head_dim=128, page_size=16, pages_per_seq=19, num_pages=64,
+             scale=0.088, kv_dtype=b.RAD_KV_BF16, ks_ptr=0, vs_ptr=0, out_ptr=24576, ws_ptr=1 << 20,
+             ws_bytes=1 << 30, err_ptr=0, stream_ptr=0)
+    a.update(over)
+    return a
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(rows=0), b.RAD_E_SHAPE),
+    (dict(groups=0), b.RAD_E_SHAPE),
+    (dict(n_head=6, n_head_kv=4), b.RAD_E_SHAPE),
+    (dict(pages_per_seq=0), b.RAD_E_SHAPE),
+    (dict(num_pages=0), b.RAD_E_SHAPE),
+    (dict(num_pages=1 << 30, page_size=16), b.RAD_E_SHAPE),
+    (dict(head_dim=96), b.RAD_E_DTYPE),
+    (dict(head_dim=213), b.RAD_E_DTYPE),
+    (dict(page_size=24), b.RAD_E_DTYPE),
+    (dict(kv_dtype=7), b.RAD_E_DTYPE),
+    (dict(q_ptr=0), b.RAD_E_ARG),
+    (dict(out_ptr=0), b.RAD_E_ARG),
+    (dict(k_ptr=8200), b.RAD_E_ARG),
+    (dict(kv_dtype=b.RAD_KV_FP8_E4M3), b.RAD_E_ARG),
+    (dict(scale=float("nan")), b.RAD_E_ARG),
+    (dict(ws_ptr=0), b.RAD_E_WORKSPACE),
+    (dict(ws_bytes=16), b.RAD_E_WORKSPACE),
+])
+def test_host_checks_refuse_before_any_device_access(over, code):
+    assert b.call_raw(**good_args(**over)) == code
+
+
+def test_zero_rows_precedes_every_other_check():
+    a = good_args(rows=0, q_ptr=0, head_dim=96, ws_ptr=0)
+    assert b.call_raw(**a) == b.RAD_E_SHAPE
+
+
+def test_valid_call_without_a_gpu_fails_loudly():
+    assert b.call_raw(**good_args()) in (b.RAD_E_CUDA, b.RAD_E_DEVICE)
+
+
+def test_workspace_sizes():
+    # decode splits: counters + flags + (max, sum) + accumulators per split slot
+    ws = b.workspace_bytes(256, 1, 32, 8, 128, 16, 512)
+    assert ws >= 256 * 8 * 16 * 4 * 130 * 4
+    assert b.workspace_bytes(1, 2048, 32, 8, 128, 16, 512) == 0      # prefill: no split
+    assert b.workspace_bytes(0, 1, 32, 8, 128, 16, 512) == 0
+    assert b.workspace_bytes(4, 1, 8, 2, 96, 16, 19) == 0
+
+
+def test_describe_names_the_kernel_choice():
+    assert "family=decode" in b.describe(1, 32, 8, 128, 16)
+    assert "family=verify" in b.describe(8, 32, 8, 128, 16, b.RAD_KV_FP8_E4M3)
+    assert "split_len=0" in b.describe(2048, 32, 8, 128, 16)
+    with pytest.raises(b.RadAttnError):
+        b.describe(1, 32, 8, 96, 16)
