@@ -30,6 +30,10 @@
 // call ("Adding a model", step 4: verified rows must equal decode rows bit
 // for bit).
 //
+// bf16 pools: the softmax weights P enter the PV product as two bf16 terms,
+// hi = bf16(p) and lo = bf16(p - hi), so the product sees p to ~2^-17; a single
+// bf16 P (2^-9) would put errors of ~1e-3 on short-context rows.
+//
 // fp8 pools (e4m3 codes, one fp32 scale per page and pool): codes are turned
 // into f16 pairs with cvt.rn.f16x2.e4m3x2 (exact), Q is rounded bf16->f16
 // (exact inside the f16 range; elements past it raise RAD_ERRW_QRANGE), the
@@ -480,7 +484,11 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
                     }
                 }
                 // ---------------- mask, online softmax
+                // bf16 pools carry P as a bf16 pair hi + lo (hi = bf16(p), lo =
+                // bf16(p - hi)), so the PV product sees p to ~2^-17 relative;
+                // fp8 pools carry P (times the page's V scale) in f16.
                 uint32_t pb[C::NQW][2];
+                uint32_t pl[C::NQW][2];
 #pragma unroll
                 for (int j = 0; j < C::NQW; ++j) {
                     float x[4];
@@ -515,8 +523,14 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
                         pb[j][0] = movmatrix_trans(pack_f16x2(x[0] * vfac, x[1] * vfac));
                         pb[j][1] = movmatrix_trans(pack_f16x2(x[2] * vfac, x[3] * vfac));
                     } else {
-                        pb[j][0] = movmatrix_trans(pack_bf16x2(x[0], x[1]));
-                        pb[j][1] = movmatrix_trans(pack_bf16x2(x[2], x[3]));
+                        const uint32_t h01 = pack_bf16x2(x[0], x[1]);
+                        const uint32_t h23 = pack_bf16x2(x[2], x[3]);
+                        const uint32_t l01 = pack_bf16x2(x[0] - bf16_lo(h01), x[1] - bf16_hi(h01));
+                        const uint32_t l23 = pack_bf16x2(x[2] - bf16_lo(h23), x[3] - bf16_hi(h23));
+                        pb[j][0] = movmatrix_trans(h01);
+                        pb[j][1] = movmatrix_trans(h23);
+                        pl[j][0] = movmatrix_trans(l01);
+                        pl[j][1] = movmatrix_trans(l23);
                     }
                 }
                 // ---------------- O^T += V^T P^T
@@ -537,7 +551,10 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
                         a2 &= m_hi;
                         a3 &= m_hi;
 #pragma unroll
-                        for (int j = 0; j < C::NQW; ++j) mma_bf16(oacc[j][dt], a0, a1, a2, a3, pb[j][0], pb[j][1]);
+                        for (int j = 0; j < C::NQW; ++j) {
+                            mma_bf16(oacc[j][dt], a0, a1, a2, a3, pb[j][0], pb[j][1]);
+                            mma_bf16(oacc[j][dt], a0, a1, a2, a3, pl[j][0], pl[j][1]);
+                        }
                     }
                 } else {
                     const int kr = kt * 16 + 2 * t4;
