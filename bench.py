@@ -71,7 +71,7 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--max-groups", type=int, default=0,
-                    help="keep only the first N sequences (small cases for profiling)")
+                    help="draw only N sequences (a smaller pool, for profiling)")
     return ap.parse_args()
 
 
@@ -258,9 +258,10 @@ def run_ours(args, rank, world, local):
     build_library()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = wl.make_workload(rank_config(args.workload, rank))
-    if args.max_groups and args.max_groups < w.groups:
-        w = w.select_groups(range(args.max_groups))
+    cfg = rank_config(args.workload, rank)
+    if args.max_groups and args.max_groups < cfg.groups:
+        cfg = replace(cfg, groups=args.max_groups)
+    w = wl.make_workload(cfg)
     c = w.cfg
     fp8 = c.kv_dtype == wl.KV_FP8_E4M3
 

@@ -81,10 +81,10 @@ enum {
                             section "Probe": a switch that cannot be honoured
                             is an error, never a silent substitution) */
     RAD_E_ARG = 3,       /* a required pointer is NULL, a pool, q or out
-                            pointer is not 16-byte aligned, or fp8 without
-                            scale arrays */
-    RAD_E_WORKSPACE = 4, /* workspace NULL or smaller than
-                            rad_attn_paged_workspace_bytes() */
+                            pointer is not 16-byte aligned, a non-finite
+                            scale, or fp8 without scale arrays */
+    RAD_E_WORKSPACE = 4, /* workspace NULL, not 256-byte aligned, or smaller
+                            than rad_attn_paged_workspace_bytes() */
     RAD_E_CUDA = 5,      /* the CUDA runtime refused a launch or a query */
     RAD_E_DEVICE = 6     /* the current device is not sm_103 (GB300) */
 };

@@ -6,10 +6,15 @@
 // ("Radiance architecture plugins", section "Declare: the metadata": n_head over
 // n_head_kv) -- against one contiguous range of the sequence's keys.
 //
-// Warp roles.  The last warp is the producer: it reads page ids from the page
-// table ("kern manifest v7", $defs.Domain: `stride` token slots per entry) and
-// issues one TMA load per (page, pool) into a ring of shared-memory stages,
-// plus bulk copies of the item's query rows.  The other warps consume stages:
+// Warp roles.  The last two warps are producers: they read page ids from the
+// page table ("kern manifest v7", $defs.Domain: `stride` token slots per
+// entry) and copy the item's K rows (one warp) and V rows (the other) into a
+// ring of shared-memory stages with 16-byte cp.async copies, straight into a
+// 128-byte-swizzled layout; the first producer also bulk-copies the item's
+// query rows.  (Each page row of one KV head is only head_dim*elem bytes, and
+// tensor-map boxes that small are issue-bound well below HBM speed on this
+// part; 16-byte copies of the same rows are not.)  The other warps consume
+// stages:
 //
 //   S^T[key][q] = K[key][:] . Q[q][:]          mma.m16n8k16, keys as M, query
 //                                              rows as N (8 per n-tile)
@@ -61,6 +66,8 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
 struct AttnParams {
     const __nv_bfloat16* q;
+    const uint8_t* k_pool;
+    const uint8_t* v_pool;
     const int32_t* page_table;
     const int32_t* seq_lens;
     const float* k_scales;
@@ -77,11 +84,11 @@ struct AttnParams {
     int qtv;               // query rows stored per partial slot: min(M, QT)
     int max_splits;        // 1 without splitting
     int split_len;         // keys per split; 0 = one range over the whole context
-    long long n_items;     // max_splits * groups * n_head_kv * n_qtiles
+    int n_items;           // max_splits * groups * n_head_kv * n_qtiles
     float scale_log2;      // scale * log2(e)
 };
 
-template <int D_, bool FP8_, int WQ_, int NQW_, int WK_, int KS_, int NS_>
+template <int D_, bool FP8_, int WQ_, int NQW_, int WK_, int KS_, int NS_, int MINB_ = 1>
 struct TileCfg {
     static constexpr int D = D_;
     static constexpr bool FP8 = FP8_;
@@ -90,16 +97,22 @@ struct TileCfg {
     static constexpr int WK = WK_;      // consumer warps along keys
     static constexpr int KS = KS_;      // keys per stage
     static constexpr int NS = NS_;      // stages
+    static constexpr int MINB = MINB_;  // CTAs meant to share an SM
     static constexpr int E = FP8 ? 1 : 2;
     static constexpr int QT = WQ * NQW * 8;
     static constexpr int NCW = WQ * WK;
     static constexpr int NCT = NCW * 32;
-    static constexpr int NTHREADS = NCT + 32;
+    static constexpr int NTHREADS = NCT + 64;   // + K and V producer warps
+    static constexpr int FULL_ARRIVALS = 64 + 1; // 64 async lane arrivals + stage meta
     static constexpr int SUBS = KS / 16;
     static constexpr int ROW_BYTES = D * E;
     static constexpr int TILE_BYTES = KS * ROW_BYTES;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
     static constexpr int MAX_PAGES_STAGE = KS / 16;
+    // A page of one KV head lands as D/BOXW blocks of [page_size][128 bytes]
+    // (one TMA box each), so 8 consecutive keys hit 8 different swizzle phases.
+    static constexpr int BOXW = 128 / E;          // elements per 128-byte row
+    static constexpr int NBOX = D / BOXW;
     static constexpr int Q_SLOT_BYTES = QT * D * 2;
     static constexpr int MSTRIDE = D + 4;   // floats per merge row (bank spread)
     static constexpr int OFF_Q = NS * STAGE_BYTES;
@@ -114,8 +127,23 @@ struct TileCfg {
     static_assert(KS % 16 == 0 && SUBS % WK == 0, "stage keys must split evenly over key warps");
     static_assert(MAX_PAGES_STAGE <= 4, "stage meta holds 4 pages");
     static_assert(D % 32 == 0, "head_dim multiple of 32");
-    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(SMEM_BYTES * MINB <= 233472 - 1024 * MINB, "shared memory budget");
+    // split-combine staging in the merge buffer: (max, sum) pairs, weights and
+    // per-column state for CH splits at a time
+    static constexpr int MERGE_FLOATS = WK * QT * MSTRIDE;
+    static constexpr int CH = (MERGE_FLOATS - 3 * QT) / (3 * QT) > 256 ? 256 : (MERGE_FLOATS - 3 * QT) / (3 * QT);
+    static constexpr int OWN = (QT * D / 4 + NCT - 1) / NCT;   // float4 outputs per thread
+    static_assert(CH >= 8, "combine chunk");
 };
+
+// Byte offset, inside a stage tile, of element d of key `key` (both relative to
+// the stage); P is the page size (16 or 32), lp = log2(P).
+template <class C>
+__device__ __forceinline__ uint32_t kv_off(int key, int d, int lp) {
+    const int P = 1 << lp;
+    return (uint32_t)(((key >> lp) * P * C::ROW_BYTES) + (d / C::BOXW) * P * 128 + (key & (P - 1)) * 128 +
+                      (d % C::BOXW) * C::E);
+}
 
 struct ItemPlan {
     int s, g, kvh, qt;
@@ -129,14 +157,14 @@ struct ItemPlan {
 };
 
 template <class C>
-__device__ __forceinline__ ItemPlan plan_item(long long item, const AttnParams& p) {
+__device__ __forceinline__ ItemPlan plan_item(int item, const AttnParams& p) {
     ItemPlan it;
-    const long long per_split = (long long)p.groups * p.n_head_kv * p.n_qtiles;
-    it.s = (int)(item / per_split);
-    long long rem = item - (long long)it.s * per_split;
+    const int per_split = p.groups * p.n_head_kv * p.n_qtiles;
+    it.s = item / per_split;
+    const int rem = item - it.s * per_split;
     const int per_g = p.n_head_kv * p.n_qtiles;
-    it.g = (int)(rem / per_g);
-    int rem2 = (int)(rem - (long long)it.g * per_g);
+    it.g = rem / per_g;
+    const int rem2 = rem - it.g * per_g;
     it.kvh = rem2 / p.n_qtiles;
     it.qt = rem2 - it.kvh * p.n_qtiles;
     if (p.split_len == 0) it.qt = p.n_qtiles - 1 - it.qt;   // causal: later tiles see more keys
@@ -188,10 +216,104 @@ __device__ __forceinline__ int d_of(int mt, int row16) {
     }
 }
 
+// Merges the partials of splits 0..n-1 of one (sequence, KV head, query tile)
+// in split order, in chunks of C::CH splits, and writes the bf16 output rows.
+// Run by every consumer thread of the CTA that took the last ticket.
 template <class C>
-__global__ void __launch_bounds__(C::NTHREADS, 1)
-    attn_tile_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                     const __grid_constant__ AttnParams p) {
+__device__ __forceinline__ void combine_splits(const AttnParams& p, const ItemPlan& it, long long gq,
+                                               uint8_t* smem, int tid) {
+    const int ns = it.n_splits, ncol = it.m_end - it.m0;
+    constexpr int D4 = C::D / 4;
+    const long long slot0 = gq * p.max_splits;
+    float* ml_s = reinterpret_cast<float*>(smem + C::OFF_MERGE);   // [CH][ncol][2]
+    float* w_s = ml_s + 2 * C::CH * C::QT;                          // [CH][ncol]
+    float* st_m = w_s + C::CH * C::QT;                              // [ncol] running max
+    float* st_l = st_m + C::QT;                                     // [ncol] running sum
+    float* st_a = st_l + C::QT;                                     // [ncol] rescale of the old state
+    if (tid < ncol) {
+        st_m[tid] = -CUDART_INF_F;
+        st_l[tid] = 0.f;
+    }
+    float4 acc[C::OWN];
+#pragma unroll
+    for (int k = 0; k < C::OWN; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    uint32_t any_bad = 0;
+    for (int s0 = 0; s0 < ns; s0 += C::CH) {
+        const int cn = min(C::CH, ns - s0);
+        named_barrier_sync(1, C::NCT);
+        for (int i = tid; i < cn * ncol; i += C::NCT) {
+            const int s = i / ncol, col = i - s * ncol;
+            const float2 v = __ldcg(reinterpret_cast<const float2*>(p.part_ml + (slot0 + s0 + s) * p.qtv * 2) + col);
+            ml_s[2 * i] = v.x;
+            ml_s[2 * i + 1] = v.y;
+        }
+        for (int i = tid; i < cn; i += C::NCT) any_bad |= __ldcg(p.part_flag + slot0 + s0 + i);
+        named_barrier_sync(1, C::NCT);
+        if (tid < ncol) {
+            const int col = tid;
+            float mx = st_m[col];
+            for (int s = 0; s < cn; ++s) mx = fmaxf(mx, ml_s[2 * (s * ncol + col)]);
+            const float m_use = (mx == -CUDART_INF_F) ? 0.f : mx;
+            const float alpha = exp2f(st_m[col] - m_use);
+            float l = st_l[col] * alpha;
+            for (int s = 0; s < cn; ++s) {
+                const float w = exp2f(ml_s[2 * (s * ncol + col)] - m_use);
+                w_s[s * ncol + col] = w;
+                l += w * ml_s[2 * (s * ncol + col) + 1];
+            }
+            st_m[col] = mx;
+            st_l[col] = l;
+            st_a[col] = alpha;
+        }
+        named_barrier_sync(1, C::NCT);
+#pragma unroll
+        for (int k = 0; k < C::OWN; ++k) {
+            const int e = tid + k * C::NCT;
+            if (e < ncol * D4) {
+                const int col = e / D4, d4 = e - col * D4;
+                const float a = st_a[col];
+                float4 r = acc[k];
+                r.x *= a; r.y *= a; r.z *= a; r.w *= a;
+                const float4* src = reinterpret_cast<const float4*>(p.part_acc + (slot0 + s0) * p.qtv * C::D) +
+                                    col * D4 + d4;
+                const long long sstride = (long long)p.qtv * D4;
+                for (int s = 0; s < cn; s += 8) {
+                    float4 v[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        v[i] = (s + i < cn) ? __ldcg(src + (s + i) * sstride) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (s + i < cn) {
+                            const float w = w_s[(s + i) * ncol + col];
+                            r.x += w * v[i].x; r.y += w * v[i].y; r.z += w * v[i].z; r.w += w * v[i].w;
+                        }
+                    }
+                }
+                acc[k] = r;
+            }
+        }
+    }
+    any_bad = named_barrier_or(1, C::NCT, any_bad != 0) ? 1u : 0u;
+#pragma unroll
+    for (int k = 0; k < C::OWN; ++k) {
+        const int e = tid + k * C::NCT;
+        if (e < ncol * D4) {
+            const int col = e / D4, d4 = e - col * D4;
+            const float inv = any_bad ? 0.f : 1.f / st_l[col];
+            const int m = it.m0 + col;
+            const int r = m / p.ratio, hl = m - r * p.ratio;
+            __nv_bfloat16* o = p.out + (((long long)it.g * p.rows + r) * p.n_head + it.kvh * p.ratio + hl) * C::D + 4 * d4;
+            const float4 a = any_bad ? make_float4(0.f, 0.f, 0.f, 0.f) : acc[k];
+            *reinterpret_cast<__nv_bfloat162*>(o) = __floats2bfloat162_rn(a.x * inv, a.y * inv);
+            *reinterpret_cast<__nv_bfloat162*>(o + 2) = __floats2bfloat162_rn(a.z * inv, a.w * inv);
+        }
+    }
+    if (any_bad && tid == 0 && p.err_word) atomicOr(p.err_word, kErrPage);
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const __grid_constant__ AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -208,7 +330,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::NS; ++i) {
-            mbar_init(bar_full + 8 * i, 1);
+            mbar_init(bar_full + 8 * i, C::FULL_ARRIVALS);
             mbar_init(bar_empty + 8 * i, C::NCW);
         }
         for (int i = 0; i < 2; ++i) {
@@ -220,20 +342,22 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     }
     __syncthreads();
 
-    if (warp == C::NCW) {
-        // ===================================================== producer warp
-        if (lane == 0) {
-            prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_v);
-        }
+    if (warp >= C::NCW) {
+        // ===================================================== producer warps
+        const int pw = warp - C::NCW;   // 0: K rows (+ query rows, stage meta), 1: V rows
+        const uint8_t* pool = pw == 0 ? p.k_pool : p.v_pool;
         const uint64_t pol_kv = policy_evict_first();
+        // Lane -> (row within a group of rows, 16-byte chunk within the row).
+        constexpr int CPR = C::ROW_BYTES / 16;          // chunks per row: 8, 16 or 32
+        constexpr int RPI = 32 / CPR;                   // rows per warp-wide copy
+        const int lrow = lane / CPR, lc = lane % CPR;
         uint32_t scount = 0, qcount = 0;
         bool abort = false;
-        for (long long item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
+        for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
             const ItemPlan it = plan_item<C>(item, p);
             if (!it.active || !it.seq_ok) continue;
             // ---- query rows of the item
-            {
+            if (pw == 0) {
                 const uint32_t slot = qcount & 1u, use = qcount >> 1;
                 if (use >= 1 && !mbar_wait_bounded(bar_qempty + 8 * slot, (use - 1) & 1u, kWaitLimitNs)) {
                     abort = true;
@@ -252,10 +376,13 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
                 }
                 ++qcount;
             }
-            // ---- KV pages of the item, batched 32 page ids at a time
+            // ---- KV pages of the item, page ids fetched 32 at a time
             const int P = p.page_size;
             const int page_hi = (it.k1 + P - 1) / P;   // exclusive
+            const uint32_t lsmem = (uint32_t)((lc >> 3) * P * 128);   // this lane's 128-byte column block
             const int32_t* trow = p.page_table + (long long)it.g * p.pages_per_seq;
+            const long long row_stride = (long long)p.n_head_kv * C::ROW_BYTES;   // bytes between token slots
+            const uint8_t* head_base = pool + (long long)it.kvh * C::ROW_BYTES + (long long)lrow * row_stride + lc * 16;
             int batch0 = -1 << 30;
             int my_pg = 0;
             float my_ks = 1.f, my_vs = 1.f;
@@ -273,7 +400,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
                         const int pg = __ldg(trow + pi);
                         my_bad = (pg < 0 || pg >= p.num_pages);
                         my_pg = my_bad ? 0 : pg;
-                        if constexpr (C::FP8) {
+                        if (C::FP8 && pw == 0) {
                             my_ks = __ldg(p.k_scales + my_pg);
                             my_vs = __ldg(p.v_scales + my_pg);
                         }
@@ -284,37 +411,41 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
                     abort = true;
                     break;
                 }
-                uint32_t bad_any = 0;
-                int pgs[C::MAX_PAGES_STAGE];
-                float kss[C::MAX_PAGES_STAGE], vss[C::MAX_PAGES_STAGE];
-#pragma unroll
-                for (int i = 0; i < C::MAX_PAGES_STAGE; ++i) {
-                    const int src = (pstart - batch0 + i) & 31;
-                    pgs[i] = __shfl_sync(0xffffffffu, my_pg, src);
-                    kss[i] = __shfl_sync(0xffffffffu, my_ks, src);
-                    vss[i] = __shfl_sync(0xffffffffu, my_vs, src);
-                    const uint32_t b = __shfl_sync(0xffffffffu, (uint32_t)my_bad, src);
-                    if (i < npages) bad_any |= b;
+                const uint32_t tile = base + slot * C::STAGE_BYTES + pw * C::TILE_BYTES;
+                for (int i = 0; i < npages; ++i) {
+                    const int pg = __shfl_sync(0xffffffffu, my_pg, (pstart - batch0 + i) & 31);
+                    const uint8_t* src = head_base + (long long)pg * P * row_stride;
+                    const uint32_t dst = tile + (uint32_t)(i * P * C::ROW_BYTES) + lsmem;
+#pragma unroll 4
+                    for (int t0 = 0; t0 < P; t0 += RPI) {
+                        const int t = t0 + lrow;
+                        cp_async_16(dst + t * 128 + (((lc & 7) ^ (t & 7)) << 4), src + (long long)t0 * row_stride,
+                                    pol_kv);
+                    }
                 }
-                if (lane == 0) {
-                    float* meta = reinterpret_cast<float*>(smem + C::OFF_META + slot * C::META_STRIDE);
+                cp_async_arrive_noinc(bar_full + 8 * slot);
+                if (pw == 0) {
+                    uint32_t bad_any = 0;
+                    float kss[C::MAX_PAGES_STAGE], vss[C::MAX_PAGES_STAGE];
 #pragma unroll
                     for (int i = 0; i < C::MAX_PAGES_STAGE; ++i) {
-                        meta[i] = kss[i];
-                        meta[4 + i] = vss[i];
+                        const int src = (pstart - batch0 + i) & 31;
+                        kss[i] = __shfl_sync(0xffffffffu, my_ks, src);
+                        vss[i] = __shfl_sync(0xffffffffu, my_vs, src);
+                        const uint32_t b = __shfl_sync(0xffffffffu, (uint32_t)my_bad, src);
+                        if (i < npages) bad_any |= b;
                     }
-                    reinterpret_cast<uint32_t*>(meta)[8] = bad_any;
-                    const uint32_t page_bytes = (uint32_t)(P * C::ROW_BYTES);
-                    mbar_arrive_expect_tx(bar_full + 8 * slot, 2u * page_bytes * (uint32_t)npages);
-                    const uint32_t kdst = base + slot * C::STAGE_BYTES;
-                    const uint32_t vdst = kdst + C::TILE_BYTES;
-                    for (int i = 0; i < npages; ++i) {
-                        const int tok = pgs[i] * P;
-                        tma_load_4d(kdst + i * page_bytes, &tm_k, bar_full + 8 * slot, 0, 0, it.kvh, tok, pol_kv);
-                        tma_load_4d(vdst + i * page_bytes, &tm_v, bar_full + 8 * slot, 0, 0, it.kvh, tok, pol_kv);
+                    if (lane == 0) {
+                        float* meta = reinterpret_cast<float*>(smem + C::OFF_META + slot * C::META_STRIDE);
+#pragma unroll
+                        for (int i = 0; i < C::MAX_PAGES_STAGE; ++i) {
+                            meta[i] = kss[i];
+                            meta[4 + i] = vss[i];
+                        }
+                        reinterpret_cast<uint32_t*>(meta)[8] = bad_any;
+                        mbar_arrive(bar_full + 8 * slot);
                     }
                 }
-                __syncwarp();
                 ++scount;
             }
             if (misc[0]) abort = true;
@@ -323,11 +454,9 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
             misc[0] = 1;
             if (lane == 0 && p.err_word) atomicOr(p.err_word, kErrTimeout);
         }
-        // Drain: make sure no copy into shared memory is still in flight.
-        if (lane == 0) {
-            const uint32_t first = scount > (uint32_t)C::NS ? scount - C::NS : 0u;
-            for (uint32_t c = first; c < scount; ++c)
-                mbar_wait_bounded(bar_full + 8 * (c % C::NS), (c / C::NS) & 1u, kWaitLimitNs);
+        // Drain: no copy into shared memory may still be in flight at exit.
+        cp_async_wait_all();
+        if (pw == 0 && lane == 0) {
             const uint32_t qfirst = qcount > 2u ? qcount - 2u : 0u;
             for (uint32_t c = qfirst; c < qcount; ++c)
                 mbar_wait_bounded(bar_qfull + 8 * (c & 1u), (c >> 1) & 1u, kWaitLimitNs);
@@ -343,7 +472,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
     uint32_t scount = 0, qcount = 0;
     bool abort = false;
 
-    for (long long item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
+    for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
         const ItemPlan it = plan_item<C>(item, p);
         if (!it.active) continue;
         if (!it.seq_ok) {
@@ -418,6 +547,7 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
         }
         uint32_t bad = 0;
         const int P = p.page_size;
+        const int lp = (P == 16) ? 4 : 5;
 
         for (int st = 0; st < it.n_stages && !abort; ++st) {
             const uint32_t slot = scount % C::NS, use = scount / C::NS;
@@ -449,24 +579,22 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
                     for (int e = 0; e < 4; ++e) sacc[j][e] = 0.f;
                 if constexpr (!C::FP8) {
                     const int mi = lane >> 3, ri = lane & 7;
-                    const uint32_t row = kt * 16 + ri + 8 * (mi & 1);
+                    const int row = kt * 16 + ri + 8 * (mi & 1);
 #pragma unroll
                     for (int ks = 0; ks < C::D / 16; ++ks) {
-                        const uint32_t off = row * C::ROW_BYTES + (16 * ks + 8 * (mi >> 1)) * 2;
+                        const uint32_t off = kv_off<C>(row, 16 * ks + 8 * (mi >> 1), lp);
                         uint32_t a0, a1, a2, a3;
                         ldsm_x4(kbase + swz128(off), a0, a1, a2, a3);
 #pragma unroll
                         for (int j = 0; j < C::NQW; ++j) mma_bf16(sacc[j], a0, a1, a2, a3, qb[j][ks][0], qb[j][ks][1]);
                     }
                 } else {
-                    const uint32_t rlo = (kt * 16 + g8) * C::ROW_BYTES;
-                    const uint32_t rhi = rlo + 8 * C::ROW_BYTES;
 #pragma unroll
                     for (int b = 0; b < C::D / 32; ++b) {
-                        const uint32_t col = 32 * b + 8 * t4;
+                        const int col = 32 * b + 8 * t4;
                         uint32_t lo0, lo1, hi0, hi1;
-                        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(lo0), "=r"(lo1) : "r"(kbase + swz128(rlo + col)));
-                        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(hi0), "=r"(hi1) : "r"(kbase + swz128(rhi + col)));
+                        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(lo0), "=r"(lo1) : "r"(kbase + swz128(kv_off<C>(kt * 16 + g8, col, lp))));
+                        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(hi0), "=r"(hi1) : "r"(kbase + swz128(kv_off<C>(kt * 16 + g8 + 8, col, lp))));
                         // k-step 2b: bytes 0..3 ; k-step 2b+1: bytes 4..7
                         const uint32_t a0 = e4m3x2_to_f16x2((uint16_t)(lo0 & 0xFFFF));
                         const uint32_t a1 = e4m3x2_to_f16x2((uint16_t)(hi0 & 0xFFFF));
@@ -537,13 +665,13 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
                 const bool edge = key0 + 16 > it.k1;   // keys past the item's range are zeroed in V
                 if constexpr (!C::FP8) {
                     const int mi = lane >> 3, ri = lane & 7;
-                    const uint32_t row = kt * 16 + ri + 8 * (mi >> 1);
+                    const int row = kt * 16 + ri + 8 * (mi >> 1);
                     const int ke = key0 + 2 * t4;
                     const uint32_t m_lo = (edge ? ((ke < it.k1 ? 0x0000FFFFu : 0u) | (ke + 1 < it.k1 ? 0xFFFF0000u : 0u)) : 0xFFFFFFFFu);
                     const uint32_t m_hi = (edge ? ((ke + 8 < it.k1 ? 0x0000FFFFu : 0u) | (ke + 9 < it.k1 ? 0xFFFF0000u : 0u)) : 0xFFFFFFFFu);
 #pragma unroll
                     for (int dt = 0; dt < C::D / 16; ++dt) {
-                        const uint32_t off = row * C::ROW_BYTES + (16 * dt + 8 * (mi & 1)) * 2;
+                        const uint32_t off = kv_off<C>(row, 16 * dt + 8 * (mi & 1), lp);
                         uint32_t a0, a1, a2, a3;
                         ldsm_x4_trans(vbase + swz128(off), a0, a1, a2, a3);
                         a0 &= m_lo;
@@ -563,12 +691,12 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
                     const bool z2 = edge && ke + 8 >= it.k1, z3 = edge && ke + 9 >= it.k1;
 #pragma unroll
                     for (int b = 0; b < C::D / 32; ++b) {
-                        const uint32_t col = 32 * b + 4 * g8;
+                        const int col = 32 * b + 4 * g8;
                         uint32_t w0, w1, w2, w3;
-                        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w0) : "r"(vbase + swz128(kr * C::ROW_BYTES + col)));
-                        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w1) : "r"(vbase + swz128((kr + 1) * C::ROW_BYTES + col)));
-                        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w2) : "r"(vbase + swz128((kr + 8) * C::ROW_BYTES + col)));
-                        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w3) : "r"(vbase + swz128((kr + 9) * C::ROW_BYTES + col)));
+                        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w0) : "r"(vbase + swz128(kv_off<C>(kr, col, lp))));
+                        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w1) : "r"(vbase + swz128(kv_off<C>(kr + 1, col, lp))));
+                        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w2) : "r"(vbase + swz128(kv_off<C>(kr + 8, col, lp))));
+                        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w3) : "r"(vbase + swz128(kv_off<C>(kr + 9, col, lp))));
                         if (z0) w0 = 0;
                         if (z1) w1 = 0;
                         if (z2) w2 = 0;
@@ -682,36 +810,18 @@ __global__ void __launch_bounds__(C::NTHREADS, 1)
             continue;
         }
         // ---------------- ticket: the last split of (g, kvh, qt) merges all of them
-        if (tid == 0) __stcg(p.part_flag + slot_idx, item_bad ? 1u : 0u);
-        __threadfence();
+        // All threads' partial stores are ordered before thread 0's gpu-scope
+        // fence by the barrier; thread 0 then takes a ticket.
         named_barrier_sync(1, C::NCT);
         bool last = false;
-        if (tid == 0) last = atomicAdd(p.counters + gq, 1u) == (uint32_t)(it.n_splits - 1);
-        if (named_barrier_or(1, C::NCT, last)) {
+        if (tid == 0) {
+            __stcg(p.part_flag + slot_idx, item_bad ? 1u : 0u);
             __threadfence();
-            const long long slot0 = gq * p.max_splits;
-            uint32_t any_bad = 0;
-            for (int s = 0; s < it.n_splits; ++s) any_bad |= __ldcg(p.part_flag + slot0 + s);
-            for (int idx = tid; idx < (it.m_end - it.m0) * C::D; idx += C::NCT) {
-                const int col = idx / C::D, d = idx - col * C::D;
-                float mx = -CUDART_INF_F;
-                for (int s = 0; s < it.n_splits; ++s)
-                    mx = fmaxf(mx, __ldcg(p.part_ml + (slot0 + s) * p.qtv * 2 + col * 2));
-                const float m_use = (mx == -CUDART_INF_F) ? 0.f : mx;
-                float acc = 0.f, l = 0.f;
-                for (int s = 0; s < it.n_splits; ++s) {
-                    const float* ml = p.part_ml + (slot0 + s) * p.qtv * 2 + col * 2;
-                    const float f = exp2f(__ldcg(ml) - m_use);
-                    l += f * __ldcg(ml + 1);
-                    acc += f * __ldcg(p.part_acc + (slot0 + s) * p.qtv * C::D + col * C::D + d);
-                }
-                const int m = it.m0 + col;
-                const int r = m / p.ratio, hl = m - r * p.ratio;
-                const float o = any_bad ? 0.f : acc / l;
-                p.out[(((long long)it.g * p.rows + r) * p.n_head + it.kvh * p.ratio + hl) * C::D + d] =
-                    __float2bfloat16_rn(o);
-            }
-            if (any_bad && tid == 0 && p.err_word) atomicOr(p.err_word, kErrPage);
+            last = atomicAdd(p.counters + gq, 1u) == (uint32_t)(it.n_splits - 1);
+            if (last) __threadfence();
+        }
+        if (named_barrier_or(1, C::NCT, last)) {
+            combine_splits<C>(p, it, gq, smem, tid);
         }
         named_barrier_sync(1, C::NCT);
     }

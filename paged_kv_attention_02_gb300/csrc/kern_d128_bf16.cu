@@ -2,8 +2,7 @@
 #include "launch.cuh"
 
 namespace rad {
-cudaError_t launch_d128_bf16(int family, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const AttnParams& p, int grid, cudaStream_t st) {
-    return launch_family<128, false>(family, tk, tv, p, grid, st);
+cudaError_t launch_d128_bf16(int family, const AttnParams& p, int sms, cudaStream_t st) {
+    return launch_family<128, false>(family, p, sms, st);
 }
 }  // namespace rad

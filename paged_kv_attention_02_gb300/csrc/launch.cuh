@@ -6,27 +6,34 @@
 
 namespace rad {
 
+// Persistent launch: as many CTAs as fit on the device at once (never more
+// than there are work items).
 template <class C>
-cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int grid,
-                       cudaStream_t st) {
+cudaError_t launch_cfg(const AttnParams& p, int sms, cudaStream_t st) {
     auto kern = attn_tile_kernel<C>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::NTHREADS, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    long long grid = (long long)sms * per_sm;
+    if (grid > p.n_items) grid = p.n_items;
+    if (grid < 1) grid = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(C::NTHREADS, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = st;
-    return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
+    return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 template <int D, bool FP8>
-cudaError_t launch_family(int family, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const AttnParams& p, int grid, cudaStream_t st) {
+cudaError_t launch_family(int family, const AttnParams& p, int sms, cudaStream_t st) {
     switch (family) {
-        case kFamDecode: return launch_cfg<typename Pick<D, FP8, kFamDecode>::T>(tk, tv, p, grid, st);
-        case kFamVerify: return launch_cfg<typename Pick<D, FP8, kFamVerify>::T>(tk, tv, p, grid, st);
-        default: return launch_cfg<typename Pick<D, FP8, kFamWide>::T>(tk, tv, p, grid, st);
+        case kFamDecode: return launch_cfg<typename Pick<D, FP8, kFamDecode>::T>(p, sms, st);
+        case kFamVerify: return launch_cfg<typename Pick<D, FP8, kFamVerify>::T>(p, sms, st);
+        default: return launch_cfg<typename Pick<D, FP8, kFamWide>::T>(p, sms, st);
     }
 }
 

@@ -2,7 +2,6 @@
 // kernel choice, workspace layout, TMA descriptors and the launch.
 #include <cuda.h>
 #include <cuda_runtime.h>
-#include <cudaTypedefs.h>
 
 #include <atomic>
 #include <cmath>
@@ -24,9 +23,6 @@ struct DeviceInfo {
     int cc_major = 0, cc_minor = 0;
 };
 DeviceInfo g_dev[kMaxDevices];
-
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::atomic<int> g_encode_ready{0};
 
 bool is_aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -113,39 +109,6 @@ int device_info(int* dev_out, int* sms_out) {
     return RAD_OK;
 }
 
-int get_encoder() {
-    if (g_encode_ready.load(std::memory_order_acquire)) return RAD_OK;
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || fn == nullptr)
-        return RAD_E_CUDA;
-    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    g_encode_ready.store(1, std::memory_order_release);
-    return RAD_OK;
-}
-
-// 4-D view of a pool [num_pages*page_size tokens][n_head_kv][head_dim] whose
-// innermost dimension is cut into 128-byte rows, so that one box is one page of
-// one KV head and the tile lands in shared memory with 128-byte swizzling.
-int encode_pool_map(CUtensorMap* m, const void* pool, int kv_dtype, int head_dim, int n_head_kv,
-                    int page_size, int num_pages) {
-    const int e = kv_dtype == RAD_KV_FP8_E4M3 ? 1 : 2;
-    const int boxw = 128 / e;
-    cuuint64_t dims[4] = {(cuuint64_t)boxw, (cuuint64_t)(head_dim / boxw), (cuuint64_t)n_head_kv,
-                          (cuuint64_t)num_pages * (cuuint64_t)page_size};
-    cuuint64_t strides[3] = {128, (cuuint64_t)head_dim * e, (cuuint64_t)n_head_kv * head_dim * e};
-    cuuint32_t box[4] = {(cuuint32_t)boxw, (cuuint32_t)(head_dim / boxw), 1, (cuuint32_t)page_size};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = g_encode(m,
-                          e == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
-                          const_cast<void*>(pool), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? RAD_OK : RAD_E_CUDA;
-}
-
 }  // namespace
 
 extern "C" {
@@ -169,8 +132,11 @@ int rad_attn_paged(const void* q, const void* k_pool, const void* v_pool, const 
     int rc = check_scalars(groups, rows, n_head, n_head_kv, head_dim, page_size, pages_per_seq, kv_dtype);
     if (rc != RAD_OK) return rc;
     if (num_pages <= 0 || (long long)num_pages * page_size > 0x7FFFFFFFll) return RAD_E_SHAPE;
+    if (make_plan(groups, rows, n_head, n_head_kv, head_dim, page_size, pages_per_seq, kv_dtype).n_items >
+        0x7FFFFFFFll)
+        return RAD_E_SHAPE;
     if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !out) return RAD_E_ARG;
-    if (!is_aligned(q, 16) || !is_aligned(k_pool, 16) || !is_aligned(v_pool, 16) || !is_aligned(out, 2) ||
+    if (!is_aligned(q, 16) || !is_aligned(k_pool, 16) || !is_aligned(v_pool, 16) || !is_aligned(out, 16) ||
         !is_aligned(page_table, 4) || !is_aligned(seq_lens, 4) || !is_aligned(err_word, 4))
         return RAD_E_ARG;
     const bool fp8 = kv_dtype == RAD_KV_FP8_E4M3;
@@ -184,16 +150,11 @@ int rad_attn_paged(const void* q, const void* k_pool, const void* v_pool, const 
     int dev = 0, sms = 0;
     rc = device_info(&dev, &sms);
     if (rc != RAD_OK) return rc;
-    rc = get_encoder();
-    if (rc != RAD_OK) return rc;
-
-    CUtensorMap tk, tv;
-    if (encode_pool_map(&tk, k_pool, kv_dtype, head_dim, n_head_kv, page_size, num_pages) != RAD_OK ||
-        encode_pool_map(&tv, v_pool, kv_dtype, head_dim, n_head_kv, page_size, num_pages) != RAD_OK)
-        return RAD_E_CUDA;
 
     AttnParams p{};
     p.q = static_cast<const __nv_bfloat16*>(q);
+    p.k_pool = static_cast<const uint8_t*>(k_pool);
+    p.v_pool = static_cast<const uint8_t*>(v_pool);
     p.page_table = page_table;
     p.seq_lens = seq_lens;
     p.k_scales = fp8 ? k_scales : nullptr;
@@ -213,7 +174,7 @@ int rad_attn_paged(const void* q, const void* k_pool, const void* v_pool, const 
     p.qtv = pl.qtv;
     p.max_splits = pl.max_splits;
     p.split_len = pl.split_len;
-    p.n_items = pl.n_items;
+    p.n_items = (int)pl.n_items;
     p.scale_log2 = scale * 1.4426950408889634f;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (pl.total_bytes > 0) {
@@ -224,14 +185,11 @@ int rad_attn_paged(const void* q, const void* k_pool, const void* v_pool, const 
         p.part_acc = reinterpret_cast<float*>(ws + pl.counters_bytes + pl.flags_bytes + pl.ml_bytes);
         if (cudaMemsetAsync(p.counters, 0, pl.counters_bytes, st) != cudaSuccess) return RAD_E_CUDA;
     }
-    const long long grid = pl.n_items < (long long)sms ? pl.n_items : (long long)sms;
     cudaError_t e;
     if (head_dim == 128)
-        e = fp8 ? rad::launch_d128_fp8(pl.family, tk, tv, p, (int)grid, st)
-                : rad::launch_d128_bf16(pl.family, tk, tv, p, (int)grid, st);
+        e = fp8 ? rad::launch_d128_fp8(pl.family, p, sms, st) : rad::launch_d128_bf16(pl.family, p, sms, st);
     else
-        e = fp8 ? rad::launch_d256_fp8(pl.family, tk, tv, p, (int)grid, st)
-                : rad::launch_d256_bf16(pl.family, tk, tv, p, (int)grid, st);
+        e = fp8 ? rad::launch_d256_fp8(pl.family, p, sms, st) : rad::launch_d256_bf16(pl.family, p, sms, st);
     return e == cudaSuccess ? RAD_OK : RAD_E_CUDA;
 }
 
@@ -247,10 +205,10 @@ int rad_attn_paged_describe(int32_t rows, int32_t n_head, int32_t n_head_kv, int
     const rad::TileInfo& t = pl.tile;
     snprintf(buf, buf_len,
              "attn_tile family=%s head_dim=%d kv=%s query_rows_per_kv_head=%d tile_rows=%d "
-             "warps(q=%d,k=%d)+producer n_tiles_per_warp=%d keys_per_stage=%d stages=%d split_len=%d "
-             "threads=%d smem=%d mma=m16n8k16.%s",
+             "warps(q=%d,k=%d)+2 producers n_tiles_per_warp=%d keys_per_stage=%d stages=%d split_len=%d "
+             "threads=%d smem=%d ctas_per_sm=%d mma=m16n8k16.%s",
              family_name(pl.family), head_dim, kv_dtype == RAD_KV_FP8_E4M3 ? "fp8e4m3" : "bf16", pl.M,
-             t.QT, t.WQ, t.WK, t.NQW, t.KS, t.NS, pl.split_len, t.threads, t.smem,
+             t.QT, t.WQ, t.WK, t.NQW, t.KS, t.NS, pl.split_len, t.threads, t.smem, t.minb,
              kv_dtype == RAD_KV_FP8_E4M3 ? "f16" : "bf16");
     return RAD_OK;
 }

@@ -14,8 +14,8 @@ constexpr int kSplitLen = 512;
 constexpr int kSplitMaxRows = 256;
 
 template <int D, bool FP8, int F> struct Pick;
-//                                         D    FP8   WQ NQW WK  KS  NS
-template <> struct Pick<128, false, kFamDecode> { using T = TileCfg<128, false, 1, 1, 4, 64, 6>; };
+//                                         D    FP8   WQ NQW WK  KS  NS  CTAs/SM
+template <> struct Pick<128, false, kFamDecode> { using T = TileCfg<128, false, 1, 1, 2, 32, 6, 2>; };
 template <> struct Pick<128, false, kFamVerify> { using T = TileCfg<128, false, 2, 2, 2, 64, 5>; };
 template <> struct Pick<128, false, kFamWide>   { using T = TileCfg<128, false, 4, 2, 1, 64, 4>; };
 template <> struct Pick<128, true,  kFamDecode> { using T = TileCfg<128, true,  1, 1, 4, 64, 8>; };
@@ -29,13 +29,13 @@ template <> struct Pick<256, true,  kFamVerify> { using T = TileCfg<256, true,  
 template <> struct Pick<256, true,  kFamWide>   { using T = TileCfg<256, true,  4, 1, 1, 32, 8>; };
 
 struct TileInfo {
-    int D, fp8, WQ, NQW, WK, KS, NS, QT, threads, smem;
+    int D, fp8, WQ, NQW, WK, KS, NS, QT, threads, smem, minb;
 };
 
 template <class C>
 constexpr TileInfo info_of() {
     return TileInfo{C::D, C::FP8 ? 1 : 0, C::WQ, C::NQW, C::WK, C::KS, C::NS, C::QT, C::NTHREADS,
-                    C::SMEM_BYTES};
+                    C::SMEM_BYTES, C::MINB};
 }
 
 template <int D, bool FP8>
@@ -48,13 +48,9 @@ inline TileInfo tile_info(int family) {
 }
 
 // One launcher per (head_dim, dtype) translation unit.
-cudaError_t launch_d128_bf16(int family, const CUtensorMap& tk, const CUtensorMap& tv,
-                             const AttnParams& p, int grid, cudaStream_t st);
-cudaError_t launch_d128_fp8(int family, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const AttnParams& p, int grid, cudaStream_t st);
-cudaError_t launch_d256_bf16(int family, const CUtensorMap& tk, const CUtensorMap& tv,
-                             const AttnParams& p, int grid, cudaStream_t st);
-cudaError_t launch_d256_fp8(int family, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const AttnParams& p, int grid, cudaStream_t st);
+cudaError_t launch_d128_bf16(int family, const AttnParams& p, int sms, cudaStream_t st);
+cudaError_t launch_d128_fp8(int family, const AttnParams& p, int sms, cudaStream_t st);
+cudaError_t launch_d256_bf16(int family, const AttnParams& p, int sms, cudaStream_t st);
+cudaError_t launch_d256_fp8(int family, const AttnParams& p, int sms, cudaStream_t st);
 
 }  // namespace rad
