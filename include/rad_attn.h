@@ -152,6 +152,43 @@ int rad_attn_paged(const void* q, const void* k_pool, const void* v_pool,
                    rad_stream_t stream);
 
 /*
+ * rad_attn_paged_noalloc -- the same op for callers that cannot allocate.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot obtain device memory at call time: a runtime that plans all of
+ * its device memory once, at load time (its own arena, or a framework's
+ * caching allocator that owns the device), and code handed only the tensors
+ * of the call (a plugin given inputs and outputs but no scratch buffer).
+ * For them a per-call cudaMalloc either fails once the arena has reserved
+ * the device or breaks the one-time memory plan.
+ *
+ * Arguments and results are those of rad_attn_paged without `workspace` and
+ * `workspace_bytes`: the scratch lives in a library-owned device array of
+ * RAD_NOALLOC_SCRATCH_BYTES, which every GPU that loads the library holds
+ * until the process exits.  The call allocates nothing (no cudaMalloc, no
+ * cudaFree, no allocating library routine).
+ *   - A call whose scratch need (rad_attn_paged_workspace_bytes) exceeds
+ *     RAD_NOALLOC_SCRATCH_BYTES returns RAD_E_WORKSPACE and launches nothing.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first
+ *     call before any stream capture on the device.
+ *   - Every call shares the one array and leaves its contents behind; each
+ *     call clears the part that must start at zero on its own stream.  Calls
+ *     whose executions overlap on the GPU (different streams, or different
+ *     host threads without ordering) race on the array and give undefined
+ *     results: order them on one stream.
+ */
+#define RAD_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+int rad_attn_paged_noalloc(const void* q, const void* k_pool, const void* v_pool,
+                           const int32_t* page_table, const int32_t* seq_lens, int32_t groups,
+                           int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_dim,
+                           int32_t page_size, int32_t pages_per_seq, int32_t num_pages,
+                           float scale, int32_t kv_dtype, const float* k_scales,
+                           const float* v_scales, void* out, uint32_t* err_word,
+                           rad_stream_t stream);
+
+/*
  * Writes a one-line, NUL-terminated description of the kernel a call of this
  * shape would launch (family, tile, split length, stages) into buf (host
  * memory, buf_len bytes) -- the pattern of "Radiance architecture plugins",

@@ -31,7 +31,10 @@ RAD_ERRW_QRANGE = 4
 RAD_ERRW_TIMEOUT = 8
 
 EXPORTS = ("rad_attn_paged", "rad_attn_paged_workspace_bytes", "rad_attn_paged_describe",
-           "rad_attn_status_string", "rad_attn_version")
+           "rad_attn_status_string", "rad_attn_version", "rad_attn_paged_noalloc")
+
+# Size of the library-owned scratch of rad_attn_paged_noalloc (include/rad_attn.h).
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _lib = None
 
@@ -63,6 +66,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.rad_attn_status_string.argtypes = [ctypes.c_int]
     lib.rad_attn_version.restype = ctypes.c_char_p
     lib.rad_attn_version.argtypes = []
+    lib.rad_attn_paged_noalloc.restype = ctypes.c_int
+    lib.rad_attn_paged_noalloc.argtypes = [p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, i32,
+                                           ctypes.c_float, i32, p, p, p, p, p]
     _lib = lib
     return lib
 
@@ -140,3 +146,24 @@ def call_raw(q_ptr, k_ptr, v_ptr, table_ptr, lens_ptr, groups, rows, n_head, n_h
         vp(q_ptr), vp(k_ptr), vp(v_ptr), vp(table_ptr), vp(lens_ptr), groups, rows, n_head, n_head_kv,
         head_dim, page_size, pages_per_seq, num_pages, float(scale), kv_dtype, vp(ks_ptr), vp(vs_ptr),
         vp(out_ptr), vp(ws_ptr), ws_bytes, vp(err_ptr), vp(stream_ptr)))
+
+
+def attn_paged_noalloc(q, k_pool, v_pool, page_table, seq_lens, *, rows, n_head, n_head_kv, head_dim,
+                       page_size, scale, kv_dtype=RAD_KV_BF16, k_scales=None, v_scales=None, out,
+                       err_word=None, stream=None):
+    """rad_attn_paged_noalloc: the op with the library's own fixed scratch.
+
+    For callers that cannot allocate device memory per call (a runtime whose
+    memory is planned once at load time, or code handed only the call's
+    tensors).  `out` must be given; nothing is allocated here or in the
+    library.  Raises RadAttnError with RAD_E_WORKSPACE when the call needs
+    more than NOALLOC_SCRATCH_BYTES of scratch.
+    """
+    groups = int(seq_lens.shape[0])
+    rc = load().rad_attn_paged_noalloc(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(seq_lens), groups, rows, n_head,
+        n_head_kv, head_dim, page_size, int(page_table.shape[1]), int(k_pool.shape[0]), float(scale),
+        kv_dtype, _ptr(k_scales), _ptr(v_scales), _ptr(out), _ptr(err_word), _stream_handle(stream))
+    if rc != RAD_OK:
+        raise RadAttnError(rc, "rad_attn_paged_noalloc")
+    return out
