@@ -172,8 +172,9 @@ int rad_attn_paged(const void* q, const void* k_pool, const void* v_pool,
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first
  *     call before any stream capture on the device.
- *   - Every call shares the one array and leaves its contents behind; each
- *     call clears the part that must start at zero on its own stream.  Calls
+ *   - Every call shares the one array and leaves its contents behind; no
+ *     part of it needs to start at zero (a call reads only what it wrote
+ *     earlier in the same call).  Calls
  *     whose executions overlap on the GPU (different streams, or different
  *     host threads without ordering) race on the array and give undefined
  *     results: order them on one stream.

@@ -27,11 +27,11 @@
 // head) at no worse than half-used n-tiles.
 //
 // Splits.  With split_len > 0 a sequence's keys are cut into ceil(L/split_len)
-// ranges whose count and boundaries depend only on L.  Each range writes a
-// partial (running max, sum, unnormalised accumulator) to the workspace; the
-// CTA that finishes a (g, kvh, qt) last -- found with an atomic ticket, no
-// waiting -- merges the partials in split order 0..n-1.  Every output row is
-// therefore the same function of its own sequence whatever else is in the
+// ranges whose count and boundaries depend only on L.  A sequence with one
+// range writes its output rows directly; otherwise each range writes a partial
+// (running max, sum, unnormalised accumulator) to the workspace and the
+// combine kernel merges the partials in split order 0..n-1.  Every output row
+// is therefore the same function of its own sequence whatever else is in the
 // call ("Adding a model", step 4: verified rows must equal decode rows bit
 // for bit).
 //
@@ -76,12 +76,12 @@ struct AttnParams {
     float* part_acc;       // [slots][qtv][D]
     float* part_ml;        // [slots][qtv][2]  (max in log2 units, sum)
     uint32_t* part_flag;   // [slots]         page-id error seen by the split
-    uint32_t* counters;    // [groups * n_head_kv * n_qtiles]; zero at launch
     uint32_t* err_word;    // optional
     int groups, rows, n_head, n_head_kv, ratio, page_size, pages_per_seq, num_pages;
     int M;                 // rows * ratio: query rows per KV head
     int n_qtiles;          // ceil(M / QT)
     int qtv;               // query rows stored per partial slot: min(M, QT)
+    int qt_rows;           // QT of the split kernel's tile
     int max_splits;        // 1 without splitting
     int split_len;         // keys per split; 0 = one range over the whole context
     int n_items;           // max_splits * groups * n_head_kv * n_qtiles
@@ -124,16 +124,11 @@ struct TileCfg {
     static constexpr int OFF_MISC = OFF_BARS + (2 * NS + 4) * 8;
     static constexpr int SMEM_USED = OFF_MISC + 16;
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;   // base alignment slack
-    static_assert(KS % 16 == 0 && SUBS % WK == 0, "stage keys must split evenly over key warps");
+    static_assert(KS % 32 == 0, "a stage holds whole pages of either page size (16 or 32 slots)");
+    static_assert(SUBS % WK == 0, "stage keys must split evenly over key warps");
     static_assert(MAX_PAGES_STAGE <= 4, "stage meta holds 4 pages");
     static_assert(D % 32 == 0, "head_dim multiple of 32");
     static_assert(SMEM_BYTES * MINB <= 233472 - 1024 * MINB, "shared memory budget");
-    // split-combine staging in the merge buffer: (max, sum) pairs, weights and
-    // per-column state for CH splits at a time
-    static constexpr int MERGE_FLOATS = WK * QT * MSTRIDE;
-    static constexpr int CH = (MERGE_FLOATS - 3 * QT) / (3 * QT) > 256 ? 256 : (MERGE_FLOATS - 3 * QT) / (3 * QT);
-    static constexpr int OWN = (QT * D / 4 + NCT - 1) / NCT;   // float4 outputs per thread
-    static_assert(CH >= 8, "combine chunk");
 };
 
 // Byte offset, inside a stage tile, of element d of key `key` (both relative to
@@ -214,102 +209,6 @@ __device__ __forceinline__ int d_of(int mt, int row16) {
     } else {
         return 16 * mt + row16;
     }
-}
-
-// Merges the partials of splits 0..n-1 of one (sequence, KV head, query tile)
-// in split order, in chunks of C::CH splits, and writes the bf16 output rows.
-// Run by every consumer thread of the CTA that took the last ticket.
-template <class C>
-__device__ __forceinline__ void combine_splits(const AttnParams& p, const ItemPlan& it, long long gq,
-                                               uint8_t* smem, int tid) {
-    const int ns = it.n_splits, ncol = it.m_end - it.m0;
-    constexpr int D4 = C::D / 4;
-    const long long slot0 = gq * p.max_splits;
-    float* ml_s = reinterpret_cast<float*>(smem + C::OFF_MERGE);   // [CH][ncol][2]
-    float* w_s = ml_s + 2 * C::CH * C::QT;                          // [CH][ncol]
-    float* st_m = w_s + C::CH * C::QT;                              // [ncol] running max
-    float* st_l = st_m + C::QT;                                     // [ncol] running sum
-    float* st_a = st_l + C::QT;                                     // [ncol] rescale of the old state
-    if (tid < ncol) {
-        st_m[tid] = -CUDART_INF_F;
-        st_l[tid] = 0.f;
-    }
-    float4 acc[C::OWN];
-#pragma unroll
-    for (int k = 0; k < C::OWN; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    uint32_t any_bad = 0;
-    for (int s0 = 0; s0 < ns; s0 += C::CH) {
-        const int cn = min(C::CH, ns - s0);
-        named_barrier_sync(1, C::NCT);
-        for (int i = tid; i < cn * ncol; i += C::NCT) {
-            const int s = i / ncol, col = i - s * ncol;
-            const float2 v = __ldcg(reinterpret_cast<const float2*>(p.part_ml + (slot0 + s0 + s) * p.qtv * 2) + col);
-            ml_s[2 * i] = v.x;
-            ml_s[2 * i + 1] = v.y;
-        }
-        for (int i = tid; i < cn; i += C::NCT) any_bad |= __ldcg(p.part_flag + slot0 + s0 + i);
-        named_barrier_sync(1, C::NCT);
-        if (tid < ncol) {
-            const int col = tid;
-            float mx = st_m[col];
-            for (int s = 0; s < cn; ++s) mx = fmaxf(mx, ml_s[2 * (s * ncol + col)]);
-            const float m_use = (mx == -CUDART_INF_F) ? 0.f : mx;
-            const float alpha = exp2f(st_m[col] - m_use);
-            float l = st_l[col] * alpha;
-            for (int s = 0; s < cn; ++s) {
-                const float w = exp2f(ml_s[2 * (s * ncol + col)] - m_use);
-                w_s[s * ncol + col] = w;
-                l += w * ml_s[2 * (s * ncol + col) + 1];
-            }
-            st_m[col] = mx;
-            st_l[col] = l;
-            st_a[col] = alpha;
-        }
-        named_barrier_sync(1, C::NCT);
-#pragma unroll
-        for (int k = 0; k < C::OWN; ++k) {
-            const int e = tid + k * C::NCT;
-            if (e < ncol * D4) {
-                const int col = e / D4, d4 = e - col * D4;
-                const float a = st_a[col];
-                float4 r = acc[k];
-                r.x *= a; r.y *= a; r.z *= a; r.w *= a;
-                const float4* src = reinterpret_cast<const float4*>(p.part_acc + (slot0 + s0) * p.qtv * C::D) +
-                                    col * D4 + d4;
-                const long long sstride = (long long)p.qtv * D4;
-                for (int s = 0; s < cn; s += 8) {
-                    float4 v[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        v[i] = (s + i < cn) ? __ldcg(src + (s + i) * sstride) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        if (s + i < cn) {
-                            const float w = w_s[(s + i) * ncol + col];
-                            r.x += w * v[i].x; r.y += w * v[i].y; r.z += w * v[i].z; r.w += w * v[i].w;
-                        }
-                    }
-                }
-                acc[k] = r;
-            }
-        }
-    }
-    any_bad = named_barrier_or(1, C::NCT, any_bad != 0) ? 1u : 0u;
-#pragma unroll
-    for (int k = 0; k < C::OWN; ++k) {
-        const int e = tid + k * C::NCT;
-        if (e < ncol * D4) {
-            const int col = e / D4, d4 = e - col * D4;
-            const float inv = any_bad ? 0.f : 1.f / st_l[col];
-            const int m = it.m0 + col;
-            const int r = m / p.ratio, hl = m - r * p.ratio;
-            __nv_bfloat16* o = p.out + (((long long)it.g * p.rows + r) * p.n_head + it.kvh * p.ratio + hl) * C::D + 4 * d4;
-            const float4 a = any_bad ? make_float4(0.f, 0.f, 0.f, 0.f) : acc[k];
-            *reinterpret_cast<__nv_bfloat162*>(o) = __floats2bfloat162_rn(a.x * inv, a.y * inv);
-            *reinterpret_cast<__nv_bfloat162*>(o + 2) = __floats2bfloat162_rn(a.z * inv, a.w * inv);
-        }
-    }
-    if (any_bad && tid == 0 && p.err_word) atomicOr(p.err_word, kErrPage);
 }
 
 template <class C>
@@ -809,20 +708,8 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
             named_barrier_sync(1, C::NCT);
             continue;
         }
-        // ---------------- ticket: the last split of (g, kvh, qt) merges all of them
-        // All threads' partial stores are ordered before thread 0's gpu-scope
-        // fence by the barrier; thread 0 then takes a ticket.
-        named_barrier_sync(1, C::NCT);
-        bool last = false;
-        if (tid == 0) {
-            __stcg(p.part_flag + slot_idx, item_bad ? 1u : 0u);
-            __threadfence();
-            last = atomicAdd(p.counters + gq, 1u) == (uint32_t)(it.n_splits - 1);
-            if (last) __threadfence();
-        }
-        if (named_barrier_or(1, C::NCT, last)) {
-            combine_splits<C>(p, it, gq, smem, tid);
-        }
+        if (tid == 0) __stcg(p.part_flag + slot_idx, item_bad ? 1u : 0u);
+        // the merge buffers are rewritten by the next item
         named_barrier_sync(1, C::NCT);
     }
     if (abort) {

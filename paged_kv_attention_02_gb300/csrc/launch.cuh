@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda_runtime.h>
 
+#include "combine.cuh"
 #include "tile_configs.cuh"
 
 namespace rad {
@@ -28,13 +29,31 @@ cudaError_t launch_cfg(const AttnParams& p, int sms, cudaStream_t st) {
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+// The split combine: one CTA per (sequence, KV head, query tile, group of
+// kCombineCols rows); CTAs of sequences with a single split exit at once.
+template <int D>
+cudaError_t launch_combine(const AttnParams& p, cudaStream_t st) {
+    const long long n_cg = (p.qt_rows + kCombineCols - 1) / kCombineCols;
+    const long long grid = (long long)p.groups * p.n_head_kv * p.n_qtiles * n_cg;
+    if (grid > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kCombineThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    return cudaLaunchKernelEx(&cfg, attn_combine_kernel<D>, p);
+}
+
 template <int D, bool FP8>
 cudaError_t launch_family(int family, const AttnParams& p, int sms, cudaStream_t st) {
+    cudaError_t e;
     switch (family) {
-        case kFamDecode: return launch_cfg<typename Pick<D, FP8, kFamDecode>::T>(p, sms, st);
-        case kFamVerify: return launch_cfg<typename Pick<D, FP8, kFamVerify>::T>(p, sms, st);
-        default: return launch_cfg<typename Pick<D, FP8, kFamWide>::T>(p, sms, st);
+        case kFamDecode: e = launch_cfg<typename Pick<D, FP8, kFamDecode>::T>(p, sms, st); break;
+        case kFamVerify: e = launch_cfg<typename Pick<D, FP8, kFamVerify>::T>(p, sms, st); break;
+        default: e = launch_cfg<typename Pick<D, FP8, kFamWide>::T>(p, sms, st); break;
     }
+    if (e != cudaSuccess || p.split_len == 0 || p.max_splits <= 1) return e;
+    return launch_combine<D>(p, st);
 }
 
 }  // namespace rad

@@ -35,7 +35,7 @@ struct Plan {
     int ratio, M, n_qtiles, qtv, max_splits;
     rad::TileInfo tile;
     long long n_items;
-    size_t counters_bytes, flags_bytes, ml_bytes, acc_bytes, total_bytes;
+    size_t flags_bytes, ml_bytes, acc_bytes, total_bytes;
 };
 
 int check_scalars(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_dim,
@@ -73,12 +73,11 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
     pl.n_items = n_gq * pl.max_splits;
     if (pl.split_len > 0) {
         const long long slots = n_gq * pl.max_splits;
-        pl.counters_bytes = round_up((size_t)n_gq * 4, 256);
         pl.flags_bytes = round_up((size_t)slots * 4, 256);
         pl.ml_bytes = round_up((size_t)slots * pl.qtv * 2 * 4, 256);
         pl.acc_bytes = round_up((size_t)slots * pl.qtv * head_dim * 4, 256);
     }
-    pl.total_bytes = pl.counters_bytes + pl.flags_bytes + pl.ml_bytes + pl.acc_bytes;
+    pl.total_bytes = pl.flags_bytes + pl.ml_bytes + pl.acc_bytes;
     return pl;
 }
 
@@ -172,6 +171,7 @@ int rad_attn_paged(const void* q, const void* k_pool, const void* v_pool, const 
     p.M = pl.M;
     p.n_qtiles = pl.n_qtiles;
     p.qtv = pl.qtv;
+    p.qt_rows = pl.tile.QT;
     p.max_splits = pl.max_splits;
     p.split_len = pl.split_len;
     p.n_items = (int)pl.n_items;
@@ -179,11 +179,9 @@ int rad_attn_paged(const void* q, const void* k_pool, const void* v_pool, const 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (pl.total_bytes > 0) {
         char* ws = static_cast<char*>(workspace);
-        p.counters = reinterpret_cast<uint32_t*>(ws);
-        p.part_flag = reinterpret_cast<uint32_t*>(ws + pl.counters_bytes);
-        p.part_ml = reinterpret_cast<float*>(ws + pl.counters_bytes + pl.flags_bytes);
-        p.part_acc = reinterpret_cast<float*>(ws + pl.counters_bytes + pl.flags_bytes + pl.ml_bytes);
-        if (cudaMemsetAsync(p.counters, 0, pl.counters_bytes, st) != cudaSuccess) return RAD_E_CUDA;
+        p.part_flag = reinterpret_cast<uint32_t*>(ws);
+        p.part_ml = reinterpret_cast<float*>(ws + pl.flags_bytes);
+        p.part_acc = reinterpret_cast<float*>(ws + pl.flags_bytes + pl.ml_bytes);
     }
     cudaError_t e;
     if (head_dim == 128)
@@ -206,10 +204,11 @@ int rad_attn_paged_describe(int32_t rows, int32_t n_head, int32_t n_head_kv, int
     snprintf(buf, buf_len,
              "attn_tile family=%s head_dim=%d kv=%s query_rows_per_kv_head=%d tile_rows=%d "
              "warps(q=%d,k=%d)+2 producers n_tiles_per_warp=%d keys_per_stage=%d stages=%d split_len=%d "
-             "threads=%d smem=%d ctas_per_sm=%d mma=m16n8k16.%s",
+             "threads=%d smem=%d ctas_per_sm=%d mma=m16n8k16.%s%s",
              family_name(pl.family), head_dim, kv_dtype == RAD_KV_FP8_E4M3 ? "fp8e4m3" : "bf16", pl.M,
              t.QT, t.WQ, t.WK, t.NQW, t.KS, t.NS, pl.split_len, t.threads, t.smem, t.minb,
-             kv_dtype == RAD_KV_FP8_E4M3 ? "f16" : "bf16");
+             kv_dtype == RAD_KV_FP8_E4M3 ? "f16" : "bf16",
+             pl.split_len > 0 ? " + attn_combine (split order)" : "");
     return RAD_OK;
 }
 

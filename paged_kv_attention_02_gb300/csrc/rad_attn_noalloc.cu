@@ -62,9 +62,8 @@ extern "C" int rad_attn_paged_noalloc(const void* q, const void* k_pool, const v
         const int rc = scratch_address(&scratch);
         if (rc != RAD_OK) return rc;
     }
-    // rad_attn_paged clears the split counters it needs (an asynchronous memset
-    // on `stream`) before its kernel runs; the rest of the scratch needs no
-    // initialisation.
+    // The scratch needs no initialisation: the combine reads only partials
+    // written earlier in the same call.
     return rad_attn_paged(q, k_pool, v_pool, page_table, seq_lens, groups, rows, n_head, n_head_kv, head_dim,
                           page_size, pages_per_seq, num_pages, scale, kv_dtype, k_scales, v_scales, out, scratch,
                           need > 0 ? (size_t)RAD_NOALLOC_SCRATCH_BYTES : 0, err_word, stream);

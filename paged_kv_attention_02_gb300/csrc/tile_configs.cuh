@@ -10,23 +10,64 @@ enum Family : int { kFamDecode = 0, kFamVerify = 1, kFamWide = 2 };
 
 // Keys per split for calls of up to kSplitMaxRows rows; longer calls (prefill
 // chunks) run one range per query tile.  A multiple of every tile's KS.
-constexpr int kSplitLen = 512;
+#ifndef RAD_SPLIT_LEN
+#define RAD_SPLIT_LEN 1024
+#endif
+constexpr int kSplitLen = RAD_SPLIT_LEN;
 constexpr int kSplitMaxRows = 256;
 
+// Tile shapes: WQ, NQW, WK, KS, NS, CTAs per SM (see TileCfg).  Each can be
+// overridden at compile time (-DRAD_TILE_...="...") for tuning sweeps.
+#ifndef RAD_TILE_D128_BF16_DEC
+#define RAD_TILE_D128_BF16_DEC 1, 1, 2, 32, 3, 3
+#endif
+#ifndef RAD_TILE_D128_BF16_VER
+#define RAD_TILE_D128_BF16_VER 2, 2, 2, 64, 5, 1
+#endif
+#ifndef RAD_TILE_D128_BF16_WIDE
+#define RAD_TILE_D128_BF16_WIDE 4, 2, 1, 64, 4, 1
+#endif
+#ifndef RAD_TILE_D128_FP8_DEC
+#define RAD_TILE_D128_FP8_DEC 1, 1, 4, 64, 8, 1
+#endif
+#ifndef RAD_TILE_D128_FP8_VER
+#define RAD_TILE_D128_FP8_VER 2, 2, 2, 64, 3, 2
+#endif
+#ifndef RAD_TILE_D128_FP8_WIDE
+#define RAD_TILE_D128_FP8_WIDE 4, 2, 1, 64, 8, 1
+#endif
+#ifndef RAD_TILE_D256_BF16_DEC
+#define RAD_TILE_D256_BF16_DEC 1, 1, 2, 32, 2, 2
+#endif
+#ifndef RAD_TILE_D256_BF16_VER
+#define RAD_TILE_D256_BF16_VER 4, 1, 2, 32, 3, 1
+#endif
+#ifndef RAD_TILE_D256_BF16_WIDE
+#define RAD_TILE_D256_BF16_WIDE 4, 1, 1, 32, 4, 1
+#endif
+#ifndef RAD_TILE_D256_FP8_DEC
+#define RAD_TILE_D256_FP8_DEC 1, 1, 4, 64, 5, 1
+#endif
+#ifndef RAD_TILE_D256_FP8_VER
+#define RAD_TILE_D256_FP8_VER 4, 1, 2, 32, 7, 1
+#endif
+#ifndef RAD_TILE_D256_FP8_WIDE
+#define RAD_TILE_D256_FP8_WIDE 4, 1, 1, 32, 8, 1
+#endif
+
 template <int D, bool FP8, int F> struct Pick;
-//                                         D    FP8   WQ NQW WK  KS  NS  CTAs/SM
-template <> struct Pick<128, false, kFamDecode> { using T = TileCfg<128, false, 1, 1, 2, 32, 6, 2>; };
-template <> struct Pick<128, false, kFamVerify> { using T = TileCfg<128, false, 2, 2, 2, 64, 5>; };
-template <> struct Pick<128, false, kFamWide>   { using T = TileCfg<128, false, 4, 2, 1, 64, 4>; };
-template <> struct Pick<128, true,  kFamDecode> { using T = TileCfg<128, true,  1, 1, 4, 64, 8>; };
-template <> struct Pick<128, true,  kFamVerify> { using T = TileCfg<128, true,  2, 2, 2, 64, 8>; };
-template <> struct Pick<128, true,  kFamWide>   { using T = TileCfg<128, true,  4, 2, 1, 64, 8>; };
-template <> struct Pick<256, false, kFamDecode> { using T = TileCfg<256, false, 1, 1, 2, 32, 6>; };
-template <> struct Pick<256, false, kFamVerify> { using T = TileCfg<256, false, 4, 1, 2, 32, 3>; };
-template <> struct Pick<256, false, kFamWide>   { using T = TileCfg<256, false, 4, 1, 1, 32, 4>; };
-template <> struct Pick<256, true,  kFamDecode> { using T = TileCfg<256, true,  1, 1, 4, 64, 5>; };
-template <> struct Pick<256, true,  kFamVerify> { using T = TileCfg<256, true,  4, 1, 2, 32, 7>; };
-template <> struct Pick<256, true,  kFamWide>   { using T = TileCfg<256, true,  4, 1, 1, 32, 8>; };
+template <> struct Pick<128, false, kFamDecode> { using T = TileCfg<128, false, RAD_TILE_D128_BF16_DEC>; };
+template <> struct Pick<128, false, kFamVerify> { using T = TileCfg<128, false, RAD_TILE_D128_BF16_VER>; };
+template <> struct Pick<128, false, kFamWide>   { using T = TileCfg<128, false, RAD_TILE_D128_BF16_WIDE>; };
+template <> struct Pick<128, true,  kFamDecode> { using T = TileCfg<128, true,  RAD_TILE_D128_FP8_DEC>; };
+template <> struct Pick<128, true,  kFamVerify> { using T = TileCfg<128, true,  RAD_TILE_D128_FP8_VER>; };
+template <> struct Pick<128, true,  kFamWide>   { using T = TileCfg<128, true,  RAD_TILE_D128_FP8_WIDE>; };
+template <> struct Pick<256, false, kFamDecode> { using T = TileCfg<256, false, RAD_TILE_D256_BF16_DEC>; };
+template <> struct Pick<256, false, kFamVerify> { using T = TileCfg<256, false, RAD_TILE_D256_BF16_VER>; };
+template <> struct Pick<256, false, kFamWide>   { using T = TileCfg<256, false, RAD_TILE_D256_BF16_WIDE>; };
+template <> struct Pick<256, true,  kFamDecode> { using T = TileCfg<256, true,  RAD_TILE_D256_FP8_DEC>; };
+template <> struct Pick<256, true,  kFamVerify> { using T = TileCfg<256, true,  RAD_TILE_D256_FP8_VER>; };
+template <> struct Pick<256, true,  kFamWide>   { using T = TileCfg<256, true,  RAD_TILE_D256_FP8_WIDE>; };
 
 struct TileInfo {
     int D, fp8, WQ, NQW, WK, KS, NS, QT, threads, smem, minb;
