@@ -48,7 +48,11 @@ FALLBACK_HBM_GBS = 6800.0
 
 # DRAM traffic per launch from the committed ncu capture (profiles/), valid only
 # while the kernel sources hash to `src_sha256`.
-NCU_TRAFFIC: dict[str, dict] = {}
+NCU_TRAFFIC: dict[str, dict] = {
+    # profiles/attn_tile_batched_decode_64seq.md: 64-sequence capture scaled by KV bytes
+    "batched_decode": {"bytes_per_launch": 4_499_400_000 + 22_500_000,
+                       "src_sha256": "968cb4f717e04b40f0059ac10e6add4d96c0d0c1419d686d4171531fab6f1809"},
+}
 
 
 def kernel_source_hash() -> str:
