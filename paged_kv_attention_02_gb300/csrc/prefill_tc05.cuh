@@ -1,0 +1,459 @@
+// Prefill-chunk attention on the 5th-generation tensor cores (tcgen05, TMEM).
+//
+// A work item is (sequence g, KV head kvh, query tile qt): 128 query rows of
+// one KV head -- rows m = r*ratio + hl, the chunk's tokens r times the query
+// heads hl that share the KV head ("Radiance architecture plugins", section
+// "Declare: the metadata": n_head over n_head_kv) -- against keys
+// 0 .. kmax-1 of the sequence, causal per row: row r sees keys 0 .. L-R+r
+// ("kern manifest v7", $defs.Fill `seq_len`; $defs.Batch `context`: a
+// prefill's expansion of the cached rows).
+//
+// Warp roles (one CTA per SM, persistent over items, heavier query tiles first):
+//   warp 5      producer: TMA loads of the item's query rows (one 4-D box per
+//               128-byte column block) and, per 128-key tile, of every page's
+//               K and V rows (one 3-D box per page and column block) into a
+//               ring of 3 stages; pages past the tile's range are loaded from
+//               an out-of-range coordinate, which TMA fills with zeros.
+//   warp 4      MMA: lane 0 issues, per tile j,
+//                 S_j   = Q K_j^T  (M 128, N 128, K = head_dim; both operands
+//                                   in shared memory, K-major, 128-byte swizzle)
+//               into one of two TMEM buffers, and then, once the softmax has
+//               written P_{j-1}, O += P_{j-1} V_{j-1} (A = P from TMEM, B = V
+//               MN-major from shared memory); tcgen05.commit signals each.
+//               The warp also zeroes V rows past the sequence's end in the
+//               tile that holds its last page (P is 0 there, V must not be NaN).
+//   warps 0-3   softmax: thread t owns query row t (TMEM lane t); per tile it
+//               reads S_j with tcgen05.ld, masks, keeps the running max in
+//               log2 units and rescales O in TMEM only when the max grew by
+//               more than 2^8 (the row's arithmetic never depends on other
+//               rows), writes P as bf16 hi + lo (hi = bf16(p), lo = bf16(p-hi))
+//               back over S_j, and at the end reads O, divides by the sum and
+//               stores the bf16 row.
+// Every wait is bounded; on a time-out the CTA sets RAD_ERRW_TIMEOUT and
+// unwinds, waiting (bounded) for its copies and MMAs before freeing TMEM.
+#pragma once
+#include <cuda.h>
+
+#include "attn_tile.cuh"
+#include "tc05.cuh"
+
+namespace rad {
+
+struct PrefillCfg {
+    static constexpr int D = 128;
+    static constexpr int BM = 128;   // query rows per item
+    static constexpr int BN = 128;   // keys per tile
+    static constexpr int NS = 2;     // K/V stages
+    static constexpr int HB_BYTES = BN * 128;             // one 128-byte column block of a tile
+    static constexpr int TILE_BYTES = BN * D * 2;         // K or V tile
+    static constexpr int Q_BYTES = BM * D * 2;
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_STAGE = Q_BYTES;
+    static constexpr int OFF_BARS = OFF_STAGE + NS * STAGE_BYTES;
+    // q_full, q_empty, k_full[NS], v_full[NS], kv_empty[NS], s_full[2], p_full[2], pv_done, o_free, final
+    static constexpr int NBARS = 2 + 3 * NS + 2 + 2 + 3;
+    static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024 + 4096;   // + tail pad
+    static constexpr int NTHREADS = 6 * 32;
+    static constexpr uint32_t TMEM_COLS = 512;            // O [0,128), S0 [128,256), S1 [256,384)
+    static constexpr float RESCALE_LOG2 = 8.f;            // rescale O when the max grows past 2^8
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+struct PrefItem {
+    int g, kvh, qt, L;
+    bool seq_ok;
+    int m0, m_end, kmax, T;
+};
+
+__device__ __forceinline__ PrefItem plan_prefill(int item, const AttnParams& p) {
+    PrefItem it;
+    const int per_g = p.n_head_kv * p.n_qtiles;
+    it.g = item / per_g;
+    const int rem = item - it.g * per_g;
+    it.kvh = rem / p.n_qtiles;
+    it.qt = p.n_qtiles - 1 - (rem - it.kvh * p.n_qtiles);   // later tiles see more keys: first
+    it.L = __ldg(p.seq_lens + it.g);
+    it.seq_ok = it.L >= p.rows && (long long)it.L <= (long long)p.pages_per_seq * p.page_size;
+    it.m0 = it.qt * PrefillCfg::BM;
+    it.m_end = min(p.M, it.m0 + PrefillCfg::BM);
+    it.kmax = it.seq_ok ? it.L - p.rows + (it.m_end - 1) / p.ratio + 1 : 0;
+    it.T = (it.kmax + PrefillCfg::BN - 1) / PrefillCfg::BN;
+    return it;
+}
+
+__global__ void __launch_bounds__(PrefillCfg::NTHREADS, 1)
+    attn_prefill_tc05_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ AttnParams p) {
+    using C = PrefillCfg;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (base - raw_addr);
+
+    const uint32_t bar_q_full = base + C::OFF_BARS;
+    const uint32_t bar_q_empty = bar_q_full + 8;
+    const uint32_t bar_k_full = bar_q_empty + 8;
+    const uint32_t bar_v_full = bar_k_full + 8 * C::NS;
+    const uint32_t bar_kv_empty = bar_v_full + 8 * C::NS;
+    const uint32_t bar_s_full = bar_kv_empty + 8 * C::NS;
+    const uint32_t bar_p_full = bar_s_full + 16;
+    const uint32_t bar_pv_done = bar_p_full + 16;
+    const uint32_t bar_o_free = bar_pv_done + 8;
+    const uint32_t bar_final = bar_o_free + 8;
+    volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);  // [0] tmem, [1] abort
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar_q_full, 1);
+        mbar_init(bar_q_empty, 1);
+        for (int i = 0; i < C::NS; ++i) {
+            mbar_init(bar_k_full + 8 * i, 1);
+            mbar_init(bar_v_full + 8 * i, 1);
+            mbar_init(bar_kv_empty + 8 * i, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_s_full + 8 * i, 1);
+            mbar_init(bar_p_full + 8 * i, 4);
+        }
+        mbar_init(bar_pv_done, 1);
+        mbar_init(bar_o_free, 4);
+        mbar_init(bar_final, 1);
+        misc[1] = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 4) {
+        tmem_alloc(base + C::OFF_MISC, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    const uint32_t t_o = tmem;
+    const uint32_t t_s = tmem + 128;   // S buffer b at t_s + 128*b
+
+    const int n_items = p.n_items;
+    bool abort = false;
+
+    if (warp == 5) {
+        // ===================================================== producer
+        const uint64_t pol = policy_evict_last();   // K/V tiles are re-read by every query tile
+        const int P = p.page_size;
+        const int ppt = C::BN / P;
+        const int oob_tok = p.num_pages * P;
+        uint32_t sc = 0, ic = 0;
+        if (lane == 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+        }
+        for (int item = blockIdx.x; item < n_items && !abort; item += gridDim.x) {
+            const PrefItem it = plan_prefill(item, p);
+            if (!it.seq_ok) continue;
+            if (ic >= 1 && !mbar_wait_bounded(bar_q_empty, (ic - 1) & 1u, kWaitLimitNs)) {
+                abort = true;
+                break;
+            }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar_q_full, C::Q_BYTES);
+#pragma unroll
+                for (int hb = 0; hb < 2; ++hb)
+                    tma_load_4d(base + C::OFF_Q + hb * C::HB_BYTES, &tm_q, bar_q_full, hb * 64, it.kvh * p.ratio,
+                                it.m0 / p.ratio, it.g, pol);
+            }
+            ++ic;
+            const int page_hi = (it.kmax + P - 1) / P;
+            const int32_t* trow = p.page_table + (long long)it.g * p.pages_per_seq;
+            int batch0 = -1 << 30, my_pg = 0;
+            for (int j = 0; j < it.T; ++j) {
+                const uint32_t st = sc % C::NS, use = sc / C::NS;
+                if (use >= 1 && !mbar_wait_bounded(bar_kv_empty + 8 * st, (use - 1) & 1u, kWaitLimitNs)) {
+                    abort = true;
+                    break;
+                }
+                const int pstart = j * ppt;
+                if (pstart + ppt > batch0 + 32) {
+                    batch0 = pstart;
+                    const int pi = batch0 + lane;
+                    my_pg = 0;
+                    if (pi < page_hi) {
+                        const int pg = __ldg(trow + pi);
+                        my_pg = (pg < 0 || pg >= p.num_pages) ? 0 : pg;
+                    }
+                }
+                const uint32_t kdst = base + C::OFF_STAGE + st * C::STAGE_BYTES;
+                const uint32_t vdst = kdst + C::TILE_BYTES;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar_k_full + 8 * st, C::TILE_BYTES);
+                    mbar_arrive_expect_tx(bar_v_full + 8 * st, C::TILE_BYTES);
+                }
+                for (int i = 0; i < ppt; ++i) {
+                    const int pi = pstart + i;
+                    const int pg = __shfl_sync(0xffffffffu, my_pg, (pi - batch0) & 31);
+                    const int tok = pi < page_hi ? pg * P : oob_tok;
+                    if (lane == 0) {
+#pragma unroll
+                        for (int hb = 0; hb < 2; ++hb) {
+                            const uint32_t o = hb * C::HB_BYTES + i * P * 128;
+                            tma_load_3d(kdst + o, &tm_k, bar_k_full + 8 * st, hb * 64, it.kvh, tok, pol);
+                            tma_load_3d(vdst + o, &tm_v, bar_v_full + 8 * st, hb * 64, it.kvh, tok, pol);
+                        }
+                    }
+                }
+                ++sc;
+            }
+            if (misc[1]) abort = true;
+        }
+        // drain: nothing may still be landing in shared memory at exit
+        if (lane == 0) {
+            const uint32_t first = sc > (uint32_t)C::NS ? sc - C::NS : 0u;
+            for (uint32_t c = first; c < sc; ++c) {
+                mbar_wait_bounded(bar_k_full + 8 * (c % C::NS), (c / C::NS) & 1u, kWaitLimitNs);
+                mbar_wait_bounded(bar_v_full + 8 * (c % C::NS), (c / C::NS) & 1u, kWaitLimitNs);
+            }
+            if (ic >= 1) mbar_wait_bounded(bar_q_full, (ic - 1) & 1u, kWaitLimitNs);
+        }
+    } else if (warp == 4) {
+        // ===================================================== MMA issue
+        constexpr uint32_t idesc_qk = umma_idesc_bf16(C::BM, C::BN, 0, 0);
+        constexpr uint32_t idesc_pv = umma_idesc_bf16(C::BM, C::D, 0, 1);
+        uint32_t sc = 0, tc = 0, ic = 0;
+        bool issued = false;
+        for (int item = blockIdx.x; item < n_items && !abort; item += gridDim.x) {
+            const PrefItem it = plan_prefill(item, p);
+            if (!it.seq_ok) continue;
+            if (!mbar_wait_bounded(bar_q_full, ic & 1u, kWaitLimitNs)) {
+                abort = true;
+                break;
+            }
+            tc_fence_after();
+            // V rows to zero: slots past the sequence's end in its last page
+            const int P = p.page_size;
+            const int zero_lo = it.L, zero_hi = ((it.L + P - 1) / P) * P;
+            for (int j = 0; j <= it.T && !abort; ++j) {
+                if (j < it.T) {
+                    const uint32_t s_ = sc + j, st = s_ % C::NS;
+                    if (!mbar_wait_bounded(bar_k_full + 8 * st, (s_ / C::NS) & 1u, kWaitLimitNs)) {
+                        abort = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t b = (tc + j) & 1u;
+                    const uint32_t kb = base + C::OFF_STAGE + st * C::STAGE_BYTES;
+                    if (lane == 0) {
+#pragma unroll
+                        for (int kk = 0; kk < C::D / 16; ++kk) {
+                            const uint32_t off = (kk >> 2) * C::HB_BYTES + (kk & 3) * 32;
+                            tc_mma_ss(t_s + 128 * b, umma_desc_sw128(base + C::OFF_Q + off, 16, 1024),
+                                      umma_desc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                        }
+                        tc_commit(bar_s_full + 8 * b);
+                        issued = true;
+                    }
+                    __syncwarp();
+                }
+                if (j >= 1) {
+                    const int jj = j - 1;
+                    const uint32_t tcj = tc + jj, b = tcj & 1u;
+                    const uint32_t s_ = sc + jj, st = s_ % C::NS;
+                    if (!mbar_wait_bounded(bar_p_full + 8 * b, (tcj >> 1) & 1u, kWaitLimitNs) ||
+                        !mbar_wait_bounded(bar_v_full + 8 * st, (s_ / C::NS) & 1u, kWaitLimitNs) ||
+                        (jj == 0 && ic >= 1 && !mbar_wait_bounded(bar_o_free, (ic - 1) & 1u, kWaitLimitNs))) {
+                        abort = true;
+                        break;
+                    }
+                    const uint32_t vb = base + C::OFF_STAGE + st * C::STAGE_BYTES + C::TILE_BYTES;
+                    // zero V rows of keys past the sequence's end held by this tile
+                    const int key0 = jj * C::BN;
+                    const int z0 = max(zero_lo, key0) - key0, z1 = min(zero_hi, key0 + C::BN) - key0;
+                    if (z0 < z1) {
+                        for (int idx = lane; idx < (z1 - z0) * 16; idx += 32) {
+                            const int row = z0 + idx / 16, c16 = idx % 16;
+                            const uint32_t a = vb + (c16 >> 3) * C::HB_BYTES + row * 128 + (((c16 & 7) ^ (row & 7)) << 4);
+                            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                    }
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t sp = t_s + 128 * b;
+#pragma unroll
+                        for (int kk = 0; kk < C::BN / 16; ++kk) {
+                            const uint64_t bd = umma_desc_sw128(vb + kk * 16 * 128, C::HB_BYTES, 1024);
+                            tc_mma_ts(t_o, sp + kk * 8, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
+                            tc_mma_ts(t_o, sp + 64 + kk * 8, bd, idesc_pv, 1u);
+                        }
+                        tc_commit(bar_pv_done);
+                        tc_commit(bar_kv_empty + 8 * st);
+                    }
+                    __syncwarp();
+                }
+            }
+            if (lane == 0 && !abort) tc_commit(bar_q_empty);
+            __syncwarp();
+            sc += it.T;
+            tc += it.T;
+            ++ic;
+            if (misc[1]) abort = true;
+        }
+        // every MMA this thread issued is complete before TMEM is released
+        if (lane == 0 && issued) {
+            tc_commit(bar_final);
+            mbar_wait_bounded(bar_final, 0, kWaitLimitNs);
+        }
+        __syncwarp();
+    } else {
+        // ===================================================== softmax (warps 0-3)
+        const int t = threadIdx.x;                                  // query row of the tile
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;      // this warp's TMEM lanes
+        const float c = p.scale_log2;
+        uint32_t tc = 0;
+        for (int item = blockIdx.x; item < n_items && !abort; item += gridDim.x) {
+            const PrefItem it = plan_prefill(item, p);
+            const int m = it.m0 + t;
+            const bool valid = m < it.m_end;
+            const int r = m / p.ratio, hl = m - r * p.ratio;
+            __nv_bfloat16* orow =
+                p.out + (((long long)it.g * p.rows + r) * p.n_head + it.kvh * p.ratio + hl) * C::D;
+            if (!it.seq_ok) {
+                if (valid)
+                    for (int i = 0; i < C::D / 8; ++i) reinterpret_cast<uint4*>(orow)[i] = make_uint4(0, 0, 0, 0);
+                if (t == 0 && p.err_word) atomicOr(p.err_word, kErrSeqLen);
+                continue;
+            }
+            // the whole sequence's page ids must be valid, or all its rows are zero
+            bool bad = false;
+            const int npg = (it.L + p.page_size - 1) / p.page_size;
+            const int32_t* trow = p.page_table + (long long)it.g * p.pages_per_seq;
+            for (int i = t; i < npg; i += 128) {
+                const int pg = __ldg(trow + i);
+                bad |= (pg < 0 || pg >= p.num_pages);
+            }
+            bad = named_barrier_or(1, 128, bad);
+            const int nk = valid ? it.L - p.rows + r + 1 : it.L;
+            float m_run = -CUDART_INF_F, l_run = 0.f;
+            for (int j = 0; j < it.T; ++j) {
+                const uint32_t tcj = tc + j, b = tcj & 1u;
+                if (!mbar_wait_bounded(bar_s_full + 8 * b, (tcj >> 1) & 1u, kWaitLimitNs)) {
+                    abort = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sc_ = t_s + 128 * b + lane_off;
+                uint32_t sv[4][32];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) tmem_ld32(sc_ + 32 * q, sv[q]);
+                const int lim = nk - j * C::BN;   // columns >= lim are masked
+                float mx = -CUDART_INF_F;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        float v = __uint_as_float(sv[q][e]);
+                        if (32 * q + e >= lim) v = -CUDART_INF_F;
+                        sv[q][e] = __float_as_uint(v);
+                        mx = fmaxf(mx, v);
+                    }
+                if (mx != -CUDART_INF_F) {
+                    const float mx_s = mx * c;
+                    if (m_run == -CUDART_INF_F) {
+                        m_run = mx_s;
+                    } else if (mx_s > m_run + C::RESCALE_LOG2) {
+                        const float alpha = exp2f(m_run - mx_s);
+                        // PV of the previous tile must have landed before O is rescaled
+                        if (!mbar_wait_bounded(bar_pv_done, (tcj - 1) & 1u, kWaitLimitNs)) {
+                            abort = true;
+                            break;
+                        }
+                        tc_fence_after();
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t ov[32];
+                            tmem_ld32(t_o + lane_off + 32 * q, ov);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                            tmem_st32(t_o + lane_off + 32 * q, ov);
+                        }
+                        tmem_wait_st();
+                        l_run *= alpha;
+                        m_run = mx_s;
+                    }
+                }
+                const float m_use = (m_run == -CUDART_INF_F) ? 0.f : m_run;
+                float psum = 0.f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t hi[16], lo[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float p0 = exp2f(__uint_as_float(sv[q][2 * e]) * c - m_use);
+                        const float p1 = exp2f(__uint_as_float(sv[q][2 * e + 1]) * c - m_use);
+                        psum += p0 + p1;
+                        const uint32_t h = pack_bf16x2(p0, p1);
+                        hi[e] = h;
+                        lo[e] = pack_bf16x2(p0 - bf16_lo(h), p1 - bf16_hi(h));
+                    }
+                    tmem_st16(sc_ + 16 * q, hi);
+                    tmem_st16(sc_ + 64 + 16 * q, lo);
+                }
+                l_run += psum;
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_p_full + 8 * b);
+                if (misc[1]) {
+                    abort = true;
+                    break;
+                }
+            }
+            if (named_barrier_or(1, 128, abort)) {
+                abort = true;
+                break;
+            }
+            // ---- epilogue: O / l -> bf16
+            const uint32_t tcl = tc + it.T - 1;
+            if (!mbar_wait_bounded(bar_pv_done, tcl & 1u, kWaitLimitNs)) abort = true;
+            tc_fence_after();
+            const float inv = (bad || l_run == 0.f) ? 0.f : 1.f / l_run;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t ov[32];
+                tmem_ld32(t_o + lane_off + 32 * q, ov);
+                if (valid) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        w[e] = bad ? 0u
+                                   : pack_bf16x2(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
+                    uint4* dst = reinterpret_cast<uint4*>(orow + 32 * q);
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4) dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+                }
+            }
+            if (bad && t == 0 && p.err_word) atomicOr(p.err_word, kErrPage);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_o_free);
+            tc += it.T;
+            if (named_barrier_or(1, 128, abort)) {
+                abort = true;
+                break;
+            }
+        }
+    }
+    if (abort) {
+        misc[1] = 1;
+        if (lane == 0 && p.err_word) atomicOr(p.err_word, kErrTimeout);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 4) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+}  // namespace rad

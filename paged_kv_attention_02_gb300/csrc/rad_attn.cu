@@ -2,6 +2,7 @@
 // kernel choice, workspace layout, TMA descriptors and the launch.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <atomic>
 #include <cmath>
@@ -23,6 +24,9 @@ struct DeviceInfo {
     int cc_major = 0, cc_minor = 0;
 };
 DeviceInfo g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::atomic<int> g_encode_ready{0};
 
 bool is_aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -57,6 +61,13 @@ rad::TileInfo tile_for(int head_dim, int kv_dtype, int family) {
     return fp8 ? rad::tile_info<256, true>(family) : rad::tile_info<256, false>(family);
 }
 
+// Prefill chunks (no split) with head_dim 128 and bf16 pools run on the
+// tcgen05 kernel when whole query heads tile its 128-row blocks.
+bool use_prefill_tc(int32_t rows, int32_t ratio, int32_t head_dim, int32_t kv_dtype) {
+    return rows > rad::kSplitMaxRows && head_dim == 128 && kv_dtype == RAD_KV_BF16 && ratio <= 128 &&
+           128 % ratio == 0;
+}
+
 Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_dim,
                int32_t page_size, int32_t pages_per_seq, int32_t kv_dtype) {
     Plan pl{};
@@ -64,7 +75,10 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
     pl.M = rows * pl.ratio;
     pl.family = pl.M <= 8 ? rad::kFamDecode : (pl.M <= 32 ? rad::kFamVerify : rad::kFamWide);
     pl.split_len = rows <= rad::kSplitMaxRows ? rad::kSplitLen : 0;
-    pl.tile = tile_for(head_dim, kv_dtype, pl.family);
+    if (use_prefill_tc(rows, pl.ratio, head_dim, kv_dtype)) pl.family = rad::kFamPrefillTC;
+    pl.tile = pl.family == rad::kFamPrefillTC
+                  ? rad::TileInfo{128, 0, 4, 0, 0, rad::PrefillTileKeys, 3, 128, 192, 0, 1}
+                  : tile_for(head_dim, kv_dtype, pl.family);
     pl.n_qtiles = (pl.M + pl.tile.QT - 1) / pl.tile.QT;
     pl.qtv = pl.M < pl.tile.QT ? pl.M : pl.tile.QT;
     const long long cap_keys = (long long)pages_per_seq * page_size;
@@ -82,7 +96,32 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
 }
 
 const char* family_name(int f) {
-    return f == rad::kFamDecode ? "decode" : (f == rad::kFamVerify ? "verify" : "wide");
+    return f == rad::kFamDecode ? "decode"
+                                : (f == rad::kFamVerify ? "verify" : (f == rad::kFamWide ? "wide" : "prefill_tc05"));
+}
+
+int get_encoder() {
+    if (g_encode_ready.load(std::memory_order_acquire)) return RAD_OK;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return RAD_E_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    g_encode_ready.store(1, std::memory_order_release);
+    return RAD_OK;
+}
+
+// Tiled TMA descriptor with 128-byte swizzle over a bf16 tensor (dims and
+// box innermost first, strides in bytes for dims 1..rank-1).
+int encode_bf16_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                    const cuuint32_t* box) {
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? RAD_OK : RAD_E_CUDA;
 }
 
 // ------------------------------------------------------------------ device facts
@@ -184,7 +223,26 @@ int rad_attn_paged(const void* q, const void* k_pool, const void* v_pool, const 
         p.part_acc = reinterpret_cast<float*>(ws + pl.flags_bytes + pl.ml_bytes);
     }
     cudaError_t e;
-    if (head_dim == 128)
+    if (pl.family == rad::kFamPrefillTC) {
+        rc = get_encoder();
+        if (rc != RAD_OK) return rc;
+        // q viewed as [groups][rows][n_head][head_dim]: one box = 128 query rows
+        // (128/ratio tokens x the ratio heads of one KV head) x 64 columns
+        const cuuint64_t qd[4] = {(cuuint64_t)head_dim, (cuuint64_t)n_head, (cuuint64_t)rows, (cuuint64_t)groups};
+        const cuuint64_t qs[3] = {(cuuint64_t)head_dim * 2, (cuuint64_t)n_head * head_dim * 2,
+                                  (cuuint64_t)rows * n_head * head_dim * 2};
+        const cuuint32_t qb[4] = {64, (cuuint32_t)pl.ratio, (cuuint32_t)(128 / pl.ratio), 1};
+        // pools viewed as [tokens][n_head_kv][head_dim]: one box = one page of one KV head x 64 columns
+        const cuuint64_t kd[3] = {(cuuint64_t)head_dim, (cuuint64_t)n_head_kv,
+                                  (cuuint64_t)num_pages * (cuuint64_t)page_size};
+        const cuuint64_t ks[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)n_head_kv * head_dim * 2};
+        const cuuint32_t kb[3] = {64, 1, (cuuint32_t)page_size};
+        CUtensorMap tq, tk, tv;
+        if (encode_bf16_map(&tq, q, 4, qd, qs, qb) != RAD_OK || encode_bf16_map(&tk, k_pool, 3, kd, ks, kb) != RAD_OK ||
+            encode_bf16_map(&tv, v_pool, 3, kd, ks, kb) != RAD_OK)
+            return RAD_E_CUDA;
+        e = rad::launch_prefill_tc05(tq, tk, tv, p, sms, st);
+    } else if (head_dim == 128)
         e = fp8 ? rad::launch_d128_fp8(pl.family, p, sms, st) : rad::launch_d128_bf16(pl.family, p, sms, st);
     else
         e = fp8 ? rad::launch_d256_fp8(pl.family, p, sms, st) : rad::launch_d256_bf16(pl.family, p, sms, st);
@@ -201,6 +259,14 @@ int rad_attn_paged_describe(int32_t rows, int32_t n_head, int32_t n_head_kv, int
     }
     const Plan pl = make_plan(1, rows, n_head, n_head_kv, head_dim, page_size, 1, kv_dtype);
     const rad::TileInfo& t = pl.tile;
+    if (pl.family == rad::kFamPrefillTC) {
+        snprintf(buf, buf_len,
+                 "attn_prefill_tc05 family=%s head_dim=%d kv=bf16 query_rows_per_kv_head=%d tile_rows=128 "
+                 "keys_per_tile=%d stages=3 warps=4 softmax+1 mma+1 producer mma=tcgen05.kind::f16 M128xN128 "
+                 "(S and O in TMEM, P bf16 hi+lo from TMEM) split_len=0",
+                 family_name(pl.family), head_dim, pl.M, rad::PrefillTileKeys);
+        return RAD_OK;
+    }
     snprintf(buf, buf_len,
              "attn_tile family=%s head_dim=%d kv=%s query_rows_per_kv_head=%d tile_rows=%d "
              "warps(q=%d,k=%d)+2 producers n_tiles_per_warp=%d keys_per_stage=%d stages=%d split_len=%d "

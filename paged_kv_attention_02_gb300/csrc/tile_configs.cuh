@@ -6,7 +6,7 @@
 
 namespace rad {
 
-enum Family : int { kFamDecode = 0, kFamVerify = 1, kFamWide = 2 };
+enum Family : int { kFamDecode = 0, kFamVerify = 1, kFamWide = 2, kFamPrefillTC = 3 };
 
 // Keys per split for calls of up to kSplitMaxRows rows; longer calls (prefill
 // chunks) run one range per query tile.  A multiple of every tile's KS.
@@ -69,6 +69,8 @@ template <> struct Pick<256, true,  kFamDecode> { using T = TileCfg<256, true,  
 template <> struct Pick<256, true,  kFamVerify> { using T = TileCfg<256, true,  RAD_TILE_D256_FP8_VER>; };
 template <> struct Pick<256, true,  kFamWide>   { using T = TileCfg<256, true,  RAD_TILE_D256_FP8_WIDE>; };
 
+constexpr int PrefillTileKeys = 128;   // keys per tile of the tcgen05 prefill kernel
+
 struct TileInfo {
     int D, fp8, WQ, NQW, WK, KS, NS, QT, threads, smem, minb;
 };
@@ -93,5 +95,7 @@ cudaError_t launch_d128_bf16(int family, const AttnParams& p, int sms, cudaStrea
 cudaError_t launch_d128_fp8(int family, const AttnParams& p, int sms, cudaStream_t st);
 cudaError_t launch_d256_bf16(int family, const AttnParams& p, int sms, cudaStream_t st);
 cudaError_t launch_d256_fp8(int family, const AttnParams& p, int sms, cudaStream_t st);
+cudaError_t launch_prefill_tc05(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const AttnParams& p, int sms, cudaStream_t st);
 
 }  // namespace rad
