@@ -64,6 +64,13 @@ constexpr uint32_t kErrTimeout = 8u;
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
+// The running max of a row moves (and its accumulator is rescaled) only when
+// new logits exceed it by more than this many powers of two.
+#ifndef RAD_LAZY_RESCALE_LOG2
+#define RAD_LAZY_RESCALE_LOG2 8.f
+#endif
+constexpr float kLazyRescaleLog2 = RAD_LAZY_RESCALE_LOG2;
+
 struct AttnParams {
     const __nv_bfloat16* q;
     const uint8_t* k_pool;
@@ -524,27 +531,36 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
                         const int key = key0 + g8 + ((e >> 1) << 3);
                         x[e] = (key < nk[j][e & 1]) ? sacc[j][e] * kfac : -CUDART_INF_F;
                     }
+                    // The running max moves only when a sub-tile's max exceeds it by
+                    // more than 2^8 (or on the first keys); weights up to 2^8 are exact
+                    // to carry, and the accumulators are rescaled only then.
                     float alpha[2];
+                    bool moved = false;
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
                         float mx = fmaxf(x[c], x[c + 2]);
                         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
                         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
                         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                        const float m_new = fmaxf(m_run[j][c], mx);
-                        const float m_use = (m_new == -CUDART_INF_F) ? 0.f : m_new;
-                        alpha[c] = exp2f(m_run[j][c] - m_use);
-                        m_run[j][c] = m_new;
+                        alpha[c] = 1.f;
+                        if (mx > m_run[j][c] + kLazyRescaleLog2 || (m_run[j][c] == -CUDART_INF_F && mx != -CUDART_INF_F)) {
+                            alpha[c] = exp2f(m_run[j][c] - mx);
+                            m_run[j][c] = mx;
+                            moved = true;
+                        }
+                        const float m_use = (m_run[j][c] == -CUDART_INF_F) ? 0.f : m_run[j][c];
                         x[c] = exp2f(x[c] - m_use);
                         x[c + 2] = exp2f(x[c + 2] - m_use);
                         l_run[j][c] = l_run[j][c] * alpha[c] + (x[c] + x[c + 2]);
                     }
+                    if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
-                    for (int mt = 0; mt < C::D / 16; ++mt) {
-                        oacc[j][mt][0] *= alpha[0];
-                        oacc[j][mt][1] *= alpha[1];
-                        oacc[j][mt][2] *= alpha[0];
-                        oacc[j][mt][3] *= alpha[1];
+                        for (int mt = 0; mt < C::D / 16; ++mt) {
+                            oacc[j][mt][0] *= alpha[0];
+                            oacc[j][mt][1] *= alpha[1];
+                            oacc[j][mt][2] *= alpha[0];
+                            oacc[j][mt][3] *= alpha[1];
+                        }
                     }
                     if constexpr (C::FP8) {
                         pb[j][0] = movmatrix_trans(pack_f16x2(x[0] * vfac, x[1] * vfac));

@@ -6,12 +6,14 @@
 
 namespace rad {
 
+static_assert(PrefillTileKeys == PrefillCfg::BN, "host and kernel agree on the key tile");
+
 cudaError_t launch_prefill_tc05(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const AttnParams& p, int sms, cudaStream_t st) {
     auto kern = attn_prefill_tc05_kernel;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PrefillCfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    long long grid = sms;
+    long long grid = (long long)sms * PrefillCfg::CTAS;
     if (grid > p.n_items) grid = p.n_items;
     if (grid < 1) grid = 1;
     cudaLaunchConfig_t cfg = {};

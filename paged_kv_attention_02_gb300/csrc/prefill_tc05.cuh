@@ -36,15 +36,18 @@
 
 #include "attn_tile.cuh"
 #include "tc05.cuh"
+#include "tile_configs.cuh"
 
 namespace rad {
 
 struct PrefillCfg {
     static constexpr int D = 128;
     static constexpr int BM = 128;   // query rows per item
-    static constexpr int BN = 128;   // keys per tile
-    static constexpr int NS = 2;     // K/V stages
-    static constexpr int HB_BYTES = BN * 128;             // one 128-byte column block of a tile
+    static constexpr int BN = RAD_PREFILL_BN;     // keys per tile (64 or 128)
+    static constexpr int NS = RAD_PREFILL_NS;     // K/V stages
+    static constexpr int CTAS = RAD_PREFILL_CTAS; // CTAs sharing an SM
+    static constexpr int HB_BYTES = BN * 128;             // one 128-byte column block of a K/V tile
+    static constexpr int QHB_BYTES = BM * 128;            // one 128-byte column block of the query tile
     static constexpr int TILE_BYTES = BN * D * 2;         // K or V tile
     static constexpr int Q_BYTES = BM * D * 2;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
@@ -54,11 +57,16 @@ struct PrefillCfg {
     // q_full, q_empty, k_full[NS], v_full[NS], kv_empty[NS], s_full[2], p_full[2], pv_done, o_free, final
     static constexpr int NBARS = 2 + 3 * NS + 2 + 2 + 3;
     static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
-    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024 + 4096;   // + tail pad
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
     static constexpr int NTHREADS = 6 * 32;
-    static constexpr uint32_t TMEM_COLS = 512;            // O [0,128), S0 [128,256), S1 [256,384)
+    // tensor memory: O in columns [0,128), S buffer b in [128 + b*BN, 128 + (b+1)*BN);
+    // P of a tile is written over its S buffer as bf16 pairs: hi in the first
+    // BN/2 columns, lo in the next BN/2
+    static constexpr uint32_t TMEM_COLS = 128 + 2 * BN <= 256 ? 256 : 512;
     static constexpr float RESCALE_LOG2 = 8.f;            // rescale O when the max grows past 2^8
-    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(BN == 64 || BN == 128, "key tile");
+    static_assert(CTAS * (SMEM_BYTES + 1024) <= 233472, "shared memory budget");
+    static_assert(CTAS * TMEM_COLS <= 512, "tensor memory budget");
 };
 
 struct PrefItem {
@@ -83,7 +91,7 @@ __device__ __forceinline__ PrefItem plan_prefill(int item, const AttnParams& p) 
     return it;
 }
 
-__global__ void __launch_bounds__(PrefillCfg::NTHREADS, 1)
+__global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
     attn_prefill_tc05_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ AttnParams p) {
     using C = PrefillCfg;
@@ -134,7 +142,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, 1)
     tc_fence_after();
     const uint32_t tmem = misc[0];
     const uint32_t t_o = tmem;
-    const uint32_t t_s = tmem + 128;   // S buffer b at t_s + 128*b
+    const uint32_t t_s = tmem + 128;   // S buffer b at t_s + BN*b
 
     const int n_items = p.n_items;
     bool abort = false;
@@ -162,7 +170,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, 1)
                 mbar_arrive_expect_tx(bar_q_full, C::Q_BYTES);
 #pragma unroll
                 for (int hb = 0; hb < 2; ++hb)
-                    tma_load_4d(base + C::OFF_Q + hb * C::HB_BYTES, &tm_q, bar_q_full, hb * 64, it.kvh * p.ratio,
+                    tma_load_4d(base + C::OFF_Q + hb * C::QHB_BYTES, &tm_q, bar_q_full, hb * 64, it.kvh * p.ratio,
                                 it.m0 / p.ratio, it.g, pol);
             }
             ++ic;
@@ -247,9 +255,10 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, 1)
                     if (lane == 0) {
 #pragma unroll
                         for (int kk = 0; kk < C::D / 16; ++kk) {
-                            const uint32_t off = (kk >> 2) * C::HB_BYTES + (kk & 3) * 32;
-                            tc_mma_ss(t_s + 128 * b, umma_desc_sw128(base + C::OFF_Q + off, 16, 1024),
-                                      umma_desc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                            const uint32_t qoff = (kk >> 2) * C::QHB_BYTES + (kk & 3) * 32;
+                            const uint32_t koff = (kk >> 2) * C::HB_BYTES + (kk & 3) * 32;
+                            tc_mma_ss(t_s + C::BN * b, umma_desc_sw128(base + C::OFF_Q + qoff, 16, 1024),
+                                      umma_desc_sw128(kb + koff, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
                         }
                         tc_commit(bar_s_full + 8 * b);
                         issued = true;
@@ -281,12 +290,12 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, 1)
                     }
                     tc_fence_after();
                     if (lane == 0) {
-                        const uint32_t sp = t_s + 128 * b;
+                        const uint32_t sp = t_s + C::BN * b;
 #pragma unroll
                         for (int kk = 0; kk < C::BN / 16; ++kk) {
                             const uint64_t bd = umma_desc_sw128(vb + kk * 16 * 128, C::HB_BYTES, 1024);
                             tc_mma_ts(t_o, sp + kk * 8, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
-                            tc_mma_ts(t_o, sp + 64 + kk * 8, bd, idesc_pv, 1u);
+                            tc_mma_ts(t_o, sp + C::BN / 2 + kk * 8, bd, idesc_pv, 1u);
                         }
                         tc_commit(bar_pv_done);
                         tc_commit(bar_kv_empty + 8 * st);
@@ -344,21 +353,27 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t sc_ = t_s + 128 * b + lane_off;
-                uint32_t sv[4][32];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) tmem_ld32(sc_ + 32 * q, sv[q]);
+                const uint32_t sc_ = t_s + C::BN * b + lane_off;
+                uint32_t sv[C::BN];
+                if constexpr (C::BN == 128) {
+                    tmem_ld128(sc_, *reinterpret_cast<uint32_t(*)[128]>(sv));
+                } else {
+                    tmem_ld64(sc_, *reinterpret_cast<uint32_t(*)[64]>(sv));
+                }
                 const int lim = nk - j * C::BN;   // columns >= lim are masked
-                float mx = -CUDART_INF_F;
+                if (lim < C::BN) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
+                    for (int e = 0; e < C::BN; ++e)
+                        if (e >= lim) sv[e] = __float_as_uint(-CUDART_INF_F);
+                }
+                // row max as 8 independent chains
+                float mx8[8];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        float v = __uint_as_float(sv[q][e]);
-                        if (32 * q + e >= lim) v = -CUDART_INF_F;
-                        sv[q][e] = __float_as_uint(v);
-                        mx = fmaxf(mx, v);
-                    }
+                for (int i = 0; i < 8; ++i) mx8[i] = __uint_as_float(sv[i]);
+#pragma unroll
+                for (int e = 8; e < C::BN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sv[e]));
+                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
                 if (mx != -CUDART_INF_F) {
                     const float mx_s = mx * c;
                     if (m_run == -CUDART_INF_F) {
@@ -385,23 +400,23 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, 1)
                     }
                 }
                 const float m_use = (m_run == -CUDART_INF_F) ? 0.f : m_run;
-                float psum = 0.f;
+                float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < C::BN / 32; ++q) {
                     uint32_t hi[16], lo[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
-                        const float p0 = exp2f(__uint_as_float(sv[q][2 * e]) * c - m_use);
-                        const float p1 = exp2f(__uint_as_float(sv[q][2 * e + 1]) * c - m_use);
-                        psum += p0 + p1;
+                        const float p0 = exp2f(__uint_as_float(sv[32 * q + 2 * e]) * c - m_use);
+                        const float p1 = exp2f(__uint_as_float(sv[32 * q + 2 * e + 1]) * c - m_use);
+                        ps8[e & 7] += p0 + p1;
                         const uint32_t h = pack_bf16x2(p0, p1);
                         hi[e] = h;
                         lo[e] = pack_bf16x2(p0 - bf16_lo(h), p1 - bf16_hi(h));
                     }
                     tmem_st16(sc_ + 16 * q, hi);
-                    tmem_st16(sc_ + 64 + 16 * q, lo);
+                    tmem_st16(sc_ + C::BN / 2 + 16 * q, lo);
                 }
-                l_run += psum;
+                l_run += ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();

@@ -77,7 +77,7 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
     pl.split_len = rows <= rad::kSplitMaxRows ? rad::kSplitLen : 0;
     if (use_prefill_tc(rows, pl.ratio, head_dim, kv_dtype)) pl.family = rad::kFamPrefillTC;
     pl.tile = pl.family == rad::kFamPrefillTC
-                  ? rad::TileInfo{128, 0, 4, 0, 0, rad::PrefillTileKeys, 3, 128, 192, 0, 1}
+                  ? rad::TileInfo{128, 0, 4, 0, 0, rad::PrefillTileKeys, RAD_PREFILL_NS, 128, 192, 0, RAD_PREFILL_CTAS}
                   : tile_for(head_dim, kv_dtype, pl.family);
     pl.n_qtiles = (pl.M + pl.tile.QT - 1) / pl.tile.QT;
     pl.qtv = pl.M < pl.tile.QT ? pl.M : pl.tile.QT;
@@ -262,9 +262,9 @@ int rad_attn_paged_describe(int32_t rows, int32_t n_head, int32_t n_head_kv, int
     if (pl.family == rad::kFamPrefillTC) {
         snprintf(buf, buf_len,
                  "attn_prefill_tc05 family=%s head_dim=%d kv=bf16 query_rows_per_kv_head=%d tile_rows=128 "
-                 "keys_per_tile=%d stages=3 warps=4 softmax+1 mma+1 producer mma=tcgen05.kind::f16 M128xN128 "
+                 "keys_per_tile=%d stages=%d ctas_per_sm=%d warps=4 softmax+1 mma+1 producer mma=tcgen05.kind::f16 "
                  "(S and O in TMEM, P bf16 hi+lo from TMEM) split_len=0",
-                 family_name(pl.family), head_dim, pl.M, rad::PrefillTileKeys);
+                 family_name(pl.family), head_dim, pl.M, rad::PrefillTileKeys, pl.tile.NS, pl.tile.minb);
         return RAD_OK;
     }
     snprintf(buf, buf_len,

@@ -69,7 +69,17 @@ template <> struct Pick<256, true,  kFamDecode> { using T = TileCfg<256, true,  
 template <> struct Pick<256, true,  kFamVerify> { using T = TileCfg<256, true,  RAD_TILE_D256_FP8_VER>; };
 template <> struct Pick<256, true,  kFamWide>   { using T = TileCfg<256, true,  RAD_TILE_D256_FP8_WIDE>; };
 
-constexpr int PrefillTileKeys = 128;   // keys per tile of the tcgen05 prefill kernel
+// tcgen05 prefill kernel: keys per tile (64 or 128), K/V stages, CTAs per SM.
+#ifndef RAD_PREFILL_BN
+#define RAD_PREFILL_BN 128
+#endif
+#ifndef RAD_PREFILL_NS
+#define RAD_PREFILL_NS 3
+#endif
+#ifndef RAD_PREFILL_CTAS
+#define RAD_PREFILL_CTAS 1
+#endif
+constexpr int PrefillTileKeys = RAD_PREFILL_BN;
 
 struct TileInfo {
     int D, fp8, WQ, NQW, WK, KS, NS, QT, threads, smem, minb;
