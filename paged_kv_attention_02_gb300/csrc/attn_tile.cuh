@@ -707,7 +707,10 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
             if (final_write) {
                 const int m = it.m0 + col;
                 const int r = m / p.ratio, hl = m - r * p.ratio;
-                const float o = item_bad ? 0.f : acc / l;
+                // acc * (1/l), the combine kernel's form, so a row written here
+                // and the same row merged from splits round identically
+                const float inv = 1.f / l;
+                const float o = item_bad ? 0.f : acc * inv;
                 p.out[(((long long)it.g * p.rows + r) * p.n_head + it.kvh * p.ratio + hl) * C::D + d] =
                     __float2bfloat16_rn(o);
             } else {

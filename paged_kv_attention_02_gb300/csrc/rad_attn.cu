@@ -73,9 +73,15 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
     Plan pl{};
     pl.ratio = n_head / n_head_kv;
     pl.M = rows * pl.ratio;
-    pl.family = pl.M <= 8 ? rad::kFamDecode : (pl.M <= 32 ? rad::kFamVerify : rad::kFamWide);
+    // Split calls: the decode tile for <= 8 query rows per KV head, else the
+    // verify tile (32 rows per query tile, as many tiles as needed); both
+    // share one key schedule.  Longer calls: the tcgen05 prefill kernel where
+    // it applies, else the wide tile.
     pl.split_len = rows <= rad::kSplitMaxRows ? rad::kSplitLen : 0;
-    if (use_prefill_tc(rows, pl.ratio, head_dim, kv_dtype)) pl.family = rad::kFamPrefillTC;
+    if (pl.split_len > 0)
+        pl.family = pl.M <= 8 ? rad::kFamDecode : rad::kFamVerify;
+    else
+        pl.family = use_prefill_tc(rows, pl.ratio, head_dim, kv_dtype) ? rad::kFamPrefillTC : rad::kFamWide;
     pl.tile = pl.family == rad::kFamPrefillTC
                   ? rad::TileInfo{128, 0, 4, 0, 0, rad::PrefillTileKeys, RAD_PREFILL_NS, 128, 192, 0, RAD_PREFILL_CTAS}
                   : tile_for(head_dim, kv_dtype, pl.family);

@@ -28,7 +28,7 @@ constexpr int kSplitMaxRows = 256;
 #define RAD_TILE_D128_BF16_WIDE 4, 2, 1, 64, 4, 1
 #endif
 #ifndef RAD_TILE_D128_FP8_DEC
-#define RAD_TILE_D128_FP8_DEC 1, 1, 4, 64, 8, 1
+#define RAD_TILE_D128_FP8_DEC 1, 1, 2, 64, 6, 2
 #endif
 #ifndef RAD_TILE_D128_FP8_VER
 #define RAD_TILE_D128_FP8_VER 2, 2, 2, 64, 3, 2
@@ -46,7 +46,7 @@ constexpr int kSplitMaxRows = 256;
 #define RAD_TILE_D256_BF16_WIDE 4, 1, 1, 32, 4, 1
 #endif
 #ifndef RAD_TILE_D256_FP8_DEC
-#define RAD_TILE_D256_FP8_DEC 1, 1, 4, 64, 5, 1
+#define RAD_TILE_D256_FP8_DEC 1, 1, 2, 32, 4, 2
 #endif
 #ifndef RAD_TILE_D256_FP8_VER
 #define RAD_TILE_D256_FP8_VER 4, 1, 2, 32, 7, 1
@@ -80,6 +80,20 @@ template <> struct Pick<256, true,  kFamWide>   { using T = TileCfg<256, true,  
 #define RAD_PREFILL_CTAS 1
 #endif
 constexpr int PrefillTileKeys = RAD_PREFILL_BN;
+
+// Split calls (decode and verify shapes) share one key schedule: two key
+// warps take alternate 16-key sub-tiles in key order, so a query row's
+// arithmetic is the same in every split tile -- a verified row equals the
+// decode step's row at its position bit for bit ("Adding a model", step 4).
+template <int D, bool FP8>
+constexpr bool same_key_schedule() {
+    using Dec = typename Pick<D, FP8, kFamDecode>::T;
+    using Ver = typename Pick<D, FP8, kFamVerify>::T;
+    return Dec::WK == 2 && Ver::WK == 2;
+}
+static_assert(same_key_schedule<128, false>() && same_key_schedule<128, true>() &&
+                  same_key_schedule<256, false>() && same_key_schedule<256, true>(),
+              "decode and verify tiles must share the key schedule");
 
 struct TileInfo {
     int D, fp8, WQ, NQW, WK, KS, NS, QT, threads, smem, minb;

@@ -29,6 +29,8 @@ MID = {
                           pages_per_seq=70),
     "ver_wide_d256": wl.Config("ver_wide_d256", 3, 8, 16, 2, 256, 32, wl.KV_BF16, 107, "fixed:8,600,1500",
                                pages_per_seq=50),
+    "ver_fp8_d256": wl.Config("ver_fp8_d256", 3, 8, 16, 2, 256, 32, wl.KV_FP8_E4M3, 112, "fixed:8,1100,2100",
+                              pages_per_seq=70),
     "ratio16": wl.Config("ratio16", 3, 1, 16, 1, 128, 16, wl.KV_BF16, 108, "fixed:5,600,1200",
                          pages_per_seq=80),
     "chunk_split": wl.Config("chunk_split", 2, 40, 8, 2, 128, 16, wl.KV_BF16, 109, "fixed:40,1500",
@@ -148,6 +150,28 @@ def test_repeated_calls_are_bit_identical(mid):
     for _ in range(3):
         c, _ = dw.run()
         assert np.array_equal(bits(a), bits(c))
+
+
+@pytest.mark.parametrize("name", ["ver_fp8", "ver_bf16", "ver_wide_d256", "ver_fp8_d256"])
+def test_verified_rows_equal_decode_rows_bit_for_bit(mid, name):
+    # "Adding a model", step 4: every verified row must equal the decode
+    # step's row bit for bit, or speculation is not lossless.  Row r of a
+    # verify round over final length L is the decode step with length L-R+r+1.
+    w, dw = mid(name)
+    R = w.cfg.rows
+    ver, err = dw.run()
+    assert err == 0
+    vb = bits(ver)
+    for r in range(R):
+        dec_cfg = wl.Config(name + "_dec", w.groups, 1, w.cfg.n_head, w.cfg.n_head_kv, w.cfg.head_dim,
+                            w.cfg.page_size, w.cfg.kv_dtype, 0, "fixed:1", pages_per_seq=w.pages_per_seq)
+        q = dw.q[:, r:r + 1].contiguous()
+        lens = dw.lens - R + r + 1
+        out = b.attn_paged(q, dw.k, dw.v, dw.table, lens, rows=1, n_head=dec_cfg.n_head,
+                           n_head_kv=dec_cfg.n_head_kv, head_dim=dec_cfg.head_dim, page_size=dec_cfg.page_size,
+                           scale=w.cfg.scale, kv_dtype=dec_cfg.kv_dtype, k_scales=dw.ks, v_scales=dw.vs)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(out)[:, 0], vb[:, r]), f"{name}: row {r} differs from its decode step"
 
 
 # ------------------------------------------------------------------ errors never fault
