@@ -62,7 +62,7 @@ def _load():
         lib.oracle_attn_paged_rows.restype = ctypes.c_int
         lib.oracle_attn_paged_rows.argtypes = [
             P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, ctypes.c_double, i32, P, P,
-            P, i64, P, P, i64, P, P, i32]
+            P, i64, P, P, i64, P, P, i32, i32]
         lib.oracle_bf16_to_f64.restype = ctypes.c_double
         lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
         lib.oracle_e4m3_to_f64.restype = ctypes.c_double
@@ -102,11 +102,12 @@ def _ptr(a):
 
 def attn_paged_rows(q, k_pool, v_pool, page_table, seq_lens, *, rows, n_head, n_head_kv, head_dim,
                     page_size, scale, kv_dtype=KV_BF16, k_scales=None, v_scales=None, sel=None,
-                    want_weights=False, n_threads=0) -> OracleResult:
+                    want_weights=False, n_threads=0, window=0) -> OracleResult:
     """Selected output rows of the op in fp64.
 
     ``sel`` is an int array of (g, r, h) triples; ``None`` selects every row and
-    returns ``out`` shaped [groups, rows, n_head, head_dim].
+    returns ``out`` shaped [groups, rows, n_head, head_dim].  ``window`` > 0
+    limits each row to its last ``window`` keys (0: no window).
     """
     q = np.ascontiguousarray(q, dtype=np.uint16)
     pool_dt = np.uint16 if kv_dtype == KV_BF16 else np.uint8
@@ -139,7 +140,7 @@ def attn_paged_rows(q, k_pool, v_pool, page_table, seq_lens, *, rows, n_head, n_
         _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(seq_lens), groups, rows, n_head,
         n_head_kv, head_dim, page_size, pages_per_seq, num_pages, float(np.float32(scale)), kv_dtype,
         _ptr(k_scales), _ptr(v_scales), _ptr(sel), n_sel, _ptr(out), _ptr(weights), wstride,
-        _ptr(n_keys), ctypes.byref(err), int(n_threads))
+        _ptr(n_keys), ctypes.byref(err), int(n_threads), int(window))
     if rc != 0:
         raise OracleError(f"oracle refused the call: code {rc}")
     if full:

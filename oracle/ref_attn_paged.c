@@ -34,6 +34,11 @@
  *   s_j  = scale * <dec(q[g][r][h][:]), k_j>
  *   out  = sum_j softmax(s)_j * v_j
  *
+ * With a sliding window W > 0 (a windowed KV group: "Radiance architecture
+ * plugins", section "Declare: buffers and KV groups", RAD_KV_WINDOW, state
+ * bounded by a window) row r sees only the last W of those keys,
+ * j = max(0, pos - W + 1) .. pos; W = 0 means no window.
+ *
  * everything in IEEE double.  The softmax is the textbook one: subtract the
  * maximum, exponentiate, divide by the sum.  No tiling, no splitting, no
  * reordering beyond that definition.
@@ -107,6 +112,7 @@ typedef struct {
     int32_t kv_dtype;
     const float* k_scales;
     const float* v_scales;
+    int32_t window;
 } oracle_call;
 
 static double pool_elem(const oracle_call* c, const void* pool, int64_t idx) {
@@ -114,12 +120,15 @@ static double pool_elem(const oracle_call* c, const void* pool, int64_t idx) {
     return oracle_e4m3_to_f64(((const uint8_t*)pool)[idx]);
 }
 
-/* Checks one group; returns its error bits (0 when the group is valid). */
+/* Checks one group; returns its error bits (0 when the group is valid).  The
+ * pages checked are those holding a key some row of the call may see. */
 static uint32_t group_error(const oracle_call* c, int32_t g) {
     int64_t L = c->seq_lens[g];
     if (L < c->rows || L > (int64_t)c->pages_per_seq * c->page_size) return ORACLE_ERRW_SEQLEN;
     int64_t pages = (L + c->page_size - 1) / c->page_size;
-    for (int64_t p = 0; p < pages; ++p) {
+    const int64_t n0 = L - c->rows + 1;                           /* keys seen by row 0 */
+    const int64_t lo = (c->window > 0 && n0 > c->window) ? n0 - c->window : 0;
+    for (int64_t p = lo / c->page_size; p < pages; ++p) {
         int32_t pg = c->page_table[(int64_t)g * c->pages_per_seq + p];
         if (pg < 0 || pg >= c->num_pages) return ORACLE_ERRW_PAGE;
     }
@@ -133,7 +142,8 @@ static void one_row(const oracle_call* c, int32_t g, int32_t r, int32_t h, doubl
     const int32_t ratio = c->n_head / c->n_head_kv;
     const int32_t kv = h / ratio;
     const int64_t L = c->seq_lens[g];
-    const int64_t n = L - c->rows + r + 1;
+    const int64_t n = L - c->rows + r + 1;                       /* keys 0 .. pos */
+    const int64_t lo = (c->window > 0 && n > c->window) ? n - c->window : 0;   /* first visible key */
     const uint16_t* qrow = c->q + (((int64_t)g * c->rows + r) * c->n_head + h) * D;
 
     double* qd = (double*)malloc(sizeof(double) * (size_t)D);
@@ -141,7 +151,7 @@ static void one_row(const oracle_call* c, int32_t g, int32_t r, int32_t h, doubl
     for (int32_t d = 0; d < D; ++d) qd[d] = oracle_bf16_to_f64(qrow[d]);
 
     double m = -INFINITY;
-    for (int64_t j = 0; j < n; ++j) {
+    for (int64_t j = lo; j < n; ++j) {
         int32_t pg = c->page_table[(int64_t)g * c->pages_per_seq + j / c->page_size];
         int64_t slot = j % c->page_size;
         int64_t base = (((int64_t)pg * c->page_size + slot) * c->n_head_kv + kv) * D;
@@ -152,12 +162,14 @@ static void one_row(const oracle_call* c, int32_t g, int32_t r, int32_t h, doubl
         if (s[j] > m) m = s[j];
     }
     double Z = 0.0;
-    for (int64_t j = 0; j < n; ++j) {
+    for (int64_t j = lo; j < n; ++j) {
         s[j] = exp(s[j] - m);
         Z += s[j];
     }
     for (int32_t d = 0; d < D; ++d) out[d] = 0.0;
-    for (int64_t j = 0; j < n; ++j) {
+    for (int64_t j = 0; j < lo; ++j)
+        if (w) w[j] = 0.0;
+    for (int64_t j = lo; j < n; ++j) {
         double wj = s[j] / Z;
         if (w) w[j] = wj;
         int32_t pg = c->page_table[(int64_t)g * c->pages_per_seq + j / c->page_size];
@@ -179,6 +191,7 @@ static int check_call(const oracle_call* c) {
     if (c->kv_dtype != ORACLE_KV_BF16 && c->kv_dtype != ORACLE_KV_FP8_E4M3) return ORACLE_E_DTYPE;
     if (!c->q || !c->k_pool || !c->v_pool || !c->page_table || !c->seq_lens) return ORACLE_E_ARG;
     if (c->kv_dtype == ORACLE_KV_FP8_E4M3 && (!c->k_scales || !c->v_scales)) return ORACLE_E_ARG;
+    if (c->window < 0) return ORACLE_E_ARG;
     return ORACLE_OK;
 }
 
@@ -196,10 +209,10 @@ int oracle_attn_paged_rows(const uint16_t* q, const void* k_pool, const void* v_
                            int32_t kv_dtype, const float* k_scales, const float* v_scales,
                            const int32_t* sel, int64_t n_sel, double* out, double* weights,
                            int64_t weights_stride, int64_t* n_keys, uint32_t* err_word,
-                           int32_t n_threads) {
+                           int32_t n_threads, int32_t window) {
     oracle_call c = {q, k_pool, v_pool, page_table, seq_lens, groups, rows, n_head, n_head_kv,
                      head_dim, page_size, pages_per_seq, num_pages, scale, kv_dtype, k_scales,
-                     v_scales};
+                     v_scales, window};
     int rc = check_call(&c);
     if (rc != ORACLE_OK) return rc;
     if (!sel || !out) return ORACLE_E_ARG;

@@ -8,11 +8,14 @@ definition with explicit positions:
     row r of a call with R rows over a sequence of final length L sits at
     position L - R + r and sees keys 0 .. L - R + r (kern manifest v7,
     $defs.Fill `seq_len`); query head h reads KV head h // (H / Hkv).
+    With a sliding window W > 0 (a RAD_KV_WINDOW group, Radiance architecture
+    plugins, "Declare: buffers and KV groups") it sees only keys
+    max(0, position - W + 1) .. position.
 """
 import math
 
 
-def attend_sequence(q_rows, keys, values, scale, n_head_kv):
+def attend_sequence(q_rows, keys, values, scale, n_head_kv, window=0):
     """q_rows: [R][H][D] floats; keys/values: [L][Hkv][D] floats.
 
     Returns out [R][H][D] as floats.
@@ -24,11 +27,13 @@ def attend_sequence(q_rows, keys, values, scale, n_head_kv):
     out = []
     for r in range(R):
         position = L - R + r
+        first = max(0, position - window + 1) if window > 0 else 0
+        visible = range(first, position + 1)
         row_out = []
         for h in range(H):
             kvh = h // group
             logits = []
-            for j in range(position + 1):
+            for j in visible:
                 acc = 0.0
                 for a, b in zip(q_rows[r][h], keys[j][kvh]):
                     acc += a * b
@@ -38,7 +43,7 @@ def attend_sequence(q_rows, keys, values, scale, n_head_kv):
             total = sum(ex)
             D = len(values[0][kvh])
             vec = [0.0] * D
-            for j, e in enumerate(ex):
+            for j, e in zip(visible, ex):
                 wgt = e / total
                 vj = values[j][kvh]
                 for d in range(D):

@@ -329,6 +329,120 @@ def test_zero_rows_is_not_a_call():
         run_oracle(dict(c, q=c["q"][:, :0]), R=0, H=2, Hkv=1, D=8, P=4, scale=0.5)
 
 
+# ----------------------------------------------------------------------------- sliding window
+# A windowed KV group (RAD_KV_WINDOW, Radiance architecture plugins, "Declare:
+# buffers and KV groups") bounds what a row sees to its last W keys.
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("shape", [
+    dict(G=3, R=1, H=4, Hkv=2, D=8, P=4, lens=[1, 13, 40], W=5),
+    dict(G=2, R=3, H=6, Hkv=2, D=4, P=2, lens=[3, 23], W=1),
+    dict(G=2, R=8, H=3, Hkv=3, D=8, P=16, lens=[8, 37], W=4),
+    dict(G=2, R=8, H=2, Hkv=1, D=8, P=4, lens=[9, 50], W=16),
+    dict(G=1, R=2, H=2, Hkv=1, D=128, P=16, lens=[40], W=100),
+])
+def test_window_matches_brute_force(shape, fp8):
+    rng = np.random.default_rng(40 + shape["W"] + shape["R"] + int(fp8))
+    s = dict(shape)
+    lens, W = s.pop("lens"), s.pop("W")
+    G, R, H, Hkv, D, P = (s[k] for k in ("G", "R", "H", "Hkv", "D", "P"))
+    c = random_case(rng, G=G, R=R, H=H, Hkv=Hkv, D=D, P=P, lens=lens, fp8=fp8)
+    scale = float(np.float32(1.0 / math.sqrt(D)))
+    res = run_oracle(c, R=R, H=H, Hkv=Hkv, D=D, P=P, scale=scale, fp8=fp8, window=W)
+    assert res.err_word == 0
+    qv = bf16_values(c["q"])
+    for g, L in enumerate(lens):
+        if fp8:
+            pages = c["table"][g]
+            ks = np.array([c["ks"][pages[j // P]] for j in range(L)], dtype=np.float64)
+            vs = np.array([c["vs"][pages[j // P]] for j in range(L)], dtype=np.float64)
+            kf = e4m3_values(c["seqs_k"][g]) * ks[:, None, None]
+            vf = e4m3_values(c["seqs_v"][g]) * vs[:, None, None]
+        else:
+            kf, vf = bf16_values(c["seqs_k"][g]), bf16_values(c["seqs_v"][g])
+        want = attend_sequence(qv[g].tolist(), kf.tolist(), vf.tolist(), scale, Hkv, window=W)
+        np.testing.assert_allclose(res.out[g], np.array(want), rtol=1e-12, atol=1e-12)
+
+
+def test_window_of_one_returns_the_current_value_row():
+    rng = np.random.default_rng(41)
+    R, H, Hkv, D, P = 4, 4, 2, 8, 4
+    c = random_case(rng, G=2, R=R, H=H, Hkv=Hkv, D=D, P=P, lens=[4, 19])
+    res = run_oracle(c, R=R, H=H, Hkv=Hkv, D=D, P=P, scale=3.0, window=1)
+    for g, L in enumerate(c["lens"]):
+        v = bf16_values(c["seqs_v"][g])
+        for r in range(R):
+            for h in range(H):
+                assert np.array_equal(res.out[g, r, h], v[L - R + r, h // (H // Hkv)])
+
+
+def test_window_row_equals_unwindowed_row_over_its_last_keys():
+    """Row r of a windowed call is the plain op over a sequence that holds only
+    the row's last W keys, re-paged from scratch (bit for bit: the same sums)."""
+    rng = np.random.default_rng(42)
+    R, H, Hkv, D, P, W = 5, 4, 2, 16, 4, 7
+    lens = [5, 11, 30]
+    c = random_case(rng, G=3, R=R, H=H, Hkv=Hkv, D=D, P=P, lens=lens)
+    res = run_oracle(c, R=R, H=H, Hkv=Hkv, D=D, P=P, scale=0.35, window=W)
+    for g, L in enumerate(lens):
+        for r in range(R):
+            pos = L - R + r
+            lo = max(0, pos - W + 1)
+            kk = [c["seqs_k"][g][lo:pos + 1]]
+            vv = [c["seqs_v"][g][lo:pos + 1]]
+            n_pages = (pos + 1 - lo + P - 1) // P + 2
+            kp, vp, table = paged_from_logical(kk, vv, P, n_pages, rng)
+            one = oracle.attn_paged(np.ascontiguousarray(c["q"][g:g + 1, r:r + 1]), kp, vp, table,
+                                    np.array([pos + 1 - lo], dtype=np.int32), rows=1, n_head=H,
+                                    n_head_kv=Hkv, head_dim=D, page_size=P, scale=0.35)
+            assert np.array_equal(res.out[g, r], one.out[0, 0])
+
+
+def test_window_covering_the_context_changes_nothing():
+    rng = np.random.default_rng(43)
+    c = random_case(rng, G=2, R=3, H=2, Hkv=1, D=8, P=4, lens=[3, 26])
+    base = run_oracle(c, R=3, H=2, Hkv=1, D=8, P=4, scale=0.5)
+    for W in (26, 27, 1 << 20):
+        win = run_oracle(c, R=3, H=2, Hkv=1, D=8, P=4, scale=0.5, window=W)
+        assert np.array_equal(base.out, win.out)
+    with pytest.raises(oracle.OracleError):
+        run_oracle(c, R=3, H=2, Hkv=1, D=8, P=4, scale=0.5, window=-1)
+
+
+def test_window_weights_vanish_below_the_window():
+    rng = np.random.default_rng(44)
+    R, W = 4, 6
+    c = random_case(rng, G=1, R=R, H=2, Hkv=1, D=8, P=4, lens=[21])
+    sel = [(0, r, h) for r in range(R) for h in range(2)]
+    res = oracle.attn_paged_rows(c["q"], c["kp"], c["vp"], c["table"], c["lens"], rows=R, n_head=2,
+                                 n_head_kv=1, head_dim=8, page_size=4, scale=1.5, sel=sel,
+                                 want_weights=True, window=W)
+    for i, (g, r, h) in enumerate(sel):
+        pos = 21 - R + r
+        w = res.weights[i]
+        assert np.all(w[:pos - W + 1] == 0) and np.all(w[pos + 1:] == 0)
+        assert np.all(w[pos - W + 1:pos + 1] > 0)
+        assert abs(w.sum() - 1.0) < 1e-12
+
+
+def test_window_pages_below_every_rows_window_are_never_read():
+    """Page ids wholly below row 0's window may be stale or invalid; the page
+    holding row 0's first visible key must still be valid."""
+    rng = np.random.default_rng(45)
+    R, P, W = 3, 4, 6
+    c = random_case(rng, G=2, R=R, H=2, Hkv=1, D=8, P=P, lens=[9, 30])
+    good = run_oracle(c, R=R, H=2, Hkv=1, D=8, P=P, scale=0.5, window=W)
+    lo0 = 30 - R + 0 - W + 1               # row 0's first visible key in group 1: 22
+    table = c["table"].copy()
+    table[1, :lo0 // P] = -7               # pages 0..4 lie below every row's window
+    res = run_oracle(dict(c, table=table), R=R, H=2, Hkv=1, D=8, P=P, scale=0.5, window=W)
+    assert res.err_word == 0 and np.array_equal(res.out, good.out)
+    table[1, lo0 // P] = c["kp"].shape[0]  # the page holding key 22 is needed
+    res = run_oracle(dict(c, table=table), R=R, H=2, Hkv=1, D=8, P=P, scale=0.5, window=W)
+    assert res.err_word == oracle.ERRW_PAGE
+    assert np.all(res.out[1] == 0) and np.array_equal(res.out[0], good.out[0])
+
+
 # ----------------------------------------------------------------------------- generator sanity
 
 def test_tiny_workload_matches_its_recipe():
