@@ -152,6 +152,33 @@ int rad_attn_paged(const void* q, const void* k_pool, const void* v_pool,
                    rad_stream_t stream);
 
 /*
+ * rad_attn_paged_window -- the op over a sliding-window KV group.
+ *
+ * A RAD_KV_WINDOW group ("Radiance architecture plugins", section "Declare:
+ * buffers and KV groups": a KV state bounded by a window) keeps only the last
+ * `window` keys of each sequence live.  Row r then sees keys
+ *   max(0, n - window) .. n - 1,   n = seq_lens[g] - rows + r + 1
+ * instead of 0 .. n - 1; `window` = 0 means no window (exactly rad_attn_paged).
+ * Every other argument, layout, status and error bit is that of
+ * rad_attn_paged, with two differences that follow from the bound:
+ *   - page ids of pages wholly below row 0's window are never read, so the
+ *     caller may leave stale or invalid ids there (a recycled page);
+ *     RAD_ERRW_PAGE covers only the pages from row 0's first visible key on;
+ *   - K/V slots of the first live page below a row's window are never used.
+ * The workspace need is rad_attn_paged_workspace_bytes() of the same shape
+ * (an upper bound: splits wholly below the window are skipped).
+ * A window < 0 returns RAD_E_ARG.  Rows of one position give the same bits
+ * in every call shape that shares its window, as rad_attn_paged's rows do.
+ */
+int rad_attn_paged_window(const void* q, const void* k_pool, const void* v_pool,
+                          const int32_t* page_table, const int32_t* seq_lens, int32_t groups,
+                          int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_dim,
+                          int32_t page_size, int32_t pages_per_seq, int32_t num_pages, float scale,
+                          int32_t kv_dtype, const float* k_scales, const float* v_scales,
+                          int32_t window, void* out, void* workspace, size_t workspace_bytes,
+                          uint32_t* err_word, rad_stream_t stream);
+
+/*
  * rad_attn_paged_noalloc -- the same op for callers that cannot allocate.
  *
  * The pages have no counterpart to this entry point; it exists for callers

@@ -31,7 +31,8 @@ RAD_ERRW_QRANGE = 4
 RAD_ERRW_TIMEOUT = 8
 
 EXPORTS = ("rad_attn_paged", "rad_attn_paged_workspace_bytes", "rad_attn_paged_describe",
-           "rad_attn_status_string", "rad_attn_version", "rad_attn_paged_noalloc")
+           "rad_attn_status_string", "rad_attn_version", "rad_attn_paged_noalloc",
+           "rad_attn_paged_window")
 
 # Size of the library-owned scratch of rad_attn_paged_noalloc (include/rad_attn.h).
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -66,6 +67,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.rad_attn_status_string.argtypes = [ctypes.c_int]
     lib.rad_attn_version.restype = ctypes.c_char_p
     lib.rad_attn_version.argtypes = []
+    lib.rad_attn_paged_window.restype = ctypes.c_int
+    lib.rad_attn_paged_window.argtypes = [p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, i32,
+                                          ctypes.c_float, i32, p, p, i32, p, p, sz, p, p]
     lib.rad_attn_paged_noalloc.restype = ctypes.c_int
     lib.rad_attn_paged_noalloc.argtypes = [p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, i32,
                                            ctypes.c_float, i32, p, p, p, p, p]
@@ -133,6 +137,31 @@ def attn_paged(q, k_pool, v_pool, page_table, seq_lens, *, rows, n_head, n_head_
         _stream_handle(stream))
     if rc != RAD_OK:
         raise RadAttnError(rc, "rad_attn_paged")
+    return out
+
+
+def attn_paged_window(q, k_pool, v_pool, page_table, seq_lens, *, rows, n_head, n_head_kv, head_dim,
+                      page_size, scale, window, kv_dtype=RAD_KV_BF16, k_scales=None, v_scales=None,
+                      out=None, workspace=None, err_word=None, stream=None):
+    """Launches rad_attn_paged_window: attn_paged over a sliding-window KV group,
+    each row seeing only its last `window` keys (0: no window).  Arguments and
+    result as attn_paged."""
+    groups = int(seq_lens.shape[0])
+    pages_per_seq = int(page_table.shape[1])
+    num_pages = int(k_pool.shape[0])
+    if out is None:
+        out = torch.empty((groups, rows, n_head, head_dim), dtype=torch.bfloat16, device=q.device)
+    need = workspace_bytes(groups, rows, n_head, n_head_kv, head_dim, page_size, pages_per_seq, kv_dtype)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().rad_attn_paged_window(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(seq_lens), groups, rows, n_head,
+        n_head_kv, head_dim, page_size, pages_per_seq, num_pages, float(scale), kv_dtype,
+        _ptr(k_scales), _ptr(v_scales), int(window), _ptr(out), _ptr(workspace), ws_bytes,
+        _ptr(err_word), _stream_handle(stream))
+    if rc != RAD_OK:
+        raise RadAttnError(rc, "rad_attn_paged_window")
     return out
 
 

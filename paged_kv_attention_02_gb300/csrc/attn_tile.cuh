@@ -92,8 +92,18 @@ struct AttnParams {
     int max_splits;        // 1 without splitting
     int split_len;         // keys per split; 0 = one range over the whole context
     int n_items;           // max_splits * groups * n_head_kv * n_qtiles
+    int window;            // > 0: each row sees only its last `window` keys; 0: no window
     float scale_log2;      // scale * log2(e)
 };
+
+// First key that query row r of a call with `rows` rows over a sequence of
+// length L may see: 0, or with a sliding window W (a RAD_KV_WINDOW group,
+// "Radiance architecture plugins", section "Declare: buffers and KV groups")
+// the first of the row's last W keys.
+__device__ __forceinline__ int first_visible_key(int L, int rows, int r, int window) {
+    const int n = L - rows + r + 1;   // keys 0 .. n-1 are causal for row r
+    return (window > 0 && n > window) ? n - window : 0;
+}
 
 template <int D_, bool FP8_, int WQ_, int NQW_, int WK_, int KS_, int NS_, int MINB_ = 1>
 struct TileCfg {
@@ -117,7 +127,8 @@ struct TileCfg {
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
     static constexpr int MAX_PAGES_STAGE = KS / 16;
     // A page of one KV head lands as D/BOXW blocks of [page_size][128 bytes]
-    // (one TMA box each), so 8 consecutive keys hit 8 different swizzle phases.
+    // (one 128-byte column block each), so 8 consecutive keys hit 8 different
+    // swizzle phases.
     static constexpr int BOXW = 128 / E;          // elements per 128-byte row
     static constexpr int NBOX = D / BOXW;
     static constexpr int Q_SLOT_BYTES = QT * D * 2;
@@ -152,13 +163,18 @@ struct ItemPlan {
     int L;
     bool seq_ok;
     bool active;
-    int n_splits;
-    int k0, k1;        // key range of the item
+    int n_splits;      // splits of the sequence, ceil(L / split_len)
+    int s_first;       // first split holding a key some row of the tile sees
+    int klo;           // first key some row of the tile sees
+    int kmax;          // keys 0 .. kmax-1 hold every key some row of the tile sees
+    int k0, k1;        // key range of the item (k0 a multiple of KS)
     int m0, m_end;     // query rows [m0, m_end) of the KV head
     int n_stages;
 };
 
-template <class C>
+// WIN: the call has a sliding window (p.window > 0); without one, every
+// window term folds away at compile time.
+template <class C, bool WIN>
 __device__ __forceinline__ ItemPlan plan_item(int item, const AttnParams& p) {
     ItemPlan it;
     const int per_split = p.groups * p.n_head_kv * p.n_qtiles;
@@ -177,21 +193,30 @@ __device__ __forceinline__ ItemPlan plan_item(int item, const AttnParams& p) {
     it.k0 = it.k1 = 0;
     it.n_stages = 0;
     it.n_splits = 1;
+    it.s_first = 0;
+    it.klo = it.kmax = 0;
     if (!it.seq_ok) {
         it.active = (it.s == 0);
         return it;
     }
     const int r_last = (it.m_end - 1) / p.ratio;
-    const int kmax = it.L - p.rows + r_last + 1;
+    it.kmax = it.L - p.rows + r_last + 1;
+    it.klo = WIN ? first_visible_key(it.L, p.rows, it.m0 / p.ratio, p.window) : 0;
+    // Stages start on absolute multiples of KS (split_len is one too), so a
+    // key falls in the same sub-tile, and goes to the same key warp, whatever
+    // the tile's first visible key: rows of different calls at one position
+    // see the same schedule.
+    const int klo_stage = (it.klo / C::KS) * C::KS;
     if (p.split_len > 0) {
         it.n_splits = (it.L + p.split_len - 1) / p.split_len;
-        it.active = it.s < it.n_splits;
-        it.k0 = it.s * p.split_len;
-        it.k1 = min(it.k0 + p.split_len, kmax);
+        it.s_first = it.klo / p.split_len;
+        it.active = it.s >= it.s_first && it.s < it.n_splits;
+        it.k0 = max(it.s * p.split_len, klo_stage);
+        it.k1 = min(it.s * p.split_len + p.split_len, it.kmax);
     } else {
         it.active = (it.s == 0);
-        it.k0 = 0;
-        it.k1 = kmax;
+        it.k0 = klo_stage;
+        it.k1 = it.kmax;
     }
     if (it.k1 < it.k0) it.k1 = it.k0;
     it.n_stages = (it.k1 - it.k0 + C::KS - 1) / C::KS;
@@ -218,7 +243,7 @@ __device__ __forceinline__ int d_of(int mt, int row16) {
     }
 }
 
-template <class C>
+template <class C, bool WIN>
 __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const __grid_constant__ AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -260,7 +285,7 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
         uint32_t scount = 0, qcount = 0;
         bool abort = false;
         for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
-            const ItemPlan it = plan_item<C>(item, p);
+            const ItemPlan it = plan_item<C, WIN>(item, p);
             if (!it.active || !it.seq_ok) continue;
             // ---- query rows of the item
             if (pw == 0) {
@@ -285,6 +310,7 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
             // ---- KV pages of the item, page ids fetched 32 at a time
             const int P = p.page_size;
             const int page_hi = (it.k1 + P - 1) / P;   // exclusive
+            const int page_lo = WIN ? it.klo / P : 0;  // pages below hold no visible key: never read
             const uint32_t lsmem = (uint32_t)((lc >> 3) * P * 128);   // this lane's 128-byte column block
             const int32_t* trow = p.page_table + (long long)it.g * p.pages_per_seq;
             const long long row_stride = (long long)p.n_head_kv * C::ROW_BYTES;   // bytes between token slots
@@ -302,7 +328,8 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
                     const int pi = batch0 + lane;
                     my_bad = false;
                     my_pg = 0;
-                    if (pi < page_hi) {
+                    my_ks = my_vs = 1.f;
+                    if ((!WIN || pi >= page_lo) && pi < page_hi) {
                         const int pg = __ldg(trow + pi);
                         my_bad = (pg < 0 || pg >= p.num_pages);
                         my_pg = my_bad ? 0 : pg;
@@ -319,6 +346,7 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
                 }
                 const uint32_t tile = base + slot * C::STAGE_BYTES + pw * C::TILE_BYTES;
                 for (int i = 0; i < npages; ++i) {
+                    if (WIN && pstart + i < page_lo) continue;   // slots stay stale: masked in S and V
                     const int pg = __shfl_sync(0xffffffffu, my_pg, (pstart - batch0 + i) & 31);
                     const uint8_t* src = head_base + (long long)pg * P * row_stride;
                     const uint32_t dst = tile + (uint32_t)(i * P * C::ROW_BYTES) + lsmem;
@@ -379,7 +407,7 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
     bool abort = false;
 
     for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
-        const ItemPlan it = plan_item<C>(item, p);
+        const ItemPlan it = plan_item<C, WIN>(item, p);
         if (!it.active) continue;
         if (!it.seq_ok) {
             // Invalid length: this group's rows become zeros (the split-0 items
@@ -396,7 +424,7 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
 
         // ---- query fragments (B operand of S^T = K Q^T), one per n-tile and k-step
         uint32_t qb[C::NQW][C::D / 16][2];
-        int nk[C::NQW][2];
+        int nk[C::NQW][2];   // a column sees keys nk - wlim .. nk - 1 (and none below 0)
         {
             const uint32_t slot = qcount & 1u, use = qcount >> 1;
             if (!mbar_wait_bounded(bar_qfull + 8 * slot, use & 1u, kWaitLimitNs)) abort = true;
@@ -452,8 +480,25 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
                 for (int e = 0; e < 4; ++e) oacc[j][mt][e] = 0.f;
         }
         uint32_t bad = 0;
+        // Pages the group needs that no item of this tile loads (below the
+        // tile's window, or past its last row's keys) are checked by the
+        // tile's first item, so every row of a group with a bad page is zero.
+        if (it.s == it.s_first) {
+            const int P_ = p.page_size;
+            const int glo = WIN ? first_visible_key(it.L, p.rows, 0, p.window) / P_ : 0;
+            const int tlo = it.klo / P_, thi = (it.kmax + P_ - 1) / P_, ghi = (it.L + P_ - 1) / P_;
+            const int32_t* trow = p.page_table + (long long)it.g * p.pages_per_seq;
+            const int n_below = tlo - glo;
+            for (int i = tid; i < n_below + (ghi - thi); i += C::NCT) {
+                const int pi = i < n_below ? glo + i : thi + (i - n_below);
+                const int pg = __ldg(trow + pi);
+                bad |= (pg < 0 || pg >= p.num_pages) ? 1u : 0u;
+            }
+        }
         const int P = p.page_size;
         const int lp = (P == 16) ? 4 : 5;
+        // key is visible to a column iff 0 <= nk - 1 - key < wlim
+        const uint32_t wlim = p.window > 0 ? (uint32_t)p.window : 0x7FFFFFFFu;
 
         for (int st = 0; st < it.n_stages && !abort; ++st) {
             const uint32_t slot = scount % C::NS, use = scount / C::NS;
@@ -529,7 +574,8 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int key = key0 + g8 + ((e >> 1) << 3);
-                        x[e] = (key < nk[j][e & 1]) ? sacc[j][e] * kfac : -CUDART_INF_F;
+                        const bool in = WIN ? (uint32_t)(nk[j][e & 1] - 1 - key) < wlim : key < nk[j][e & 1];
+                        x[e] = in ? sacc[j][e] * kfac : -CUDART_INF_F;
                     }
                     // The running max moves only when a sub-tile's max exceeds it by
                     // more than 2^8 (or on the first keys); weights up to 2^8 are exact
@@ -577,13 +623,16 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
                     }
                 }
                 // ---------------- O^T += V^T P^T
-                const bool edge = key0 + 16 > it.k1;   // keys past the item's range are zeroed in V
+                // keys outside [klo, k1) are zeroed in V: past the item's range
+                // the slots may hold anything, below klo they may be stale
+                const bool edge = key0 + 16 > it.k1 || (WIN && key0 < it.klo);
+                const auto vis = [&](int k) { return (!WIN || k >= it.klo) && k < it.k1; };
                 if constexpr (!C::FP8) {
                     const int mi = lane >> 3, ri = lane & 7;
                     const int row = kt * 16 + ri + 8 * (mi >> 1);
                     const int ke = key0 + 2 * t4;
-                    const uint32_t m_lo = (edge ? ((ke < it.k1 ? 0x0000FFFFu : 0u) | (ke + 1 < it.k1 ? 0xFFFF0000u : 0u)) : 0xFFFFFFFFu);
-                    const uint32_t m_hi = (edge ? ((ke + 8 < it.k1 ? 0x0000FFFFu : 0u) | (ke + 9 < it.k1 ? 0xFFFF0000u : 0u)) : 0xFFFFFFFFu);
+                    const uint32_t m_lo = (edge ? ((vis(ke) ? 0x0000FFFFu : 0u) | (vis(ke + 1) ? 0xFFFF0000u : 0u)) : 0xFFFFFFFFu);
+                    const uint32_t m_hi = (edge ? ((vis(ke + 8) ? 0x0000FFFFu : 0u) | (vis(ke + 9) ? 0xFFFF0000u : 0u)) : 0xFFFFFFFFu);
 #pragma unroll
                     for (int dt = 0; dt < C::D / 16; ++dt) {
                         const uint32_t off = kv_off<C>(row, 16 * dt + 8 * (mi & 1), lp);
@@ -602,8 +651,8 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
                 } else {
                     const int kr = kt * 16 + 2 * t4;
                     const int ke = key0 + 2 * t4;
-                    const bool z0 = edge && ke >= it.k1, z1 = edge && ke + 1 >= it.k1;
-                    const bool z2 = edge && ke + 8 >= it.k1, z3 = edge && ke + 9 >= it.k1;
+                    const bool z0 = edge && !vis(ke), z1 = edge && !vis(ke + 1);
+                    const bool z2 = edge && !vis(ke + 8), z3 = edge && !vis(ke + 9);
 #pragma unroll
                     for (int b = 0; b < C::D / 32; ++b) {
                         const int col = 32 * b + 4 * g8;
@@ -684,7 +733,8 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
         // Stage-meta `bad` words were OR-ed per warp; make them CTA-wide.
         const bool item_bad = named_barrier_or(1, C::NCT, bad != 0);
 
-        const bool final_write = (p.split_len == 0) || it.n_splits == 1;
+        // one split holding visible keys: the row is written here, else partials
+        const bool final_write = (p.split_len == 0) || it.n_splits - it.s_first == 1;
         const long long gq = ((long long)it.g * p.n_head_kv + it.kvh) * p.n_qtiles + it.qt;
         const long long slot_idx = gq * p.max_splits + it.s;
         float* pacc = p.part_acc + slot_idx * p.qtv * C::D;

@@ -2,11 +2,14 @@
 // kernel wrote for every (sequence, KV head, query tile) whose context was cut
 // into more than one split, and writes the bf16 output rows.
 //
-// For one output row with partials (m_s, l_s, acc_s), s = 0..n-1 (m in log2
-// units, acc unnormalised):
+// For one output row with partials (m_s, l_s, acc_s), s = s0..n-1 (m in log2
+// units, acc unnormalised; s0 > 0 only with a sliding window, when the query
+// tile's rows see no key of splits below s0):
 //     M = max_s m_s,  out = (sum_s 2^(m_s - M) acc_s) / (sum_s 2^(m_s - M) l_s)
-// Sums run in split order 0..n-1, in fixed chunks of CH splits, so a row's
-// bits depend only on its own sequence -- never on the batch around it.
+// Sums run in split order, in chunks of CH splits aligned to multiples of CH,
+// so a row's bits depend only on its own sequence -- never on the batch
+// around it.  A split none of whose keys a row sees has m = -inf, l = 0,
+// acc = 0 and adds exact zeros.
 #pragma once
 #include <cuda_bf16.h>
 #include <math_constants.h>
@@ -39,8 +42,9 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __g
     const int L = __ldg(p.seq_lens + g);
     if (L < p.rows || (long long)L > (long long)p.pages_per_seq * p.page_size) return;  // zeros already written
     const int ns = (L + p.split_len - 1) / p.split_len;
-    if (ns <= 1) return;                                                              // written directly
     const int t_m0 = qt * p.qt_rows;
+    const int s_first = first_visible_key(L, p.rows, t_m0 / p.ratio, p.window) / p.split_len;
+    if (ns - s_first <= 1) return;                                                    // written directly
     const int t_ncol = min(p.M, t_m0 + p.qt_rows) - t_m0;
     const int c0 = cgi * CG;
     const int ncol = min(CG, t_ncol - c0);
@@ -56,8 +60,8 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __g
 #pragma unroll
     for (int k = 0; k < OWN; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     uint32_t any_bad = 0;
-    for (int s0 = 0; s0 < ns; s0 += CH) {
-        const int cn = min(CH, ns - s0);
+    for (int s0 = s_first; s0 < ns; s0 = (s0 / CH + 1) * CH) {
+        const int cn = min((s0 / CH + 1) * CH, ns) - s0;
         __syncthreads();
         for (int i = tid; i < cn * ncol; i += NT) {
             const int s = i / ncol, col = i - s * ncol;

@@ -10,7 +10,9 @@ static_assert(PrefillTileKeys == PrefillCfg::BN, "host and kernel agree on the k
 
 cudaError_t launch_prefill_tc05(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const AttnParams& p, int sms, cudaStream_t st) {
-    auto kern = attn_prefill_tc05_kernel;
+    // the general kernel for a sliding window or a scale <= 0, else the lean one
+    auto kern = (p.window > 0 || p.scale_log2 <= 0.f) ? attn_prefill_tc05_kernel<true>
+                                                      : attn_prefill_tc05_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PrefillCfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     long long grid = (long long)sms * PrefillCfg::CTAS;

@@ -8,10 +8,11 @@
 namespace rad {
 
 // Persistent launch: as many CTAs as fit on the device at once (never more
-// than there are work items).
+// than there are work items).  Calls with a sliding window run the kernel
+// built with the window terms, others the one without.
 template <class C>
 cudaError_t launch_cfg(const AttnParams& p, int sms, cudaStream_t st) {
-    auto kern = attn_tile_kernel<C>;
+    auto kern = p.window > 0 ? attn_tile_kernel<C, true> : attn_tile_kernel<C, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     int per_sm = 0;

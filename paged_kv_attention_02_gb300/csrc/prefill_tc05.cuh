@@ -6,7 +6,10 @@
 // "Declare: the metadata": n_head over n_head_kv) -- against keys
 // 0 .. kmax-1 of the sequence, causal per row: row r sees keys 0 .. L-R+r
 // ("kern manifest v7", $defs.Fill `seq_len`; $defs.Batch `context`: a
-// prefill's expansion of the cached rows).
+// prefill's expansion of the cached rows), or with a sliding window W only
+// the last W of them ("Radiance architecture plugins", section "Declare:
+// buffers and KV groups", RAD_KV_WINDOW); key tiles wholly below the tile's
+// first row's window are skipped.
 //
 // Warp roles (one CTA per SM, persistent over items, heavier query tiles first):
 //   warp 5      producer: TMA loads of the item's query rows (one 4-D box per
@@ -21,7 +24,9 @@
 //               written P_{j-1}, O += P_{j-1} V_{j-1} (A = P from TMEM, B = V
 //               MN-major from shared memory); tcgen05.commit signals each.
 //               The warp also zeroes V rows past the sequence's end in the
-//               tile that holds its last page (P is 0 there, V must not be NaN).
+//               tile that holds its last page, and the rows below the tile's
+//               first visible key in the first live page of a window (P is 0
+//               there, V must not be NaN).
 //   warps 0-3   softmax: thread t owns query row t (TMEM lane t); per tile it
 //               reads S_j with tcgen05.ld, masks, keeps the running max in
 //               log2 units and rescales O in TMEM only when the max grew by
@@ -72,9 +77,15 @@ struct PrefillCfg {
 struct PrefItem {
     int g, kvh, qt, L;
     bool seq_ok;
-    int m0, m_end, kmax, T;
+    int m0, m_end, kmax;
+    int klo;    // first key some row of the tile sees
+    int kt0;    // first key tile processed: klo / BN
+    int T;      // key tiles processed: kt0 .. kt0+T-1
 };
 
+// GEN: the call has a sliding window or a scale <= 0; without either, those
+// terms fold away at compile time.
+template <bool GEN>
 __device__ __forceinline__ PrefItem plan_prefill(int item, const AttnParams& p) {
     PrefItem it;
     const int per_g = p.n_head_kv * p.n_qtiles;
@@ -87,10 +98,13 @@ __device__ __forceinline__ PrefItem plan_prefill(int item, const AttnParams& p) 
     it.m0 = it.qt * PrefillCfg::BM;
     it.m_end = min(p.M, it.m0 + PrefillCfg::BM);
     it.kmax = it.seq_ok ? it.L - p.rows + (it.m_end - 1) / p.ratio + 1 : 0;
-    it.T = (it.kmax + PrefillCfg::BN - 1) / PrefillCfg::BN;
+    it.klo = (GEN && it.seq_ok) ? first_visible_key(it.L, p.rows, it.m0 / p.ratio, p.window) : 0;
+    it.kt0 = it.klo / PrefillCfg::BN;
+    it.T = (it.kmax + PrefillCfg::BN - 1) / PrefillCfg::BN - it.kt0;
     return it;
 }
 
+template <bool GEN>
 __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
     attn_prefill_tc05_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ AttnParams p) {
@@ -160,7 +174,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
             prefetch_tmap(&tm_v);
         }
         for (int item = blockIdx.x; item < n_items && !abort; item += gridDim.x) {
-            const PrefItem it = plan_prefill(item, p);
+            const PrefItem it = plan_prefill<GEN>(item, p);
             if (!it.seq_ok) continue;
             if (ic >= 1 && !mbar_wait_bounded(bar_q_empty, (ic - 1) & 1u, kWaitLimitNs)) {
                 abort = true;
@@ -175,6 +189,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
             }
             ++ic;
             const int page_hi = (it.kmax + P - 1) / P;
+            const int page_lo = GEN ? it.klo / P : 0;   // pages below hold no visible key: never read
             const int32_t* trow = p.page_table + (long long)it.g * p.pages_per_seq;
             int batch0 = -1 << 30, my_pg = 0;
             for (int j = 0; j < it.T; ++j) {
@@ -183,12 +198,12 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
                     abort = true;
                     break;
                 }
-                const int pstart = j * ppt;
+                const int pstart = (it.kt0 + j) * ppt;
                 if (pstart + ppt > batch0 + 32) {
                     batch0 = pstart;
                     const int pi = batch0 + lane;
                     my_pg = 0;
-                    if (pi < page_hi) {
+                    if ((!GEN || pi >= page_lo) && pi < page_hi) {
                         const int pg = __ldg(trow + pi);
                         my_pg = (pg < 0 || pg >= p.num_pages) ? 0 : pg;
                     }
@@ -202,7 +217,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
                 for (int i = 0; i < ppt; ++i) {
                     const int pi = pstart + i;
                     const int pg = __shfl_sync(0xffffffffu, my_pg, (pi - batch0) & 31);
-                    const int tok = pi < page_hi ? pg * P : oob_tok;
+                    const int tok = ((!GEN || pi >= page_lo) && pi < page_hi) ? pg * P : oob_tok;
                     if (lane == 0) {
 #pragma unroll
                         for (int hb = 0; hb < 2; ++hb) {
@@ -232,16 +247,18 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
         uint32_t sc = 0, tc = 0, ic = 0;
         bool issued = false;
         for (int item = blockIdx.x; item < n_items && !abort; item += gridDim.x) {
-            const PrefItem it = plan_prefill(item, p);
+            const PrefItem it = plan_prefill<GEN>(item, p);
             if (!it.seq_ok) continue;
             if (!mbar_wait_bounded(bar_q_full, ic & 1u, kWaitLimitNs)) {
                 abort = true;
                 break;
             }
             tc_fence_after();
-            // V rows to zero: slots past the sequence's end in its last page
+            // V rows to zero: slots past the sequence's end in its last page,
+            // and slots of the first live page below the tile's first visible key
             const int P = p.page_size;
             const int zero_lo = it.L, zero_hi = ((it.L + P - 1) / P) * P;
+            const int head_lo = (it.klo / P) * P, head_hi = it.klo;
             for (int j = 0; j <= it.T && !abort; ++j) {
                 if (j < it.T) {
                     const uint32_t s_ = sc + j, st = s_ % C::NS;
@@ -277,11 +294,14 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
                     }
                     const uint32_t vb = base + C::OFF_STAGE + st * C::STAGE_BYTES + C::TILE_BYTES;
                     // zero V rows of keys past the sequence's end held by this tile
-                    const int key0 = jj * C::BN;
+                    const int key0 = (it.kt0 + jj) * C::BN;
                     const int z0 = max(zero_lo, key0) - key0, z1 = min(zero_hi, key0 + C::BN) - key0;
-                    if (z0 < z1) {
-                        for (int idx = lane; idx < (z1 - z0) * 16; idx += 32) {
-                            const int row = z0 + idx / 16, c16 = idx % 16;
+                    const int h0 = max(head_lo, key0) - key0, h1 = min(head_hi, key0 + C::BN) - key0;
+                    const int nz = max(z1 - z0, 0), nh = GEN ? max(h1 - h0, 0) : 0;
+                    if (nz + nh > 0) {
+                        for (int idx = lane; idx < (nz + nh) * 16; idx += 32) {
+                            const int rr = idx / 16, c16 = idx % 16;
+                            const int row = rr < nz ? z0 + rr : h0 + (rr - nz);
                             const uint32_t a = vb + (c16 >> 3) * C::HB_BYTES + row * 128 + (((c16 & 7) ^ (row & 7)) << 4);
                             asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
                         }
@@ -323,7 +343,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
         const float c = p.scale_log2;
         uint32_t tc = 0;
         for (int item = blockIdx.x; item < n_items && !abort; item += gridDim.x) {
-            const PrefItem it = plan_prefill(item, p);
+            const PrefItem it = plan_prefill<GEN>(item, p);
             const int m = it.m0 + t;
             const bool valid = m < it.m_end;
             const int r = m / p.ratio, hl = m - r * p.ratio;
@@ -335,16 +355,19 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
                 if (t == 0 && p.err_word) atomicOr(p.err_word, kErrSeqLen);
                 continue;
             }
-            // the whole sequence's page ids must be valid, or all its rows are zero
+            // every page id the sequence's rows need must be valid, or all its
+            // rows are zero
             bool bad = false;
             const int npg = (it.L + p.page_size - 1) / p.page_size;
+            const int pg0 = GEN ? first_visible_key(it.L, p.rows, 0, p.window) / p.page_size : 0;
             const int32_t* trow = p.page_table + (long long)it.g * p.pages_per_seq;
-            for (int i = t; i < npg; i += 128) {
+            for (int i = pg0 + t; i < npg; i += 128) {
                 const int pg = __ldg(trow + i);
                 bad |= (pg < 0 || pg >= p.num_pages);
             }
             bad = named_barrier_or(1, 128, bad);
             const int nk = valid ? it.L - p.rows + r + 1 : it.L;
+            const int nlo = (GEN && valid) ? first_visible_key(it.L, p.rows, r, p.window) : 0;   // row sees nlo .. nk-1
             float m_run = -CUDART_INF_F, l_run = 0.f;
             for (int j = 0; j < it.T; ++j) {
                 const uint32_t tcj = tc + j, b = tcj & 1u;
@@ -360,11 +383,21 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
                 } else {
                     tmem_ld64(sc_, *reinterpret_cast<uint32_t(*)[64]>(sv));
                 }
-                const int lim = nk - j * C::BN;   // columns >= lim are masked
-                if (lim < C::BN) {
+                // Logits are scaled by c after the max; a scale <= 0 would turn
+                // that order around (and -inf * 0 into NaN), so then the tile is
+                // scaled first and c taken as 1.
+                float cs = c;
+                if (GEN && c <= 0.f) {
+#pragma unroll
+                    for (int e = 0; e < C::BN; ++e) sv[e] = __float_as_uint(__uint_as_float(sv[e]) * c);
+                    cs = 1.f;
+                }
+                const int key0 = (it.kt0 + j) * C::BN;
+                const int lim = nk - key0, lim_lo = nlo - key0;   // columns outside [lim_lo, lim) are masked
+                if (lim < C::BN || (GEN && lim_lo > 0)) {
 #pragma unroll
                     for (int e = 0; e < C::BN; ++e)
-                        if (e >= lim) sv[e] = __float_as_uint(-CUDART_INF_F);
+                        if (e >= lim || (GEN && e < lim_lo)) sv[e] = __float_as_uint(-CUDART_INF_F);
                 }
                 // row max as 8 independent chains
                 float mx8[8];
@@ -375,7 +408,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
                 const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                        fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
                 if (mx != -CUDART_INF_F) {
-                    const float mx_s = mx * c;
+                    const float mx_s = mx * cs;
                     if (m_run == -CUDART_INF_F) {
                         m_run = mx_s;
                     } else if (mx_s > m_run + C::RESCALE_LOG2) {
@@ -406,8 +439,8 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
                     uint32_t hi[16], lo[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
-                        const float p0 = exp2f(__uint_as_float(sv[32 * q + 2 * e]) * c - m_use);
-                        const float p1 = exp2f(__uint_as_float(sv[32 * q + 2 * e + 1]) * c - m_use);
+                        const float p0 = exp2f(__uint_as_float(sv[32 * q + 2 * e]) * cs - m_use);
+                        const float p1 = exp2f(__uint_as_float(sv[32 * q + 2 * e + 1]) * cs - m_use);
                         ps8[e & 7] += p0 + p1;
                         const uint32_t h = pack_bf16x2(p0, p1);
                         hi[e] = h;

@@ -153,6 +153,12 @@ int device_info(int* dev_out, int* sms_out) {
     return RAD_OK;
 }
 
+int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const int32_t* page_table,
+                    const int32_t* seq_lens, int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv,
+                    int32_t head_dim, int32_t page_size, int32_t pages_per_seq, int32_t num_pages, float scale,
+                    int32_t kv_dtype, const float* k_scales, const float* v_scales, int32_t window, void* out,
+                    void* workspace, size_t workspace_bytes, uint32_t* err_word, rad_stream_t stream);
+
 }  // namespace
 
 extern "C" {
@@ -173,6 +179,31 @@ int rad_attn_paged(const void* q, const void* k_pool, const void* v_pool, const 
                    int32_t num_pages, float scale, int32_t kv_dtype, const float* k_scales,
                    const float* v_scales, void* out, void* workspace, size_t workspace_bytes,
                    uint32_t* err_word, rad_stream_t stream) {
+    return attn_paged_impl(q, k_pool, v_pool, page_table, seq_lens, groups, rows, n_head, n_head_kv, head_dim,
+                           page_size, pages_per_seq, num_pages, scale, kv_dtype, k_scales, v_scales, 0, out,
+                           workspace, workspace_bytes, err_word, stream);
+}
+
+int rad_attn_paged_window(const void* q, const void* k_pool, const void* v_pool, const int32_t* page_table,
+                          const int32_t* seq_lens, int32_t groups, int32_t rows, int32_t n_head,
+                          int32_t n_head_kv, int32_t head_dim, int32_t page_size, int32_t pages_per_seq,
+                          int32_t num_pages, float scale, int32_t kv_dtype, const float* k_scales,
+                          const float* v_scales, int32_t window, void* out, void* workspace,
+                          size_t workspace_bytes, uint32_t* err_word, rad_stream_t stream) {
+    return attn_paged_impl(q, k_pool, v_pool, page_table, seq_lens, groups, rows, n_head, n_head_kv, head_dim,
+                           page_size, pages_per_seq, num_pages, scale, kv_dtype, k_scales, v_scales, window, out,
+                           workspace, workspace_bytes, err_word, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const int32_t* page_table,
+                    const int32_t* seq_lens, int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv,
+                    int32_t head_dim, int32_t page_size, int32_t pages_per_seq, int32_t num_pages, float scale,
+                    int32_t kv_dtype, const float* k_scales, const float* v_scales, int32_t window, void* out,
+                    void* workspace, size_t workspace_bytes, uint32_t* err_word, rad_stream_t stream) {
     int rc = check_scalars(groups, rows, n_head, n_head_kv, head_dim, page_size, pages_per_seq, kv_dtype);
     if (rc != RAD_OK) return rc;
     if (num_pages <= 0 || (long long)num_pages * page_size > 0x7FFFFFFFll) return RAD_E_SHAPE;
@@ -186,7 +217,7 @@ int rad_attn_paged(const void* q, const void* k_pool, const void* v_pool, const 
     const bool fp8 = kv_dtype == RAD_KV_FP8_E4M3;
     if (fp8 && (!k_scales || !v_scales || !is_aligned(k_scales, 4) || !is_aligned(v_scales, 4)))
         return RAD_E_ARG;
-    if (!std::isfinite(scale)) return RAD_E_ARG;
+    if (!std::isfinite(scale) || window < 0) return RAD_E_ARG;
     const Plan pl = make_plan(groups, rows, n_head, n_head_kv, head_dim, page_size, pages_per_seq, kv_dtype);
     if (pl.total_bytes > 0 && (!workspace || workspace_bytes < pl.total_bytes || !is_aligned(workspace, 256)))
         return RAD_E_WORKSPACE;
@@ -220,6 +251,7 @@ int rad_attn_paged(const void* q, const void* k_pool, const void* v_pool, const 
     p.max_splits = pl.max_splits;
     p.split_len = pl.split_len;
     p.n_items = (int)pl.n_items;
+    p.window = window;
     p.scale_log2 = scale * 1.4426950408889634f;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (pl.total_bytes > 0) {
@@ -254,6 +286,10 @@ int rad_attn_paged(const void* q, const void* k_pool, const void* v_pool, const 
         e = fp8 ? rad::launch_d256_fp8(pl.family, p, sms, st) : rad::launch_d256_bf16(pl.family, p, sms, st);
     return e == cudaSuccess ? RAD_OK : RAD_E_CUDA;
 }
+
+}  // namespace
+
+extern "C" {
 
 int rad_attn_paged_describe(int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_dim,
                             int32_t page_size, int32_t kv_dtype, char* buf, size_t buf_len) {

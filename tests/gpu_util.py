@@ -32,23 +32,35 @@ class DevWorkload:
         self.table = torch.from_numpy(w.page_table).to(device)
         self.lens = torch.from_numpy(w.seq_lens).to(device)
 
-    def run(self, q=None, table=None, lens=None, stream=None, out=None, workspace=None):
+    def run(self, q=None, table=None, lens=None, stream=None, out=None, workspace=None, window=None,
+            scale=None, k=None, v=None):
+        """One call through rad_attn_paged, or rad_attn_paged_window when
+        `window` is given; returns (out, err_word)."""
         c = self.w.cfg
         err = torch.zeros(1, dtype=torch.int32, device=self.q.device)
-        out = b.attn_paged(self.q if q is None else q, self.k, self.v,
-                           self.table if table is None else table, self.lens if lens is None else lens,
-                           rows=c.rows, n_head=c.n_head, n_head_kv=c.n_head_kv,
-                           head_dim=c.meta.get("head_dim", c.head_dim), page_size=c.page_size,
-                           scale=c.scale, kv_dtype=c.kv_dtype, k_scales=self.ks, v_scales=self.vs,
-                           out=out, workspace=workspace, err_word=err, stream=stream)
+        args = (self.q if q is None else q, self.k if k is None else k, self.v if v is None else v,
+                self.table if table is None else table, self.lens if lens is None else lens)
+        kw = dict(rows=c.rows, n_head=c.n_head, n_head_kv=c.n_head_kv,
+                  head_dim=c.meta.get("head_dim", c.head_dim), page_size=c.page_size,
+                  scale=c.scale if scale is None else scale, kv_dtype=c.kv_dtype, k_scales=self.ks,
+                  v_scales=self.vs, out=out, workspace=workspace, err_word=err, stream=stream)
+        if window is None:
+            out = b.attn_paged(*args, **kw)
+        else:
+            out = b.attn_paged_window(*args, window=window, **kw)
         torch.cuda.synchronize()
         return out, int(err.item())
 
 
-def oracle_rows(w: wl.Workload, sel=None):
+def oracle_rows(w: wl.Workload, sel=None, window=0, scale=None, page_table=None):
     import oracle
-    return oracle.attn_paged_rows(w.q, w.k_pool, w.v_pool, w.page_table, w.seq_lens, sel=sel,
-                                  k_scales=w.k_scales, v_scales=w.v_scales, **w.call_args())
+    args = w.call_args()
+    if scale is not None:
+        args["scale"] = scale
+    return oracle.attn_paged_rows(w.q, w.k_pool, w.v_pool,
+                                  w.page_table if page_table is None else page_table, w.seq_lens,
+                                  sel=sel, k_scales=w.k_scales, v_scales=w.v_scales, window=window,
+                                  **args)
 
 
 def assert_parity(gpu: np.ndarray, ref: np.ndarray, fp8: bool, what=""):

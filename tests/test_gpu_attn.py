@@ -217,6 +217,34 @@ def test_verify_bad_page_in_a_late_split_zeroes_every_row(mid):
     assert np.all(ob[4] == 0) and np.array_equal(ob[:4], gb[:4])
 
 
+@pytest.mark.parametrize("name", ["chunk_split", "prefill", "prefill_fp8_d256"])
+def test_bad_last_page_zeroes_rows_of_every_query_tile(mid, name):
+    # Calls with several query tiles per KV head: the early tiles never load
+    # the last page, yet a bad id there zeroes every row of the group.
+    w, dw = mid(name)
+    good, _ = dw.run()
+    g = w.groups - 1
+    last = (int(w.seq_lens[g]) - 1) // w.cfg.page_size
+    table = dw.table.clone()
+    table[g, last] = -2
+    o, err = dw.run(table=table)
+    assert err == b.RAD_ERRW_PAGE
+    ob, gb = bits(o), bits(good)
+    assert np.all(ob[g] == 0) and np.array_equal(ob[:g], gb[:g])
+
+
+@pytest.mark.parametrize("name", ["prefill", "dec128", "ver_fp8", "chunk_split"])
+@pytest.mark.parametrize("scale", [0.0, -0.07])
+def test_zero_and_negative_scales_match_oracle(mid, name, scale):
+    # scale 0: every visible key weighs the same; scale < 0 reverses the order
+    # of the logits (the row max is taken after scaling).
+    w, dw = mid(name)
+    out, err = dw.run(scale=scale)
+    assert err == 0
+    ref = oracle_rows(w, scale=scale)
+    assert_parity(as_f64(out), ref.out, dw.fp8, f"{name} scale {scale}")
+
+
 def test_refused_shapes_write_nothing(mid):
     w, dw = mid("dec128")
     canary = torch.full((w.groups, 1, 32, 128), 7.0, dtype=torch.bfloat16, device="cuda")
