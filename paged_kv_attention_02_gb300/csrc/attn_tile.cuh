@@ -132,18 +132,27 @@ struct TileCfg {
     static constexpr int BOXW = 128 / E;          // elements per 128-byte row
     static constexpr int NBOX = D / BOXW;
     static constexpr int Q_SLOT_BYTES = QT * D * 2;
-    static constexpr int MSTRIDE = D + 4;   // floats per merge row (bank spread)
     static constexpr int OFF_Q = NS * STAGE_BYTES;
     static constexpr int OFF_MERGE = OFF_Q + 2 * Q_SLOT_BYTES;
-    static constexpr int OFF_ML = OFF_MERGE + WK * QT * MSTRIDE * 4;
-    static constexpr int OFF_META = OFF_ML + WK * QT * 2 * 4;
+    // merge: one warp state [query column][head dim] (each of two key warps
+    // publishes half of its own), every key warp's (max, sum) per query
+    // column, and the merged (max, sum)
+    static constexpr int MSTRIDE = D + 4;   // floats per merge row (bank spread)
+    static constexpr int MERGE_BYTES = QT * MSTRIDE * 4;
+    static constexpr int ML_BYTES = WK > 1 ? WQ * WK * NQW * 4 * 16 : 0;
+    static constexpr int OFF_ML = OFF_MERGE + MERGE_BYTES;
+    static constexpr int OFF_MLF = OFF_ML + ML_BYTES;
+    static constexpr int OFF_META = OFF_MLF + QT * 8;
     static constexpr int META_STRIDE = 64;  // ks[4], vs[4], bad, pad
     static constexpr int OFF_BARS = OFF_META + NS * META_STRIDE;
     static constexpr int OFF_MISC = OFF_BARS + (2 * NS + 4) * 8;
     static constexpr int SMEM_USED = OFF_MISC + 16;
-    static constexpr int SMEM_BYTES = SMEM_USED + 1024;   // base alignment slack
+    // The swizzle is applied to offsets in software (not by address bits), so
+    // 128-byte alignment of the base is all the copies and ldmatrix need.
+    static constexpr int SMEM_BYTES = SMEM_USED + 128;    // base alignment slack
     static_assert(KS % 32 == 0, "a stage holds whole pages of either page size (16 or 32 slots)");
     static_assert(SUBS % WK == 0, "stage keys must split evenly over key warps");
+    static_assert(WK == 1 || WK == 2, "the merge pairs at most two key warps");
     static_assert(MAX_PAGES_STAGE <= 4, "stage meta holds 4 pages");
     static_assert(D % 32 == 0, "head_dim multiple of 32");
     static_assert(SMEM_BYTES * MINB <= 233472 - 1024 * MINB, "shared memory budget");
@@ -247,7 +256,7 @@ template <class C, bool WIN>
 __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const __grid_constant__ AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
-    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    const uint32_t base = (raw_addr + 127u) & ~127u;
     uint8_t* smem = smem_raw + (base - raw_addr);
 
     const uint32_t bar_full = base + C::OFF_BARS;
@@ -710,74 +719,128 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
                 l += __shfl_xor_sync(0xffffffffu, l, 16);
                 l_run[j][c] = l;
             }
-        // ---------------- stage this warp's state in shared memory
-        float* mrg = reinterpret_cast<float*>(smem + C::OFF_MERGE) + wk * C::QT * C::MSTRIDE;
-        float* mml = reinterpret_cast<float*>(smem + C::OFF_ML) + wk * C::QT * 2;
+        // ---------------- merge the key warps' states
+        // One [query column][head dim] buffer holds a single warp state.  With
+        // two key warps per query group each owns half of the d-tiles: it
+        // publishes the other half into the buffer, then merges its own half
+        // from its registers and the published values and writes the result
+        // back in place (every element is published, read and rewritten by
+        // fixed lanes, ordered by the barriers).  The merge sums in key-warp
+        // order 0, 1 whichever warp performs it.  All consumer threads then
+        // write the tile out with coalesced 16-byte reads.
+        constexpr int MT = C::D / 16;
+        constexpr int MTW = MT / C::WK;   // d-tiles owned per key warp
+        const int own0 = wk * MTW;
+        float* mrg = reinterpret_cast<float*>(smem + C::OFF_MERGE);       // [QT][MSTRIDE]
+        float4* mlpub = reinterpret_cast<float4*>(smem + C::OFF_ML);      // [wq][wk][j][t4]
+        float2* mlfin = reinterpret_cast<float2*>(smem + C::OFF_MLF);     // [QT] merged (max, sum)
+        if constexpr (C::WK > 1) {
 #pragma unroll
-        for (int j = 0; j < C::NQW; ++j) {
+            for (int j = 0; j < C::NQW; ++j) {
 #pragma unroll
-            for (int mt = 0; mt < C::D / 16; ++mt)
+                for (int mt = 0; mt < MT; ++mt) {
+                    if (mt >= own0 && mt < own0 + MTW) continue;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int col = lane_col<C>(wq, j, t4, e & 1);
-                    mrg[col * C::MSTRIDE + d_of<C>(mt, g8 + ((e >> 1) << 3))] = oacc[j][mt][e];
+                    for (int e = 0; e < 4; ++e)
+                        mrg[lane_col<C>(wq, j, t4, e & 1) * C::MSTRIDE + d_of<C>(mt, g8 + ((e >> 1) << 3))] =
+                            oacc[j][mt][e];
                 }
-            if (g8 == 0)
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const int col = lane_col<C>(wq, j, t4, c);
-                    mml[col * 2 + 0] = m_run[j][c];
-                    mml[col * 2 + 1] = l_run[j][c];
-                }
+                if (g8 == 0)
+                    mlpub[((wq * C::WK + wk) * C::NQW + j) * 4 + t4] =
+                        make_float4(m_run[j][0], l_run[j][0], m_run[j][1], l_run[j][1]);
+            }
         }
-        // Stage-meta `bad` words were OR-ed per warp; make them CTA-wide.
+        // Stage-meta `bad` words were OR-ed per warp; make them CTA-wide (this
+        // barrier also orders the published states before their reads).
         const bool item_bad = named_barrier_or(1, C::NCT, bad != 0);
 
         // one split holding visible keys: the row is written here, else partials
         const bool final_write = (p.split_len == 0) || it.n_splits - it.s_first == 1;
-        const long long gq = ((long long)it.g * p.n_head_kv + it.kvh) * p.n_qtiles + it.qt;
-        const long long slot_idx = gq * p.max_splits + it.s;
-        float* pacc = p.part_acc + slot_idx * p.qtv * C::D;
-        float* pml = p.part_ml + slot_idx * p.qtv * 2;
-        const float* mrg0 = reinterpret_cast<const float*>(smem + C::OFF_MERGE);
-        const float* mml0 = reinterpret_cast<const float*>(smem + C::OFF_ML);
-        for (int idx = tid; idx < (it.m_end - it.m0) * C::D; idx += C::NCT) {
-            const int col = idx / C::D, d = idx - col * C::D;
-            float mw = -CUDART_INF_F;
 #pragma unroll
-            for (int w = 0; w < C::WK; ++w) mw = fmaxf(mw, mml0[(w * C::QT + col) * 2]);
-            const float m_use = (mw == -CUDART_INF_F) ? 0.f : mw;
-            float acc = 0.f, l = 0.f;
+        for (int j = 0; j < C::NQW; ++j) {
+            float fw[2][C::WK], scale_out[2];   // scale_out: 1/l per column
 #pragma unroll
-            for (int w = 0; w < C::WK; ++w) {
-                const float f = exp2f(mml0[(w * C::QT + col) * 2] - m_use);
-                acc += f * mrg0[(w * C::QT + col) * C::MSTRIDE + d];
-                l += f * mml0[(w * C::QT + col) * 2 + 1];
-            }
-            if (final_write) {
-                const int m = it.m0 + col;
-                const int r = m / p.ratio, hl = m - r * p.ratio;
+            for (int c = 0; c < 2; ++c) {
+                float mv[C::WK], lv[C::WK];
+#pragma unroll
+                for (int w = 0; w < C::WK; ++w) {
+                    if (C::WK == 1) {
+                        mv[w] = m_run[j][c];
+                        lv[w] = l_run[j][c];
+                    } else {
+                        const float4 o = mlpub[((wq * C::WK + w) * C::NQW + j) * 4 + t4];
+                        mv[w] = c ? o.z : o.x;
+                        lv[w] = c ? o.w : o.y;
+                    }
+                }
+                float mx = mv[0];
+#pragma unroll
+                for (int w = 1; w < C::WK; ++w) mx = fmaxf(mx, mv[w]);
+                const float m_use = (mx == -CUDART_INF_F) ? 0.f : mx;
+#pragma unroll
+                for (int w = 0; w < C::WK; ++w) fw[c][w] = exp2f(mv[w] - m_use);
+                float l = fw[c][0] * lv[0];
+#pragma unroll
+                for (int w = 1; w < C::WK; ++w) l = fmaf(fw[c][w], lv[w], l);
                 // acc * (1/l), the combine kernel's form, so a row written here
                 // and the same row merged from splits round identically
-                const float inv = 1.f / l;
-                const float o = item_bad ? 0.f : acc * inv;
-                p.out[(((long long)it.g * p.rows + r) * p.n_head + it.kvh * p.ratio + hl) * C::D + d] =
-                    __float2bfloat16_rn(o);
-            } else {
-                __stcg(pacc + col * C::D + d, acc);
-                if (d == 0) {
-                    __stcg(pml + col * 2, mw);
-                    __stcg(pml + col * 2 + 1, l);
+                scale_out[c] = 1.f / l;
+                const int col = lane_col<C>(wq, j, t4, c);
+                if (!final_write && wk == 0 && g8 == 0) mlfin[col] = make_float2(mx, l);
+            }
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                if (mt < own0 || mt >= own0 + MTW) continue;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c = e & 1;
+                    float* slot = mrg + lane_col<C>(wq, j, t4, c) * C::MSTRIDE + d_of<C>(mt, g8 + ((e >> 1) << 3));
+                    float acc;
+                    if constexpr (C::WK == 1) {
+                        acc = fw[c][0] * oacc[j][mt][e];
+                    } else {
+                        const float other = *slot;
+                        const float a0 = wk == 0 ? oacc[j][mt][e] : other;
+                        const float a1 = wk == 0 ? other : oacc[j][mt][e];
+                        acc = fmaf(fw[c][1], a1, fw[c][0] * a0);
+                    }
+                    *slot = final_write ? (item_bad ? 0.f : acc * scale_out[c]) : acc;
                 }
             }
         }
-        if (final_write) {
-            if (item_bad && tid == 0 && p.err_word) atomicOr(p.err_word, kErrPage);
-            // the merge buffers are rewritten by the next item
-            named_barrier_sync(1, C::NCT);
-            continue;
+        named_barrier_sync(1, C::NCT);
+        {
+            const int ncols = it.m_end - it.m0;
+            constexpr int D4 = C::D / 4;
+            if (final_write) {
+                for (int idx = tid; idx < ncols * D4; idx += C::NCT) {
+                    const int col = idx / D4, d4 = idx - col * D4;
+                    const float4 v = *reinterpret_cast<const float4*>(mrg + col * C::MSTRIDE + 4 * d4);
+                    const int m = it.m0 + col;
+                    const int r = m / p.ratio, hl = m - r * p.ratio;
+                    __nv_bfloat16* o =
+                        p.out + (((long long)it.g * p.rows + r) * p.n_head + it.kvh * p.ratio + hl) * C::D + 4 * d4;
+                    uint2 w;
+                    w.x = pack_bf16x2(v.x, v.y);
+                    w.y = pack_bf16x2(v.z, v.w);
+                    *reinterpret_cast<uint2*>(o) = w;
+                }
+                if (item_bad && tid == 0 && p.err_word) atomicOr(p.err_word, kErrPage);
+            } else {
+                const long long gq = ((long long)it.g * p.n_head_kv + it.kvh) * p.n_qtiles + it.qt;
+                const long long slot_idx = gq * p.max_splits + it.s;
+                float* pacc = p.part_acc + slot_idx * p.qtv * C::D;
+                float* pml = p.part_ml + slot_idx * p.qtv * 2;
+                for (int idx = tid; idx < ncols * D4; idx += C::NCT) {
+                    const int col = idx / D4, d4 = idx - col * D4;
+                    __stcg(reinterpret_cast<float4*>(pacc + col * C::D) + d4,
+                           *reinterpret_cast<const float4*>(mrg + col * C::MSTRIDE + 4 * d4));
+                }
+                for (int col = tid; col < ncols; col += C::NCT)
+                    __stcg(reinterpret_cast<float2*>(pml) + col, mlfin[col]);
+                if (tid == 0) __stcg(p.part_flag + slot_idx, item_bad ? 1u : 0u);
+            }
         }
-        if (tid == 0) __stcg(p.part_flag + slot_idx, item_bad ? 1u : 0u);
         // the merge buffers are rewritten by the next item
         named_barrier_sync(1, C::NCT);
     }

@@ -37,7 +37,7 @@ constexpr int kSplitMaxRows = 256;
 #define RAD_TILE_D128_FP8_WIDE 4, 2, 1, 64, 8, 1
 #endif
 #ifndef RAD_TILE_D256_BF16_DEC
-#define RAD_TILE_D256_BF16_DEC 1, 1, 2, 32, 2, 2
+#define RAD_TILE_D256_BF16_DEC 1, 1, 2, 32, 3, 2
 #endif
 #ifndef RAD_TILE_D256_BF16_VER
 #define RAD_TILE_D256_BF16_VER 4, 1, 2, 32, 3, 1
