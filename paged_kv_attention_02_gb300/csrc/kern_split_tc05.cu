@@ -1,0 +1,52 @@
+// Launcher of the tcgen05 split kernel (head_dim 128, fp8 KV pools) and of
+// the split combine after it.
+#include <cuda_runtime.h>
+
+#include "launch.cuh"
+#include "split_tc05.cuh"
+#include "tile_configs.cuh"
+
+namespace rad {
+
+namespace {
+
+template <int N, bool WIN>
+cudaError_t launch_n(const AttnParams& p, int sms, cudaStream_t st) {
+    using C = SplitTcCfg<N>;
+    auto kern = attn_split_tc05_kernel<N, WIN>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    long long grid = sms;   // one CTA per SM (shared memory), persistent over the items
+    if (grid > p.n_items) grid = p.n_items;
+    if (grid < 1) grid = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(C::NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = st;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+}  // namespace
+
+TileInfo split_tc05_info(int n) {
+    if (n == 16) {
+        using C = SplitTcCfg<16>;
+        return TileInfo{128, 1, 4, 0, 0, C::BK, C::NS, C::N, C::NTHREADS, C::SMEM_BYTES, 1};
+    }
+    using C = SplitTcCfg<32>;
+    return TileInfo{128, 1, 4, 0, 0, C::BK, C::NS, C::N, C::NTHREADS, C::SMEM_BYTES, 1};
+}
+
+cudaError_t launch_split_tc05(const AttnParams& p, int sms, cudaStream_t st) {
+    cudaError_t e;
+    const bool win = p.window > 0;
+    if (p.qt_rows == 16)
+        e = win ? launch_n<16, true>(p, sms, st) : launch_n<16, false>(p, sms, st);
+    else
+        e = win ? launch_n<32, true>(p, sms, st) : launch_n<32, false>(p, sms, st);
+    if (e != cudaSuccess || p.max_splits <= 1) return e;
+    return launch_combine<128>(p, st);
+}
+
+}  // namespace rad

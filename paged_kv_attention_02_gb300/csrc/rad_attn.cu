@@ -78,13 +78,18 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
     // share one key schedule.  Longer calls: the tcgen05 prefill kernel where
     // it applies, else the wide tile.
     pl.split_len = rows <= rad::kSplitMaxRows ? rad::kSplitLen : 0;
-    if (pl.split_len > 0)
+    if (pl.split_len > 0 && RAD_SPLIT_TC05 && head_dim == 128 && kv_dtype == RAD_KV_FP8_E4M3)
+        pl.family = rad::kFamSplitTC;
+    else if (pl.split_len > 0)
         pl.family = pl.M <= 8 ? rad::kFamDecode : rad::kFamVerify;
     else
         pl.family = use_prefill_tc(rows, pl.ratio, head_dim, kv_dtype) ? rad::kFamPrefillTC : rad::kFamWide;
-    pl.tile = pl.family == rad::kFamPrefillTC
-                  ? rad::TileInfo{128, 0, 4, 0, 0, rad::PrefillTileKeys, RAD_PREFILL_NS, 128, 192, 0, RAD_PREFILL_CTAS}
-                  : tile_for(head_dim, kv_dtype, pl.family);
+    if (pl.family == rad::kFamPrefillTC)
+        pl.tile = rad::TileInfo{128, 0, 4, 0, 0, rad::PrefillTileKeys, RAD_PREFILL_NS, 128, 192, 0, RAD_PREFILL_CTAS};
+    else if (pl.family == rad::kFamSplitTC)
+        pl.tile = rad::split_tc05_info(rad::split_tc05_rows(pl.M));
+    else
+        pl.tile = tile_for(head_dim, kv_dtype, pl.family);
     pl.n_qtiles = (pl.M + pl.tile.QT - 1) / pl.tile.QT;
     pl.qtv = pl.M < pl.tile.QT ? pl.M : pl.tile.QT;
     const long long cap_keys = (long long)pages_per_seq * page_size;
@@ -102,8 +107,13 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
 }
 
 const char* family_name(int f) {
-    return f == rad::kFamDecode ? "decode"
-                                : (f == rad::kFamVerify ? "verify" : (f == rad::kFamWide ? "wide" : "prefill_tc05"));
+    switch (f) {
+        case rad::kFamDecode: return "decode";
+        case rad::kFamVerify: return "verify";
+        case rad::kFamWide: return "wide";
+        case rad::kFamPrefillTC: return "prefill_tc05";
+        default: return "split_tc05";
+    }
 }
 
 int get_encoder() {
@@ -280,6 +290,8 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
             encode_bf16_map(&tv, v_pool, 3, kd, ks, kb) != RAD_OK)
             return RAD_E_CUDA;
         e = rad::launch_prefill_tc05(tq, tk, tv, p, sms, st);
+    } else if (pl.family == rad::kFamSplitTC) {
+        e = rad::launch_split_tc05(p, sms, st);
     } else if (head_dim == 128)
         e = fp8 ? rad::launch_d128_fp8(pl.family, p, sms, st) : rad::launch_d128_bf16(pl.family, p, sms, st);
     else
@@ -301,6 +313,15 @@ int rad_attn_paged_describe(int32_t rows, int32_t n_head, int32_t n_head_kv, int
     }
     const Plan pl = make_plan(1, rows, n_head, n_head_kv, head_dim, page_size, 1, kv_dtype);
     const rad::TileInfo& t = pl.tile;
+    if (pl.family == rad::kFamSplitTC) {
+        snprintf(buf, buf_len,
+                 "attn_split_tc05 family=%s head_dim=%d kv=fp8e4m3 query_rows_per_kv_head=%d tile_rows=%d "
+                 "keys_per_tile=%d stages=%d ctas_per_sm=1 warps=4 workers+1 mma+2 producers "
+                 "mma=tcgen05.kind::f16 (keys as M, query rows as N; K/V e4m3 -> f16 once per tile) "
+                 "split_len=%d + attn_combine (split order)",
+                 family_name(pl.family), head_dim, pl.M, t.QT, t.KS, t.NS, pl.split_len);
+        return RAD_OK;
+    }
     if (pl.family == rad::kFamPrefillTC) {
         snprintf(buf, buf_len,
                  "attn_prefill_tc05 family=%s head_dim=%d kv=bf16 query_rows_per_kv_head=%d tile_rows=128 "

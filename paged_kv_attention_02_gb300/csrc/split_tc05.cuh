@@ -1,0 +1,723 @@
+// Split-call attention on the 5th-generation tensor cores (tcgen05, TMEM) for
+// fp8-e4m3 KV pools with head_dim 128: the decode and speculative-verify call
+// shapes ("kern manifest v7", $defs.Batch) of the `attn_paged` op.
+//
+// Work items and partial results are those of attn_tile.cuh: (split s,
+// sequence g, KV head kvh, query tile qt) with N query rows per tile (the
+// rows x n_head/n_head_kv query heads sharing the KV head), splits of
+// split_len keys whose count depends only on the sequence length, and the
+// same combine kernel.
+//
+// Keys are the MMA's M dimension (128 per tile) and the query rows its N:
+//   S^T[key][q] = K[key][:] . Q[q][:]        M 128, N, K = head_dim
+//   O^T[d][q]  += V^T[d][key] . P^T[key][q]   M = head_dim 128, N, K = 128 keys
+// so a decode step's few query rows per KV head cost a narrow N instead of
+// an idle M.  Warp roles (one CTA per SM, persistent):
+//   warps 5, 6  producers: page ids from the page table ("kern manifest v7",
+//               $defs.Domain), 16-byte cp.async copies of each tile's e4m3 K
+//               rows (warp 5) and V rows (warp 6) into a staging ring, the
+//               per-page scales, and a 1-D bulk copy of the query rows.
+//   warp 4      MMA: one lane issues tcgen05.mma.kind::f16 from shared-memory
+//               operands into TMEM and commits to mbarriers.
+//   warps 0-3   workers, thread t <-> key t of the tile <-> TMEM lane t:
+//               convert staged e4m3 rows to f16 once per tile (exact) in the
+//               128-byte-swizzled layout the MMA reads, run the online
+//               softmax of key t against every query row (one tcgen05.ld of
+//               the key's N logits), write P^T, and in the epilogue read
+//               O^T (lane t = head-dim element t) and store the rows.
+// Per query row, the running max moves (and O and the sums are rescaled)
+// only when a tile's logits exceed it by more than 2^8; the per-row sums are
+// kept per key slot and reduced once per item in a fixed order, so a row's
+// arithmetic depends only on its own sequence and on its position, never on
+// the other rows of the call.
+//
+// Every mbarrier wait is bounded; a time-out sets RAD_ERRW_TIMEOUT and the
+// roles unwind (the workers only at a barrier all four reach), waiting
+// (bounded) for their copies and MMAs before TMEM is freed.
+#pragma once
+#include <cuda.h>
+
+#include "attn_tile.cuh"
+#include "tc05.cuh"
+
+#ifndef RAD_SPLITTC_NS
+#define RAD_SPLITTC_NS 3
+#endif
+
+namespace rad {
+
+template <int N_>
+struct SplitTcCfg {
+    static constexpr int D = 128;      // head dim
+    static constexpr int BK = 128;     // keys per tile: the MMA's M
+    static constexpr int N = N_;       // query rows per item: the MMA's N
+    static constexpr int QT = N;       // (item planner) query rows per tile
+    static constexpr int KS = BK;      // (item planner) keys per stage
+    static constexpr int NS = RAD_SPLITTC_NS;
+    static constexpr int ROW = 128;                  // bytes of one e4m3 key row
+    static constexpr int STG_TILE = BK * ROW;        // 16 KB: K or V of one tile
+    static constexpr int STG_BYTES = 2 * STG_TILE;
+    static constexpr int ATOM = BK * 128;            // f16 tile: stride between 64-column blocks
+    static constexpr int F16_TILE = 2 * ATOM;        // [column block 2][key 128][128 B]
+    static constexpr int QATOM = N * 128;
+    static constexpr int Q16_BYTES = 2 * QATOM;      // [column block 2][q N][128 B]
+    static constexpr int QSTG_BYTES = N * D * 2;     // bf16 query rows, one slot
+    static constexpr int PATOM = N * 128;
+    static constexpr int P_BYTES = 2 * PATOM;        // [key block 2][q N][128 B]
+    static constexpr int MAXPG = BK / 16;            // pages per tile
+    static constexpr int META_STRIDE = 128;          // ks[8], vs[8], bad
+    static constexpr int OFF_STG = 0;
+    static constexpr int OFF_K16 = OFF_STG + NS * STG_BYTES;
+    static constexpr int OFF_V16 = OFF_K16 + F16_TILE;
+    static constexpr int OFF_Q16 = OFF_V16 + F16_TILE;
+    static constexpr int OFF_P = OFF_Q16 + Q16_BYTES;
+    static constexpr int OFF_QSTG = OFF_P + 2 * P_BYTES;
+    static constexpr int OFF_META = OFF_QSTG + 2 * QSTG_BYTES;
+    static constexpr int OFF_RED = OFF_META + NS * META_STRIDE;    // [4][N] partials + [N] totals
+    static constexpr int OFF_BARS = OFF_RED + 5 * N * 4;
+    // stg_full[NS], stg_empty[NS], qstg_full[2], qstg_empty[2], q16_full,
+    // k16_full, v16_full, p_full[2], s_full[2], pv_done, o_free, final
+    static constexpr int NBARS = 2 * NS + 4 + 3 + 2 + 2 + 3;
+    static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;          // [0] tmem, [1] abort, [2] worker abort
+    static constexpr int SMEM_USED = OFF_MISC + 16;
+    static constexpr int SMEM_BYTES = SMEM_USED + 1024;   // 1 KB alignment of the swizzled operand tiles
+    static constexpr int NTHREADS = 7 * 32;
+    static constexpr int FULL_ARRIVALS = 64 + 1;          // 64 async lane arrivals + stage meta
+    static constexpr uint32_t TMEM_COLS = 3 * N <= 64 ? 64 : 128;   // S[2] and O
+    static_assert(N == 16 || N == 32, "query rows per item");
+    static_assert(OFF_K16 % 1024 == 0 && OFF_V16 % 1024 == 0 && OFF_Q16 % 1024 == 0 && OFF_P % 1024 == 0,
+                  "swizzled operand tiles on 1 KB boundaries");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+__device__ __forceinline__ void sts16(uint32_t a, float x) {
+    asm volatile("{\n\t.reg .b16 h;\n\tcvt.rn.f16.f32 h, %1;\n\tst.shared.b16 [%0], h;\n\t}" ::"r"(a), "f"(x)
+                 : "memory");
+}
+
+// Thread t converts key row t of a staged tile (128 e4m3 codes, 16-byte chunks
+// swizzled by t & 7) into 128 f16 values of an f16 tile [column block][key]
+// [128 B] with the same 128-byte swizzle; `zero` writes zeros instead.
+template <class C>
+__device__ __forceinline__ void convert_row(uint32_t src, uint32_t dst, int t, bool zero) {
+    const uint32_t sw = (uint32_t)(t & 7);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 v = zero ? make_uint4(0u, 0u, 0u, 0u) : lds128(src + t * 128 + ((c ^ sw) << 4));
+        const uint32_t h0 = e4m3x2_to_f16x2((uint16_t)(v.x & 0xFFFFu)), h1 = e4m3x2_to_f16x2((uint16_t)(v.x >> 16));
+        const uint32_t h2 = e4m3x2_to_f16x2((uint16_t)(v.y & 0xFFFFu)), h3 = e4m3x2_to_f16x2((uint16_t)(v.y >> 16));
+        const uint32_t h4 = e4m3x2_to_f16x2((uint16_t)(v.z & 0xFFFFu)), h5 = e4m3x2_to_f16x2((uint16_t)(v.z >> 16));
+        const uint32_t h6 = e4m3x2_to_f16x2((uint16_t)(v.w & 0xFFFFu)), h7 = e4m3x2_to_f16x2((uint16_t)(v.w >> 16));
+        // codes 16c .. 16c+15 -> f16 chunks 2c, 2c+1 of the row (8 values each)
+        const uint32_t row = dst + (c >> 2) * C::ATOM + t * 128;
+        const uint32_t ch = (uint32_t)((c & 3) * 2);
+        sts128(row + ((ch ^ sw) << 4), h0, h1, h2, h3);
+        sts128(row + (((ch + 1) ^ sw) << 4), h4, h5, h6, h7);
+    }
+}
+
+// Reduces v over the 32 lanes of the warp so that lane l returns the result
+// for column l & (N-1) (max or sum); the combination tree is fixed by lane
+// bits (16, 8, 4, 2, 1), whatever N.
+template <int N, bool MAX>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[N], int lane) {
+    if constexpr (N == 16) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const float o = __shfl_xor_sync(0xffffffffu, v[k], 16);
+            v[k] = MAX ? fmaxf(v[k], o) : v[k] + o;
+        }
+    }
+#pragma unroll
+    for (int o = N / 2; o >= 1; o >>= 1) {
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int k = 0; k < o; ++k) {
+            const float send = upper ? v[k] : v[k + o];
+            const float keep = upper ? v[k + o] : v[k];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, o);
+            v[k] = MAX ? fmaxf(keep, recv) : keep + recv;
+        }
+    }
+    return v[0];
+}
+
+// All four worker warps: totals of v over the 128 worker threads, per column,
+// into tot[N] of every thread (warp partials combined in warp order 0..3).
+template <int N, bool MAX>
+__device__ __forceinline__ void workers_reduce(float (&v)[N], float (&tot)[N], float* red, int warp, int lane,
+                                               int t) {
+    const float mine = warp_transpose_reduce<N, MAX>(v, lane);
+    if (lane < N) red[warp * N + lane] = mine;
+    named_barrier_sync(2, 128);
+    if (t < N) {
+        float a = red[t];
+#pragma unroll
+        for (int w = 1; w < 4; ++w) a = MAX ? fmaxf(a, red[w * N + t]) : a + red[w * N + t];
+        red[4 * N + t] = a;
+    }
+    named_barrier_sync(2, 128);
+#pragma unroll
+    for (int q = 0; q < N; q += 4) {
+        const uint4 f = lds128(smem_addr(red + 4 * N + q));
+        tot[q] = __uint_as_float(f.x);
+        tot[q + 1] = __uint_as_float(f.y);
+        tot[q + 2] = __uint_as_float(f.z);
+        tot[q + 3] = __uint_as_float(f.w);
+    }
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_ldN(uint32_t taddr, uint32_t (&r)[N]) {
+    if constexpr (N == 16) tmem_ld16(taddr, r);
+    else tmem_ld32(taddr, r);
+}
+template <int N>
+__device__ __forceinline__ void tmem_stN(uint32_t taddr, const uint32_t (&r)[N]) {
+    if constexpr (N == 16) tmem_st16(taddr, r);
+    else tmem_st32(taddr, r);
+}
+
+template <int N, bool WIN>
+__global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
+    attn_split_tc05_kernel(const __grid_constant__ AttnParams p) {
+    using C = SplitTcCfg<N>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (base - raw_addr);
+
+    const uint32_t bar_stg_full = base + C::OFF_BARS;
+    const uint32_t bar_stg_empty = bar_stg_full + 8 * C::NS;
+    const uint32_t bar_qstg_full = bar_stg_empty + 8 * C::NS;
+    const uint32_t bar_qstg_empty = bar_qstg_full + 16;
+    const uint32_t bar_q16_full = bar_qstg_empty + 16;
+    const uint32_t bar_k16_full = bar_q16_full + 8;
+    const uint32_t bar_v16_full = bar_k16_full + 8;
+    const uint32_t bar_p_full = bar_v16_full + 8;
+    const uint32_t bar_s_full = bar_p_full + 16;
+    const uint32_t bar_pv_done = bar_s_full + 16;
+    const uint32_t bar_o_free = bar_pv_done + 8;
+    const uint32_t bar_final = bar_o_free + 8;
+    volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::NS; ++i) {
+            mbar_init(bar_stg_full + 8 * i, C::FULL_ARRIVALS);
+            mbar_init(bar_stg_empty + 8 * i, 4);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_qstg_full + 8 * i, 1);
+            mbar_init(bar_qstg_empty + 8 * i, 4);
+            mbar_init(bar_p_full + 8 * i, 4);
+            mbar_init(bar_s_full + 8 * i, 1);
+        }
+        mbar_init(bar_q16_full, 4);
+        mbar_init(bar_k16_full, 4);
+        mbar_init(bar_v16_full, 4);
+        mbar_init(bar_pv_done, 1);
+        mbar_init(bar_o_free, 4);
+        mbar_init(bar_final, 1);
+        misc[1] = 0;
+        misc[2] = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 4) {
+        tmem_alloc(base + C::OFF_MISC, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    const uint32_t t_s = tmem;            // S buffer b: columns [b*N, b*N + N)
+    const uint32_t t_o = tmem + 2 * N;    // O^T: columns [2N, 3N)
+    bool abort = false;
+
+    if (warp >= 5) {
+        // ===================================================== producers
+        const int pw = warp - 5;   // 0: K rows, query rows and stage meta; 1: V rows
+        const uint8_t* pool = pw == 0 ? p.k_pool : p.v_pool;
+        const uint64_t pol_kv = policy_evict_first();
+        constexpr int RPI = 4;     // rows per warp-wide copy: 8 lanes x 16 B per 128-byte row
+        const int lrow = lane >> 3, lc = lane & 7;
+        uint32_t scount = 0, qcount = 0;
+        for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
+            const ItemPlan it = plan_item<C, WIN>(item, p);
+            if (!it.active || !it.seq_ok || it.n_stages == 0) continue;
+            if (pw == 0) {
+                const uint32_t slot = qcount & 1u, use = qcount >> 1;
+                if (use >= 1 && !mbar_wait_bounded(bar_qstg_empty + 8 * slot, (use - 1) & 1u, kWaitLimitNs)) {
+                    abort = true;
+                    break;
+                }
+                const int nrows = it.m_end - it.m0;
+                if (lane == 0) mbar_arrive_expect_tx(bar_qstg_full + 8 * slot, (uint32_t)(nrows * C::D * 2));
+                __syncwarp();
+                const uint32_t qdst = base + C::OFF_QSTG + slot * C::QSTG_BYTES;
+                for (int i = lane; i < nrows; i += 32) {
+                    const int m = it.m0 + i;
+                    const int r = m / p.ratio, hl = m - r * p.ratio;
+                    const __nv_bfloat16* src =
+                        p.q + (((long long)it.g * p.rows + r) * p.n_head + it.kvh * p.ratio + hl) * C::D;
+                    bulk_load(qdst + i * C::D * 2, src, C::D * 2, bar_qstg_full + 8 * slot);
+                }
+                ++qcount;
+            }
+            const int P = p.page_size;
+            const int page_hi = (it.k1 + P - 1) / P;
+            const int page_lo = WIN ? it.klo / P : 0;
+            const int32_t* trow = p.page_table + (long long)it.g * p.pages_per_seq;
+            const long long row_stride = (long long)p.n_head_kv * C::ROW;
+            const uint8_t* head_base = pool + (long long)it.kvh * C::ROW + (long long)lrow * row_stride + lc * 16;
+            int batch0 = -1 << 30;
+            int my_pg = 0;
+            float my_ks = 1.f, my_vs = 1.f;
+            bool my_bad = false;
+            for (int st = 0; st < it.n_stages; ++st) {
+                const int key0 = it.k0 + st * C::BK;
+                const int pstart = key0 / P;
+                const int npages = min(C::BK / P, page_hi - pstart);
+                if (pstart + npages > batch0 + 32) {
+                    batch0 = pstart;
+                    const int pi = batch0 + lane;
+                    my_bad = false;
+                    my_pg = 0;
+                    my_ks = my_vs = 1.f;
+                    if ((!WIN || pi >= page_lo) && pi < page_hi) {
+                        const int pg = __ldg(trow + pi);
+                        my_bad = (pg < 0 || pg >= p.num_pages);
+                        my_pg = my_bad ? 0 : pg;
+                        if (pw == 0) {
+                            my_ks = __ldg(p.k_scales + my_pg);
+                            my_vs = __ldg(p.v_scales + my_pg);
+                        }
+                    }
+                }
+                const uint32_t slot = scount % C::NS, use = scount / C::NS;
+                if (use >= 1 && !mbar_wait_bounded(bar_stg_empty + 8 * slot, (use - 1) & 1u, kWaitLimitNs)) {
+                    abort = true;
+                    break;
+                }
+                const uint32_t tile = base + C::OFF_STG + slot * C::STG_BYTES + pw * C::STG_TILE;
+                for (int i = 0; i < npages; ++i) {
+                    if (WIN && pstart + i < page_lo) continue;   // stale rows: masked in S, zeroed in V
+                    const int pg = __shfl_sync(0xffffffffu, my_pg, (pstart - batch0 + i) & 31);
+                    const uint8_t* src = head_base + (long long)pg * P * row_stride;
+                    const uint32_t dst = tile + (uint32_t)(i * P * 128);
+#pragma unroll 4
+                    for (int t0 = 0; t0 < P; t0 += RPI) {
+                        const int t = t0 + lrow;   // slot in the page; key i*P + t of the tile
+                        cp_async_16(dst + t * 128 + ((lc ^ (t & 7)) << 4), src + (long long)t0 * row_stride, pol_kv);
+                    }
+                }
+                cp_async_arrive_noinc(bar_stg_full + 8 * slot);
+                if (pw == 0) {
+                    uint32_t bad_any = 0;
+                    float kss[C::MAXPG], vss[C::MAXPG];
+#pragma unroll
+                    for (int i = 0; i < C::MAXPG; ++i) {
+                        const int src = (pstart - batch0 + i) & 31;
+                        kss[i] = __shfl_sync(0xffffffffu, my_ks, src);
+                        vss[i] = __shfl_sync(0xffffffffu, my_vs, src);
+                        const uint32_t b = __shfl_sync(0xffffffffu, (uint32_t)my_bad, src);
+                        if (i < npages) bad_any |= b;
+                    }
+                    if (lane == 0) {
+                        float* meta = reinterpret_cast<float*>(smem + C::OFF_META + slot * C::META_STRIDE);
+#pragma unroll
+                        for (int i = 0; i < C::MAXPG; ++i) {
+                            meta[i] = kss[i];
+                            meta[8 + i] = vss[i];
+                        }
+                        reinterpret_cast<uint32_t*>(meta)[16] = bad_any;
+                        mbar_arrive(bar_stg_full + 8 * slot);
+                    }
+                }
+                ++scount;
+            }
+            if (misc[1]) abort = true;
+        }
+        cp_async_wait_all();
+        if (pw == 0 && lane == 0) {
+            const uint32_t qfirst = qcount > 2u ? qcount - 2u : 0u;
+            for (uint32_t c = qfirst; c < qcount; ++c)
+                mbar_wait_bounded(bar_qstg_full + 8 * (c & 1u), (c >> 1) & 1u, kWaitLimitNs);
+        }
+    } else if (warp == 4) {
+        // ===================================================== MMA issue
+        constexpr uint32_t idesc_qk = umma_idesc_f16(128, N, 0, 0);   // A = K (K-major), B = Q (K-major)
+        constexpr uint32_t idesc_pv = umma_idesc_f16(128, N, 1, 0);   // A = V^T (MN-major), B = P^T (K-major)
+        const uint32_t k16 = base + C::OFF_K16, v16 = base + C::OFF_V16, q16 = base + C::OFF_Q16;
+        uint32_t tcnt = 0, kcnt = 0, vcnt = 0, icnt = 0;
+        bool issued = false;
+        for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
+            const ItemPlan it = plan_item<C, WIN>(item, p);
+            if (!it.active || !it.seq_ok || it.n_stages == 0) continue;
+            const int T = it.n_stages;
+            if (!mbar_wait_bounded(bar_q16_full, icnt & 1u, kWaitLimitNs)) {
+                abort = true;
+                break;
+            }
+            for (int j = 0; j <= T && !abort; ++j) {
+                if (j < T) {
+                    if (!mbar_wait_bounded(bar_k16_full, kcnt & 1u, kWaitLimitNs)) {
+                        abort = true;
+                        break;
+                    }
+                    ++kcnt;
+                    tc_fence_after();
+                    const uint32_t b = (tcnt + j) & 1u;
+                    if (lane == 0) {
+#pragma unroll
+                        for (int kk = 0; kk < C::D / 16; ++kk) {
+                            const uint32_t off = (kk >> 2) * C::ATOM + (kk & 3) * 32;
+                            const uint32_t qoff = (kk >> 2) * C::QATOM + (kk & 3) * 32;
+                            tc_mma_ss(t_s + N * b, umma_desc_sw128(k16 + off, 16, 1024),
+                                      umma_desc_sw128(q16 + qoff, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                        }
+                        tc_commit(bar_s_full + 8 * b);
+                        issued = true;
+                    }
+                    __syncwarp();
+                }
+                if (j >= 1) {
+                    const int jj = j - 1;
+                    const uint32_t tt = tcnt + jj, b = tt & 1u;
+                    if (!mbar_wait_bounded(bar_p_full + 8 * b, (tt >> 1) & 1u, kWaitLimitNs) ||
+                        !mbar_wait_bounded(bar_v16_full, vcnt & 1u, kWaitLimitNs) ||
+                        (jj == 0 && icnt >= 1 && !mbar_wait_bounded(bar_o_free, (icnt - 1) & 1u, kWaitLimitNs))) {
+                        abort = true;
+                        break;
+                    }
+                    ++vcnt;
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t pt = base + C::OFF_P + b * C::P_BYTES;
+#pragma unroll
+                        for (int kk = 0; kk < C::BK / 16; ++kk) {
+                            const uint64_t ad = umma_desc_sw128(v16 + kk * 16 * 128, C::ATOM, 1024);
+                            const uint64_t bd = umma_desc_sw128(pt + (kk >> 2) * C::PATOM + (kk & 3) * 32, 16, 1024);
+                            tc_mma_ss(t_o, ad, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        tc_commit(bar_pv_done);
+                    }
+                    __syncwarp();
+                }
+            }
+            tcnt += T;
+            ++icnt;
+            if (misc[1]) abort = true;
+        }
+        // every MMA this thread issued is complete before TMEM is released
+        if (lane == 0 && issued) {
+            tc_commit(bar_final);
+            mbar_wait_bounded(bar_final, 0, kWaitLimitNs);
+        }
+        __syncwarp();
+    } else {
+        // ===================================================== workers (warps 0-3)
+        const int t = threadIdx.x;                                   // key slot / TMEM lane / head-dim element
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const uint32_t k16 = base + C::OFF_K16, v16 = base + C::OFF_V16, q16 = base + C::OFF_Q16;
+        float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
+        // P^T store offsets of key slot t for the 8 swizzle phases of a row q
+        uint32_t poff[8];
+#pragma unroll
+        for (int qq = 0; qq < 8; ++qq)
+            poff[qq] = (uint32_t)((t >> 6) * C::PATOM + ((((t & 63) >> 3) ^ qq) << 4) + (t & 7) * 2);
+        uint32_t scount = 0, qcount = 0, tcnt = 0;
+        // A time-out seen by this thread; published to the other workers at the
+        // next barrier they all reach, where all four warps leave together.
+        bool lab = false;
+        for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
+            const ItemPlan it = plan_item<C, WIN>(item, p);
+            if (!it.active) continue;
+            if (!it.seq_ok) {
+                for (int idx = t; idx < (it.m_end - it.m0) * C::D; idx += 128) {
+                    const int m = it.m0 + idx / C::D, d = idx % C::D;
+                    const int r = m / p.ratio, hl = m - r * p.ratio;
+                    p.out[(((long long)it.g * p.rows + r) * p.n_head + it.kvh * p.ratio + hl) * C::D + d] =
+                        __float2bfloat16_rn(0.f);
+                }
+                if (t == 0 && p.err_word) atomicOr(p.err_word, kErrSeqLen);
+                continue;
+            }
+            const int T = it.n_stages;
+            const int nrows = it.m_end - it.m0;
+            if (T == 0) {
+                // A later split none of whose keys this query tile's rows see
+                // (never the tile's first split): an empty partial.
+                const long long gq = ((long long)it.g * p.n_head_kv + it.kvh) * p.n_qtiles + it.qt;
+                const long long slot_idx = gq * p.max_splits + it.s;
+                float* pacc = p.part_acc + slot_idx * p.qtv * C::D;
+                float* pml = p.part_ml + slot_idx * p.qtv * 2;
+                for (int q = 0; q < nrows; ++q) __stcg(pacc + q * C::D + t, 0.f);
+                if (t < nrows) __stcg(reinterpret_cast<float2*>(pml) + t, make_float2(-CUDART_INF_F, 0.f));
+                if (t == 0) __stcg(p.part_flag + slot_idx, 0u);
+                continue;
+            }
+            uint32_t bad = 0;
+            // pages the group needs that no item of this query tile loads
+            if (it.s == it.s_first) {
+                const int P_ = p.page_size;
+                const int glo = WIN ? first_visible_key(it.L, p.rows, 0, p.window) / P_ : 0;
+                const int tlo = it.klo / P_, thi = (it.kmax + P_ - 1) / P_, ghi = (it.L + P_ - 1) / P_;
+                const int32_t* trow = p.page_table + (long long)it.g * p.pages_per_seq;
+                const int n_below = tlo - glo;
+                for (int i = t; i < n_below + (ghi - thi); i += 128) {
+                    const int pi = i < n_below ? glo + i : thi + (i - n_below);
+                    const int pg = __ldg(trow + pi);
+                    bad |= (pg < 0 || pg >= p.num_pages) ? 1u : 0u;
+                }
+            }
+            // ---- query rows: bf16 -> f16 (exact inside the f16 range) into the B operand tile
+            {
+                const uint32_t slot = qcount & 1u, use = qcount >> 1;
+                if (!mbar_wait_bounded(bar_qstg_full + 8 * slot, use & 1u, kWaitLimitNs)) lab = true;
+                const uint32_t qs = base + C::OFF_QSTG + slot * C::QSTG_BYTES;
+                bool qbad = false;
+                for (int i = t; i < N * 16; i += 128) {
+                    const int row = i >> 4, ch = i & 15;   // ch: 8 head-dim elements
+                    uint32_t w[4] = {0u, 0u, 0u, 0u};
+                    if (row < nrows && !lab) {
+                        const uint4 v = lds128(qs + row * (C::D * 2) + ch * 16);
+                        const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float f0 = bf16_lo(x[e]), f1 = bf16_hi(x[e]);
+                            qbad |= fabsf(f0) > 65504.f || fabsf(f1) > 65504.f;
+                            w[e] = pack_f16x2(f0, f1);
+                        }
+                    }
+                    const uint32_t dst = q16 + (ch >> 3) * C::QATOM + row * 128 + ((((uint32_t)ch & 7u) ^ (row & 7)) << 4);
+                    sts128(dst, w[0], w[1], w[2], w[3]);
+                }
+                if (qbad && p.err_word) atomicOr(p.err_word, kErrQRange);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar_q16_full);
+                    mbar_arrive(bar_qstg_empty + 8 * slot);
+                }
+                ++qcount;
+            }
+            // ---- per query row state (identical in every worker thread)
+            float mu[N], thr[N], lsum[N];
+#pragma unroll
+            for (int q = 0; q < N; ++q) {
+                mu[q] = 0.f;                 // running max in log2 units (0 while no key was seen)
+                thr[q] = -CUDART_INF_F;      // logits above this move the max
+                lsum[q] = 0.f;               // this key slot's share of the row sum
+            }
+            const int nk0 = it.L - p.rows + it.m0 / p.ratio + 1;                    // keys row q=0 sees
+            const int klo_last = WIN ? first_visible_key(it.L, p.rows, (it.m_end - 1) / p.ratio, p.window) : 0;
+            // ---- prologue: tile 0's K and V rows to f16, and key t's page scales
+            // (read before the stage goes back to the producers)
+            float kc_cur, vs_cur, kc_nxt = 0.f, vs_nxt = 0.f;
+            {
+                const uint32_t slot = scount % C::NS, use = scount / C::NS;
+                if (!lab && !mbar_wait_bounded(bar_stg_full + 8 * slot, use & 1u, kWaitLimitNs)) lab = true;
+                const uint32_t stg = base + C::OFF_STG + slot * C::STG_BYTES;
+                const int key = it.k0 + t;
+                convert_row<C>(stg, k16, t, lab);
+                convert_row<C>(stg + C::STG_TILE, v16, t, lab || key < it.klo || key >= it.k1);
+                const float* meta = reinterpret_cast<const float*>(smem + C::OFF_META + slot * C::META_STRIDE);
+                kc_cur = p.scale_log2 * meta[t / p.page_size];
+                vs_cur = meta[8 + t / p.page_size];
+                bad |= reinterpret_cast<const uint32_t*>(meta)[16];
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar_k16_full);
+                    mbar_arrive(bar_v16_full);
+                    mbar_arrive(bar_stg_empty + 8 * slot);
+                }
+            }
+            for (int j = 0; j < T; ++j) {
+                const uint32_t tt = tcnt + j, b = tt & 1u;
+                const int kbase = it.k0 + j * C::BK;
+                // S(j) = QK(j) done: the K f16 tile is free again
+                if (!lab && !mbar_wait_bounded(bar_s_full + 8 * b, (tt >> 1) & 1u, kWaitLimitNs)) lab = true;
+                tc_fence_after();
+                if (j + 1 < T) {
+                    const uint32_t s1 = (scount + j + 1) % C::NS, u1 = (scount + j + 1) / C::NS;
+                    if (!lab && !mbar_wait_bounded(bar_stg_full + 8 * s1, u1 & 1u, kWaitLimitNs)) lab = true;
+                    convert_row<C>(base + C::OFF_STG + s1 * C::STG_BYTES, k16, t, lab);
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_k16_full);
+                }
+                // ---- softmax of key kbase + t against the N query rows
+                uint32_t sv[N];
+                tmem_ldN<N>(t_s + N * b + lane_off, sv);
+                const float c_t = kc_cur, vs_t = vs_cur;
+                float xs[N];
+                const bool full = kbase + C::BK <= it.k1 && kbase + C::BK <= nk0 && kbase >= klo_last;
+                if (full) {
+#pragma unroll
+                    for (int q = 0; q < N; ++q) xs[q] = __uint_as_float(sv[q]) * c_t;
+                } else {
+                    // key k is visible to row q (query row m0+q at position L-R+(m0+q)/ratio)
+                    // iff qc <= q < qw; thresholds clamped to [-1, N]
+                    const int key = kbase + t;
+                    const long long dk = (long long)key - (it.L - p.rows + 1);
+                    long long qc = (dk + 1) * p.ratio - it.m0;
+                    long long qw = WIN ? (dk + p.window + 1) * p.ratio - it.m0 : (long long)N;
+                    qc = qc < -1 ? -1 : (qc > N ? N : qc);
+                    qw = qw < -1 ? -1 : (qw > N ? N : qw);
+                    const bool in_item = key >= it.klo && key < it.k1;
+                    const int qci = in_item ? (int)qc : N, qwi = (int)qw;
+#pragma unroll
+                    for (int q = 0; q < N; ++q)
+                        xs[q] = (q >= qci && q < qwi) ? __uint_as_float(sv[q]) * c_t : -CUDART_INF_F;
+                }
+                bool trig = false;
+#pragma unroll
+                for (int q = 0; q < N; ++q) trig |= xs[q] > thr[q];
+                if (lab) misc[2] = 1u;
+                const bool any_trig = named_barrier_or(2, 128, trig);
+                if (misc[2]) {
+                    abort = true;
+                    break;
+                }
+                if (any_trig) {
+                    // tile max per row; a row's max moves only past 2^8 (or on its first keys)
+                    float v[N], mx[N];
+#pragma unroll
+                    for (int q = 0; q < N; ++q) v[q] = xs[q];
+                    workers_reduce<N, true>(v, mx, red, warp, lane, t);
+                    float alpha[N];
+                    bool moved_any = false;
+#pragma unroll
+                    for (int q = 0; q < N; ++q) {
+                        const bool first = thr[q] == -CUDART_INF_F;
+                        const bool mv = first ? mx[q] != -CUDART_INF_F : mx[q] > thr[q];
+                        alpha[q] = 1.f;
+                        if (mv) {
+                            alpha[q] = first ? 0.f : exp2f(mu[q] - mx[q]);
+                            mu[q] = mx[q];
+                            thr[q] = mx[q] + kLazyRescaleLog2;
+                            lsum[q] *= alpha[q];
+                            moved_any = true;
+                        }
+                    }
+                    if (moved_any && j > 0) {
+                        // O holds PV(0 .. j-1), complete (waited below in tile j-1)
+                        uint32_t ov[N];
+                        tmem_ldN<N>(t_o + lane_off, ov);
+#pragma unroll
+                        for (int q = 0; q < N; ++q) ov[q] = __float_as_uint(__uint_as_float(ov[q]) * alpha[q]);
+                        tmem_stN<N>(t_o + lane_off, ov);
+                        tmem_wait_st();
+                    }
+                }
+                // ---- P^T[key][q] = f16(2^(x - max) * V scale), sums without the V scale
+                const uint32_t pt = base + C::OFF_P + b * C::P_BYTES;
+#pragma unroll
+                for (int q = 0; q < N; ++q) {
+                    const float pr = exp2f(xs[q] - mu[q]);
+                    lsum[q] += pr;
+                    sts16(pt + poff[q & 7] + q * 128, pr * vs_t);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_p_full + 8 * b);
+                // ---- PV(j) done: V f16 tile and O free; convert tile j+1's V rows
+                if (!lab && !mbar_wait_bounded(bar_pv_done, tt & 1u, kWaitLimitNs)) lab = true;
+                tc_fence_after();
+                if (j + 1 < T) {
+                    const uint32_t s1 = (scount + j + 1) % C::NS;
+                    const int key = kbase + C::BK + t;
+                    convert_row<C>(base + C::OFF_STG + s1 * C::STG_BYTES + C::STG_TILE, v16, t,
+                                   lab || key < it.klo || key >= it.k1);
+                    const float* meta = reinterpret_cast<const float*>(smem + C::OFF_META + s1 * C::META_STRIDE);
+                    kc_nxt = p.scale_log2 * meta[t / p.page_size];
+                    vs_nxt = meta[8 + t / p.page_size];
+                    bad |= reinterpret_cast<const uint32_t*>(meta)[16];
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(bar_v16_full);
+                        mbar_arrive(bar_stg_empty + 8 * s1);
+                    }
+                }
+                kc_cur = kc_nxt;
+                vs_cur = vs_nxt;
+            }
+            if (abort) break;
+            scount += T;
+            tcnt += T;
+            // ---- epilogue: row sums over the 128 key slots, O^T (lane t = head-dim element t)
+            float ltot[N];
+            workers_reduce<N, false>(lsum, ltot, red, warp, lane, t);
+            if (lab) misc[2] = 1u;
+            const bool item_bad = named_barrier_or(2, 128, bad != 0);
+            if (misc[2]) {
+                abort = true;
+                break;
+            }
+            uint32_t ov[N];
+            tmem_ldN<N>(t_o + lane_off, ov);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_o_free);
+            const bool final_write = it.n_splits - it.s_first == 1;
+            if (final_write) {
+                int r = it.m0 / p.ratio, hl = it.m0 - r * p.ratio;
+#pragma unroll
+                for (int q = 0; q < N; ++q) {
+                    if (q < nrows) {
+                        // acc * (1/l), the combine kernel's form
+                        const float o = item_bad ? 0.f : __uint_as_float(ov[q]) * (1.f / ltot[q]);
+                        p.out[(((long long)it.g * p.rows + r) * p.n_head + it.kvh * p.ratio + hl) * C::D + t] =
+                            __float2bfloat16_rn(o);
+                    }
+                    if (++hl == p.ratio) {
+                        hl = 0;
+                        ++r;
+                    }
+                }
+                if (item_bad && t == 0 && p.err_word) atomicOr(p.err_word, kErrPage);
+            } else {
+                const long long gq = ((long long)it.g * p.n_head_kv + it.kvh) * p.n_qtiles + it.qt;
+                const long long slot_idx = gq * p.max_splits + it.s;
+                float* pacc = p.part_acc + slot_idx * p.qtv * C::D;
+                float* pml = p.part_ml + slot_idx * p.qtv * 2;
+#pragma unroll
+                for (int q = 0; q < N; ++q) {
+                    if (q < nrows) {
+                        __stcg(pacc + q * C::D + t, __uint_as_float(ov[q]));
+                        if (t == q)
+                            __stcg(reinterpret_cast<float2*>(pml) + q,
+                                   make_float2(ltot[q] == 0.f ? -CUDART_INF_F : mu[q], ltot[q]));
+                    }
+                }
+                if (t == 0) __stcg(p.part_flag + slot_idx, item_bad ? 1u : 0u);
+            }
+        }
+    }
+    if (abort) {
+        misc[1] = 1;
+        if (lane == 0 && p.err_word) atomicOr(p.err_word, kErrTimeout);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 4) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+}  // namespace rad

@@ -6,7 +6,17 @@
 
 namespace rad {
 
-enum Family : int { kFamDecode = 0, kFamVerify = 1, kFamWide = 2, kFamPrefillTC = 3 };
+enum Family : int { kFamDecode = 0, kFamVerify = 1, kFamWide = 2, kFamPrefillTC = 3, kFamSplitTC = 4 };
+
+// Split calls (decode and verify shapes) with head_dim 128 and fp8 pools run
+// on the tcgen05 split kernel (split_tc05.cuh); 0 keeps them on the mma.sync
+// tile kernel.
+#ifndef RAD_SPLIT_TC05
+#define RAD_SPLIT_TC05 1
+#endif
+// Query rows per item of the tcgen05 split kernel for a call with M query
+// rows per KV head: 16 or 32 (the MMA's N).
+inline int split_tc05_rows(int M) { return M <= 16 ? 16 : 32; }
 
 // Keys per split for calls of up to kSplitMaxRows rows; longer calls (prefill
 // chunks) run one range per query tile.  A multiple of every tile's KS.
@@ -121,5 +131,7 @@ cudaError_t launch_d256_bf16(int family, const AttnParams& p, int sms, cudaStrea
 cudaError_t launch_d256_fp8(int family, const AttnParams& p, int sms, cudaStream_t st);
 cudaError_t launch_prefill_tc05(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const AttnParams& p, int sms, cudaStream_t st);
+cudaError_t launch_split_tc05(const AttnParams& p, int sms, cudaStream_t st);
+TileInfo split_tc05_info(int n);
 
 }  // namespace rad

@@ -93,7 +93,11 @@ def test_workspace_sizes():
 
 def test_describe_names_the_kernel_choice():
     assert "family=decode" in b.describe(1, 32, 8, 128, 16)
-    assert "family=verify" in b.describe(8, 32, 8, 128, 16, b.RAD_KV_FP8_E4M3)
+    assert "family=verify" in b.describe(8, 32, 8, 128, 16)
+    assert "family=verify" in b.describe(8, 16, 2, 256, 32, b.RAD_KV_FP8_E4M3)
+    # fp8 pools with head_dim 128: decode and verify shapes share the tcgen05 split kernel
+    assert "family=split_tc05" in b.describe(8, 32, 8, 128, 16, b.RAD_KV_FP8_E4M3)
+    assert "family=split_tc05" in b.describe(1, 8, 8, 128, 16, b.RAD_KV_FP8_E4M3)
     assert "split_len=0" in b.describe(2048, 32, 8, 128, 16)
     with pytest.raises(b.RadAttnError):
         b.describe(1, 32, 8, 96, 16)
