@@ -13,18 +13,20 @@
 //   O^T[d][q]  += V^T[d][key] . P^T[key][q]   M = head_dim 128, N, K = 128 keys
 // so a decode step's few query rows per KV head cost a narrow N instead of
 // an idle M.  Warp roles (one CTA per SM, persistent):
-//   warps 5, 6  producers: page ids from the page table ("kern manifest v7",
+//   warps 9, 10 producers: page ids from the page table ("kern manifest v7",
 //               $defs.Domain), 16-byte cp.async copies of each tile's e4m3 K
-//               rows (warp 5) and V rows (warp 6) into a staging ring, the
-//               per-page scales, and a 1-D bulk copy of the query rows.
-//   warp 4      MMA: one lane issues tcgen05.mma.kind::f16 from shared-memory
+//               rows (warp 9) and V rows (warp 10) into two staging rings,
+//               the per-page scales, and a 1-D bulk copy of the query rows.
+//   warp 8      MMA: one lane issues tcgen05.mma.kind::f16 from shared-memory
 //               operands into TMEM and commits to mbarriers.
-//   warps 0-3   workers, thread t <-> key t of the tile <-> TMEM lane t:
-//               convert staged e4m3 rows to f16 once per tile (exact) in the
+//   warps 0-7   workers; thread t serves key slot k = t % 128 (TMEM lane k)
+//               and half h = t / 128 of the query rows (warps w and w+4 share
+//               TMEM lanes 32(w%4)..): convert its half of key row k of the
+//               staged e4m3 tiles to f16 once per tile (exact) in the
 //               128-byte-swizzled layout the MMA reads, run the online
-//               softmax of key t against every query row (one tcgen05.ld of
-//               the key's N logits), write P^T, and in the epilogue read
-//               O^T (lane t = head-dim element t) and store the rows.
+//               softmax of key k against its half of the query rows, write
+//               P^T, and in the epilogue read O^T (lane k = head-dim element
+//               k) and store its rows.
 // Per query row, the running max moves (and O and the sums are rescaled)
 // only when a tile's logits exceed it by more than 2^8; the per-row sums are
 // kept per key slot and reduced once per item in a fixed order, so a row's
@@ -51,6 +53,7 @@ struct SplitTcCfg {
     static constexpr int D = 128;      // head dim
     static constexpr int BK = 128;     // keys per tile: the MMA's M
     static constexpr int N = N_;       // query rows per item: the MMA's N
+    static constexpr int HALF = N / 2; // query rows per worker thread
     static constexpr int QT = N;       // (item planner) query rows per tile
     static constexpr int KS = BK;      // (item planner) keys per stage
     static constexpr int NS = RAD_SPLITTC_NS;
@@ -66,23 +69,27 @@ struct SplitTcCfg {
     static constexpr int P_BYTES = 2 * PATOM;        // [key block 2][q N][128 B]
     static constexpr int MAXPG = BK / 16;            // pages per tile
     static constexpr int META_STRIDE = 128;          // ks[8], vs[8], bad
-    static constexpr int OFF_STG = 0;
+    // K and V staging rings (NS stages each), one f16 K tile, two f16 V tiles
+    static constexpr int OFF_STG = 0;            // stage i: K at i*STG_BYTES, V at +STG_TILE
     static constexpr int OFF_K16 = OFF_STG + NS * STG_BYTES;
-    static constexpr int OFF_V16 = OFF_K16 + F16_TILE;
-    static constexpr int OFF_Q16 = OFF_V16 + F16_TILE;
+    static constexpr int OFF_V16 = OFF_K16 + F16_TILE;          // two buffers
+    static constexpr int OFF_Q16 = OFF_V16 + 2 * F16_TILE;
     static constexpr int OFF_P = OFF_Q16 + Q16_BYTES;
-    static constexpr int OFF_QSTG = OFF_P + 2 * P_BYTES;
-    static constexpr int OFF_META = OFF_QSTG + 2 * QSTG_BYTES;
+    static constexpr int OFF_QSTG = OFF_P + 2 * P_BYTES;        // one slot
+    static constexpr int OFF_META = OFF_QSTG + QSTG_BYTES;
     static constexpr int OFF_RED = OFF_META + NS * META_STRIDE;    // [4][N] partials + [N] totals
-    static constexpr int OFF_BARS = OFF_RED + 5 * N * 4;
-    // stg_full[NS], stg_empty[NS], qstg_full[2], qstg_empty[2], q16_full,
-    // k16_full, v16_full, p_full[2], s_full[2], pv_done, o_free, final
-    static constexpr int NBARS = 2 * NS + 4 + 3 + 2 + 2 + 3;
+    static constexpr int OFF_BARS = OFF_RED + 5 * N * 4;   // [2][4][HALF] partials + [2][HALF] totals
+    // k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], qstg_full, qstg_empty,
+    // q16_full, k16_full, v16_full[2], p_full[2], s_full[2], pv_done[2], o_free, final
+    static constexpr int NBARS = 4 * NS + 2 + 2 + 2 + 2 + 2 + 2 + 2;
     static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;          // [0] tmem, [1] abort, [2] worker abort
     static constexpr int SMEM_USED = OFF_MISC + 16;
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;   // 1 KB alignment of the swizzled operand tiles
-    static constexpr int NTHREADS = 7 * 32;
-    static constexpr int FULL_ARRIVALS = 64 + 1;          // 64 async lane arrivals + stage meta
+    static constexpr int NWORK = 8;                      // worker warps
+    static constexpr int W_MMA = 8, W_PROD = 9;
+    static constexpr int NTHREADS = 11 * 32;
+    static constexpr int K_ARRIVALS = 32 + 1;             // 32 async lane arrivals + stage meta
+    static constexpr int V_ARRIVALS = 32;
     static constexpr uint32_t TMEM_COLS = 3 * N <= 64 ? 64 : 128;   // S[2] and O
     static_assert(N == 16 || N == 32, "query rows per item");
     static_assert(OFF_K16 % 1024 == 0 && OFF_V16 % 1024 == 0 && OFF_Q16 % 1024 == 0 && OFF_P % 1024 == 0,
@@ -103,14 +110,16 @@ __device__ __forceinline__ void sts16(uint32_t a, float x) {
                  : "memory");
 }
 
-// Thread t converts key row t of a staged tile (128 e4m3 codes, 16-byte chunks
-// swizzled by t & 7) into 128 f16 values of an f16 tile [column block][key]
-// [128 B] with the same 128-byte swizzle; `zero` writes zeros instead.
+// Converts half h of key row t of a staged tile (128 e4m3 codes, 16-byte
+// chunks swizzled by t & 7): codes 64h .. 64h+63 become column block h of an
+// f16 tile [column block][key][128 B] with the same 128-byte swizzle; `zero`
+// writes zeros instead.
 template <class C>
-__device__ __forceinline__ void convert_row(uint32_t src, uint32_t dst, int t, bool zero) {
+__device__ __forceinline__ void convert_half_row(uint32_t src, uint32_t dst, int t, int h, bool zero) {
     const uint32_t sw = (uint32_t)(t & 7);
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
+    for (int cc = 0; cc < 4; ++cc) {
+        const int c = 4 * h + cc;
         const uint4 v = zero ? make_uint4(0u, 0u, 0u, 0u) : lds128(src + t * 128 + ((c ^ sw) << 4));
         const uint32_t h0 = e4m3x2_to_f16x2((uint16_t)(v.x & 0xFFFFu)), h1 = e4m3x2_to_f16x2((uint16_t)(v.x >> 16));
         const uint32_t h2 = e4m3x2_to_f16x2((uint16_t)(v.y & 0xFFFFu)), h3 = e4m3x2_to_f16x2((uint16_t)(v.y >> 16));
@@ -125,19 +134,20 @@ __device__ __forceinline__ void convert_row(uint32_t src, uint32_t dst, int t, b
 }
 
 // Reduces v over the 32 lanes of the warp so that lane l returns the result
-// for column l & (N-1) (max or sum); the combination tree is fixed by lane
-// bits (16, 8, 4, 2, 1), whatever N.
-template <int N, bool MAX>
-__device__ __forceinline__ float warp_transpose_reduce(float (&v)[N], int lane) {
-    if constexpr (N == 16) {
+// for column l & (V-1) (max or sum); the combination tree is fixed by lane
+// bits (16, 8, 4, 2, 1), whatever V.
+template <int V, bool MAX>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[V], int lane) {
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const float o = __shfl_xor_sync(0xffffffffu, v[k], 16);
-            v[k] = MAX ? fmaxf(v[k], o) : v[k] + o;
+    for (int o = 16; o >= V; o >>= 1) {
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const float x = __shfl_xor_sync(0xffffffffu, v[k], o);
+            v[k] = MAX ? fmaxf(v[k], x) : v[k] + x;
         }
     }
 #pragma unroll
-    for (int o = N / 2; o >= 1; o >>= 1) {
+    for (int o = V / 2; o >= 1; o >>= 1) {
         const bool upper = (lane & o) != 0;
 #pragma unroll
         for (int k = 0; k < o; ++k) {
@@ -150,24 +160,25 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[N], int lane) 
     return v[0];
 }
 
-// All four worker warps: totals of v over the 128 worker threads, per column,
-// into tot[N] of every thread (warp partials combined in warp order 0..3).
-template <int N, bool MAX>
-__device__ __forceinline__ void workers_reduce(float (&v)[N], float (&tot)[N], float* red, int warp, int lane,
-                                               int t) {
-    const float mine = warp_transpose_reduce<N, MAX>(v, lane);
-    if (lane < N) red[warp * N + lane] = mine;
-    named_barrier_sync(2, 128);
-    if (t < N) {
-        float a = red[t];
+// All eight worker warps: for each half h of the query rows, totals of v over
+// the 128 key slots, per row, into tot[V] of every thread of that half (the
+// partials of the four warps of a half combined in warp order).
+template <int V, bool MAX>
+__device__ __forceinline__ void workers_reduce(float (&v)[V], float (&tot)[V], float* red, int wq, int h, int lane,
+                                               int k) {
+    const float mine = warp_transpose_reduce<V, MAX>(v, lane);
+    if (lane < V) red[(h * 4 + wq) * V + lane] = mine;
+    named_barrier_sync(2, 256);
+    if (k < V) {
+        float a = red[(h * 4) * V + k];
 #pragma unroll
-        for (int w = 1; w < 4; ++w) a = MAX ? fmaxf(a, red[w * N + t]) : a + red[w * N + t];
-        red[4 * N + t] = a;
+        for (int w = 1; w < 4; ++w) a = MAX ? fmaxf(a, red[(h * 4 + w) * V + k]) : a + red[(h * 4 + w) * V + k];
+        red[8 * V + h * V + k] = a;
     }
-    named_barrier_sync(2, 128);
+    named_barrier_sync(2, 256);
 #pragma unroll
-    for (int q = 0; q < N; q += 4) {
-        const uint4 f = lds128(smem_addr(red + 4 * N + q));
+    for (int q = 0; q < V; q += 4) {
+        const uint4 f = lds128(smem_addr(red + 8 * V + h * V + q));
         tot[q] = __uint_as_float(f.x);
         tot[q + 1] = __uint_as_float(f.y);
         tot[q + 2] = __uint_as_float(f.z);
@@ -175,15 +186,15 @@ __device__ __forceinline__ void workers_reduce(float (&v)[N], float (&tot)[N], f
     }
 }
 
-template <int N>
-__device__ __forceinline__ void tmem_ldN(uint32_t taddr, uint32_t (&r)[N]) {
-    if constexpr (N == 16) tmem_ld16(taddr, r);
-    else tmem_ld32(taddr, r);
+template <int V>
+__device__ __forceinline__ void tmem_ldV(uint32_t taddr, uint32_t (&r)[V]) {
+    if constexpr (V == 8) tmem_ld8(taddr, r);
+    else tmem_ld16(taddr, r);
 }
-template <int N>
-__device__ __forceinline__ void tmem_stN(uint32_t taddr, const uint32_t (&r)[N]) {
-    if constexpr (N == 16) tmem_st16(taddr, r);
-    else tmem_st32(taddr, r);
+template <int V>
+__device__ __forceinline__ void tmem_stV(uint32_t taddr, const uint32_t (&r)[V]) {
+    if constexpr (V == 8) tmem_st8(taddr, r);
+    else tmem_st16(taddr, r);
 }
 
 template <int N, bool WIN>
@@ -195,17 +206,19 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
     uint8_t* smem = smem_raw + (base - raw_addr);
 
-    const uint32_t bar_stg_full = base + C::OFF_BARS;
-    const uint32_t bar_stg_empty = bar_stg_full + 8 * C::NS;
-    const uint32_t bar_qstg_full = bar_stg_empty + 8 * C::NS;
-    const uint32_t bar_qstg_empty = bar_qstg_full + 16;
-    const uint32_t bar_q16_full = bar_qstg_empty + 16;
+    const uint32_t bar_k_full = base + C::OFF_BARS;
+    const uint32_t bar_k_empty = bar_k_full + 8 * C::NS;
+    const uint32_t bar_v_full = bar_k_empty + 8 * C::NS;
+    const uint32_t bar_v_empty = bar_v_full + 8 * C::NS;
+    const uint32_t bar_qstg_full = bar_v_empty + 8 * C::NS;
+    const uint32_t bar_qstg_empty = bar_qstg_full + 8;
+    const uint32_t bar_q16_full = bar_qstg_empty + 8;
     const uint32_t bar_k16_full = bar_q16_full + 8;
-    const uint32_t bar_v16_full = bar_k16_full + 8;
-    const uint32_t bar_p_full = bar_v16_full + 8;
-    const uint32_t bar_s_full = bar_p_full + 16;
-    const uint32_t bar_pv_done = bar_s_full + 16;
-    const uint32_t bar_o_free = bar_pv_done + 8;
+    const uint32_t bar_v16_full = bar_k16_full + 8;     // [2], per f16 V buffer
+    const uint32_t bar_p_full = bar_v16_full + 16;      // [2], per P buffer
+    const uint32_t bar_s_full = bar_p_full + 16;        // [2], per S buffer
+    const uint32_t bar_pv_done = bar_s_full + 16;       // [2], PV of tiles of each parity
+    const uint32_t bar_o_free = bar_pv_done + 16;
     const uint32_t bar_final = bar_o_free + 8;
     volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
 
@@ -214,26 +227,28 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::NS; ++i) {
-            mbar_init(bar_stg_full + 8 * i, C::FULL_ARRIVALS);
-            mbar_init(bar_stg_empty + 8 * i, 4);
+            mbar_init(bar_k_full + 8 * i, C::K_ARRIVALS);
+            mbar_init(bar_k_empty + 8 * i, C::NWORK);
+            mbar_init(bar_v_full + 8 * i, C::V_ARRIVALS);
+            mbar_init(bar_v_empty + 8 * i, C::NWORK);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bar_qstg_full + 8 * i, 1);
-            mbar_init(bar_qstg_empty + 8 * i, 4);
-            mbar_init(bar_p_full + 8 * i, 4);
+            mbar_init(bar_v16_full + 8 * i, C::NWORK);
+            mbar_init(bar_p_full + 8 * i, C::NWORK);
             mbar_init(bar_s_full + 8 * i, 1);
+            mbar_init(bar_pv_done + 8 * i, 1);
         }
-        mbar_init(bar_q16_full, 4);
-        mbar_init(bar_k16_full, 4);
-        mbar_init(bar_v16_full, 4);
-        mbar_init(bar_pv_done, 1);
-        mbar_init(bar_o_free, 4);
+        mbar_init(bar_qstg_full, 1);
+        mbar_init(bar_qstg_empty, C::NWORK);
+        mbar_init(bar_q16_full, C::NWORK);
+        mbar_init(bar_k16_full, C::NWORK);
+        mbar_init(bar_o_free, C::NWORK);
         mbar_init(bar_final, 1);
         misc[1] = 0;
         misc[2] = 0;
         fence_mbarrier_init();
     }
-    if (warp == 4) {
+    if (warp == C::W_MMA) {
         tmem_alloc(base + C::OFF_MISC, C::TMEM_COLS);
         tmem_relinquish();
     }
@@ -245,9 +260,9 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
     const uint32_t t_o = tmem + 2 * N;    // O^T: columns [2N, 3N)
     bool abort = false;
 
-    if (warp >= 5) {
+    if (warp >= C::W_PROD) {
         // ===================================================== producers
-        const int pw = warp - 5;   // 0: K rows, query rows and stage meta; 1: V rows
+        const int pw = warp - C::W_PROD;   // 0: K rows, query rows and stage meta; 1: V rows
         const uint8_t* pool = pw == 0 ? p.k_pool : p.v_pool;
         const uint64_t pol_kv = policy_evict_first();
         constexpr int RPI = 4;     // rows per warp-wide copy: 8 lanes x 16 B per 128-byte row
@@ -257,21 +272,20 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
             const ItemPlan it = plan_item<C, WIN>(item, p);
             if (!it.active || !it.seq_ok || it.n_stages == 0) continue;
             if (pw == 0) {
-                const uint32_t slot = qcount & 1u, use = qcount >> 1;
-                if (use >= 1 && !mbar_wait_bounded(bar_qstg_empty + 8 * slot, (use - 1) & 1u, kWaitLimitNs)) {
+                if (qcount >= 1 && !mbar_wait_bounded(bar_qstg_empty, (qcount - 1) & 1u, kWaitLimitNs)) {
                     abort = true;
                     break;
                 }
                 const int nrows = it.m_end - it.m0;
-                if (lane == 0) mbar_arrive_expect_tx(bar_qstg_full + 8 * slot, (uint32_t)(nrows * C::D * 2));
+                if (lane == 0) mbar_arrive_expect_tx(bar_qstg_full, (uint32_t)(nrows * C::D * 2));
                 __syncwarp();
-                const uint32_t qdst = base + C::OFF_QSTG + slot * C::QSTG_BYTES;
+                const uint32_t qdst = base + C::OFF_QSTG;
                 for (int i = lane; i < nrows; i += 32) {
                     const int m = it.m0 + i;
                     const int r = m / p.ratio, hl = m - r * p.ratio;
                     const __nv_bfloat16* src =
                         p.q + (((long long)it.g * p.rows + r) * p.n_head + it.kvh * p.ratio + hl) * C::D;
-                    bulk_load(qdst + i * C::D * 2, src, C::D * 2, bar_qstg_full + 8 * slot);
+                    bulk_load(qdst + i * C::D * 2, src, C::D * 2, bar_qstg_full);
                 }
                 ++qcount;
             }
@@ -306,7 +320,8 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                     }
                 }
                 const uint32_t slot = scount % C::NS, use = scount / C::NS;
-                if (use >= 1 && !mbar_wait_bounded(bar_stg_empty + 8 * slot, (use - 1) & 1u, kWaitLimitNs)) {
+                const uint32_t bar_empty = (pw == 0 ? bar_k_empty : bar_v_empty) + 8 * slot;
+                if (use >= 1 && !mbar_wait_bounded(bar_empty, (use - 1) & 1u, kWaitLimitNs)) {
                     abort = true;
                     break;
                 }
@@ -322,7 +337,7 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                         cp_async_16(dst + t * 128 + ((lc ^ (t & 7)) << 4), src + (long long)t0 * row_stride, pol_kv);
                     }
                 }
-                cp_async_arrive_noinc(bar_stg_full + 8 * slot);
+                cp_async_arrive_noinc((pw == 0 ? bar_k_full : bar_v_full) + 8 * slot);
                 if (pw == 0) {
                     uint32_t bad_any = 0;
                     float kss[C::MAXPG], vss[C::MAXPG];
@@ -342,7 +357,7 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                             meta[8 + i] = vss[i];
                         }
                         reinterpret_cast<uint32_t*>(meta)[16] = bad_any;
-                        mbar_arrive(bar_stg_full + 8 * slot);
+                        mbar_arrive(bar_k_full + 8 * slot);
                     }
                 }
                 ++scount;
@@ -350,17 +365,13 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
             if (misc[1]) abort = true;
         }
         cp_async_wait_all();
-        if (pw == 0 && lane == 0) {
-            const uint32_t qfirst = qcount > 2u ? qcount - 2u : 0u;
-            for (uint32_t c = qfirst; c < qcount; ++c)
-                mbar_wait_bounded(bar_qstg_full + 8 * (c & 1u), (c >> 1) & 1u, kWaitLimitNs);
-        }
-    } else if (warp == 4) {
+        if (pw == 0 && lane == 0 && qcount >= 1) mbar_wait_bounded(bar_qstg_full, (qcount - 1) & 1u, kWaitLimitNs);
+    } else if (warp == C::W_MMA) {
         // ===================================================== MMA issue
         constexpr uint32_t idesc_qk = umma_idesc_f16(128, N, 0, 0);   // A = K (K-major), B = Q (K-major)
         constexpr uint32_t idesc_pv = umma_idesc_f16(128, N, 1, 0);   // A = V^T (MN-major), B = P^T (K-major)
-        const uint32_t k16 = base + C::OFF_K16, v16 = base + C::OFF_V16, q16 = base + C::OFF_Q16;
-        uint32_t tcnt = 0, kcnt = 0, vcnt = 0, icnt = 0;
+        const uint32_t k16 = base + C::OFF_K16, q16 = base + C::OFF_Q16;
+        uint32_t tcnt = 0, kcnt = 0, icnt = 0;
         bool issued = false;
         for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
             const ItemPlan it = plan_item<C, WIN>(item, p);
@@ -396,22 +407,22 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                     const int jj = j - 1;
                     const uint32_t tt = tcnt + jj, b = tt & 1u;
                     if (!mbar_wait_bounded(bar_p_full + 8 * b, (tt >> 1) & 1u, kWaitLimitNs) ||
-                        !mbar_wait_bounded(bar_v16_full, vcnt & 1u, kWaitLimitNs) ||
+                        !mbar_wait_bounded(bar_v16_full + 8 * b, (tt >> 1) & 1u, kWaitLimitNs) ||
                         (jj == 0 && icnt >= 1 && !mbar_wait_bounded(bar_o_free, (icnt - 1) & 1u, kWaitLimitNs))) {
                         abort = true;
                         break;
                     }
-                    ++vcnt;
                     tc_fence_after();
                     if (lane == 0) {
                         const uint32_t pt = base + C::OFF_P + b * C::P_BYTES;
+                        const uint32_t vt = base + C::OFF_V16 + b * C::F16_TILE;
 #pragma unroll
                         for (int kk = 0; kk < C::BK / 16; ++kk) {
-                            const uint64_t ad = umma_desc_sw128(v16 + kk * 16 * 128, C::ATOM, 1024);
+                            const uint64_t ad = umma_desc_sw128(vt + kk * 16 * 128, C::ATOM, 1024);
                             const uint64_t bd = umma_desc_sw128(pt + (kk >> 2) * C::PATOM + (kk & 3) * 32, 16, 1024);
                             tc_mma_ss(t_o, ad, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
                         }
-                        tc_commit(bar_pv_done);
+                        tc_commit(bar_pv_done + 8 * b);
                     }
                     __syncwarp();
                 }
@@ -427,25 +438,30 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
         }
         __syncwarp();
     } else {
-        // ===================================================== workers (warps 0-3)
-        const int t = threadIdx.x;                                   // key slot / TMEM lane / head-dim element
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        // ===================================================== workers (warps 0-7)
+        constexpr int V = C::HALF;
+        const int t = threadIdx.x;                 // 0 .. 255
+        const int k = t & 127;                     // key slot / TMEM lane / head-dim element
+        const int h = t >> 7;                      // half of the query rows: rows h*V .. h*V+V-1
+        const int wq = warp & 3;                   // TMEM lane quarter
+        const int col0 = h * V;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t k16 = base + C::OFF_K16, v16 = base + C::OFF_V16, q16 = base + C::OFF_Q16;
         float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
-        // P^T store offsets of key slot t for the 8 swizzle phases of a row q
+        // P^T store offsets of key slot k for the 8 swizzle phases of a row q
         uint32_t poff[8];
 #pragma unroll
         for (int qq = 0; qq < 8; ++qq)
-            poff[qq] = (uint32_t)((t >> 6) * C::PATOM + ((((t & 63) >> 3) ^ qq) << 4) + (t & 7) * 2);
+            poff[qq] = (uint32_t)((k >> 6) * C::PATOM + ((((k & 63) >> 3) ^ qq) << 4) + (k & 7) * 2);
         uint32_t scount = 0, qcount = 0, tcnt = 0;
         // A time-out seen by this thread; published to the other workers at the
-        // next barrier they all reach, where all four warps leave together.
+        // next barrier they all reach, where all eight warps leave together.
         bool lab = false;
         for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
             const ItemPlan it = plan_item<C, WIN>(item, p);
             if (!it.active) continue;
             if (!it.seq_ok) {
-                for (int idx = t; idx < (it.m_end - it.m0) * C::D; idx += 128) {
+                for (int idx = t; idx < (it.m_end - it.m0) * C::D; idx += 256) {
                     const int m = it.m0 + idx / C::D, d = idx % C::D;
                     const int r = m / p.ratio, hl = m - r * p.ratio;
                     p.out[(((long long)it.g * p.rows + r) * p.n_head + it.kvh * p.ratio + hl) * C::D + d] =
@@ -463,7 +479,7 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                 const long long slot_idx = gq * p.max_splits + it.s;
                 float* pacc = p.part_acc + slot_idx * p.qtv * C::D;
                 float* pml = p.part_ml + slot_idx * p.qtv * 2;
-                for (int q = 0; q < nrows; ++q) __stcg(pacc + q * C::D + t, 0.f);
+                for (int q = h; q < nrows; q += 2) __stcg(pacc + q * C::D + k, 0.f);
                 if (t < nrows) __stcg(reinterpret_cast<float2*>(pml) + t, make_float2(-CUDART_INF_F, 0.f));
                 if (t == 0) __stcg(p.part_flag + slot_idx, 0u);
                 continue;
@@ -476,7 +492,7 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                 const int tlo = it.klo / P_, thi = (it.kmax + P_ - 1) / P_, ghi = (it.L + P_ - 1) / P_;
                 const int32_t* trow = p.page_table + (long long)it.g * p.pages_per_seq;
                 const int n_below = tlo - glo;
-                for (int i = t; i < n_below + (ghi - thi); i += 128) {
+                for (int i = t; i < n_below + (ghi - thi); i += 256) {
                     const int pi = i < n_below ? glo + i : thi + (i - n_below);
                     const int pg = __ldg(trow + pi);
                     bad |= (pg < 0 || pg >= p.num_pages) ? 1u : 0u;
@@ -484,11 +500,10 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
             }
             // ---- query rows: bf16 -> f16 (exact inside the f16 range) into the B operand tile
             {
-                const uint32_t slot = qcount & 1u, use = qcount >> 1;
-                if (!mbar_wait_bounded(bar_qstg_full + 8 * slot, use & 1u, kWaitLimitNs)) lab = true;
-                const uint32_t qs = base + C::OFF_QSTG + slot * C::QSTG_BYTES;
+                if (!lab && !mbar_wait_bounded(bar_qstg_full, qcount & 1u, kWaitLimitNs)) lab = true;
+                const uint32_t qs = base + C::OFF_QSTG;
                 bool qbad = false;
-                for (int i = t; i < N * 16; i += 128) {
+                for (int i = t; i < N * 16; i += 256) {
                     const int row = i >> 4, ch = i & 15;   // ch: 8 head-dim elements
                     uint32_t w[4] = {0u, 0u, 0u, 0u};
                     if (row < nrows && !lab) {
@@ -509,100 +524,113 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(bar_q16_full);
-                    mbar_arrive(bar_qstg_empty + 8 * slot);
+                    mbar_arrive(bar_qstg_empty);
                 }
                 ++qcount;
             }
-            // ---- per query row state (identical in every worker thread)
-            float mu[N], thr[N], lsum[N];
+            // ---- per query row state of this thread's half (identical across its key slots)
+            float mu[V], thr[V], lsum[V];
 #pragma unroll
-            for (int q = 0; q < N; ++q) {
+            for (int q = 0; q < V; ++q) {
                 mu[q] = 0.f;                 // running max in log2 units (0 while no key was seen)
                 thr[q] = -CUDART_INF_F;      // logits above this move the max
                 lsum[q] = 0.f;               // this key slot's share of the row sum
             }
             const int nk0 = it.L - p.rows + it.m0 / p.ratio + 1;                    // keys row q=0 sees
             const int klo_last = WIN ? first_visible_key(it.L, p.rows, (it.m_end - 1) / p.ratio, p.window) : 0;
-            // ---- prologue: tile 0's K and V rows to f16, and key t's page scales
-            // (read before the stage goes back to the producers)
-            float kc_cur, vs_cur, kc_nxt = 0.f, vs_nxt = 0.f;
-            {
-                const uint32_t slot = scount % C::NS, use = scount / C::NS;
-                if (!lab && !mbar_wait_bounded(bar_stg_full + 8 * slot, use & 1u, kWaitLimitNs)) lab = true;
-                const uint32_t stg = base + C::OFF_STG + slot * C::STG_BYTES;
-                const int key = it.k0 + t;
-                convert_row<C>(stg, k16, t, lab);
-                convert_row<C>(stg + C::STG_TILE, v16, t, lab || key < it.klo || key >= it.k1);
+            // Staged K rows of tile i -> the f16 K tile; key k's page scales and
+            // the stage's page-id flag are read before the stage is released.
+            float kc_cur = 0.f, vs_cur = 0.f, kc_nxt = 0.f, vs_nxt = 0.f;
+            const auto load_k = [&](int i, float& kc, float& vs) {
+                const uint32_t slot = (scount + i) % C::NS, use = (scount + i) / C::NS;
+                if (!lab && !mbar_wait_bounded(bar_k_full + 8 * slot, use & 1u, kWaitLimitNs)) lab = true;
+                convert_half_row<C>(base + C::OFF_STG + slot * C::STG_BYTES, k16, k, h, lab);
                 const float* meta = reinterpret_cast<const float*>(smem + C::OFF_META + slot * C::META_STRIDE);
-                kc_cur = p.scale_log2 * meta[t / p.page_size];
-                vs_cur = meta[8 + t / p.page_size];
+                kc = p.scale_log2 * meta[k / p.page_size];
+                vs = meta[8 + k / p.page_size];
                 bad |= reinterpret_cast<const uint32_t*>(meta)[16];
                 fence_proxy_async_smem();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(bar_k16_full);
-                    mbar_arrive(bar_v16_full);
-                    mbar_arrive(bar_stg_empty + 8 * slot);
+                    mbar_arrive(bar_k_empty + 8 * slot);
                 }
-            }
+            };
+            // Staged V rows of tile i -> f16 V buffer (tcnt + i) & 1, zero outside
+            // the item's keys (P is 0 there; the slots may hold anything).
+            const auto load_v = [&](int i) {
+                const uint32_t slot = (scount + i) % C::NS, use = (scount + i) / C::NS;
+                const uint32_t vb = (tcnt + i) & 1u;
+                if (!lab && !mbar_wait_bounded(bar_v_full + 8 * slot, use & 1u, kWaitLimitNs)) lab = true;
+                const int key = it.k0 + i * C::BK + k;
+                convert_half_row<C>(base + C::OFF_STG + slot * C::STG_BYTES + C::STG_TILE, v16 + vb * C::F16_TILE, k, h,
+                                    lab || key < it.klo || key >= it.k1);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar_v16_full + 8 * vb);
+                    mbar_arrive(bar_v_empty + 8 * slot);
+                }
+            };
+            // Waits until PV of tile tt (an index over all tiles of this CTA) is done.
+            const auto wait_pv = [&](uint32_t tt) {
+                if (!lab && !mbar_wait_bounded(bar_pv_done + 8 * (tt & 1u), (tt >> 1) & 1u, kWaitLimitNs)) lab = true;
+                tc_fence_after();
+            };
+            // ---- prologue (the previous item's MMAs are all done: its epilogue waited)
+            load_k(0, kc_cur, vs_cur);
+            load_v(0);
             for (int j = 0; j < T; ++j) {
                 const uint32_t tt = tcnt + j, b = tt & 1u;
                 const int kbase = it.k0 + j * C::BK;
                 // S(j) = QK(j) done: the K f16 tile is free again
                 if (!lab && !mbar_wait_bounded(bar_s_full + 8 * b, (tt >> 1) & 1u, kWaitLimitNs)) lab = true;
                 tc_fence_after();
-                if (j + 1 < T) {
-                    const uint32_t s1 = (scount + j + 1) % C::NS, u1 = (scount + j + 1) / C::NS;
-                    if (!lab && !mbar_wait_bounded(bar_stg_full + 8 * s1, u1 & 1u, kWaitLimitNs)) lab = true;
-                    convert_row<C>(base + C::OFF_STG + s1 * C::STG_BYTES, k16, t, lab);
-                    fence_proxy_async_smem();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_k16_full);
-                }
-                // ---- softmax of key kbase + t against the N query rows
-                uint32_t sv[N];
-                tmem_ldN<N>(t_s + N * b + lane_off, sv);
+                if (j + 1 < T) load_k(j + 1, kc_nxt, vs_nxt);
+                // ---- softmax of key kbase + k against this half's query rows
+                uint32_t sv[V];
+                tmem_ldV<V>(t_s + N * b + col0 + lane_off, sv);
                 const float c_t = kc_cur, vs_t = vs_cur;
-                float xs[N];
+                float xs[V];
                 const bool full = kbase + C::BK <= it.k1 && kbase + C::BK <= nk0 && kbase >= klo_last;
                 if (full) {
 #pragma unroll
-                    for (int q = 0; q < N; ++q) xs[q] = __uint_as_float(sv[q]) * c_t;
+                    for (int q = 0; q < V; ++q) xs[q] = __uint_as_float(sv[q]) * c_t;
                 } else {
-                    // key k is visible to row q (query row m0+q at position L-R+(m0+q)/ratio)
+                    // key is visible to row q (query row m0+q at position L-R+(m0+q)/ratio)
                     // iff qc <= q < qw; thresholds clamped to [-1, N]
-                    const int key = kbase + t;
+                    const int key = kbase + k;
                     const long long dk = (long long)key - (it.L - p.rows + 1);
                     long long qc = (dk + 1) * p.ratio - it.m0;
                     long long qw = WIN ? (dk + p.window + 1) * p.ratio - it.m0 : (long long)N;
                     qc = qc < -1 ? -1 : (qc > N ? N : qc);
                     qw = qw < -1 ? -1 : (qw > N ? N : qw);
                     const bool in_item = key >= it.klo && key < it.k1;
-                    const int qci = in_item ? (int)qc : N, qwi = (int)qw;
+                    const int qci = in_item ? (int)qc - col0 : V, qwi = (int)qw - col0;
 #pragma unroll
-                    for (int q = 0; q < N; ++q)
+                    for (int q = 0; q < V; ++q)
                         xs[q] = (q >= qci && q < qwi) ? __uint_as_float(sv[q]) * c_t : -CUDART_INF_F;
                 }
                 bool trig = false;
 #pragma unroll
-                for (int q = 0; q < N; ++q) trig |= xs[q] > thr[q];
+                for (int q = 0; q < V; ++q) trig |= xs[q] > thr[q];
                 if (lab) misc[2] = 1u;
-                const bool any_trig = named_barrier_or(2, 128, trig);
+                const bool any_trig = named_barrier_or(2, 256, trig);
                 if (misc[2]) {
                     abort = true;
                     break;
                 }
                 if (any_trig) {
                     // tile max per row; a row's max moves only past 2^8 (or on its first keys)
-                    float v[N], mx[N];
+                    float v[V], mx[V];
 #pragma unroll
-                    for (int q = 0; q < N; ++q) v[q] = xs[q];
-                    workers_reduce<N, true>(v, mx, red, warp, lane, t);
-                    float alpha[N];
+                    for (int q = 0; q < V; ++q) v[q] = xs[q];
+                    workers_reduce<V, true>(v, mx, red, wq, h, lane, k);
+                    float alpha[V];
                     bool moved_any = false;
 #pragma unroll
-                    for (int q = 0; q < N; ++q) {
+                    for (int q = 0; q < V; ++q) {
                         const bool first = thr[q] == -CUDART_INF_F;
                         const bool mv = first ? mx[q] != -CUDART_INF_F : mx[q] > thr[q];
                         alpha[q] = 1.f;
@@ -615,75 +643,65 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                         }
                     }
                     if (moved_any && j > 0) {
-                        // O holds PV(0 .. j-1), complete (waited below in tile j-1)
-                        uint32_t ov[N];
-                        tmem_ldN<N>(t_o + lane_off, ov);
+                        // O must hold PV(0 .. j-1) complete before it is rescaled
+                        wait_pv(tt - 1);
+                        uint32_t ov[V];
+                        tmem_ldV<V>(t_o + col0 + lane_off, ov);
 #pragma unroll
-                        for (int q = 0; q < N; ++q) ov[q] = __float_as_uint(__uint_as_float(ov[q]) * alpha[q]);
-                        tmem_stN<N>(t_o + lane_off, ov);
+                        for (int q = 0; q < V; ++q) ov[q] = __float_as_uint(__uint_as_float(ov[q]) * alpha[q]);
+                        tmem_stV<V>(t_o + col0 + lane_off, ov);
                         tmem_wait_st();
                     }
                 }
-                // ---- P^T[key][q] = f16(2^(x - max) * V scale), sums without the V scale
+                // ---- P^T[key][q] = f16(2^(x - max) * V scale), sums without the V scale;
+                // the P buffer was last read by PV(j-2)
+                if (j >= 2) wait_pv(tt - 2);
                 const uint32_t pt = base + C::OFF_P + b * C::P_BYTES;
 #pragma unroll
-                for (int q = 0; q < N; ++q) {
+                for (int q = 0; q < V; ++q) {
                     const float pr = exp2f(xs[q] - mu[q]);
                     lsum[q] += pr;
-                    sts16(pt + poff[q & 7] + q * 128, pr * vs_t);
+                    sts16(pt + poff[q & 7] + (col0 + q) * 128, pr * vs_t);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_p_full + 8 * b);
-                // ---- PV(j) done: V f16 tile and O free; convert tile j+1's V rows
-                if (!lab && !mbar_wait_bounded(bar_pv_done, tt & 1u, kWaitLimitNs)) lab = true;
-                tc_fence_after();
+                // ---- tile j+1's V rows into the other f16 V buffer, last read by PV(j-1)
                 if (j + 1 < T) {
-                    const uint32_t s1 = (scount + j + 1) % C::NS;
-                    const int key = kbase + C::BK + t;
-                    convert_row<C>(base + C::OFF_STG + s1 * C::STG_BYTES + C::STG_TILE, v16, t,
-                                   lab || key < it.klo || key >= it.k1);
-                    const float* meta = reinterpret_cast<const float*>(smem + C::OFF_META + s1 * C::META_STRIDE);
-                    kc_nxt = p.scale_log2 * meta[t / p.page_size];
-                    vs_nxt = meta[8 + t / p.page_size];
-                    bad |= reinterpret_cast<const uint32_t*>(meta)[16];
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(bar_v16_full);
-                        mbar_arrive(bar_stg_empty + 8 * s1);
-                    }
+                    if (j >= 1) wait_pv(tt - 1);
+                    load_v(j + 1);
                 }
                 kc_cur = kc_nxt;
                 vs_cur = vs_nxt;
             }
             if (abort) break;
+            wait_pv(tcnt + T - 1);
             scount += T;
             tcnt += T;
-            // ---- epilogue: row sums over the 128 key slots, O^T (lane t = head-dim element t)
-            float ltot[N];
-            workers_reduce<N, false>(lsum, ltot, red, warp, lane, t);
+            // ---- epilogue: row sums over the 128 key slots, O^T (lane k = head-dim element k)
+            float ltot[V];
+            workers_reduce<V, false>(lsum, ltot, red, wq, h, lane, k);
             if (lab) misc[2] = 1u;
-            const bool item_bad = named_barrier_or(2, 128, bad != 0);
+            const bool item_bad = named_barrier_or(2, 256, bad != 0);
             if (misc[2]) {
                 abort = true;
                 break;
             }
-            uint32_t ov[N];
-            tmem_ldN<N>(t_o + lane_off, ov);
+            uint32_t ov[V];
+            tmem_ldV<V>(t_o + col0 + lane_off, ov);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_o_free);
             const bool final_write = it.n_splits - it.s_first == 1;
             if (final_write) {
-                int r = it.m0 / p.ratio, hl = it.m0 - r * p.ratio;
+                int r = (it.m0 + col0) / p.ratio, hl = (it.m0 + col0) - r * p.ratio;
 #pragma unroll
-                for (int q = 0; q < N; ++q) {
-                    if (q < nrows) {
+                for (int q = 0; q < V; ++q) {
+                    if (col0 + q < nrows) {
                         // acc * (1/l), the combine kernel's form
                         const float o = item_bad ? 0.f : __uint_as_float(ov[q]) * (1.f / ltot[q]);
-                        p.out[(((long long)it.g * p.rows + r) * p.n_head + it.kvh * p.ratio + hl) * C::D + t] =
+                        p.out[(((long long)it.g * p.rows + r) * p.n_head + it.kvh * p.ratio + hl) * C::D + k] =
                             __float2bfloat16_rn(o);
                     }
                     if (++hl == p.ratio) {
@@ -698,11 +716,11 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                 float* pacc = p.part_acc + slot_idx * p.qtv * C::D;
                 float* pml = p.part_ml + slot_idx * p.qtv * 2;
 #pragma unroll
-                for (int q = 0; q < N; ++q) {
-                    if (q < nrows) {
-                        __stcg(pacc + q * C::D + t, __uint_as_float(ov[q]));
-                        if (t == q)
-                            __stcg(reinterpret_cast<float2*>(pml) + q,
+                for (int q = 0; q < V; ++q) {
+                    if (col0 + q < nrows) {
+                        __stcg(pacc + (col0 + q) * C::D + k, __uint_as_float(ov[q]));
+                        if (k == q)
+                            __stcg(reinterpret_cast<float2*>(pml) + col0 + q,
                                    make_float2(ltot[q] == 0.f ? -CUDART_INF_F : mu[q], ltot[q]));
                     }
                 }
@@ -717,7 +735,7 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 4) tmem_dealloc(tmem, C::TMEM_COLS);
+    if (warp == C::W_MMA) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
 }  // namespace rad
