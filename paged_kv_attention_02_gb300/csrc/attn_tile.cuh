@@ -183,8 +183,15 @@ struct ItemPlan {
 
 // WIN: the call has a sliding window (p.window > 0); without one, every
 // window term folds away at compile time.
+// Sequence index of a work item (items are split-major).
+__device__ __forceinline__ int item_group(int item, const AttnParams& p) {
+    const int per_split = p.groups * p.n_head_kv * p.n_qtiles;
+    return (item % per_split) / (p.n_head_kv * p.n_qtiles);
+}
+
+// The plan of a work item given its sequence length (L < 0: load it).
 template <class C, bool WIN>
-__device__ __forceinline__ ItemPlan plan_item(int item, const AttnParams& p) {
+__device__ __forceinline__ ItemPlan plan_item(int item, const AttnParams& p, int L_known = -1) {
     ItemPlan it;
     const int per_split = p.groups * p.n_head_kv * p.n_qtiles;
     it.s = item / per_split;
@@ -195,7 +202,7 @@ __device__ __forceinline__ ItemPlan plan_item(int item, const AttnParams& p) {
     it.kvh = rem2 / p.n_qtiles;
     it.qt = rem2 - it.kvh * p.n_qtiles;
     if (p.split_len == 0) it.qt = p.n_qtiles - 1 - it.qt;   // causal: later tiles see more keys
-    it.L = __ldg(p.seq_lens + it.g);
+    it.L = L_known >= 0 ? L_known : __ldg(p.seq_lens + it.g);
     it.seq_ok = it.L >= p.rows && (long long)it.L <= (long long)p.pages_per_seq * p.page_size;
     it.m0 = it.qt * C::QT;
     it.m_end = min(p.M, it.m0 + C::QT);

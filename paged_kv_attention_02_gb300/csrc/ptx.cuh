@@ -179,7 +179,7 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1,
 // Two e4m3 codes (low byte = element 0) -> f16x2 (low half = element 0).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
     uint32_t r;
-    asm volatile("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(codes));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(codes));
     return r;
 }
 

@@ -9,24 +9,38 @@
 // same combine kernel.
 //
 // Keys are the MMA's M dimension (128 per tile) and the query rows its N:
-//   S^T[key][q] = K[key][:] . Q[q][:]        M 128, N, K = head_dim
-//   O^T[d][q]  += V^T[d][key] . P^T[key][q]   M = head_dim 128, N, K = 128 keys
+//   S^T[key][q] = K[key][:] . Q[q][:]        kind::f8f6f4, M 128, N, K = head_dim:
+//                                            K straight from the staged e4m3 rows,
+//                                            Q as two e4m3 terms (below)
+//   O^T[d][q]  += V^T[d][key] . P^T[key][q]   kind::f16, M = head_dim 128, N, K = 128
+//                                            keys: V converted to f16, P in f16
+// Q row q is split as q * 2^k = hi + lo, each term e4m3 (k per row puts the
+// row's largest |q| in [128, 256)): hi is q * 2^k rounded to 4 significant
+// bits, and the remainder of a bf16 value (8 significant bits) then has at
+// most 4, so lo holds it exactly -- the two terms are q itself, except where
+// lo falls into e4m3's subnormal range (elements below 2^-8 of the row's
+// largest).  The tensor core forms the products exactly in fp32 and the
+// logits are scaled back by 2^-k.
 // so a decode step's few query rows per KV head cost a narrow N instead of
 // an idle M.  Warp roles (one CTA per SM, persistent):
-//   warps 9, 10 producers: page ids from the page table ("kern manifest v7",
+//   last two    producers: page ids from the page table ("kern manifest v7",
 //               $defs.Domain), 16-byte cp.async copies of each tile's e4m3 K
-//               rows (warp 9) and V rows (warp 10) into two staging rings,
+//               rows and V rows (one warp each) into two staging rings,
 //               the per-page scales, and a 1-D bulk copy of the query rows.
-//   warp 8      MMA: one lane issues tcgen05.mma.kind::f16 from shared-memory
-//               operands into TMEM and commits to mbarriers.
-//   warps 0-7   workers; thread t serves key slot k = t % 128 (TMEM lane k)
-//               and half h = t / 128 of the query rows (warps w and w+4 share
-//               TMEM lanes 32(w%4)..): convert its half of key row k of the
-//               staged e4m3 tiles to f16 once per tile (exact) in the
-//               128-byte-swizzled layout the MMA reads, run the online
-//               softmax of key k against its half of the query rows, write
-//               P^T, and in the epilogue read O^T (lane k = head-dim element
-//               k) and store its rows.
+//   warp 4G     QK MMA: one lane issues the tcgen05.mma of S^T per tile as
+//               soon as its K stage has landed and its TMEM S buffer is free
+//               (up to NSB tiles ahead of the softmax, across items).
+//   warp 4G+1   PV MMA: one lane issues O^T += V^T P^T per tile once the
+//               workers published P and the f16 V tile.
+//   warps 0 .. 4G-1  workers; thread t serves key slot k = t % 128 (TMEM
+//               lane k) and group h = t / 128 of the query rows (warps w,
+//               w+4, .. share TMEM lanes 32(w%4)..): split the item's query
+//               rows into e4m3 terms, convert its share of key row k of the
+//               staged e4m3 V tile to f16 once per tile (exact) in the
+//               128-byte-swizzled layout the MMA reads, run the online softmax
+//               of key k against its group of query rows, write P^T, and in
+//               the epilogue read O^T (lane k = head-dim element k) and store
+//               its rows.
 // Per query row, the running max moves (and O and the sums are rescaled)
 // only when a tile's logits exceed it by more than 2^8; the per-row sums are
 // kept per key slot and reduced once per item in a fixed order, so a row's
@@ -45,6 +59,15 @@
 #ifndef RAD_SPLITTC_NS
 #define RAD_SPLITTC_NS 3
 #endif
+// Groups G the query rows of an item are split into among the workers (4G
+// worker warps, G per TMEM lane quarter).
+#ifndef RAD_SPLITTC_GROUPS
+#define RAD_SPLITTC_GROUPS 2
+#endif
+// Producer warps per tensor (K, V); each takes every PPW-th page of a tile.
+#ifndef RAD_SPLITTC_PPW
+#define RAD_SPLITTC_PPW 1
+#endif
 
 namespace rad {
 
@@ -53,7 +76,10 @@ struct SplitTcCfg {
     static constexpr int D = 128;      // head dim
     static constexpr int BK = 128;     // keys per tile: the MMA's M
     static constexpr int N = N_;       // query rows per item: the MMA's N
-    static constexpr int HALF = N / 2; // query rows per worker thread
+    static constexpr int NSB = 3;      // S buffers: QK runs up to two tiles ahead of PV
+    static constexpr int G = RAD_SPLITTC_GROUPS;
+    static constexpr int V = N / G;    // query rows per worker thread
+    static constexpr int CPT = 8 / G;  // 16-byte chunks of a V row each worker converts
     static constexpr int QT = N;       // (item planner) query rows per tile
     static constexpr int KS = BK;      // (item planner) keys per stage
     static constexpr int NS = RAD_SPLITTC_NS;
@@ -62,74 +88,89 @@ struct SplitTcCfg {
     static constexpr int STG_BYTES = 2 * STG_TILE;
     static constexpr int ATOM = BK * 128;            // f16 tile: stride between 64-column blocks
     static constexpr int F16_TILE = 2 * ATOM;        // [column block 2][key 128][128 B]
-    static constexpr int QATOM = N * 128;
-    static constexpr int Q16_BYTES = 2 * QATOM;      // [column block 2][q N][128 B]
+    static constexpr int Q8_TERM = N * 128;          // one e4m3 term of the query rows: [q N][128 B]
+    static constexpr int QTERMS = 2;                 // e4m3 terms per query row (hi, lo)
+    static constexpr int Q8_BYTES = QTERMS * Q8_TERM;
     static constexpr int QSTG_BYTES = N * D * 2;     // bf16 query rows, one slot
     static constexpr int PATOM = N * 128;
     static constexpr int P_BYTES = 2 * PATOM;        // [key block 2][q N][128 B]
     static constexpr int MAXPG = BK / 16;            // pages per tile
     static constexpr int META_STRIDE = 128;          // ks[8], vs[8], bad
-    // K and V staging rings (NS stages each), one f16 K tile, two f16 V tiles
+    // K and V staging rings (NS stages each; a staged K tile is the QK MMA's A
+    // operand as it lands), two f16 V tiles, the query terms, two P tiles
     static constexpr int OFF_STG = 0;            // stage i: K at i*STG_BYTES, V at +STG_TILE
-    static constexpr int OFF_K16 = OFF_STG + NS * STG_BYTES;
-    static constexpr int OFF_V16 = OFF_K16 + F16_TILE;          // two buffers
-    static constexpr int OFF_Q16 = OFF_V16 + 2 * F16_TILE;
-    static constexpr int OFF_P = OFF_Q16 + Q16_BYTES;
+    static constexpr int OFF_V16 = OFF_STG + NS * STG_BYTES;    // two buffers
+    static constexpr int OFF_Q8 = OFF_V16 + 2 * F16_TILE;
+    static constexpr int OFF_P = OFF_Q8 + Q8_BYTES;
     static constexpr int OFF_QSTG = OFF_P + 2 * P_BYTES;        // one slot
     static constexpr int OFF_META = OFF_QSTG + QSTG_BYTES;
-    static constexpr int OFF_RED = OFF_META + NS * META_STRIDE;    // [4][N] partials + [N] totals
-    static constexpr int OFF_BARS = OFF_RED + 5 * N * 4;   // [2][4][HALF] partials + [2][HALF] totals
+    static constexpr int OFF_RED = OFF_META + NS * META_STRIDE;
+    static constexpr int OFF_ISQ = OFF_RED + 5 * N * 4;    // red: [G][4][V] partials + [G][V] totals
+    static constexpr int OFF_BARS = OFF_ISQ + N * 4;       // isq: 2^-k of each query row
     // k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], qstg_full, qstg_empty,
-    // q16_full, k16_full, v16_full[2], p_full[2], s_full[2], pv_done[2], o_free, final
-    static constexpr int NBARS = 4 * NS + 2 + 2 + 2 + 2 + 2 + 2 + 2;
+    // q8_full, (unused), v16_full[2], p_full[2], s_full[NSB], s_empty[NSB], pv_done[2],
+    // o_free, final_qk, final_pv
+    static constexpr int NBARS = 4 * NS + 2 + 2 + 2 + 2 + 2 * NSB + 2 + 3;
     static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;          // [0] tmem, [1] abort, [2] worker abort
     static constexpr int SMEM_USED = OFF_MISC + 16;
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;   // 1 KB alignment of the swizzled operand tiles
-    static constexpr int NWORK = 8;                      // worker warps
-    static constexpr int W_MMA = 8, W_PROD = 9;
-    static constexpr int NTHREADS = 11 * 32;
-    static constexpr int K_ARRIVALS = 32 + 1;             // 32 async lane arrivals + stage meta
-    static constexpr int V_ARRIVALS = 32;
-    static constexpr uint32_t TMEM_COLS = 3 * N <= 64 ? 64 : 128;   // S[2] and O
+    static constexpr int NWORK = 4 * G;                  // worker warps
+    static constexpr int NWT = NWORK * 32;               // worker threads
+    static constexpr int PPW = RAD_SPLITTC_PPW;
+    static constexpr int W_QK = NWORK, W_PV = NWORK + 1, W_PROD = NWORK + 2;
+    static constexpr int NTHREADS = (NWORK + 2 + 2 * PPW) * 32;
+    static constexpr int K_ARRIVALS = 32 * PPW + 1;       // async lane arrivals + stage meta
+    static constexpr int V_ARRIVALS = 32 * PPW;
+    static constexpr uint32_t TMEM_COLS = (NSB + 1) * N <= 64 ? 64 : 128;   // S[NSB] and O
     static_assert(N == 16 || N == 32, "query rows per item");
-    static_assert(OFF_K16 % 1024 == 0 && OFF_V16 % 1024 == 0 && OFF_Q16 % 1024 == 0 && OFF_P % 1024 == 0,
+    static_assert((G == 2 || G == 4) && V >= 4, "query-row groups");
+    static_assert(STG_BYTES % 1024 == 0 && OFF_V16 % 1024 == 0 && OFF_Q8 % 1024 == 0 && OFF_P % 1024 == 0 &&
+                      Q8_TERM % 1024 == 0,
                   "swizzled operand tiles on 1 KB boundaries");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-__device__ __forceinline__ uint4 lds128(uint32_t a) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
-    return v;
+
+// Two floats -> two e4m3 codes (round to nearest even, saturating; `lo` in the
+// low byte).
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
 }
-__device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
-}
-__device__ __forceinline__ void sts16(uint32_t a, float x) {
-    asm volatile("{\n\t.reg .b16 h;\n\tcvt.rn.f16.f32 h, %1;\n\tst.shared.b16 [%0], h;\n\t}" ::"r"(a), "f"(x)
-                 : "memory");
+// Exact values of two e4m3 codes (the low byte first).
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t codes) {
+    const uint32_t h = e4m3x2_to_f16x2((uint16_t)codes);
+    return __half22float2(*reinterpret_cast<const __half2*>(&h));
 }
 
-// Converts half h of key row t of a staged tile (128 e4m3 codes, 16-byte
-// chunks swizzled by t & 7): codes 64h .. 64h+63 become column block h of an
-// f16 tile [column block][key][128 B] with the same 128-byte swizzle; `zero`
-// writes zeros instead.
+// Converts share h of key row t of a staged tile (128 e4m3 codes, 16-byte
+// chunks swizzled by t & 7): chunks h*CPT .. h*CPT+CPT-1 (16 codes each)
+// become f16 in an f16 tile [column block][key][128 B] with the same 128-byte
+// swizzle; `zero` writes zeros instead.  Plain shared-memory loads and stores
+// (ordered by the barrier waits and fences around the call) so they can be
+// scheduled freely.
 template <class C>
-__device__ __forceinline__ void convert_half_row(uint32_t src, uint32_t dst, int t, int h, bool zero) {
+__device__ __forceinline__ void convert_row_share(const uint8_t* src, uint8_t* dst, int t, int h, bool zero) {
     const uint32_t sw = (uint32_t)(t & 7);
+    uint4 in[C::CPT];
 #pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-        const int c = 4 * h + cc;
-        const uint4 v = zero ? make_uint4(0u, 0u, 0u, 0u) : lds128(src + t * 128 + ((c ^ sw) << 4));
+    for (int cc = 0; cc < C::CPT; ++cc)
+        in[cc] = zero ? make_uint4(0u, 0u, 0u, 0u)
+                      : *reinterpret_cast<const uint4*>(src + t * 128 + (((C::CPT * h + cc) ^ sw) << 4));
+#pragma unroll
+    for (int cc = 0; cc < C::CPT; ++cc) {
+        const int c = C::CPT * h + cc;
+        const uint4 v = in[cc];
         const uint32_t h0 = e4m3x2_to_f16x2((uint16_t)(v.x & 0xFFFFu)), h1 = e4m3x2_to_f16x2((uint16_t)(v.x >> 16));
         const uint32_t h2 = e4m3x2_to_f16x2((uint16_t)(v.y & 0xFFFFu)), h3 = e4m3x2_to_f16x2((uint16_t)(v.y >> 16));
         const uint32_t h4 = e4m3x2_to_f16x2((uint16_t)(v.z & 0xFFFFu)), h5 = e4m3x2_to_f16x2((uint16_t)(v.z >> 16));
         const uint32_t h6 = e4m3x2_to_f16x2((uint16_t)(v.w & 0xFFFFu)), h7 = e4m3x2_to_f16x2((uint16_t)(v.w >> 16));
         // codes 16c .. 16c+15 -> f16 chunks 2c, 2c+1 of the row (8 values each)
-        const uint32_t row = dst + (c >> 2) * C::ATOM + t * 128;
+        uint8_t* row = dst + (c >> 2) * C::ATOM + t * 128;
         const uint32_t ch = (uint32_t)((c & 3) * 2);
-        sts128(row + ((ch ^ sw) << 4), h0, h1, h2, h3);
-        sts128(row + (((ch + 1) ^ sw) << 4), h4, h5, h6, h7);
+        *reinterpret_cast<uint4*>(row + ((ch ^ sw) << 4)) = make_uint4(h0, h1, h2, h3);
+        *reinterpret_cast<uint4*>(row + (((ch + 1) ^ sw) << 4)) = make_uint4(h4, h5, h6, h7);
     }
 }
 
@@ -160,40 +201,43 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[V], int lane) 
     return v[0];
 }
 
-// All eight worker warps: for each half h of the query rows, totals of v over
-// the 128 key slots, per row, into tot[V] of every thread of that half (the
-// partials of the four warps of a half combined in warp order).
-template <int V, bool MAX>
+// All worker warps: for each group h of the query rows, totals of v over the
+// 128 key slots, per row, into tot[V] of every thread of that group (the
+// partials of the four warps of a group combined in warp order).
+template <int V, int NWT, bool MAX>
 __device__ __forceinline__ void workers_reduce(float (&v)[V], float (&tot)[V], float* red, int wq, int h, int lane,
                                                int k) {
+    constexpr int TOT = NWT / 32 * V;   // offset of the totals: [G][4][V] partials first
     const float mine = warp_transpose_reduce<V, MAX>(v, lane);
     if (lane < V) red[(h * 4 + wq) * V + lane] = mine;
-    named_barrier_sync(2, 256);
+    named_barrier_sync(2, NWT);
     if (k < V) {
         float a = red[(h * 4) * V + k];
 #pragma unroll
         for (int w = 1; w < 4; ++w) a = MAX ? fmaxf(a, red[(h * 4 + w) * V + k]) : a + red[(h * 4 + w) * V + k];
-        red[8 * V + h * V + k] = a;
+        red[TOT + h * V + k] = a;
     }
-    named_barrier_sync(2, 256);
+    named_barrier_sync(2, NWT);
 #pragma unroll
     for (int q = 0; q < V; q += 4) {
-        const uint4 f = lds128(smem_addr(red + 8 * V + h * V + q));
-        tot[q] = __uint_as_float(f.x);
-        tot[q + 1] = __uint_as_float(f.y);
-        tot[q + 2] = __uint_as_float(f.z);
-        tot[q + 3] = __uint_as_float(f.w);
+        const float4 f = *reinterpret_cast<const float4*>(red + TOT + h * V + q);
+        tot[q] = f.x;
+        tot[q + 1] = f.y;
+        tot[q + 2] = f.z;
+        tot[q + 3] = f.w;
     }
 }
 
 template <int V>
 __device__ __forceinline__ void tmem_ldV(uint32_t taddr, uint32_t (&r)[V]) {
-    if constexpr (V == 8) tmem_ld8(taddr, r);
+    if constexpr (V == 4) tmem_ld4(taddr, r);
+    else if constexpr (V == 8) tmem_ld8(taddr, r);
     else tmem_ld16(taddr, r);
 }
 template <int V>
 __device__ __forceinline__ void tmem_stV(uint32_t taddr, const uint32_t (&r)[V]) {
-    if constexpr (V == 8) tmem_st8(taddr, r);
+    if constexpr (V == 4) tmem_st4(taddr, r);
+    else if constexpr (V == 8) tmem_st8(taddr, r);
     else tmem_st16(taddr, r);
 }
 
@@ -212,14 +256,14 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
     const uint32_t bar_v_empty = bar_v_full + 8 * C::NS;
     const uint32_t bar_qstg_full = bar_v_empty + 8 * C::NS;
     const uint32_t bar_qstg_empty = bar_qstg_full + 8;
-    const uint32_t bar_q16_full = bar_qstg_empty + 8;
-    const uint32_t bar_k16_full = bar_q16_full + 8;
-    const uint32_t bar_v16_full = bar_k16_full + 8;     // [2], per f16 V buffer
+    const uint32_t bar_q8_full = bar_qstg_empty + 8;
+    const uint32_t bar_v16_full = bar_q8_full + 16;     // [2], per f16 V buffer
     const uint32_t bar_p_full = bar_v16_full + 16;      // [2], per P buffer
-    const uint32_t bar_s_full = bar_p_full + 16;        // [2], per S buffer
-    const uint32_t bar_pv_done = bar_s_full + 16;       // [2], PV of tiles of each parity
+    const uint32_t bar_s_full = bar_p_full + 16;        // [NSB], per S buffer
+    const uint32_t bar_s_empty = bar_s_full + 8 * C::NSB;   // [NSB], S read by the workers
+    const uint32_t bar_pv_done = bar_s_empty + 8 * C::NSB;  // [2], PV of tiles of each parity
     const uint32_t bar_o_free = bar_pv_done + 16;
-    const uint32_t bar_final = bar_o_free + 8;
+    const uint32_t bar_final = bar_o_free + 8;          // [2]: QK warp, PV warp
     volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);
 
     const int warp = threadIdx.x >> 5;
@@ -228,27 +272,30 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::NS; ++i) {
             mbar_init(bar_k_full + 8 * i, C::K_ARRIVALS);
-            mbar_init(bar_k_empty + 8 * i, C::NWORK);
+            mbar_init(bar_k_empty + 8 * i, 1 + C::NWORK);   // the QK MMA's commit + the workers' scale reads
             mbar_init(bar_v_full + 8 * i, C::V_ARRIVALS);
             mbar_init(bar_v_empty + 8 * i, C::NWORK);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_v16_full + 8 * i, C::NWORK);
             mbar_init(bar_p_full + 8 * i, C::NWORK);
-            mbar_init(bar_s_full + 8 * i, 1);
             mbar_init(bar_pv_done + 8 * i, 1);
+        }
+        for (int i = 0; i < C::NSB; ++i) {
+            mbar_init(bar_s_full + 8 * i, 1);
+            mbar_init(bar_s_empty + 8 * i, C::NWORK);
         }
         mbar_init(bar_qstg_full, 1);
         mbar_init(bar_qstg_empty, C::NWORK);
-        mbar_init(bar_q16_full, C::NWORK);
-        mbar_init(bar_k16_full, C::NWORK);
+        mbar_init(bar_q8_full, C::NWORK);
         mbar_init(bar_o_free, C::NWORK);
         mbar_init(bar_final, 1);
+        mbar_init(bar_final + 8, 1);
         misc[1] = 0;
         misc[2] = 0;
         fence_mbarrier_init();
     }
-    if (warp == C::W_MMA) {
+    if (warp == C::W_QK) {
         tmem_alloc(base + C::OFF_MISC, C::TMEM_COLS);
         tmem_relinquish();
     }
@@ -256,13 +303,15 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
-    const uint32_t t_s = tmem;            // S buffer b: columns [b*N, b*N + N)
-    const uint32_t t_o = tmem + 2 * N;    // O^T: columns [2N, 3N)
+    const uint32_t t_s = tmem;                  // S buffer b: columns [b*N, b*N + N)
+    const uint32_t t_o = tmem + C::NSB * N;     // O^T: columns [NSB*N, NSB*N + N)
     bool abort = false;
 
     if (warp >= C::W_PROD) {
         // ===================================================== producers
-        const int pw = warp - C::W_PROD;   // 0: K rows, query rows and stage meta; 1: V rows
+        const int pr = warp - C::W_PROD;
+        const int pw = pr / C::PPW;        // 0: K rows (the first K warp also query rows, stage meta); 1: V rows
+        const int pj = pr % C::PPW;        // this warp's pages of a tile: i % PPW == pj
         const uint8_t* pool = pw == 0 ? p.k_pool : p.v_pool;
         const uint64_t pol_kv = policy_evict_first();
         constexpr int RPI = 4;     // rows per warp-wide copy: 8 lanes x 16 B per 128-byte row
@@ -271,7 +320,7 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
         for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
             const ItemPlan it = plan_item<C, WIN>(item, p);
             if (!it.active || !it.seq_ok || it.n_stages == 0) continue;
-            if (pw == 0) {
+            if (pr == 0) {
                 if (qcount >= 1 && !mbar_wait_bounded(bar_qstg_empty, (qcount - 1) & 1u, kWaitLimitNs)) {
                     abort = true;
                     break;
@@ -326,7 +375,7 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                     break;
                 }
                 const uint32_t tile = base + C::OFF_STG + slot * C::STG_BYTES + pw * C::STG_TILE;
-                for (int i = 0; i < npages; ++i) {
+                for (int i = pj; i < npages; i += C::PPW) {
                     if (WIN && pstart + i < page_lo) continue;   // stale rows: masked in S, zeroed in V
                     const int pg = __shfl_sync(0xffffffffu, my_pg, (pstart - batch0 + i) & 31);
                     const uint8_t* src = head_base + (long long)pg * P * row_stride;
@@ -338,7 +387,7 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                     }
                 }
                 cp_async_arrive_noinc((pw == 0 ? bar_k_full : bar_v_full) + 8 * slot);
-                if (pw == 0) {
+                if (pr == 0) {
                     uint32_t bad_any = 0;
                     float kss[C::MAXPG], vss[C::MAXPG];
 #pragma unroll
@@ -365,69 +414,49 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
             if (misc[1]) abort = true;
         }
         cp_async_wait_all();
-        if (pw == 0 && lane == 0 && qcount >= 1) mbar_wait_bounded(bar_qstg_full, (qcount - 1) & 1u, kWaitLimitNs);
-    } else if (warp == C::W_MMA) {
-        // ===================================================== MMA issue
-        constexpr uint32_t idesc_qk = umma_idesc_f16(128, N, 0, 0);   // A = K (K-major), B = Q (K-major)
-        constexpr uint32_t idesc_pv = umma_idesc_f16(128, N, 1, 0);   // A = V^T (MN-major), B = P^T (K-major)
-        const uint32_t k16 = base + C::OFF_K16, q16 = base + C::OFF_Q16;
-        uint32_t tcnt = 0, kcnt = 0, icnt = 0;
+        if (pr == 0 && lane == 0 && qcount >= 1) mbar_wait_bounded(bar_qstg_full, (qcount - 1) & 1u, kWaitLimitNs);
+    } else if (warp == C::W_QK) {
+        // ===================================================== QK MMA issue
+        constexpr uint32_t idesc_qk = umma_idesc_e4m3(128, N);        // A = K, B = Q terms (both K-major)
+        const uint32_t q8 = base + C::OFF_Q8;
+        uint32_t tcnt = 0, scnt = 0, icnt = 0;
         bool issued = false;
         for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
             const ItemPlan it = plan_item<C, WIN>(item, p);
             if (!it.active || !it.seq_ok || it.n_stages == 0) continue;
             const int T = it.n_stages;
-            if (!mbar_wait_bounded(bar_q16_full, icnt & 1u, kWaitLimitNs)) {
+            if (!mbar_wait_bounded(bar_q8_full, icnt & 1u, kWaitLimitNs)) {
                 abort = true;
                 break;
             }
-            for (int j = 0; j <= T && !abort; ++j) {
-                if (j < T) {
-                    if (!mbar_wait_bounded(bar_k16_full, kcnt & 1u, kWaitLimitNs)) {
-                        abort = true;
-                        break;
-                    }
-                    ++kcnt;
-                    tc_fence_after();
-                    const uint32_t b = (tcnt + j) & 1u;
-                    if (lane == 0) {
-#pragma unroll
-                        for (int kk = 0; kk < C::D / 16; ++kk) {
-                            const uint32_t off = (kk >> 2) * C::ATOM + (kk & 3) * 32;
-                            const uint32_t qoff = (kk >> 2) * C::QATOM + (kk & 3) * 32;
-                            tc_mma_ss(t_s + N * b, umma_desc_sw128(k16 + off, 16, 1024),
-                                      umma_desc_sw128(q16 + qoff, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
-                        }
-                        tc_commit(bar_s_full + 8 * b);
-                        issued = true;
-                    }
-                    __syncwarp();
+            for (int i = 0; i < T; ++i) {
+                const uint32_t tt = tcnt + i, sb = tt % C::NSB;
+                const uint32_t slot = (scnt + i) % C::NS, use = (scnt + i) / C::NS;
+                // the S buffer was read by the workers NSB tiles ago; the K stage has landed
+                if ((tt >= (uint32_t)C::NSB &&
+                     !mbar_wait_bounded(bar_s_empty + 8 * sb, ((tt / C::NSB) - 1) & 1u, kWaitLimitNs)) ||
+                    !mbar_wait_bounded(bar_k_full + 8 * slot, use & 1u, kWaitLimitNs)) {
+                    abort = true;
+                    break;
                 }
-                if (j >= 1) {
-                    const int jj = j - 1;
-                    const uint32_t tt = tcnt + jj, b = tt & 1u;
-                    if (!mbar_wait_bounded(bar_p_full + 8 * b, (tt >> 1) & 1u, kWaitLimitNs) ||
-                        !mbar_wait_bounded(bar_v16_full + 8 * b, (tt >> 1) & 1u, kWaitLimitNs) ||
-                        (jj == 0 && icnt >= 1 && !mbar_wait_bounded(bar_o_free, (icnt - 1) & 1u, kWaitLimitNs))) {
-                        abort = true;
-                        break;
-                    }
-                    tc_fence_after();
-                    if (lane == 0) {
-                        const uint32_t pt = base + C::OFF_P + b * C::P_BYTES;
-                        const uint32_t vt = base + C::OFF_V16 + b * C::F16_TILE;
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t kt = base + C::OFF_STG + slot * C::STG_BYTES;
 #pragma unroll
-                        for (int kk = 0; kk < C::BK / 16; ++kk) {
-                            const uint64_t ad = umma_desc_sw128(vt + kk * 16 * 128, C::ATOM, 1024);
-                            const uint64_t bd = umma_desc_sw128(pt + (kk >> 2) * C::PATOM + (kk & 3) * 32, 16, 1024);
-                            tc_mma_ss(t_o, ad, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
-                        }
-                        tc_commit(bar_pv_done + 8 * b);
-                    }
-                    __syncwarp();
+                    for (int term = 0; term < C::QTERMS; ++term)
+#pragma unroll
+                        for (int kk = 0; kk < C::D / 32; ++kk)
+                            tc_mma_ss_f8(t_s + N * sb, umma_desc_sw128(kt + kk * 32, 16, 1024),
+                                         umma_desc_sw128(q8 + term * C::Q8_TERM + kk * 32, 16, 1024), idesc_qk,
+                                         (term > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(bar_s_full + 8 * sb);
+                    tc_commit(bar_k_empty + 8 * slot);
+                    issued = true;
                 }
+                __syncwarp();
             }
             tcnt += T;
+            scnt += T;
             ++icnt;
             if (misc[1]) abort = true;
         }
@@ -437,16 +466,61 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
             mbar_wait_bounded(bar_final, 0, kWaitLimitNs);
         }
         __syncwarp();
+    } else if (warp == C::W_PV) {
+        // ===================================================== PV MMA issue
+        constexpr uint32_t idesc_pv = umma_idesc_f16(128, N, 1, 0);   // A = V^T (MN-major), B = P^T (K-major)
+        uint32_t tcnt = 0, icnt = 0;
+        bool issued = false;
+        for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
+            const ItemPlan it = plan_item<C, WIN>(item, p);
+            if (!it.active || !it.seq_ok || it.n_stages == 0) continue;
+            const int T = it.n_stages;
+            for (int j = 0; j < T; ++j) {
+                const uint32_t tt = tcnt + j, b = tt & 1u;
+                if (!mbar_wait_bounded(bar_p_full + 8 * b, (tt >> 1) & 1u, kWaitLimitNs) ||
+                    !mbar_wait_bounded(bar_v16_full + 8 * b, (tt >> 1) & 1u, kWaitLimitNs) ||
+                    (j == 0 && icnt >= 1 && !mbar_wait_bounded(bar_o_free, (icnt - 1) & 1u, kWaitLimitNs))) {
+                    abort = true;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t pt = base + C::OFF_P + b * C::P_BYTES;
+                    const uint32_t vt = base + C::OFF_V16 + b * C::F16_TILE;
+#pragma unroll
+                    for (int kk = 0; kk < C::BK / 16; ++kk) {
+                        const uint64_t ad = umma_desc_sw128(vt + kk * 16 * 128, C::ATOM, 1024);
+                        const uint64_t bd = umma_desc_sw128(pt + (kk >> 2) * C::PATOM + (kk & 3) * 32, 16, 1024);
+                        tc_mma_ss(t_o, ad, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(bar_pv_done + 8 * b);
+                    issued = true;
+                }
+                __syncwarp();
+            }
+            if (abort) break;
+            tcnt += T;
+            ++icnt;
+            if (misc[1]) abort = true;
+        }
+        if (lane == 0 && issued) {
+            tc_commit(bar_final + 8);
+            mbar_wait_bounded(bar_final + 8, 0, kWaitLimitNs);
+        }
+        __syncwarp();
     } else {
-        // ===================================================== workers (warps 0-7)
-        constexpr int V = C::HALF;
-        const int t = threadIdx.x;                 // 0 .. 255
+        // ===================================================== workers
+        constexpr int V = C::V;
+        constexpr int NWT = C::NWT;
+        const int t = threadIdx.x;                 // 0 .. NWT-1
         const int k = t & 127;                     // key slot / TMEM lane / head-dim element
-        const int h = t >> 7;                      // half of the query rows: rows h*V .. h*V+V-1
+        const int h = t >> 7;                      // group of the query rows: rows h*V .. h*V+V-1
         const int wq = warp & 3;                   // TMEM lane quarter
         const int col0 = h * V;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-        const uint32_t k16 = base + C::OFF_K16, v16 = base + C::OFF_V16, q16 = base + C::OFF_Q16;
+        uint8_t* const v16p = smem + C::OFF_V16;
+        uint8_t* const q8p = smem + C::OFF_Q8;
+        float* const isq = reinterpret_cast<float*>(smem + C::OFF_ISQ);
         float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
         // P^T store offsets of key slot k for the 8 swizzle phases of a row q
         uint32_t poff[8];
@@ -455,35 +529,121 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
             poff[qq] = (uint32_t)((k >> 6) * C::PATOM + ((((k & 63) >> 3) ^ qq) << 4) + (k & 7) * 2);
         uint32_t scount = 0, qcount = 0, tcnt = 0;
         // A time-out seen by this thread; published to the other workers at the
-        // next barrier they all reach, where all eight warps leave together.
+        // next barrier they all reach, where all worker warps leave together.
         bool lab = false;
-        for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
-            const ItemPlan it = plan_item<C, WIN>(item, p);
-            if (!it.active) continue;
-            if (!it.seq_ok) {
-                for (int idx = t; idx < (it.m_end - it.m0) * C::D; idx += 256) {
-                    const int m = it.m0 + idx / C::D, d = idx % C::D;
-                    const int r = m / p.ratio, hl = m - r * p.ratio;
-                    p.out[(((long long)it.g * p.rows + r) * p.n_head + it.kvh * p.ratio + hl) * C::D + d] =
-                        __float2bfloat16_rn(0.f);
+        uint32_t icnt = 0;
+        // Items that need no pipeline (an invalid sequence length: zero rows; a
+        // later split none of whose keys the tile's rows see: an empty partial)
+        // are written as they are met; returns the next item that does need it.
+        const auto next_real = [&](int item, int L_first) -> int {
+            for (; item < p.n_items; item += gridDim.x, L_first = -1) {
+                const ItemPlan it = plan_item<C, WIN>(item, p, L_first);
+                if (!it.active) continue;
+                if (!it.seq_ok) {
+                    for (int idx = t; idx < (it.m_end - it.m0) * C::D; idx += NWT) {
+                        const int m = it.m0 + idx / C::D, d = idx % C::D;
+                        const int r = m / p.ratio, hl = m - r * p.ratio;
+                        p.out[(((long long)it.g * p.rows + r) * p.n_head + it.kvh * p.ratio + hl) * C::D + d] =
+                            __float2bfloat16_rn(0.f);
+                    }
+                    if (t == 0 && p.err_word) atomicOr(p.err_word, kErrSeqLen);
+                    continue;
                 }
-                if (t == 0 && p.err_word) atomicOr(p.err_word, kErrSeqLen);
-                continue;
+                const int nrows = it.m_end - it.m0;
+                if (it.n_stages == 0) {
+                    // A later split none of whose keys this query tile's rows see
+                    // (never the tile's first split): an empty partial.
+                    const long long gq = ((long long)it.g * p.n_head_kv + it.kvh) * p.n_qtiles + it.qt;
+                    const long long slot_idx = gq * p.max_splits + it.s;
+                    float* pacc = p.part_acc + slot_idx * p.qtv * C::D;
+                    float* pml = p.part_ml + slot_idx * p.qtv * 2;
+                    for (int q = h; q < nrows; q += C::G) __stcg(pacc + q * C::D + k, 0.f);
+                    if (t < nrows) __stcg(reinterpret_cast<float2*>(pml) + t, make_float2(-CUDART_INF_F, 0.f));
+                    if (t == 0) __stcg(p.part_flag + slot_idx, 0u);
+                    continue;
+                }
+                return item;
             }
+            return p.n_items;
+        };
+        // The query rows of an item, split into e4m3 terms for its QK MMAs
+        // (the previous item's QKs are all done: its S tiles were read).
+        const auto convert_q = [&](const ItemPlan& it) {
+            const int nrows = it.m_end - it.m0;
+            {
+                if (!lab && !mbar_wait_bounded(bar_qstg_full, qcount & 1u, kWaitLimitNs)) lab = true;
+                const uint8_t* qs = smem + C::OFF_QSTG;
+                // 16 threads (a half-warp) per row, 8 head-dim elements each
+                for (int i = t; i < N * 16; i += NWT) {
+                    const int row = i >> 4, ch = i & 15;
+                    float f[8];
+                    float amax = 0.f;
+                    if (row < nrows && !lab) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(qs + row * (C::D * 2) + ch * 16);
+                        const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            f[2 * e] = bf16_lo(x[e]);
+                            f[2 * e + 1] = bf16_hi(x[e]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) f[e] = 0.f;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
+#pragma unroll
+                    for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+                    // 2^k with amax * 2^k in [128, 256): k = 7 - floor(log2 amax), kept a normal float
+                    const int ex = amax > 0.f ? (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 : 7;
+                    const int kx = max(-126, min(127, 7 - ex));
+                    const float sq = __uint_as_float((uint32_t)(kx + 127) << 23);
+                    uint32_t w[2][2];
+#pragma unroll
+                    for (int e = 0; e < 8; e += 2) {
+                        const float v0 = f[e] * sq, v1 = f[e + 1] * sq;
+                        const uint32_t hi = f32x2_to_e4m3x2(v0, v1);
+                        const float2 hv = e4m3x2_to_f32x2(hi);
+                        const uint32_t lo = f32x2_to_e4m3x2(v0 - hv.x, v1 - hv.y);
+                        const int wi = e >> 2, sh = (e & 3) * 8;
+                        if (sh == 0) {
+                            w[0][wi] = hi;
+                            w[1][wi] = lo;
+                        } else {
+                            w[0][wi] |= hi << sh;
+                            w[1][wi] |= lo << sh;
+                        }
+                    }
+                    // element 8ch of the row: 16-byte chunk ch/2 (swizzled by row & 7), byte 8 (ch & 1)
+                    const uint32_t off = row * 128 + ((((uint32_t)ch >> 1) ^ (row & 7)) << 4) + (ch & 1) * 8;
+#pragma unroll
+                    for (int term = 0; term < C::QTERMS; ++term)
+                        *reinterpret_cast<uint2*>(q8p + term * C::Q8_TERM + off) = make_uint2(w[term][0], w[term][1]);
+                    if (ch == 0) isq[row] = __uint_as_float((uint32_t)(127 - kx) << 23);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar_q8_full);
+                    mbar_arrive(bar_qstg_empty);
+                }
+                ++qcount;
+                named_barrier_sync(2, NWT);   // every row's 2^-k visible to all workers
+            }
+        };
+        int cur = next_real(blockIdx.x, -1);
+        if (cur < p.n_items) convert_q(plan_item<C, WIN>(cur, p));
+        if (lab) misc[2] = 1u;
+        named_barrier_sync(2, NWT);
+        if (misc[2]) abort = true;
+        while (cur < p.n_items && !abort) {
+            const ItemPlan it = plan_item<C, WIN>(cur, p);
             const int T = it.n_stages;
             const int nrows = it.m_end - it.m0;
-            if (T == 0) {
-                // A later split none of whose keys this query tile's rows see
-                // (never the tile's first split): an empty partial.
-                const long long gq = ((long long)it.g * p.n_head_kv + it.kvh) * p.n_qtiles + it.qt;
-                const long long slot_idx = gq * p.max_splits + it.s;
-                float* pacc = p.part_acc + slot_idx * p.qtv * C::D;
-                float* pml = p.part_ml + slot_idx * p.qtv * 2;
-                for (int q = h; q < nrows; q += 2) __stcg(pacc + q * C::D + k, 0.f);
-                if (t < nrows) __stcg(reinterpret_cast<float2*>(pml) + t, make_float2(-CUDART_INF_F, 0.f));
-                if (t == 0) __stcg(p.part_flag + slot_idx, 0u);
-                continue;
-            }
+            // the next candidate item's sequence length, loaded now and used after
+            // this item's tiles (a dependent load there stalls the item boundary)
+            const int cand = cur + gridDim.x;
+            const int L_cand = cand < p.n_items ? __ldg(p.seq_lens + item_group(cand, p)) : -1;
             uint32_t bad = 0;
             // pages the group needs that no item of this query tile loads
             if (it.s == it.s_first) {
@@ -492,41 +652,11 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                 const int tlo = it.klo / P_, thi = (it.kmax + P_ - 1) / P_, ghi = (it.L + P_ - 1) / P_;
                 const int32_t* trow = p.page_table + (long long)it.g * p.pages_per_seq;
                 const int n_below = tlo - glo;
-                for (int i = t; i < n_below + (ghi - thi); i += 256) {
+                for (int i = t; i < n_below + (ghi - thi); i += NWT) {
                     const int pi = i < n_below ? glo + i : thi + (i - n_below);
                     const int pg = __ldg(trow + pi);
                     bad |= (pg < 0 || pg >= p.num_pages) ? 1u : 0u;
                 }
-            }
-            // ---- query rows: bf16 -> f16 (exact inside the f16 range) into the B operand tile
-            {
-                if (!lab && !mbar_wait_bounded(bar_qstg_full, qcount & 1u, kWaitLimitNs)) lab = true;
-                const uint32_t qs = base + C::OFF_QSTG;
-                bool qbad = false;
-                for (int i = t; i < N * 16; i += 256) {
-                    const int row = i >> 4, ch = i & 15;   // ch: 8 head-dim elements
-                    uint32_t w[4] = {0u, 0u, 0u, 0u};
-                    if (row < nrows && !lab) {
-                        const uint4 v = lds128(qs + row * (C::D * 2) + ch * 16);
-                        const uint32_t x[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float f0 = bf16_lo(x[e]), f1 = bf16_hi(x[e]);
-                            qbad |= fabsf(f0) > 65504.f || fabsf(f1) > 65504.f;
-                            w[e] = pack_f16x2(f0, f1);
-                        }
-                    }
-                    const uint32_t dst = q16 + (ch >> 3) * C::QATOM + row * 128 + ((((uint32_t)ch & 7u) ^ (row & 7)) << 4);
-                    sts128(dst, w[0], w[1], w[2], w[3]);
-                }
-                if (qbad && p.err_word) atomicOr(p.err_word, kErrQRange);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(bar_q16_full);
-                    mbar_arrive(bar_qstg_empty);
-                }
-                ++qcount;
             }
             // ---- per query row state of this thread's half (identical across its key slots)
             float mu[V], thr[V], lsum[V];
@@ -538,24 +668,19 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
             }
             const int nk0 = it.L - p.rows + it.m0 / p.ratio + 1;                    // keys row q=0 sees
             const int klo_last = WIN ? first_visible_key(it.L, p.rows, (it.m_end - 1) / p.ratio, p.window) : 0;
-            // Staged K rows of tile i -> the f16 K tile; key k's page scales and
-            // the stage's page-id flag are read before the stage is released.
-            float kc_cur = 0.f, vs_cur = 0.f, kc_nxt = 0.f, vs_nxt = 0.f;
-            const auto load_k = [&](int i, float& kc, float& vs) {
+            // Key k's page scales of tile i and the stage's page-id flag, read
+            // before the K stage goes back to the producer (which also waits for
+            // the QK MMA that reads it).
+            float kc_cur = 0.f, vs_cur = 0.f;
+            const auto read_scales = [&](int i) {
                 const uint32_t slot = (scount + i) % C::NS, use = (scount + i) / C::NS;
                 if (!lab && !mbar_wait_bounded(bar_k_full + 8 * slot, use & 1u, kWaitLimitNs)) lab = true;
-                convert_half_row<C>(base + C::OFF_STG + slot * C::STG_BYTES, k16, k, h, lab);
                 const float* meta = reinterpret_cast<const float*>(smem + C::OFF_META + slot * C::META_STRIDE);
-                kc = p.scale_log2 * meta[k / p.page_size];
-                vs = meta[8 + k / p.page_size];
+                kc_cur = p.scale_log2 * meta[k / p.page_size];
+                vs_cur = meta[8 + k / p.page_size];
                 bad |= reinterpret_cast<const uint32_t*>(meta)[16];
-                fence_proxy_async_smem();
-                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(bar_k16_full);
-                    mbar_arrive(bar_k_empty + 8 * slot);
-                }
+                if (lane == 0) mbar_arrive(bar_k_empty + 8 * slot);
             };
             // Staged V rows of tile i -> f16 V buffer (tcnt + i) & 1, zero outside
             // the item's keys (P is 0 there; the slots may hold anything).
@@ -564,8 +689,8 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                 const uint32_t vb = (tcnt + i) & 1u;
                 if (!lab && !mbar_wait_bounded(bar_v_full + 8 * slot, use & 1u, kWaitLimitNs)) lab = true;
                 const int key = it.k0 + i * C::BK + k;
-                convert_half_row<C>(base + C::OFF_STG + slot * C::STG_BYTES + C::STG_TILE, v16 + vb * C::F16_TILE, k, h,
-                                    lab || key < it.klo || key >= it.k1);
+                convert_row_share<C>(smem + C::OFF_STG + slot * C::STG_BYTES + C::STG_TILE, v16p + vb * C::F16_TILE, k,
+                                    h, lab || key < it.klo || key >= it.k1);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
@@ -579,24 +704,35 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                 tc_fence_after();
             };
             // ---- prologue (the previous item's MMAs are all done: its epilogue waited)
-            load_k(0, kc_cur, vs_cur);
             load_v(0);
             for (int j = 0; j < T; ++j) {
-                const uint32_t tt = tcnt + j, b = tt & 1u;
+                const uint32_t tt = tcnt + j, b = tt & 1u, sb = tt % C::NSB;
                 const int kbase = it.k0 + j * C::BK;
-                // S(j) = QK(j) done: the K f16 tile is free again
-                if (!lab && !mbar_wait_bounded(bar_s_full + 8 * b, (tt >> 1) & 1u, kWaitLimitNs)) lab = true;
+                // S(j) = QK(j) done
+                if (!lab && !mbar_wait_bounded(bar_s_full + 8 * sb, (tt / C::NSB) & 1u, kWaitLimitNs)) lab = true;
                 tc_fence_after();
-                if (j + 1 < T) load_k(j + 1, kc_nxt, vs_nxt);
+                read_scales(j);
                 // ---- softmax of key kbase + k against this half's query rows
                 uint32_t sv[V];
-                tmem_ldV<V>(t_s + N * b + col0 + lane_off, sv);
+                tmem_ldV<V>(t_s + N * sb + col0 + lane_off, sv);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_s_empty + 8 * sb);
                 const float c_t = kc_cur, vs_t = vs_cur;
+                float sc[V];   // logit scale of each of this half's rows: page K scale x scale x 2^-k_row
+#pragma unroll
+                for (int q = 0; q < V; q += 4) {
+                    const float4 f = *reinterpret_cast<const float4*>(isq + col0 + q);
+                    sc[q] = c_t * f.x;
+                    sc[q + 1] = c_t * f.y;
+                    sc[q + 2] = c_t * f.z;
+                    sc[q + 3] = c_t * f.w;
+                }
                 float xs[V];
                 const bool full = kbase + C::BK <= it.k1 && kbase + C::BK <= nk0 && kbase >= klo_last;
                 if (full) {
 #pragma unroll
-                    for (int q = 0; q < V; ++q) xs[q] = __uint_as_float(sv[q]) * c_t;
+                    for (int q = 0; q < V; ++q) xs[q] = __uint_as_float(sv[q]) * sc[q];
                 } else {
                     // key is visible to row q (query row m0+q at position L-R+(m0+q)/ratio)
                     // iff qc <= q < qw; thresholds clamped to [-1, N]
@@ -610,13 +746,13 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                     const int qci = in_item ? (int)qc - col0 : V, qwi = (int)qw - col0;
 #pragma unroll
                     for (int q = 0; q < V; ++q)
-                        xs[q] = (q >= qci && q < qwi) ? __uint_as_float(sv[q]) * c_t : -CUDART_INF_F;
+                        xs[q] = (q >= qci && q < qwi) ? __uint_as_float(sv[q]) * sc[q] : -CUDART_INF_F;
                 }
                 bool trig = false;
 #pragma unroll
                 for (int q = 0; q < V; ++q) trig |= xs[q] > thr[q];
                 if (lab) misc[2] = 1u;
-                const bool any_trig = named_barrier_or(2, 256, trig);
+                const bool any_trig = named_barrier_or(2, NWT, trig);
                 if (misc[2]) {
                     abort = true;
                     break;
@@ -626,7 +762,7 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                     float v[V], mx[V];
 #pragma unroll
                     for (int q = 0; q < V; ++q) v[q] = xs[q];
-                    workers_reduce<V, true>(v, mx, red, wq, h, lane, k);
+                    workers_reduce<V, NWT, true>(v, mx, red, wq, h, lane, k);
                     float alpha[V];
                     bool moved_any = false;
 #pragma unroll
@@ -656,12 +792,12 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                 // ---- P^T[key][q] = f16(2^(x - max) * V scale), sums without the V scale;
                 // the P buffer was last read by PV(j-2)
                 if (j >= 2) wait_pv(tt - 2);
-                const uint32_t pt = base + C::OFF_P + b * C::P_BYTES;
+                uint8_t* const pt = smem + C::OFF_P + b * C::P_BYTES;
 #pragma unroll
                 for (int q = 0; q < V; ++q) {
                     const float pr = exp2f(xs[q] - mu[q]);
                     lsum[q] += pr;
-                    sts16(pt + poff[q & 7] + (col0 + q) * 128, pr * vs_t);
+                    *reinterpret_cast<__half*>(pt + poff[q & 7] + (col0 + q) * 128) = __float2half_rn(pr * vs_t);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -672,18 +808,17 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                     if (j >= 1) wait_pv(tt - 1);
                     load_v(j + 1);
                 }
-                kc_cur = kc_nxt;
-                vs_cur = vs_nxt;
             }
             if (abort) break;
-            wait_pv(tcnt + T - 1);
-            scount += T;
-            tcnt += T;
+            // ---- the next item's query rows now, so its QKs run during this epilogue
+            const int nxt = next_real(cand, L_cand);
+            if (nxt < p.n_items) convert_q(plan_item<C, WIN>(nxt, p, nxt == cand ? L_cand : -1));
             // ---- epilogue: row sums over the 128 key slots, O^T (lane k = head-dim element k)
+            wait_pv(tcnt + T - 1);
             float ltot[V];
-            workers_reduce<V, false>(lsum, ltot, red, wq, h, lane, k);
+            workers_reduce<V, NWT, false>(lsum, ltot, red, wq, h, lane, k);
             if (lab) misc[2] = 1u;
-            const bool item_bad = named_barrier_or(2, 256, bad != 0);
+            const bool item_bad = named_barrier_or(2, NWT, bad != 0);
             if (misc[2]) {
                 abort = true;
                 break;
@@ -726,6 +861,10 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                 }
                 if (t == 0) __stcg(p.part_flag + slot_idx, item_bad ? 1u : 0u);
             }
+            scount += T;
+            tcnt += T;
+            ++icnt;
+            cur = nxt;
         }
     }
     if (abort) {
@@ -735,7 +874,7 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == C::W_MMA) tmem_dealloc(tmem, C::TMEM_COLS);
+    if (warp == C::W_QK) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
 }  // namespace rad
