@@ -50,8 +50,8 @@ FALLBACK_HBM_GBS = 6800.0
 # while the kernel sources hash to `src_sha256`.
 NCU_TRAFFIC: dict[str, dict] = {
     # profiles/attn_tile_batched_decode_64seq.md: 64-sequence capture scaled by KV bytes
-    "batched_decode": {"bytes_per_launch": 4_499_400_000 + 22_500_000,
-                       "src_sha256": "968cb4f717e04b40f0059ac10e6add4d96c0d0c1419d686d4171531fab6f1809"},
+    "batched_decode": {"bytes_per_launch": 4_499_500_000 + 22_760_000,
+                       "src_sha256": "8e47937ef23adabfa3ebaf80e2da7cd566f5cdf1f98627a5af0415bad0bc2206"},
 }
 
 
@@ -388,12 +388,23 @@ def run_ours(args, rank, world, local):
         "e2e": {"value": tot_bytes / (e2e_max * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": e2e_max,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "KV pools resident (persistent state); q, page table, seq_lens in and out back per step"},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_step(w),
         "kernel": b.describe(c.rows, c.n_head, c.n_head_kv, c.head_dim, c.page_size, c.kv_dtype),
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     print(json.dumps(line), flush=True)
+
+
+def launches_per_step(w) -> int:
+    """Kernels one call launches: the attention kernel, plus the split combine
+    when a sequence of the call's capacity can span more than one split."""
+    from paged_kv_attention_02_gb300 import binding as b
+    c = w.cfg
+    desc = b.describe(c.rows, c.n_head, c.n_head_kv, c.head_dim, c.page_size, c.kv_dtype)
+    split_len = int(desc.split("split_len=")[1].split()[0])
+    combine = "attn_combine" in desc and split_len > 0 and w.pages_per_seq * c.page_size > split_len
+    return 1 + int(combine)
 
 
 def main():
