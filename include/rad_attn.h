@@ -180,6 +180,44 @@ int rad_attn_paged_window(const void* q, const void* k_pool, const void* v_pool,
                           uint32_t* err_word, rad_stream_t stream);
 
 /*
+ * rad_attn_paged_ex -- every argument of the op in one struct that grows only
+ * at its end behind `struct_size` (the ABI rule of "Radiance architecture
+ * plugins", section "Declare: drafters, encoders, generators": adding a field
+ * does not move the ABI).
+ *
+ *   struct_size  sizeof(RadAttnPagedArgs) as the caller compiled it.  It must
+ *                cover at least the fields up to err_word (the base call);
+ *                fields past it take their defaults (window = 0).  A struct
+ *                larger than this library's is accepted only when the bytes
+ *                past the fields it knows are all zero, since a non-zero
+ *                field it does not know is a switch it cannot honour
+ *                (RAD_E_ARG, nothing launched).
+ *   the fields   as in rad_attn_paged / rad_attn_paged_window.
+ * Returns the status rad_attn_paged_window returns for the same arguments.
+ */
+typedef struct RadAttnPagedArgs {
+    size_t struct_size;
+    const void* q;
+    const void* k_pool;
+    const void* v_pool;
+    const int32_t* page_table;
+    const int32_t* seq_lens;
+    int32_t groups, rows, n_head, n_head_kv, head_dim, page_size, pages_per_seq, num_pages;
+    float scale;
+    int32_t kv_dtype;
+    const float* k_scales;
+    const float* v_scales;
+    void* out;
+    void* workspace;
+    size_t workspace_bytes;
+    uint32_t* err_word;
+    /* ---- fields added after the base call (defaults when struct_size ends before them) */
+    int32_t window;   /* sliding window: each row sees its last `window` keys; 0 = none */
+} RadAttnPagedArgs;
+
+int rad_attn_paged_ex(const RadAttnPagedArgs* args, rad_stream_t stream);
+
+/*
  * rad_attn_paged_noalloc -- the same op for callers that cannot allocate.
  *
  * The pages have no counterpart to this entry point; it exists for callers

@@ -32,7 +32,19 @@ RAD_ERRW_TIMEOUT = 8
 
 EXPORTS = ("rad_attn_paged", "rad_attn_paged_workspace_bytes", "rad_attn_paged_describe",
            "rad_attn_status_string", "rad_attn_version", "rad_attn_paged_noalloc",
-           "rad_attn_paged_window")
+           "rad_attn_paged_window", "rad_attn_paged_ex")
+
+
+class RadAttnPagedArgs(ctypes.Structure):
+    """Mirror of `RadAttnPagedArgs` in include/rad_attn.h (natural C alignment)."""
+    _fields_ = [("struct_size", ctypes.c_size_t), ("q", ctypes.c_void_p), ("k_pool", ctypes.c_void_p),
+                ("v_pool", ctypes.c_void_p), ("page_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+                ("groups", ctypes.c_int32), ("rows", ctypes.c_int32), ("n_head", ctypes.c_int32),
+                ("n_head_kv", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("pages_per_seq", ctypes.c_int32), ("num_pages", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("kv_dtype", ctypes.c_int32), ("k_scales", ctypes.c_void_p), ("v_scales", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("err_word", ctypes.c_void_p), ("window", ctypes.c_int32)]
 
 # Size of the library-owned scratch of rad_attn_paged_noalloc (include/rad_attn.h).
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -70,6 +82,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.rad_attn_paged_window.restype = ctypes.c_int
     lib.rad_attn_paged_window.argtypes = [p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, i32,
                                           ctypes.c_float, i32, p, p, i32, p, p, sz, p, p]
+    lib.rad_attn_paged_ex.restype = ctypes.c_int
+    lib.rad_attn_paged_ex.argtypes = [p, p]
     lib.rad_attn_paged_noalloc.restype = ctypes.c_int
     lib.rad_attn_paged_noalloc.argtypes = [p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, i32,
                                            ctypes.c_float, i32, p, p, p, p, p]
@@ -163,6 +177,12 @@ def attn_paged_window(q, k_pool, v_pool, page_table, seq_lens, *, rows, n_head, 
     if rc != RAD_OK:
         raise RadAttnError(rc, "rad_attn_paged_window")
     return out
+
+
+def attn_paged_ex(args: RadAttnPagedArgs, stream=None) -> int:
+    """rad_attn_paged_ex on a filled RadAttnPagedArgs; returns the status
+    (callers that want an exception check it against RAD_OK)."""
+    return int(load().rad_attn_paged_ex(ctypes.byref(args), _stream_handle(stream)))
 
 
 def call_raw(q_ptr, k_ptr, v_ptr, table_ptr, lens_ptr, groups, rows, n_head, n_head_kv, head_dim,

@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <cstddef>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -203,6 +204,24 @@ int rad_attn_paged_window(const void* q, const void* k_pool, const void* v_pool,
     return attn_paged_impl(q, k_pool, v_pool, page_table, seq_lens, groups, rows, n_head, n_head_kv, head_dim,
                            page_size, pages_per_seq, num_pages, scale, kv_dtype, k_scales, v_scales, window, out,
                            workspace, workspace_bytes, err_word, stream);
+}
+
+int rad_attn_paged_ex(const RadAttnPagedArgs* a, rad_stream_t stream) {
+    if (!a) return RAD_E_ARG;
+    const size_t base = offsetof(RadAttnPagedArgs, err_word) + sizeof(a->err_word);
+    if (a->struct_size < base) return RAD_E_ARG;
+    if (a->struct_size > sizeof(RadAttnPagedArgs)) {
+        // a newer caller: the fields this library does not know must be zero
+        const unsigned char* tail = reinterpret_cast<const unsigned char*>(a) + sizeof(RadAttnPagedArgs);
+        for (size_t i = 0; i < a->struct_size - sizeof(RadAttnPagedArgs); ++i)
+            if (tail[i] != 0) return RAD_E_ARG;
+    }
+    const int32_t window =
+        a->struct_size >= offsetof(RadAttnPagedArgs, window) + sizeof(a->window) ? a->window : 0;
+    return attn_paged_impl(a->q, a->k_pool, a->v_pool, a->page_table, a->seq_lens, a->groups, a->rows, a->n_head,
+                           a->n_head_kv, a->head_dim, a->page_size, a->pages_per_seq, a->num_pages, a->scale,
+                           a->kv_dtype, a->k_scales, a->v_scales, window, a->out, a->workspace, a->workspace_bytes,
+                           a->err_word, stream);
 }
 
 }  // extern "C"

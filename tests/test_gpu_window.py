@@ -148,3 +148,47 @@ def test_negative_window_is_refused(win):
     assert e.value.status == b.RAD_E_ARG
     torch.cuda.synchronize()
     assert torch.all(canary == 5.0)
+
+
+def _ex_args(dw, window, out, ws, err, struct_size=None):
+    import ctypes
+    c = dw.w.cfg
+    a = b.RadAttnPagedArgs()
+    a.struct_size = ctypes.sizeof(b.RadAttnPagedArgs) if struct_size is None else struct_size
+    a.q, a.k_pool, a.v_pool = dw.q.data_ptr(), dw.k.data_ptr(), dw.v.data_ptr()
+    a.page_table, a.seq_lens = dw.table.data_ptr(), dw.lens.data_ptr()
+    a.groups, a.rows, a.n_head, a.n_head_kv = dw.w.groups, c.rows, c.n_head, c.n_head_kv
+    a.head_dim, a.page_size = c.head_dim, c.page_size
+    a.pages_per_seq, a.num_pages = dw.table.shape[1], dw.k.shape[0]
+    a.scale, a.kv_dtype = c.scale, c.kv_dtype
+    a.k_scales = dw.ks.data_ptr() if dw.ks is not None else None
+    a.v_scales = dw.vs.data_ptr() if dw.vs is not None else None
+    a.out, a.workspace = out.data_ptr(), ws.data_ptr()
+    a.workspace_bytes = ws.numel()
+    a.err_word = err.data_ptr()
+    a.window = window
+    return a
+
+
+@pytest.mark.parametrize("name", ["ver_fp8_w513", "dec128_w1000"])
+def test_ex_entry_equals_the_window_and_plain_calls(win, name):
+    import ctypes
+    w, dw, W = win(name)
+    c = w.cfg
+    ref, _ = dw.run(window=W)
+    need = b.workspace_bytes(w.groups, c.rows, c.n_head, c.n_head_kv, c.head_dim, c.page_size, w.pages_per_seq,
+                             c.kv_dtype)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.full_like(ref, 3.0)
+    assert b.attn_paged_ex(_ex_args(dw, W, out, ws, err)) == b.RAD_OK
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0 and np.array_equal(bits(out), bits(ref))
+    # the base call's struct (ending before `window`): no window, whatever the field holds
+    plain = DevWorkload(wl.make_workload(WIN[name][0], poison=True))
+    pref, _ = plain.run()
+    base = b.RadAttnPagedArgs.err_word.offset + ctypes.sizeof(ctypes.c_void_p)
+    out2 = torch.full_like(ref, 3.0)
+    assert b.attn_paged_ex(_ex_args(plain, 77, out2, ws, err, struct_size=base)) == b.RAD_OK
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(out2), bits(pref))

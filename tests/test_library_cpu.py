@@ -101,3 +101,43 @@ def test_describe_names_the_kernel_choice():
     assert "split_len=0" in b.describe(2048, 32, 8, 128, 16)
     with pytest.raises(b.RadAttnError):
         b.describe(1, 32, 8, 96, 16)
+
+
+def test_args_struct_matches_the_c_layout(tmp_path):
+    """The binding's RadAttnPagedArgs mirror has the header's size and offsets."""
+    fields = [f for f, _ in b.RadAttnPagedArgs._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "rad_attn.h"\nint main(void) {\n'
+                   '  printf("%zu\\n", sizeof(RadAttnPagedArgs));\n' +
+                   "".join(f'  printf("%zu\\n", offsetof(RadAttnPagedArgs, {f}));\n' for f in fields) +
+                   "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    import subprocess
+    subprocess.check_call(["gcc", "-std=c11", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)])
+    got = [int(x) for x in subprocess.check_output([str(exe)]).split()]
+    assert got[0] == ctypes.sizeof(b.RadAttnPagedArgs)
+    assert got[1:] == [getattr(b.RadAttnPagedArgs, f).offset for f in fields]
+
+
+def _ex_status(struct_size, tail=b"", groups=0):
+    """Status of rad_attn_paged_ex for an otherwise empty call (no device access)."""
+    buf = ctypes.create_string_buffer(ctypes.sizeof(b.RadAttnPagedArgs) + len(tail))
+    args = b.RadAttnPagedArgs.from_buffer(buf)
+    args.struct_size = struct_size
+    args.groups, args.rows = groups, 1
+    ctypes.memmove(ctypes.addressof(buf) + ctypes.sizeof(b.RadAttnPagedArgs), tail, len(tail))
+    return int(b.load().rad_attn_paged_ex(ctypes.byref(args), None))
+
+
+def test_ex_struct_size_rules():
+    full = ctypes.sizeof(b.RadAttnPagedArgs)
+    base = b.RadAttnPagedArgs.err_word.offset + ctypes.sizeof(ctypes.c_void_p)
+    assert int(b.load().rad_attn_paged_ex(None, None)) == b.RAD_E_ARG
+    assert _ex_status(0) == b.RAD_E_ARG
+    assert _ex_status(base - 1) == b.RAD_E_ARG
+    # the base call (no window field) and the full struct reach the scalar checks: groups = 0
+    assert _ex_status(base) == b.RAD_E_SHAPE
+    assert _ex_status(full) == b.RAD_E_SHAPE
+    # a newer caller: zero fields past the known ones are accepted, a non-zero one is refused
+    assert _ex_status(full + 8, tail=bytes(8)) == b.RAD_E_SHAPE
+    assert _ex_status(full + 8, tail=b"\0\0\0\1\0\0\0\0") == b.RAD_E_ARG
