@@ -36,6 +36,8 @@ KV_BF16 = 0
 KV_FP8_E4M3 = 1
 ERRW_SEQLEN = 1
 ERRW_PAGE = 2
+ERRW_CUSEQ = 16
+ERRW_MASK = 32
 
 _lib = None
 
@@ -62,7 +64,7 @@ def _load():
         lib.oracle_attn_paged_rows.restype = ctypes.c_int
         lib.oracle_attn_paged_rows.argtypes = [
             P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, ctypes.c_double, i32, P, P,
-            P, i64, P, P, i64, P, P, i32, i32]
+            P, i64, P, P, i64, P, P, i32, i32, P, P]
         lib.oracle_bf16_to_f64.restype = ctypes.c_double
         lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
         lib.oracle_e4m3_to_f64.restype = ctypes.c_double
@@ -102,12 +104,21 @@ def _ptr(a):
 
 def attn_paged_rows(q, k_pool, v_pool, page_table, seq_lens, *, rows, n_head, n_head_kv, head_dim,
                     page_size, scale, kv_dtype=KV_BF16, k_scales=None, v_scales=None, sel=None,
-                    want_weights=False, n_threads=0, window=0) -> OracleResult:
+                    want_weights=False, n_threads=0, window=0, cu_seqlens=None,
+                    tree_mask=None) -> OracleResult:
     """Selected output rows of the op in fp64.
 
     ``sel`` is an int array of (g, r, h) triples; ``None`` selects every row and
     returns ``out`` shaped [groups, rows, n_head, head_dim].  ``window`` > 0
     limits each row to its last ``window`` keys (0: no window).
+
+    ``cu_seqlens`` (int32 [groups + 1]) makes the rows ragged: group g has
+    cu[g+1] - cu[g] rows at q rows cu[g] .., ``q`` is [q_rows, n_head, head_dim]
+    and ``rows`` is the largest count.  The full selection then returns ``out``
+    shaped like ``q`` (rows no group names stay zero), and a group with
+    malformed entries is still touched, so that its error bit shows.
+    ``tree_mask`` (uint32, one word per q row) makes each row see the cached
+    keys plus the call's keys of its own bits (its path in a draft tree).
     """
     q = np.ascontiguousarray(q, dtype=np.uint16)
     pool_dt = np.uint16 if kv_dtype == KV_BF16 else np.uint8
@@ -122,10 +133,31 @@ def attn_paged_rows(q, k_pool, v_pool, page_table, seq_lens, *, rows, n_head, n_
         k_scales = np.ascontiguousarray(k_scales, dtype=np.float32)
     if v_scales is not None:
         v_scales = np.ascontiguousarray(v_scales, dtype=np.float32)
+    if cu_seqlens is not None:
+        cu_seqlens = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+        if cu_seqlens.shape != (groups + 1,):
+            raise OracleError("cu_seqlens needs groups + 1 entries")
+    if tree_mask is not None:
+        tree_mask = np.ascontiguousarray(tree_mask, dtype=np.uint32)
     full = sel is None
-    if full:
+    ragged_rows = None   # q row of every selected triple, ragged full selection only
+    if full and cu_seqlens is None:
         gg, rr, hh = np.meshgrid(np.arange(groups), np.arange(rows), np.arange(n_head), indexing="ij")
         sel = np.stack([gg.ravel(), rr.ravel(), hh.ravel()], axis=1)
+    elif full:
+        trip, qrow = [], []
+        for g in range(groups):
+            a, b = int(cu_seqlens[g]), int(cu_seqlens[g + 1])
+            if a < 0 or b < a or b - a > rows:
+                trip.append((g, 0, 0))       # touched for its error bit, output dropped
+                qrow.append(-1)
+                continue
+            for r in range(b - a):
+                for h in range(n_head):
+                    trip.append((g, r, h))
+                    qrow.append(a + r)
+        sel = np.array(trip, dtype=np.int32).reshape(-1, 3)
+        ragged_rows = np.array(qrow, dtype=np.int64)
     sel = np.ascontiguousarray(np.asarray(sel, dtype=np.int32).reshape(-1, 3))
     n_sel = sel.shape[0]
     out = np.zeros((n_sel, head_dim), dtype=np.float64)
@@ -140,10 +172,16 @@ def attn_paged_rows(q, k_pool, v_pool, page_table, seq_lens, *, rows, n_head, n_
         _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(seq_lens), groups, rows, n_head,
         n_head_kv, head_dim, page_size, pages_per_seq, num_pages, float(np.float32(scale)), kv_dtype,
         _ptr(k_scales), _ptr(v_scales), _ptr(sel), n_sel, _ptr(out), _ptr(weights), wstride,
-        _ptr(n_keys), ctypes.byref(err), int(n_threads), int(window))
+        _ptr(n_keys), ctypes.byref(err), int(n_threads), int(window), _ptr(cu_seqlens),
+        _ptr(tree_mask))
     if rc != 0:
         raise OracleError(f"oracle refused the call: code {rc}")
-    if full:
+    if full and ragged_rows is not None:
+        flat = np.zeros((q.shape[0], n_head, head_dim), dtype=np.float64)
+        keep = ragged_rows >= 0
+        flat[ragged_rows[keep], sel[keep, 2]] = out[keep]
+        out = flat
+    elif full:
         out = out.reshape(groups, rows, n_head, head_dim)
     return OracleResult(out=out, err_word=int(err.value), weights=weights, n_keys=n_keys)
 

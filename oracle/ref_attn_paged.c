@@ -39,6 +39,29 @@
  * bounded by a window) row r sees only the last W of those keys,
  * j = max(0, pos - W + 1) .. pos; W = 0 means no window.
  *
+ * Ragged rows ("kern manifest v7", $defs.Fill `cu_seqlens`: exclusive prefix
+ * sums of rows per sequence, groups + 1 entries; "Radiance architecture
+ * plugins", section "Step: issuing the graph": `q_lens`, `max_q_len`, and
+ * `cu_seqlens` holds absolute offsets into the token operands).  With
+ * cu_seqlens given, group g has R_g = cu[g+1] - cu[g] rows, its row r is row
+ * cu[g] + r of q (and of the output), and `rows` is the call's max_q_len.
+ * Everything above holds with R_g in place of rows.  A group with R_g == 0 has
+ * no rows and no error.  An entry with cu[g] < 0, R_g < 0 or R_g > rows makes
+ * the group's rows unknowable: error bit CUSEQ, nothing is computed for it.
+ *
+ * Tree verify ("Adding a model", step 4: forward_tree; "Radiance architecture
+ * plugins", section "Declare: drafters, encoders, generators":
+ * rad_drafter_tree, a tree over the proposals).  The call's R_g rows are the
+ * nodes of a draft tree flattened parents-first; node r's key was written at
+ * position L - R_g + r.  With tree_mask given, word tree_mask[row of node r]
+ * has bit i set iff node i is node r itself or one of its ancestors, and row
+ * r sees the cached keys 0 .. L - R_g - 1 plus the call's keys whose bit is
+ * set.  This is a decode over the path from the root to the node: the same
+ * keys, in the same order.  A chain (bits 0..r) is the causal case above.
+ * A word without bit r, or with a bit above r (a descendant), is an error:
+ * bit MASK, the group's rows are zero.  Trees hold at most 32 nodes
+ * (rows <= 32) and take no sliding window.
+ *
  * everything in IEEE double.  The softmax is the textbook one: subtract the
  * maximum, exponentiate, divide by the sum.  No tiling, no splitting, no
  * reordering beyond that definition.
@@ -48,9 +71,10 @@
  * a strided host tensor whose outermost extent is the host's page count).
  *
  * Error behaviour (mirrors the op's contract): a group whose seq_len is below
- * `rows` or above pages_per_seq*page_size, or whose visible keys name a page
- * outside [0, num_pages), gets all-zero output rows and sets a bit in the
- * returned error word.  "Zero rows is not a call" ("Radiance architecture
+ * its row count or above pages_per_seq*page_size (SEQLEN), whose visible keys
+ * name a page outside [0, num_pages) (PAGE), or whose tree mask is malformed
+ * (MASK) gets all-zero output rows and sets a bit in the returned error word;
+ * a group whose cu_seqlens entries are malformed sets CUSEQ.  "Zero rows is not a call" ("Radiance architecture
  * plugins", section "Step: issuing the graph"): rows == 0 or groups == 0
  * returns ORACLE_E_SHAPE and writes nothing.
  */
@@ -72,6 +96,8 @@
 
 #define ORACLE_ERRW_SEQLEN 1u
 #define ORACLE_ERRW_PAGE 2u
+#define ORACLE_ERRW_CUSEQ 16u
+#define ORACLE_ERRW_MASK 32u
 
 /* bfloat16: the upper 16 bits of an IEEE binary32.  Placing the bits there
  * gives the float exactly; widening to double is exact. */
@@ -113,7 +139,22 @@ typedef struct {
     const float* k_scales;
     const float* v_scales;
     int32_t window;
+    const int32_t* cu_seqlens;   /* NULL: group g has `rows` rows, q row g*rows + r */
+    const uint32_t* tree_mask;   /* NULL: causal rows */
 } oracle_call;
+
+/* Rows of group g, and the q/output row of its row 0. */
+static int64_t group_rows(const oracle_call* c, int32_t g) {
+    return c->cu_seqlens ? (int64_t)c->cu_seqlens[g + 1] - c->cu_seqlens[g] : (int64_t)c->rows;
+}
+static int64_t group_row0(const oracle_call* c, int32_t g) {
+    return c->cu_seqlens ? (int64_t)c->cu_seqlens[g] : (int64_t)g * c->rows;
+}
+static int cu_entry_ok(const oracle_call* c, int32_t g) {
+    if (!c->cu_seqlens) return 1;
+    const int64_t R = group_rows(c, g);
+    return c->cu_seqlens[g] >= 0 && R >= 0 && R <= c->rows;
+}
 
 static double pool_elem(const oracle_call* c, const void* pool, int64_t idx) {
     if (c->kv_dtype == ORACLE_KV_BF16) return oracle_bf16_to_f64(((const uint16_t*)pool)[idx]);
@@ -123,16 +164,26 @@ static double pool_elem(const oracle_call* c, const void* pool, int64_t idx) {
 /* Checks one group; returns its error bits (0 when the group is valid).  The
  * pages checked are those holding a key some row of the call may see. */
 static uint32_t group_error(const oracle_call* c, int32_t g) {
+    if (!cu_entry_ok(c, g)) return ORACLE_ERRW_CUSEQ;
+    const int64_t R = group_rows(c, g);
+    if (R == 0) return 0;                                         /* no rows: nothing to check */
     int64_t L = c->seq_lens[g];
-    if (L < c->rows || L > (int64_t)c->pages_per_seq * c->page_size) return ORACLE_ERRW_SEQLEN;
+    if (L < R || L > (int64_t)c->pages_per_seq * c->page_size) return ORACLE_ERRW_SEQLEN;
+    uint32_t e = 0;
+    if (c->tree_mask)
+        for (int64_t r = 0; r < R; ++r)
+            if ((c->tree_mask[group_row0(c, g) + r] >> r) != 1u) e |= ORACLE_ERRW_MASK;
     int64_t pages = (L + c->page_size - 1) / c->page_size;
-    const int64_t n0 = L - c->rows + 1;                           /* keys seen by row 0 */
+    const int64_t n0 = L - R + 1;                                 /* keys seen by row 0 */
     const int64_t lo = (c->window > 0 && n0 > c->window) ? n0 - c->window : 0;
     for (int64_t p = lo / c->page_size; p < pages; ++p) {
         int32_t pg = c->page_table[(int64_t)g * c->pages_per_seq + p];
-        if (pg < 0 || pg >= c->num_pages) return ORACLE_ERRW_PAGE;
+        if (pg < 0 || pg >= c->num_pages) {
+            e |= ORACLE_ERRW_PAGE;
+            break;
+        }
     }
-    return 0;
+    return e;
 }
 
 /* One output row.  `w` (optional, length >= n) receives the softmax weights. */
@@ -142,9 +193,13 @@ static void one_row(const oracle_call* c, int32_t g, int32_t r, int32_t h, doubl
     const int32_t ratio = c->n_head / c->n_head_kv;
     const int32_t kv = h / ratio;
     const int64_t L = c->seq_lens[g];
-    const int64_t n = L - c->rows + r + 1;                       /* keys 0 .. pos */
+    const int64_t R = group_rows(c, g);
+    const int64_t n = L - R + r + 1;                             /* keys 0 .. pos */
     const int64_t lo = (c->window > 0 && n > c->window) ? n - c->window : 0;   /* first visible key */
-    const uint16_t* qrow = c->q + (((int64_t)g * c->rows + r) * c->n_head + h) * D;
+    const int64_t c0 = L - R;                                    /* key of the call's row 0 */
+    const uint32_t tm = c->tree_mask ? c->tree_mask[group_row0(c, g) + r] : 0u;
+#define VISIBLE(j) ((j) >= lo && (!c->tree_mask || (j) < c0 || ((tm >> ((j) - c0)) & 1u)))
+    const uint16_t* qrow = c->q + ((group_row0(c, g) + r) * c->n_head + h) * D;
 
     double* qd = (double*)malloc(sizeof(double) * (size_t)D);
     double* s = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
@@ -152,6 +207,7 @@ static void one_row(const oracle_call* c, int32_t g, int32_t r, int32_t h, doubl
 
     double m = -INFINITY;
     for (int64_t j = lo; j < n; ++j) {
+        if (!VISIBLE(j)) continue;
         int32_t pg = c->page_table[(int64_t)g * c->pages_per_seq + j / c->page_size];
         int64_t slot = j % c->page_size;
         int64_t base = (((int64_t)pg * c->page_size + slot) * c->n_head_kv + kv) * D;
@@ -163,13 +219,15 @@ static void one_row(const oracle_call* c, int32_t g, int32_t r, int32_t h, doubl
     }
     double Z = 0.0;
     for (int64_t j = lo; j < n; ++j) {
+        if (!VISIBLE(j)) continue;
         s[j] = exp(s[j] - m);
         Z += s[j];
     }
     for (int32_t d = 0; d < D; ++d) out[d] = 0.0;
-    for (int64_t j = 0; j < lo; ++j)
+    for (int64_t j = 0; j < n; ++j)
         if (w) w[j] = 0.0;
     for (int64_t j = lo; j < n; ++j) {
+        if (!VISIBLE(j)) continue;
         double wj = s[j] / Z;
         if (w) w[j] = wj;
         int32_t pg = c->page_table[(int64_t)g * c->pages_per_seq + j / c->page_size];
@@ -181,6 +239,7 @@ static void one_row(const oracle_call* c, int32_t g, int32_t r, int32_t h, doubl
     if (n_keys_out) *n_keys_out = n;
     free(qd);
     free(s);
+#undef VISIBLE
 }
 
 static int check_call(const oracle_call* c) {
@@ -192,6 +251,8 @@ static int check_call(const oracle_call* c) {
     if (!c->q || !c->k_pool || !c->v_pool || !c->page_table || !c->seq_lens) return ORACLE_E_ARG;
     if (c->kv_dtype == ORACLE_KV_FP8_E4M3 && (!c->k_scales || !c->v_scales)) return ORACLE_E_ARG;
     if (c->window < 0) return ORACLE_E_ARG;
+    if (c->tree_mask && c->rows > 32) return ORACLE_E_SHAPE;
+    if (c->tree_mask && c->window > 0) return ORACLE_E_ARG;
     return ORACLE_OK;
 }
 
@@ -209,10 +270,11 @@ int oracle_attn_paged_rows(const uint16_t* q, const void* k_pool, const void* v_
                            int32_t kv_dtype, const float* k_scales, const float* v_scales,
                            const int32_t* sel, int64_t n_sel, double* out, double* weights,
                            int64_t weights_stride, int64_t* n_keys, uint32_t* err_word,
-                           int32_t n_threads, int32_t window) {
+                           int32_t n_threads, int32_t window, const int32_t* cu_seqlens,
+                           const uint32_t* tree_mask) {
     oracle_call c = {q, k_pool, v_pool, page_table, seq_lens, groups, rows, n_head, n_head_kv,
                      head_dim, page_size, pages_per_seq, num_pages, scale, kv_dtype, k_scales,
-                     v_scales, window};
+                     v_scales, window, cu_seqlens, tree_mask};
     int rc = check_call(&c);
     if (rc != ORACLE_OK) return rc;
     if (!sel || !out) return ORACLE_E_ARG;
@@ -220,6 +282,8 @@ int oracle_attn_paged_rows(const uint16_t* q, const void* k_pool, const void* v_
         const int32_t* t = sel + 3 * i;
         if (t[0] < 0 || t[0] >= groups || t[1] < 0 || t[1] >= rows || t[2] < 0 || t[2] >= n_head)
             return ORACLE_E_ARG;
+        /* a row past its group's count (the group's entries being valid) names nothing */
+        if (cu_entry_ok(&c, t[0]) && t[1] >= group_rows(&c, t[0])) return ORACLE_E_ARG;
     }
     uint32_t* gerr = (uint32_t*)calloc((size_t)groups, sizeof(uint32_t));
     for (int32_t g = 0; g < groups; ++g) gerr[g] = group_error(&c, g);

@@ -11,11 +11,26 @@ definition with explicit positions:
     With a sliding window W > 0 (a RAD_KV_WINDOW group, Radiance architecture
     plugins, "Declare: buffers and KV groups") it sees only keys
     max(0, position - W + 1) .. position.
+
+    Tree verify ("Adding a model", step 4: forward_tree): with parents given,
+    the call's R rows are draft-tree nodes flattened parents-first (parents[r]
+    < r, or -1 for a node hanging off the cached context), and row r sees the
+    cached keys 0 .. L - R - 1 plus the keys of the nodes on its own path to
+    the context, itself included.
 """
 import math
 
 
-def attend_sequence(q_rows, keys, values, scale, n_head_kv, window=0):
+def path_of(parents, r):
+    """Nodes from r up to the cached context, r first."""
+    path = []
+    while r >= 0:
+        path.append(r)
+        r = parents[r]
+    return path
+
+
+def attend_sequence(q_rows, keys, values, scale, n_head_kv, window=0, parents=None):
     """q_rows: [R][H][D] floats; keys/values: [L][Hkv][D] floats.
 
     Returns out [R][H][D] as floats.
@@ -29,6 +44,8 @@ def attend_sequence(q_rows, keys, values, scale, n_head_kv, window=0):
         position = L - R + r
         first = max(0, position - window + 1) if window > 0 else 0
         visible = range(first, position + 1)
+        if parents is not None:
+            visible = list(range(L - R)) + sorted(L - R + i for i in path_of(parents, r))
         row_out = []
         for h in range(H):
             kvh = h // group
