@@ -94,9 +94,10 @@ enum { RAD_KV_BF16 = 0, RAD_KV_FP8_E4M3 = 1 };
 
 /* Device-side error bits, OR-ed into *err_word by the kernel ("kern manifest
  * v7", $defs.Fill `error`: a one-word error flag read after every call;
- * nonzero is a failed step).  A group that raises RAD_ERRW_SEQLEN or
- * RAD_ERRW_PAGE gets all-zero output rows; the other groups are unaffected.
- * No out-of-bounds access happens in either case. */
+ * nonzero is a failed step).  A group that raises RAD_ERRW_SEQLEN,
+ * RAD_ERRW_PAGE or RAD_ERRW_MASK gets all-zero output rows; one that raises
+ * RAD_ERRW_CUSEQ gets none written (its rows are unknown); the other groups
+ * are unaffected.  No out-of-bounds access happens in any case. */
 enum {
     RAD_ERRW_SEQLEN = 1u,  /* seq_lens[g] < rows or > pages_per_seq*page_size */
     RAD_ERRW_PAGE = 2u,    /* a page id the group needs is outside [0, num_pages) */
@@ -104,8 +105,12 @@ enum {
                               the f16 range (|q| > 65504) -- that row's output
                               is not meaningful (head_dim 128 carries q exactly
                               and never raises it) */
-    RAD_ERRW_TIMEOUT = 8u  /* an internal wait ran past its time limit; the
+    RAD_ERRW_TIMEOUT = 8u, /* an internal wait ran past its time limit; the
                               affected outputs are not meaningful */
+    RAD_ERRW_CUSEQ = 16u,  /* ragged rows: cu_seqlens[g] < 0, cu_seqlens[g+1] <
+                              cu_seqlens[g], or more rows than `rows` */
+    RAD_ERRW_MASK = 32u    /* tree rows: a mask word without its own row's bit,
+                              or with the bit of a later row */
 };
 
 /*
@@ -187,13 +192,50 @@ int rad_attn_paged_window(const void* q, const void* k_pool, const void* v_pool,
  *
  *   struct_size  sizeof(RadAttnPagedArgs) as the caller compiled it.  It must
  *                cover at least the fields up to err_word (the base call);
- *                fields past it take their defaults (window = 0).  A struct
- *                larger than this library's is accepted only when the bytes
- *                past the fields it knows are all zero, since a non-zero
- *                field it does not know is a switch it cannot honour
- *                (RAD_E_ARG, nothing launched).
- *   the fields   as in rad_attn_paged / rad_attn_paged_window.
- * Returns the status rad_attn_paged_window returns for the same arguments.
+ *                fields past it take their defaults (window = 0, no
+ *                cu_seqlens, no tree_mask).  A struct larger than this
+ *                library's is accepted only when the bytes past the fields
+ *                it knows are all zero, since a non-zero field it does not
+ *                know is a switch it cannot honour (RAD_E_ARG, nothing
+ *                launched).
+ *   the fields   as in rad_attn_paged / rad_attn_paged_window, and:
+ *
+ *   cu_seqlens   ragged rows ("kern manifest v7", $defs.Fill `cu_seqlens`:
+ *                exclusive prefix sums of rows per sequence, groups + 1
+ *                entries; "Radiance architecture plugins", section "Step:
+ *                issuing the graph": `q_lens`, `max_q_len`, and the offsets
+ *                are absolute into the token operands).  Device int32
+ *                [groups + 1], or NULL for `rows` rows per group.  Group g
+ *                then has R_g = cu[g+1] - cu[g] rows; its row r is row
+ *                cu[g] + r of q and of out (both [*][n_head][head_dim]), sits
+ *                at position seq_lens[g] - R_g + r and sees keys up to it.
+ *                `rows` is the call's largest R_g (max_q_len): it picks the
+ *                kernel and sizes the workspace.  A group with R_g = 0 is
+ *                skipped; out rows that no group names are not written.
+ *                Entries with cu[g] < 0, R_g < 0 or R_g > rows raise
+ *                RAD_ERRW_CUSEQ for the group.  Offsets are read on the
+ *                device; the caller guarantees that q and out hold every row
+ *                they name.
+ *   tree_mask    tree verify ("Adding a model", step 4: forward_tree;
+ *                "Radiance architecture plugins", section "Declare:
+ *                drafters, encoders, generators": a tree over the
+ *                proposals).  Device uint32, one word per q row (indexed like
+ *                q's rows), or NULL for causal rows.  A group's R_g rows are
+ *                the nodes of a draft tree flattened parents-first, node r's
+ *                K/V written at position seq_lens[g] - R_g + r; bit i of node
+ *                r's word is set iff node i is r or one of its ancestors.
+ *                Row r sees every key below the call's first position plus
+ *                the call's keys whose bits are set: a decode over its path.
+ *                A chain (bits 0..r) gives the causal call's bits exactly.
+ *                Words must hold their own bit and no later node's
+ *                (RAD_ERRW_MASK otherwise).  Requires rows <= 32
+ *                (RAD_E_SHAPE) and window == 0 (RAD_E_ARG).
+ *
+ * Calls with cu_seqlens or tree_mask run on the mma.sync tile kernels only;
+ * their workspace need is rad_attn_paged_ex_workspace_bytes(args), which may
+ * differ from rad_attn_paged_workspace_bytes() of the same shape.
+ * Returns the status rad_attn_paged_window returns for the same arguments,
+ * RAD_E_ARG for a cu_seqlens or tree_mask pointer not 4-byte aligned.
  */
 typedef struct RadAttnPagedArgs {
     size_t struct_size;
@@ -212,10 +254,17 @@ typedef struct RadAttnPagedArgs {
     size_t workspace_bytes;
     uint32_t* err_word;
     /* ---- fields added after the base call (defaults when struct_size ends before them) */
-    int32_t window;   /* sliding window: each row sees its last `window` keys; 0 = none */
+    int32_t window;                /* sliding window: each row sees its last `window` keys; 0 = none */
+    const int32_t* cu_seqlens;     /* ragged rows: [groups + 1] absolute row offsets; NULL = `rows` each */
+    const uint32_t* tree_mask;     /* tree rows: one word per q row; NULL = causal */
 } RadAttnPagedArgs;
 
 int rad_attn_paged_ex(const RadAttnPagedArgs* args, rad_stream_t stream);
+
+/* Bytes of workspace rad_attn_paged_ex needs for these arguments (pointers
+ * are not read; only their presence counts).  0 for arguments it would
+ * refuse on shape, dtype or struct_size. */
+size_t rad_attn_paged_ex_workspace_bytes(const RadAttnPagedArgs* args);
 
 /*
  * rad_attn_paged_noalloc -- the same op for callers that cannot allocate.

@@ -29,10 +29,12 @@ RAD_ERRW_SEQLEN = 1
 RAD_ERRW_PAGE = 2
 RAD_ERRW_QRANGE = 4
 RAD_ERRW_TIMEOUT = 8
+RAD_ERRW_CUSEQ = 16
+RAD_ERRW_MASK = 32
 
 EXPORTS = ("rad_attn_paged", "rad_attn_paged_workspace_bytes", "rad_attn_paged_describe",
            "rad_attn_status_string", "rad_attn_version", "rad_attn_paged_noalloc",
-           "rad_attn_paged_window", "rad_attn_paged_ex")
+           "rad_attn_paged_window", "rad_attn_paged_ex", "rad_attn_paged_ex_workspace_bytes")
 
 
 class RadAttnPagedArgs(ctypes.Structure):
@@ -44,7 +46,8 @@ class RadAttnPagedArgs(ctypes.Structure):
                 ("pages_per_seq", ctypes.c_int32), ("num_pages", ctypes.c_int32), ("scale", ctypes.c_float),
                 ("kv_dtype", ctypes.c_int32), ("k_scales", ctypes.c_void_p), ("v_scales", ctypes.c_void_p),
                 ("out", ctypes.c_void_p), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
-                ("err_word", ctypes.c_void_p), ("window", ctypes.c_int32)]
+                ("err_word", ctypes.c_void_p), ("window", ctypes.c_int32), ("cu_seqlens", ctypes.c_void_p),
+                ("tree_mask", ctypes.c_void_p)]
 
 # Size of the library-owned scratch of rad_attn_paged_noalloc (include/rad_attn.h).
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -84,6 +87,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                           ctypes.c_float, i32, p, p, i32, p, p, sz, p, p]
     lib.rad_attn_paged_ex.restype = ctypes.c_int
     lib.rad_attn_paged_ex.argtypes = [p, p]
+    lib.rad_attn_paged_ex_workspace_bytes.restype = sz
+    lib.rad_attn_paged_ex_workspace_bytes.argtypes = [p]
     lib.rad_attn_paged_noalloc.restype = ctypes.c_int
     lib.rad_attn_paged_noalloc.argtypes = [p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, i32,
                                            ctypes.c_float, i32, p, p, p, p, p]
@@ -183,6 +188,51 @@ def attn_paged_ex(args: RadAttnPagedArgs, stream=None) -> int:
     """rad_attn_paged_ex on a filled RadAttnPagedArgs; returns the status
     (callers that want an exception check it against RAD_OK)."""
     return int(load().rad_attn_paged_ex(ctypes.byref(args), _stream_handle(stream)))
+
+
+def ex_workspace_bytes(args: RadAttnPagedArgs) -> int:
+    return int(load().rad_attn_paged_ex_workspace_bytes(ctypes.byref(args)))
+
+
+def attn_paged_general(q, k_pool, v_pool, page_table, seq_lens, *, rows, n_head, n_head_kv, head_dim,
+                       page_size, scale, kv_dtype=RAD_KV_BF16, k_scales=None, v_scales=None,
+                       cu_seqlens=None, tree_mask=None, window=0, out=None, workspace=None,
+                       err_word=None, stream=None):
+    """The op through rad_attn_paged_ex with every optional field.
+
+    cu_seqlens: int32 [groups + 1] absolute row offsets (ragged rows; ``rows``
+    is then the largest count and q is [q_rows, n_head, head_dim]); tree_mask:
+    uint32 words (as int32) indexed like q's rows (draft-tree rows); window:
+    sliding window.  Without cu_seqlens q is [groups, rows, n_head, head_dim].
+    Returns `out` (allocated like q when None; rows no group names are not
+    written).
+    """
+    groups = int(seq_lens.shape[0])
+    if out is None:
+        out = torch.empty(tuple(q.shape), dtype=torch.bfloat16, device=q.device)
+    a = RadAttnPagedArgs()
+    a.struct_size = ctypes.sizeof(RadAttnPagedArgs)
+    a.q, a.k_pool, a.v_pool = q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr()
+    a.page_table, a.seq_lens = page_table.data_ptr(), seq_lens.data_ptr()
+    a.groups, a.rows, a.n_head, a.n_head_kv, a.head_dim = groups, rows, n_head, n_head_kv, head_dim
+    a.page_size, a.pages_per_seq, a.num_pages = page_size, int(page_table.shape[1]), int(k_pool.shape[0])
+    a.scale, a.kv_dtype = float(scale), kv_dtype
+    a.k_scales = None if k_scales is None else k_scales.data_ptr()
+    a.v_scales = None if v_scales is None else v_scales.data_ptr()
+    a.cu_seqlens = None if cu_seqlens is None else cu_seqlens.data_ptr()
+    a.tree_mask = None if tree_mask is None else tree_mask.data_ptr()
+    a.window = int(window)
+    a.out = out.data_ptr()
+    need = ex_workspace_bytes(a)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    a.workspace = None if workspace is None else workspace.data_ptr()
+    a.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    a.err_word = None if err_word is None else err_word.data_ptr()
+    rc = attn_paged_ex(a, stream)
+    if rc != RAD_OK:
+        raise RadAttnError(rc, "rad_attn_paged_ex")
+    return out
 
 
 def call_raw(q_ptr, k_ptr, v_ptr, table_ptr, lens_ptr, groups, rows, n_head, n_head_kv, head_dim,

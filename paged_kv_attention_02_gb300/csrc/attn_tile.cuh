@@ -61,6 +61,14 @@ constexpr uint32_t kErrSeqLen = 1u;
 constexpr uint32_t kErrPage = 2u;
 constexpr uint32_t kErrQRange = 4u;
 constexpr uint32_t kErrTimeout = 8u;
+constexpr uint32_t kErrCuSeq = 16u;
+constexpr uint32_t kErrMask = 32u;
+
+// Row-visibility modes of the tile kernel: causal rows, causal rows with a
+// sliding window, or draft-tree rows (a per-row mask over the call's keys).
+constexpr int kModeCausal = 0;
+constexpr int kModeWindow = 1;
+constexpr int kModeTree = 2;
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
@@ -84,8 +92,10 @@ struct AttnParams {
     float* part_ml;        // [slots][qtv][2]  (max in log2 units, sum)
     uint32_t* part_flag;   // [slots]         page-id error seen by the split
     uint32_t* err_word;    // optional
-    int groups, rows, n_head, n_head_kv, ratio, page_size, pages_per_seq, num_pages;
-    int M;                 // rows * ratio: query rows per KV head
+    const int32_t* cu_seqlens;   // [groups + 1] absolute q row offsets, or null: `rows` rows per group
+    const uint32_t* tree_mask;   // one word per q row (bit i: sees the call's key i), or null: causal
+    int groups, rows, n_head, n_head_kv, ratio, page_size, pages_per_seq, num_pages;   // rows: max per group
+    int M;                 // rows * ratio: query rows per KV head (the most of any group)
     int n_qtiles;          // ceil(M / QT)
     int qtv;               // query rows stored per partial slot: min(M, QT)
     int qt_rows;           // QT of the split kernel's tile
@@ -103,6 +113,27 @@ struct AttnParams {
 __device__ __forceinline__ int first_visible_key(int L, int rows, int r, int window) {
     const int n = L - rows + r + 1;   // keys 0 .. n-1 are causal for row r
     return (window > 0 && n > window) ? n - window : 0;
+}
+
+// Rows of group g and the q/output row of its row 0.  Without cu_seqlens every
+// group has `rows` rows at g*rows; with it ("kern manifest v7", $defs.Fill
+// `cu_seqlens`: exclusive prefix sums of rows per sequence, absolute offsets)
+// group g has cu[g+1] - cu[g].  Returns false for entries that name no valid
+// row range (a negative offset or count, or more rows than the call's most).
+struct GroupRows {
+    long long row0;
+    int n;
+};
+__device__ __forceinline__ bool group_rows(const AttnParams& p, int g, GroupRows& gr) {
+    if (!p.cu_seqlens) {
+        gr.row0 = (long long)g * p.rows;
+        gr.n = p.rows;
+        return true;
+    }
+    const int a = __ldg(p.cu_seqlens + g), b = __ldg(p.cu_seqlens + g + 1);
+    gr.row0 = a;
+    gr.n = b - a;
+    return a >= 0 && b >= a && b - a <= p.rows;
 }
 
 template <int D_, bool FP8_, int WQ_, int NQW_, int WK_, int KS_, int NS_, int MINB_ = 1>
@@ -170,6 +201,9 @@ __device__ __forceinline__ uint32_t kv_off(int key, int d, int lp) {
 struct ItemPlan {
     int s, g, kvh, qt;
     int L;
+    long long qrow0;   // q/output row of the group's row 0
+    int qlen;          // the group's rows
+    bool cu_ok;        // the group's cu_seqlens entries are valid
     bool seq_ok;
     bool active;
     int n_splits;      // splits of the sequence, ceil(L / split_len)
@@ -202,22 +236,35 @@ __device__ __forceinline__ ItemPlan plan_item(int item, const AttnParams& p, int
     it.kvh = rem2 / p.n_qtiles;
     it.qt = rem2 - it.kvh * p.n_qtiles;
     if (p.split_len == 0) it.qt = p.n_qtiles - 1 - it.qt;   // causal: later tiles see more keys
+    GroupRows gr;
+    it.cu_ok = group_rows(p, it.g, gr);
+    it.qrow0 = gr.row0;
+    it.qlen = gr.n;
     it.L = L_known >= 0 ? L_known : __ldg(p.seq_lens + it.g);
-    it.seq_ok = it.L >= p.rows && (long long)it.L <= (long long)p.pages_per_seq * p.page_size;
+    it.seq_ok = it.cu_ok && it.L >= it.qlen && (long long)it.L <= (long long)p.pages_per_seq * p.page_size;
     it.m0 = it.qt * C::QT;
-    it.m_end = min(p.M, it.m0 + C::QT);
+    it.m_end = it.cu_ok ? min(it.qlen * p.ratio, it.m0 + C::QT) : it.m0;
     it.k0 = it.k1 = 0;
     it.n_stages = 0;
     it.n_splits = 1;
     it.s_first = 0;
     it.klo = it.kmax = 0;
+    if (!it.cu_ok) {
+        // malformed offsets: one item of the group raises the error bit, no row is written
+        it.active = (it.s == 0 && it.kvh == 0 && it.qt == 0);
+        return it;
+    }
+    if (it.m_end <= it.m0) {   // no row of the group in this query tile
+        it.active = false;
+        return it;
+    }
     if (!it.seq_ok) {
         it.active = (it.s == 0);
         return it;
     }
     const int r_last = (it.m_end - 1) / p.ratio;
-    it.kmax = it.L - p.rows + r_last + 1;
-    it.klo = WIN ? first_visible_key(it.L, p.rows, it.m0 / p.ratio, p.window) : 0;
+    it.kmax = it.L - it.qlen + r_last + 1;
+    it.klo = WIN ? first_visible_key(it.L, it.qlen, it.m0 / p.ratio, p.window) : 0;
     // Stages start on absolute multiples of KS (split_len is one too), so a
     // key falls in the same sub-tile, and goes to the same key warp, whatever
     // the tile's first visible key: rows of different calls at one position
@@ -259,8 +306,10 @@ __device__ __forceinline__ int d_of(int mt, int row16) {
     }
 }
 
-template <class C, bool WIN>
+template <class C, int MODE>
 __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const __grid_constant__ AttnParams p) {
+    constexpr bool WIN = MODE == kModeWindow;
+    constexpr bool TREE = MODE == kModeTree;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t base = (raw_addr + 127u) & ~127u;
@@ -285,6 +334,7 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
             mbar_init(bar_qempty + 8 * i, C::NCW);
         }
         misc[0] = 0;  // abort flag (set by any warp that timed out)
+        misc[1] = 0;  // error bits of the current item (RAD_ERRW_* values)
         fence_mbarrier_init();
     }
     __syncthreads();
@@ -318,7 +368,7 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
                     const int m = it.m0 + i;
                     const int r = m / p.ratio, hl = m - r * p.ratio;
                     const __nv_bfloat16* src =
-                        p.q + (((long long)it.g * p.rows + r) * p.n_head + it.kvh * p.ratio + hl) * C::D;
+                        p.q + ((it.qrow0 + r) * p.n_head + it.kvh * p.ratio + hl) * C::D;
                     bulk_load(qdst + i * C::D * 2, src, C::D * 2, bar_qfull + 8 * slot);
                 }
                 ++qcount;
@@ -392,7 +442,7 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
                             meta[i] = kss[i];
                             meta[4 + i] = vss[i];
                         }
-                        reinterpret_cast<uint32_t*>(meta)[8] = bad_any;
+                        reinterpret_cast<uint32_t*>(meta)[8] = bad_any ? kErrPage : 0u;
                         mbar_arrive(bar_full + 8 * slot);
                     }
                 }
@@ -427,20 +477,23 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
         if (!it.active) continue;
         if (!it.seq_ok) {
             // Invalid length: this group's rows become zeros (the split-0 items
-            // of every query tile write them).
+            // of every query tile write them).  Malformed cu_seqlens entries
+            // name no rows: only the error bit.
             for (int idx = tid; idx < (it.m_end - it.m0) * C::D; idx += C::NCT) {
                 const int m = it.m0 + idx / C::D, d = idx % C::D;
                 const int r = m / p.ratio, hl = m - r * p.ratio;
-                p.out[(((long long)it.g * p.rows + r) * p.n_head + it.kvh * p.ratio + hl) * C::D + d] =
-                    __float2bfloat16_rn(0.f);
+                p.out[((it.qrow0 + r) * p.n_head + it.kvh * p.ratio + hl) * C::D + d] = __float2bfloat16_rn(0.f);
             }
-            if (tid == 0 && p.err_word) atomicOr(p.err_word, kErrSeqLen);
+            if (tid == 0 && p.err_word) atomicOr(p.err_word, it.cu_ok ? kErrSeqLen : kErrCuSeq);
             continue;
         }
 
         // ---- query fragments (B operand of S^T = K Q^T), one per n-tile and k-step
         uint32_t qb[C::NQW][C::D / 16][2];
         int nk[C::NQW][2];   // a column sees keys nk - wlim .. nk - 1 (and none below 0)
+        // tree rows: bit i set iff the column sees key nk - 1 - i (its own path
+        // among the call's keys, every cached key below them)
+        uint32_t amask[C::NQW][2];
         {
             const uint32_t slot = qcount & 1u, use = qcount >> 1;
             if (!mbar_wait_bounded(bar_qfull + 8 * slot, use & 1u, kWaitLimitNs)) abort = true;
@@ -475,7 +528,14 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     const int m = it.m0 + lane_col<C>(wq, j, t4, c);
-                    nk[j][c] = (m < it.m_end) ? it.L - p.rows + m / p.ratio + 1 : 0;
+                    const int r = m / p.ratio;
+                    nk[j][c] = (m < it.m_end) ? it.L - it.qlen + r + 1 : 0;
+                    amask[j][c] = 0u;
+                    if (TREE && m < it.m_end) {
+                        // word bit i (the call's key i) -> bit r - i; bits past r are cached keys
+                        const uint32_t w = __ldg(p.tree_mask + it.qrow0 + r);
+                        amask[j][c] = (__brev(w) >> (31 - r)) | (r < 31 ? ~0u << (r + 1) : 0u);
+                    }
                 }
             }
             if (C::FP8 && qrange_bad && p.err_word) atomicOr(p.err_word, kErrQRange);
@@ -495,20 +555,27 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
 #pragma unroll
                 for (int e = 0; e < 4; ++e) oacc[j][mt][e] = 0.f;
         }
-        uint32_t bad = 0;
+        uint32_t bad = 0;   // RAD_ERRW_* bits seen by this thread
+        // Every item checks all mask words of its group (at most 32), so every
+        // row of a group with a malformed word is zero: a word must hold its
+        // own row's bit and no later row's.
+        if (TREE && tid < it.qlen) {
+            const uint32_t w = __ldg(p.tree_mask + it.qrow0 + tid);
+            if ((w >> tid) != 1u) bad |= kErrMask;
+        }
         // Pages the group needs that no item of this tile loads (below the
         // tile's window, or past its last row's keys) are checked by the
         // tile's first item, so every row of a group with a bad page is zero.
         if (it.s == it.s_first) {
             const int P_ = p.page_size;
-            const int glo = WIN ? first_visible_key(it.L, p.rows, 0, p.window) / P_ : 0;
+            const int glo = WIN ? first_visible_key(it.L, it.qlen, 0, p.window) / P_ : 0;
             const int tlo = it.klo / P_, thi = (it.kmax + P_ - 1) / P_, ghi = (it.L + P_ - 1) / P_;
             const int32_t* trow = p.page_table + (long long)it.g * p.pages_per_seq;
             const int n_below = tlo - glo;
             for (int i = tid; i < n_below + (ghi - thi); i += C::NCT) {
                 const int pi = i < n_below ? glo + i : thi + (i - n_below);
                 const int pg = __ldg(trow + pi);
-                bad |= (pg < 0 || pg >= p.num_pages) ? 1u : 0u;
+                bad |= (pg < 0 || pg >= p.num_pages) ? kErrPage : 0u;
             }
         }
         const int P = p.page_size;
@@ -590,7 +657,13 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int key = key0 + g8 + ((e >> 1) << 3);
-                        const bool in = WIN ? (uint32_t)(nk[j][e & 1] - 1 - key) < wlim : key < nk[j][e & 1];
+                        bool in;
+                        if constexpr (TREE) {
+                            const uint32_t du = (uint32_t)(nk[j][e & 1] - 1 - key);   // distance back from the row
+                            in = du < 32u ? ((amask[j][e & 1] >> du) & 1u) != 0u : du < 0x80000000u;
+                        } else {
+                            in = WIN ? (uint32_t)(nk[j][e & 1] - 1 - key) < wlim : key < nk[j][e & 1];
+                        }
                         x[e] = in ? sacc[j][e] * kfac : -CUDART_INF_F;
                     }
                     // The running max moves only when a sub-tile's max exceeds it by
@@ -759,7 +832,9 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
         }
         // Stage-meta `bad` words were OR-ed per warp; make them CTA-wide (this
         // barrier also orders the published states before their reads).
+        if (bad) atomicOr(const_cast<uint32_t*>(misc + 1), bad);
         const bool item_bad = named_barrier_or(1, C::NCT, bad != 0);
+        const uint32_t bad_bits = item_bad ? misc[1] : 0u;
 
         // one split holding visible keys: the row is written here, else partials
         const bool final_write = (p.split_len == 0) || it.n_splits - it.s_first == 1;
@@ -825,14 +900,13 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
                     const float4 v = *reinterpret_cast<const float4*>(mrg + col * C::MSTRIDE + 4 * d4);
                     const int m = it.m0 + col;
                     const int r = m / p.ratio, hl = m - r * p.ratio;
-                    __nv_bfloat16* o =
-                        p.out + (((long long)it.g * p.rows + r) * p.n_head + it.kvh * p.ratio + hl) * C::D + 4 * d4;
+                    __nv_bfloat16* o = p.out + ((it.qrow0 + r) * p.n_head + it.kvh * p.ratio + hl) * C::D + 4 * d4;
                     uint2 w;
                     w.x = pack_bf16x2(v.x, v.y);
                     w.y = pack_bf16x2(v.z, v.w);
                     *reinterpret_cast<uint2*>(o) = w;
                 }
-                if (item_bad && tid == 0 && p.err_word) atomicOr(p.err_word, kErrPage);
+                if (item_bad && tid == 0 && p.err_word) atomicOr(p.err_word, bad_bits);
             } else {
                 const long long gq = ((long long)it.g * p.n_head_kv + it.kvh) * p.n_qtiles + it.qt;
                 const long long slot_idx = gq * p.max_splits + it.s;
@@ -845,11 +919,12 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
                 }
                 for (int col = tid; col < ncols; col += C::NCT)
                     __stcg(reinterpret_cast<float2*>(pml) + col, mlfin[col]);
-                if (tid == 0) __stcg(p.part_flag + slot_idx, item_bad ? 1u : 0u);
+                if (tid == 0) __stcg(p.part_flag + slot_idx, bad_bits);
             }
         }
-        // the merge buffers are rewritten by the next item
+        // the merge buffers (and the error word) are rewritten by the next item
         named_barrier_sync(1, C::NCT);
+        if (tid == 0 && item_bad) misc[1] = 0u;
     }
     if (abort) {
         misc[0] = 1;

@@ -32,6 +32,7 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __g
     __shared__ float ml_s[CH * CG * 2];
     __shared__ float w_s[CH * CG];
     __shared__ float st_m[CG], st_l[CG], st_a[CG];
+    __shared__ uint32_t bad_bits;
 
     const int n_cg = (p.qt_rows + CG - 1) / CG;
     const int cgi = blockIdx.x % n_cg;
@@ -39,13 +40,17 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __g
     const int qt = gq % p.n_qtiles;
     const int kvh = (gq / p.n_qtiles) % p.n_head_kv;
     const int g = gq / (p.n_qtiles * p.n_head_kv);
+    GroupRows gr;
+    if (!group_rows(p, g, gr)) return;                                                // no rows named
     const int L = __ldg(p.seq_lens + g);
-    if (L < p.rows || (long long)L > (long long)p.pages_per_seq * p.page_size) return;  // zeros already written
+    if (L < gr.n || (long long)L > (long long)p.pages_per_seq * p.page_size) return;  // zeros already written
     const int ns = (L + p.split_len - 1) / p.split_len;
     const int t_m0 = qt * p.qt_rows;
-    const int s_first = first_visible_key(L, p.rows, t_m0 / p.ratio, p.window) / p.split_len;
+    const int g_m = gr.n * p.ratio;                                                   // the group's query rows
+    if (t_m0 >= g_m) return;
+    const int s_first = first_visible_key(L, gr.n, t_m0 / p.ratio, p.window) / p.split_len;
     if (ns - s_first <= 1) return;                                                    // written directly
-    const int t_ncol = min(p.M, t_m0 + p.qt_rows) - t_m0;
+    const int t_ncol = min(g_m, t_m0 + p.qt_rows) - t_m0;
     const int c0 = cgi * CG;
     const int ncol = min(CG, t_ncol - c0);
     if (ncol <= 0) return;
@@ -56,6 +61,7 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __g
         st_m[tid] = -CUDART_INF_F;
         st_l[tid] = 0.f;
     }
+    if (tid == 0) bad_bits = 0u;
     float4 acc[OWN];
 #pragma unroll
     for (int k = 0; k < OWN; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -123,6 +129,7 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __g
             }
         }
     }
+    if (any_bad) atomicOr(&bad_bits, any_bad);
     const bool bad = __syncthreads_or(any_bad != 0);
 #pragma unroll
     for (int k = 0; k < OWN; ++k) {
@@ -132,14 +139,14 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __g
             const float inv = bad ? 0.f : 1.f / st_l[col];
             const int m = t_m0 + c0 + col;
             const int r = m / p.ratio, hl = m - r * p.ratio;
-            __nv_bfloat16* o =
-                p.out + (((long long)g * p.rows + r) * p.n_head + kvh * p.ratio + hl) * D + 4 * d4;
+            __nv_bfloat16* o = p.out + ((gr.row0 + r) * p.n_head + kvh * p.ratio + hl) * D + 4 * d4;
             const float4 a = bad ? make_float4(0.f, 0.f, 0.f, 0.f) : acc[k];
             *reinterpret_cast<__nv_bfloat162*>(o) = __floats2bfloat162_rn(a.x * inv, a.y * inv);
             *reinterpret_cast<__nv_bfloat162*>(o + 2) = __floats2bfloat162_rn(a.z * inv, a.w * inv);
         }
     }
-    if (bad && tid == 0 && cgi == 0 && p.err_word) atomicOr(p.err_word, kErrPage);
+    // the partials' flags hold the RAD_ERRW_* bits their items saw
+    if (bad && tid == 0 && cgi == 0 && p.err_word) atomicOr(p.err_word, bad_bits);
 }
 
 }  // namespace rad

@@ -9,10 +9,13 @@ namespace rad {
 
 // Persistent launch: as many CTAs as fit on the device at once (never more
 // than there are work items).  Calls with a sliding window run the kernel
-// built with the window terms, others the one without.
+// built with the window terms, calls with tree masks the one with the mask
+// test, others the plain causal one.
 template <class C>
 cudaError_t launch_cfg(const AttnParams& p, int sms, cudaStream_t st) {
-    auto kern = p.window > 0 ? attn_tile_kernel<C, true> : attn_tile_kernel<C, false>;
+    auto kern = p.window > 0  ? attn_tile_kernel<C, kModeWindow>
+                : p.tree_mask ? attn_tile_kernel<C, kModeTree>
+                              : attn_tile_kernel<C, kModeCausal>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     int per_sm = 0;

@@ -69,8 +69,10 @@ bool use_prefill_tc(int32_t rows, int32_t ratio, int32_t head_dim, int32_t kv_dt
            128 % ratio == 0;
 }
 
+// `general`: a call with ragged rows (cu_seqlens) or tree masks, which only
+// the tile kernels take.
 Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_dim,
-               int32_t page_size, int32_t pages_per_seq, int32_t kv_dtype) {
+               int32_t page_size, int32_t pages_per_seq, int32_t kv_dtype, bool general = false) {
     Plan pl{};
     pl.ratio = n_head / n_head_kv;
     pl.M = rows * pl.ratio;
@@ -79,12 +81,13 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
     // share one key schedule.  Longer calls: the tcgen05 prefill kernel where
     // it applies, else the wide tile.
     pl.split_len = rows <= rad::kSplitMaxRows ? rad::kSplitLen : 0;
-    if (pl.split_len > 0 && RAD_SPLIT_TC05 && head_dim == 128 && kv_dtype == RAD_KV_FP8_E4M3)
+    if (pl.split_len > 0 && RAD_SPLIT_TC05 && !general && head_dim == 128 && kv_dtype == RAD_KV_FP8_E4M3)
         pl.family = rad::kFamSplitTC;
     else if (pl.split_len > 0)
         pl.family = pl.M <= 8 ? rad::kFamDecode : rad::kFamVerify;
     else
-        pl.family = use_prefill_tc(rows, pl.ratio, head_dim, kv_dtype) ? rad::kFamPrefillTC : rad::kFamWide;
+        pl.family = !general && use_prefill_tc(rows, pl.ratio, head_dim, kv_dtype) ? rad::kFamPrefillTC
+                                                                                   : rad::kFamWide;
     if (pl.family == rad::kFamPrefillTC)
         pl.tile = rad::TileInfo{128, 0, 4, 0, 0, rad::PrefillTileKeys, RAD_PREFILL_NS, 128, 192, 0, RAD_PREFILL_CTAS};
     else if (pl.family == rad::kFamSplitTC)
@@ -167,8 +170,29 @@ int device_info(int* dev_out, int* sms_out) {
 int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const int32_t* page_table,
                     const int32_t* seq_lens, int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv,
                     int32_t head_dim, int32_t page_size, int32_t pages_per_seq, int32_t num_pages, float scale,
-                    int32_t kv_dtype, const float* k_scales, const float* v_scales, int32_t window, void* out,
-                    void* workspace, size_t workspace_bytes, uint32_t* err_word, rad_stream_t stream);
+                    int32_t kv_dtype, const float* k_scales, const float* v_scales, int32_t window,
+                    const int32_t* cu_seqlens, const uint32_t* tree_mask, void* out, void* workspace,
+                    size_t workspace_bytes, uint32_t* err_word, rad_stream_t stream);
+
+// Fields of a RadAttnPagedArgs that an older caller's struct_size leaves out read as zero.
+template <class T>
+T ex_field(const RadAttnPagedArgs* a, const T RadAttnPagedArgs::*field, size_t offset) {
+    return a->struct_size >= offset + sizeof(T) ? a->*field : T{};
+}
+
+// Common struct_size rules of the ex entry points: RAD_OK, or RAD_E_ARG.
+int check_ex_struct(const RadAttnPagedArgs* a) {
+    if (!a) return RAD_E_ARG;
+    const size_t base = offsetof(RadAttnPagedArgs, err_word) + sizeof(a->err_word);
+    if (a->struct_size < base) return RAD_E_ARG;
+    if (a->struct_size > sizeof(RadAttnPagedArgs)) {
+        // a newer caller: the fields this library does not know must be zero
+        const unsigned char* tail = reinterpret_cast<const unsigned char*>(a) + sizeof(RadAttnPagedArgs);
+        for (size_t i = 0; i < a->struct_size - sizeof(RadAttnPagedArgs); ++i)
+            if (tail[i] != 0) return RAD_E_ARG;
+    }
+    return RAD_OK;
+}
 
 }  // namespace
 
@@ -191,8 +215,8 @@ int rad_attn_paged(const void* q, const void* k_pool, const void* v_pool, const 
                    const float* v_scales, void* out, void* workspace, size_t workspace_bytes,
                    uint32_t* err_word, rad_stream_t stream) {
     return attn_paged_impl(q, k_pool, v_pool, page_table, seq_lens, groups, rows, n_head, n_head_kv, head_dim,
-                           page_size, pages_per_seq, num_pages, scale, kv_dtype, k_scales, v_scales, 0, out,
-                           workspace, workspace_bytes, err_word, stream);
+                           page_size, pages_per_seq, num_pages, scale, kv_dtype, k_scales, v_scales, 0, nullptr,
+                           nullptr, out, workspace, workspace_bytes, err_word, stream);
 }
 
 int rad_attn_paged_window(const void* q, const void* k_pool, const void* v_pool, const int32_t* page_table,
@@ -202,26 +226,32 @@ int rad_attn_paged_window(const void* q, const void* k_pool, const void* v_pool,
                           const float* v_scales, int32_t window, void* out, void* workspace,
                           size_t workspace_bytes, uint32_t* err_word, rad_stream_t stream) {
     return attn_paged_impl(q, k_pool, v_pool, page_table, seq_lens, groups, rows, n_head, n_head_kv, head_dim,
-                           page_size, pages_per_seq, num_pages, scale, kv_dtype, k_scales, v_scales, window, out,
-                           workspace, workspace_bytes, err_word, stream);
+                           page_size, pages_per_seq, num_pages, scale, kv_dtype, k_scales, v_scales, window,
+                           nullptr, nullptr, out, workspace, workspace_bytes, err_word, stream);
 }
 
 int rad_attn_paged_ex(const RadAttnPagedArgs* a, rad_stream_t stream) {
-    if (!a) return RAD_E_ARG;
-    const size_t base = offsetof(RadAttnPagedArgs, err_word) + sizeof(a->err_word);
-    if (a->struct_size < base) return RAD_E_ARG;
-    if (a->struct_size > sizeof(RadAttnPagedArgs)) {
-        // a newer caller: the fields this library does not know must be zero
-        const unsigned char* tail = reinterpret_cast<const unsigned char*>(a) + sizeof(RadAttnPagedArgs);
-        for (size_t i = 0; i < a->struct_size - sizeof(RadAttnPagedArgs); ++i)
-            if (tail[i] != 0) return RAD_E_ARG;
-    }
-    const int32_t window =
-        a->struct_size >= offsetof(RadAttnPagedArgs, window) + sizeof(a->window) ? a->window : 0;
+    const int rc = check_ex_struct(a);
+    if (rc != RAD_OK) return rc;
+    const int32_t window = ex_field(a, &RadAttnPagedArgs::window, offsetof(RadAttnPagedArgs, window));
+    const int32_t* cu = ex_field(a, &RadAttnPagedArgs::cu_seqlens, offsetof(RadAttnPagedArgs, cu_seqlens));
+    const uint32_t* tm = ex_field(a, &RadAttnPagedArgs::tree_mask, offsetof(RadAttnPagedArgs, tree_mask));
     return attn_paged_impl(a->q, a->k_pool, a->v_pool, a->page_table, a->seq_lens, a->groups, a->rows, a->n_head,
                            a->n_head_kv, a->head_dim, a->page_size, a->pages_per_seq, a->num_pages, a->scale,
-                           a->kv_dtype, a->k_scales, a->v_scales, window, a->out, a->workspace, a->workspace_bytes,
-                           a->err_word, stream);
+                           a->kv_dtype, a->k_scales, a->v_scales, window, cu, tm, a->out, a->workspace,
+                           a->workspace_bytes, a->err_word, stream);
+}
+
+size_t rad_attn_paged_ex_workspace_bytes(const RadAttnPagedArgs* a) {
+    if (check_ex_struct(a) != RAD_OK) return 0;
+    if (check_scalars(a->groups, a->rows, a->n_head, a->n_head_kv, a->head_dim, a->page_size, a->pages_per_seq,
+                      a->kv_dtype) != RAD_OK)
+        return 0;
+    const bool general = ex_field(a, &RadAttnPagedArgs::cu_seqlens, offsetof(RadAttnPagedArgs, cu_seqlens)) ||
+                         ex_field(a, &RadAttnPagedArgs::tree_mask, offsetof(RadAttnPagedArgs, tree_mask));
+    return make_plan(a->groups, a->rows, a->n_head, a->n_head_kv, a->head_dim, a->page_size, a->pages_per_seq,
+                     a->kv_dtype, general)
+        .total_bytes;
 }
 
 }  // extern "C"
@@ -231,23 +261,26 @@ namespace {
 int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const int32_t* page_table,
                     const int32_t* seq_lens, int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv,
                     int32_t head_dim, int32_t page_size, int32_t pages_per_seq, int32_t num_pages, float scale,
-                    int32_t kv_dtype, const float* k_scales, const float* v_scales, int32_t window, void* out,
-                    void* workspace, size_t workspace_bytes, uint32_t* err_word, rad_stream_t stream) {
+                    int32_t kv_dtype, const float* k_scales, const float* v_scales, int32_t window,
+                    const int32_t* cu_seqlens, const uint32_t* tree_mask, void* out, void* workspace,
+                    size_t workspace_bytes, uint32_t* err_word, rad_stream_t stream) {
     int rc = check_scalars(groups, rows, n_head, n_head_kv, head_dim, page_size, pages_per_seq, kv_dtype);
     if (rc != RAD_OK) return rc;
     if (num_pages <= 0 || (long long)num_pages * page_size > 0x7FFFFFFFll) return RAD_E_SHAPE;
-    if (make_plan(groups, rows, n_head, n_head_kv, head_dim, page_size, pages_per_seq, kv_dtype).n_items >
-        0x7FFFFFFFll)
-        return RAD_E_SHAPE;
+    if (tree_mask && rows > 32) return RAD_E_SHAPE;   // a mask word covers 32 nodes
+    const bool general = cu_seqlens || tree_mask;
+    const Plan pl = make_plan(groups, rows, n_head, n_head_kv, head_dim, page_size, pages_per_seq, kv_dtype, general);
+    if (pl.n_items > 0x7FFFFFFFll) return RAD_E_SHAPE;
     if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !out) return RAD_E_ARG;
     if (!is_aligned(q, 16) || !is_aligned(k_pool, 16) || !is_aligned(v_pool, 16) || !is_aligned(out, 16) ||
-        !is_aligned(page_table, 4) || !is_aligned(seq_lens, 4) || !is_aligned(err_word, 4))
+        !is_aligned(page_table, 4) || !is_aligned(seq_lens, 4) || !is_aligned(err_word, 4) ||
+        !is_aligned(cu_seqlens, 4) || !is_aligned(tree_mask, 4))
         return RAD_E_ARG;
     const bool fp8 = kv_dtype == RAD_KV_FP8_E4M3;
     if (fp8 && (!k_scales || !v_scales || !is_aligned(k_scales, 4) || !is_aligned(v_scales, 4)))
         return RAD_E_ARG;
     if (!std::isfinite(scale) || window < 0) return RAD_E_ARG;
-    const Plan pl = make_plan(groups, rows, n_head, n_head_kv, head_dim, page_size, pages_per_seq, kv_dtype);
+    if (tree_mask && window > 0) return RAD_E_ARG;    // tree rows take no sliding window
     if (pl.total_bytes > 0 && (!workspace || workspace_bytes < pl.total_bytes || !is_aligned(workspace, 256)))
         return RAD_E_WORKSPACE;
 
@@ -265,6 +298,8 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
     p.v_scales = fp8 ? v_scales : nullptr;
     p.out = static_cast<__nv_bfloat16*>(out);
     p.err_word = err_word;
+    p.cu_seqlens = cu_seqlens;
+    p.tree_mask = tree_mask;
     p.groups = groups;
     p.rows = rows;
     p.n_head = n_head;

@@ -859,7 +859,7 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                                    make_float2(ltot[q] == 0.f ? -CUDART_INF_F : mu[q], ltot[q]));
                     }
                 }
-                if (t == 0) __stcg(p.part_flag + slot_idx, item_bad ? 1u : 0u);
+                if (t == 0) __stcg(p.part_flag + slot_idx, item_bad ? kErrPage : 0u);
             }
             scount += T;
             tcnt += T;

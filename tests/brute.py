@@ -20,14 +20,7 @@ definition with explicit positions:
 """
 import math
 
-
-def path_of(parents, r):
-    """Nodes from r up to the cached context, r first."""
-    path = []
-    while r >= 0:
-        path.append(r)
-        r = parents[r]
-    return path
+from trees import path_of
 
 
 def attend_sequence(q_rows, keys, values, scale, n_head_kv, window=0, parents=None):

@@ -8,6 +8,9 @@ from paged_kv_attention_02_gb300 import workloads as wl
 
 # Tolerances: bf16 pools -- max |gpu - ref| <= 1e-2 and, per element,
 # |gpu - ref| / max(|ref|, 1e-2) <= 2e-2; fp8 pools -- max |gpu - ref| <= 4e-2.
+# The output is bf16, so no kernel can return ref itself: the absolute bounds
+# count the error beyond the rounding of ref to the nearest bf16 (at most half
+# a bf16 ulp, 2^-9 |ref|), which past |ref| = 4 alone can exceed 1e-2.
 BF16_ABS, BF16_REL, REL_FLOOR, FP8_ABS = 1e-2, 2e-2, 1e-2, 4e-2
 
 
@@ -63,15 +66,23 @@ def oracle_rows(w: wl.Workload, sel=None, window=0, scale=None, page_table=None)
                                   **args)
 
 
+def bf16_rounding(ref: np.ndarray) -> np.ndarray:
+    """|bf16_rne(ref) - ref|: the part of any bf16 output's error that comes
+    from the output format alone."""
+    r = torch.from_numpy(np.ascontiguousarray(ref, dtype=np.float64))
+    return (r.to(torch.bfloat16).to(torch.float64) - r).abs().numpy()
+
+
 def assert_parity(gpu: np.ndarray, ref: np.ndarray, fp8: bool, what=""):
     assert gpu.shape == ref.shape, what
     assert np.all(np.isfinite(gpu)), f"{what}: non-finite GPU output"
     d = np.abs(gpu - ref)
+    excess = d - bf16_rounding(ref)   # error beyond the output's own rounding
     if fp8:
-        assert d.max() <= FP8_ABS, f"{what}: max abs {d.max():.3e} > {FP8_ABS}"
+        assert excess.max() <= FP8_ABS, f"{what}: max abs {d.max():.3e} (beyond bf16 rounding {excess.max():.3e}) > {FP8_ABS}"
     else:
         rel = d / np.maximum(np.abs(ref), REL_FLOOR)
-        assert d.max() <= BF16_ABS, f"{what}: max abs {d.max():.3e} > {BF16_ABS}"
+        assert excess.max() <= BF16_ABS, f"{what}: max abs {d.max():.3e} (beyond bf16 rounding {excess.max():.3e}) > {BF16_ABS}"
         assert rel.max() <= BF16_REL, f"{what}: max rel {rel.max():.3e} > {BF16_REL}"
 
 

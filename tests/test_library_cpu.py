@@ -141,3 +141,44 @@ def test_ex_struct_size_rules():
     # a newer caller: zero fields past the known ones are accepted, a non-zero one is refused
     assert _ex_status(full + 8, tail=bytes(8)) == b.RAD_E_SHAPE
     assert _ex_status(full + 8, tail=b"\0\0\0\1\0\0\0\0") == b.RAD_E_ARG
+
+
+def _general_args(rows=8, cu=0, tree=0, window=0, head_dim=128, kv_dtype=b.RAD_KV_BF16):
+    """A filled RadAttnPagedArgs with fake (aligned, never dereferenced) pointers."""
+    a = b.RadAttnPagedArgs()
+    a.struct_size = ctypes.sizeof(b.RadAttnPagedArgs)
+    fake = 1 << 20
+    a.q = a.k_pool = a.v_pool = a.out = fake
+    a.page_table = a.seq_lens = a.k_scales = a.v_scales = fake
+    a.groups, a.rows, a.n_head, a.n_head_kv, a.head_dim = 4, rows, 32, 8, head_dim
+    a.page_size, a.pages_per_seq, a.num_pages, a.scale, a.kv_dtype = 16, 64, 256, 0.08, kv_dtype
+    a.cu_seqlens, a.tree_mask, a.window = cu or None, tree or None, window
+    return a
+
+
+def test_ragged_and_tree_calls_the_host_refuses_before_any_device_access():
+    fake = 1 << 20
+    st = lambda a: int(b.load().rad_attn_paged_ex(ctypes.byref(a), None))
+    assert st(_general_args(tree=fake, window=4)) == b.RAD_E_ARG        # tree rows take no window
+    assert st(_general_args(rows=33, tree=fake)) == b.RAD_E_SHAPE       # a mask word covers 32 nodes
+    assert st(_general_args(cu=fake + 2)) == b.RAD_E_ARG                # offsets not 4-byte aligned
+    assert st(_general_args(tree=fake + 1)) == b.RAD_E_ARG              # mask words not 4-byte aligned
+    assert st(_general_args(cu=fake, tree=fake, rows=0)) == b.RAD_E_SHAPE   # zero rows is not a call
+
+
+def test_ex_workspace_follows_the_kernel_the_call_takes():
+    fake = 1 << 20
+    ws = lambda a: b.ex_workspace_bytes(a)
+    for hd, dt in ((128, b.RAD_KV_BF16), (256, b.RAD_KV_FP8_E4M3), (128, b.RAD_KV_FP8_E4M3)):
+        a = _general_args(head_dim=hd, kv_dtype=dt)
+        assert ws(a) == b.workspace_bytes(4, 8, 32, 8, hd, 16, 64, dt) > 0
+    # fp8 head_dim 128 verify: the uniform call runs the tcgen05 split kernel,
+    # a ragged or tree call the verify tile; both split, with their own tiles
+    assert ws(_general_args(cu=fake, kv_dtype=b.RAD_KV_FP8_E4M3)) > 0
+    assert ws(_general_args(cu=fake, kv_dtype=b.RAD_KV_FP8_E4M3)) == \
+        ws(_general_args(tree=fake, kv_dtype=b.RAD_KV_FP8_E4M3))
+    # chunks past the split limit need none, on either path
+    assert ws(_general_args(rows=300, cu=fake)) == 0 == b.workspace_bytes(4, 300, 32, 8, 128, 16, 64)
+    bad = _general_args()
+    bad.struct_size = 8
+    assert ws(bad) == 0

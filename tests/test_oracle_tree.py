@@ -17,19 +17,9 @@ import numpy as np
 import pytest
 
 import oracle
-from brute import attend_sequence, path_of
+from brute import attend_sequence
 from test_oracle import bf16_bits, bf16_values, e4m3_values, paged_from_logical, random_case, run_oracle
-
-
-def mask_words(parents):
-    """Tree-mask word of every node: bit i for each node on its path."""
-    return np.array([sum(1 << i for i in path_of(parents, r)) for r in range(len(parents))],
-                    dtype=np.uint32)
-
-
-def random_parents(rng, R, forest=True):
-    lo = -1 if forest else 0
-    return [-1] + [int(rng.integers(lo, r)) for r in range(1, R)]
+from trees import mask_words, path_of, random_parents
 
 
 def logical_kv(c, g, P, fp8):
