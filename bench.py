@@ -194,9 +194,16 @@ def hbm_peak():
 def time_oracle(w: wl.Workload, groups_idx) -> tuple[float, int]:
     import oracle
     sub = w.select_groups(groups_idx)
+    extra = {}
+    q = sub.q
+    if sub.ragged:
+        q, cu, mask = sub.packed()
+        extra = dict(cu_seqlens=cu, tree_mask=mask)
+    elif sub.tree_mask is not None:
+        extra = dict(tree_mask=sub.tree_mask)
     t0 = time.perf_counter()
-    oracle.attn_paged_rows(sub.q, sub.k_pool, sub.v_pool, sub.page_table, sub.seq_lens,
-                           k_scales=sub.k_scales, v_scales=sub.v_scales, **sub.call_args())
+    oracle.attn_paged_rows(q, sub.k_pool, sub.v_pool, sub.page_table, sub.seq_lens,
+                           k_scales=sub.k_scales, v_scales=sub.v_scales, **extra, **sub.call_args())
     return time.perf_counter() - t0, wl.kv_bytes(sub)
 
 
@@ -246,7 +253,9 @@ def run_reference(args, rank, world):
 # ---------------------------------------------------------------- GPU arm
 def workload_config(w: wl.Workload) -> dict:
     c = w.cfg
-    return {"workload": f"{c.name}: {w.groups} seqs x rows={c.rows}, n_head={c.n_head}, "
+    rows = f"rows {c.q_lens} (ragged, cu_seqlens)" if c.q_lens else f"rows={c.rows}"
+    tree = f", {'ragged ' if c.q_lens else ''}draft trees (random forests, tree_mask)" if c.tree else ""
+    return {"workload": f"{c.name}: {w.groups} seqs x {rows}{tree}, n_head={c.n_head}, "
                         f"n_head_kv={c.n_head_kv}, head_dim={c.head_dim}, page_size={c.page_size}, "
                         f"ctx {c.lens}, {'fp8-e4m3' if c.kv_dtype else 'bf16'} KV, seed {c.seed}",
             "groups": w.groups, "rows": c.rows, "n_head": c.n_head, "n_head_kv": c.n_head_kv,
@@ -275,21 +284,37 @@ def run_ours(args, rank, world, local):
             t = t.view(torch.int16).view(torch.bfloat16)
         return t.to(dev)
 
-    q = to_dev(w.q.view(np.int16), True)
+    # ragged and tree calls go through rad_attn_paged_ex with their offsets / mask words
+    general = w.ragged or w.tree_mask is not None
+    q_np, cu_np, mask_np = w.q, None, None
+    if w.ragged:
+        q_np, cu_np, mask_np = w.packed()
+    elif w.tree_mask is not None:
+        mask_np = w.tree_mask.reshape(-1)
+    q = to_dev(q_np.view(np.int16), True)
+    cu = None if cu_np is None else to_dev(cu_np)
+    mask = None if mask_np is None else to_dev(mask_np.view(np.int32))
+    total_rows = int(q_np.shape[0]) if w.ragged else 0
     k = to_dev(w.k_pool) if fp8 else to_dev(w.k_pool.view(np.int16), True)
     v = to_dev(w.v_pool) if fp8 else to_dev(w.v_pool.view(np.int16), True)
     ks = to_dev(w.k_scales) if fp8 else None
     vs = to_dev(w.v_scales) if fp8 else None
     table = to_dev(w.page_table)
     lens = to_dev(w.seq_lens)
-    out = torch.empty((w.groups, c.rows, c.n_head, c.head_dim), dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(max(1, b.workspace_bytes(w.groups, c.rows, c.n_head, c.n_head_kv, c.head_dim,
-                                               c.page_size, w.pages_per_seq, c.kv_dtype)),
-                     dtype=torch.uint8, device=dev)
+    out = torch.empty(tuple(q.shape), dtype=torch.bfloat16, device=dev)
+    shape = b.shape_args(w.groups, c.rows, c.n_head, c.n_head_kv, c.head_dim, c.page_size, w.pages_per_seq,
+                         c.kv_dtype, ragged=w.ragged, tree=w.tree_mask is not None, total_rows=total_rows)
+    ws = torch.empty(max(1, b.ex_workspace_bytes(shape)), dtype=torch.uint8, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
-    def call(qq=q, tt=table, ll=lens, oo=out):
+    def call(qq=q, tt=table, ll=lens, oo=out, cc=cu, mm=mask):
+        if general:
+            b.attn_paged_general(qq, k, v, tt, ll, rows=c.rows, n_head=c.n_head, n_head_kv=c.n_head_kv,
+                                 head_dim=c.head_dim, page_size=c.page_size, scale=c.scale, kv_dtype=c.kv_dtype,
+                                 k_scales=ks, v_scales=vs, cu_seqlens=cc, tree_mask=mm, total_rows=total_rows,
+                                 out=oo, workspace=ws, err_word=err, stream=stream)
+            return
         b.attn_paged(qq, k, v, tt, ll, rows=c.rows, n_head=c.n_head, n_head_kv=c.n_head_kv,
                      head_dim=c.head_dim, page_size=c.page_size, scale=c.scale, kv_dtype=c.kv_dtype,
                      k_scales=ks, v_scales=vs, out=oo, workspace=ws, err_word=err, stream=stream)
@@ -329,17 +354,26 @@ def run_ours(args, rank, world, local):
     assert int(err.item()) == 0
 
     # ---- end to end: per-step inputs from pinned host memory, result back to host
-    q_h = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16).pin_memory()
+    q_h = torch.from_numpy(q_np.view(np.int16)).view(torch.bfloat16).pin_memory()
     t_h = torch.from_numpy(w.page_table).pin_memory()
     l_h = torch.from_numpy(w.seq_lens).pin_memory()
     o_h = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
     q_d, t_d, l_d = torch.empty_like(q), torch.empty_like(table), torch.empty_like(lens)
+    # per-step row offsets and mask words travel with the step's other inputs
+    c_h = None if cu is None else torch.from_numpy(cu_np).pin_memory()
+    m_h = None if mask is None else torch.from_numpy(mask_np.view(np.int32)).pin_memory()
+    c_d = None if cu is None else torch.empty_like(cu)
+    m_d = None if mask is None else torch.empty_like(mask)
 
     def e2e_step():
         q_d.copy_(q_h, non_blocking=True)
         t_d.copy_(t_h, non_blocking=True)
         l_d.copy_(l_h, non_blocking=True)
-        call(q_d, t_d, l_d, out)
+        if c_d is not None:
+            c_d.copy_(c_h, non_blocking=True)
+        if m_d is not None:
+            m_d.copy_(m_h, non_blocking=True)
+        call(q_d, t_d, l_d, out, c_d, m_d)
         o_h.copy_(out, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -357,6 +391,7 @@ def run_ours(args, rank, world, local):
     barrier(world)
     e2e_ms = e0.elapsed_time(e1) / args.steps
     h2d = q_h.numel() * 2 + t_h.numel() * 4 + l_h.numel() * 4
+    h2d += (0 if c_h is None else c_h.numel() * 4) + (0 if m_h is None else m_h.numel() * 4)
     d2h = o_h.numel() * 2
 
     nbytes = wl.kv_bytes(w)
@@ -365,7 +400,7 @@ def run_ours(args, rank, world, local):
     e2e_max = reduce_max(e2e_ms, world)
     tot_bytes = reduce_sum(float(nbytes), world)
     tot_tokens = reduce_sum(float(tokens), world)
-    tot_rows = reduce_sum(float(w.groups * c.rows), world)
+    tot_rows = reduce_sum(float(w.rows_of().sum()), world)
     if rank != 0:
         return
     value = tot_bytes / (ms_max * 1e-3) / 1e9
@@ -389,22 +424,31 @@ def run_ours(args, rank, world, local):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "KV pools resident (persistent state); q, page table, seq_lens in and out back per step"},
         "gpu_launches": args.steps * launches_per_step(w),
-        "kernel": b.describe(c.rows, c.n_head, c.n_head_kv, c.head_dim, c.page_size, c.kv_dtype),
+        "kernel": describe(w),
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     print(json.dumps(line), flush=True)
 
 
-def launches_per_step(w) -> int:
-    """Kernels one call launches: the attention kernel, plus the split combine
-    when a sequence of the call's capacity can span more than one split."""
+def describe(w) -> str:
+    """The library's description of the kernels a call of this workload runs."""
     from paged_kv_attention_02_gb300 import binding as b
     c = w.cfg
-    desc = b.describe(c.rows, c.n_head, c.n_head_kv, c.head_dim, c.page_size, c.kv_dtype)
+    return b.ex_describe(b.shape_args(w.groups, c.rows, c.n_head, c.n_head_kv, c.head_dim, c.page_size,
+                                      w.pages_per_seq, c.kv_dtype, ragged=w.ragged,
+                                      tree=w.tree_mask is not None))
+
+
+def launches_per_step(w) -> int:
+    """Kernels one call launches: the attention kernel, plus the split combine
+    when a sequence of the call's capacity can span more than one split, plus
+    the tile map of a ragged call."""
+    c = w.cfg
+    desc = describe(w)
     split_len = int(desc.split("split_len=")[1].split()[0])
     combine = "attn_combine" in desc and split_len > 0 and w.pages_per_seq * c.page_size > split_len
-    return 1 + int(combine)
+    return 1 + int(combine) + int("ragged_tile_map" in desc)
 
 
 def main():

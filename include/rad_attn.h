@@ -230,6 +230,17 @@ int rad_attn_paged_window(const void* q, const void* k_pool, const void* v_pool,
  *                Words must hold their own bit and no later node's
  *                (RAD_ERRW_MASK otherwise).  Requires rows <= 32
  *                (RAD_E_SHAPE) and window == 0 (RAD_E_ARG).
+ *   total_rows   ragged rows: an upper bound on the call's rows, cu[groups]
+ *                - cu[0] (RadBatch `n_tok`, "Radiance architecture plugins",
+ *                section "Step: issuing the graph"), known to the host that
+ *                built the batch.  The work and the workspace of a ragged
+ *                call run over its query tiles, at most
+ *                ceil(total_rows * n_head/n_head_kv / tile rows) + groups
+ *                of them; 0 sizes them for `rows` rows per sequence
+ *                instead.  A call whose offsets hold more rows than the
+ *                bound raises RAD_ERRW_CUSEQ and leaves the rows past it
+ *                unwritten.  Negative: RAD_E_ARG.  A ragged call first runs a
+ *                small kernel that maps its query tiles into the workspace.
  *
  * Calls with cu_seqlens or tree_mask run on the mma.sync tile kernels only;
  * their workspace need is rad_attn_paged_ex_workspace_bytes(args), which may
@@ -257,6 +268,7 @@ typedef struct RadAttnPagedArgs {
     int32_t window;                /* sliding window: each row sees its last `window` keys; 0 = none */
     const int32_t* cu_seqlens;     /* ragged rows: [groups + 1] absolute row offsets; NULL = `rows` each */
     const uint32_t* tree_mask;     /* tree rows: one word per q row; NULL = causal */
+    int32_t total_rows;            /* ragged rows: bound on cu[groups] - cu[0]; 0 = unknown */
 } RadAttnPagedArgs;
 
 int rad_attn_paged_ex(const RadAttnPagedArgs* args, rad_stream_t stream);
@@ -265,6 +277,11 @@ int rad_attn_paged_ex(const RadAttnPagedArgs* args, rad_stream_t stream);
  * are not read; only their presence counts).  0 for arguments it would
  * refuse on shape, dtype or struct_size. */
 size_t rad_attn_paged_ex_workspace_bytes(const RadAttnPagedArgs* args);
+
+/* rad_attn_paged_describe for the call these arguments make (the kernels of
+ * a ragged or tree call differ from the uniform call's).  Pointers are not
+ * read; only their presence counts.  Same buffer rules and results. */
+int rad_attn_paged_ex_describe(const RadAttnPagedArgs* args, char* buf, size_t buf_len);
 
 /*
  * rad_attn_paged_noalloc -- the same op for callers that cannot allocate.

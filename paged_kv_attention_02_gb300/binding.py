@@ -34,7 +34,8 @@ RAD_ERRW_MASK = 32
 
 EXPORTS = ("rad_attn_paged", "rad_attn_paged_workspace_bytes", "rad_attn_paged_describe",
            "rad_attn_status_string", "rad_attn_version", "rad_attn_paged_noalloc",
-           "rad_attn_paged_window", "rad_attn_paged_ex", "rad_attn_paged_ex_workspace_bytes")
+           "rad_attn_paged_window", "rad_attn_paged_ex", "rad_attn_paged_ex_workspace_bytes",
+           "rad_attn_paged_ex_describe")
 
 
 class RadAttnPagedArgs(ctypes.Structure):
@@ -47,7 +48,7 @@ class RadAttnPagedArgs(ctypes.Structure):
                 ("kv_dtype", ctypes.c_int32), ("k_scales", ctypes.c_void_p), ("v_scales", ctypes.c_void_p),
                 ("out", ctypes.c_void_p), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
                 ("err_word", ctypes.c_void_p), ("window", ctypes.c_int32), ("cu_seqlens", ctypes.c_void_p),
-                ("tree_mask", ctypes.c_void_p)]
+                ("tree_mask", ctypes.c_void_p), ("total_rows", ctypes.c_int32)]
 
 # Size of the library-owned scratch of rad_attn_paged_noalloc (include/rad_attn.h).
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -89,6 +90,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.rad_attn_paged_ex.argtypes = [p, p]
     lib.rad_attn_paged_ex_workspace_bytes.restype = sz
     lib.rad_attn_paged_ex_workspace_bytes.argtypes = [p]
+    lib.rad_attn_paged_ex_describe.restype = ctypes.c_int
+    lib.rad_attn_paged_ex_describe.argtypes = [p, ctypes.c_char_p, sz]
     lib.rad_attn_paged_noalloc.restype = ctypes.c_int
     lib.rad_attn_paged_noalloc.argtypes = [p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, i32,
                                            ctypes.c_float, i32, p, p, p, p, p]
@@ -194,18 +197,41 @@ def ex_workspace_bytes(args: RadAttnPagedArgs) -> int:
     return int(load().rad_attn_paged_ex_workspace_bytes(ctypes.byref(args)))
 
 
+def shape_args(groups, rows, n_head, n_head_kv, head_dim, page_size, pages_per_seq, kv_dtype=RAD_KV_BF16,
+               ragged=False, tree=False, total_rows=0) -> RadAttnPagedArgs:
+    """A RadAttnPagedArgs carrying only a call's shape (and whether it has
+    cu_seqlens / tree_mask), for the workspace and describe queries."""
+    a = RadAttnPagedArgs()
+    a.struct_size = ctypes.sizeof(RadAttnPagedArgs)
+    a.groups, a.rows, a.n_head, a.n_head_kv, a.head_dim = groups, rows, n_head, n_head_kv, head_dim
+    a.page_size, a.pages_per_seq, a.kv_dtype = page_size, pages_per_seq, kv_dtype
+    a.cu_seqlens = 16 if ragged else None     # presence only: never dereferenced by the queries
+    a.tree_mask = 16 if tree else None
+    a.total_rows = total_rows
+    return a
+
+
+def ex_describe(args: RadAttnPagedArgs) -> str:
+    buf = ctypes.create_string_buffer(512)
+    rc = load().rad_attn_paged_ex_describe(ctypes.byref(args), buf, len(buf))
+    if rc != RAD_OK:
+        raise RadAttnError(rc, "rad_attn_paged_ex_describe")
+    return buf.value.decode()
+
+
 def attn_paged_general(q, k_pool, v_pool, page_table, seq_lens, *, rows, n_head, n_head_kv, head_dim,
                        page_size, scale, kv_dtype=RAD_KV_BF16, k_scales=None, v_scales=None,
-                       cu_seqlens=None, tree_mask=None, window=0, out=None, workspace=None,
-                       err_word=None, stream=None):
+                       cu_seqlens=None, tree_mask=None, window=0, total_rows=None, out=None,
+                       workspace=None, err_word=None, stream=None):
     """The op through rad_attn_paged_ex with every optional field.
 
     cu_seqlens: int32 [groups + 1] absolute row offsets (ragged rows; ``rows``
     is then the largest count and q is [q_rows, n_head, head_dim]); tree_mask:
     uint32 words (as int32) indexed like q's rows (draft-tree rows); window:
     sliding window.  Without cu_seqlens q is [groups, rows, n_head, head_dim].
-    Returns `out` (allocated like q when None; rows no group names are not
-    written).
+    total_rows bounds the rows a ragged call names (default: q's rows, which
+    hold every row the offsets may name).  Returns `out` (allocated like q
+    when None; rows no group names are not written).
     """
     groups = int(seq_lens.shape[0])
     if out is None:
@@ -222,6 +248,8 @@ def attn_paged_general(q, k_pool, v_pool, page_table, seq_lens, *, rows, n_head,
     a.cu_seqlens = None if cu_seqlens is None else cu_seqlens.data_ptr()
     a.tree_mask = None if tree_mask is None else tree_mask.data_ptr()
     a.window = int(window)
+    if cu_seqlens is not None:
+        a.total_rows = int(q.shape[0]) if total_rows is None else int(total_rows)
     a.out = out.data_ptr()
     need = ex_workspace_bytes(a)
     if workspace is None and need > 0:

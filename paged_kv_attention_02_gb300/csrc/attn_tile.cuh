@@ -94,9 +94,13 @@ struct AttnParams {
     uint32_t* err_word;    // optional
     const int32_t* cu_seqlens;   // [groups + 1] absolute q row offsets, or null: `rows` rows per group
     const uint32_t* tree_mask;   // one word per q row (bit i: sees the call's key i), or null: causal
+    // Ragged calls (cu_seqlens given): (sequence, query tile) of each of the
+    // call's query tiles in sequence order, (-1, 0) past the last; n_qtiles
+    // is then the bound on the call's tiles, not a per-sequence count.
+    const int2* tile_map;
     int groups, rows, n_head, n_head_kv, ratio, page_size, pages_per_seq, num_pages;   // rows: max per group
     int M;                 // rows * ratio: query rows per KV head (the most of any group)
-    int n_qtiles;          // ceil(M / QT)
+    int n_qtiles;          // ceil(M / QT) per sequence; ragged calls: tiles of the whole call (a bound)
     int qtv;               // query rows stored per partial slot: min(M, QT)
     int qt_rows;           // QT of the split kernel's tile
     int max_splits;        // 1 without splitting
@@ -200,6 +204,7 @@ __device__ __forceinline__ uint32_t kv_off(int key, int d, int lp) {
 
 struct ItemPlan {
     int s, g, kvh, qt;
+    long long gq;      // partial-slot group of the item: (sequence, KV head, query tile)
     int L;
     long long qrow0;   // q/output row of the group's row 0
     int qlen;          // the group's rows
@@ -227,15 +232,38 @@ __device__ __forceinline__ int item_group(int item, const AttnParams& p) {
 template <class C, bool WIN>
 __device__ __forceinline__ ItemPlan plan_item(int item, const AttnParams& p, int L_known = -1) {
     ItemPlan it;
-    const int per_split = p.groups * p.n_head_kv * p.n_qtiles;
-    it.s = item / per_split;
-    const int rem = item - it.s * per_split;
-    const int per_g = p.n_head_kv * p.n_qtiles;
-    it.g = rem / per_g;
-    const int rem2 = rem - it.g * per_g;
-    it.kvh = rem2 / p.n_qtiles;
-    it.qt = rem2 - it.kvh * p.n_qtiles;
-    if (p.split_len == 0) it.qt = p.n_qtiles - 1 - it.qt;   // causal: later tiles see more keys
+    if (p.tile_map) {
+        // ragged: items are (split, tile of the call, KV head)
+        const int per_split = p.n_qtiles * p.n_head_kv;
+        it.s = item / per_split;
+        const int rem = item - it.s * per_split;
+        const int t = rem / p.n_head_kv;
+        it.kvh = rem - t * p.n_head_kv;
+        it.gq = (long long)t * p.n_head_kv + it.kvh;
+        const int2 gm = __ldg(p.tile_map + t);
+        if (gm.x < 0) {   // past the call's last tile
+            it.g = it.qt = it.L = it.qlen = 0;
+            it.qrow0 = 0;
+            it.active = it.seq_ok = it.cu_ok = false;
+            it.m0 = it.m_end = it.k0 = it.k1 = it.klo = it.kmax = 0;
+            it.n_stages = it.s_first = 0;
+            it.n_splits = 1;
+            return it;
+        }
+        it.g = gm.x;
+        it.qt = gm.y;
+    } else {
+        const int per_split = p.groups * p.n_head_kv * p.n_qtiles;
+        it.s = item / per_split;
+        const int rem = item - it.s * per_split;
+        const int per_g = p.n_head_kv * p.n_qtiles;
+        it.g = rem / per_g;
+        const int rem2 = rem - it.g * per_g;
+        it.kvh = rem2 / p.n_qtiles;
+        it.qt = rem2 - it.kvh * p.n_qtiles;
+        if (p.split_len == 0) it.qt = p.n_qtiles - 1 - it.qt;   // causal: later tiles see more keys
+        it.gq = ((long long)it.g * p.n_head_kv + it.kvh) * p.n_qtiles + it.qt;
+    }
     GroupRows gr;
     it.cu_ok = group_rows(p, it.g, gr);
     it.qrow0 = gr.row0;
@@ -908,8 +936,7 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
                 }
                 if (item_bad && tid == 0 && p.err_word) atomicOr(p.err_word, bad_bits);
             } else {
-                const long long gq = ((long long)it.g * p.n_head_kv + it.kvh) * p.n_qtiles + it.qt;
-                const long long slot_idx = gq * p.max_splits + it.s;
+                const long long slot_idx = it.gq * p.max_splits + it.s;
                 float* pacc = p.part_acc + slot_idx * p.qtv * C::D;
                 float* pml = p.part_ml + slot_idx * p.qtv * 2;
                 for (int idx = tid; idx < ncols * D4; idx += C::NCT) {

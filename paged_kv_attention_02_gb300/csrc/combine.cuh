@@ -36,10 +36,19 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const __g
 
     const int n_cg = (p.qt_rows + CG - 1) / CG;
     const int cgi = blockIdx.x % n_cg;
-    const int gq = blockIdx.x / n_cg;                 // (g, kvh, qt)
-    const int qt = gq % p.n_qtiles;
-    const int kvh = (gq / p.n_qtiles) % p.n_head_kv;
-    const int g = gq / (p.n_qtiles * p.n_head_kv);
+    const int gq = blockIdx.x / n_cg;                 // (g, kvh, qt), ragged calls (tile, kvh)
+    int g, kvh, qt;
+    if (p.tile_map) {
+        kvh = gq % p.n_head_kv;
+        const int2 gm = __ldg(p.tile_map + gq / p.n_head_kv);
+        if (gm.x < 0) return;                                                         // past the last tile
+        g = gm.x;
+        qt = gm.y;
+    } else {
+        qt = gq % p.n_qtiles;
+        kvh = (gq / p.n_qtiles) % p.n_head_kv;
+        g = gq / (p.n_qtiles * p.n_head_kv);
+    }
     GroupRows gr;
     if (!group_rows(p, g, gr)) return;                                                // no rows named
     const int L = __ldg(p.seq_lens + g);

@@ -38,7 +38,8 @@ cudaError_t launch_cfg(const AttnParams& p, int sms, cudaStream_t st) {
 template <int D>
 cudaError_t launch_combine(const AttnParams& p, cudaStream_t st) {
     const long long n_cg = (p.qt_rows + kCombineCols - 1) / kCombineCols;
-    const long long grid = (long long)p.groups * p.n_head_kv * p.n_qtiles * n_cg;
+    const long long n_gq = (long long)(p.tile_map ? 1 : p.groups) * p.n_head_kv * p.n_qtiles;
+    const long long grid = n_gq * n_cg;
     if (grid > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
@@ -51,6 +52,8 @@ cudaError_t launch_combine(const AttnParams& p, cudaStream_t st) {
 template <int D, bool FP8>
 cudaError_t launch_family(int family, const AttnParams& p, int sms, cudaStream_t st) {
     cudaError_t e;
+    // a ragged call maps its query tiles first
+    if (p.tile_map && (e = launch_ragged_tile_map(p, st)) != cudaSuccess) return e;
     switch (family) {
         case kFamDecode: e = launch_cfg<typename Pick<D, FP8, kFamDecode>::T>(p, sms, st); break;
         case kFamVerify: e = launch_cfg<typename Pick<D, FP8, kFamVerify>::T>(p, sms, st); break;

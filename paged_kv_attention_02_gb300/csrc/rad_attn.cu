@@ -38,9 +38,10 @@ struct Plan {
     int family;
     int split_len;
     int ratio, M, n_qtiles, qtv, max_splits;
+    bool ragged;       // items and partial slots run over the call's query tiles (a tile map)
     rad::TileInfo tile;
     long long n_items;
-    size_t flags_bytes, ml_bytes, acc_bytes, total_bytes;
+    size_t map_bytes, flags_bytes, ml_bytes, acc_bytes, total_bytes;
 };
 
 int check_scalars(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_dim,
@@ -70,9 +71,12 @@ bool use_prefill_tc(int32_t rows, int32_t ratio, int32_t head_dim, int32_t kv_dt
 }
 
 // `general`: a call with ragged rows (cu_seqlens) or tree masks, which only
-// the tile kernels take.
+// the tile kernels take.  `ragged_rows` >= 0 marks a ragged call: its work and
+// workspace run over the call's query tiles, bounded with the caller's total
+// of rows when it gives one (> 0), else with `rows` rows per sequence.
 Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_dim,
-               int32_t page_size, int32_t pages_per_seq, int32_t kv_dtype, bool general = false) {
+               int32_t page_size, int32_t pages_per_seq, int32_t kv_dtype, bool general = false,
+               long long ragged_rows = -1) {
     Plan pl{};
     pl.ratio = n_head / n_head_kv;
     pl.M = rows * pl.ratio;
@@ -98,7 +102,20 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
     pl.qtv = pl.M < pl.tile.QT ? pl.M : pl.tile.QT;
     const long long cap_keys = (long long)pages_per_seq * page_size;
     pl.max_splits = pl.split_len > 0 ? (int)((cap_keys + pl.split_len - 1) / pl.split_len) : 1;
-    const long long n_gq = (long long)groups * n_head_kv * pl.n_qtiles;
+    long long n_gq = (long long)groups * n_head_kv * pl.n_qtiles;
+    pl.ragged = ragged_rows >= 0;
+    if (pl.ragged) {
+        // sum over sequences of ceil(R_g * ratio / QT) <= ceil(total * ratio / QT) + groups
+        long long tiles = (long long)groups * pl.n_qtiles;
+        if (ragged_rows > 0) {
+            const long long b = (ragged_rows * pl.ratio + pl.tile.QT - 1) / pl.tile.QT + groups;
+            if (b < tiles) tiles = b;
+        }
+        if (tiles > 0x7FFFFFFFll) tiles = 0x7FFFFFFFll;
+        pl.n_qtiles = (int)tiles;
+        n_gq = tiles * n_head_kv;
+        pl.map_bytes = round_up((size_t)tiles * 8, 256);
+    }
     pl.n_items = n_gq * pl.max_splits;
     if (pl.split_len > 0) {
         const long long slots = n_gq * pl.max_splits;
@@ -106,7 +123,7 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
         pl.ml_bytes = round_up((size_t)slots * pl.qtv * 2 * 4, 256);
         pl.acc_bytes = round_up((size_t)slots * pl.qtv * head_dim * 4, 256);
     }
-    pl.total_bytes = pl.flags_bytes + pl.ml_bytes + pl.acc_bytes;
+    pl.total_bytes = pl.map_bytes + pl.flags_bytes + pl.ml_bytes + pl.acc_bytes;
     return pl;
 }
 
@@ -171,8 +188,8 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
                     const int32_t* seq_lens, int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv,
                     int32_t head_dim, int32_t page_size, int32_t pages_per_seq, int32_t num_pages, float scale,
                     int32_t kv_dtype, const float* k_scales, const float* v_scales, int32_t window,
-                    const int32_t* cu_seqlens, const uint32_t* tree_mask, void* out, void* workspace,
-                    size_t workspace_bytes, uint32_t* err_word, rad_stream_t stream);
+                    const int32_t* cu_seqlens, const uint32_t* tree_mask, int32_t total_rows, void* out,
+                    void* workspace, size_t workspace_bytes, uint32_t* err_word, rad_stream_t stream);
 
 // Fields of a RadAttnPagedArgs that an older caller's struct_size leaves out read as zero.
 template <class T>
@@ -216,7 +233,7 @@ int rad_attn_paged(const void* q, const void* k_pool, const void* v_pool, const 
                    uint32_t* err_word, rad_stream_t stream) {
     return attn_paged_impl(q, k_pool, v_pool, page_table, seq_lens, groups, rows, n_head, n_head_kv, head_dim,
                            page_size, pages_per_seq, num_pages, scale, kv_dtype, k_scales, v_scales, 0, nullptr,
-                           nullptr, out, workspace, workspace_bytes, err_word, stream);
+                           nullptr, 0, out, workspace, workspace_bytes, err_word, stream);
 }
 
 int rad_attn_paged_window(const void* q, const void* k_pool, const void* v_pool, const int32_t* page_table,
@@ -227,7 +244,7 @@ int rad_attn_paged_window(const void* q, const void* k_pool, const void* v_pool,
                           size_t workspace_bytes, uint32_t* err_word, rad_stream_t stream) {
     return attn_paged_impl(q, k_pool, v_pool, page_table, seq_lens, groups, rows, n_head, n_head_kv, head_dim,
                            page_size, pages_per_seq, num_pages, scale, kv_dtype, k_scales, v_scales, window,
-                           nullptr, nullptr, out, workspace, workspace_bytes, err_word, stream);
+                           nullptr, nullptr, 0, out, workspace, workspace_bytes, err_word, stream);
 }
 
 int rad_attn_paged_ex(const RadAttnPagedArgs* a, rad_stream_t stream) {
@@ -236,9 +253,10 @@ int rad_attn_paged_ex(const RadAttnPagedArgs* a, rad_stream_t stream) {
     const int32_t window = ex_field(a, &RadAttnPagedArgs::window, offsetof(RadAttnPagedArgs, window));
     const int32_t* cu = ex_field(a, &RadAttnPagedArgs::cu_seqlens, offsetof(RadAttnPagedArgs, cu_seqlens));
     const uint32_t* tm = ex_field(a, &RadAttnPagedArgs::tree_mask, offsetof(RadAttnPagedArgs, tree_mask));
+    const int32_t total = ex_field(a, &RadAttnPagedArgs::total_rows, offsetof(RadAttnPagedArgs, total_rows));
     return attn_paged_impl(a->q, a->k_pool, a->v_pool, a->page_table, a->seq_lens, a->groups, a->rows, a->n_head,
                            a->n_head_kv, a->head_dim, a->page_size, a->pages_per_seq, a->num_pages, a->scale,
-                           a->kv_dtype, a->k_scales, a->v_scales, window, cu, tm, a->out, a->workspace,
+                           a->kv_dtype, a->k_scales, a->v_scales, window, cu, tm, total, a->out, a->workspace,
                            a->workspace_bytes, a->err_word, stream);
 }
 
@@ -247,10 +265,12 @@ size_t rad_attn_paged_ex_workspace_bytes(const RadAttnPagedArgs* a) {
     if (check_scalars(a->groups, a->rows, a->n_head, a->n_head_kv, a->head_dim, a->page_size, a->pages_per_seq,
                       a->kv_dtype) != RAD_OK)
         return 0;
-    const bool general = ex_field(a, &RadAttnPagedArgs::cu_seqlens, offsetof(RadAttnPagedArgs, cu_seqlens)) ||
-                         ex_field(a, &RadAttnPagedArgs::tree_mask, offsetof(RadAttnPagedArgs, tree_mask));
+    const bool ragged = ex_field(a, &RadAttnPagedArgs::cu_seqlens, offsetof(RadAttnPagedArgs, cu_seqlens));
+    const bool general = ragged || ex_field(a, &RadAttnPagedArgs::tree_mask, offsetof(RadAttnPagedArgs, tree_mask));
+    const int32_t total = ex_field(a, &RadAttnPagedArgs::total_rows, offsetof(RadAttnPagedArgs, total_rows));
+    if (total < 0) return 0;
     return make_plan(a->groups, a->rows, a->n_head, a->n_head_kv, a->head_dim, a->page_size, a->pages_per_seq,
-                     a->kv_dtype, general)
+                     a->kv_dtype, general, ragged ? total : -1)
         .total_bytes;
 }
 
@@ -262,14 +282,16 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
                     const int32_t* seq_lens, int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv,
                     int32_t head_dim, int32_t page_size, int32_t pages_per_seq, int32_t num_pages, float scale,
                     int32_t kv_dtype, const float* k_scales, const float* v_scales, int32_t window,
-                    const int32_t* cu_seqlens, const uint32_t* tree_mask, void* out, void* workspace,
-                    size_t workspace_bytes, uint32_t* err_word, rad_stream_t stream) {
+                    const int32_t* cu_seqlens, const uint32_t* tree_mask, int32_t total_rows, void* out,
+                    void* workspace, size_t workspace_bytes, uint32_t* err_word, rad_stream_t stream) {
     int rc = check_scalars(groups, rows, n_head, n_head_kv, head_dim, page_size, pages_per_seq, kv_dtype);
     if (rc != RAD_OK) return rc;
     if (num_pages <= 0 || (long long)num_pages * page_size > 0x7FFFFFFFll) return RAD_E_SHAPE;
     if (tree_mask && rows > 32) return RAD_E_SHAPE;   // a mask word covers 32 nodes
+    if (total_rows < 0) return RAD_E_ARG;
     const bool general = cu_seqlens || tree_mask;
-    const Plan pl = make_plan(groups, rows, n_head, n_head_kv, head_dim, page_size, pages_per_seq, kv_dtype, general);
+    const Plan pl = make_plan(groups, rows, n_head, n_head_kv, head_dim, page_size, pages_per_seq, kv_dtype, general,
+                              cu_seqlens ? total_rows : -1);
     if (pl.n_items > 0x7FFFFFFFll) return RAD_E_SHAPE;
     if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !out) return RAD_E_ARG;
     if (!is_aligned(q, 16) || !is_aligned(k_pool, 16) || !is_aligned(v_pool, 16) || !is_aligned(out, 16) ||
@@ -320,9 +342,13 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (pl.total_bytes > 0) {
         char* ws = static_cast<char*>(workspace);
-        p.part_flag = reinterpret_cast<uint32_t*>(ws);
-        p.part_ml = reinterpret_cast<float*>(ws + pl.flags_bytes);
-        p.part_acc = reinterpret_cast<float*>(ws + pl.flags_bytes + pl.ml_bytes);
+        if (pl.ragged) p.tile_map = reinterpret_cast<const int2*>(ws);
+        ws += pl.map_bytes;
+        if (pl.split_len > 0) {
+            p.part_flag = reinterpret_cast<uint32_t*>(ws);
+            p.part_ml = reinterpret_cast<float*>(ws + pl.flags_bytes);
+            p.part_acc = reinterpret_cast<float*>(ws + pl.flags_bytes + pl.ml_bytes);
+        }
     }
     cudaError_t e;
     if (pl.family == rad::kFamPrefillTC) {
@@ -357,21 +383,28 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
 
 extern "C" {
 
-int rad_attn_paged_describe(int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_dim,
-                            int32_t page_size, int32_t kv_dtype, char* buf, size_t buf_len) {
+}  // extern "C"
+
+namespace {
+
+int describe_call(int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_dim, int32_t page_size,
+                  int32_t kv_dtype, bool general, bool ragged, char* buf, size_t buf_len) {
     const int rc = check_scalars(1, rows, n_head, n_head_kv, head_dim, page_size, 1, kv_dtype);
     if (!buf || buf_len == 0) return rc != RAD_OK ? rc : RAD_E_ARG;
     if (rc != RAD_OK) {
         snprintf(buf, buf_len, "refused: %s", rad_attn_status_string(rc));
         return rc;
     }
-    const Plan pl = make_plan(1, rows, n_head, n_head_kv, head_dim, page_size, 1, kv_dtype);
+    const Plan pl = make_plan(1, rows, n_head, n_head_kv, head_dim, page_size, 1, kv_dtype, general);
     const rad::TileInfo& t = pl.tile;
+    // a ragged call first maps its query tiles (one small kernel)
+    const char* pre = ragged ? "ragged_tile_map + " : "";
     if (pl.family == rad::kFamSplitTC) {
         snprintf(buf, buf_len,
                  "attn_split_tc05 family=%s head_dim=%d kv=fp8e4m3 query_rows_per_kv_head=%d tile_rows=%d "
-                 "keys_per_tile=%d stages=%d ctas_per_sm=1 warps=4 workers+1 mma+2 producers "
-                 "mma=tcgen05.kind::f16 (keys as M, query rows as N; K/V e4m3 -> f16 once per tile) "
+                 "keys_per_tile=%d stages=%d ctas_per_sm=1 warps=8 workers+1 qk+1 pv+2 producers "
+                 "mma=tcgen05 (keys as M, query rows as N; QK kind::f8f6f4 on the staged e4m3 K with Q as two "
+                 "e4m3 terms, PV kind::f16 with V e4m3 -> f16 once per tile) "
                  "split_len=%d + attn_combine (split order)",
                  family_name(pl.family), head_dim, pl.M, t.QT, t.KS, t.NS, pl.split_len);
         return RAD_OK;
@@ -385,14 +418,35 @@ int rad_attn_paged_describe(int32_t rows, int32_t n_head, int32_t n_head_kv, int
         return RAD_OK;
     }
     snprintf(buf, buf_len,
-             "attn_tile family=%s head_dim=%d kv=%s query_rows_per_kv_head=%d tile_rows=%d "
+             "%sattn_tile family=%s head_dim=%d kv=%s query_rows_per_kv_head=%d tile_rows=%d "
              "warps(q=%d,k=%d)+2 producers n_tiles_per_warp=%d keys_per_stage=%d stages=%d split_len=%d "
              "threads=%d smem=%d ctas_per_sm=%d mma=m16n8k16.%s%s",
-             family_name(pl.family), head_dim, kv_dtype == RAD_KV_FP8_E4M3 ? "fp8e4m3" : "bf16", pl.M,
+             pre, family_name(pl.family), head_dim, kv_dtype == RAD_KV_FP8_E4M3 ? "fp8e4m3" : "bf16", pl.M,
              t.QT, t.WQ, t.WK, t.NQW, t.KS, t.NS, pl.split_len, t.threads, t.smem, t.minb,
              kv_dtype == RAD_KV_FP8_E4M3 ? "f16" : "bf16",
              pl.split_len > 0 ? " + attn_combine (split order)" : "");
     return RAD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int rad_attn_paged_describe(int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_dim,
+                            int32_t page_size, int32_t kv_dtype, char* buf, size_t buf_len) {
+    return describe_call(rows, n_head, n_head_kv, head_dim, page_size, kv_dtype, false, false, buf, buf_len);
+}
+
+int rad_attn_paged_ex_describe(const RadAttnPagedArgs* a, char* buf, size_t buf_len) {
+    const int rc = check_ex_struct(a);
+    if (rc != RAD_OK) {
+        if (buf && buf_len) snprintf(buf, buf_len, "refused: %s", rad_attn_status_string(rc));
+        return rc;
+    }
+    const bool ragged = ex_field(a, &RadAttnPagedArgs::cu_seqlens, offsetof(RadAttnPagedArgs, cu_seqlens));
+    const bool general = ragged || ex_field(a, &RadAttnPagedArgs::tree_mask, offsetof(RadAttnPagedArgs, tree_mask));
+    return describe_call(a->rows, a->n_head, a->n_head_kv, a->head_dim, a->page_size, a->kv_dtype, general, ragged,
+                         buf, buf_len);
 }
 
 const char* rad_attn_status_string(int status) {

@@ -133,5 +133,8 @@ cudaError_t launch_prefill_tc05(const CUtensorMap& tq, const CUtensorMap& tk, co
                                 const AttnParams& p, int sms, cudaStream_t st);
 cudaError_t launch_split_tc05(const AttnParams& p, int sms, cudaStream_t st);
 TileInfo split_tc05_info(int n);
+// Ragged calls: the tile map into p.tile_map (one CTA), before the tile kernel.
+constexpr int kTileMapThreads = 1024;
+cudaError_t launch_ragged_tile_map(const AttnParams& p, cudaStream_t st);
 
 }  // namespace rad

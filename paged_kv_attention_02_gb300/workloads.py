@@ -63,6 +63,13 @@ class Config:
     pages_per_seq: int        # page-table row stride (capacity in pages)
     pool_pages: int | None = None   # None: exactly the pages the sequences need
     meta: dict = field(default_factory=dict)
+    # Ragged rows: "NxR,..." gives N sequences of R rows each, in call order
+    # (a mixed step: decode rows, verify rounds and prefill chunks side by
+    # side); `rows` is then the largest R.  None: every sequence has `rows`.
+    q_lens: str | None = None
+    # Draft-tree rows: each sequence's rows are a random forest of proposals
+    # flattened parents-first, given to the op as one mask word per row.
+    tree: bool = False
 
     @property
     def scale(self) -> float:
@@ -89,19 +96,55 @@ CONFIGS: dict[str, Config] = {
     "prefill_chunk": Config("prefill_chunk", 1, 2048, 32, 8, 128, 16, KV_BF16, 4, "fixed:8192",
                             pages_per_seq=512, pool_pages=512,
                             meta=dict(n_head=32, n_head_kv=8, head_dim=128, n_embd=4096)),
+    # The verify round as a draft tree of 8 proposals per sequence instead of
+    # a chain ("Radiance architecture plugins", section "Declare: drafters,
+    # encoders, generators": rad_drafter_tree).
+    "tree_verify": Config("tree_verify", 64, 8, 32, 8, 128, 16, KV_FP8_E4M3, 5, "uniform:2048,16384",
+                          pages_per_seq=1024, tree=True,
+                          meta=dict(n_head=32, n_head_kv=8, head_dim=128, n_embd=4096)),
+    # A continuous-batching step ("Radiance architecture plugins", section
+    # "Step: issuing the graph": a prefill chunk beside decode rows, decode
+    # first): 96 decode rows, 24 verify rounds of 8 and one 256-row chunk.
+    "mixed_step": Config("mixed_step", 121, 256, 32, 8, 128, 16, KV_BF16, 6, "uniform:512,8192",
+                         pages_per_seq=512, q_lens="96x1,24x8,1x256",
+                         meta=dict(n_head=32, n_head_kv=8, head_dim=128, n_embd=4096)),
 }
 
 
 @dataclass
 class Workload:
     cfg: Config
-    q: np.ndarray            # uint16 bf16 bits [G, R, H, D]
+    q: np.ndarray            # uint16 bf16 bits [G, R, H, D]; ragged: [T, H, D] packed by q_lens
     k_pool: np.ndarray       # uint16 or uint8 [num_pages, P, Hkv, D]
     v_pool: np.ndarray
     page_table: np.ndarray   # int32 [G, pages_per_seq]
     seq_lens: np.ndarray     # int32 [G]
     k_scales: np.ndarray | None   # float32 [num_pages] (fp8 only)
     v_scales: np.ndarray | None
+    q_lens: np.ndarray | None = None     # int32 [G] rows per sequence (ragged calls)
+    tree_mask: np.ndarray | None = None  # uint32 [G, R] path bits per row (tree calls)
+
+    @property
+    def ragged(self) -> bool:
+        return self.q_lens is not None
+
+    def rows_of(self) -> np.ndarray:
+        """Rows of every sequence (int64 [G])."""
+        if self.q_lens is None:
+            return np.full(self.groups, self.cfg.rows, dtype=np.int64)
+        return self.q_lens.astype(np.int64)
+
+    def packed(self):
+        """The op's ragged inputs: q [T, H, D] with sequence g's rows at
+        cu[g] .. cu[g+1]-1, cu int32 [G + 1], and the mask words of those rows
+        (or None)."""
+        ql = self.rows_of()
+        cu = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+        q = self.q if self.ragged else self.q.reshape(-1, *self.q.shape[2:])
+        mask = None
+        if self.tree_mask is not None:
+            mask = np.concatenate([self.tree_mask[g, :ql[g]] for g in range(self.groups)])
+        return np.ascontiguousarray(q), cu, mask
 
     @property
     def groups(self) -> int:
@@ -123,9 +166,53 @@ class Workload:
     def select_groups(self, idx) -> "Workload":
         """The same pool, with only the listed sequences (in that order) in the call."""
         idx = np.asarray(idx, dtype=np.int64)
-        return replace(self, q=np.ascontiguousarray(self.q[idx]),
+        if self.ragged:
+            _, cu, _ = self.packed()
+            q = np.concatenate([self.q[cu[g]:cu[g + 1]] for g in idx], axis=0)
+        else:
+            q = self.q[idx]
+        return replace(self, q=np.ascontiguousarray(q),
                        page_table=np.ascontiguousarray(self.page_table[idx]),
-                       seq_lens=np.ascontiguousarray(self.seq_lens[idx]))
+                       seq_lens=np.ascontiguousarray(self.seq_lens[idx]),
+                       q_lens=None if self.q_lens is None else np.ascontiguousarray(self.q_lens[idx]),
+                       tree_mask=None if self.tree_mask is None else np.ascontiguousarray(self.tree_mask[idx]))
+
+
+# ---------------------------------------------------------------- draft trees
+# A draft tree of R proposals is flattened parents-first: parents[r] < r, or
+# -1 for a node hanging directly off the cached context.  The op takes one
+# mask word per node with bit i set for every node i on the node's path.
+
+def path_of(parents, r):
+    """Nodes from r up to the cached context, r first."""
+    path = []
+    while r >= 0:
+        path.append(r)
+        r = parents[r]
+    return path
+
+
+def mask_words(parents):
+    """Tree-mask word of every node: bit i for each node on its path."""
+    return np.array([sum(1 << i for i in path_of(parents, r)) for r in range(len(parents))],
+                    dtype=np.uint32)
+
+
+def random_parents(rng, R, forest=True):
+    lo = -1 if forest else 0
+    return [-1] + [int(rng.integers(lo, r)) for r in range(1, R)]
+
+
+def chain(R):
+    return list(range(-1, R - 1))
+
+
+def parse_q_lens(spec: str) -> list[int]:
+    out = []
+    for part in spec.split(","):
+        n, r = part.split("x")
+        out += [int(r)] * int(n)
+    return out
 
 
 def draw_seq_lens(cfg: Config, rng: np.random.Generator) -> np.ndarray:
@@ -192,6 +279,11 @@ def make_workload(cfg: Config | str, *, poison: bool = False, threads: int | Non
     ss_meta, ss_q, ss_k, ss_v = np.random.SeedSequence(cfg.seed).spawn(4)
     rng = np.random.Generator(np.random.PCG64(ss_meta))
     seq_lens = draw_seq_lens(cfg, rng)
+    q_lens = None
+    if cfg.q_lens is not None:
+        q_lens = np.array(parse_q_lens(cfg.q_lens), dtype=np.int32)
+        assert q_lens.shape == (cfg.groups,) and int(q_lens.max()) == cfg.rows
+        seq_lens = np.maximum(seq_lens, q_lens)
     P = cfg.page_size
     n_pages_seq = (seq_lens.astype(np.int64) + P - 1) // P
     assert int(n_pages_seq.max()) <= cfg.pages_per_seq
@@ -206,15 +298,22 @@ def make_workload(cfg: Config | str, *, poison: bool = False, threads: int | Non
         page_table[g, :n] = perm[off:off + n]
         off += n
 
-    q32 = np.random.Generator(np.random.PCG64(ss_q)).standard_normal(
-        (cfg.groups, cfg.rows, cfg.n_head, cfg.head_dim), dtype=np.float32)
+    q_shape = ((int(q_lens.sum()),) if q_lens is not None else (cfg.groups, cfg.rows)) + (cfg.n_head, cfg.head_dim)
+    q32 = np.random.Generator(np.random.PCG64(ss_q)).standard_normal(q_shape, dtype=np.float32)
     q = _f32_to_bf16_bits(q32)
     page_elems = P * cfg.n_head_kv * cfg.head_dim
     k_flat, k_scales = _fill_pool(ss_k, num_pages, page_elems, cfg.kv_dtype, threads)
     v_flat, v_scales = _fill_pool(ss_v, num_pages, page_elems, cfg.kv_dtype, threads)
     shape = (num_pages, P, cfg.n_head_kv, cfg.head_dim)
+    tree_mask = None
+    if cfg.tree:
+        assert cfg.rows <= 32
+        tree_mask = np.zeros((cfg.groups, cfg.rows), dtype=np.uint32)
+        for g in range(cfg.groups):
+            n = cfg.rows if q_lens is None else int(q_lens[g])
+            tree_mask[g, :n] = mask_words(random_parents(rng, n)) if n else []
     w = Workload(cfg, q, k_flat.reshape(shape), v_flat.reshape(shape), page_table, seq_lens,
-                 k_scales, v_scales)
+                 k_scales, v_scales, q_lens, tree_mask)
     if poison:
         poison_unused(w)
     return w
@@ -244,7 +343,9 @@ def kv_bytes(w: Workload) -> int:
     every KV head, the per-page scales (fp8) and the page-table entries read."""
     c = w.cfg
     e = 2 if c.kv_dtype == KV_BF16 else 1
-    L = w.seq_lens.astype(np.int64)
+    # a sequence with rows reads every key (its last row, or with a tree each
+    # node its own key, sees them); one without rows reads nothing
+    L = np.where(w.rows_of() > 0, w.seq_lens.astype(np.int64), 0)
     pages = (L + c.page_size - 1) // c.page_size
     b = int(L.sum()) * c.n_head_kv * c.head_dim * 2 * e
     if c.kv_dtype == KV_FP8_E4M3:
@@ -256,13 +357,24 @@ def kv_bytes(w: Workload) -> int:
 def aux_bytes(w: Workload) -> int:
     """Q read, output written and seq_lens read by one call."""
     c = w.cfg
-    return 2 * w.groups * c.rows * c.n_head * c.head_dim * 2 + 4 * w.groups
+    b = 2 * int(w.rows_of().sum()) * c.n_head * c.head_dim * 2 + 4 * w.groups
+    if w.ragged:
+        b += 4 * (w.groups + 1)
+    if w.tree_mask is not None:
+        b += 4 * int(w.rows_of().sum())
+    return b
 
 
 def attended_flops(w: Workload) -> int:
     """4*D flops (QK and PV multiply-adds) per visible (row, head, key)."""
     c = w.cfg
     L = w.seq_lens.astype(np.int64)
-    R = c.rows
-    keys = sum(int(((L - R + r + 1)).sum()) for r in range(R))
+    R = w.rows_of()
+    keys = 0
+    for g in range(w.groups):
+        for r in range(int(R[g])):
+            if w.tree_mask is not None:
+                keys += int(L[g] - R[g]) + bin(int(w.tree_mask[g, r])).count("1")
+            else:
+                keys += int(L[g] - R[g] + r + 1)
     return keys * c.n_head * 4 * c.head_dim

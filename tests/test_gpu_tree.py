@@ -92,7 +92,7 @@ def tree_masks(w, parents):
     return np.stack([mask_words(pa) for pa in parents]).astype(np.uint32)
 
 
-def run_general(dw, q_bits, rows, cu=None, mask=None, window=0, lens=None):
+def run_general(dw, q_bits, rows, cu=None, mask=None, window=0, lens=None, total_rows=None):
     """One rad_attn_paged_ex call; returns (out bits, err word)."""
     c = dw.w.cfg
     q = bf16_tensor(q_bits)
@@ -105,7 +105,7 @@ def run_general(dw, q_bits, rows, cu=None, mask=None, window=0, lens=None):
     b.attn_paged_general(q, dw.k, dw.v, dw.table, dw.lens if lens is None else lens, rows=rows,
                          n_head=c.n_head, n_head_kv=c.n_head_kv, head_dim=c.head_dim, page_size=c.page_size,
                          scale=c.scale, kv_dtype=c.kv_dtype, k_scales=dw.ks, v_scales=dw.vs, cu_seqlens=cu_t,
-                         tree_mask=mask_t, window=window, out=out, err_word=err)
+                         tree_mask=mask_t, window=window, total_rows=total_rows, out=out, err_word=err)
     torch.cuda.synchronize()
     return bits(out), int(err.item())
 
@@ -215,6 +215,38 @@ def test_ragged_malformed_offsets_flag_their_group_and_write_nothing_of_it(wls):
     got, err = run_general(dw, q, 8, cu=neg)
     assert err == b.RAD_ERRW_CUSEQ
     assert np.array_equal(got[cu[1]:], good[cu[1]:])
+
+
+@pytest.mark.parametrize("name", ["d128_fp8", "chunk_d128"])
+def test_ragged_row_total_bounds_the_work(wls, name):
+    """The exact row total and no total (0: sized for `rows` per sequence)
+    give the same bits as q's row count.  A total of one row bounds the call
+    to ceil(ratio / tile rows) + groups tiles: past that the call raises
+    RAD_ERRW_CUSEQ and runs only its first tiles, in sequence order."""
+    w, dw = wls("ragged", name)
+    q_lens = RAGGED[name][1]
+    q, cu = ragged_q(w, q_lens, base=2, tail=5)
+    ref, _ = run_general(dw, q, max(q_lens), cu=cu)
+    for total in (int(cu[-1] - cu[0]), 0):
+        got, err = run_general(dw, q, max(q_lens), cu=cu, total_rows=total)
+        assert err == 0 and np.array_equal(got, ref), total
+    c = w.cfg
+    ratio = c.n_head // c.n_head_kv
+    desc = b.ex_describe(b.shape_args(w.groups, max(q_lens), c.n_head, c.n_head_kv, c.head_dim, c.page_size,
+                                      w.pages_per_seq, c.kv_dtype, ragged=True))
+    qt = int(desc.split("tile_rows=")[1].split()[0])
+    tiles = [-(-ql * ratio // qt) for ql in q_lens]
+    bound = -(-ratio // qt) + len(q_lens)
+    got, err = run_general(dw, q, max(q_lens), cu=cu, total_rows=1)
+    assert err == (b.RAD_ERRW_CUSEQ if sum(tiles) > bound else 0)
+    done = 0   # rows of the tiles within the bound match; the rest stay unwritten
+    for g, ql in enumerate(q_lens):
+        run = max(0, min(tiles[g], bound - done))
+        rows_run = min(ql, run * qt // ratio)
+        a = int(cu[g])
+        assert np.array_equal(got[a:a + rows_run], ref[a:a + rows_run]), g
+        assert np.all(got[a + rows_run:a + ql] == np.int16(SENTINEL)), g
+        done += tiles[g]
 
 
 def test_ragged_sequence_shorter_than_its_rows_is_zero_and_flagged(wls):

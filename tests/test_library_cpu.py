@@ -174,11 +174,36 @@ def test_ex_workspace_follows_the_kernel_the_call_takes():
         assert ws(a) == b.workspace_bytes(4, 8, 32, 8, hd, 16, 64, dt) > 0
     # fp8 head_dim 128 verify: the uniform call runs the tcgen05 split kernel,
     # a ragged or tree call the verify tile; both split, with their own tiles
-    assert ws(_general_args(cu=fake, kv_dtype=b.RAD_KV_FP8_E4M3)) > 0
+    assert ws(_general_args(tree=fake, kv_dtype=b.RAD_KV_FP8_E4M3)) > 0
+    # a ragged call adds its tile map: 4 sequences x 1 tile x 8 bytes, rounded to 256
     assert ws(_general_args(cu=fake, kv_dtype=b.RAD_KV_FP8_E4M3)) == \
-        ws(_general_args(tree=fake, kv_dtype=b.RAD_KV_FP8_E4M3))
-    # chunks past the split limit need none, on either path
-    assert ws(_general_args(rows=300, cu=fake)) == 0 == b.workspace_bytes(4, 300, 32, 8, 128, 16, 64)
+        ws(_general_args(tree=fake, kv_dtype=b.RAD_KV_FP8_E4M3)) + 256
+    # the caller's row total bounds the tiles: 4 sequences of up to 256 rows
+    # (ratio 4, 32-row tiles: 32 tiles each) holding 40 rows in all need at
+    # most ceil(160 / 32) + 4 = 9 tiles instead of 128
+    big = _general_args(rows=256, cu=fake)
+    small = _general_args(rows=256, cu=fake)
+    small.total_rows = 40
+    assert ws(small) < ws(big) // 10
+    small.total_rows = -1
+    assert ws(small) == 0
+    assert int(b.load().rad_attn_paged_ex(ctypes.byref(small), None)) == b.RAD_E_ARG
+    # chunks past the split limit need no partials: a uniform call needs
+    # nothing, a ragged one its tile map (4 x ceil(1200 / 64) tiles x 8 bytes)
+    assert b.workspace_bytes(4, 300, 32, 8, 128, 16, 64) == 0
+    assert ws(_general_args(rows=300, cu=fake)) == 768
     bad = _general_args()
     bad.struct_size = 8
     assert ws(bad) == 0
+
+
+def test_ex_describe_names_the_kernels_of_ragged_and_tree_calls():
+    shape = lambda **kw: b.shape_args(64, 8, 32, 8, 128, 16, 1024, b.RAD_KV_FP8_E4M3, **kw)
+    assert "family=split_tc05" in b.ex_describe(shape())
+    tree = b.ex_describe(shape(tree=True))
+    assert tree.startswith("attn_tile family=verify") and "attn_combine" in tree
+    rag = b.ex_describe(shape(ragged=True))
+    assert rag.startswith("ragged_tile_map + attn_tile family=verify")
+    chunk = b.ex_describe(b.shape_args(4, 300, 32, 8, 128, 16, 64, ragged=True))
+    assert chunk.startswith("ragged_tile_map + attn_tile family=wide") and "split_len=0" in chunk
+    assert b.describe(300, 32, 8, 128, 16).startswith("attn_prefill_tc05")
