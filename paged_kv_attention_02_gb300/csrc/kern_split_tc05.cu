@@ -10,10 +10,12 @@ namespace rad {
 
 namespace {
 
-template <int N, bool WIN>
+template <int N>
 cudaError_t launch_n(const AttnParams& p, int sms, cudaStream_t st) {
     using C = SplitTcCfg<N>;
-    auto kern = attn_split_tc05_kernel<N, WIN>;
+    auto kern = p.window > 0  ? attn_split_tc05_kernel<N, kModeWindow>
+                : p.tree_mask ? attn_split_tc05_kernel<N, kModeTree>
+                              : attn_split_tc05_kernel<N, kModeCausal>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     long long grid = sms;   // one CTA per SM (shared memory), persistent over the items
@@ -39,12 +41,7 @@ TileInfo split_tc05_info(int n) {
 }
 
 cudaError_t launch_split_tc05(const AttnParams& p, int sms, cudaStream_t st) {
-    cudaError_t e;
-    const bool win = p.window > 0;
-    if (p.qt_rows == 16)
-        e = win ? launch_n<16, true>(p, sms, st) : launch_n<16, false>(p, sms, st);
-    else
-        e = win ? launch_n<32, true>(p, sms, st) : launch_n<32, false>(p, sms, st);
+    const cudaError_t e = p.qt_rows == 16 ? launch_n<16>(p, sms, st) : launch_n<32>(p, sms, st);
     if (e != cudaSuccess || p.max_splits <= 1) return e;
     return launch_combine<128>(p, st);
 }

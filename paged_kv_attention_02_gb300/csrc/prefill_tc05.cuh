@@ -59,8 +59,8 @@ struct PrefillCfg {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_STAGE = Q_BYTES;
     static constexpr int OFF_BARS = OFF_STAGE + NS * STAGE_BYTES;
-    // q_full, q_empty, k_full[NS], v_full[NS], kv_empty[NS], s_full[2], p_full[2], pv_done, o_free, final
-    static constexpr int NBARS = 2 + 3 * NS + 2 + 2 + 3;
+    // q_full, q_empty, k_full[NS], v_full[NS], kv_empty[NS], s_full[2], p_full[2], pv_done[2], o_free, final
+    static constexpr int NBARS = 2 + 3 * NS + 2 + 2 + 2 + 2;
     static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
     static constexpr int NTHREADS = 6 * 32;
@@ -121,8 +121,14 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
     const uint32_t bar_kv_empty = bar_v_full + 8 * C::NS;
     const uint32_t bar_s_full = bar_kv_empty + 8 * C::NS;
     const uint32_t bar_p_full = bar_s_full + 16;
-    const uint32_t bar_pv_done = bar_p_full + 16;
-    const uint32_t bar_o_free = bar_pv_done + 8;
+    // PV of tile t completes a phase of pv_done[t & 1].  A thread that has seen
+    // S of tile t knows PV(t-2) is done (the MMA warp issues QK(t) after
+    // PV(t-2), and a commit tracks every earlier operation of its thread), so
+    // its waits for PV(t-1) or PV(t) are never more than one phase ahead of a
+    // barrier: a single barrier would let a wait for PV(t) pass on the parity
+    // of a still-pending PV(t-1).
+    const uint32_t bar_pv_done = bar_p_full + 16;   // [2]
+    const uint32_t bar_o_free = bar_pv_done + 16;
     const uint32_t bar_final = bar_o_free + 8;
     volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);  // [0] tmem, [1] abort
 
@@ -142,6 +148,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
             mbar_init(bar_p_full + 8 * i, 4);
         }
         mbar_init(bar_pv_done, 1);
+        mbar_init(bar_pv_done + 8, 1);
         mbar_init(bar_o_free, 4);
         mbar_init(bar_final, 1);
         misc[1] = 0;
@@ -317,7 +324,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
                             tc_mma_ts(t_o, sp + kk * 8, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
                             tc_mma_ts(t_o, sp + C::BN / 2 + kk * 8, bd, idesc_pv, 1u);
                         }
-                        tc_commit(bar_pv_done);
+                        tc_commit(bar_pv_done + 8 * (tcj & 1u));
                         tc_commit(bar_kv_empty + 8 * st);
                     }
                     __syncwarp();
@@ -371,7 +378,9 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
             float m_run = -CUDART_INF_F, l_run = 0.f;
             for (int j = 0; j < it.T; ++j) {
                 const uint32_t tcj = tc + j, b = tcj & 1u;
-                if (!mbar_wait_bounded(bar_s_full + 8 * b, (tcj >> 1) & 1u, kWaitLimitNs)) {
+                // (every exit from here is taken by the whole warp: the tcgen05
+                // loads and stores below are warp-collective)
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar_s_full + 8 * b, (tcj >> 1) & 1u, kWaitLimitNs))) {
                     abort = true;
                     break;
                 }
@@ -407,29 +416,42 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
                 for (int e = 8; e < C::BN; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sv[e]));
                 const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                        fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                // A row whose max grew past 2^8 rescales its O row.  tcgen05.ld/st
+                // are warp-collective, so the warp rescales together when any of
+                // its rows needs it; the others multiply by exactly 1.
+                bool need = false;
+                float alpha = 1.f, m_new = m_run;
                 if (mx != -CUDART_INF_F) {
                     const float mx_s = mx * cs;
                     if (m_run == -CUDART_INF_F) {
-                        m_run = mx_s;
+                        m_run = mx_s;   // first keys of the row: nothing accumulated yet
                     } else if (mx_s > m_run + C::RESCALE_LOG2) {
-                        const float alpha = exp2f(m_run - mx_s);
-                        // PV of the previous tile must have landed before O is rescaled
-                        if (!mbar_wait_bounded(bar_pv_done, (tcj - 1) & 1u, kWaitLimitNs)) {
-                            abort = true;
-                            break;
-                        }
-                        tc_fence_after();
+                        need = true;
+                        alpha = exp2f(m_run - mx_s);
+                        m_new = mx_s;
+                    }
+                }
+                if (__any_sync(0xffffffffu, need)) {
+                    // PV of the previous tile must have landed before O is rescaled
+                    const uint32_t tp = tcj - 1;   // the previous tile
+                    const bool ok = mbar_wait_bounded(bar_pv_done + 8 * (tp & 1u), (tp >> 1) & 1u, kWaitLimitNs);
+                    if (!__all_sync(0xffffffffu, ok)) {
+                        abort = true;
+                        break;
+                    }
+                    tc_fence_after();
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint32_t ov[32];
-                            tmem_ld32(t_o + lane_off + 32 * q, ov);
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t ov[32];
+                        tmem_ld32(t_o + lane_off + 32 * q, ov);
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                            tmem_st32(t_o + lane_off + 32 * q, ov);
-                        }
-                        tmem_wait_st();
+                        for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                        tmem_st32(t_o + lane_off + 32 * q, ov);
+                    }
+                    tmem_wait_st();
+                    if (need) {
                         l_run *= alpha;
-                        m_run = mx_s;
+                        m_run = m_new;
                     }
                 }
                 const float m_use = (m_run == -CUDART_INF_F) ? 0.f : m_run;
@@ -454,7 +476,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_p_full + 8 * b);
-                if (misc[1]) {
+                if (__any_sync(0xffffffffu, misc[1] != 0)) {
                     abort = true;
                     break;
                 }
@@ -465,7 +487,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
             }
             // ---- epilogue: O / l -> bf16
             const uint32_t tcl = tc + it.T - 1;
-            if (!mbar_wait_bounded(bar_pv_done, tcl & 1u, kWaitLimitNs)) abort = true;
+            if (!mbar_wait_bounded(bar_pv_done + 8 * (tcl & 1u), (tcl >> 1) & 1u, kWaitLimitNs)) abort = true;
             tc_fence_after();
             const float inv = (bad || l_run == 0.f) ? 0.f : 1.f / l_run;
 #pragma unroll

@@ -70,10 +70,11 @@ bool use_prefill_tc(int32_t rows, int32_t ratio, int32_t head_dim, int32_t kv_dt
            128 % ratio == 0;
 }
 
-// `general`: a call with ragged rows (cu_seqlens) or tree masks, which only
-// the tile kernels take.  `ragged_rows` >= 0 marks a ragged call: its work and
-// workspace run over the call's query tiles, bounded with the caller's total
-// of rows when it gives one (> 0), else with `rows` rows per sequence.
+// `general`: a call with ragged rows (cu_seqlens) or tree masks.  Ragged
+// calls run on the tile kernels only; tree calls also on the tcgen05 split
+// kernel.  `ragged_rows` >= 0 marks a ragged call: its work and workspace run
+// over the call's query tiles, bounded with the caller's total of rows when
+// it gives one (> 0), else with `rows` rows per sequence.
 Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_dim,
                int32_t page_size, int32_t pages_per_seq, int32_t kv_dtype, bool general = false,
                long long ragged_rows = -1) {
@@ -85,7 +86,8 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
     // share one key schedule.  Longer calls: the tcgen05 prefill kernel where
     // it applies, else the wide tile.
     pl.split_len = rows <= rad::kSplitMaxRows ? rad::kSplitLen : 0;
-    if (pl.split_len > 0 && RAD_SPLIT_TC05 && !general && head_dim == 128 && kv_dtype == RAD_KV_FP8_E4M3)
+    const bool ragged = ragged_rows >= 0;
+    if (pl.split_len > 0 && RAD_SPLIT_TC05 && !ragged && head_dim == 128 && kv_dtype == RAD_KV_FP8_E4M3)
         pl.family = rad::kFamSplitTC;
     else if (pl.split_len > 0)
         pl.family = pl.M <= 8 ? rad::kFamDecode : rad::kFamVerify;
@@ -103,7 +105,7 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
     const long long cap_keys = (long long)pages_per_seq * page_size;
     pl.max_splits = pl.split_len > 0 ? (int)((cap_keys + pl.split_len - 1) / pl.split_len) : 1;
     long long n_gq = (long long)groups * n_head_kv * pl.n_qtiles;
-    pl.ragged = ragged_rows >= 0;
+    pl.ragged = ragged;
     if (pl.ragged) {
         // sum over sequences of ceil(R_g * ratio / QT) <= ceil(total * ratio / QT) + groups
         long long tiles = (long long)groups * pl.n_qtiles;
@@ -395,7 +397,7 @@ int describe_call(int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_
         snprintf(buf, buf_len, "refused: %s", rad_attn_status_string(rc));
         return rc;
     }
-    const Plan pl = make_plan(1, rows, n_head, n_head_kv, head_dim, page_size, 1, kv_dtype, general);
+    const Plan pl = make_plan(1, rows, n_head, n_head_kv, head_dim, page_size, 1, kv_dtype, general, ragged ? 0 : -1);
     const rad::TileInfo& t = pl.tile;
     // a ragged call first maps its query tiles (one small kernel)
     const char* pre = ragged ? "ragged_tile_map + " : "";

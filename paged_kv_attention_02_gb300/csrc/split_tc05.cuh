@@ -106,7 +106,8 @@ struct SplitTcCfg {
     static constexpr int OFF_META = OFF_QSTG + QSTG_BYTES;
     static constexpr int OFF_RED = OFF_META + NS * META_STRIDE;
     static constexpr int OFF_ISQ = OFF_RED + 5 * N * 4;    // red: [G][4][V] partials + [G][V] totals
-    static constexpr int OFF_BARS = OFF_ISQ + N * 4;       // isq: 2^-k of each query row
+    static constexpr int OFF_TMW = OFF_ISQ + N * 4;        // isq: 2^-k of each query row
+    static constexpr int OFF_BARS = OFF_TMW + N * 4;       // tmw: tree-mask word of each query row
     // k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], qstg_full, qstg_empty,
     // q8_full, (unused), v16_full[2], p_full[2], s_full[NSB], s_empty[NSB], pv_done[2],
     // o_free, final_qk, final_pv
@@ -241,10 +242,14 @@ __device__ __forceinline__ void tmem_stV(uint32_t taddr, const uint32_t (&r)[V])
     else tmem_st16(taddr, r);
 }
 
-template <int N, bool WIN>
+// MODE: kModeCausal, kModeWindow or kModeTree (draft-tree rows, uniform row
+// counts: bit i of a row's mask word lets it see the call's key i).
+template <int N, int MODE>
 __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
     attn_split_tc05_kernel(const __grid_constant__ AttnParams p) {
     using C = SplitTcCfg<N>;
+    constexpr bool WIN = MODE == kModeWindow;
+    constexpr bool TREE = MODE == kModeTree;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -405,7 +410,7 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                             meta[i] = kss[i];
                             meta[8 + i] = vss[i];
                         }
-                        reinterpret_cast<uint32_t*>(meta)[16] = bad_any;
+                        reinterpret_cast<uint32_t*>(meta)[16] = bad_any ? kErrPage : 0u;
                         mbar_arrive(bar_k_full + 8 * slot);
                     }
                 }
@@ -521,6 +526,7 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
         uint8_t* const v16p = smem + C::OFF_V16;
         uint8_t* const q8p = smem + C::OFF_Q8;
         float* const isq = reinterpret_cast<float*>(smem + C::OFF_ISQ);
+        uint32_t* const tmw = reinterpret_cast<uint32_t*>(smem + C::OFF_TMW);
         float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
         // P^T store offsets of key slot k for the 8 swizzle phases of a row q
         uint32_t poff[8];
@@ -620,6 +626,9 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                     for (int term = 0; term < C::QTERMS; ++term)
                         *reinterpret_cast<uint2*>(q8p + term * C::Q8_TERM + off) = make_uint2(w[term][0], w[term][1]);
                     if (ch == 0) isq[row] = __uint_as_float((uint32_t)(127 - kx) << 23);
+                    if (TREE && ch == 0)
+                        tmw[row] = row < nrows ? __ldg(p.tree_mask + (long long)it.g * p.rows + (it.m0 + row) / p.ratio)
+                                               : 0u;
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -655,8 +664,15 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                 for (int i = t; i < n_below + (ghi - thi); i += NWT) {
                     const int pi = i < n_below ? glo + i : thi + (i - n_below);
                     const int pg = __ldg(trow + pi);
-                    bad |= (pg < 0 || pg >= p.num_pages) ? 1u : 0u;
+                    bad |= (pg < 0 || pg >= p.num_pages) ? kErrPage : 0u;
                 }
+            }
+            // every item checks all mask words of its group, so a malformed word
+            // zeroes every row of the group: a word holds its own row's bit and
+            // no later row's
+            if (TREE && t < p.rows) {
+                const uint32_t w = __ldg(p.tree_mask + (long long)it.g * p.rows + t);
+                if ((w >> t) != 1u) bad |= kErrMask;
             }
             // ---- per query row state of this thread's half (identical across its key slots)
             float mu[V], thr[V], lsum[V];
@@ -729,10 +745,21 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                     sc[q + 3] = c_t * f.w;
                 }
                 float xs[V];
-                const bool full = kbase + C::BK <= it.k1 && kbase + C::BK <= nk0 && kbase >= klo_last;
+                // tree rows see every cached key but, of the call's keys, only their paths
+                const int n_full = TREE ? it.L - p.rows : nk0;
+                const bool full = kbase + C::BK <= it.k1 && kbase + C::BK <= n_full && kbase >= klo_last;
                 if (full) {
 #pragma unroll
                     for (int q = 0; q < V; ++q) xs[q] = __uint_as_float(sv[q]) * sc[q];
+                } else if (TREE) {
+                    const int key = kbase + k;
+                    const int i = key - (it.L - p.rows);   // the call's key i, or a cached key (< 0)
+                    const bool in_item = key >= it.klo && key < it.k1;
+#pragma unroll
+                    for (int q = 0; q < V; ++q) {
+                        const bool vis = in_item && (i < 0 || ((tmw[col0 + q] >> i) & 1u));
+                        xs[q] = vis ? __uint_as_float(sv[q]) * sc[q] : -CUDART_INF_F;
+                    }
                 } else {
                     // key is visible to row q (query row m0+q at position L-R+(m0+q)/ratio)
                     // iff qc <= q < qw; thresholds clamped to [-1, N]
@@ -818,11 +845,14 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
             float ltot[V];
             workers_reduce<V, NWT, false>(lsum, ltot, red, wq, h, lane, k);
             if (lab) misc[2] = 1u;
-            const bool item_bad = named_barrier_or(2, NWT, bad != 0);
+            const bool page_bad = named_barrier_or(2, NWT, (bad & kErrPage) != 0);
             if (misc[2]) {
                 abort = true;
                 break;
             }
+            const bool mask_bad = TREE && named_barrier_or(2, NWT, (bad & kErrMask) != 0);
+            const bool item_bad = page_bad || mask_bad;
+            const uint32_t bad_bits = (page_bad ? kErrPage : 0u) | (mask_bad ? kErrMask : 0u);
             uint32_t ov[V];
             tmem_ldV<V>(t_o + col0 + lane_off, ov);
             tc_fence_before();
@@ -844,7 +874,7 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                         ++r;
                     }
                 }
-                if (item_bad && t == 0 && p.err_word) atomicOr(p.err_word, kErrPage);
+                if (item_bad && t == 0 && p.err_word) atomicOr(p.err_word, bad_bits);
             } else {
                 const long long gq = ((long long)it.g * p.n_head_kv + it.kvh) * p.n_qtiles + it.qt;
                 const long long slot_idx = gq * p.max_splits + it.s;
@@ -859,7 +889,7 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                                    make_float2(ltot[q] == 0.f ? -CUDART_INF_F : mu[q], ltot[q]));
                     }
                 }
-                if (t == 0) __stcg(p.part_flag + slot_idx, item_bad ? kErrPage : 0u);
+                if (t == 0) __stcg(p.part_flag + slot_idx, bad_bits);
             }
             scount += T;
             tcnt += T;

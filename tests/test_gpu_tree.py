@@ -312,12 +312,12 @@ def test_chain_mask_equals_the_causal_call_bit_for_bit(wls, name):
     mask = np.tile(mask_words(chain(R)), G)
     tree, err = run_general(dw, w.q, R, mask=mask)
     assert err == 0
-    # the causal call on the same kernel: uniform offsets make it a ragged call
-    causal, _ = run_general(dw, w.q.reshape(G * R, *w.q.shape[2:]), R, cu=np.arange(G + 1) * R)
-    assert np.array_equal(tree.reshape(causal.shape), causal)
+    out, err = dw.run()   # the causal call through rad_attn_paged: the same kernel
+    assert err == 0 and np.array_equal(tree, bits(out))
 
 
-@pytest.mark.parametrize("name", ["t8_d128_bf16", "t32_d256_bf16", "t16_d256_fp8"])
+@pytest.mark.parametrize("name", ["t8_d128_bf16", "t32_d256_bf16", "t16_d256_fp8", "t8_d128_fp8",
+                                  "t32_d128_fp8_r8"])
 def test_chain_prefix_nodes_equal_the_decode_rows_bit_for_bit(wls, name):
     """A node whose ancestors are exactly the nodes before it sits where a
     decode step would, over the same keys: the rows are equal bit for bit."""
@@ -343,10 +343,11 @@ def test_chain_prefix_nodes_equal_the_decode_rows_bit_for_bit(wls, name):
             assert np.array_equal(got[g, r], dec[g]), (name, g, r)
 
 
-def test_rows_do_not_see_keys_off_their_path(wls):
+@pytest.mark.parametrize("name", ["t8_d128_bf16", "t8_d128_fp8"])
+def test_rows_do_not_see_keys_off_their_path(wls, name):
     """Changing the K/V of one node changes no row whose path misses it, and
     changing other nodes' mask words changes no row at all but theirs."""
-    w, dw = wls("tree", "t8_d128_bf16")
+    w, dw = wls("tree", name)
     R, G, P = w.cfg.rows, w.groups, w.cfg.page_size
     parents, mask = tree_inputs(w, True, 903)
     base, _ = run_general(dw, w.q, R, mask=mask.reshape(-1))
@@ -355,8 +356,12 @@ def test_rows_do_not_see_keys_off_their_path(wls):
     for g in range(G):
         pos = int(w.seq_lens[g]) - R + j
         pg = int(w.page_table[g, pos // P])
-        k2[pg, pos % P] = -k2[pg, pos % P] * 3
-        v2[pg, pos % P] = v2[pg, pos % P] + 5
+        if dw.fp8:   # other finite e4m3 codes: flip the sign bit, step the mantissa
+            k2[pg, pos % P] ^= 0x80
+            v2[pg, pos % P] = torch.where((v2[pg, pos % P] & 0x7F) < 0x70, v2[pg, pos % P] + 8, v2[pg, pos % P] - 8)
+        else:
+            k2[pg, pos % P] = -k2[pg, pos % P] * 3
+            v2[pg, pos % P] = v2[pg, pos % P] + 5
     dw2 = DevWorkload(w)
     dw2.k, dw2.v = k2, v2
     got, _ = run_general(dw2, w.q, R, mask=mask.reshape(-1))

@@ -172,12 +172,13 @@ def test_ex_workspace_follows_the_kernel_the_call_takes():
     for hd, dt in ((128, b.RAD_KV_BF16), (256, b.RAD_KV_FP8_E4M3), (128, b.RAD_KV_FP8_E4M3)):
         a = _general_args(head_dim=hd, kv_dtype=dt)
         assert ws(a) == b.workspace_bytes(4, 8, 32, 8, hd, 16, 64, dt) > 0
-    # fp8 head_dim 128 verify: the uniform call runs the tcgen05 split kernel,
-    # a ragged or tree call the verify tile; both split, with their own tiles
-    assert ws(_general_args(tree=fake, kv_dtype=b.RAD_KV_FP8_E4M3)) > 0
-    # a ragged call adds its tile map: 4 sequences x 1 tile x 8 bytes, rounded to 256
+    # fp8 head_dim 128 verify: uniform and tree calls run the tcgen05 split
+    # kernel, a ragged call the verify tile; a ragged call adds its tile map
+    # (4 sequences x 1 tile x 8 bytes, rounded to 256)
+    assert ws(_general_args(tree=fake, kv_dtype=b.RAD_KV_FP8_E4M3)) == \
+        b.workspace_bytes(4, 8, 32, 8, 128, 16, 64, b.RAD_KV_FP8_E4M3)
     assert ws(_general_args(cu=fake, kv_dtype=b.RAD_KV_FP8_E4M3)) == \
-        ws(_general_args(tree=fake, kv_dtype=b.RAD_KV_FP8_E4M3)) + 256
+        ws(_general_args(tree=fake, kv_dtype=b.RAD_KV_BF16)) + 256
     # the caller's row total bounds the tiles: 4 sequences of up to 256 rows
     # (ratio 4, 32-row tiles: 32 tiles each) holding 40 rows in all need at
     # most ceil(160 / 32) + 4 = 9 tiles instead of 128
@@ -200,7 +201,8 @@ def test_ex_workspace_follows_the_kernel_the_call_takes():
 def test_ex_describe_names_the_kernels_of_ragged_and_tree_calls():
     shape = lambda **kw: b.shape_args(64, 8, 32, 8, 128, 16, 1024, b.RAD_KV_FP8_E4M3, **kw)
     assert "family=split_tc05" in b.ex_describe(shape())
-    tree = b.ex_describe(shape(tree=True))
+    assert "family=split_tc05" in b.ex_describe(shape(tree=True))
+    tree = b.ex_describe(b.shape_args(64, 8, 32, 8, 128, 16, 1024, tree=True))
     assert tree.startswith("attn_tile family=verify") and "attn_combine" in tree
     rag = b.ex_describe(shape(ragged=True))
     assert rag.startswith("ragged_tile_map + attn_tile family=verify")
