@@ -212,7 +212,7 @@ def shape_args(groups, rows, n_head, n_head_kv, head_dim, page_size, pages_per_s
 
 
 def ex_describe(args: RadAttnPagedArgs) -> str:
-    buf = ctypes.create_string_buffer(512)
+    buf = ctypes.create_string_buffer(2048)
     rc = load().rad_attn_paged_ex_describe(ctypes.byref(args), buf, len(buf))
     if rc != RAD_OK:
         raise RadAttnError(rc, "rad_attn_paged_ex_describe")

@@ -52,8 +52,6 @@ cudaError_t launch_combine(const AttnParams& p, cudaStream_t st) {
 template <int D, bool FP8>
 cudaError_t launch_family(int family, const AttnParams& p, int sms, cudaStream_t st) {
     cudaError_t e;
-    // a ragged call maps its query tiles first
-    if (p.tile_map && (e = launch_ragged_tile_map(p, st)) != cudaSuccess) return e;
     switch (family) {
         case kFamDecode: e = launch_cfg<typename Pick<D, FP8, kFamDecode>::T>(p, sms, st); break;
         case kFamVerify: e = launch_cfg<typename Pick<D, FP8, kFamVerify>::T>(p, sms, st); break;

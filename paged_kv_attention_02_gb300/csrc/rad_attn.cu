@@ -42,6 +42,17 @@ struct Plan {
     rad::TileInfo tile;
     long long n_items;
     size_t map_bytes, flags_bytes, ml_bytes, acc_bytes, total_bytes;
+    // A ragged call whose family is the verify or wide tile runs its
+    // decode-shaped sequences (at most the decode tile's rows per KV head) on
+    // the decode tile instead, as a second tile list: `dec`.  The two tiles
+    // share one key schedule, so a row's bits do not depend on which runs it.
+    bool dual;
+    struct Part {
+        rad::TileInfo tile;
+        int n_qtiles, qtv;
+        long long n_items;
+        size_t map_bytes, flags_bytes, ml_bytes, acc_bytes;
+    } dec;
 };
 
 int check_scalars(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_dim,
@@ -126,6 +137,25 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
         pl.acc_bytes = round_up((size_t)slots * pl.qtv * head_dim * 4, 256);
     }
     pl.total_bytes = pl.map_bytes + pl.flags_bytes + pl.ml_bytes + pl.acc_bytes;
+    pl.dual = pl.ragged && (pl.family == rad::kFamVerify || pl.family == rad::kFamWide);
+    if (pl.dual) {
+        Plan::Part& d = pl.dec;
+        d.tile = tile_for(head_dim, kv_dtype, rad::kFamDecode);
+        // a decode-shaped sequence has one tile of at most QT rows, and at least one row
+        long long tiles = groups;
+        if (ragged_rows > 0 && ragged_rows < tiles) tiles = ragged_rows;
+        d.n_qtiles = (int)tiles;
+        d.qtv = d.tile.QT;
+        d.n_items = tiles * n_head_kv * pl.max_splits;
+        d.map_bytes = round_up((size_t)tiles * 8, 256);
+        if (pl.split_len > 0) {
+            const long long slots = tiles * n_head_kv * pl.max_splits;
+            d.flags_bytes = round_up((size_t)slots * 4, 256);
+            d.ml_bytes = round_up((size_t)slots * d.qtv * 2 * 4, 256);
+            d.acc_bytes = round_up((size_t)slots * d.qtv * head_dim * 4, 256);
+        }
+        pl.total_bytes += d.map_bytes + d.flags_bytes + d.ml_bytes + d.acc_bytes;
+    }
     return pl;
 }
 
@@ -294,7 +324,7 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
     const bool general = cu_seqlens || tree_mask;
     const Plan pl = make_plan(groups, rows, n_head, n_head_kv, head_dim, page_size, pages_per_seq, kv_dtype, general,
                               cu_seqlens ? total_rows : -1);
-    if (pl.n_items > 0x7FFFFFFFll) return RAD_E_SHAPE;
+    if (pl.n_items > 0x7FFFFFFFll || (pl.dual && pl.dec.n_items > 0x7FFFFFFFll)) return RAD_E_SHAPE;
     if (!q || !k_pool || !v_pool || !page_table || !seq_lens || !out) return RAD_E_ARG;
     if (!is_aligned(q, 16) || !is_aligned(k_pool, 16) || !is_aligned(v_pool, 16) || !is_aligned(out, 16) ||
         !is_aligned(page_table, 4) || !is_aligned(seq_lens, 4) || !is_aligned(err_word, 4) ||
@@ -342,6 +372,9 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
     p.window = window;
     p.scale_log2 = scale * 1.4426950408889634f;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // decode-shaped sequences of a dual ragged call: the decode tile's own
+    // tile list and partials
+    AttnParams pd = p;
     if (pl.total_bytes > 0) {
         char* ws = static_cast<char*>(workspace);
         if (pl.ragged) p.tile_map = reinterpret_cast<const int2*>(ws);
@@ -351,8 +384,44 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
             p.part_ml = reinterpret_cast<float*>(ws + pl.flags_bytes);
             p.part_acc = reinterpret_cast<float*>(ws + pl.flags_bytes + pl.ml_bytes);
         }
+        ws += pl.flags_bytes + pl.ml_bytes + pl.acc_bytes;
+        if (pl.dual) {
+            const Plan::Part& d = pl.dec;
+            pd = p;
+            pd.tile_map = reinterpret_cast<const int2*>(ws);
+            ws += d.map_bytes;
+            if (pl.split_len > 0) {
+                pd.part_flag = reinterpret_cast<uint32_t*>(ws);
+                pd.part_ml = reinterpret_cast<float*>(ws + d.flags_bytes);
+                pd.part_acc = reinterpret_cast<float*>(ws + d.flags_bytes + d.ml_bytes);
+            }
+            pd.n_qtiles = d.n_qtiles;
+            pd.qtv = d.qtv;
+            pd.qt_rows = d.tile.QT;
+            pd.n_items = (int)d.n_items;
+        }
     }
     cudaError_t e;
+    if (pl.ragged) {
+        // the tile lists of the call's sequence classes, on the device
+        rad::RaggedMaps m{};
+        m.map[0] = const_cast<int2*>(pl.dual ? pd.tile_map : p.tile_map);
+        m.qt[0] = pl.dual ? pd.qt_rows : p.qt_rows;
+        m.bound[0] = pl.dual ? pd.n_qtiles : p.n_qtiles;
+        m.map[1] = pl.dual ? const_cast<int2*>(p.tile_map) : nullptr;
+        m.qt[1] = p.qt_rows;
+        m.bound[1] = p.n_qtiles;
+        m.split_m = pd.qt_rows;
+        e = rad::launch_ragged_tile_map(p, m, st);
+        if (e != cudaSuccess) return RAD_E_CUDA;
+    }
+    if (pl.dual) {
+        e = head_dim == 128 ? (fp8 ? rad::launch_d128_fp8(rad::kFamDecode, pd, sms, st)
+                                   : rad::launch_d128_bf16(rad::kFamDecode, pd, sms, st))
+                            : (fp8 ? rad::launch_d256_fp8(rad::kFamDecode, pd, sms, st)
+                                   : rad::launch_d256_bf16(rad::kFamDecode, pd, sms, st));
+        if (e != cudaSuccess) return RAD_E_CUDA;
+    }
     if (pl.family == rad::kFamPrefillTC) {
         rc = get_encoder();
         if (rc != RAD_OK) return rc;
@@ -380,14 +449,6 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
         e = fp8 ? rad::launch_d256_fp8(pl.family, p, sms, st) : rad::launch_d256_bf16(pl.family, p, sms, st);
     return e == cudaSuccess ? RAD_OK : RAD_E_CUDA;
 }
-
-}  // namespace
-
-extern "C" {
-
-}  // extern "C"
-
-namespace {
 
 int describe_call(int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_dim, int32_t page_size,
                   int32_t kv_dtype, bool general, bool ragged, char* buf, size_t buf_len) {
@@ -419,14 +480,27 @@ int describe_call(int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_
                  family_name(pl.family), head_dim, pl.M, rad::PrefillTileKeys, pl.tile.NS, pl.tile.minb);
         return RAD_OK;
     }
-    snprintf(buf, buf_len,
-             "%sattn_tile family=%s head_dim=%d kv=%s query_rows_per_kv_head=%d tile_rows=%d "
-             "warps(q=%d,k=%d)+2 producers n_tiles_per_warp=%d keys_per_stage=%d stages=%d split_len=%d "
-             "threads=%d smem=%d ctas_per_sm=%d mma=m16n8k16.%s%s",
-             pre, family_name(pl.family), head_dim, kv_dtype == RAD_KV_FP8_E4M3 ? "fp8e4m3" : "bf16", pl.M,
-             t.QT, t.WQ, t.WK, t.NQW, t.KS, t.NS, pl.split_len, t.threads, t.smem, t.minb,
-             kv_dtype == RAD_KV_FP8_E4M3 ? "f16" : "bf16",
-             pl.split_len > 0 ? " + attn_combine (split order)" : "");
+    const auto tile_desc = [&](char* b, size_t n, int family, const rad::TileInfo& ti, int rows_kv) {
+        return snprintf(b, n,
+                        "attn_tile family=%s head_dim=%d kv=%s query_rows_per_kv_head=%d tile_rows=%d "
+                        "warps(q=%d,k=%d)+2 producers n_tiles_per_warp=%d keys_per_stage=%d stages=%d split_len=%d "
+                        "threads=%d smem=%d ctas_per_sm=%d mma=m16n8k16.%s%s",
+                        family_name(family), head_dim, kv_dtype == RAD_KV_FP8_E4M3 ? "fp8e4m3" : "bf16", rows_kv,
+                        ti.QT, ti.WQ, ti.WK, ti.NQW, ti.KS, ti.NS, pl.split_len, ti.threads, ti.smem, ti.minb,
+                        kv_dtype == RAD_KV_FP8_E4M3 ? "f16" : "bf16",
+                        pl.split_len > 0 ? " + attn_combine (split order)" : "");
+    };
+    int used = snprintf(buf, buf_len, "%s", pre);
+    if (pl.dual && used >= 0 && (size_t)used < buf_len) {
+        // sequences with at most the decode tile's rows per KV head run on it
+        const int k = tile_desc(buf + used, buf_len - used, rad::kFamDecode, pl.dec.tile, pl.dec.tile.QT);
+        if (k > 0) used += k;
+        if ((size_t)used < buf_len) {
+            const int k2 = snprintf(buf + used, buf_len - used, " + ");
+            if (k2 > 0) used += k2;
+        }
+    }
+    if (used >= 0 && (size_t)used < buf_len) tile_desc(buf + used, buf_len - used, pl.family, t, pl.M);
     return RAD_OK;
 }
 

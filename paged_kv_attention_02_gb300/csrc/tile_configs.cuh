@@ -32,7 +32,7 @@ constexpr int kSplitMaxRows = 256;
 #define RAD_TILE_D128_BF16_DEC 1, 1, 2, 32, 3, 3
 #endif
 #ifndef RAD_TILE_D128_BF16_VER
-#define RAD_TILE_D128_BF16_VER 2, 2, 2, 64, 5, 1
+#define RAD_TILE_D128_BF16_VER 4, 1, 2, 64, 2, 2
 #endif
 #ifndef RAD_TILE_D128_BF16_WIDE
 #define RAD_TILE_D128_BF16_WIDE 4, 2, 1, 64, 4, 1
@@ -133,8 +133,16 @@ cudaError_t launch_prefill_tc05(const CUtensorMap& tq, const CUtensorMap& tk, co
                                 const AttnParams& p, int sms, cudaStream_t st);
 cudaError_t launch_split_tc05(const AttnParams& p, int sms, cudaStream_t st);
 TileInfo split_tc05_info(int n);
-// Ragged calls: the tile map into p.tile_map (one CTA), before the tile kernel.
+// Ragged calls: the tile maps (one CTA), before the tile kernels.  map[1]
+// null: one class; else sequences with at most split_m query rows per KV head
+// go to map[0] (tiles of qt[0] rows), the rest to map[1].
 constexpr int kTileMapThreads = 1024;
-cudaError_t launch_ragged_tile_map(const AttnParams& p, cudaStream_t st);
+struct RaggedMaps {
+    int2* map[2];
+    int qt[2];
+    int bound[2];
+    int split_m;
+};
+cudaError_t launch_ragged_tile_map(const AttnParams& p, const RaggedMaps& m, cudaStream_t st);
 
 }  // namespace rad

@@ -178,6 +178,18 @@ class Workload:
                        tree_mask=None if self.tree_mask is None else np.ascontiguousarray(self.tree_mask[idx]))
 
 
+def compact_pool(w: Workload) -> Workload:
+    """The same call over a pool holding only the pages its sequences use
+    (page ids renumbered in pool order), e.g. after select_groups."""
+    used = np.unique(w.page_table[w.page_table >= 0])
+    remap = np.full(w.num_pages, -1, dtype=np.int32)
+    remap[used] = np.arange(used.size, dtype=np.int32)
+    table = np.where(w.page_table >= 0, remap[np.maximum(w.page_table, 0)], -1).astype(np.int32)
+    sc = (lambda a: None if a is None else np.ascontiguousarray(a[used]))
+    return replace(w, k_pool=np.ascontiguousarray(w.k_pool[used]), v_pool=np.ascontiguousarray(w.v_pool[used]),
+                   page_table=table, k_scales=sc(w.k_scales), v_scales=sc(w.v_scales))
+
+
 # ---------------------------------------------------------------- draft trees
 # A draft tree of R proposals is flattened parents-first: parents[r] < r, or
 # -1 for a node hanging directly off the cached context.  The op takes one

@@ -220,9 +220,11 @@ def test_ragged_malformed_offsets_flag_their_group_and_write_nothing_of_it(wls):
 @pytest.mark.parametrize("name", ["d128_fp8", "chunk_d128"])
 def test_ragged_row_total_bounds_the_work(wls, name):
     """The exact row total and no total (0: sized for `rows` per sequence)
-    give the same bits as q's row count.  A total of one row bounds the call
-    to ceil(ratio / tile rows) + groups tiles: past that the call raises
-    RAD_ERRW_CUSEQ and runs only its first tiles, in sequence order."""
+    give the same bits as q's row count.  A total of one row bounds each tile
+    list: the decode tile's (sequences of at most its rows per KV head) to one
+    tile, the main tile's to ceil(ratio / tile rows) + groups; past a bound the
+    call raises RAD_ERRW_CUSEQ and runs only the list's first tiles, in
+    sequence order."""
     w, dw = wls("ragged", name)
     q_lens = RAGGED[name][1]
     q, cu = ragged_q(w, q_lens, base=2, tail=5)
@@ -234,19 +236,28 @@ def test_ragged_row_total_bounds_the_work(wls, name):
     ratio = c.n_head // c.n_head_kv
     desc = b.ex_describe(b.shape_args(w.groups, max(q_lens), c.n_head, c.n_head_kv, c.head_dim, c.page_size,
                                       w.pages_per_seq, c.kv_dtype, ragged=True))
-    qt = int(desc.split("tile_rows=")[1].split()[0])
-    tiles = [-(-ql * ratio // qt) for ql in q_lens]
-    bound = -(-ratio // qt) + len(q_lens)
+    qts = [int(x.split()[0]) for x in desc.split("tile_rows=")[1:]]
+    dual = len(qts) == 2
+    qt_dec, qt_main = (qts[0], qts[1]) if dual else (None, qts[0])
+    G = len(q_lens)
+    bounds = {"dec": 1, "main": min(-(-ratio // qt_main) + G, G * -(-max(q_lens) * ratio // qt_main))}
     got, err = run_general(dw, q, max(q_lens), cu=cu, total_rows=1)
-    assert err == (b.RAD_ERRW_CUSEQ if sum(tiles) > bound else 0)
-    done = 0   # rows of the tiles within the bound match; the rest stay unwritten
+    done = {"dec": 0, "main": 0}
+    over = False
     for g, ql in enumerate(q_lens):
-        run = max(0, min(tiles[g], bound - done))
+        if ql == 0:
+            continue
+        cls = "dec" if dual and ql * ratio <= qt_dec else "main"
+        qt = qt_dec if cls == "dec" else qt_main
+        tiles = -(-ql * ratio // qt)
+        run = max(0, min(tiles, bounds[cls] - done[cls]))
+        over |= run < tiles
         rows_run = min(ql, run * qt // ratio)
         a = int(cu[g])
         assert np.array_equal(got[a:a + rows_run], ref[a:a + rows_run]), g
         assert np.all(got[a + rows_run:a + ql] == np.int16(SENTINEL)), g
-        done += tiles[g]
+        done[cls] += tiles
+    assert err == (b.RAD_ERRW_CUSEQ if over else 0)
 
 
 def test_ragged_sequence_shorter_than_its_rows_is_zero_and_flagged(wls):

@@ -5,9 +5,11 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 from paged_kv_attention_02_gb300 import binding as b
+from paged_kv_attention_02_gb300 import workloads as wl
 from paged_kv_attention_02_gb300.build import build_library
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "rad_attn.h")
@@ -173,12 +175,14 @@ def test_ex_workspace_follows_the_kernel_the_call_takes():
         a = _general_args(head_dim=hd, kv_dtype=dt)
         assert ws(a) == b.workspace_bytes(4, 8, 32, 8, hd, 16, 64, dt) > 0
     # fp8 head_dim 128 verify: uniform and tree calls run the tcgen05 split
-    # kernel, a ragged call the verify tile; a ragged call adds its tile map
-    # (4 sequences x 1 tile x 8 bytes, rounded to 256)
+    # kernel; a ragged call runs the verify tile plus, for its decode-shaped
+    # sequences, the decode tile: two tile maps (256 bytes each here) and two
+    # sets of partials
     assert ws(_general_args(tree=fake, kv_dtype=b.RAD_KV_FP8_E4M3)) == \
         b.workspace_bytes(4, 8, 32, 8, 128, 16, 64, b.RAD_KV_FP8_E4M3)
-    assert ws(_general_args(cu=fake, kv_dtype=b.RAD_KV_FP8_E4M3)) == \
-        ws(_general_args(tree=fake, kv_dtype=b.RAD_KV_BF16)) + 256
+    verify_part = ws(_general_args(tree=fake, kv_dtype=b.RAD_KV_BF16))
+    decode_part = b.workspace_bytes(4, 2, 32, 8, 128, 16, 64)   # the decode tile's partials: 8-row slots
+    assert ws(_general_args(cu=fake, kv_dtype=b.RAD_KV_FP8_E4M3)) == verify_part + decode_part + 2 * 256
     # the caller's row total bounds the tiles: 4 sequences of up to 256 rows
     # (ratio 4, 32-row tiles: 32 tiles each) holding 40 rows in all need at
     # most ceil(160 / 32) + 4 = 9 tiles instead of 128
@@ -190,9 +194,10 @@ def test_ex_workspace_follows_the_kernel_the_call_takes():
     assert ws(small) == 0
     assert int(b.load().rad_attn_paged_ex(ctypes.byref(small), None)) == b.RAD_E_ARG
     # chunks past the split limit need no partials: a uniform call needs
-    # nothing, a ragged one its tile map (4 x ceil(1200 / 64) tiles x 8 bytes)
+    # nothing, a ragged one its tile maps (4 x ceil(1200 / 64) tiles x 8 bytes
+    # for the wide tile, 4 x 8 bytes for the decode tile, each rounded to 256)
     assert b.workspace_bytes(4, 300, 32, 8, 128, 16, 64) == 0
-    assert ws(_general_args(rows=300, cu=fake)) == 768
+    assert ws(_general_args(rows=300, cu=fake)) == 768 + 256
     bad = _general_args()
     bad.struct_size = 8
     assert ws(bad) == 0
@@ -205,7 +210,25 @@ def test_ex_describe_names_the_kernels_of_ragged_and_tree_calls():
     tree = b.ex_describe(b.shape_args(64, 8, 32, 8, 128, 16, 1024, tree=True))
     assert tree.startswith("attn_tile family=verify") and "attn_combine" in tree
     rag = b.ex_describe(shape(ragged=True))
-    assert rag.startswith("ragged_tile_map + attn_tile family=verify")
+    assert rag.startswith("ragged_tile_map + attn_tile family=decode")
+    assert " + attn_tile family=verify" in rag and rag.count("attn_combine") == 2
     chunk = b.ex_describe(b.shape_args(4, 300, 32, 8, 128, 16, 64, ragged=True))
-    assert chunk.startswith("ragged_tile_map + attn_tile family=wide") and "split_len=0" in chunk
+    assert chunk.startswith("ragged_tile_map + attn_tile family=decode") and " + attn_tile family=wide" in chunk
+    assert "attn_combine" not in chunk
+    dec = b.ex_describe(b.shape_args(4, 2, 32, 8, 128, 16, 64, ragged=True))
+    assert dec.startswith("ragged_tile_map + attn_tile family=decode") and dec.count("attn_tile") == 1
     assert b.describe(300, 32, 8, 128, 16).startswith("attn_prefill_tc05")
+
+
+def test_compact_pool_keeps_the_call():
+    """A subset of sequences re-paged into a pool of only their pages gives the
+    oracle's same bits."""
+    import oracle
+    w = wl.make_workload("tiny_decode")
+    sub = w.select_groups([3, 1])
+    small = wl.compact_pool(sub)
+    assert small.num_pages == int(((sub.seq_lens + 15) // 16).sum())
+    a = oracle.attn_paged(sub.q, sub.k_pool, sub.v_pool, sub.page_table, sub.seq_lens, **sub.call_args()).out
+    c = oracle.attn_paged(small.q, small.k_pool, small.v_pool, small.page_table, small.seq_lens,
+                          **small.call_args()).out
+    assert np.array_equal(a, c)
