@@ -85,7 +85,7 @@ struct PrefItem {
 
 // GEN: the call has a sliding window or a scale <= 0; without either, those
 // terms fold away at compile time.
-template <bool GEN>
+template <bool GEN, int BM = PrefillCfg::BM, int BN = PrefillCfg::BN>
 __device__ __forceinline__ PrefItem plan_prefill(int item, const AttnParams& p) {
     PrefItem it;
     const int per_g = p.n_head_kv * p.n_qtiles;
@@ -95,12 +95,12 @@ __device__ __forceinline__ PrefItem plan_prefill(int item, const AttnParams& p) 
     it.qt = p.n_qtiles - 1 - (rem - it.kvh * p.n_qtiles);   // later tiles see more keys: first
     it.L = __ldg(p.seq_lens + it.g);
     it.seq_ok = it.L >= p.rows && (long long)it.L <= (long long)p.pages_per_seq * p.page_size;
-    it.m0 = it.qt * PrefillCfg::BM;
-    it.m_end = min(p.M, it.m0 + PrefillCfg::BM);
+    it.m0 = it.qt * BM;
+    it.m_end = min(p.M, it.m0 + BM);
     it.kmax = it.seq_ok ? it.L - p.rows + (it.m_end - 1) / p.ratio + 1 : 0;
     it.klo = (GEN && it.seq_ok) ? first_visible_key(it.L, p.rows, it.m0 / p.ratio, p.window) : 0;
-    it.kt0 = it.klo / PrefillCfg::BN;
-    it.T = (it.kmax + PrefillCfg::BN - 1) / PrefillCfg::BN - it.kt0;
+    it.kt0 = it.klo / BN;
+    it.T = (it.kmax + BN - 1) / BN - it.kt0;
     return it;
 }
 

@@ -185,6 +185,19 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
 
 // Packs (lo, hi) into bf16x2 / f16x2 with round-to-nearest-even; `lo` lands in
 // the low 16 bits.
+// Two floats -> two e4m3 codes (round to nearest even, saturating; `lo` in the
+// low byte).
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// Exact values of two e4m3 codes (the low byte first).
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t codes) {
+    const uint32_t h = e4m3x2_to_f16x2((uint16_t)codes);
+    return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));

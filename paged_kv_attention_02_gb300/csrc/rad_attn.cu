@@ -74,11 +74,11 @@ rad::TileInfo tile_for(int head_dim, int kv_dtype, int family) {
     return fp8 ? rad::tile_info<256, true>(family) : rad::tile_info<256, false>(family);
 }
 
-// Prefill chunks (no split) with head_dim 128 and bf16 pools run on the
-// tcgen05 kernel when whole query heads tile its 128-row blocks.
+// Prefill chunks (no split) with head_dim 128 run on the tcgen05 prefill
+// kernels (bf16 and fp8 pools) when whole query heads tile their 128-row blocks.
 bool use_prefill_tc(int32_t rows, int32_t ratio, int32_t head_dim, int32_t kv_dtype) {
-    return rows > rad::kSplitMaxRows && head_dim == 128 && kv_dtype == RAD_KV_BF16 && ratio <= 128 &&
-           128 % ratio == 0;
+    (void)kv_dtype;
+    return rows > rad::kSplitMaxRows && head_dim == 128 && ratio <= 128 && 128 % ratio == 0;
 }
 
 // `general`: a call with ragged rows (cu_seqlens) or tree masks.  Ragged
@@ -182,15 +182,19 @@ int get_encoder() {
     return RAD_OK;
 }
 
-// Tiled TMA descriptor with 128-byte swizzle over a bf16 tensor (dims and
-// box innermost first, strides in bytes for dims 1..rank-1).
-int encode_bf16_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-                    const cuuint32_t* box) {
+// Tiled TMA descriptor with 128-byte swizzle over a bf16 or byte (e4m3 code)
+// tensor (dims and box innermost first, strides in bytes for dims 1..rank-1).
+int encode_map(CUtensorMap* m, CUtensorMapDataType type, const void* ptr, int rank, const cuuint64_t* dims,
+               const cuuint64_t* strides, const cuuint32_t* box) {
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box,
-                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    CUresult r = g_encode(m, type, rank, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? RAD_OK : RAD_E_CUDA;
+}
+int encode_bf16_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                    const cuuint32_t* box) {
+    return encode_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ptr, rank, dims, strides, box);
 }
 
 // ------------------------------------------------------------------ device facts
@@ -422,7 +426,20 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
                                    : rad::launch_d256_bf16(rad::kFamDecode, pd, sms, st));
         if (e != cudaSuccess) return RAD_E_CUDA;
     }
-    if (pl.family == rad::kFamPrefillTC) {
+    if (pl.family == rad::kFamPrefillTC && fp8) {
+        rc = get_encoder();
+        if (rc != RAD_OK) return rc;
+        // e4m3 pools viewed as [tokens][n_head_kv][128 bytes]: one box = one page of one KV head
+        const cuuint64_t kd[3] = {(cuuint64_t)head_dim, (cuuint64_t)n_head_kv,
+                                  (cuuint64_t)num_pages * (cuuint64_t)page_size};
+        const cuuint64_t ks[2] = {(cuuint64_t)head_dim, (cuuint64_t)n_head_kv * head_dim};
+        const cuuint32_t kb[3] = {(cuuint32_t)head_dim, 1, (cuuint32_t)page_size};
+        CUtensorMap tk, tv;
+        if (encode_map(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, k_pool, 3, kd, ks, kb) != RAD_OK ||
+            encode_map(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, v_pool, 3, kd, ks, kb) != RAD_OK)
+            return RAD_E_CUDA;
+        e = rad::launch_prefill_fp8(tk, tv, p, sms, st);
+    } else if (pl.family == rad::kFamPrefillTC) {
         rc = get_encoder();
         if (rc != RAD_OK) return rc;
         // q viewed as [groups][rows][n_head][head_dim]: one box = 128 query rows
@@ -470,6 +487,15 @@ int describe_call(int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_
                  "e4m3 terms, PV kind::f16 with V e4m3 -> f16 once per tile) "
                  "split_len=%d + attn_combine (split order)",
                  family_name(pl.family), head_dim, pl.M, t.QT, t.KS, t.NS, pl.split_len);
+        return RAD_OK;
+    }
+    if (pl.family == rad::kFamPrefillTC && kv_dtype == RAD_KV_FP8_E4M3) {
+        snprintf(buf, buf_len,
+                 "attn_prefill_tc05 family=%s head_dim=%d kv=fp8e4m3 query_rows_per_kv_head=%d tile_rows=128 "
+                 "keys_per_tile=128 stages=%d ctas_per_sm=1 warps=4 softmax+1 mma+1 producer+2 v converters "
+                 "mma=tcgen05 (QK kind::f8f6f4 on the staged e4m3 K with Q as two e4m3 terms, PV kind::f16 with "
+                 "V e4m3 -> f16 once per tile and P f16 from TMEM) split_len=0",
+                 family_name(pl.family), head_dim, pl.M, RAD_PREFILL_FP8_NS);
         return RAD_OK;
     }
     if (pl.family == rad::kFamPrefillTC) {

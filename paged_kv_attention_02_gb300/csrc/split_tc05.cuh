@@ -132,19 +132,6 @@ struct SplitTcCfg {
 };
 
 
-// Two floats -> two e4m3 codes (round to nearest even, saturating; `lo` in the
-// low byte).
-__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-// Exact values of two e4m3 codes (the low byte first).
-__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t codes) {
-    const uint32_t h = e4m3x2_to_f16x2((uint16_t)codes);
-    return __half22float2(*reinterpret_cast<const __half2*>(&h));
-}
-
 // Converts share h of key row t of a staged tile (128 e4m3 codes, 16-byte
 // chunks swizzled by t & 7): chunks h*CPT .. h*CPT+CPT-1 (16 codes each)
 // become f16 in an f16 tile [column block][key][128 B] with the same 128-byte

@@ -86,6 +86,9 @@ template <> struct Pick<256, true,  kFamWide>   { using T = TileCfg<256, true,  
 #ifndef RAD_PREFILL_NS
 #define RAD_PREFILL_NS 3
 #endif
+#ifndef RAD_PREFILL_FP8_NS
+#define RAD_PREFILL_FP8_NS 3   // stages of the fp8 tcgen05 prefill kernel
+#endif
 #ifndef RAD_PREFILL_CTAS
 #define RAD_PREFILL_CTAS 1
 #endif
@@ -131,6 +134,8 @@ cudaError_t launch_d256_bf16(int family, const AttnParams& p, int sms, cudaStrea
 cudaError_t launch_d256_fp8(int family, const AttnParams& p, int sms, cudaStream_t st);
 cudaError_t launch_prefill_tc05(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const AttnParams& p, int sms, cudaStream_t st);
+cudaError_t launch_prefill_fp8(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
+                               cudaStream_t st);
 cudaError_t launch_split_tc05(const AttnParams& p, int sms, cudaStream_t st);
 TileInfo split_tc05_info(int n);
 // Ragged calls: the tile maps (one CTA), before the tile kernels.  map[1]

@@ -96,6 +96,10 @@ CONFIGS: dict[str, Config] = {
     "prefill_chunk": Config("prefill_chunk", 1, 2048, 32, 8, 128, 16, KV_BF16, 4, "fixed:8192",
                             pages_per_seq=512, pool_pages=512,
                             meta=dict(n_head=32, n_head_kv=8, head_dim=128, n_embd=4096)),
+    # The prefill chunk over fp8-e4m3 pools (per-page scales).
+    "prefill_chunk_fp8": Config("prefill_chunk_fp8", 1, 2048, 32, 8, 128, 16, KV_FP8_E4M3, 7, "fixed:8192",
+                                pages_per_seq=512, pool_pages=512,
+                                meta=dict(n_head=32, n_head_kv=8, head_dim=128, n_embd=4096)),
     # The verify round as a draft tree of 8 proposals per sequence instead of
     # a chain ("Radiance architecture plugins", section "Declare: drafters,
     # encoders, generators": rad_drafter_tree).

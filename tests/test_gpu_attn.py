@@ -39,6 +39,13 @@ MID = {
                          pages_per_seq=64),
     "prefill_fp8_d256": wl.Config("prefill_fp8_d256", 1, 260, 4, 1, 256, 32, wl.KV_FP8_E4M3, 111,
                                   "fixed:900", pages_per_seq=30),
+    # head_dim 128 fp8 prefill chunks: the tcgen05 e4m3 kernel (ratios 4, 8, 1; both page sizes)
+    "prefill_fp8": wl.Config("prefill_fp8", 2, 300, 8, 2, 128, 16, wl.KV_FP8_E4M3, 113, "fixed:300,1000",
+                             pages_per_seq=64),
+    "prefill_fp8_p32_r8": wl.Config("prefill_fp8_p32_r8", 1, 520, 16, 2, 128, 32, wl.KV_FP8_E4M3, 114,
+                                    "fixed:1800", pages_per_seq=60),
+    "prefill_fp8_r1": wl.Config("prefill_fp8_r1", 2, 272, 4, 4, 128, 16, wl.KV_FP8_E4M3, 115,
+                                "fixed:272,2000", pages_per_seq=130),
 }
 
 
@@ -137,8 +144,9 @@ def test_full_size_rows_are_bit_identical_across_batch_compositions(full, name):
             assert np.array_equal(ob[i], base[g]), f"group {g} in a shuffled padded batch"
 
 
-def test_prefill_rows_bit_identical_alone_and_batched(mid):
-    w, dw = mid("prefill")
+@pytest.mark.parametrize("name", ["prefill", "prefill_fp8", "prefill_fp8_r1"])
+def test_prefill_rows_bit_identical_alone_and_batched(mid, name):
+    w, dw = mid(name)
     out, _ = dw.run()
     o1, _ = dw.run(q=dw.q[1:2], table=dw.table[1:2], lens=dw.lens[1:2])
     assert np.array_equal(bits(o1)[0], bits(out)[1])
@@ -217,7 +225,7 @@ def test_verify_bad_page_in_a_late_split_zeroes_every_row(mid):
     assert np.all(ob[4] == 0) and np.array_equal(ob[:4], gb[:4])
 
 
-@pytest.mark.parametrize("name", ["chunk_split", "prefill", "prefill_fp8_d256"])
+@pytest.mark.parametrize("name", ["chunk_split", "prefill", "prefill_fp8_d256", "prefill_fp8"])
 def test_bad_last_page_zeroes_rows_of_every_query_tile(mid, name):
     # Calls with several query tiles per KV head: the early tiles never load
     # the last page, yet a bad id there zeroes every row of the group.
@@ -233,7 +241,7 @@ def test_bad_last_page_zeroes_rows_of_every_query_tile(mid, name):
     assert np.all(ob[g] == 0) and np.array_equal(ob[:g], gb[:g])
 
 
-@pytest.mark.parametrize("name", ["prefill", "dec128", "ver_fp8", "chunk_split"])
+@pytest.mark.parametrize("name", ["prefill", "dec128", "ver_fp8", "chunk_split", "prefill_fp8"])
 @pytest.mark.parametrize("scale", [0.0, -0.07])
 def test_zero_and_negative_scales_match_oracle(mid, name, scale):
     # scale 0: every visible key weighs the same; scale < 0 reverses the order

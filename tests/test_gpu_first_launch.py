@@ -40,6 +40,8 @@ CASES = [
     ("split_tc05_verify", (6, 8, 32, 8, 128, 16, 1, 211, "fixed:8,900,2000,3100,40,5000"), 320, 0),
     ("tile_decode", (8, 1, 32, 8, 128, 16, 0, 212, "fixed:1,17,700,1025,2048,3000,4100,5000"), 320, 0),
     ("tile_verify_d256", (4, 8, 16, 2, 256, 32, 0, 213, "fixed:8,700,2100,4000"), 130, 0),
+    ("prefill_fp8_window", (3, 300, 8, 2, 128, 16, 1, 214, "fixed:300,1000,2500"), 160, 257),
+    ("prefill_fp8_plain", (2, 384, 8, 2, 128, 16, 1, 215, "fixed:384,2000"), 160, 0),
 ]
 
 

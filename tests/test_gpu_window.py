@@ -41,6 +41,10 @@ WIN = {
                                  pages_per_seq=60), 64),
     "prefill_fp8_d256_w100": (wl.Config("prefill_fp8_d256_w100", 1, 260, 4, 1, 256, 32, wl.KV_FP8_E4M3,
                                         211, "fixed:900", pages_per_seq=30), 100),
+    "prefill_fp8_w257": (wl.Config("prefill_fp8_w257", 3, 300, 8, 2, 128, 16, wl.KV_FP8_E4M3, 212,
+                                   "fixed:300,1000,2500", pages_per_seq=160), 257),
+    "prefill_fp8_w64": (wl.Config("prefill_fp8_w64", 1, 520, 4, 1, 128, 32, wl.KV_FP8_E4M3, 213, "fixed:1800",
+                                  pages_per_seq=60), 64),
 }
 
 
@@ -86,7 +90,7 @@ def test_window_matches_oracle_everywhere(win, name):
     assert_parity(as_f64(out), ref.out, dw.fp8, name)
 
 
-@pytest.mark.parametrize("name", ["ver_fp8_w513", "prefill_tc_w257", "dec_d256_w48"])
+@pytest.mark.parametrize("name", ["ver_fp8_w513", "prefill_tc_w257", "dec_d256_w48", "prefill_fp8_w257"])
 def test_window_zero_and_window_past_the_context_equal_the_plain_op(name):
     w = wl.make_workload(WIN[name][0], poison=True)      # nothing poisoned below a window
     dw = DevWorkload(w)
@@ -114,7 +118,7 @@ def test_windowed_verified_rows_equal_windowed_decode_rows_bit_for_bit(win, name
         assert np.array_equal(bits(out)[:, 0], vb[:, r]), f"{name}: row {r} differs from its decode step"
 
 
-@pytest.mark.parametrize("name", ["dec128_w1000", "ver_fp8_w513", "prefill_tc_w257"])
+@pytest.mark.parametrize("name", ["dec128_w1000", "ver_fp8_w513", "prefill_tc_w257", "prefill_fp8_w64"])
 def test_windowed_rows_are_bit_identical_alone_and_batched(win, name):
     w, dw, W = win(name)
     out, _ = dw.run(window=W)
