@@ -12,21 +12,26 @@
 // first row's window are skipped.
 //
 // Warp roles (one CTA per SM, persistent over items, heavier query tiles first):
-//   warp 5      producer: TMA loads of the item's query rows (one 4-D box per
+//   warp 6      K producer: TMA loads of the item's query rows (one 4-D box per
 //               128-byte column block) and, per 128-key tile, of every page's
-//               K and V rows (one 3-D box per page and column block) into a
-//               ring of 3 stages; pages past the tile's range are loaded from
-//               an out-of-range coordinate, which TMA fills with zeros.
-//   warp 4      MMA: lane 0 issues, per tile j,
-//                 S_j   = Q K_j^T  (M 128, N 128, K = head_dim; both operands
-//                                   in shared memory, K-major, 128-byte swizzle)
-//               into one of two TMEM buffers, and then, once the softmax has
-//               written P_{j-1}, O += P_{j-1} V_{j-1} (A = P from TMEM, B = V
-//               MN-major from shared memory); tcgen05.commit signals each.
-//               The warp also zeroes V rows past the sequence's end in the
-//               tile that holds its last page, and the rows below the tile's
-//               first visible key in the first live page of a window (P is 0
-//               there, V must not be NaN).
+//               K rows (one 3-D box per page and column block) into a ring of
+//               K tiles, each free again once its QK is done; pages past the
+//               tile's range load from an out-of-range coordinate (zero fill).
+//   warp 7      V producer: the same for V rows, into a ring of V tiles, each
+//               free again once its PV is done.  (With one ring of K+V stages
+//               a tile's K waited for its PV too, and a stage's ~1.8 us load
+//               could not hide behind three stages.)
+//   warp 4      QK issue: lane 0 issues S_j = Q K_j^T (M 128, N 128, K =
+//               head_dim; both operands in shared memory, K-major, 128-byte
+//               swizzle) into TMEM buffer j & 1 once K_j landed and PV_{j-2}
+//               (which read the P held there) is done.
+//   warp 5      PV issue: once the softmax has written P_j, lane 0 issues
+//               O += P_j V_j (A = P from TMEM, B = V MN-major from shared
+//               memory).  The warp also zeroes V rows past the sequence's end
+//               in the tile that holds its last page, and the rows below the
+//               tile's first visible key in the first live page of a window
+//               (P is 0 there, V must not be NaN).  Separate issuing warps keep
+//               a late K tile from holding up the PV of a finished P.
 //   warps 0-3   softmax: thread t owns query row t (TMEM lane t); per tile it
 //               reads S_j with tcgen05.ld, masks, keeps the running max in
 //               log2 units and rescales O in TMEM only when the max grew by
@@ -49,21 +54,24 @@ struct PrefillCfg {
     static constexpr int D = 128;
     static constexpr int BM = 128;   // query rows per item
     static constexpr int BN = RAD_PREFILL_BN;     // keys per tile (64 or 128)
-    static constexpr int NS = RAD_PREFILL_NS;     // K/V stages
+    static constexpr int NSK = RAD_PREFILL_NSK;   // K stages: a K tile is free once its QK is done
+    static constexpr int NSV = RAD_PREFILL_NSV;   // V stages: a V tile is free once its PV is done
     static constexpr int CTAS = RAD_PREFILL_CTAS; // CTAs sharing an SM
     static constexpr int HB_BYTES = BN * 128;             // one 128-byte column block of a K/V tile
     static constexpr int QHB_BYTES = BM * 128;            // one 128-byte column block of the query tile
     static constexpr int TILE_BYTES = BN * D * 2;         // K or V tile
     static constexpr int Q_BYTES = BM * D * 2;
-    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_STAGE = Q_BYTES;
-    static constexpr int OFF_BARS = OFF_STAGE + NS * STAGE_BYTES;
-    // q_full, q_empty, k_full[NS], v_full[NS], kv_empty[NS], s_full[2], p_full[2], pv_done[2], o_free, final
-    static constexpr int NBARS = 2 + 3 * NS + 2 + 2 + 2 + 2;
+    static constexpr int OFF_K = Q_BYTES;                    // NSK K tiles
+    static constexpr int OFF_V = OFF_K + NSK * TILE_BYTES;   // NSV V tiles
+    static constexpr int OFF_BARS = OFF_V + NSV * TILE_BYTES;
+    // q_full, q_empty, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[2], p_full[2],
+    // pv_done[2], o_free, final[2] (one per issuing warp)
+    static constexpr int NBARS = 2 + 2 * NSK + 2 * NSV + 2 + 2 + 2 + 1 + 2;
     static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
-    static constexpr int NTHREADS = 6 * 32;
+    static constexpr int NTHREADS = 8 * 32;   // 4 softmax, QK issue, PV issue, K (+Q) and V producers
+    static constexpr int W_QK = 4, W_PV = 5, W_PROD_K = 6, W_PROD_V = 7;
     // tensor memory: O in columns [0,128), S buffer b in [128 + b*BN, 128 + (b+1)*BN);
     // P of a tile is written over its S buffer as bf16 pairs: hi in the first
     // BN/2 columns, lo in the next BN/2
@@ -117,9 +125,10 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
     const uint32_t bar_q_full = base + C::OFF_BARS;
     const uint32_t bar_q_empty = bar_q_full + 8;
     const uint32_t bar_k_full = bar_q_empty + 8;
-    const uint32_t bar_v_full = bar_k_full + 8 * C::NS;
-    const uint32_t bar_kv_empty = bar_v_full + 8 * C::NS;
-    const uint32_t bar_s_full = bar_kv_empty + 8 * C::NS;
+    const uint32_t bar_k_empty = bar_k_full + 8 * C::NSK;
+    const uint32_t bar_v_full = bar_k_empty + 8 * C::NSK;
+    const uint32_t bar_v_empty = bar_v_full + 8 * C::NSV;
+    const uint32_t bar_s_full = bar_v_empty + 8 * C::NSV;
     const uint32_t bar_p_full = bar_s_full + 16;
     // PV of tile t completes a phase of pv_done[t & 1].  A thread that has seen
     // S of tile t knows PV(t-2) is done (the MMA warp issues QK(t) after
@@ -138,10 +147,13 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
     if (threadIdx.x == 0) {
         mbar_init(bar_q_full, 1);
         mbar_init(bar_q_empty, 1);
-        for (int i = 0; i < C::NS; ++i) {
+        for (int i = 0; i < C::NSK; ++i) {
             mbar_init(bar_k_full + 8 * i, 1);
+            mbar_init(bar_k_empty + 8 * i, 1);
+        }
+        for (int i = 0; i < C::NSV; ++i) {
             mbar_init(bar_v_full + 8 * i, 1);
-            mbar_init(bar_kv_empty + 8 * i, 1);
+            mbar_init(bar_v_empty + 8 * i, 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_s_full + 8 * i, 1);
@@ -151,10 +163,11 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
         mbar_init(bar_pv_done + 8, 1);
         mbar_init(bar_o_free, 4);
         mbar_init(bar_final, 1);
+        mbar_init(bar_final + 8, 1);
         misc[1] = 0;
         fence_mbarrier_init();
     }
-    if (warp == 4) {
+    if (warp == C::W_QK) {
         tmem_alloc(base + C::OFF_MISC, C::TMEM_COLS);
         tmem_relinquish();
     }
@@ -168,40 +181,47 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
     const int n_items = p.n_items;
     bool abort = false;
 
-    if (warp == 5) {
-        // ===================================================== producer
+    if (warp == C::W_PROD_K || warp == C::W_PROD_V) {
+        // ===================================================== producers: K (and the query tile), V
+        const bool is_k = warp == C::W_PROD_K;
+        const int NSX = is_k ? C::NSK : C::NSV;
+        const uint32_t bar_full = is_k ? bar_k_full : bar_v_full;
+        const uint32_t bar_empty = is_k ? bar_k_empty : bar_v_empty;
+        const uint32_t ring = base + (is_k ? C::OFF_K : C::OFF_V);
+        const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
         const uint64_t pol = policy_evict_last();   // K/V tiles are re-read by every query tile
         const int P = p.page_size;
         const int ppt = C::BN / P;
         const int oob_tok = p.num_pages * P;
         uint32_t sc = 0, ic = 0;
         if (lane == 0) {
-            prefetch_tmap(&tm_q);
-            prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_v);
+            if (is_k) prefetch_tmap(&tm_q);
+            prefetch_tmap(tm);
         }
         for (int item = blockIdx.x; item < n_items && !abort; item += gridDim.x) {
             const PrefItem it = plan_prefill<GEN>(item, p);
             if (!it.seq_ok) continue;
-            if (ic >= 1 && !mbar_wait_bounded(bar_q_empty, (ic - 1) & 1u, kWaitLimitNs)) {
-                abort = true;
-                break;
-            }
-            if (lane == 0) {
-                mbar_arrive_expect_tx(bar_q_full, C::Q_BYTES);
+            if (is_k) {
+                if (ic >= 1 && !mbar_wait_bounded(bar_q_empty, (ic - 1) & 1u, kWaitLimitNs)) {
+                    abort = true;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar_q_full, C::Q_BYTES);
 #pragma unroll
-                for (int hb = 0; hb < 2; ++hb)
-                    tma_load_4d(base + C::OFF_Q + hb * C::QHB_BYTES, &tm_q, bar_q_full, hb * 64, it.kvh * p.ratio,
-                                it.m0 / p.ratio, it.g, pol);
+                    for (int hb = 0; hb < 2; ++hb)
+                        tma_load_4d(base + C::OFF_Q + hb * C::QHB_BYTES, &tm_q, bar_q_full, hb * 64, it.kvh * p.ratio,
+                                    it.m0 / p.ratio, it.g, pol);
+                }
+                ++ic;
             }
-            ++ic;
             const int page_hi = (it.kmax + P - 1) / P;
             const int page_lo = GEN ? it.klo / P : 0;   // pages below hold no visible key: never read
             const int32_t* trow = p.page_table + (long long)it.g * p.pages_per_seq;
             int batch0 = -1 << 30, my_pg = 0;
             for (int j = 0; j < it.T; ++j) {
-                const uint32_t st = sc % C::NS, use = sc / C::NS;
-                if (use >= 1 && !mbar_wait_bounded(bar_kv_empty + 8 * st, (use - 1) & 1u, kWaitLimitNs)) {
+                const uint32_t st = sc % (uint32_t)NSX, use = sc / (uint32_t)NSX;
+                if (use >= 1 && !mbar_wait_bounded(bar_empty + 8 * st, (use - 1) & 1u, kWaitLimitNs)) {
                     abort = true;
                     break;
                 }
@@ -215,23 +235,17 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
                         my_pg = (pg < 0 || pg >= p.num_pages) ? 0 : pg;
                     }
                 }
-                const uint32_t kdst = base + C::OFF_STAGE + st * C::STAGE_BYTES;
-                const uint32_t vdst = kdst + C::TILE_BYTES;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(bar_k_full + 8 * st, C::TILE_BYTES);
-                    mbar_arrive_expect_tx(bar_v_full + 8 * st, C::TILE_BYTES);
-                }
+                const uint32_t dst = ring + st * C::TILE_BYTES;
+                if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * st, C::TILE_BYTES);
                 for (int i = 0; i < ppt; ++i) {
                     const int pi = pstart + i;
                     const int pg = __shfl_sync(0xffffffffu, my_pg, (pi - batch0) & 31);
                     const int tok = ((!GEN || pi >= page_lo) && pi < page_hi) ? pg * P : oob_tok;
                     if (lane == 0) {
 #pragma unroll
-                        for (int hb = 0; hb < 2; ++hb) {
-                            const uint32_t o = hb * C::HB_BYTES + i * P * 128;
-                            tma_load_3d(kdst + o, &tm_k, bar_k_full + 8 * st, hb * 64, it.kvh, tok, pol);
-                            tma_load_3d(vdst + o, &tm_v, bar_v_full + 8 * st, hb * 64, it.kvh, tok, pol);
-                        }
+                        for (int hb = 0; hb < 2; ++hb)
+                            tma_load_3d(dst + hb * C::HB_BYTES + i * P * 128, tm, bar_full + 8 * st, hb * 64, it.kvh,
+                                        tok, pol);
                     }
                 }
                 ++sc;
@@ -240,17 +254,14 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
         }
         // drain: nothing may still be landing in shared memory at exit
         if (lane == 0) {
-            const uint32_t first = sc > (uint32_t)C::NS ? sc - C::NS : 0u;
-            for (uint32_t c = first; c < sc; ++c) {
-                mbar_wait_bounded(bar_k_full + 8 * (c % C::NS), (c / C::NS) & 1u, kWaitLimitNs);
-                mbar_wait_bounded(bar_v_full + 8 * (c % C::NS), (c / C::NS) & 1u, kWaitLimitNs);
-            }
-            if (ic >= 1) mbar_wait_bounded(bar_q_full, (ic - 1) & 1u, kWaitLimitNs);
+            const uint32_t first = sc > (uint32_t)NSX ? sc - NSX : 0u;
+            for (uint32_t c = first; c < sc; ++c)
+                mbar_wait_bounded(bar_full + 8 * (c % NSX), (c / NSX) & 1u, kWaitLimitNs);
+            if (is_k && ic >= 1) mbar_wait_bounded(bar_q_full, (ic - 1) & 1u, kWaitLimitNs);
         }
-    } else if (warp == 4) {
-        // ===================================================== MMA issue
+    } else if (warp == C::W_QK) {
+        // ===================================================== QK issue
         constexpr uint32_t idesc_qk = umma_idesc_bf16(C::BM, C::BN, 0, 0);
-        constexpr uint32_t idesc_pv = umma_idesc_bf16(C::BM, C::D, 0, 1);
         uint32_t sc = 0, tc = 0, ic = 0;
         bool issued = false;
         for (int item = blockIdx.x; item < n_items && !abort; item += gridDim.x) {
@@ -261,75 +272,31 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
                 break;
             }
             tc_fence_after();
-            // V rows to zero: slots past the sequence's end in its last page,
-            // and slots of the first live page below the tile's first visible key
-            const int P = p.page_size;
-            const int zero_lo = it.L, zero_hi = ((it.L + P - 1) / P) * P;
-            const int head_lo = (it.klo / P) * P, head_hi = it.klo;
-            for (int j = 0; j <= it.T && !abort; ++j) {
-                if (j < it.T) {
-                    const uint32_t s_ = sc + j, st = s_ % C::NS;
-                    if (!mbar_wait_bounded(bar_k_full + 8 * st, (s_ / C::NS) & 1u, kWaitLimitNs)) {
-                        abort = true;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t b = (tc + j) & 1u;
-                    const uint32_t kb = base + C::OFF_STAGE + st * C::STAGE_BYTES;
-                    if (lane == 0) {
-#pragma unroll
-                        for (int kk = 0; kk < C::D / 16; ++kk) {
-                            const uint32_t qoff = (kk >> 2) * C::QHB_BYTES + (kk & 3) * 32;
-                            const uint32_t koff = (kk >> 2) * C::HB_BYTES + (kk & 3) * 32;
-                            tc_mma_ss(t_s + C::BN * b, umma_desc_sw128(base + C::OFF_Q + qoff, 16, 1024),
-                                      umma_desc_sw128(kb + koff, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
-                        }
-                        tc_commit(bar_s_full + 8 * b);
-                        issued = true;
-                    }
-                    __syncwarp();
+            for (int j = 0; j < it.T; ++j) {
+                const uint32_t s_ = sc + j, st = s_ % C::NSK, tcj = tc + j, b = tcj & 1u;
+                // K landed, and S buffer b is free: PV(tcj - 2) read the P it held
+                if (!mbar_wait_bounded(bar_k_full + 8 * st, (s_ / C::NSK) & 1u, kWaitLimitNs) ||
+                    (tcj >= 2 && !mbar_wait_bounded(bar_pv_done + 8 * b, ((tcj - 2) >> 1) & 1u, kWaitLimitNs))) {
+                    abort = true;
+                    break;
                 }
-                if (j >= 1) {
-                    const int jj = j - 1;
-                    const uint32_t tcj = tc + jj, b = tcj & 1u;
-                    const uint32_t s_ = sc + jj, st = s_ % C::NS;
-                    if (!mbar_wait_bounded(bar_p_full + 8 * b, (tcj >> 1) & 1u, kWaitLimitNs) ||
-                        !mbar_wait_bounded(bar_v_full + 8 * st, (s_ / C::NS) & 1u, kWaitLimitNs) ||
-                        (jj == 0 && ic >= 1 && !mbar_wait_bounded(bar_o_free, (ic - 1) & 1u, kWaitLimitNs))) {
-                        abort = true;
-                        break;
-                    }
-                    const uint32_t vb = base + C::OFF_STAGE + st * C::STAGE_BYTES + C::TILE_BYTES;
-                    // zero V rows of keys past the sequence's end held by this tile
-                    const int key0 = (it.kt0 + jj) * C::BN;
-                    const int z0 = max(zero_lo, key0) - key0, z1 = min(zero_hi, key0 + C::BN) - key0;
-                    const int h0 = max(head_lo, key0) - key0, h1 = min(head_hi, key0 + C::BN) - key0;
-                    const int nz = max(z1 - z0, 0), nh = GEN ? max(h1 - h0, 0) : 0;
-                    if (nz + nh > 0) {
-                        for (int idx = lane; idx < (nz + nh) * 16; idx += 32) {
-                            const int rr = idx / 16, c16 = idx % 16;
-                            const int row = rr < nz ? z0 + rr : h0 + (rr - nz);
-                            const uint32_t a = vb + (c16 >> 3) * C::HB_BYTES + row * 128 + (((c16 & 7) ^ (row & 7)) << 4);
-                            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
-                        }
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                    }
-                    tc_fence_after();
-                    if (lane == 0) {
-                        const uint32_t sp = t_s + C::BN * b;
+                tc_fence_after();
+                const uint32_t kb = base + C::OFF_K + st * C::TILE_BYTES;
+                if (lane == 0) {
 #pragma unroll
-                        for (int kk = 0; kk < C::BN / 16; ++kk) {
-                            const uint64_t bd = umma_desc_sw128(vb + kk * 16 * 128, C::HB_BYTES, 1024);
-                            tc_mma_ts(t_o, sp + kk * 8, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
-                            tc_mma_ts(t_o, sp + C::BN / 2 + kk * 8, bd, idesc_pv, 1u);
-                        }
-                        tc_commit(bar_pv_done + 8 * (tcj & 1u));
-                        tc_commit(bar_kv_empty + 8 * st);
+                    for (int kk = 0; kk < C::D / 16; ++kk) {
+                        const uint32_t qoff = (kk >> 2) * C::QHB_BYTES + (kk & 3) * 32;
+                        const uint32_t koff = (kk >> 2) * C::HB_BYTES + (kk & 3) * 32;
+                        tc_mma_ss(t_s + C::BN * b, umma_desc_sw128(base + C::OFF_Q + qoff, 16, 1024),
+                                  umma_desc_sw128(kb + koff, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
                     }
-                    __syncwarp();
+                    tc_commit(bar_s_full + 8 * b);
+                    tc_commit(bar_k_empty + 8 * st);   // the K tile is read once QK is done
+                    issued = true;
                 }
+                __syncwarp();
             }
+            // the query tile is read once the item's QKs are done
             if (lane == 0 && !abort) tc_commit(bar_q_empty);
             __syncwarp();
             sc += it.T;
@@ -341,6 +308,69 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
         if (lane == 0 && issued) {
             tc_commit(bar_final);
             mbar_wait_bounded(bar_final, 0, kWaitLimitNs);
+        }
+        __syncwarp();
+    } else if (warp == C::W_PV) {
+        // ===================================================== PV issue
+        constexpr uint32_t idesc_pv = umma_idesc_bf16(C::BM, C::D, 0, 1);
+        uint32_t sc = 0, tc = 0, ic = 0;
+        bool issued = false;
+        for (int item = blockIdx.x; item < n_items && !abort; item += gridDim.x) {
+            const PrefItem it = plan_prefill<GEN>(item, p);
+            if (!it.seq_ok) continue;
+            // V rows to zero: slots past the sequence's end in its last page,
+            // and slots of the first live page below the tile's first visible key
+            const int P = p.page_size;
+            const int zero_lo = it.L, zero_hi = ((it.L + P - 1) / P) * P;
+            const int head_lo = (it.klo / P) * P, head_hi = it.klo;
+            for (int jj = 0; jj < it.T; ++jj) {
+                const uint32_t tcj = tc + jj, b = tcj & 1u;
+                const uint32_t s_ = sc + jj, st = s_ % C::NSV;
+                if (!mbar_wait_bounded(bar_p_full + 8 * b, (tcj >> 1) & 1u, kWaitLimitNs) ||
+                    !mbar_wait_bounded(bar_v_full + 8 * st, (s_ / C::NSV) & 1u, kWaitLimitNs) ||
+                    (jj == 0 && ic >= 1 && !mbar_wait_bounded(bar_o_free, (ic - 1) & 1u, kWaitLimitNs))) {
+                    abort = true;
+                    break;
+                }
+                const uint32_t vb = base + C::OFF_V + st * C::TILE_BYTES;
+                // zero V rows of keys past the sequence's end held by this tile
+                const int key0 = (it.kt0 + jj) * C::BN;
+                const int z0 = max(zero_lo, key0) - key0, z1 = min(zero_hi, key0 + C::BN) - key0;
+                const int h0 = max(head_lo, key0) - key0, h1 = min(head_hi, key0 + C::BN) - key0;
+                const int nz = max(z1 - z0, 0), nh = GEN ? max(h1 - h0, 0) : 0;
+                if (nz + nh > 0) {
+                    for (int idx = lane; idx < (nz + nh) * 16; idx += 32) {
+                        const int rr = idx / 16, c16 = idx % 16;
+                        const int row = rr < nz ? z0 + rr : h0 + (rr - nz);
+                        const uint32_t a = vb + (c16 >> 3) * C::HB_BYTES + row * 128 + (((c16 & 7) ^ (row & 7)) << 4);
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t sp = t_s + C::BN * b;
+#pragma unroll
+                    for (int kk = 0; kk < C::BN / 16; ++kk) {
+                        const uint64_t bd = umma_desc_sw128(vb + kk * 16 * 128, C::HB_BYTES, 1024);
+                        tc_mma_ts(t_o, sp + kk * 8, bd, idesc_pv, (jj > 0 || kk > 0) ? 1u : 0u);
+                        tc_mma_ts(t_o, sp + C::BN / 2 + kk * 8, bd, idesc_pv, 1u);
+                    }
+                    tc_commit(bar_pv_done + 8 * b);
+                    tc_commit(bar_v_empty + 8 * st);   // the V tile is read once PV is done
+                    issued = true;
+                }
+                __syncwarp();
+            }
+            sc += it.T;
+            tc += it.T;
+            ++ic;
+            if (misc[1]) abort = true;
+        }
+        if (lane == 0 && issued) {
+            tc_commit(bar_final + 8);
+            mbar_wait_bounded(bar_final + 8, 0, kWaitLimitNs);
         }
         __syncwarp();
     } else {
@@ -523,7 +553,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 4) tmem_dealloc(tmem, C::TMEM_COLS);
+    if (warp == C::W_QK) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
 }  // namespace rad

@@ -106,7 +106,8 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
         pl.family = !general && use_prefill_tc(rows, pl.ratio, head_dim, kv_dtype) ? rad::kFamPrefillTC
                                                                                    : rad::kFamWide;
     if (pl.family == rad::kFamPrefillTC)
-        pl.tile = rad::TileInfo{128, 0, 4, 0, 0, rad::PrefillTileKeys, RAD_PREFILL_NS, 128, 192, 0, RAD_PREFILL_CTAS};
+        pl.tile = rad::TileInfo{128, 0, 4, 0, 0, rad::PrefillTileKeys, RAD_PREFILL_NSK + RAD_PREFILL_NSV, 128, 256, 0,
+                                RAD_PREFILL_CTAS};
     else if (pl.family == rad::kFamSplitTC)
         pl.tile = rad::split_tc05_info(rad::split_tc05_rows(pl.M));
     else
@@ -501,9 +502,10 @@ int describe_call(int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_
     if (pl.family == rad::kFamPrefillTC) {
         snprintf(buf, buf_len,
                  "attn_prefill_tc05 family=%s head_dim=%d kv=bf16 query_rows_per_kv_head=%d tile_rows=128 "
-                 "keys_per_tile=%d stages=%d ctas_per_sm=%d warps=4 softmax+1 mma+1 producer mma=tcgen05.kind::f16 "
-                 "(S and O in TMEM, P bf16 hi+lo from TMEM) split_len=0",
-                 family_name(pl.family), head_dim, pl.M, rad::PrefillTileKeys, pl.tile.NS, pl.tile.minb);
+                 "keys_per_tile=%d k_stages=%d v_stages=%d ctas_per_sm=%d warps=4 softmax+1 qk+1 pv+2 producers "
+                 "mma=tcgen05.kind::f16 (S and O in TMEM, P bf16 hi+lo from TMEM) split_len=0",
+                 family_name(pl.family), head_dim, pl.M, rad::PrefillTileKeys, RAD_PREFILL_NSK, RAD_PREFILL_NSV,
+                 pl.tile.minb);
         return RAD_OK;
     }
     const auto tile_desc = [&](char* b, size_t n, int family, const rad::TileInfo& ti, int rows_kv) {

@@ -83,8 +83,11 @@ template <> struct Pick<256, true,  kFamWide>   { using T = TileCfg<256, true,  
 #ifndef RAD_PREFILL_BN
 #define RAD_PREFILL_BN 128
 #endif
-#ifndef RAD_PREFILL_NS
-#define RAD_PREFILL_NS 3
+#ifndef RAD_PREFILL_NSK
+#define RAD_PREFILL_NSK 2   // K stages of the bf16 tcgen05 prefill kernel
+#endif
+#ifndef RAD_PREFILL_NSV
+#define RAD_PREFILL_NSV 2   // V stages
 #endif
 #ifndef RAD_PREFILL_FP8_NS
 #define RAD_PREFILL_FP8_NS 3   // stages of the fp8 tcgen05 prefill kernel
