@@ -5,7 +5,9 @@
 //
 // Work items, masks and the item order are those of the bf16 tcgen05 prefill
 // kernel (prefill_tc05.cuh): (sequence g, KV head kvh, 128 query rows), keys
-// 0 .. kmax-1, causal per row, an optional sliding window.
+// 0 .. kmax-1, causal per row, an optional sliding window.  The CTAs take the
+// items with a plain stride: the snake that the bf16 kernel uses measured 3%
+// slower here.
 //
 //   S_j  = Q K_j^T     kind::f8f6f4, M 128 query rows, N 128 keys, K = head_dim:
 //                      K straight from the TMA-staged e4m3 rows; each query row
@@ -19,22 +21,32 @@
 //                      128-byte-swizzled MN-major tile
 //
 // Warp roles (one CTA per SM, persistent, heavier query tiles first):
-//   warp 5      producer: page ids and per-page K/V scales (the scales of a
-//               stage's pages into its meta block), TMA loads of every page's
-//               e4m3 K and V rows (one 3-D box per page: P rows x 128 bytes)
-//               into a ring of stages; pages outside the tile's range load
-//               from an out-of-range coordinate (zero fill).
-//   warp 4      MMA: lane 0 issues QK per tile (2 terms x 4 K-steps) and, once
-//               the softmax wrote P_{j-1} and the converters V_{j-1}, PV.
+//   warp 6      K producer: page ids and per-page K/V scales (the scales of a
+//               tile's pages into the K stage's meta block), TMA loads of every
+//               page's e4m3 K rows (one 3-D box per page: P rows x 128 bytes)
+//               into a ring of K stages, each free once its QK is done and the
+//               softmax has read its scales; pages outside the tile's range
+//               load from an out-of-range coordinate (zero fill).
+//   warp 7      V producer: the same for V rows into a ring of V stages, each
+//               free once converted.
+//   warp 4      QK: lane 0 issues QK per tile (2 terms x 4 K-steps) into TMEM
+//               buffer j & 1 once K_j landed and PV_{j-2} is done; then the
+//               warp turns key rows 0-63 of the staged e4m3 V_j into f16
+//               buffer j & 1 (zeros for keys outside the sequence or below the
+//               tile's window) while the softmax works on S_j.
+//   warp 5      V: converts key rows 64-127 the same way, then, once P_j is
+//               written and the QK warp's rows are converted, lane 0 issues
+//               PV.  (One warp converting all 128 rows measured 8% slower: it
+//               then noticed P_j late.)
 //   warps 0-3   softmax: thread t owns query row t; per item it splits its row
 //               of Q into the two e4m3 terms; per tile it reads S_j, scales
 //               and masks the logits, keeps the running max (lazy rescale of O
 //               past 2^8, warp-wide), writes P over S_j and finally O / l.
-//   warps 6-7   V converters: thread c turns key rows c and c + 64 of the
-//               staged V tile into f16 (zeros for keys outside the sequence or
-//               below the tile's window), once per tile.
 // PV of tile t completes a phase of pv_done[t & 1]; every wait on it is at most
-// one phase ahead (see prefill_tc05.cuh).  Every wait is bounded.
+// one phase ahead (see prefill_tc05.cuh).  The QK warp's conversion of tile t
+// completes a phase of v16_full[t & 1]; it starts only after PV(t-2), which
+// waited for tile t-2's phase, so the V warp's wait on it is never two phases
+// behind either.  Every wait is bounded.
 #pragma once
 #include <cuda.h>
 
@@ -47,33 +59,73 @@ struct PrefillFp8Cfg {
     static constexpr int D = 128;
     static constexpr int BM = 128;                  // query rows per item
     static constexpr int BN = 128;                  // keys per tile
-    static constexpr int NS = RAD_PREFILL_FP8_NS;   // K/V stages
+    static constexpr int NSK = RAD_PREFILL_FP8_NSK;   // K stages (with the tile's page scales)
+    static constexpr int NSV = RAD_PREFILL_FP8_NSV;   // V stages
+    static constexpr int QK_VROWS = 64;               // V rows the QK warp converts per tile (the V warp: the rest)
     static constexpr int Q8_TERM = BM * 128;        // one e4m3 term of the query tile: [row][128 B]
     static constexpr int KV_TILE = BN * 128;        // e4m3 K or V rows of one tile
-    static constexpr int STAGE_BYTES = 2 * KV_TILE;
     static constexpr int ATOM = BN * 128;           // one 64-column block of the f16 V tile
     static constexpr int V16_BYTES = 2 * ATOM;
-    static constexpr int META_STRIDE = 64;          // ks[8], vs[8] of a stage's pages
+    static constexpr int META_STRIDE = 64;          // ks[8], vs[8] of a tile's pages
     static constexpr int OFF_Q8 = 0;
-    static constexpr int OFF_STAGE = OFF_Q8 + 2 * Q8_TERM;
-    static constexpr int OFF_V16 = OFF_STAGE + NS * STAGE_BYTES;
+    static constexpr int OFF_K = OFF_Q8 + 2 * Q8_TERM;
+    static constexpr int OFF_V = OFF_K + NSK * KV_TILE;
+    static constexpr int OFF_V16 = OFF_V + NSV * KV_TILE;
     static constexpr int OFF_META = OFF_V16 + 2 * V16_BYTES;
-    static constexpr int OFF_BARS = OFF_META + NS * META_STRIDE;
-    // q8_full, q8_empty, k_full[NS], v_full[NS], kv_empty[NS], s_full[2], p_full[2],
-    // v16_full[2], pv_done[2], o_free, final
-    static constexpr int NBARS = 2 + 3 * NS + 2 + 2 + 2 + 2 + 2;
+    static constexpr int OFF_BARS = OFF_META + NSK * META_STRIDE;
+    // q8_full, q8_empty, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[2], p_full[2],
+    // pv_done[2], v16_full[2], o_free, final[2]
+    static constexpr int NBARS = 2 + 2 * NSK + 2 * NSV + 2 + 2 + 2 + 2 + 1 + 2;
     static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // 1 KB alignment of the swizzled tiles
     static constexpr int NTHREADS = 8 * 32;   // 8 warps: the softmax threads keep 255 registers
-    static constexpr int W_MMA = 4, W_PROD = 5, W_CONV = 6, NCONV = 2;
-    // a stage is free once QK read its K (a commit), the converters read its V
-    // and the softmax warps read its scales
-    static constexpr int KV_EMPTY_ARRIVALS = 1 + NCONV + 4;
+    static constexpr int W_QK = 4, W_V = 5, W_PROD_K = 6, W_PROD_V = 7;
+    // a K stage is free once QK read its K (a commit) and the softmax warps read its scales
+    static constexpr int K_EMPTY_ARRIVALS = 1 + 4;
     static constexpr uint32_t TMEM_COLS = 512;      // O in [0,128), S buffer b in [128 + 128 b, ...)
     static constexpr float RESCALE_LOG2 = 8.f;
-    static_assert(OFF_STAGE % 1024 == 0 && OFF_V16 % 1024 == 0 && STAGE_BYTES % 1024 == 0, "1 KB tiles");
+    static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && OFF_V16 % 1024 == 0 && KV_TILE % 1024 == 0, "1 KB tiles");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(QK_VROWS % 32 == 0 && QK_VROWS > 0 && QK_VROWS < BN, "both warps convert whole 32-row groups");
 };
+
+// Key rows row0 + lane + 32 i (i < n) of a staged e4m3 V tile -> the f16
+// MN-major tile PV reads (128-byte swizzle, two 64-column blocks); keys outside
+// [zlo, L) become zeros.
+__device__ __forceinline__ void convert_v_rows(const uint8_t* stage, uint8_t* v16, int row0, int n, int key0, int zlo,
+                                               int L, int lane) {
+    using C = PrefillFp8Cfg;
+    const uint32_t sw = (uint32_t)(lane & 7);   // (row0 + lane + 32 i) & 7: row0 is a multiple of 32
+#pragma unroll 1
+    for (int i = 0; i < n; ++i) {
+        const int row = row0 + lane + 32 * i;
+        const int key = key0 + row;
+        const bool zero = key < zlo || key >= L;
+        const uint8_t* src = stage + row * 128;
+        uint8_t* dst = v16 + row * 128;
+        uint4 in[8];   // the row's loads first: stores below may alias them as far as the compiler knows
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)
+            in[ch] = zero ? make_uint4(0u, 0u, 0u, 0u) : *reinterpret_cast<const uint4*>(src + (((uint32_t)ch ^ sw) << 4));
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+            // codes 16ch .. 16ch+15 -> f16 chunks 2ch, 2ch+1 of the row, column block ch / 4
+            const uint4 v = in[ch];
+            const uint32_t h0 = e4m3x2_to_f16x2((uint16_t)(v.x & 0xFFFFu));
+            const uint32_t h1 = e4m3x2_to_f16x2((uint16_t)(v.x >> 16));
+            const uint32_t h2 = e4m3x2_to_f16x2((uint16_t)(v.y & 0xFFFFu));
+            const uint32_t h3 = e4m3x2_to_f16x2((uint16_t)(v.y >> 16));
+            const uint32_t h4 = e4m3x2_to_f16x2((uint16_t)(v.z & 0xFFFFu));
+            const uint32_t h5 = e4m3x2_to_f16x2((uint16_t)(v.z >> 16));
+            const uint32_t h6 = e4m3x2_to_f16x2((uint16_t)(v.w & 0xFFFFu));
+            const uint32_t h7 = e4m3x2_to_f16x2((uint16_t)(v.w >> 16));
+            uint8_t* blk = dst + (ch >> 2) * C::ATOM;
+            const uint32_t c2 = (uint32_t)((ch & 3) * 2);
+            *reinterpret_cast<uint4*>(blk + ((c2 ^ sw) << 4)) = make_uint4(h0, h1, h2, h3);
+            *reinterpret_cast<uint4*>(blk + (((c2 + 1) ^ sw) << 4)) = make_uint4(h4, h5, h6, h7);
+        }
+    }
+}
 
 template <bool GEN>
 __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
@@ -88,13 +140,14 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
     const uint32_t bar_q8_full = base + C::OFF_BARS;
     const uint32_t bar_q8_empty = bar_q8_full + 8;
     const uint32_t bar_k_full = bar_q8_empty + 8;
-    const uint32_t bar_v_full = bar_k_full + 8 * C::NS;
-    const uint32_t bar_kv_empty = bar_v_full + 8 * C::NS;
-    const uint32_t bar_s_full = bar_kv_empty + 8 * C::NS;   // [2]
+    const uint32_t bar_k_empty = bar_k_full + 8 * C::NSK;
+    const uint32_t bar_v_full = bar_k_empty + 8 * C::NSK;
+    const uint32_t bar_v_empty = bar_v_full + 8 * C::NSV;
+    const uint32_t bar_s_full = bar_v_empty + 8 * C::NSV;   // [2]
     const uint32_t bar_p_full = bar_s_full + 16;            // [2]
-    const uint32_t bar_v16_full = bar_p_full + 16;          // [2]
-    const uint32_t bar_pv_done = bar_v16_full + 16;         // [2], by tile parity
-    const uint32_t bar_o_free = bar_pv_done + 16;
+    const uint32_t bar_pv_done = bar_p_full + 16;           // [2], by tile parity
+    const uint32_t bar_v16_full = bar_pv_done + 16;         // [2], by tile parity: the QK warp's V rows converted
+    const uint32_t bar_o_free = bar_v16_full + 16;
     const uint32_t bar_final = bar_o_free + 8;
     volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);  // [0] tmem, [1] abort
 
@@ -104,23 +157,27 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
     if (threadIdx.x == 0) {
         mbar_init(bar_q8_full, 4);
         mbar_init(bar_q8_empty, 1);
-        for (int i = 0; i < C::NS; ++i) {
+        for (int i = 0; i < C::NSK; ++i) {
             mbar_init(bar_k_full + 8 * i, 1);
+            mbar_init(bar_k_empty + 8 * i, C::K_EMPTY_ARRIVALS);
+        }
+        for (int i = 0; i < C::NSV; ++i) {
             mbar_init(bar_v_full + 8 * i, 1);
-            mbar_init(bar_kv_empty + 8 * i, C::KV_EMPTY_ARRIVALS);
+            mbar_init(bar_v_empty + 8 * i, 2);   // both converting warps
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_s_full + 8 * i, 1);
             mbar_init(bar_p_full + 8 * i, 4);
-            mbar_init(bar_v16_full + 8 * i, C::NCONV);
             mbar_init(bar_pv_done + 8 * i, 1);
+            mbar_init(bar_v16_full + 8 * i, 1);
         }
         mbar_init(bar_o_free, 4);
         mbar_init(bar_final, 1);
+        mbar_init(bar_final + 8, 1);
         misc[1] = 0;
         fence_mbarrier_init();
     }
-    if (warp == C::W_MMA) {
+    if (warp == C::W_QK) {
         tmem_alloc(base + C::OFF_MISC, C::TMEM_COLS);
         tmem_relinquish();
     }
@@ -136,16 +193,21 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
     const int ppt = C::BN / P;       // pages per key tile (8 or 4)
     bool abort = false;
 
-    if (warp == C::W_PROD) {
-        // ===================================================== producer
+    if (warp == C::W_PROD_K || warp == C::W_PROD_V) {
+        // ===================================================== producers: K (+ the tile's scales), V
+        const bool is_k = warp == C::W_PROD_K;
+        const int NSX = is_k ? C::NSK : C::NSV;
+        const uint32_t bar_full = is_k ? bar_k_full : bar_v_full;
+        const uint32_t bar_empty = is_k ? bar_k_empty : bar_v_empty;
+        const uint32_t ring = base + (is_k ? C::OFF_K : C::OFF_V);
+        const CUtensorMap* tm = is_k ? &tm_k : &tm_v;
         const uint64_t pol = policy_evict_last();   // K/V tiles are re-read by every query tile
         const int oob_tok = p.num_pages * P;
         uint32_t sc = 0;
-        if (lane == 0) {
-            prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_v);
-        }
-        for (int item = blockIdx.x; item < n_items && !abort; item += gridDim.x) {
+        if (lane == 0) prefetch_tmap(tm);
+        for (int rd = 0; rd * (int)gridDim.x < n_items && !abort; ++rd) {
+            const int item = prefill_item_of<false>(rd, blockIdx.x, gridDim.x);
+            if (item >= n_items) break;
             const PrefItem it = plan_prefill<GEN, C::BM, C::BN>(item, p);
             if (!it.seq_ok) continue;
             const int page_hi = (it.kmax + P - 1) / P;
@@ -154,8 +216,8 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
             int batch0 = -1 << 30, my_pg = 0;
             float my_ks = 1.f, my_vs = 1.f;
             for (int j = 0; j < it.T; ++j) {
-                const uint32_t st = sc % C::NS, use = sc / C::NS;
-                if (use >= 1 && !mbar_wait_bounded(bar_kv_empty + 8 * st, (use - 1) & 1u, kWaitLimitNs)) {
+                const uint32_t st = sc % (uint32_t)NSX, use = sc / (uint32_t)NSX;
+                if (use >= 1 && !mbar_wait_bounded(bar_empty + 8 * st, (use - 1) & 1u, kWaitLimitNs)) {
                     abort = true;
                     break;
                 }
@@ -168,8 +230,10 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
                     if ((!GEN || pi >= page_lo) && pi < page_hi) {
                         const int pg = __ldg(trow + pi);
                         my_pg = (pg < 0 || pg >= p.num_pages) ? 0 : pg;
-                        my_ks = __ldg(p.k_scales + my_pg);
-                        my_vs = __ldg(p.v_scales + my_pg);
+                        if (is_k) {
+                            my_ks = __ldg(p.k_scales + my_pg);
+                            my_vs = __ldg(p.v_scales + my_pg);
+                        }
                     }
                 }
                 float kss[8], vss[8];
@@ -179,28 +243,24 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
                     kss[i] = __shfl_sync(0xffffffffu, my_ks, src);
                     vss[i] = __shfl_sync(0xffffffffu, my_vs, src);
                 }
-                const uint32_t kdst = base + C::OFF_STAGE + st * C::STAGE_BYTES;
-                const uint32_t vdst = kdst + C::KV_TILE;
+                const uint32_t dst = ring + st * C::KV_TILE;
                 if (lane == 0) {
-                    // the stage's page scales, released with the K-full arrive below
-                    float* meta = reinterpret_cast<float*>(smem + C::OFF_META + st * C::META_STRIDE);
+                    if (is_k) {
+                        // the tile's page scales, released with the K-full arrive below
+                        float* meta = reinterpret_cast<float*>(smem + C::OFF_META + st * C::META_STRIDE);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        meta[i] = kss[i];
-                        meta[8 + i] = vss[i];
+                        for (int i = 0; i < 8; ++i) {
+                            meta[i] = kss[i];
+                            meta[8 + i] = vss[i];
+                        }
                     }
-                    mbar_arrive_expect_tx(bar_k_full + 8 * st, C::KV_TILE);
-                    mbar_arrive_expect_tx(bar_v_full + 8 * st, C::KV_TILE);
+                    mbar_arrive_expect_tx(bar_full + 8 * st, C::KV_TILE);
                 }
                 for (int i = 0; i < ppt; ++i) {
                     const int pi = pstart + i;
                     const int pg = __shfl_sync(0xffffffffu, my_pg, (pi - batch0) & 31);
                     const int tok = ((!GEN || pi >= page_lo) && pi < page_hi) ? pg * P : oob_tok;
-                    if (lane == 0) {
-                        const uint32_t o = (uint32_t)(i * P * 128);
-                        tma_load_3d(kdst + o, &tm_k, bar_k_full + 8 * st, 0, it.kvh, tok, pol);
-                        tma_load_3d(vdst + o, &tm_v, bar_v_full + 8 * st, 0, it.kvh, tok, pol);
-                    }
+                    if (lane == 0) tma_load_3d(dst + (uint32_t)(i * P * 128), tm, bar_full + 8 * st, 0, it.kvh, tok, pol);
                 }
                 ++sc;
             }
@@ -208,19 +268,18 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
         }
         // drain: nothing may still be landing in shared memory at exit
         if (lane == 0) {
-            const uint32_t first = sc > (uint32_t)C::NS ? sc - C::NS : 0u;
-            for (uint32_t c = first; c < sc; ++c) {
-                mbar_wait_bounded(bar_k_full + 8 * (c % C::NS), (c / C::NS) & 1u, kWaitLimitNs);
-                mbar_wait_bounded(bar_v_full + 8 * (c % C::NS), (c / C::NS) & 1u, kWaitLimitNs);
-            }
+            const uint32_t first = sc > (uint32_t)NSX ? sc - NSX : 0u;
+            for (uint32_t c = first; c < sc; ++c)
+                mbar_wait_bounded(bar_full + 8 * (c % NSX), (c / NSX) & 1u, kWaitLimitNs);
         }
-    } else if (warp == C::W_MMA) {
-        // ===================================================== MMA issue
+    } else if (warp == C::W_QK) {
+        // ===================================================== QK issue
         constexpr uint32_t idesc_qk = umma_idesc_e4m3(C::BM, C::BN);
-        constexpr uint32_t idesc_pv = umma_idesc_f16(C::BM, C::D, 0, 1);
         uint32_t sc = 0, tc = 0, ic = 0;
         bool issued = false;
-        for (int item = blockIdx.x; item < n_items && !abort; item += gridDim.x) {
+        for (int rd = 0; rd * (int)gridDim.x < n_items && !abort; ++rd) {
+            const int item = prefill_item_of<false>(rd, blockIdx.x, gridDim.x);
+            if (item >= n_items) break;
             const PrefItem it = plan_prefill<GEN, C::BM, C::BN>(item, p);
             if (!it.seq_ok) continue;
             if (!mbar_wait_bounded(bar_q8_full, ic & 1u, kWaitLimitNs)) {
@@ -228,52 +287,46 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
                 break;
             }
             tc_fence_after();
-            for (int j = 0; j <= it.T && !abort; ++j) {
-                if (j < it.T) {
-                    const uint32_t s_ = sc + j, st = s_ % C::NS;
-                    if (!mbar_wait_bounded(bar_k_full + 8 * st, (s_ / C::NS) & 1u, kWaitLimitNs)) {
-                        abort = true;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t b = (tc + j) & 1u;
-                    const uint32_t kb = base + C::OFF_STAGE + st * C::STAGE_BYTES;
-                    if (lane == 0) {
-#pragma unroll
-                        for (int term = 0; term < 2; ++term)
-#pragma unroll
-                            for (int kk = 0; kk < C::D / 32; ++kk)
-                                tc_mma_ss_f8(t_s + C::BN * b,
-                                             umma_desc_sw128(base + C::OFF_Q8 + term * C::Q8_TERM + kk * 32, 16, 1024),
-                                             umma_desc_sw128(kb + kk * 32, 16, 1024), idesc_qk,
-                                             (term > 0 || kk > 0) ? 1u : 0u);
-                        tc_commit(bar_s_full + 8 * b);
-                        tc_commit(bar_kv_empty + 8 * st);
-                        if (j == it.T - 1) tc_commit(bar_q8_empty);   // the item's query terms are read
-                        issued = true;
-                    }
-                    __syncwarp();
+            for (int j = 0; j < it.T; ++j) {
+                const uint32_t s_ = sc + j, st = s_ % C::NSK, tcj = tc + j, b = tcj & 1u;
+                // K landed, and S buffer b is free: PV(tcj - 2) read the P it held
+                bool ok = mbar_wait_bounded(bar_k_full + 8 * st, (s_ / C::NSK) & 1u, kWaitLimitNs);
+                if (ok && tcj >= 2) ok = mbar_wait_bounded(bar_pv_done + 8 * b, ((tcj - 2) >> 1) & 1u, kWaitLimitNs);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    abort = true;
+                    break;
                 }
-                if (j >= 1) {
-                    const int jj = j - 1;
-                    const uint32_t tcj = tc + jj, b = tcj & 1u;
-                    if (!mbar_wait_bounded(bar_p_full + 8 * b, (tcj >> 1) & 1u, kWaitLimitNs) ||
-                        !mbar_wait_bounded(bar_v16_full + 8 * b, (tcj >> 1) & 1u, kWaitLimitNs) ||
-                        (jj == 0 && ic >= 1 && !mbar_wait_bounded(bar_o_free, (ic - 1) & 1u, kWaitLimitNs))) {
-                        abort = true;
-                        break;
-                    }
-                    tc_fence_after();
-                    if (lane == 0) {
-                        const uint32_t sp = t_s + C::BN * b;
-                        const uint32_t vb = base + C::OFF_V16 + b * C::V16_BYTES;
+                tc_fence_after();
+                const uint32_t kb = base + C::OFF_K + st * C::KV_TILE;
+                if (lane == 0) {
 #pragma unroll
-                        for (int kk = 0; kk < C::BN / 16; ++kk)
-                            tc_mma_ts(t_o, sp + kk * 8, umma_desc_sw128(vb + kk * 16 * 128, C::ATOM, 1024), idesc_pv,
-                                      (jj > 0 || kk > 0) ? 1u : 0u);
-                        tc_commit(bar_pv_done + 8 * b);
-                    }
-                    __syncwarp();
+                    for (int term = 0; term < 2; ++term)
+#pragma unroll
+                        for (int kk = 0; kk < C::D / 32; ++kk)
+                            tc_mma_ss_f8(t_s + C::BN * b,
+                                         umma_desc_sw128(base + C::OFF_Q8 + term * C::Q8_TERM + kk * 32, 16, 1024),
+                                         umma_desc_sw128(kb + kk * 32, 16, 1024), idesc_qk,
+                                         (term > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(bar_s_full + 8 * b);
+                    tc_commit(bar_k_empty + 8 * st);
+                    if (j == it.T - 1) tc_commit(bar_q8_empty);   // the item's query terms are read
+                    issued = true;
+                }
+                __syncwarp();
+                // key rows 0 .. QK_VROWS-1 of V_j -> f16 buffer b (free: PV(tcj - 2) is done)
+                // while the softmax works on S_j
+                const uint32_t sv = s_ % C::NSV;
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar_v_full + 8 * sv, (s_ / C::NSV) & 1u, kWaitLimitNs))) {
+                    abort = true;
+                    break;
+                }
+                convert_v_rows(smem + C::OFF_V + sv * C::KV_TILE, smem + C::OFF_V16 + b * C::V16_BYTES, 0,
+                               C::QK_VROWS / 32, (it.kt0 + j) * C::BN, GEN ? it.klo : 0, it.L, lane);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar_v16_full + 8 * b);
+                    mbar_arrive(bar_v_empty + 8 * sv);
                 }
             }
             sc += it.T;
@@ -287,17 +340,20 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
             mbar_wait_bounded(bar_final, 0, kWaitLimitNs);
         }
         __syncwarp();
-    } else if (warp >= C::W_CONV) {
-        // ===================================================== V converters
-        const int c0 = threadIdx.x - C::W_CONV * 32;   // key rows c0 and c0 + 64 of the tile
-        uint32_t sc = 0, tc = 0;
-        for (int item = blockIdx.x; item < n_items && !abort; item += gridDim.x) {
+    } else if (warp == C::W_V) {
+        // ===================================================== V: conversion and PV issue
+        constexpr uint32_t idesc_pv = umma_idesc_f16(C::BM, C::D, 0, 1);
+        uint32_t sc = 0, tc = 0, ic = 0;
+        bool issued = false;
+        for (int rd = 0; rd * (int)gridDim.x < n_items && !abort; ++rd) {
+            const int item = prefill_item_of<false>(rd, blockIdx.x, gridDim.x);
+            if (item >= n_items) break;
             const PrefItem it = plan_prefill<GEN, C::BM, C::BN>(item, p);
             if (!it.seq_ok) continue;
             const int zlo = GEN ? it.klo : 0;   // keys below the tile's window may hold anything
             for (int j = 0; j < it.T; ++j) {
-                const uint32_t s_ = sc + j, st = s_ % C::NS, tcj = tc + j, b = tcj & 1u;
-                bool ok = mbar_wait_bounded(bar_v_full + 8 * st, (s_ / C::NS) & 1u, kWaitLimitNs);
+                const uint32_t s_ = sc + j, st = s_ % C::NSV, tcj = tc + j, b = tcj & 1u;
+                bool ok = mbar_wait_bounded(bar_v_full + 8 * st, (s_ / C::NSV) & 1u, kWaitLimitNs);
                 // f16 buffer b was last read by PV(tcj - 2)
                 if (ok && tcj >= 2)
                     ok = mbar_wait_bounded(bar_pv_done + 8 * b, ((tcj - 2) >> 1) & 1u, kWaitLimitNs);
@@ -305,55 +361,53 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
                     abort = true;
                     break;
                 }
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const int c = c0 + 64 * half;
-                    const uint32_t sw = (uint32_t)(c & 7);
-                    const int key = (it.kt0 + j) * C::BN + c;
-                    const bool zero = key < zlo || key >= it.L;
-                    const uint8_t* src = smem + C::OFF_STAGE + st * C::STAGE_BYTES + C::KV_TILE + c * 128;
-                    uint8_t* dst = smem + C::OFF_V16 + b * C::V16_BYTES + c * 128;
-                    uint4 in[8];
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch)
-                        in[ch] = zero ? make_uint4(0u, 0u, 0u, 0u)
-                                      : *reinterpret_cast<const uint4*>(src + (((uint32_t)ch ^ sw) << 4));
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
-                        // codes 16ch .. 16ch+15 -> f16 chunks 2ch, 2ch+1 of the row, column block ch / 4
-                        const uint4 v = in[ch];
-                        const uint32_t h0 = e4m3x2_to_f16x2((uint16_t)(v.x & 0xFFFFu));
-                        const uint32_t h1 = e4m3x2_to_f16x2((uint16_t)(v.x >> 16));
-                        const uint32_t h2 = e4m3x2_to_f16x2((uint16_t)(v.y & 0xFFFFu));
-                        const uint32_t h3 = e4m3x2_to_f16x2((uint16_t)(v.y >> 16));
-                        const uint32_t h4 = e4m3x2_to_f16x2((uint16_t)(v.z & 0xFFFFu));
-                        const uint32_t h5 = e4m3x2_to_f16x2((uint16_t)(v.z >> 16));
-                        const uint32_t h6 = e4m3x2_to_f16x2((uint16_t)(v.w & 0xFFFFu));
-                        const uint32_t h7 = e4m3x2_to_f16x2((uint16_t)(v.w >> 16));
-                        uint8_t* row = dst + (ch >> 2) * C::ATOM;
-                        const uint32_t c2 = (uint32_t)((ch & 3) * 2);
-                        *reinterpret_cast<uint4*>(row + ((c2 ^ sw) << 4)) = make_uint4(h0, h1, h2, h3);
-                        *reinterpret_cast<uint4*>(row + (((c2 + 1) ^ sw) << 4)) = make_uint4(h4, h5, h6, h7);
-                    }
-                }
+                // key rows QK_VROWS .. 127 of the staged tile -> f16 (the QK warp converts the rows below)
+                convert_v_rows(smem + C::OFF_V + st * C::KV_TILE, smem + C::OFF_V16 + b * C::V16_BYTES, C::QK_VROWS,
+                               (C::BN - C::QK_VROWS) / 32,
+                               (it.kt0 + j) * C::BN, zlo, it.L, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(bar_v16_full + 8 * b);
-                    mbar_arrive(bar_kv_empty + 8 * st);
+                if (lane == 0) mbar_arrive(bar_v_empty + 8 * st);   // the staged V tile is read
+                // PV once P is written (and, at an item's first tile, O was read out)
+                ok = mbar_wait_bounded(bar_p_full + 8 * b, (tcj >> 1) & 1u, kWaitLimitNs);
+                if (ok) ok = mbar_wait_bounded(bar_v16_full + 8 * b, (tcj >> 1) & 1u, kWaitLimitNs);
+                if (ok && j == 0 && ic >= 1) ok = mbar_wait_bounded(bar_o_free, (ic - 1) & 1u, kWaitLimitNs);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    abort = true;
+                    break;
                 }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t sp = t_s + C::BN * b;
+                    const uint32_t vb = base + C::OFF_V16 + b * C::V16_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < C::BN / 16; ++kk)
+                        tc_mma_ts(t_o, sp + kk * 8, umma_desc_sw128(vb + kk * 16 * 128, C::ATOM, 1024), idesc_pv,
+                                  (j > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(bar_pv_done + 8 * b);
+                    issued = true;
+                }
+                __syncwarp();
             }
             sc += it.T;
             tc += it.T;
+            ++ic;
             if (__any_sync(0xffffffffu, misc[1] != 0)) abort = true;
         }
+        if (lane == 0 && issued) {
+            tc_commit(bar_final + 8);
+            mbar_wait_bounded(bar_final + 8, 0, kWaitLimitNs);
+        }
+        __syncwarp();
     } else {
         // ===================================================== softmax (warps 0-3)
         const int t = threadIdx.x;                                  // query row of the tile
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;      // this warp's TMEM lanes
         const int lp = (P == 16) ? 4 : 5;
         uint32_t sc = 0, tc = 0, ic = 0;
-        for (int item = blockIdx.x; item < n_items && !abort; item += gridDim.x) {
+        for (int rd = 0; rd * (int)gridDim.x < n_items && !abort; ++rd) {
+            const int item = prefill_item_of<false>(rd, blockIdx.x, gridDim.x);
+            if (item >= n_items) break;
             const PrefItem it = plan_prefill<GEN, C::BM, C::BN>(item, p);
             const int m = it.m0 + t;
             const bool valid = m < it.m_end;
@@ -435,11 +489,11 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
             float m_run = -CUDART_INF_F, l_run = 0.f;
             for (int j = 0; j < it.T; ++j) {
                 const uint32_t tcj = tc + j, b = tcj & 1u;
-                const uint32_t s_ = sc + j, st = s_ % C::NS;
-                // S_j landed, and the stage's scales are visible (its K-full phase is
+                const uint32_t s_ = sc + j, st = s_ % C::NSK;
+                // S_j landed, and the K stage's scales are visible (its K-full phase is
                 // complete: QK waited for it); the stage is released after the reads
                 bool ok = mbar_wait_bounded(bar_s_full + 8 * b, (tcj >> 1) & 1u, kWaitLimitNs);
-                if (ok) ok = mbar_wait_bounded(bar_k_full + 8 * st, (s_ / C::NS) & 1u, kWaitLimitNs);
+                if (ok) ok = mbar_wait_bounded(bar_k_full + 8 * st, (s_ / C::NSK) & 1u, kWaitLimitNs);
                 if (!__all_sync(0xffffffffu, ok)) {
                     abort = true;
                     break;
@@ -452,7 +506,7 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
                     vf[q16] = meta[8 + ((q16 * 16) >> lp)];
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar_kv_empty + 8 * st);
+                if (lane == 0) mbar_arrive(bar_k_empty + 8 * st);
                 tc_fence_after();
                 const uint32_t sc_addr = t_s + C::BN * b + lane_off;
                 uint32_t sv[C::BN];
@@ -577,7 +631,7 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == C::W_MMA) tmem_dealloc(tmem, C::TMEM_COLS);
+    if (warp == C::W_QK) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
 }  // namespace rad

@@ -91,16 +91,30 @@ struct PrefItem {
     int T;      // key tiles processed: kt0 .. kt0+T-1
 };
 
+// The item a persistent CTA b of G takes in its round r.  SNAKE: rounds deal
+// the heavy-first item order out in alternating directions, so the CTAs'
+// key-tile totals stay close where a plain stride gives the first CTAs a
+// heavier item in every round (on the 1 x 2048-row chunk over 8192 keys, the
+// busiest CTA's 229 key tiles become 220, against a mean of 190); without it,
+// a plain stride.  Past n_items in the last round: no item.
+template <bool SNAKE>
+__device__ __forceinline__ int prefill_item_of(int r, int b, int G) {
+    return r * G + ((SNAKE && (r & 1)) ? G - 1 - b : b);
+}
+
 // GEN: the call has a sliding window or a scale <= 0; without either, those
 // terms fold away at compile time.
 template <bool GEN, int BM = PrefillCfg::BM, int BN = PrefillCfg::BN>
 __device__ __forceinline__ PrefItem plan_prefill(int item, const AttnParams& p) {
+    // item order: query tile rank first (later tiles see more keys, so they come
+    // first), then sequence, then KV head
     PrefItem it;
-    const int per_g = p.n_head_kv * p.n_qtiles;
-    it.g = item / per_g;
-    const int rem = item - it.g * per_g;
-    it.kvh = rem / p.n_qtiles;
-    it.qt = p.n_qtiles - 1 - (rem - it.kvh * p.n_qtiles);   // later tiles see more keys: first
+    const int per_rank = p.groups * p.n_head_kv;
+    const int rank = item / per_rank;
+    const int rem = item - rank * per_rank;
+    it.g = rem / p.n_head_kv;
+    it.kvh = rem - it.g * p.n_head_kv;
+    it.qt = p.n_qtiles - 1 - rank;
     it.L = __ldg(p.seq_lens + it.g);
     it.seq_ok = it.L >= p.rows && (long long)it.L <= (long long)p.pages_per_seq * p.page_size;
     it.m0 = it.qt * BM;
@@ -198,7 +212,9 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
             if (is_k) prefetch_tmap(&tm_q);
             prefetch_tmap(tm);
         }
-        for (int item = blockIdx.x; item < n_items && !abort; item += gridDim.x) {
+        for (int rd = 0; rd * (int)gridDim.x < n_items && !abort; ++rd) {
+            const int item = prefill_item_of<true>(rd, blockIdx.x, gridDim.x);
+            if (item >= n_items) break;
             const PrefItem it = plan_prefill<GEN>(item, p);
             if (!it.seq_ok) continue;
             if (is_k) {
@@ -264,7 +280,9 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
         constexpr uint32_t idesc_qk = umma_idesc_bf16(C::BM, C::BN, 0, 0);
         uint32_t sc = 0, tc = 0, ic = 0;
         bool issued = false;
-        for (int item = blockIdx.x; item < n_items && !abort; item += gridDim.x) {
+        for (int rd = 0; rd * (int)gridDim.x < n_items && !abort; ++rd) {
+            const int item = prefill_item_of<true>(rd, blockIdx.x, gridDim.x);
+            if (item >= n_items) break;
             const PrefItem it = plan_prefill<GEN>(item, p);
             if (!it.seq_ok) continue;
             if (!mbar_wait_bounded(bar_q_full, ic & 1u, kWaitLimitNs)) {
@@ -315,7 +333,9 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
         constexpr uint32_t idesc_pv = umma_idesc_bf16(C::BM, C::D, 0, 1);
         uint32_t sc = 0, tc = 0, ic = 0;
         bool issued = false;
-        for (int item = blockIdx.x; item < n_items && !abort; item += gridDim.x) {
+        for (int rd = 0; rd * (int)gridDim.x < n_items && !abort; ++rd) {
+            const int item = prefill_item_of<true>(rd, blockIdx.x, gridDim.x);
+            if (item >= n_items) break;
             const PrefItem it = plan_prefill<GEN>(item, p);
             if (!it.seq_ok) continue;
             // V rows to zero: slots past the sequence's end in its last page,
@@ -379,7 +399,9 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;      // this warp's TMEM lanes
         const float c = p.scale_log2;
         uint32_t tc = 0;
-        for (int item = blockIdx.x; item < n_items && !abort; item += gridDim.x) {
+        for (int rd = 0; rd * (int)gridDim.x < n_items && !abort; ++rd) {
+            const int item = prefill_item_of<true>(rd, blockIdx.x, gridDim.x);
+            if (item >= n_items) break;
             const PrefItem it = plan_prefill<GEN>(item, p);
             const int m = it.m0 + t;
             const bool valid = m < it.m_end;

@@ -493,10 +493,11 @@ int describe_call(int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_
     if (pl.family == rad::kFamPrefillTC && kv_dtype == RAD_KV_FP8_E4M3) {
         snprintf(buf, buf_len,
                  "attn_prefill_tc05 family=%s head_dim=%d kv=fp8e4m3 query_rows_per_kv_head=%d tile_rows=128 "
-                 "keys_per_tile=128 stages=%d ctas_per_sm=1 warps=4 softmax+1 mma+1 producer+2 v converters "
-                 "mma=tcgen05 (QK kind::f8f6f4 on the staged e4m3 K with Q as two e4m3 terms, PV kind::f16 with "
-                 "V e4m3 -> f16 once per tile and P f16 from TMEM) split_len=0",
-                 family_name(pl.family), head_dim, pl.M, RAD_PREFILL_FP8_NS);
+                 "keys_per_tile=128 k_stages=%d v_stages=%d ctas_per_sm=1 warps=4 softmax+1 qk (+ half the v "
+                 "convert)+1 pv (+ half the v convert)+2 producers mma=tcgen05 (QK kind::f8f6f4 on the staged e4m3 "
+                 "K with Q as two e4m3 terms, PV kind::f16 with V e4m3 -> f16 once per tile and P f16 from TMEM) "
+                 "split_len=0",
+                 family_name(pl.family), head_dim, pl.M, RAD_PREFILL_FP8_NSK, RAD_PREFILL_FP8_NSV);
         return RAD_OK;
     }
     if (pl.family == rad::kFamPrefillTC) {

@@ -89,8 +89,11 @@ template <> struct Pick<256, true,  kFamWide>   { using T = TileCfg<256, true,  
 #ifndef RAD_PREFILL_NSV
 #define RAD_PREFILL_NSV 2   // V stages
 #endif
-#ifndef RAD_PREFILL_FP8_NS
-#define RAD_PREFILL_FP8_NS 3   // stages of the fp8 tcgen05 prefill kernel
+#ifndef RAD_PREFILL_FP8_NSK
+#define RAD_PREFILL_FP8_NSK 4   // K stages of the fp8 tcgen05 prefill kernel
+#endif
+#ifndef RAD_PREFILL_FP8_NSV
+#define RAD_PREFILL_FP8_NSV 3   // V stages
 #endif
 #ifndef RAD_PREFILL_CTAS
 #define RAD_PREFILL_CTAS 1
