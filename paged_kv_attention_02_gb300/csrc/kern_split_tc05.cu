@@ -11,7 +11,7 @@ namespace rad {
 namespace {
 
 template <int N>
-cudaError_t launch_n(const AttnParams& p, int sms, cudaStream_t st) {
+cudaError_t launch_n(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms, cudaStream_t st) {
     using C = SplitTcCfg<N>;
     auto kern = p.window > 0  ? attn_split_tc05_kernel<N, kModeWindow>
                 : p.tree_mask ? attn_split_tc05_kernel<N, kModeTree>
@@ -26,7 +26,7 @@ cudaError_t launch_n(const AttnParams& p, int sms, cudaStream_t st) {
     cfg.blockDim = dim3(C::NTHREADS, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = st;
-    return cudaLaunchKernelEx(&cfg, kern, p);
+    return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 
 }  // namespace
@@ -40,8 +40,9 @@ TileInfo split_tc05_info(int n) {
     return TileInfo{128, 1, 4, 0, 0, C::BK, C::NS, C::N, C::NTHREADS, C::SMEM_BYTES, 1};
 }
 
-cudaError_t launch_split_tc05(const AttnParams& p, int sms, cudaStream_t st) {
-    const cudaError_t e = p.qt_rows == 16 ? launch_n<16>(p, sms, st) : launch_n<32>(p, sms, st);
+cudaError_t launch_split_tc05(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
+                              cudaStream_t st) {
+    const cudaError_t e = p.qt_rows == 16 ? launch_n<16>(tk, tv, p, sms, st) : launch_n<32>(tk, tv, p, sms, st);
     if (e != cudaSuccess || p.max_splits <= 1) return e;
     return launch_combine<128>(p, st);
 }

@@ -427,7 +427,7 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
                                    : rad::launch_d256_bf16(rad::kFamDecode, pd, sms, st));
         if (e != cudaSuccess) return RAD_E_CUDA;
     }
-    if (pl.family == rad::kFamPrefillTC && fp8) {
+    if ((pl.family == rad::kFamPrefillTC && fp8) || pl.family == rad::kFamSplitTC) {
         rc = get_encoder();
         if (rc != RAD_OK) return rc;
         // e4m3 pools viewed as [tokens][n_head_kv][128 bytes]: one box = one page of one KV head
@@ -439,7 +439,8 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
         if (encode_map(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, k_pool, 3, kd, ks, kb) != RAD_OK ||
             encode_map(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, v_pool, 3, kd, ks, kb) != RAD_OK)
             return RAD_E_CUDA;
-        e = rad::launch_prefill_fp8(tk, tv, p, sms, st);
+        e = pl.family == rad::kFamSplitTC ? rad::launch_split_tc05(tk, tv, p, sms, st)
+                                          : rad::launch_prefill_fp8(tk, tv, p, sms, st);
     } else if (pl.family == rad::kFamPrefillTC) {
         rc = get_encoder();
         if (rc != RAD_OK) return rc;
@@ -459,8 +460,6 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
             encode_bf16_map(&tv, v_pool, 3, kd, ks, kb) != RAD_OK)
             return RAD_E_CUDA;
         e = rad::launch_prefill_tc05(tq, tk, tv, p, sms, st);
-    } else if (pl.family == rad::kFamSplitTC) {
-        e = rad::launch_split_tc05(p, sms, st);
     } else if (head_dim == 128)
         e = fp8 ? rad::launch_d128_fp8(pl.family, p, sms, st) : rad::launch_d128_bf16(pl.family, p, sms, st);
     else
@@ -483,9 +482,10 @@ int describe_call(int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_
     if (pl.family == rad::kFamSplitTC) {
         snprintf(buf, buf_len,
                  "attn_split_tc05 family=%s head_dim=%d kv=fp8e4m3 query_rows_per_kv_head=%d tile_rows=%d "
-                 "keys_per_tile=%d stages=%d ctas_per_sm=1 warps=8 workers+1 qk+1 pv+2 producers "
-                 "mma=tcgen05 (keys as M, query rows as N; QK kind::f8f6f4 on the staged e4m3 K with Q as two "
-                 "e4m3 terms, PV kind::f16 with V e4m3 -> f16 once per tile) "
+                 "keys_per_tile=%d stages=%d ctas_per_sm=1 warps=8 workers+1 qk (+ half the v convert)+1 pv "
+                 "(+ half the v convert)+2 tma producers mma=tcgen05 (keys as M, query rows as N; QK "
+                 "kind::f8f6f4 on the staged e4m3 K with Q as two e4m3 terms, PV kind::f16 with V e4m3 -> f16 "
+                 "once per tile) "
                  "split_len=%d + attn_combine (split order)",
                  family_name(pl.family), head_dim, pl.M, t.QT, t.KS, t.NS, pl.split_len);
         return RAD_OK;

@@ -24,23 +24,31 @@
 // so a decode step's few query rows per KV head cost a narrow N instead of
 // an idle M.  Warp roles (one CTA per SM, persistent):
 //   last two    producers: page ids from the page table ("kern manifest v7",
-//               $defs.Domain), 16-byte cp.async copies of each tile's e4m3 K
-//               rows and V rows (one warp each) into two staging rings,
-//               the per-page scales, and a 1-D bulk copy of the query rows.
+//               $defs.Domain), one TMA box per page (page_size rows x 128
+//               bytes of the KV head) of each tile's e4m3 K rows and V rows
+//               (one warp each, one issuing lane) into the staging ring, the
+//               per-page scales, and a 1-D bulk copy of the query rows.
+//               (16-byte cp.async copies took the producer ~2300 cycles per
+//               tile to issue, which then set the tile period.)
 //   warp 4G     QK MMA: one lane issues the tcgen05.mma of S^T per tile as
 //               soon as its K stage has landed and its TMEM S buffer is free
-//               (up to NSB tiles ahead of the softmax, across items).
-//   warp 4G+1   PV MMA: one lane issues O^T += V^T P^T per tile once the
-//               workers published P and the f16 V tile.
+//               (up to NSB tiles ahead of the softmax, across items); then the
+//               warp converts key rows 0-63 of the previous tile's staged e4m3
+//               V rows to f16 (exact) in the 128-byte-swizzled layout the MMA
+//               reads, into f16 buffer (t-1) & 1 once PV of tile t-3 has read
+//               it (at an item's last tile, also tile t's rows).
+//   warp 4G+1   PV MMA: converts key rows 64-127 of tile t the same way, then
+//               one lane issues O^T += V^T P^T once the workers published P
+//               and the QK warp's rows are converted.
 //   warps 0 .. 4G-1  workers; thread t serves key slot k = t % 128 (TMEM
 //               lane k) and group h = t / 128 of the query rows (warps w,
 //               w+4, .. share TMEM lanes 32(w%4)..): split the item's query
-//               rows into e4m3 terms, convert its share of key row k of the
-//               staged e4m3 V tile to f16 once per tile (exact) in the
-//               128-byte-swizzled layout the MMA reads, run the online softmax
-//               of key k against its group of query rows, write P^T, and in
-//               the epilogue read O^T (lane k = head-dim element k) and store
-//               its rows.
+//               rows into e4m3 terms, run the online softmax of key k against
+//               its group of query rows, write P^T, and in the epilogue read
+//               O^T (lane k = head-dim element k) and store its rows.
+//               (The V conversion ran on the workers before: 800 of the 3200
+//               cycles of a tile's chain through them, in a globaltimer /
+//               clock64 trace of one CTA.)
 // Per query row, the running max moves (and O and the sums are rescaled)
 // only when a tile's logits exceed it by more than 2^8; the per-row sums are
 // kept per key slot and reduced once per item in a fixed order, so a row's
@@ -64,10 +72,6 @@
 #ifndef RAD_SPLITTC_GROUPS
 #define RAD_SPLITTC_GROUPS 2
 #endif
-// Producer warps per tensor (K, V); each takes every PPW-th page of a tile.
-#ifndef RAD_SPLITTC_PPW
-#define RAD_SPLITTC_PPW 1
-#endif
 
 namespace rad {
 
@@ -79,7 +83,6 @@ struct SplitTcCfg {
     static constexpr int NSB = 3;      // S buffers: QK runs up to two tiles ahead of PV
     static constexpr int G = RAD_SPLITTC_GROUPS;
     static constexpr int V = N / G;    // query rows per worker thread
-    static constexpr int CPT = 8 / G;  // 16-byte chunks of a V row each worker converts
     static constexpr int QT = N;       // (item planner) query rows per tile
     static constexpr int KS = BK;      // (item planner) keys per stage
     static constexpr int NS = RAD_SPLITTC_NS;
@@ -117,11 +120,10 @@ struct SplitTcCfg {
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;   // 1 KB alignment of the swizzled operand tiles
     static constexpr int NWORK = 4 * G;                  // worker warps
     static constexpr int NWT = NWORK * 32;               // worker threads
-    static constexpr int PPW = RAD_SPLITTC_PPW;
     static constexpr int W_QK = NWORK, W_PV = NWORK + 1, W_PROD = NWORK + 2;
-    static constexpr int NTHREADS = (NWORK + 2 + 2 * PPW) * 32;
-    static constexpr int K_ARRIVALS = 32 * PPW + 1;       // async lane arrivals + stage meta
-    static constexpr int V_ARRIVALS = 32 * PPW;
+    static constexpr int NTHREADS = (NWORK + 4) * 32;
+    static constexpr int K_ARRIVALS = 1;   // the producer's expect-tx arrive (it also releases the stage meta)
+    static constexpr int V_ARRIVALS = 1;
     static constexpr uint32_t TMEM_COLS = (NSB + 1) * N <= 64 ? 64 : 128;   // S[NSB] and O
     static_assert(N == 16 || N == 32, "query rows per item");
     static_assert((G == 2 || G == 4) && V >= 4, "query-row groups");
@@ -132,24 +134,20 @@ struct SplitTcCfg {
 };
 
 
-// Converts share h of key row t of a staged tile (128 e4m3 codes, 16-byte
-// chunks swizzled by t & 7): chunks h*CPT .. h*CPT+CPT-1 (16 codes each)
-// become f16 in an f16 tile [column block][key][128 B] with the same 128-byte
-// swizzle; `zero` writes zeros instead.  Plain shared-memory loads and stores
-// (ordered by the barrier waits and fences around the call) so they can be
-// scheduled freely.
+// Converts key row t of a staged tile (128 e4m3 codes, 16-byte chunks
+// swizzled by t & 7) to f16 in an f16 tile [column block][key][128 B] with the
+// same 128-byte swizzle; `zero` writes zeros instead.  The row's loads come
+// first: the stores after them may alias them as far as the compiler knows.
 template <class C>
-__device__ __forceinline__ void convert_row_share(const uint8_t* src, uint8_t* dst, int t, int h, bool zero) {
+__device__ __forceinline__ void convert_key_row(const uint8_t* src, uint8_t* dst, int t, bool zero) {
     const uint32_t sw = (uint32_t)(t & 7);
-    uint4 in[C::CPT];
+    uint4 in[8];
 #pragma unroll
-    for (int cc = 0; cc < C::CPT; ++cc)
-        in[cc] = zero ? make_uint4(0u, 0u, 0u, 0u)
-                      : *reinterpret_cast<const uint4*>(src + t * 128 + (((C::CPT * h + cc) ^ sw) << 4));
+    for (int c = 0; c < 8; ++c)
+        in[c] = zero ? make_uint4(0u, 0u, 0u, 0u) : *reinterpret_cast<const uint4*>(src + t * 128 + ((c ^ sw) << 4));
 #pragma unroll
-    for (int cc = 0; cc < C::CPT; ++cc) {
-        const int c = C::CPT * h + cc;
-        const uint4 v = in[cc];
+    for (int c = 0; c < 8; ++c) {
+        const uint4 v = in[c];
         const uint32_t h0 = e4m3x2_to_f16x2((uint16_t)(v.x & 0xFFFFu)), h1 = e4m3x2_to_f16x2((uint16_t)(v.x >> 16));
         const uint32_t h2 = e4m3x2_to_f16x2((uint16_t)(v.y & 0xFFFFu)), h3 = e4m3x2_to_f16x2((uint16_t)(v.y >> 16));
         const uint32_t h4 = e4m3x2_to_f16x2((uint16_t)(v.z & 0xFFFFu)), h5 = e4m3x2_to_f16x2((uint16_t)(v.z >> 16));
@@ -159,6 +157,23 @@ __device__ __forceinline__ void convert_row_share(const uint8_t* src, uint8_t* d
         const uint32_t ch = (uint32_t)((c & 3) * 2);
         *reinterpret_cast<uint4*>(row + ((ch ^ sw) << 4)) = make_uint4(h0, h1, h2, h3);
         *reinterpret_cast<uint4*>(row + (((ch + 1) ^ sw) << 4)) = make_uint4(h4, h5, h6, h7);
+    }
+}
+
+// Key rows lane + 32 r, r = r0 .. r0 + 1, of staged V tile `slot` -> f16 V
+// buffer vb, zeros outside the item's keys [klo, k1) (P is 0 there; those
+// slots may hold anything).  Called by the QK warp (r0 = 0) and the PV warp
+// (r0 = 2) once per tile.
+template <class C>
+__device__ __forceinline__ void convert_v_half(uint8_t* smem, uint32_t slot, uint32_t vb, int r0, int key0, int klo,
+                                               int k1, int lane) {
+    const uint8_t* src = smem + C::OFF_STG + slot * C::STG_BYTES + C::STG_TILE;
+    uint8_t* dst = smem + C::OFF_V16 + vb * C::F16_TILE;
+#pragma unroll 1
+    for (int r = r0; r < r0 + 2; ++r) {
+        const int t = lane + 32 * r;
+        const int key = key0 + t;
+        convert_key_row<C>(src, dst, t, key < klo || key >= k1);
     }
 }
 
@@ -233,7 +248,8 @@ __device__ __forceinline__ void tmem_stV(uint32_t taddr, const uint32_t (&r)[V])
 // counts: bit i of a row's mask word lets it see the call's key i).
 template <int N, int MODE>
 __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
-    attn_split_tc05_kernel(const __grid_constant__ AttnParams p) {
+    attn_split_tc05_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                           const __grid_constant__ AttnParams p) {
     using C = SplitTcCfg<N>;
     constexpr bool WIN = MODE == kModeWindow;
     constexpr bool TREE = MODE == kModeTree;
@@ -249,7 +265,7 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
     const uint32_t bar_qstg_full = bar_v_empty + 8 * C::NS;
     const uint32_t bar_qstg_empty = bar_qstg_full + 8;
     const uint32_t bar_q8_full = bar_qstg_empty + 8;
-    const uint32_t bar_v16_full = bar_q8_full + 16;     // [2], per f16 V buffer
+    const uint32_t bar_v16_full = bar_q8_full + 16;     // [2], per f16 V buffer: the QK warp's half converted
     const uint32_t bar_p_full = bar_v16_full + 16;      // [2], per P buffer
     const uint32_t bar_s_full = bar_p_full + 16;        // [NSB], per S buffer
     const uint32_t bar_s_empty = bar_s_full + 8 * C::NSB;   // [NSB], S read by the workers
@@ -266,10 +282,10 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
             mbar_init(bar_k_full + 8 * i, C::K_ARRIVALS);
             mbar_init(bar_k_empty + 8 * i, 1 + C::NWORK);   // the QK MMA's commit + the workers' scale reads
             mbar_init(bar_v_full + 8 * i, C::V_ARRIVALS);
-            mbar_init(bar_v_empty + 8 * i, C::NWORK);
+            mbar_init(bar_v_empty + 8 * i, 2);   // converted: the QK warp's and the PV warp's rows
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bar_v16_full + 8 * i, C::NWORK);
+            mbar_init(bar_v16_full + 8 * i, 1);   // the QK warp's rows of the tile
             mbar_init(bar_p_full + 8 * i, C::NWORK);
             mbar_init(bar_pv_done + 8 * i, 1);
         }
@@ -301,18 +317,18 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
 
     if (warp >= C::W_PROD) {
         // ===================================================== producers
-        const int pr = warp - C::W_PROD;
-        const int pw = pr / C::PPW;        // 0: K rows (the first K warp also query rows, stage meta); 1: V rows
-        const int pj = pr % C::PPW;        // this warp's pages of a tile: i % PPW == pj
-        const uint8_t* pool = pw == 0 ? p.k_pool : p.v_pool;
+        const int pw = warp - C::W_PROD;   // 0: K rows (also the query rows and the stage meta); 1: V rows
+        const CUtensorMap* tm = pw == 0 ? &tm_k : &tm_v;
         const uint64_t pol_kv = policy_evict_first();
-        constexpr int RPI = 4;     // rows per warp-wide copy: 8 lanes x 16 B per 128-byte row
-        const int lrow = lane >> 3, lc = lane & 7;
+        const uint32_t bar_full = pw == 0 ? bar_k_full : bar_v_full;
+        const uint32_t bar_empty = pw == 0 ? bar_k_empty : bar_v_empty;
+        const int oob_tok = p.num_pages * p.page_size;   // a row past the pool: TMA fills the box with zeros
         uint32_t scount = 0, qcount = 0;
+        if (lane == 0) prefetch_tmap(tm);
         for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
             const ItemPlan it = plan_item<C, WIN>(item, p);
             if (!it.active || !it.seq_ok || it.n_stages == 0) continue;
-            if (pr == 0) {
+            if (pw == 0) {
                 if (qcount >= 1 && !mbar_wait_bounded(bar_qstg_empty, (qcount - 1) & 1u, kWaitLimitNs)) {
                     abort = true;
                     break;
@@ -331,11 +347,10 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                 ++qcount;
             }
             const int P = p.page_size;
+            const int ppt = C::BK / P;    // pages per tile
             const int page_hi = (it.k1 + P - 1) / P;
             const int page_lo = WIN ? it.klo / P : 0;
             const int32_t* trow = p.page_table + (long long)it.g * p.pages_per_seq;
-            const long long row_stride = (long long)p.n_head_kv * C::ROW;
-            const uint8_t* head_base = pool + (long long)it.kvh * C::ROW + (long long)lrow * row_stride + lc * 16;
             int batch0 = -1 << 30;
             int my_pg = 0;
             float my_ks = 1.f, my_vs = 1.f;
@@ -343,8 +358,7 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
             for (int st = 0; st < it.n_stages; ++st) {
                 const int key0 = it.k0 + st * C::BK;
                 const int pstart = key0 / P;
-                const int npages = min(C::BK / P, page_hi - pstart);
-                if (pstart + npages > batch0 + 32) {
+                if (pstart + ppt > batch0 + 32) {
                     batch0 = pstart;
                     const int pi = batch0 + lane;
                     my_bad = false;
@@ -361,25 +375,13 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                     }
                 }
                 const uint32_t slot = scount % C::NS, use = scount / C::NS;
-                const uint32_t bar_empty = (pw == 0 ? bar_k_empty : bar_v_empty) + 8 * slot;
-                if (use >= 1 && !mbar_wait_bounded(bar_empty, (use - 1) & 1u, kWaitLimitNs)) {
+                if (use >= 1 && !mbar_wait_bounded(bar_empty + 8 * slot, (use - 1) & 1u, kWaitLimitNs)) {
                     abort = true;
                     break;
                 }
                 const uint32_t tile = base + C::OFF_STG + slot * C::STG_BYTES + pw * C::STG_TILE;
-                for (int i = pj; i < npages; i += C::PPW) {
-                    if (WIN && pstart + i < page_lo) continue;   // stale rows: masked in S, zeroed in V
-                    const int pg = __shfl_sync(0xffffffffu, my_pg, (pstart - batch0 + i) & 31);
-                    const uint8_t* src = head_base + (long long)pg * P * row_stride;
-                    const uint32_t dst = tile + (uint32_t)(i * P * 128);
-#pragma unroll 4
-                    for (int t0 = 0; t0 < P; t0 += RPI) {
-                        const int t = t0 + lrow;   // slot in the page; key i*P + t of the tile
-                        cp_async_16(dst + t * 128 + ((lc ^ (t & 7)) << 4), src + (long long)t0 * row_stride, pol_kv);
-                    }
-                }
-                cp_async_arrive_noinc((pw == 0 ? bar_k_full : bar_v_full) + 8 * slot);
-                if (pr == 0) {
+                if (pw == 0) {
+                    // the tile's page scales and page-id flag, released by the arrive below
                     uint32_t bad_any = 0;
                     float kss[C::MAXPG], vss[C::MAXPG];
 #pragma unroll
@@ -388,7 +390,7 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                         kss[i] = __shfl_sync(0xffffffffu, my_ks, src);
                         vss[i] = __shfl_sync(0xffffffffu, my_vs, src);
                         const uint32_t b = __shfl_sync(0xffffffffu, (uint32_t)my_bad, src);
-                        if (i < npages) bad_any |= b;
+                        if (i < ppt && pstart + i < page_hi) bad_any |= b;
                     }
                     if (lane == 0) {
                         float* meta = reinterpret_cast<float*>(smem + C::OFF_META + slot * C::META_STRIDE);
@@ -398,21 +400,61 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                             meta[8 + i] = vss[i];
                         }
                         reinterpret_cast<uint32_t*>(meta)[16] = bad_any ? kErrPage : 0u;
-                        mbar_arrive(bar_k_full + 8 * slot);
                     }
                 }
+                // one 3-D box per page (P rows x 128 bytes of this KV head, 128-byte swizzle,
+                // the layout the MMA and the conversion read); pages outside the item's
+                // range (past the sequence, or below the window) load zeros
+                int pg_i[C::MAXPG];
+#pragma unroll
+                for (int i = 0; i < C::MAXPG; ++i) pg_i[i] = __shfl_sync(0xffffffffu, my_pg, (pstart - batch0 + i) & 31);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar_full + 8 * slot, (uint32_t)C::STG_TILE);
+#pragma unroll
+                    for (int i = 0; i < C::MAXPG; ++i) {
+                        if (i < ppt) {
+                            const int pi = pstart + i;
+                            const int tok = ((!WIN || pi >= page_lo) && pi < page_hi) ? pg_i[i] * P : oob_tok;
+                            tma_load_3d(tile + (uint32_t)(i * P * C::ROW), tm, bar_full + 8 * slot, 0, it.kvh, tok,
+                                        pol_kv);
+                        }
+                    }
+                }
+                __syncwarp();
                 ++scount;
             }
             if (misc[1]) abort = true;
         }
-        cp_async_wait_all();
-        if (pr == 0 && lane == 0 && qcount >= 1) mbar_wait_bounded(bar_qstg_full, (qcount - 1) & 1u, kWaitLimitNs);
+        // drain: nothing may still be landing in shared memory at exit
+        if (lane == 0) {
+            const uint32_t first = scount > (uint32_t)C::NS ? scount - C::NS : 0u;
+            for (uint32_t c = first; c < scount; ++c)
+                mbar_wait_bounded(bar_full + 8 * (c % C::NS), (c / C::NS) & 1u, kWaitLimitNs);
+            if (pw == 0 && qcount >= 1) mbar_wait_bounded(bar_qstg_full, (qcount - 1) & 1u, kWaitLimitNs);
+        }
+        __syncwarp();
     } else if (warp == C::W_QK) {
         // ===================================================== QK MMA issue
         constexpr uint32_t idesc_qk = umma_idesc_e4m3(128, N);        // A = K, B = Q terms (both K-major)
         const uint32_t q8 = base + C::OFF_Q8;
         uint32_t tcnt = 0, scnt = 0, icnt = 0;
         bool issued = false;
+        // Key rows 0 .. 63 of tile tt (an index over all tiles of this CTA; its
+        // stage is tt % NS) -> f16 buffer tt & 1, last read by PV(tt - 2).
+        const auto convert_qk_half = [&](uint32_t tt, int key0, const ItemPlan& it) -> bool {
+            const uint32_t slot = tt % C::NS, vb = tt & 1u;
+            bool ok = mbar_wait_bounded(bar_v_full + 8 * slot, (tt / C::NS) & 1u, kWaitLimitNs);
+            if (ok && tt >= 2) ok = mbar_wait_bounded(bar_pv_done + 8 * vb, ((tt - 2) >> 1) & 1u, kWaitLimitNs);
+            if (!__all_sync(0xffffffffu, ok)) return false;
+            convert_v_half<C>(smem, slot, vb, 0, key0, it.klo, it.k1, lane);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bar_v16_full + 8 * vb);
+                mbar_arrive(bar_v_empty + 8 * slot);
+            }
+            return true;
+        };
         for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
             const ItemPlan it = plan_item<C, WIN>(item, p);
             if (!it.active || !it.seq_ok || it.n_stages == 0) continue;
@@ -446,6 +488,15 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                     issued = true;
                 }
                 __syncwarp();
+                // key rows 0 .. 63 of the previous tile of the item (its f16 buffer was
+                // freed by PV(tt - 3)), and at the item's last tile of this one too (freed
+                // by PV(tt - 2)), so no PV waits for the next item's first QK; converting
+                // tile tt itself here would hold QK(tt + 1) until PV(tt - 2) is done
+                if ((i >= 1 && !convert_qk_half(tt - 1, it.k0 + (i - 1) * C::BK, it)) ||
+                    (i == T - 1 && !convert_qk_half(tt, it.k0 + i * C::BK, it))) {
+                    abort = true;
+                    break;
+                }
             }
             tcnt += T;
             scnt += T;
@@ -469,6 +520,19 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
             const int T = it.n_stages;
             for (int j = 0; j < T; ++j) {
                 const uint32_t tt = tcnt + j, b = tt & 1u;
+                // key rows 64 .. 127 of V_j -> f16 buffer b (last read by PV(tt - 2)) while
+                // the workers run the softmax of tile j
+                const uint32_t slot = tt % C::NS, use = tt / C::NS;
+                bool ok = mbar_wait_bounded(bar_v_full + 8 * slot, use & 1u, kWaitLimitNs);
+                if (ok && tt >= 2) ok = mbar_wait_bounded(bar_pv_done + 8 * b, ((tt - 2) >> 1) & 1u, kWaitLimitNs);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    abort = true;
+                    break;
+                }
+                convert_v_half<C>(smem, slot, b, 2, it.k0 + j * C::BK, it.klo, it.k1, lane);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_v_empty + 8 * slot);
                 if (!mbar_wait_bounded(bar_p_full + 8 * b, (tt >> 1) & 1u, kWaitLimitNs) ||
                     !mbar_wait_bounded(bar_v16_full + 8 * b, (tt >> 1) & 1u, kWaitLimitNs) ||
                     (j == 0 && icnt >= 1 && !mbar_wait_bounded(bar_o_free, (icnt - 1) & 1u, kWaitLimitNs))) {
@@ -510,7 +574,6 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
         const int wq = warp & 3;                   // TMEM lane quarter
         const int col0 = h * V;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-        uint8_t* const v16p = smem + C::OFF_V16;
         uint8_t* const q8p = smem + C::OFF_Q8;
         float* const isq = reinterpret_cast<float*>(smem + C::OFF_ISQ);
         uint32_t* const tmw = reinterpret_cast<uint32_t*>(smem + C::OFF_TMW);
@@ -685,29 +748,11 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_k_empty + 8 * slot);
             };
-            // Staged V rows of tile i -> f16 V buffer (tcnt + i) & 1, zero outside
-            // the item's keys (P is 0 there; the slots may hold anything).
-            const auto load_v = [&](int i) {
-                const uint32_t slot = (scount + i) % C::NS, use = (scount + i) / C::NS;
-                const uint32_t vb = (tcnt + i) & 1u;
-                if (!lab && !mbar_wait_bounded(bar_v_full + 8 * slot, use & 1u, kWaitLimitNs)) lab = true;
-                const int key = it.k0 + i * C::BK + k;
-                convert_row_share<C>(smem + C::OFF_STG + slot * C::STG_BYTES + C::STG_TILE, v16p + vb * C::F16_TILE, k,
-                                    h, lab || key < it.klo || key >= it.k1);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(bar_v16_full + 8 * vb);
-                    mbar_arrive(bar_v_empty + 8 * slot);
-                }
-            };
             // Waits until PV of tile tt (an index over all tiles of this CTA) is done.
             const auto wait_pv = [&](uint32_t tt) {
                 if (!lab && !mbar_wait_bounded(bar_pv_done + 8 * (tt & 1u), (tt >> 1) & 1u, kWaitLimitNs)) lab = true;
                 tc_fence_after();
             };
-            // ---- prologue (the previous item's MMAs are all done: its epilogue waited)
-            load_v(0);
             for (int j = 0; j < T; ++j) {
                 const uint32_t tt = tcnt + j, b = tt & 1u, sb = tt % C::NSB;
                 const int kbase = it.k0 + j * C::BK;
@@ -817,11 +862,6 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_p_full + 8 * b);
-                // ---- tile j+1's V rows into the other f16 V buffer, last read by PV(j-1)
-                if (j + 1 < T) {
-                    if (j >= 1) wait_pv(tt - 1);
-                    load_v(j + 1);
-                }
             }
             if (abort) break;
             // ---- the next item's query rows now, so its QKs run during this epilogue

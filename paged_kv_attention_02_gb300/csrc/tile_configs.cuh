@@ -142,7 +142,8 @@ cudaError_t launch_prefill_tc05(const CUtensorMap& tq, const CUtensorMap& tk, co
                                 const AttnParams& p, int sms, cudaStream_t st);
 cudaError_t launch_prefill_fp8(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
                                cudaStream_t st);
-cudaError_t launch_split_tc05(const AttnParams& p, int sms, cudaStream_t st);
+cudaError_t launch_split_tc05(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
+                              cudaStream_t st);
 TileInfo split_tc05_info(int n);
 // Ragged calls: the tile maps (one CTA), before the tile kernels.  map[1]
 // null: one class; else sequences with at most split_m query rows per KV head
