@@ -98,8 +98,10 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
     // it applies, else the wide tile.
     pl.split_len = rows <= rad::kSplitMaxRows ? rad::kSplitLen : 0;
     const bool ragged = ragged_rows >= 0;
-    if (pl.split_len > 0 && RAD_SPLIT_TC05 && !ragged && head_dim == 128 && kv_dtype == RAD_KV_FP8_E4M3)
+    if (pl.split_len > 0 && RAD_SPLIT_TC05 && !ragged && head_dim == 128 && kv_dtype == RAD_KV_FP8_E4M3) {
         pl.family = rad::kFamSplitTC;
+        pl.split_len = rad::kSplitLenTC;
+    }
     else if (pl.split_len > 0)
         pl.family = pl.M <= 8 ? rad::kFamDecode : rad::kFamVerify;
     else

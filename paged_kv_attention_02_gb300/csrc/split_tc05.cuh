@@ -122,8 +122,8 @@ struct SplitTcCfg {
     static constexpr int NWT = NWORK * 32;               // worker threads
     static constexpr int W_QK = NWORK, W_PV = NWORK + 1, W_PROD = NWORK + 2;
     static constexpr int NTHREADS = (NWORK + 4) * 32;
-    static constexpr int K_ARRIVALS = 1;   // the producer's expect-tx arrive (it also releases the stage meta)
-    static constexpr int V_ARRIVALS = 1;
+    static constexpr int K_ARRIVALS = MAXPG;   // the producer's expect-tx arrive + 7 lanes' meta arrives
+    static constexpr int V_ARRIVALS = 1;       // the producer's expect-tx arrive
     static constexpr uint32_t TMEM_COLS = (NSB + 1) * N <= 64 ? 64 : 128;   // S[NSB] and O
     static_assert(N == 16 || N == 32, "query rows per item");
     static_assert((G == 2 || G == 4) && V >= 4, "query-row groups");
@@ -380,46 +380,36 @@ __global__ void __launch_bounds__(SplitTcCfg<N>::NTHREADS, 1)
                     break;
                 }
                 const uint32_t tile = base + C::OFF_STG + slot * C::STG_BYTES + pw * C::STG_TILE;
+                // lane i < ppt: page i of the tile (its id, scales and flag in one shuffle each)
+                const int pi = pstart + lane;
+                const int srcl = (pstart - batch0 + lane) & 31;
+                const int pg = __shfl_sync(0xffffffffu, my_pg, srcl);
+                const bool mine = lane < ppt;
+                const bool live = mine && (!WIN || pi >= page_lo) && pi < page_hi;
                 if (pw == 0) {
                     // the tile's page scales and page-id flag, released by the arrive below
-                    uint32_t bad_any = 0;
-                    float kss[C::MAXPG], vss[C::MAXPG];
-#pragma unroll
-                    for (int i = 0; i < C::MAXPG; ++i) {
-                        const int src = (pstart - batch0 + i) & 31;
-                        kss[i] = __shfl_sync(0xffffffffu, my_ks, src);
-                        vss[i] = __shfl_sync(0xffffffffu, my_vs, src);
-                        const uint32_t b = __shfl_sync(0xffffffffu, (uint32_t)my_bad, src);
-                        if (i < ppt && pstart + i < page_hi) bad_any |= b;
+                    const float ksl = __shfl_sync(0xffffffffu, my_ks, srcl);
+                    const float vsl = __shfl_sync(0xffffffffu, my_vs, srcl);
+                    const bool badl = __shfl_sync(0xffffffffu, (uint32_t)my_bad, srcl) != 0u;
+                    const bool bad_any = __any_sync(0xffffffffu, mine && pi < page_hi && badl);
+                    // each of lanes 0 .. MAXPG-1 releases its own entries with its arrive
+                    float* meta = reinterpret_cast<float*>(smem + C::OFF_META + slot * C::META_STRIDE);
+                    if (lane < C::MAXPG) {
+                        meta[lane] = ksl;
+                        meta[8 + lane] = vsl;
                     }
-                    if (lane == 0) {
-                        float* meta = reinterpret_cast<float*>(smem + C::OFF_META + slot * C::META_STRIDE);
-#pragma unroll
-                        for (int i = 0; i < C::MAXPG; ++i) {
-                            meta[i] = kss[i];
-                            meta[8 + i] = vss[i];
-                        }
-                        reinterpret_cast<uint32_t*>(meta)[16] = bad_any ? kErrPage : 0u;
-                    }
+                    if (lane == 0) reinterpret_cast<uint32_t*>(meta)[16] = bad_any ? kErrPage : 0u;
+                    if (lane > 0 && lane < C::MAXPG) mbar_arrive(bar_full + 8 * slot);
                 }
                 // one 3-D box per page (P rows x 128 bytes of this KV head, 128-byte swizzle,
-                // the layout the MMA and the conversion read); pages outside the item's
-                // range (past the sequence, or below the window) load zeros
-                int pg_i[C::MAXPG];
-#pragma unroll
-                for (int i = 0; i < C::MAXPG; ++i) pg_i[i] = __shfl_sync(0xffffffffu, my_pg, (pstart - batch0 + i) & 31);
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(bar_full + 8 * slot, (uint32_t)C::STG_TILE);
-#pragma unroll
-                    for (int i = 0; i < C::MAXPG; ++i) {
-                        if (i < ppt) {
-                            const int pi = pstart + i;
-                            const int tok = ((!WIN || pi >= page_lo) && pi < page_hi) ? pg_i[i] * P : oob_tok;
-                            tma_load_3d(tile + (uint32_t)(i * P * C::ROW), tm, bar_full + 8 * slot, 0, it.kvh, tok,
-                                        pol_kv);
-                        }
-                    }
-                }
+                // the layout the MMA and the conversion read), issued by lanes 0 .. ppt-1;
+                // pages outside the item's range (past the sequence, or below the window)
+                // load zeros
+                if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * slot, (uint32_t)C::STG_TILE);
+                __syncwarp();
+                if (mine)
+                    tma_load_3d(tile + (uint32_t)(lane * P * C::ROW), tm, bar_full + 8 * slot, 0, it.kvh,
+                                live ? pg * P : oob_tok, pol_kv);
                 __syncwarp();
                 ++scount;
             }

@@ -24,6 +24,13 @@ inline int split_tc05_rows(int M) { return M <= 16 ? 16 : 32; }
 #define RAD_SPLIT_LEN 1024
 #endif
 constexpr int kSplitLen = RAD_SPLIT_LEN;
+// The tcgen05 split kernel's splits (fp8 head_dim-128 split calls): each work
+// item pays a fixed cost (query-row split, epilogue, the wait for its last PV)
+// that longer splits spread over more key tiles.
+#ifndef RAD_SPLITTC_LEN
+#define RAD_SPLITTC_LEN 2048
+#endif
+constexpr int kSplitLenTC = RAD_SPLITTC_LEN;
 constexpr int kSplitMaxRows = 256;
 
 // Tile shapes: WQ, NQW, WK, KS, NS, CTAs per SM (see TileCfg).  Each can be

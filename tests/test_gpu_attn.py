@@ -25,6 +25,11 @@ MID = {
                               "fixed:40,900,1700", pages_per_seq=60),
     "ver_fp8": wl.Config("ver_fp8", 5, 8, 32, 8, 128, 16, wl.KV_FP8_E4M3, 105, "fixed:8,9,520,1000,2050",
                          pages_per_seq=130),
+    # the tcgen05 split kernel's 2048-key splits: lengths on both sides of 1, 2 and 3 splits
+    "ver_fp8_splits": wl.Config("ver_fp8_splits", 6, 8, 32, 8, 128, 16, wl.KV_FP8_E4M3, 116,
+                                "fixed:2047,2048,2049,4095,4097,6145", pages_per_seq=390),
+    "dec_fp8_splits": wl.Config("dec_fp8_splits", 5, 1, 32, 8, 128, 32, wl.KV_FP8_E4M3, 117,
+                                "fixed:2047,2048,2049,4096,4097", pages_per_seq=130),
     "ver_bf16": wl.Config("ver_bf16", 4, 8, 8, 2, 128, 16, wl.KV_BF16, 106, "fixed:8,100,513,1100",
                           pages_per_seq=70),
     "ver_wide_d256": wl.Config("ver_wide_d256", 3, 8, 16, 2, 256, 32, wl.KV_BF16, 107, "fixed:8,600,1500",
