@@ -1,0 +1,44 @@
+"""Host-side logic of bench.py, on CPU: which workloads are timed after an L2
+flush, what the line's `l2` note says, and where the roofline peaks come from."""
+import json
+import os
+from types import SimpleNamespace
+
+import bench
+from paged_kv_attention_02_gb300 import workloads as wl
+
+
+def _sized(kv_bytes, q_bytes=1 << 20, table_bytes=1 << 16):
+    """A stand-in workload with arrays of the given sizes (only .nbytes is read)."""
+    half = SimpleNamespace(nbytes=kv_bytes // 2)
+    return SimpleNamespace(k_pool=half, v_pool=half, q=SimpleNamespace(nbytes=q_bytes),
+                           page_table=SimpleNamespace(nbytes=table_bytes))
+
+
+def test_inputs_that_fit_twice_in_l2_are_flushed_and_larger_ones_are_not():
+    assert bench.fits_l2(_sized(1 << 20))                        # the tiny decode's 1 MB pool
+    assert bench.fits_l2(_sized(34 * 10**6, q_bytes=17 * 10**6))  # a prefill chunk's pools and rows
+    assert not bench.fits_l2(_sized(4_500 * 10**6))              # the batched decode's pools
+    edge = 2 * bench.L2_BYTES
+    assert not bench.fits_l2(_sized(edge, q_bytes=0, table_bytes=0))
+    assert bench.fits_l2(_sized(edge - 2, q_bytes=0, table_bytes=0))
+
+
+def test_the_flush_buffer_is_larger_than_l2():
+    assert bench.FLUSH_BYTES > bench.L2_BYTES
+
+
+def test_the_l2_note_names_the_method_that_ran():
+    w = wl.make_workload("tiny_decode")
+    assert bench.workload_config(w)["l2"] == bench.L2_FLUSHED
+    assert bench.workload_config(w, l2="host")["l2"] == "host"
+    big = _sized(4_500 * 10**6)
+    assert bench.fits_l2(big) is False
+    assert "exceed" in bench.L2_LARGE and "flush" in bench.L2_FLUSHED
+
+
+def test_roofline_peaks_come_from_the_measured_file():
+    with open(os.path.join(bench.ROOT, "MEASURED_PEAKS.json")) as f:
+        peaks = json.load(f)
+    assert bench.hbm_peak() == (float(peaks["hbm_gbs"]), "measured")
+    assert bench.tensor_peak() == (float(peaks["bf16_tflops"]), "measured")
