@@ -83,6 +83,30 @@ def test_tiny_decode_matches_oracle_everywhere():
     assert_parity(as_f64(out), oracle_rows(w).out, False, "tiny_decode")
 
 
+# ------------------------------------------------------------------ contexts past one combine chunk
+
+# The combine kernel stages a row's partials 128 splits at a time: these contexts
+# have more splits than that (1024-key splits on the tile kernel, 2048 on the
+# tcgen05 split kernel), so rows merge across chunk boundaries.
+LONG = {
+    "long_dec_bf16": wl.Config("long_dec_bf16", 2, 1, 8, 2, 128, 16, wl.KV_BF16, 121, "fixed:140000,1000",
+                               pages_per_seq=8760),
+    "long_ver_fp8": wl.Config("long_ver_fp8", 1, 8, 8, 2, 128, 32, wl.KV_FP8_E4M3, 122, "fixed:270000",
+                              pages_per_seq=8440),
+}
+
+
+@pytest.mark.parametrize("name", list(LONG))
+def test_contexts_past_one_combine_chunk_match_oracle(name):
+    w = wl.make_workload(LONG[name], poison=True)
+    dw = DevWorkload(w)
+    out, err = dw.run()
+    assert err == 0
+    assert_parity(as_f64(out), oracle_rows(w).out, dw.fp8, name)
+    del dw
+    torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------------ full-size configurations
 
 @pytest.fixture(scope="module")
