@@ -213,6 +213,26 @@ def test_verified_rows_equal_decode_rows_bit_for_bit(mid, name):
 
 # ------------------------------------------------------------------ errors never fault
 
+def test_q_beyond_f16_range_flags_head_dim_256_fp8_only(mid):
+    """fp8 pools with head_dim 256 round q to f16: an element past its range
+    raises RAD_ERRW_QRANGE (the other groups still match the oracle); head_dim
+    128 splits q exactly into two e4m3 terms and raises nothing."""
+    big = 100352.0   # a bf16 value past the f16 maximum (65504)
+    for name, flagged in (("dec_fp8_d256", True), ("dec_fp8_ratio1", False)):
+        w, dw = mid(name)
+        q = w.q.copy()
+        q[0, 0, 0, 5] = np.array([big], dtype=np.float32).view(np.uint32)[0] >> 16   # bf16 bits
+        qd = torch.from_numpy(np.ascontiguousarray(q).view(np.int16)).view(torch.bfloat16).cuda()
+        out, err = dw.run(q=qd)
+        if flagged:
+            assert err & b.RAD_ERRW_QRANGE
+            ref = oracle_rows(w)
+            assert_parity(as_f64(out)[1:], ref.out[1:], True, name)
+        else:
+            assert err == 0
+            assert np.all(np.isfinite(as_f64(out)))
+
+
 def test_bad_inputs_flag_errors_and_zero_only_their_group(mid):
     w, dw = mid("dec128")
     good, _ = dw.run()
