@@ -462,3 +462,35 @@ def test_fp8_generator_codes_decode_within_half_an_ulp():
     assert np.all(np.isfinite(x))
     amax = np.abs(e4m3_values(w.k_pool)).reshape(w.num_pages, -1).max(axis=1)
     assert np.all(amax == 448.0)
+
+
+# ----------------------------------------------------------------------------- random tiny shapes
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_tiny_shapes_match_brute_force(seed):
+    """Seeded random tiny calls -- rows, GQA grouping, page size, lengths from
+    the row count up, fp8 or bf16 codes, with or without a window -- against
+    the pure-Python brute force over the contiguous sequences."""
+    r = np.random.default_rng(5000 + seed)
+    G, R = int(r.integers(1, 4)), int(r.integers(1, 6))
+    Hkv, ratio = int(r.integers(1, 4)), int(r.integers(1, 4))
+    H, D, P = Hkv * ratio, int(r.choice([2, 4, 8])), int(r.choice([1, 2, 4, 8]))
+    fp8 = bool(r.integers(0, 2))
+    lens = [R + int(r.integers(0, 30)) for _ in range(G)]
+    W = int(r.choice([0, 0, 1, 3, 10]))
+    c = random_case(r, G=G, R=R, H=H, Hkv=Hkv, D=D, P=P, lens=lens, fp8=fp8)
+    scale = float(np.float32(r.uniform(0.05, 1.5)))
+    res = run_oracle(c, R=R, H=H, Hkv=Hkv, D=D, P=P, scale=scale, fp8=fp8, window=W)
+    assert res.err_word == 0
+    qv = bf16_values(c["q"])
+    for g, L in enumerate(lens):
+        if fp8:
+            pages = c["table"][g]
+            ks = np.array([c["ks"][pages[j // P]] for j in range(L)], dtype=np.float64)
+            vs = np.array([c["vs"][pages[j // P]] for j in range(L)], dtype=np.float64)
+            kf = e4m3_values(c["seqs_k"][g]) * ks[:, None, None]
+            vf = e4m3_values(c["seqs_v"][g]) * vs[:, None, None]
+        else:
+            kf, vf = bf16_values(c["seqs_k"][g]), bf16_values(c["seqs_v"][g])
+        want = attend_sequence(qv[g].tolist(), kf.tolist(), vf.tolist(), scale, Hkv, window=W)
+        np.testing.assert_allclose(res.out[g], np.array(want), rtol=1e-12, atol=1e-12)
