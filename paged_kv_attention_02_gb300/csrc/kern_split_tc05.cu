@@ -8,17 +8,20 @@
 
 namespace rad {
 
-namespace {
+TileInfo split_tc05_info() {
+    using C = SplitTcCfg;
+    return TileInfo{128, 1, 4, 0, 0, C::BK, C::NSK, C::QT, C::NTHREADS, C::SMEM_BYTES, 1};
+}
 
-template <int N>
-cudaError_t launch_n(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms, cudaStream_t st) {
-    using C = SplitTcCfg<N>;
-    auto kern = p.window > 0  ? attn_split_tc05_kernel<N, kModeWindow>
-                : p.tree_mask ? attn_split_tc05_kernel<N, kModeTree>
-                              : attn_split_tc05_kernel<N, kModeCausal>;
+cudaError_t launch_split_tc05(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
+                              cudaStream_t st) {
+    using C = SplitTcCfg;
+    auto kern = p.window > 0  ? attn_split_tc05_kernel<kModeWindow>
+                : p.tree_mask ? attn_split_tc05_kernel<kModeTree>
+                              : attn_split_tc05_kernel<kModeCausal>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    long long grid = sms;   // one CTA per SM (shared memory), persistent over the items
+    long long grid = sms;   // one CTA per SM (shared memory, all of TMEM), persistent over the items
     if (grid > p.n_items) grid = p.n_items;
     if (grid < 1) grid = 1;
     cudaLaunchConfig_t cfg = {};
@@ -26,23 +29,7 @@ cudaError_t launch_n(const CUtensorMap& tk, const CUtensorMap& tv, const AttnPar
     cfg.blockDim = dim3(C::NTHREADS, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = st;
-    return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
-}
-
-}  // namespace
-
-TileInfo split_tc05_info(int n) {
-    if (n == 16) {
-        using C = SplitTcCfg<16>;
-        return TileInfo{128, 1, 4, 0, 0, C::BK, C::NS, C::N, C::NTHREADS, C::SMEM_BYTES, 1};
-    }
-    using C = SplitTcCfg<32>;
-    return TileInfo{128, 1, 4, 0, 0, C::BK, C::NS, C::N, C::NTHREADS, C::SMEM_BYTES, 1};
-}
-
-cudaError_t launch_split_tc05(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
-                              cudaStream_t st) {
-    const cudaError_t e = p.qt_rows == 16 ? launch_n<16>(tk, tv, p, sms, st) : launch_n<32>(tk, tv, p, sms, st);
+    e = cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
     if (e != cudaSuccess || p.max_splits <= 1) return e;
     return launch_combine<128>(p, st);
 }

@@ -111,7 +111,7 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
         pl.tile = rad::TileInfo{128, 0, 4, 0, 0, rad::PrefillTileKeys, RAD_PREFILL_NSK + RAD_PREFILL_NSV, 128, 256, 0,
                                 RAD_PREFILL_CTAS};
     else if (pl.family == rad::kFamSplitTC)
-        pl.tile = rad::split_tc05_info(rad::split_tc05_rows(pl.M));
+        pl.tile = rad::split_tc05_info();
     else
         pl.tile = tile_for(head_dim, kv_dtype, pl.family);
     pl.n_qtiles = (pl.M + pl.tile.QT - 1) / pl.tile.QT;
@@ -484,10 +484,10 @@ int describe_call(int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_
     if (pl.family == rad::kFamSplitTC) {
         snprintf(buf, buf_len,
                  "attn_split_tc05 family=%s head_dim=%d kv=fp8e4m3 query_rows_per_kv_head=%d tile_rows=%d "
-                 "keys_per_tile=%d stages=%d ctas_per_sm=1 warps=8 workers+1 qk (+ half the v convert)+1 pv "
-                 "(+ half the v convert)+2 tma producers mma=tcgen05 (keys as M, query rows as N; QK "
-                 "kind::f8f6f4 on the staged e4m3 K with Q as two e4m3 terms, PV kind::f16 with V e4m3 -> f16 "
-                 "once per tile) "
+                 "keys_per_tile=%d stages=%d ctas_per_sm=1 warps=12 4 softmax (a quarter of each tile's keys "
+                 "each)+1 qk+1 pv+2 tma producers+4 v converters mma=tcgen05 (query rows as M, four copies; keys "
+                 "as N; QK kind::f8f6f4 on the staged e4m3 K with Q as two e4m3 terms, PV kind::f16 with P from "
+                 "TMEM and V e4m3 -> f16 once per tile) "
                  "split_len=%d + attn_combine (split order)",
                  family_name(pl.family), head_dim, pl.M, t.QT, t.KS, t.NS, pl.split_len);
         return RAD_OK;

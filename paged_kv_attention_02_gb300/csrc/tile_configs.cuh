@@ -14,9 +14,6 @@ enum Family : int { kFamDecode = 0, kFamVerify = 1, kFamWide = 2, kFamPrefillTC 
 #ifndef RAD_SPLIT_TC05
 #define RAD_SPLIT_TC05 1
 #endif
-// Query rows per item of the tcgen05 split kernel for a call with M query
-// rows per KV head: 16 or 32 (the MMA's N).
-inline int split_tc05_rows(int M) { return M <= 16 ? 16 : 32; }
 
 // Keys per split for calls of up to kSplitMaxRows rows; longer calls (prefill
 // chunks) run one range per query tile.  A multiple of every tile's KS.
@@ -151,7 +148,7 @@ cudaError_t launch_prefill_fp8(const CUtensorMap& tk, const CUtensorMap& tv, con
                                cudaStream_t st);
 cudaError_t launch_split_tc05(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
                               cudaStream_t st);
-TileInfo split_tc05_info(int n);
+TileInfo split_tc05_info();
 // Ragged calls: the tile maps (one CTA), before the tile kernels.  map[1]
 // null: one class; else sequences with at most split_m query rows per KV head
 // go to map[0] (tiles of qt[0] rows), the rest to map[1].
