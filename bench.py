@@ -50,8 +50,8 @@ FALLBACK_HBM_GBS = 6800.0
 # while the kernel sources hash to `src_sha256`.
 NCU_TRAFFIC: dict[str, dict] = {
     # profiles/attn_tile_batched_decode_64seq.md: 64-sequence capture scaled by KV bytes
-    "batched_decode": {"bytes_per_launch": 4_499_400_000 + 21_800_000,
-                       "src_sha256": "72d342ebf71f6a424eaf31faa81d6c432df93daa1d14a75f915e68e729ea4e7f"},
+    "batched_decode": {"bytes_per_launch": 4_499_400_000 + 20_100_000,
+                       "src_sha256": "001b2f1fdc8ca78ea7f2b85f2b1dc3eef7d2d82a999105deaa0ed95d1456bea6"},
 }
 
 
