@@ -57,10 +57,10 @@
 #include "tc05.cuh"
 
 #ifndef RAD_SPLITTC_NSK
-#define RAD_SPLITTC_NSK 3
+#define RAD_SPLITTC_NSK 4
 #endif
 #ifndef RAD_SPLITTC_NSV
-#define RAD_SPLITTC_NSV 3
+#define RAD_SPLITTC_NSV 2
 #endif
 
 namespace rad {
