@@ -498,7 +498,8 @@ def launches_per_step(w) -> int:
     the tile map of a ragged call."""
     c = w.cfg
     desc = describe(w)
-    kernels = desc.count("attn_tile family") + desc.count("attn_split_tc05 ") + desc.count("attn_prefill_tc05 ")
+    kernels = (desc.count("attn_tile family") + desc.count("attn_split_tc05 ") + desc.count("attn_split_bf16_tc05 ")
+               + desc.count("attn_prefill_tc05 "))
     split_len = int(desc.split("split_len=")[1].split()[0])
     combines = desc.count("attn_combine") if split_len > 0 and w.pages_per_seq * c.page_size > split_len else 0
     return kernels + combines + int("ragged_tile_map" in desc)

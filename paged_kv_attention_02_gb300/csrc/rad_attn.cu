@@ -81,9 +81,10 @@ bool use_prefill_tc(int32_t rows, int32_t ratio, int32_t head_dim, int32_t kv_dt
     return rows > rad::kSplitMaxRows && head_dim == 128 && ratio <= 128 && 128 % ratio == 0;
 }
 
-// `general`: a call with ragged rows (cu_seqlens) or tree masks.  Ragged
-// calls run on the tile kernels only; tree calls also on the tcgen05 split
-// kernel.  `ragged_rows` >= 0 marks a ragged call: its work and workspace run
+// `general`: a call with ragged rows (cu_seqlens) or tree masks.  Split calls
+// with head_dim 128 run on the tcgen05 split kernels whether ragged or not,
+// with or without tree masks; the others on the tile kernels.  `ragged_rows`
+// >= 0 marks a ragged call: its work and workspace run
 // over the call's query tiles, bounded with the caller's total of rows when
 // it gives one (> 0), else with `rows` rows per sequence.
 Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_dim,
@@ -98,8 +99,12 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
     // it applies, else the wide tile.
     pl.split_len = rows <= rad::kSplitMaxRows ? rad::kSplitLen : 0;
     const bool ragged = ragged_rows >= 0;
-    if (pl.split_len > 0 && RAD_SPLIT_TC05 && !ragged && head_dim == 128 && kv_dtype == RAD_KV_FP8_E4M3) {
+    if (pl.split_len > 0 && RAD_SPLIT_TC05 && head_dim == 128 && kv_dtype == RAD_KV_FP8_E4M3) {
         pl.family = rad::kFamSplitTC;
+        pl.split_len = rad::kSplitLenTC;
+    }
+    else if (pl.split_len > 0 && RAD_SPLIT_BF16_TC05 && head_dim == 128 && kv_dtype == RAD_KV_BF16) {
+        pl.family = rad::kFamSplitBf;
         pl.split_len = rad::kSplitLenTC;
     }
     else if (pl.split_len > 0)
@@ -112,6 +117,8 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
                                 RAD_PREFILL_CTAS};
     else if (pl.family == rad::kFamSplitTC)
         pl.tile = rad::split_tc05_info();
+    else if (pl.family == rad::kFamSplitBf)
+        pl.tile = rad::split_bf16_tc05_info();
     else
         pl.tile = tile_for(head_dim, kv_dtype, pl.family);
     pl.n_qtiles = (pl.M + pl.tile.QT - 1) / pl.tile.QT;
@@ -168,6 +175,7 @@ const char* family_name(int f) {
         case rad::kFamVerify: return "verify";
         case rad::kFamWide: return "wide";
         case rad::kFamPrefillTC: return "prefill_tc05";
+        case rad::kFamSplitBf: return "split_bf16_tc05";
         default: return "split_tc05";
     }
 }
@@ -443,6 +451,18 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
             return RAD_E_CUDA;
         e = pl.family == rad::kFamSplitTC ? rad::launch_split_tc05(tk, tv, p, sms, st)
                                           : rad::launch_prefill_fp8(tk, tv, p, sms, st);
+    } else if (pl.family == rad::kFamSplitBf) {
+        rc = get_encoder();
+        if (rc != RAD_OK) return rc;
+        // pools viewed as [tokens][n_head_kv][head_dim]: one box = one page of one KV head x 64 columns
+        const cuuint64_t kd[3] = {(cuuint64_t)head_dim, (cuuint64_t)n_head_kv,
+                                  (cuuint64_t)num_pages * (cuuint64_t)page_size};
+        const cuuint64_t ks[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)n_head_kv * head_dim * 2};
+        const cuuint32_t kb[3] = {64, 1, (cuuint32_t)page_size};
+        CUtensorMap tk, tv;
+        if (encode_bf16_map(&tk, k_pool, 3, kd, ks, kb) != RAD_OK || encode_bf16_map(&tv, v_pool, 3, kd, ks, kb) != RAD_OK)
+            return RAD_E_CUDA;
+        e = rad::launch_split_bf16_tc05(tk, tv, p, sms, st);
     } else if (pl.family == rad::kFamPrefillTC) {
         rc = get_encoder();
         if (rc != RAD_OK) return rc;
@@ -483,13 +503,23 @@ int describe_call(int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_
     const char* pre = ragged ? "ragged_tile_map + " : "";
     if (pl.family == rad::kFamSplitTC) {
         snprintf(buf, buf_len,
-                 "attn_split_tc05 family=%s head_dim=%d kv=fp8e4m3 query_rows_per_kv_head=%d tile_rows=%d "
+                 "%sattn_split_tc05 family=%s head_dim=%d kv=fp8e4m3 query_rows_per_kv_head=%d tile_rows=%d "
                  "keys_per_tile=%d stages=%d ctas_per_sm=1 warps=12 4 softmax (a quarter of each tile's keys "
                  "each)+1 qk+1 pv+2 tma producers+4 v converters mma=tcgen05 (query rows as M, four copies; keys "
                  "as N; QK kind::f8f6f4 on the staged e4m3 K with Q as two e4m3 terms, PV kind::f16 with P from "
                  "TMEM and V e4m3 -> f16 once per tile) "
                  "split_len=%d + attn_combine (split order)",
-                 family_name(pl.family), head_dim, pl.M, t.QT, t.KS, t.NS, pl.split_len);
+                 pre, family_name(pl.family), head_dim, pl.M, t.QT, t.KS, t.NS, pl.split_len);
+        return RAD_OK;
+    }
+    if (pl.family == rad::kFamSplitBf) {
+        snprintf(buf, buf_len,
+                 "%sattn_split_bf16_tc05 family=%s head_dim=%d kv=bf16 query_rows_per_kv_head=%d tile_rows=%d "
+                 "keys_per_tile=%d stages=%d ctas_per_sm=1 warps=9 4 softmax (a quarter of each tile's keys "
+                 "each)+1 qk+1 pv+2 tma producers+1 query rows mma=tcgen05 (query rows as M, four copies; keys as "
+                 "N; QK kind::f16 bf16, PV kind::f16 with P from TMEM as bf16 hi+lo over S) "
+                 "split_len=%d + attn_combine (split order)",
+                 pre, family_name(pl.family), head_dim, pl.M, t.QT, t.KS, t.NS, pl.split_len);
         return RAD_OK;
     }
     if (pl.family == rad::kFamPrefillTC && kv_dtype == RAD_KV_FP8_E4M3) {

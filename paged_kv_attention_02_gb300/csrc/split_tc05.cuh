@@ -500,11 +500,12 @@ __global__ void __launch_bounds__(SplitTcCfg::NTHREADS, 1)
             const long long orow = (it.qrow0 + tok) * p.n_head + it.kvh * p.ratio + hl;   // q/out row
             const long long slot_idx = it.gq * p.max_splits + it.s;
             if (!it.seq_ok) {
-                // an invalid sequence length: the group's rows are zeros
+                // an invalid sequence length: the group's rows are zeros (malformed
+                // offsets name no rows: only the error bit)
                 if (w == 0 && valid)
                     for (int i = 0; i < C::D / 8; ++i)
                         reinterpret_cast<uint4*>(p.out + orow * C::D)[i] = make_uint4(0u, 0u, 0u, 0u);
-                if (t == 0 && p.err_word) atomicOr(p.err_word, kErrSeqLen);
+                if (t == 0 && p.err_word) atomicOr(p.err_word, it.cu_ok ? kErrSeqLen : kErrCuSeq);
                 continue;
             }
             if (it.n_stages == 0) {
@@ -539,11 +540,11 @@ __global__ void __launch_bounds__(SplitTcCfg::NTHREADS, 1)
             // no later row's
             uint32_t tmw = 0;
             if (TREE) {
-                if (t < p.rows) {
-                    const uint32_t wd = __ldg(p.tree_mask + (long long)it.g * p.rows + t);
+                if (t < it.qlen) {
+                    const uint32_t wd = __ldg(p.tree_mask + it.qrow0 + t);
                     if ((wd >> t) != 1u) bad |= kErrMask;
                 }
-                tmw = valid ? __ldg(p.tree_mask + (long long)it.g * p.rows + tok) : 0u;
+                tmw = valid ? __ldg(p.tree_mask + it.qrow0 + tok) : 0u;
             }
             // the rows' 2^-k, from the converters' split of this item's query rows
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar_q8_full, ic & 1u, kWaitLimitNs))) abort = true;

@@ -6,13 +6,19 @@
 
 namespace rad {
 
-enum Family : int { kFamDecode = 0, kFamVerify = 1, kFamWide = 2, kFamPrefillTC = 3, kFamSplitTC = 4 };
+enum Family : int { kFamDecode = 0, kFamVerify = 1, kFamWide = 2, kFamPrefillTC = 3, kFamSplitTC = 4, kFamSplitBf = 5 };
 
 // Split calls (decode and verify shapes) with head_dim 128 and fp8 pools run
 // on the tcgen05 split kernel (split_tc05.cuh); 0 keeps them on the mma.sync
 // tile kernel.
 #ifndef RAD_SPLIT_TC05
 #define RAD_SPLIT_TC05 1
+#endif
+// Split calls (decode and verify shapes) with head_dim 128 and bf16 pools run
+// on the bf16 tcgen05 split kernel (split_bf16_tc05.cuh); 0 keeps them on the
+// mma.sync tile kernel.
+#ifndef RAD_SPLIT_BF16_TC05
+#define RAD_SPLIT_BF16_TC05 0
 #endif
 
 // Keys per split for calls of up to kSplitMaxRows rows; longer calls (prefill
@@ -149,6 +155,9 @@ cudaError_t launch_prefill_fp8(const CUtensorMap& tk, const CUtensorMap& tv, con
 cudaError_t launch_split_tc05(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
                               cudaStream_t st);
 TileInfo split_tc05_info();
+cudaError_t launch_split_bf16_tc05(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
+                                   cudaStream_t st);
+TileInfo split_bf16_tc05_info();
 // Ragged calls: the tile maps (one CTA), before the tile kernels.  map[1]
 // null: one class; else sequences with at most split_m query rows per KV head
 // go to map[0] (tiles of qt[0] rows), the rest to map[1].

@@ -179,7 +179,7 @@ def test_ragged_rows_are_bit_identical_alone_and_batched(wls, name):
         assert np.array_equal(alone, got[cu[g]:cu[g] + ql]), f"{name}: group {g}"
 
 
-@pytest.mark.parametrize("name", ["d128_bf16", "d128_bf16_dec", "d256_bf16", "d256_fp8"])
+@pytest.mark.parametrize("name", ["d128_bf16", "d128_bf16_dec", "d128_fp8", "d256_bf16", "d256_fp8"])
 def test_ragged_rows_equal_the_uniform_call_bit_for_bit(wls, name):
     """Each group's rows equal a uniform call over that sequence with rows =
     its own count (both on the tile kernels, whose per-row arithmetic and key

@@ -93,9 +93,23 @@ def test_workspace_sizes():
     assert b.workspace_bytes(4, 1, 8, 2, 96, 16, 19) == 0
 
 
+def bf16_tc() -> bool:
+    """Whether the library was built with the bf16 tcgen05 split kernel (a compile-time switch)."""
+    return "split_bf16_tc05" in b.describe(8, 32, 8, 128, 16)
+
+
 def test_describe_names_the_kernel_choice():
-    assert "family=decode" in b.describe(1, 32, 8, 128, 16)
-    assert "family=verify" in b.describe(8, 32, 8, 128, 16)
+    # bf16 pools with head_dim 128: decode and verify shapes share one family, the
+    # bf16 tcgen05 split kernel when it is built in, else the tile kernel's decode
+    # (<= 8 query rows per KV head) and verify tiles
+    if bf16_tc():
+        assert "family=split_bf16_tc05" in b.describe(1, 32, 8, 128, 16)
+        assert "family=split_bf16_tc05" in b.describe(8, 32, 8, 128, 16)
+    else:
+        assert "family=decode" in b.describe(1, 32, 8, 128, 16)
+        assert "family=verify" in b.describe(8, 32, 8, 128, 16)
+    assert "family=decode" in b.describe(1, 32, 8, 256, 16)
+    assert "family=verify" in b.describe(8, 32, 8, 256, 16)
     assert "family=verify" in b.describe(8, 16, 2, 256, 32, b.RAD_KV_FP8_E4M3)
     # fp8 pools with head_dim 128: decode and verify shapes share the tcgen05 split kernel
     assert "family=split_tc05" in b.describe(8, 32, 8, 128, 16, b.RAD_KV_FP8_E4M3)
@@ -174,15 +188,19 @@ def test_ex_workspace_follows_the_kernel_the_call_takes():
     for hd, dt in ((128, b.RAD_KV_BF16), (256, b.RAD_KV_FP8_E4M3), (128, b.RAD_KV_FP8_E4M3)):
         a = _general_args(head_dim=hd, kv_dtype=dt)
         assert ws(a) == b.workspace_bytes(4, 8, 32, 8, hd, 16, 64, dt) > 0
-    # fp8 head_dim 128 verify: uniform and tree calls run the tcgen05 split
-    # kernel; a ragged call runs the verify tile plus, for its decode-shaped
-    # sequences, the decode tile: two tile maps (256 bytes each here) and two
-    # sets of partials
-    assert ws(_general_args(tree=fake, kv_dtype=b.RAD_KV_FP8_E4M3)) == \
-        b.workspace_bytes(4, 8, 32, 8, 128, 16, 64, b.RAD_KV_FP8_E4M3)
-    verify_part = ws(_general_args(tree=fake, kv_dtype=b.RAD_KV_BF16))
-    decode_part = b.workspace_bytes(4, 2, 32, 8, 128, 16, 64)   # the decode tile's partials: 8-row slots
-    assert ws(_general_args(cu=fake, kv_dtype=b.RAD_KV_FP8_E4M3)) == verify_part + decode_part + 2 * 256
+    # head_dim 128: uniform, tree and ragged calls run the tcgen05 split kernels;
+    # a ragged call adds its tile map (256 bytes here)
+    for dt in (b.RAD_KV_BF16, b.RAD_KV_FP8_E4M3) if bf16_tc() else (b.RAD_KV_FP8_E4M3,):
+        uniform = b.workspace_bytes(4, 8, 32, 8, 128, 16, 64, dt)
+        assert ws(_general_args(tree=fake, kv_dtype=dt)) == uniform
+        assert ws(_general_args(cu=fake, kv_dtype=dt)) == uniform + 256
+    # head_dim 256: a ragged call runs the verify tile plus, for its
+    # decode-shaped sequences, the decode tile: two tile maps and two sets of
+    # partials
+    fp8 = b.RAD_KV_FP8_E4M3
+    verify_part = ws(_general_args(tree=fake, head_dim=256, kv_dtype=fp8))
+    decode_part = b.workspace_bytes(4, 2, 32, 8, 256, 16, 64, fp8)   # the decode tile's partials: 8-row slots
+    assert ws(_general_args(cu=fake, head_dim=256, kv_dtype=fp8)) == verify_part + decode_part + 2 * 256
     # the caller's row total bounds the tiles: 4 sequences of up to 256 rows
     # (ratio 4, 32-row tiles: 32 tiles each) holding 40 rows in all need at
     # most ceil(160 / 32) + 4 = 9 tiles instead of 128
@@ -208,15 +226,23 @@ def test_ex_describe_names_the_kernels_of_ragged_and_tree_calls():
     assert "family=split_tc05" in b.ex_describe(shape())
     assert "family=split_tc05" in b.ex_describe(shape(tree=True))
     tree = b.ex_describe(b.shape_args(64, 8, 32, 8, 128, 16, 1024, tree=True))
-    assert tree.startswith("attn_tile family=verify") and "attn_combine" in tree
+    assert tree.startswith("attn_split_bf16_tc05 family=split_bf16_tc05" if bf16_tc() else "attn_tile family=verify")
+    assert "attn_combine" in tree
+    tree256 = b.ex_describe(b.shape_args(64, 8, 32, 8, 256, 16, 1024, tree=True))
+    assert tree256.startswith("attn_tile family=verify") and "attn_combine" in tree256
     rag = b.ex_describe(shape(ragged=True))
-    assert rag.startswith("ragged_tile_map + attn_tile family=decode")
-    assert " + attn_tile family=verify" in rag and rag.count("attn_combine") == 2
+    assert rag.startswith("ragged_tile_map + attn_split_tc05 family=split_tc05") and rag.count("attn_combine") == 1
+    rag256 = b.ex_describe(b.shape_args(64, 8, 32, 8, 256, 16, 1024, b.RAD_KV_FP8_E4M3, ragged=True))
+    assert rag256.startswith("ragged_tile_map + attn_tile family=decode")
+    assert " + attn_tile family=verify" in rag256 and rag256.count("attn_combine") == 2
     chunk = b.ex_describe(b.shape_args(4, 300, 32, 8, 128, 16, 64, ragged=True))
     assert chunk.startswith("ragged_tile_map + attn_tile family=decode") and " + attn_tile family=wide" in chunk
     assert "attn_combine" not in chunk
     dec = b.ex_describe(b.shape_args(4, 2, 32, 8, 128, 16, 64, ragged=True))
-    assert dec.startswith("ragged_tile_map + attn_tile family=decode") and dec.count("attn_tile") == 1
+    assert dec.startswith("ragged_tile_map + attn_split_bf16_tc05 family=split_bf16_tc05" if bf16_tc()
+                          else "ragged_tile_map + attn_tile family=decode")
+    dec256 = b.ex_describe(b.shape_args(4, 2, 32, 8, 256, 16, 64, ragged=True))
+    assert dec256.startswith("ragged_tile_map + attn_tile family=decode") and dec256.count("attn_tile") == 1
     assert b.describe(300, 32, 8, 128, 16).startswith("attn_prefill_tc05")
 
 
