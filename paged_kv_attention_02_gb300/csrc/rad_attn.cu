@@ -515,8 +515,8 @@ int describe_call(int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_
     if (pl.family == rad::kFamSplitBf) {
         snprintf(buf, buf_len,
                  "%sattn_split_bf16_tc05 family=%s head_dim=%d kv=bf16 query_rows_per_kv_head=%d tile_rows=%d "
-                 "keys_per_tile=%d stages=%d ctas_per_sm=1 warps=9 4 softmax (a quarter of each tile's keys "
-                 "each)+1 qk+1 pv+2 tma producers+1 query rows mma=tcgen05 (query rows as M, four copies; keys as "
+                 "keys_per_tile=%d stages=%d ctas_per_sm=1 warps=13 4 softmax (a quarter of each tile's keys "
+                 "each)+1 qk+1 pv+2 tma producers+1 query rows+4 epilogue (two O buffers) mma=tcgen05 (query rows as M, four copies; keys as "
                  "N; QK kind::f16 bf16, PV kind::f16 with P from TMEM as bf16 hi+lo over S) "
                  "split_len=%d + attn_combine (split order)",
                  pre, family_name(pl.family), head_dim, pl.M, t.QT, t.KS, t.NS, pl.split_len);

@@ -16,25 +16,37 @@
 //                MN-major operand
 // P is written over S in TMEM (S buffer b's 128 columns hold P_hi in the
 // first 64 and P_lo in the last 64; in lane 32w + r only keys 32w .. 32w+31
-// are non-zero), so TMEM holds O and two S/P buffers.
+// are non-zero), so TMEM holds two O buffers (by item parity) and two S/P
+// buffers (by tile parity).
 //
 // Warp roles (one CTA per SM, persistent):
-//   warps 0-3  softmax (quarter w, thread = query row r)
-//   warp 4     QK: once K_j landed and PV_{j-2} is done (S/P buffer j & 1
-//              free), lane 0 issues QK_j.
-//   warp 5     PV: once P_j is written and V_j landed, lane 0 issues PV_j;
-//              its commit also frees the V stage.  On a tile that straddles
-//              the item's key range it first zeroes the V rows outside it.
-//   warps 6, 7 K and V producers: page ids, one TMA box per page and 64-column
-//              block (page_size rows x 128 bytes of the KV head), issued by
-//              lanes 0 .. 2 * pages - 1; pages outside the item's range load
-//              zeros.
-//   warp 8     query rows: the item's rows, four copies, in the 128-byte
-//              swizzled K-major layout, once the previous item's QKs are done.
+//   warps 0-3   softmax (quarter w, thread = query row r); at an item's end
+//               they hand its (max, sum) per quarter and its error bits to the
+//               epilogue warps and go on with the next item.
+//   warp 4      QK: once K_j landed and PV_{j-2} is done (S/P buffer j & 1
+//               free), lane 0 issues QK_j.
+//   warp 5      PV: once P_j is written and V_j landed, lane 0 issues PV_j into
+//               the item's O buffer (at an item's first tile, once the epilogue
+//               has read that buffer out); its commit also frees the V stage.
+//               On a tile that straddles the item's key range it first zeroes
+//               the V rows outside it.
+//   warps 6, 7  K and V producers: page ids, one TMA box per page and 64-column
+//               block (page_size rows x 128 bytes of the KV head), issued by
+//               lanes 0 .. 2 * pages - 1; pages outside the item's range load
+//               zeros.
+//   warp 8      query rows: the item's rows, four copies, in the 128-byte
+//               swizzled K-major layout, once the previous item's QKs are done.
+//   warps 9-12  epilogue: warp 9 + i reads TMEM lane quarter (9 + i) & 3 of
+//               the item's O buffer, and the four merge the quarters of each row
+//               in warp order (a 16 KB scratch), then store the row or the
+//               split's partial; an item's merge overlaps the next item's tiles.
 // PV of tile t completes a phase of pv_done[t & 1]; a thread that has seen
 // S(t) knows PV(t-2) is done (QK(t) waited for it), so no wait on pv_done is
-// two phases ahead of its barrier.  Every wait is bounded; a time-out sets
-// RAD_ERRW_TIMEOUT and the roles unwind.
+// two phases ahead of its barrier.  The O buffers' barriers (o_full, ml_full,
+// o_free) complete once per item of that parity, and each role waits on them
+// in order, the softmax for the epilogue two items back before it reuses that
+// hand-off slot.  Every wait is bounded; a time-out sets RAD_ERRW_TIMEOUT and
+// the roles unwind.
 #pragma once
 #include <cuda.h>
 
@@ -67,18 +79,19 @@ struct SplitBf16Cfg {
     static constexpr int OFF_K = OFF_Q + 2 * Q_BLK;
     static constexpr int OFF_V = OFF_K + NSK * KV_TILE;
     static constexpr int OFF_SCR = OFF_V + NSV * KV_TILE;
-    static constexpr int OFF_ML = OFF_SCR + SCR_BYTES;      // [2][4][32]: the quarters' row max, sum
-    static constexpr int OFF_META = OFF_ML + 2 * 4 * 32 * 4;
+    static constexpr int OFF_ML = OFF_SCR + SCR_BYTES;      // [O buffer][max, sum][quarter][32 rows]
+    static constexpr int OFF_FLAGS = OFF_ML + 2 * 2 * 4 * 32 * 4;   // [O buffer]: the item's error bits
+    static constexpr int OFF_META = OFF_FLAGS + 16;
     static constexpr int OFF_BARS = OFF_META + NSK * META_STRIDE;
     // q_full, q_empty, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[2], p_full[2],
-    // pv_done[2], o_free, final[2]
-    static constexpr int NBARS = 2 + 2 * NSK + 2 * NSV + 2 + 2 + 2 + 1 + 2;
+    // pv_done[2], o_full[2], ml_full[2], o_free[2], final[2]
+    static constexpr int NBARS = 2 + 2 * NSK + 2 * NSV + 2 + 2 + 2 + 2 + 2 + 2 + 2;
     static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // 1 KB alignment of the swizzled tiles
-    static constexpr int NTHREADS = 9 * 32;
-    static constexpr int W_QK = 4, W_PV = 5, W_PROD_K = 6, W_PROD_V = 7, W_Q = 8;
+    static constexpr int NTHREADS = 13 * 32;
+    static constexpr int W_QK = 4, W_PV = 5, W_PROD_K = 6, W_PROD_V = 7, W_Q = 8, W_EPI = 9;
     static constexpr int K_EMPTY_ARRIVALS = 1 + 4;            // the QK commit + the softmax warps' flag reads
-    static constexpr uint32_t TMEM_COLS = 512;   // O [0,128), S/P_b [128 + 128b, ...)
+    static constexpr uint32_t TMEM_COLS = 512;   // O_b [128b, ...), S/P_b [256 + 128b, ...)
     static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && KV_TILE % 1024 == 0, "1 KB tiles");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -106,8 +119,10 @@ __global__ void __launch_bounds__(SplitBf16Cfg::NTHREADS, 1)
     const uint32_t bar_s_full = bar_v_empty + 8 * C::NSV;   // [2]
     const uint32_t bar_p_full = bar_s_full + 16;            // [2]
     const uint32_t bar_pv_done = bar_p_full + 16;           // [2], by tile parity
-    const uint32_t bar_o_free = bar_pv_done + 16;
-    const uint32_t bar_final = bar_o_free + 8;              // [2]: QK warp, PV warp
+    const uint32_t bar_o_full = bar_pv_done + 16;           // [2], by O buffer: the item's last PV done
+    const uint32_t bar_ml_full = bar_o_full + 16;           // [2], by O buffer: the softmax's hand-off
+    const uint32_t bar_o_free = bar_ml_full + 16;           // [2], by O buffer: read out by the epilogue
+    const uint32_t bar_final = bar_o_free + 16;             // [2]: QK warp, PV warp
     volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);  // [0] tmem, [1] abort
 
     const int warp = threadIdx.x >> 5;
@@ -129,7 +144,13 @@ __global__ void __launch_bounds__(SplitBf16Cfg::NTHREADS, 1)
             mbar_init(bar_p_full + 8 * i, 4);
             mbar_init(bar_pv_done + 8 * i, 1);
         }
-        mbar_init(bar_o_free, 4);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_o_full + 8 * i, 1);
+            mbar_init(bar_ml_full + 8 * i, 4);
+            mbar_init(bar_o_free + 8 * i, 4);
+        }
+        reinterpret_cast<uint32_t*>(smem + C::OFF_FLAGS)[0] = 0u;
+        reinterpret_cast<uint32_t*>(smem + C::OFF_FLAGS)[1] = 0u;
         mbar_init(bar_final, 1);
         mbar_init(bar_final + 8, 1);
         misc[1] = 0;
@@ -143,8 +164,8 @@ __global__ void __launch_bounds__(SplitBf16Cfg::NTHREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
-    const uint32_t t_o = tmem;
-    const uint32_t t_s = tmem + 128;   // S/P buffer b at t_s + 128 b
+    const uint32_t t_o = tmem;         // O buffer b (by item parity) at t_o + 128 b
+    const uint32_t t_s = tmem + 256;   // S/P buffer b (by tile parity) at t_s + 128 b
     bool abort = false;
 
     // items that run the pipeline: active, a valid sequence length, keys to see
@@ -321,10 +342,13 @@ __global__ void __launch_bounds__(SplitBf16Cfg::NTHREADS, 1)
             const int T = it.n_stages;
             for (int j = 0; j < T; ++j) {
                 const uint32_t tcj = tc + j, b = tcj & 1u, sv = tcj % C::NSV;
-                // P_j written, V_j landed, and at an item's first tile the previous item's O read out
+                // P_j written, V_j landed, and at an item's first tile its O buffer read out
+                // (the item two before)
+                const uint32_t t_ob = t_o + 128 * (ic & 1u);
                 bool ok = mbar_wait_bounded(bar_p_full + 8 * b, (tcj >> 1) & 1u, kWaitLimitNs);
                 if (ok) ok = mbar_wait_bounded(bar_v_full + 8 * sv, (tcj / C::NSV) & 1u, kWaitLimitNs);
-                if (ok && j == 0 && ic >= 1) ok = mbar_wait_bounded(bar_o_free, (ic - 1) & 1u, kWaitLimitNs);
+                if (ok && j == 0 && ic >= 2)
+                    ok = mbar_wait_bounded(bar_o_free + 8 * (ic & 1u), ((ic - 2) >> 1) & 1u, kWaitLimitNs);
                 if (!__all_sync(0xffffffffu, ok)) {
                     abort = true;
                     break;
@@ -351,11 +375,12 @@ __global__ void __launch_bounds__(SplitBf16Cfg::NTHREADS, 1)
 #pragma unroll
                     for (int kk = 0; kk < C::BK / 16; ++kk) {
                         const uint64_t bd = umma_desc_sw128(vb + kk * 16 * 128, C::BLK, 1024);
-                        tc_mma_ts(t_o, tp + kk * 8, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);   // P_hi
-                        tc_mma_ts(t_o, tp + 64 + kk * 8, bd, idesc_pv, 1u);                      // P_lo
+                        tc_mma_ts(t_ob, tp + kk * 8, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);   // P_hi
+                        tc_mma_ts(t_ob, tp + 64 + kk * 8, bd, idesc_pv, 1u);                      // P_lo
                     }
                     tc_commit(bar_pv_done + 8 * b);
                     tc_commit(bar_v_empty + 8 * sv);
+                    if (j == T - 1) tc_commit(bar_o_full + 8 * (ic & 1u));
                     issued = true;
                 }
                 __syncwarp();
@@ -369,6 +394,121 @@ __global__ void __launch_bounds__(SplitBf16Cfg::NTHREADS, 1)
             mbar_wait_bounded(bar_final + 8, 0, kWaitLimitNs);
         }
         __syncwarp();
+    } else if (warp >= C::W_EPI) {
+        // ===================================================== epilogue (warps 9-12)
+        // Warp 9 + i reads TMEM lane quarter w = (9 + i) & 3: the O of softmax warp w.
+        const int w = warp & 3;
+        const int r = lane;                                     // query row r of the item
+        const uint32_t lane_off = (uint32_t)(w * 32) << 16;
+        const int t = threadIdx.x - C::W_EPI * 32;              // 0 .. 127
+        float* const ml = reinterpret_cast<float*>(smem + C::OFF_ML);
+        uint32_t* const flags = reinterpret_cast<uint32_t*>(smem + C::OFF_FLAGS);
+        uint8_t* const scr = smem + C::OFF_SCR;
+        uint32_t ic = 0;
+        for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
+            const ItemPlan it = plan_item<C, WIN>(item, p);
+            if (!real(it)) continue;
+            // the item's last PV done and the softmax warps' hand-off
+            const uint32_t ob = ic & 1u;
+            bool ok = mbar_wait_bounded(bar_o_full + 8 * ob, (ic >> 1) & 1u, kWaitLimitNs);
+            if (ok) ok = mbar_wait_bounded(bar_ml_full + 8 * ob, (ic >> 1) & 1u, kWaitLimitNs);
+            if (named_barrier_or(2, 128, !__all_sync(0xffffffffu, ok) || misc[1] != 0)) {   // all leave together
+                abort = true;
+                break;
+            }
+            tc_fence_after();
+            const float* const mlb = ml + ob * 256;
+            const int nrows = it.m_end - it.m0;
+            const int m = it.m0 + r;
+            const bool valid = r < nrows;
+            const int tok = m / p.ratio, hl = m - tok * p.ratio;
+            const long long orow = (it.qrow0 + tok) * p.n_head + it.kvh * p.ratio + hl;   // q/out row
+            const long long slot_idx = it.gq * p.max_splits + it.s;
+            // ---- the four quarters' (max, sum, O) of row r, merged in warp order
+            const uint32_t item_bits = flags[ob];
+            const bool page_bad = (item_bits & kErrPage) != 0;
+            const bool mask_bad = TREE && (item_bits & kErrMask) != 0;
+            const bool item_bad = page_bad || mask_bad;
+            const uint32_t bad_bits = (page_bad ? kErrPage : 0u) | (mask_bad ? kErrMask : 0u);
+            float mq[4], M = -CUDART_INF_F;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                mq[q] = mlb[q * 32 + r];
+                M = fmaxf(M, mq[q]);
+            }
+            const float mu = (M == -CUDART_INF_F) ? 0.f : M;
+            float L = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) L += exp2f(mq[q] - mu) * mlb[128 + q * 32 + r];
+            const float f_me = exp2f(mq[w] - mu);
+            const bool final_write = it.n_splits - it.s_first == 1;
+            const float inv = L == 0.f ? 0.f : 1.f / L;
+            float* pacc = p.part_acc + slot_idx * p.qtv * C::D;
+            for (int c = 0; c < 4; ++c) {
+                // quarter w's scaled O of row r, columns 32c .. 32c+31, 16-byte chunks
+                // swizzled by the row
+                uint32_t ov[32];
+                tmem_ld32(t_o + 128 * ob + lane_off + 32 * c, ov);
+                float4* mine = reinterpret_cast<float4*>(scr + (w * 32 + r) * 128);
+#pragma unroll
+                for (int e4 = 0; e4 < 8; ++e4)
+                    mine[e4 ^ (r & 7)] = make_float4(__uint_as_float(ov[4 * e4]) * f_me, __uint_as_float(ov[4 * e4 + 1]) * f_me,
+                                                     __uint_as_float(ov[4 * e4 + 2]) * f_me,
+                                                     __uint_as_float(ov[4 * e4 + 3]) * f_me);
+                if (c == 3) {
+                    // O is read out: the next item's first PV may overwrite it
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_o_free + 8 * ob);
+                }
+                named_barrier_sync(2, 128);
+                if (c == 0 && t == 0) flags[ob] = 0u;   // read by all: reset for the item two on
+                // row r, columns 32c + 8w .. 32c + 8w + 7: the four quarters summed in order
+                float a[8];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float4 s4 = reinterpret_cast<const float4*>(scr + r * 128)[(2 * w + h) ^ (r & 7)];
+#pragma unroll
+                    for (int q = 1; q < 4; ++q) {
+                        const float4 v4 = reinterpret_cast<const float4*>(scr + (q * 32 + r) * 128)[(2 * w + h) ^ (r & 7)];
+                        s4.x += v4.x;
+                        s4.y += v4.y;
+                        s4.z += v4.z;
+                        s4.w += v4.w;
+                    }
+                    a[4 * h] = s4.x;
+                    a[4 * h + 1] = s4.y;
+                    a[4 * h + 2] = s4.z;
+                    a[4 * h + 3] = s4.w;
+                }
+                const int d0 = 32 * c + 8 * w;
+                if (valid) {
+                    if (final_write) {
+                        // acc * (1/l), the combine kernel's form; a bad item's rows are zeros
+                        uint4 o = make_uint4(0u, 0u, 0u, 0u);
+                        if (!item_bad) {
+                            o.x = pack_bf16x2(a[0] * inv, a[1] * inv);
+                            o.y = pack_bf16x2(a[2] * inv, a[3] * inv);
+                            o.z = pack_bf16x2(a[4] * inv, a[5] * inv);
+                            o.w = pack_bf16x2(a[6] * inv, a[7] * inv);
+                        }
+                        *reinterpret_cast<uint4*>(p.out + orow * C::D + d0) = o;
+                    } else {
+                        __stcg(reinterpret_cast<float4*>(pacc + r * C::D + d0), make_float4(a[0], a[1], a[2], a[3]));
+                        __stcg(reinterpret_cast<float4*>(pacc + r * C::D + d0) + 1, make_float4(a[4], a[5], a[6], a[7]));
+                    }
+                }
+                named_barrier_sync(2, 128);   // the scratch is free for the next chunk
+            }
+            if (final_write) {
+                if (item_bad && t == 0 && p.err_word) atomicOr(p.err_word, bad_bits);
+            } else {
+                float* pml = p.part_ml + slot_idx * p.qtv * 2;
+                if (w == 0 && valid) __stcg(reinterpret_cast<float2*>(pml) + r, make_float2(L == 0.f ? -CUDART_INF_F : M, L));
+                if (t == 0) __stcg(p.part_flag + slot_idx, bad_bits);
+            }
+            ++ic;
+        }
     } else {
         // ===================================================== softmax (warps 0-3)
         const int w = warp;                                     // quarter: keys 32w .. 32w+31 of a tile
@@ -376,7 +516,7 @@ __global__ void __launch_bounds__(SplitBf16Cfg::NTHREADS, 1)
         const uint32_t lane_off = (uint32_t)(w * 32) << 16;     // this warp's TMEM lanes
         const int t = threadIdx.x;                              // 0 .. 127
         float* const ml = reinterpret_cast<float*>(smem + C::OFF_ML);
-        uint8_t* const scr = smem + C::OFF_SCR;
+        uint32_t* const flags = reinterpret_cast<uint32_t*>(smem + C::OFF_FLAGS);
         uint32_t tc = 0, ic = 0;
         for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
             const ItemPlan it = plan_item<C, WIN>(item, p);
@@ -507,10 +647,10 @@ __global__ void __launch_bounds__(SplitBf16Cfg::NTHREADS, 1)
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         uint32_t ov[32];
-                        tmem_ld32(t_o + lane_off + 32 * q, ov);
+                        tmem_ld32(t_o + 128 * (ic & 1u) + lane_off + 32 * q, ov);
 #pragma unroll
                         for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                        tmem_st32(t_o + lane_off + 32 * q, ov);
+                        tmem_st32(t_o + 128 * (ic & 1u) + lane_off + 32 * q, ov);
                     }
                     tmem_wait_st();
                     if (need) {
@@ -559,101 +699,22 @@ __global__ void __launch_bounds__(SplitBf16Cfg::NTHREADS, 1)
                     break;
                 }
             }
-            if (named_barrier_or(1, 128, abort)) {
+            if (abort) break;
+            // ---- hand-off: this quarter's (max, sum) of row r and the item's error bits
+            // go to the epilogue warps, once they have read out the item two before (its
+            // slot and O buffer are this item's)
+            const uint32_t ob = ic & 1u;
+            if (ic >= 2 &&
+                !__all_sync(0xffffffffu, mbar_wait_bounded(bar_o_free + 8 * ob, ((ic - 2) >> 1) & 1u, kWaitLimitNs))) {
                 abort = true;
                 break;
             }
-            // ---- epilogue: the four quarters' (max, sum, O) of row r, merged in warp order
-            const uint32_t tcl = tc + T - 1;
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar_pv_done + 8 * (tcl & 1u), (tcl >> 1) & 1u, kWaitLimitNs)))
-                abort = true;
-            tc_fence_after();
-            if (named_barrier_or(1, 128, abort)) {   // all four warps leave together
-                abort = true;
-                break;
-            }
-            ml[w * 32 + r] = m_run;
-            ml[128 + w * 32 + r] = l_run;
-            const bool page_bad = named_barrier_or(1, 128, (bad & kErrPage) != 0);
-            const bool mask_bad = TREE && named_barrier_or(1, 128, (bad & kErrMask) != 0);
-            const bool item_bad = page_bad || mask_bad;
-            const uint32_t bad_bits = (page_bad ? kErrPage : 0u) | (mask_bad ? kErrMask : 0u);
-            float mq[4], M = -CUDART_INF_F;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                mq[q] = ml[q * 32 + r];
-                M = fmaxf(M, mq[q]);
-            }
-            const float mu = (M == -CUDART_INF_F) ? 0.f : M;
-            float L = 0.f;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) L += exp2f(mq[q] - mu) * ml[128 + q * 32 + r];
-            const float f_me = exp2f(m_run - mu);
-            const bool final_write = it.n_splits - it.s_first == 1;
-            const float inv = L == 0.f ? 0.f : 1.f / L;
-            float* pacc = p.part_acc + slot_idx * p.qtv * C::D;
-            for (int c = 0; c < 4; ++c) {
-                // quarter w's scaled O of row r, columns 32c .. 32c+31, 16-byte chunks
-                // swizzled by the row
-                uint32_t ov[32];
-                tmem_ld32(t_o + lane_off + 32 * c, ov);
-                float4* mine = reinterpret_cast<float4*>(scr + (w * 32 + r) * 128);
-#pragma unroll
-                for (int e4 = 0; e4 < 8; ++e4)
-                    mine[e4 ^ (r & 7)] = make_float4(__uint_as_float(ov[4 * e4]) * f_me, __uint_as_float(ov[4 * e4 + 1]) * f_me,
-                                                     __uint_as_float(ov[4 * e4 + 2]) * f_me,
-                                                     __uint_as_float(ov[4 * e4 + 3]) * f_me);
-                if (c == 3) {
-                    // O is read out: the next item's first PV may overwrite it
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_o_free);
-                }
-                named_barrier_sync(1, 128);
-                // row r, columns 32c + 8w .. 32c + 8w + 7: the four quarters summed in order
-                float a[8];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float4 s4 = reinterpret_cast<const float4*>(scr + r * 128)[(2 * w + h) ^ (r & 7)];
-#pragma unroll
-                    for (int q = 1; q < 4; ++q) {
-                        const float4 v4 = reinterpret_cast<const float4*>(scr + (q * 32 + r) * 128)[(2 * w + h) ^ (r & 7)];
-                        s4.x += v4.x;
-                        s4.y += v4.y;
-                        s4.z += v4.z;
-                        s4.w += v4.w;
-                    }
-                    a[4 * h] = s4.x;
-                    a[4 * h + 1] = s4.y;
-                    a[4 * h + 2] = s4.z;
-                    a[4 * h + 3] = s4.w;
-                }
-                const int d0 = 32 * c + 8 * w;
-                if (valid) {
-                    if (final_write) {
-                        // acc * (1/l), the combine kernel's form; a bad item's rows are zeros
-                        uint4 o = make_uint4(0u, 0u, 0u, 0u);
-                        if (!item_bad) {
-                            o.x = pack_bf16x2(a[0] * inv, a[1] * inv);
-                            o.y = pack_bf16x2(a[2] * inv, a[3] * inv);
-                            o.z = pack_bf16x2(a[4] * inv, a[5] * inv);
-                            o.w = pack_bf16x2(a[6] * inv, a[7] * inv);
-                        }
-                        *reinterpret_cast<uint4*>(p.out + orow * C::D + d0) = o;
-                    } else {
-                        __stcg(reinterpret_cast<float4*>(pacc + r * C::D + d0), make_float4(a[0], a[1], a[2], a[3]));
-                        __stcg(reinterpret_cast<float4*>(pacc + r * C::D + d0) + 1, make_float4(a[4], a[5], a[6], a[7]));
-                    }
-                }
-                named_barrier_sync(1, 128);   // the scratch is free for the next chunk
-            }
-            if (final_write) {
-                if (item_bad && t == 0 && p.err_word) atomicOr(p.err_word, bad_bits);
-            } else {
-                float* pml = p.part_ml + slot_idx * p.qtv * 2;
-                if (w == 0 && valid) __stcg(reinterpret_cast<float2*>(pml) + r, make_float2(L == 0.f ? -CUDART_INF_F : M, L));
-                if (t == 0) __stcg(p.part_flag + slot_idx, bad_bits);
-            }
+            ml[ob * 256 + w * 32 + r] = m_run;
+            ml[ob * 256 + 128 + w * 32 + r] = l_run;
+            const uint32_t bad_w = __reduce_or_sync(0xffffffffu, bad);
+            if (lane == 0 && bad_w) atomicOr(flags + ob, bad_w);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_ml_full + 8 * ob);
             tc += T;
             ++ic;
         }

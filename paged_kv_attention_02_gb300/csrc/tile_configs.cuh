@@ -18,7 +18,7 @@ enum Family : int { kFamDecode = 0, kFamVerify = 1, kFamWide = 2, kFamPrefillTC 
 // on the bf16 tcgen05 split kernel (split_bf16_tc05.cuh); 0 keeps them on the
 // mma.sync tile kernel.
 #ifndef RAD_SPLIT_BF16_TC05
-#define RAD_SPLIT_BF16_TC05 0
+#define RAD_SPLIT_BF16_TC05 1
 #endif
 
 // Keys per split for calls of up to kSplitMaxRows rows; longer calls (prefill
