@@ -49,9 +49,9 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM traffic per launch from the committed ncu capture (profiles/), valid only
 # while the kernel sources hash to `src_sha256`.
 NCU_TRAFFIC: dict[str, dict] = {
-    # profiles/attn_tile_batched_decode_64seq.md: 64-sequence capture scaled by KV bytes
-    "batched_decode": {"bytes_per_launch": 4_499_400_000 + 20_100_000,
-                       "src_sha256": "001b2f1fdc8ca78ea7f2b85f2b1dc3eef7d2d82a999105deaa0ed95d1456bea6"},
+    # profiles/attn_split_bf16_tc05_batched_decode_64seq.md: 64-sequence capture scaled by KV bytes
+    "batched_decode": {"bytes_per_launch": 4_499_500_000 + 21_500_000,
+                       "src_sha256": "cb8fa407ecc50295466ff8c3d1d4b22428af00143ba30b59c5af6d87865fbbb1"},
 }
 
 
