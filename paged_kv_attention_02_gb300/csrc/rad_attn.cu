@@ -118,7 +118,7 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
     else if (pl.family == rad::kFamSplitTC)
         pl.tile = rad::split_tc05_info();
     else if (pl.family == rad::kFamSplitBf)
-        pl.tile = rad::split_bf16_tc05_info();
+        pl.tile = rad::split_bf16_tc05_info(pl.M <= 8);
     else
         pl.tile = tile_for(head_dim, kv_dtype, pl.family);
     pl.n_qtiles = (pl.M + pl.tile.QT - 1) / pl.tile.QT;
@@ -462,7 +462,7 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
         CUtensorMap tk, tv;
         if (encode_bf16_map(&tk, k_pool, 3, kd, ks, kb) != RAD_OK || encode_bf16_map(&tv, v_pool, 3, kd, ks, kb) != RAD_OK)
             return RAD_E_CUDA;
-        e = rad::launch_split_bf16_tc05(tk, tv, p, sms, st);
+        e = rad::launch_split_bf16_tc05(tk, tv, p, sms, st, pl.M <= 8);
     } else if (pl.family == rad::kFamPrefillTC) {
         rc = get_encoder();
         if (rc != RAD_OK) return rc;

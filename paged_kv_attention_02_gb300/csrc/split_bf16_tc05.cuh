@@ -59,24 +59,41 @@
 #ifndef RAD_SPLITBF_NSV
 #define RAD_SPLITBF_NSV 2
 #endif
+// Stages of the form for calls with at most 8 query rows per KV head, whose
+// query rows take 2 KB instead of 32 KB.
+#ifndef RAD_SPLITBF_FEW_NSK
+#define RAD_SPLITBF_FEW_NSK 3
+#endif
+#ifndef RAD_SPLITBF_FEW_NSV
+#define RAD_SPLITBF_FEW_NSV 3
+#endif
 
 namespace rad {
 
+// FEW: every item has at most 8 query rows (calls with at most 8 query rows
+// per KV head).  The query operand then holds those 8 rows once, and its
+// descriptor's 8-row group stride is 0, so all 16 groups of M = 128 read them:
+// lane 32w + r holds row r % 8, the item's row r for r < 8, and the rows
+// beyond are masked as before.  Nothing else changes, so a row's bits are
+// those of the other form.
+template <bool FEW>
 struct SplitBf16Cfg {
     static constexpr int D = 128;                   // head dim
     static constexpr int BK = 128;                  // keys per tile
     static constexpr int QT = 32;                   // (item planner) query rows per item
     static constexpr int KS = BK;                   // (item planner) keys per stage
-    static constexpr int NSK = RAD_SPLITBF_NSK;     // K stages (with the tile's page-id flag)
-    static constexpr int NSV = RAD_SPLITBF_NSV;     // V stages
+    static constexpr int NSK = FEW ? RAD_SPLITBF_FEW_NSK : RAD_SPLITBF_NSK;   // K stages (with the page-id flag)
+    static constexpr int NSV = FEW ? RAD_SPLITBF_FEW_NSV : RAD_SPLITBF_NSV;   // V stages
     static constexpr int BLK = BK * 128;            // one 64-column block of a K or V tile: [key][128 B]
     static constexpr int KV_TILE = 2 * BLK;
-    static constexpr int Q_BLK = 128 * 128;         // one 64-column block of the four copies of the rows
+    static constexpr int Q_ROWS = FEW ? 8 : 128;    // query operand rows held: 8, or four copies of 32
+    static constexpr int Q_BLK = Q_ROWS * 128;      // one 64-column block of them
+    static constexpr uint32_t Q_SBO = FEW ? 0u : 1024u;   // the A descriptor's 8-row group stride
     static constexpr int MAXPG = BK / 16;           // pages per tile
     static constexpr int META_STRIDE = 128;         // [16]: the tile's page-id flag
     static constexpr int SCR_BYTES = 4 * 32 * 128;  // the merge: [warp][row][32 floats], chunks swizzled
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + 2 * Q_BLK;
+    static constexpr int OFF_K = OFF_Q + 2 * Q_BLK;    // 1 KB-aligned: 2 KB or 32 KB
     static constexpr int OFF_V = OFF_K + NSK * KV_TILE;
     static constexpr int OFF_SCR = OFF_V + NSV * KV_TILE;
     static constexpr int OFF_ML = OFF_SCR + SCR_BYTES;      // [O buffer][max, sum][quarter][32 rows]
@@ -98,11 +115,11 @@ struct SplitBf16Cfg {
 
 // MODE: kModeCausal, kModeWindow or kModeTree (draft-tree rows, uniform row
 // counts: bit i of a row's mask word lets it see the call's key i).
-template <int MODE>
-__global__ void __launch_bounds__(SplitBf16Cfg::NTHREADS, 1)
+template <int MODE, bool FEW>
+__global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
     attn_split_bf16_tc05_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                                 const __grid_constant__ AttnParams p) {
-    using C = SplitBf16Cfg;
+    using C = SplitBf16Cfg<FEW>;
     constexpr bool WIN = MODE == kModeWindow;
     constexpr bool TREE = MODE == kModeTree;
     extern __shared__ uint8_t smem_raw[];
@@ -263,11 +280,13 @@ __global__ void __launch_bounds__(SplitBf16Cfg::NTHREADS, 1)
                 abort = true;
                 break;
             }
-            // copy c at rows 32c + r of the M = 128 operand; elements 8i .. 8i+7 in
-            // block i / 8, 16-byte chunk i % 8 (swizzled by the row)
+            // copy c at rows 32c + r of the M = 128 operand (FEW: rows 0-7 once);
+            // elements 8i .. 8i+7 in block i / 8, 16-byte chunk i % 8 (swizzled by
+            // the row)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < (FEW ? 1 : 4); ++c) {
                 const int qr = 32 * c + lane;
+                if (FEW && lane >= 8) break;
                 uint8_t* dst = smem + C::OFF_Q + qr * 128;
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
@@ -311,7 +330,7 @@ __global__ void __launch_bounds__(SplitBf16Cfg::NTHREADS, 1)
                         const uint32_t off = (uint32_t)((kk >> 2) * C::BLK + (kk & 3) * 32);
                         tc_mma_ss(t_s + 128 * b,
                                   umma_desc_sw128(base + C::OFF_Q + (uint32_t)((kk >> 2) * C::Q_BLK + (kk & 3) * 32), 16,
-                                                  1024),
+                                                  C::Q_SBO),
                                   umma_desc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
                     }
                     tc_commit(bar_s_full + 8 * b);

@@ -156,8 +156,8 @@ cudaError_t launch_split_tc05(const CUtensorMap& tk, const CUtensorMap& tv, cons
                               cudaStream_t st);
 TileInfo split_tc05_info();
 cudaError_t launch_split_bf16_tc05(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
-                                   cudaStream_t st);
-TileInfo split_bf16_tc05_info();
+                                   cudaStream_t st, bool few);
+TileInfo split_bf16_tc05_info(bool few);
 // Ragged calls: the tile maps (one CTA), before the tile kernels.  map[1]
 // null: one class; else sequences with at most split_m query rows per KV head
 // go to map[0] (tiles of qt[0] rows), the rest to map[1].
