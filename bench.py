@@ -50,8 +50,8 @@ FALLBACK_HBM_GBS = 6800.0
 # while the kernel sources hash to `src_sha256`.
 NCU_TRAFFIC: dict[str, dict] = {
     # profiles/attn_split_bf16_tc05_batched_decode_64seq.md: 64-sequence capture scaled by KV bytes
-    "batched_decode": {"bytes_per_launch": 4_499_500_000 + 21_500_000,
-                       "src_sha256": "cb8fa407ecc50295466ff8c3d1d4b22428af00143ba30b59c5af6d87865fbbb1"},
+    "batched_decode": {"bytes_per_launch": 4_499_500_000 + 20_200_000,
+                       "src_sha256": "539ccd95913fc2c62588decd569bd8d2e1fe0e48f5e8e9db841270f11aa8647a"},
 }
 
 
