@@ -242,9 +242,12 @@ int rad_attn_paged_window(const void* q, const void* k_pool, const void* v_pool,
  *                unwritten.  Negative: RAD_E_ARG.  A ragged call first runs a
  *                small kernel that maps its query tiles into the workspace.
  *
- * Calls with cu_seqlens or tree_mask run on the mma.sync tile kernels only;
- * their workspace need is rad_attn_paged_ex_workspace_bytes(args), which may
- * differ from rad_attn_paged_workspace_bytes() of the same shape.
+ * Calls with cu_seqlens or tree_mask run on the same kernel family as a
+ * uniform call of their shape when head_dim is 128 (the tcgen05 split kernels
+ * for calls of at most 256 rows), else on the mma.sync tile kernels, so their
+ * rows keep the uniform call's bits; their workspace need is
+ * rad_attn_paged_ex_workspace_bytes(args), which may differ from
+ * rad_attn_paged_workspace_bytes() of the same shape.
  * Returns the status rad_attn_paged_window returns for the same arguments,
  * RAD_E_ARG for a cu_seqlens or tree_mask pointer not 4-byte aligned.
  */
