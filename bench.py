@@ -51,7 +51,7 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC: dict[str, dict] = {
     # profiles/attn_split_bf16_tc05_batched_decode_64seq.md: 64-sequence capture scaled by KV bytes
     "batched_decode": {"bytes_per_launch": 4_499_500_000 + 20_200_000,
-                       "src_sha256": "539ccd95913fc2c62588decd569bd8d2e1fe0e48f5e8e9db841270f11aa8647a"},
+                       "src_sha256": "d9c485962b741bef7061e794a1ade571092f6afaced02c5fea4373d38c12118b"},
 }
 
 

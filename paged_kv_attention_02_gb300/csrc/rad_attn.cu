@@ -116,7 +116,7 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
         pl.tile = rad::TileInfo{128, 0, 4, 0, 0, rad::PrefillTileKeys, RAD_PREFILL_NSK + RAD_PREFILL_NSV, 128, 256, 0,
                                 RAD_PREFILL_CTAS};
     else if (pl.family == rad::kFamSplitTC)
-        pl.tile = rad::split_tc05_info();
+        pl.tile = rad::split_tc05_info(pl.M <= 8);
     else if (pl.family == rad::kFamSplitBf)
         pl.tile = rad::split_bf16_tc05_info(pl.M <= 8);
     else
@@ -449,7 +449,7 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
         if (encode_map(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, k_pool, 3, kd, ks, kb) != RAD_OK ||
             encode_map(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, v_pool, 3, kd, ks, kb) != RAD_OK)
             return RAD_E_CUDA;
-        e = pl.family == rad::kFamSplitTC ? rad::launch_split_tc05(tk, tv, p, sms, st)
+        e = pl.family == rad::kFamSplitTC ? rad::launch_split_tc05(tk, tv, p, sms, st, pl.M <= 8)
                                           : rad::launch_prefill_fp8(tk, tv, p, sms, st);
     } else if (pl.family == rad::kFamSplitBf) {
         rc = get_encoder();

@@ -59,19 +59,33 @@
 #ifndef RAD_SPLITTC_NSK
 #define RAD_SPLITTC_NSK 4
 #endif
+// Stages of the form for calls with at most 8 query rows per KV head.
+#ifndef RAD_SPLITTC_FEW_NSK
+#define RAD_SPLITTC_FEW_NSK 4
+#endif
+#ifndef RAD_SPLITTC_FEW_NSV
+#define RAD_SPLITTC_FEW_NSV 2
+#endif
 #ifndef RAD_SPLITTC_NSV
-#define RAD_SPLITTC_NSV 2
+#define RAD_SPLITTC_NSV 3
 #endif
 
 namespace rad {
 
+// FEW: calls with at most 8 query rows per KV head (decode steps) take their
+// own stage counts (same-box: four K and two V stages suit them, four and three
+// the verify calls).  Nothing else changes, so a row's bits are those of the
+// other form.  (Holding a decode item's 8 rows once, with a zero 8-row group
+// stride in the QK descriptor as the bf16 kernel does, made this kernel's
+// decode slower.)
+template <bool FEW>
 struct SplitTcCfg {
     static constexpr int D = 128;                   // head dim
     static constexpr int BK = 128;                  // keys per tile
     static constexpr int QT = 32;                   // (item planner) query rows per item
     static constexpr int KS = BK;                   // (item planner) keys per stage
-    static constexpr int NSK = RAD_SPLITTC_NSK;      // K stages (with the tile's page scales)
-    static constexpr int NSV = RAD_SPLITTC_NSV;      // V stages
+    static constexpr int NSK = FEW ? RAD_SPLITTC_FEW_NSK : RAD_SPLITTC_NSK;   // K stages (with the page scales)
+    static constexpr int NSV = FEW ? RAD_SPLITTC_FEW_NSV : RAD_SPLITTC_NSV;   // V stages
     static constexpr int ROW = 128;                 // bytes of one e4m3 key row
     static constexpr int KV_TILE = BK * ROW;        // e4m3 K or V rows of one tile
     static constexpr int ATOM = BK * 128;           // one 64-column block of the f16 V tile
@@ -109,7 +123,7 @@ struct SplitTcCfg {
 // the item: P is 0 there, the staged row may hold anything).  The row's loads
 // come before its stores, which may alias them as far as the compiler knows.
 __device__ __forceinline__ void convert_v_row(const uint8_t* stage, uint8_t* v16, int row, bool zero) {
-    using C = SplitTcCfg;
+    using C = SplitTcCfg<false>;   // the f16 tile's layout is the same in both forms
     const uint32_t sw = (uint32_t)(row & 7);
     const uint8_t* src = stage + row * 128;
     uint8_t* dst = v16 + row * 128;
@@ -138,11 +152,11 @@ __device__ __forceinline__ void convert_v_row(const uint8_t* stage, uint8_t* v16
 
 // MODE: kModeCausal, kModeWindow or kModeTree (draft-tree rows, uniform row
 // counts: bit i of a row's mask word lets it see the call's key i).
-template <int MODE>
-__global__ void __launch_bounds__(SplitTcCfg::NTHREADS, 1)
+template <int MODE, bool FEW>
+__global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
     attn_split_tc05_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                                 const __grid_constant__ AttnParams p) {
-    using C = SplitTcCfg;
+    using C = SplitTcCfg<FEW>;
     constexpr bool WIN = MODE == kModeWindow;
     constexpr bool TREE = MODE == kModeTree;
     extern __shared__ uint8_t smem_raw[];

@@ -153,8 +153,8 @@ cudaError_t launch_prefill_tc05(const CUtensorMap& tq, const CUtensorMap& tk, co
 cudaError_t launch_prefill_fp8(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
                                cudaStream_t st);
 cudaError_t launch_split_tc05(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
-                              cudaStream_t st);
-TileInfo split_tc05_info();
+                              cudaStream_t st, bool few);
+TileInfo split_tc05_info(bool few);
 cudaError_t launch_split_bf16_tc05(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
                                    cudaStream_t st, bool few);
 TileInfo split_bf16_tc05_info(bool few);
