@@ -46,10 +46,11 @@ METRIC = "paged-decode KV GB/s and seq-tokens/s (fraction of GB300 HBM peak) at 
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM traffic per launch from the committed ncu capture (profiles/), valid only
-# while the kernel sources hash to `src_sha256`.
+# DRAM traffic per launch of the dominant kernel plus the combine, from the
+# committed ncu captures (a capture of fewer sequences scaled by the KV bytes
+# where the workload is too large to capture), valid only while the kernel
+# sources hash to `src_sha256`.
 NCU_TRAFFIC: dict[str, dict] = {
-    # profiles/attn_split_bf16_tc05_batched_decode_64seq.md: 64-sequence capture scaled by KV bytes
     "batched_decode": {"bytes_per_launch": 4_499_500_000 + 20_200_000,
                        "src_sha256": "d9c485962b741bef7061e794a1ade571092f6afaced02c5fea4373d38c12118b"},
 }
@@ -76,6 +77,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--max-groups", type=int, default=0,
                     help="draw only N sequences (a smaller pool, for profiling)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only --workload, not the other configurations beside it")
     return ap.parse_args()
 
 
@@ -290,128 +293,232 @@ def workload_config(w: wl.Workload, l2: str | None = None) -> dict:
             "l2": l2 if l2 is not None else (L2_FLUSHED if fits_l2(w) else L2_LARGE)}
 
 
+# The configurations of the op's headline measurement: the batched decode is the
+# metric's own configuration, the others are measured beside it in the same run.
+PER_CONFIG = ["tiny_decode", "batched_decode", "hybrid_decode", "spec_verify", "prefill_chunk"]
+PREWINDOW_S = 1.0   # untimed replays before a timed window, with the clock sampler running
+
+
+class Step:
+    """One workload on the device: its inputs, one call of the op through the
+    C ABI, and (unless disabled) the call captured in a CUDA graph."""
+
+    def __init__(self, w: wl.Workload, dev, use_graph: bool):
+        from paged_kv_attention_02_gb300 import binding as b
+        self.w = w
+        c = w.cfg
+        self.fp8 = c.kv_dtype == wl.KV_FP8_E4M3
+
+        def to_dev(a, as_bf16=False):
+            t = torch.from_numpy(np.ascontiguousarray(a))
+            if as_bf16:
+                t = t.view(torch.int16).view(torch.bfloat16)
+            return t.to(dev)
+
+        # ragged and tree calls go through rad_attn_paged_ex with their offsets / mask words
+        self.general = w.ragged or w.tree_mask is not None
+        q_np, cu_np, mask_np = w.q, None, None
+        if w.ragged:
+            q_np, cu_np, mask_np = w.packed()
+        elif w.tree_mask is not None:
+            mask_np = w.tree_mask.reshape(-1)
+        self.q_np, self.cu_np, self.mask_np = q_np, cu_np, mask_np
+        self.q = to_dev(q_np.view(np.int16), True)
+        self.cu = None if cu_np is None else to_dev(cu_np)
+        self.mask = None if mask_np is None else to_dev(mask_np.view(np.int32))
+        self.total_rows = int(q_np.shape[0]) if w.ragged else 0
+        self.k = to_dev(w.k_pool) if self.fp8 else to_dev(w.k_pool.view(np.int16), True)
+        self.v = to_dev(w.v_pool) if self.fp8 else to_dev(w.v_pool.view(np.int16), True)
+        self.ks = to_dev(w.k_scales) if self.fp8 else None
+        self.vs = to_dev(w.v_scales) if self.fp8 else None
+        self.table = to_dev(w.page_table)
+        self.lens = to_dev(w.seq_lens)
+        self.out = torch.empty(tuple(self.q.shape), dtype=torch.bfloat16, device=dev)
+        shape = b.shape_args(w.groups, c.rows, c.n_head, c.n_head_kv, c.head_dim, c.page_size, w.pages_per_seq,
+                             c.kv_dtype, ragged=w.ragged, tree=w.tree_mask is not None, total_rows=self.total_rows)
+        self.ws = torch.empty(max(1, b.ex_workspace_bytes(shape)), dtype=torch.uint8, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.stream = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(self.stream):
+            self.call()
+        torch.cuda.synchronize()
+        assert int(self.err.item()) == 0, f"{c.name}: error word {int(self.err.item())}"
+        self.step = self.call
+        if use_graph:
+            self.graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.graph, stream=self.stream):
+                self.call()
+            self.step = self.graph.replay
+        # a workload whose inputs fit in L2 is timed step by step, each after an L2 flush
+        self.flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if fits_l2(w) else None
+
+    def call(self, qq=None, tt=None, ll=None, oo=None, cc=None, mm=None):
+        from paged_kv_attention_02_gb300 import binding as b
+        c = self.w.cfg
+        qq = self.q if qq is None else qq
+        tt = self.table if tt is None else tt
+        ll = self.lens if ll is None else ll
+        oo = self.out if oo is None else oo
+        if self.general:
+            b.attn_paged_general(qq, self.k, self.v, tt, ll, rows=c.rows, n_head=c.n_head, n_head_kv=c.n_head_kv,
+                                 head_dim=c.head_dim, page_size=c.page_size, scale=c.scale, kv_dtype=c.kv_dtype,
+                                 k_scales=self.ks, v_scales=self.vs, cu_seqlens=self.cu if cc is None else cc,
+                                 tree_mask=self.mask if mm is None else mm, total_rows=self.total_rows, out=oo,
+                                 workspace=self.ws, err_word=self.err, stream=self.stream)
+            return
+        b.attn_paged(qq, self.k, self.v, tt, ll, rows=c.rows, n_head=c.n_head, n_head_kv=c.n_head_kv,
+                     head_dim=c.head_dim, page_size=c.page_size, scale=c.scale, kv_dtype=c.kv_dtype,
+                     k_scales=self.ks, v_scales=self.vs, out=oo, workspace=self.ws, err_word=self.err,
+                     stream=self.stream)
+
+    def timed(self, fn, steps: int) -> float:
+        """ms per step of fn over `steps` steps on the step's stream (CUDA
+        events on that stream)."""
+        st = self.stream
+        if self.flush_buf is None:
+            a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            with torch.cuda.stream(st):
+                for _ in range(steps):
+                    fn()
+            z.record(st)
+            torch.cuda.synchronize()
+            return a.elapsed_time(z) / steps
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        with torch.cuda.stream(st):
+            for a, z in pairs:
+                self.flush_buf.fill_(1)
+                a.record(st)
+                fn()
+                z.record(st)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(z) for a, z in pairs) / steps
+
+    def prewindow(self, seconds: float):
+        """Untimed replays of the step (with the flush where the step is
+        timed after one) for about `seconds`, so the clock sampler sees the
+        GPU under this load before the timed window."""
+        with torch.cuda.stream(self.stream):
+            self.step()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        self.timed(self.step, 1)
+        one = max(time.perf_counter() - t0, 1e-5)
+        n = int(min(200000, max(1, seconds / one)))
+        t_end = time.perf_counter() + seconds
+        while time.perf_counter() < t_end:
+            with torch.cuda.stream(self.stream):
+                for _ in range(min(n, 2000)):
+                    if self.flush_buf is not None:
+                        self.flush_buf.fill_(1)
+                    self.step()
+            torch.cuda.synchronize()
+
+
+def measure_device(st: Step, steps: int, warmup: int, world: int, sampler: ClockSampler | None) -> dict:
+    """Warm-up, an untimed pre-window under the clock sampler, then exactly
+    `steps` timed replays bracketed by a barrier and a synchronize."""
+    with torch.cuda.stream(st.stream):
+        for _ in range(max(3, warmup)):
+            st.step()
+    torch.cuda.synchronize()
+    pre0 = time.time()
+    st.prewindow(PREWINDOW_S)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall0 = time.time()
+    ms = st.timed(st.step, steps)
+    wall1 = time.time()
+    barrier(world)
+    assert int(st.err.item()) == 0
+    clocks = None
+    if sampler is not None:
+        time.sleep(0.12)   # the sample taken at the window's end
+        timed = sampler.summary(wall0, wall1)
+        pre = sampler.summary(pre0, wall0)
+        clocks = {"sm_mhz": timed["sm_mhz"], "sm_max_mhz": timed["sm_max_mhz"],
+                  "reasons": sorted(set(timed["reasons"]) | set(pre["reasons"])), "samples": timed["samples"],
+                  "prewindow": dict(pre, seconds=round(wall0 - pre0, 3),
+                                    note="untimed replays of the same step right before the timed window")}
+        both = sampler.summary(pre0, wall1)
+        clocks["samples_under_load"] = both["samples"]
+        clocks["sm_mhz_under_load"] = both["sm_mhz"]
+    return {"ms": ms, "clocks": clocks}
+
+
+def roofline_of(w: wl.Workload, ms: float, desc: str) -> dict:
+    nbytes = wl.kv_bytes(w) + wl.aux_bytes(w)
+    tr = NCU_TRAFFIC.get(w.cfg.name)
+    traffic = tr["bytes_per_launch"] if tr and tr.get("src_sha256") == kernel_source_hash() else None
+    if "split_len=0" in desc:
+        # a prefill chunk (no splits): bound by the tensor pipe, not by HBM
+        tpeak, tpeak_src = tensor_peak()
+        flops = wl.attended_flops(w)
+        t_ach = flops / (ms * 1e-3) / 1e12
+        return {"bound": "tensor", "achieved": t_ach, "peak": tpeak, "unit": "TFLOP/s", "frac": t_ach / tpeak,
+                "traffic": traffic, "peak_source": tpeak_src, "algorithmic_flops_per_launch": flops,
+                "kv_bytes_per_launch": nbytes}
+    peak, peak_src = hbm_peak()
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": traffic, "peak_source": peak_src, "algorithmic_bytes_per_launch": nbytes,
+            "kv_bytes_per_launch": wl.kv_bytes(w), "aux_bytes_per_launch": wl.aux_bytes(w)}
+
+
+def config_entry(w: wl.Workload, ms: float, clocks, graph: bool) -> dict:
+    """One configuration's figures, for the per_config table."""
+    desc = describe(w)
+    rl = roofline_of(w, ms, desc)
+    nbytes = wl.kv_bytes(w) + wl.aux_bytes(w)
+    return {"workload": workload_config(w)["workload"], "ms_per_step": ms,
+            "kv_gbs": nbytes / (ms * 1e-3) / 1e9,
+            "seq_tokens_per_s": float(w.seq_lens.astype(np.int64).sum()) / (ms * 1e-3),
+            "rows_per_s": float(w.rows_of().sum()) / (ms * 1e-3),
+            "roofline": {k: rl[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")},
+            "l2": L2_FLUSHED if fits_l2(w) else L2_LARGE, "graph": graph, "clocks": clocks,
+            "kernel": desc.split(" family=")[0]}
+
+
+def make_bench_workload(name: str, rank: int, max_groups: int = 0) -> wl.Workload:
+    cfg = rank_config(name, rank)
+    subset = max_groups and max_groups < cfg.groups
+    if subset and not cfg.q_lens:
+        cfg = replace(cfg, groups=max_groups)
+    w = wl.make_workload(cfg)
+    if subset and cfg.q_lens:
+        # a ragged step keeps its mix: sequences spread evenly over the call order
+        w = wl.compact_pool(
+            w.select_groups(np.unique(np.linspace(0, cfg.groups - 1, max_groups).round().astype(int))))
+    return w
+
+
 def run_ours(args, rank, world, local):
-    from paged_kv_attention_02_gb300 import binding as b
     from paged_kv_attention_02_gb300.build import build_library
 
     build_library()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    cfg = rank_config(args.workload, rank)
-    subset = args.max_groups and args.max_groups < cfg.groups
-    if subset and not cfg.q_lens:
-        cfg = replace(cfg, groups=args.max_groups)
-    w = wl.make_workload(cfg)
-    if subset and cfg.q_lens:
-        # a ragged step keeps its mix: sequences spread evenly over the call order
-        w = wl.compact_pool(
-            w.select_groups(np.unique(np.linspace(0, cfg.groups - 1, args.max_groups).round().astype(int))))
+    w = make_bench_workload(args.workload, rank, args.max_groups)
     c = w.cfg
     fp8 = c.kv_dtype == wl.KV_FP8_E4M3
-
-    def to_dev(a, as_bf16=False):
-        t = torch.from_numpy(np.ascontiguousarray(a))
-        if as_bf16:
-            t = t.view(torch.int16).view(torch.bfloat16)
-        return t.to(dev)
-
-    # ragged and tree calls go through rad_attn_paged_ex with their offsets / mask words
-    general = w.ragged or w.tree_mask is not None
-    q_np, cu_np, mask_np = w.q, None, None
-    if w.ragged:
-        q_np, cu_np, mask_np = w.packed()
-    elif w.tree_mask is not None:
-        mask_np = w.tree_mask.reshape(-1)
-    q = to_dev(q_np.view(np.int16), True)
-    cu = None if cu_np is None else to_dev(cu_np)
-    mask = None if mask_np is None else to_dev(mask_np.view(np.int32))
-    total_rows = int(q_np.shape[0]) if w.ragged else 0
-    k = to_dev(w.k_pool) if fp8 else to_dev(w.k_pool.view(np.int16), True)
-    v = to_dev(w.v_pool) if fp8 else to_dev(w.v_pool.view(np.int16), True)
-    ks = to_dev(w.k_scales) if fp8 else None
-    vs = to_dev(w.v_scales) if fp8 else None
-    table = to_dev(w.page_table)
-    lens = to_dev(w.seq_lens)
-    out = torch.empty(tuple(q.shape), dtype=torch.bfloat16, device=dev)
-    shape = b.shape_args(w.groups, c.rows, c.n_head, c.n_head_kv, c.head_dim, c.page_size, w.pages_per_seq,
-                         c.kv_dtype, ragged=w.ragged, tree=w.tree_mask is not None, total_rows=total_rows)
-    ws = torch.empty(max(1, b.ex_workspace_bytes(shape)), dtype=torch.uint8, device=dev)
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
-    stream = torch.cuda.Stream(device=dev)
-
-    def call(qq=q, tt=table, ll=lens, oo=out, cc=cu, mm=mask):
-        if general:
-            b.attn_paged_general(qq, k, v, tt, ll, rows=c.rows, n_head=c.n_head, n_head_kv=c.n_head_kv,
-                                 head_dim=c.head_dim, page_size=c.page_size, scale=c.scale, kv_dtype=c.kv_dtype,
-                                 k_scales=ks, v_scales=vs, cu_seqlens=cc, tree_mask=mm, total_rows=total_rows,
-                                 out=oo, workspace=ws, err_word=err, stream=stream)
-            return
-        b.attn_paged(qq, k, v, tt, ll, rows=c.rows, n_head=c.n_head, n_head_kv=c.n_head_kv,
-                     head_dim=c.head_dim, page_size=c.page_size, scale=c.scale, kv_dtype=c.kv_dtype,
-                     k_scales=ks, v_scales=vs, out=oo, workspace=ws, err_word=err, stream=stream)
-
-    with torch.cuda.stream(stream):
-        call()
-    torch.cuda.synchronize()
-    assert int(err.item()) == 0, f"error word {int(err.item())}"
-
-    step = call
-    if not args.no_graph:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            call()
-        step = g.replay
-
-    # A workload whose inputs fit in L2 is timed step by step, each after an L2 flush
-    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if fits_l2(w) else None
-
-    def timed(fn, steps: int) -> float:
-        """ms per step of fn over `steps` steps on `stream` (events on that stream)."""
-        if flush_buf is None:
-            a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            with torch.cuda.stream(stream):
-                for _ in range(steps):
-                    fn()
-            z.record(stream)
-            torch.cuda.synchronize()
-            return a.elapsed_time(z) / steps
-        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-        with torch.cuda.stream(stream):
-            for a, z in pairs:
-                flush_buf.fill_(1)
-                a.record(stream)
-                fn()
-                z.record(stream)
-        torch.cuda.synchronize()
-        return sum(a.elapsed_time(z) for a, z in pairs) / steps
+    st = Step(w, dev, not args.no_graph)
 
     sampler = ClockSampler(local)
     # ---- device-resident timing
-    with torch.cuda.stream(stream):
-        for _ in range(max(3, args.warmup)):
-            step()
-    torch.cuda.synchronize()
-    barrier(world)
-    wall0 = time.time()
-    ms = timed(step, args.steps)
-    wall1 = time.time()
-    barrier(world)
-    clocks = sampler.summary(wall0, wall1)
-    sampler.stop()
-    assert int(err.item()) == 0
+    dm = measure_device(st, args.steps, args.warmup, world, sampler)
+    ms = dm["ms"]
 
     # ---- end to end: per-step inputs from pinned host memory, result back to host
-    q_h = torch.from_numpy(q_np.view(np.int16)).view(torch.bfloat16).pin_memory()
+    q_h = torch.from_numpy(st.q_np.view(np.int16)).view(torch.bfloat16).pin_memory()
     t_h = torch.from_numpy(w.page_table).pin_memory()
     l_h = torch.from_numpy(w.seq_lens).pin_memory()
-    o_h = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
-    q_d, t_d, l_d = torch.empty_like(q), torch.empty_like(table), torch.empty_like(lens)
+    o_h = torch.empty(st.out.shape, dtype=torch.bfloat16).pin_memory()
+    q_d, t_d, l_d = torch.empty_like(st.q), torch.empty_like(st.table), torch.empty_like(st.lens)
     # per-step row offsets and mask words travel with the step's other inputs
-    c_h = None if cu is None else torch.from_numpy(cu_np).pin_memory()
-    m_h = None if mask is None else torch.from_numpy(mask_np.view(np.int32)).pin_memory()
-    c_d = None if cu is None else torch.empty_like(cu)
-    m_d = None if mask is None else torch.empty_like(mask)
+    c_h = None if st.cu is None else torch.from_numpy(st.cu_np).pin_memory()
+    m_h = None if st.mask is None else torch.from_numpy(st.mask_np.view(np.int32)).pin_memory()
+    c_d = None if st.cu is None else torch.empty_like(st.cu)
+    m_d = None if st.mask is None else torch.empty_like(st.mask)
 
     def e2e_step():
         q_d.copy_(q_h, non_blocking=True)
@@ -421,47 +528,49 @@ def run_ours(args, rank, world, local):
             c_d.copy_(c_h, non_blocking=True)
         if m_d is not None:
             m_d.copy_(m_h, non_blocking=True)
-        call(q_d, t_d, l_d, out, c_d, m_d)
-        o_h.copy_(out, non_blocking=True)
+        st.call(q_d, t_d, l_d, st.out, c_d, m_d)
+        o_h.copy_(st.out, non_blocking=True)
 
-    with torch.cuda.stream(stream):
+    with torch.cuda.stream(st.stream):
         for _ in range(max(3, args.warmup)):
             e2e_step()
     torch.cuda.synchronize()
     barrier(world)
-    e2e_ms = timed(e2e_step, args.steps)
+    e2e_ms = st.timed(e2e_step, args.steps)
     barrier(world)
     h2d = q_h.numel() * 2 + t_h.numel() * 4 + l_h.numel() * 4
     h2d += (0 if c_h is None else c_h.numel() * 4) + (0 if m_h is None else m_h.numel() * 4)
     d2h = o_h.numel() * 2
 
-    nbytes = wl.kv_bytes(w)
+    nbytes = wl.kv_bytes(w) + wl.aux_bytes(w)
     tokens = int(w.seq_lens.astype(np.int64).sum())
     ms_max = reduce_max(ms, world)
     e2e_max = reduce_max(e2e_ms, world)
     tot_bytes = reduce_sum(float(nbytes), world)
     tot_tokens = reduce_sum(float(tokens), world)
     tot_rows = reduce_sum(float(w.rows_of().sum()), world)
+
+    # ---- the other configurations, device-resident, one GPU only
+    per_config = None
+    if world == 1 and not args.no_per_config and not args.max_groups:
+        per_config = {args.workload: config_entry(w, ms, dm["clocks"], not args.no_graph)}
+        del st
+        torch.cuda.empty_cache()
+        for name in PER_CONFIG:
+            if name == args.workload:
+                continue
+            wo = make_bench_workload(name, rank)
+            so = Step(wo, dev, not args.no_graph)
+            mo = measure_device(so, args.steps, args.warmup, world, sampler)
+            per_config[name] = config_entry(wo, mo["ms"], mo["clocks"], not args.no_graph)
+            del so, wo
+            torch.cuda.empty_cache()
+    sampler.stop()
     if rank != 0:
         return
     value = tot_bytes / (ms_max * 1e-3) / 1e9
-    peak, peak_src = hbm_peak()
-    achieved = nbytes / (ms * 1e-3) / 1e9
-    tr = NCU_TRAFFIC.get(c.name)
-    traffic = tr["bytes_per_launch"] if tr and tr.get("src_sha256") == kernel_source_hash() else None
+    peak, _ = hbm_peak()
     desc = describe(w)
-    if "split_len=0" in desc:
-        # a prefill chunk (no splits): bound by the tensor pipe, not by HBM
-        tpeak, tpeak_src = tensor_peak()
-        flops = wl.attended_flops(w)
-        t_ach = flops / (ms * 1e-3) / 1e12
-        roofline = {"bound": "tensor", "achieved": t_ach, "peak": tpeak, "unit": "TFLOP/s",
-                    "frac": t_ach / tpeak, "traffic": traffic, "peak_source": tpeak_src,
-                    "algorithmic_flops_per_launch": flops, "kv_bytes_per_launch": nbytes}
-    else:
-        roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                    "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
-                    "algorithmic_bytes_per_launch": nbytes}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
@@ -470,14 +579,16 @@ def run_ours(args, rank, world, local):
         "seq_tokens_per_s": tot_tokens / (ms_max * 1e-3),
         "rows_per_s": tot_rows / (ms_max * 1e-3),
         "hbm_frac": value / world / peak,
-        "roofline": roofline,
-        "clocks": clocks,
+        "roofline": roofline_of(w, ms, desc),
+        "clocks": dm["clocks"],
         "e2e": {"value": tot_bytes / (e2e_max * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": e2e_max,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "KV pools resident (persistent state); q, page table, seq_lens in and out back per step"},
         "gpu_launches": args.steps * launches_per_step(w),
         "kernel": desc,
     }
+    if per_config is not None:
+        line["per_config"] = per_config
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     print(json.dumps(line), flush=True)

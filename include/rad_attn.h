@@ -105,8 +105,10 @@ enum {
                               the f16 range (|q| > 65504) -- that row's output
                               is not meaningful (head_dim 128 carries q exactly
                               and never raises it) */
-    RAD_ERRW_TIMEOUT = 8u, /* an internal wait ran past its time limit; the
-                              affected outputs are not meaningful */
+    RAD_ERRW_TIMEOUT = 8u, /* an internal wait ran past its time limit (2 s
+                              by default); the kernel unwinds and returns,
+                              the affected outputs are not meaningful, and
+                              later calls on the stream are unaffected */
     RAD_ERRW_CUSEQ = 16u,  /* ragged rows: cu_seqlens[g] < 0, cu_seqlens[g+1] <
                               cu_seqlens[g], or more rows than `rows` */
     RAD_ERRW_MASK = 32u    /* tree rows: a mask word without its own row's bit,
@@ -287,6 +289,31 @@ size_t rad_attn_paged_ex_workspace_bytes(const RadAttnPagedArgs* args);
 int rad_attn_paged_ex_describe(const RadAttnPagedArgs* args, char* buf, size_t buf_len);
 
 /*
+ * rad_attn_paged_fault_test -- a test hook for the time-out path of the
+ * device error word ("kern manifest v7", $defs.Fill `error`: a one-word
+ * error flag the host reads after the call).
+ *
+ * Runs the call described by `args` exactly as rad_attn_paged_ex does, with
+ * two test-only settings:
+ *   wait_limit_ns  the limit of every bounded wait inside the kernels, in
+ *                  [1e6, 2e9] ns; 0 keeps the default (2 s).
+ *   fault          RAD_FAULT_NONE, or RAD_FAULT_SKIP_FIRST_K_TILE: the K
+ *                  producer of the first CTA leaves its first K tile's copy
+ *                  unissued, so the waits on that tile run out; the kernel
+ *                  then sets RAD_ERRW_TIMEOUT in err_word, unwinds its warp
+ *                  roles (copies in flight drained, tensor memory freed) and
+ *                  returns, leaving that CTA's rows unwritten.
+ * The fault is honoured only by calls that run on the bf16 tcgen05 split
+ * kernel (split calls with head_dim 128 over bf16 pools); any other call
+ * with a fault, an unknown fault or a limit outside the range returns
+ * RAD_E_ARG and launches nothing.  Nothing here is meant for production use.
+ */
+enum { RAD_FAULT_NONE = 0, RAD_FAULT_SKIP_FIRST_K_TILE = 1 };
+
+int rad_attn_paged_fault_test(const RadAttnPagedArgs* args, uint64_t wait_limit_ns, int32_t fault,
+                              rad_stream_t stream);
+
+/*
  * rad_attn_paged_noalloc -- the same op for callers that cannot allocate.
  *
  * The pages have no counterpart to this entry point; it exists for callers
@@ -306,7 +333,10 @@ int rad_attn_paged_ex_describe(const RadAttnPagedArgs* args, char* buf, size_t b
  *     RAD_NOALLOC_SCRATCH_BYTES returns RAD_E_WORKSPACE and launches nothing.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first
- *     call before any stream capture on the device.
+ *     call before any stream capture on the device.  The address is kept
+ *     per device together with the context it was found in; after a device
+ *     reset (or a new primary context) the next call looks it up again, so
+ *     that call too should come before any capture.
  *   - Every call shares the one array and leaves its contents behind; no
  *     part of it needs to start at zero (a call reads only what it wrote
  *     earlier in the same call).  Calls

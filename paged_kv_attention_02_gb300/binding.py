@@ -35,7 +35,11 @@ RAD_ERRW_MASK = 32
 EXPORTS = ("rad_attn_paged", "rad_attn_paged_workspace_bytes", "rad_attn_paged_describe",
            "rad_attn_status_string", "rad_attn_version", "rad_attn_paged_noalloc",
            "rad_attn_paged_window", "rad_attn_paged_ex", "rad_attn_paged_ex_workspace_bytes",
-           "rad_attn_paged_ex_describe")
+           "rad_attn_paged_ex_describe", "rad_attn_paged_fault_test")
+
+# Test-only faults of rad_attn_paged_fault_test (include/rad_attn.h).
+RAD_FAULT_NONE = 0
+RAD_FAULT_SKIP_FIRST_K_TILE = 1
 
 
 class RadAttnPagedArgs(ctypes.Structure):
@@ -92,6 +96,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.rad_attn_paged_ex_workspace_bytes.argtypes = [p]
     lib.rad_attn_paged_ex_describe.restype = ctypes.c_int
     lib.rad_attn_paged_ex_describe.argtypes = [p, ctypes.c_char_p, sz]
+    lib.rad_attn_paged_fault_test.restype = ctypes.c_int
+    lib.rad_attn_paged_fault_test.argtypes = [p, ctypes.c_uint64, i32, p]
     lib.rad_attn_paged_noalloc.restype = ctypes.c_int
     lib.rad_attn_paged_noalloc.argtypes = [p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, i32,
                                            ctypes.c_float, i32, p, p, p, p, p]
@@ -233,6 +239,36 @@ def attn_paged_general(q, k_pool, v_pool, page_table, seq_lens, *, rows, n_head,
     hold every row the offsets may name).  Returns `out` (allocated like q
     when None; rows no group names are not written).
     """
+    a, out, workspace = _general_args(q, k_pool, v_pool, page_table, seq_lens, rows, n_head, n_head_kv, head_dim,
+                                      page_size, scale, kv_dtype, k_scales, v_scales, cu_seqlens, tree_mask,
+                                      window, total_rows, out, workspace, err_word)
+    rc = attn_paged_ex(a, stream)
+    if rc != RAD_OK:
+        raise RadAttnError(rc, "rad_attn_paged_ex")
+    return out
+
+
+def attn_paged_fault_test(q, k_pool, v_pool, page_table, seq_lens, *, rows, n_head, n_head_kv, head_dim,
+                          page_size, scale, wait_limit_ns=0, fault=RAD_FAULT_NONE, kv_dtype=RAD_KV_BF16,
+                          k_scales=None, v_scales=None, out=None, workspace=None, err_word=None, stream=None):
+    """rad_attn_paged_fault_test: attn_paged_general's call with a test's
+    wait limit (ns, 0 = the default) and injected fault.  Returns `out`."""
+    a, out, workspace = _general_args(q, k_pool, v_pool, page_table, seq_lens, rows, n_head, n_head_kv, head_dim,
+                                      page_size, scale, kv_dtype, k_scales, v_scales, None, None, 0, None, out,
+                                      workspace, err_word)
+    rc = int(load().rad_attn_paged_fault_test(ctypes.byref(a), int(wait_limit_ns), int(fault),
+                                              _stream_handle(stream)))
+    if rc != RAD_OK:
+        raise RadAttnError(rc, "rad_attn_paged_fault_test")
+    return out
+
+
+def _general_args(q, k_pool, v_pool, page_table, seq_lens, rows, n_head, n_head_kv, head_dim, page_size, scale,
+                  kv_dtype, k_scales, v_scales, cu_seqlens, tree_mask, window, total_rows, out, workspace,
+                  err_word):
+    """A filled RadAttnPagedArgs (with `out` and the workspace allocated by
+    torch when not given); returns (args, out, workspace), the last two kept
+    alive by the caller for the call."""
     groups = int(seq_lens.shape[0])
     if out is None:
         out = torch.empty(tuple(q.shape), dtype=torch.bfloat16, device=q.device)
@@ -257,10 +293,7 @@ def attn_paged_general(q, k_pool, v_pool, page_table, seq_lens, *, rows, n_head,
     a.workspace = None if workspace is None else workspace.data_ptr()
     a.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     a.err_word = None if err_word is None else err_word.data_ptr()
-    rc = attn_paged_ex(a, stream)
-    if rc != RAD_OK:
-        raise RadAttnError(rc, "rad_attn_paged_ex")
-    return out
+    return a, out, workspace
 
 
 def call_raw(q_ptr, k_ptr, v_ptr, table_ptr, lens_ptr, groups, rows, n_head, n_head_kv, head_dim,

@@ -70,7 +70,13 @@ constexpr int kModeCausal = 0;
 constexpr int kModeWindow = 1;
 constexpr int kModeTree = 2;
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // default limit of each bounded wait: 2 s
+
+// Test-only fault injection (AttnParams::fault): the K producer of the tcgen05
+// bf16 split kernel in CTA 0 leaves its first tile's copy unissued, so the
+// waits on that tile run out and the kernel unwinds with kErrTimeout.
+constexpr int kFaultNone = 0;
+constexpr int kFaultSkipFirstKTile = 1;
 
 // The running max of a row moves (and its accumulator is rescaled) only when
 // new logits exceed it by more than this many powers of two.
@@ -108,6 +114,8 @@ struct AttnParams {
     int n_items;           // max_splits * groups * n_head_kv * n_qtiles
     int window;            // > 0: each row sees only its last `window` keys; 0: no window
     float scale_log2;      // scale * log2(e)
+    uint64_t wait_ns;      // limit of each bounded wait (kWaitLimitNs unless a test lowers it)
+    int fault;             // kFaultNone, or a test's injected fault
 };
 
 // First key that query row r of a call with `rows` rows over a sequence of
@@ -384,7 +392,7 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
             // ---- query rows of the item
             if (pw == 0) {
                 const uint32_t slot = qcount & 1u, use = qcount >> 1;
-                if (use >= 1 && !mbar_wait_bounded(bar_qempty + 8 * slot, (use - 1) & 1u, kWaitLimitNs)) {
+                if (use >= 1 && !mbar_wait_bounded(bar_qempty + 8 * slot, (use - 1) & 1u, p.wait_ns)) {
                     abort = true;
                     break;
                 }
@@ -434,7 +442,7 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
                     }
                 }
                 const uint32_t slot = scount % C::NS, use = scount / C::NS;
-                if (use >= 1 && !mbar_wait_bounded(bar_empty + 8 * slot, (use - 1) & 1u, kWaitLimitNs)) {
+                if (use >= 1 && !mbar_wait_bounded(bar_empty + 8 * slot, (use - 1) & 1u, p.wait_ns)) {
                     abort = true;
                     break;
                 }
@@ -487,7 +495,7 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
         if (pw == 0 && lane == 0) {
             const uint32_t qfirst = qcount > 2u ? qcount - 2u : 0u;
             for (uint32_t c = qfirst; c < qcount; ++c)
-                mbar_wait_bounded(bar_qfull + 8 * (c & 1u), (c >> 1) & 1u, kWaitLimitNs);
+                mbar_wait_bounded(bar_qfull + 8 * (c & 1u), (c >> 1) & 1u, p.wait_ns);
         }
         return;
     }
@@ -524,7 +532,7 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
         uint32_t amask[C::NQW][2];
         {
             const uint32_t slot = qcount & 1u, use = qcount >> 1;
-            if (!mbar_wait_bounded(bar_qfull + 8 * slot, use & 1u, kWaitLimitNs)) abort = true;
+            if (!mbar_wait_bounded(bar_qfull + 8 * slot, use & 1u, p.wait_ns)) abort = true;
             const uint8_t* qs = smem + C::OFF_Q + slot * C::Q_SLOT_BYTES;
             bool qrange_bad = false;
 #pragma unroll
@@ -613,7 +621,7 @@ __global__ void __launch_bounds__(C::NTHREADS, C::MINB) attn_tile_kernel(const _
 
         for (int st = 0; st < it.n_stages && !abort; ++st) {
             const uint32_t slot = scount % C::NS, use = scount / C::NS;
-            if (!mbar_wait_bounded(bar_full + 8 * slot, use & 1u, kWaitLimitNs)) {
+            if (!mbar_wait_bounded(bar_full + 8 * slot, use & 1u, p.wait_ns)) {
                 abort = true;
                 break;
             }

@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
             float my_ks = 1.f, my_vs = 1.f;
             for (int j = 0; j < it.T; ++j) {
                 const uint32_t st = sc % (uint32_t)NSX, use = sc / (uint32_t)NSX;
-                if (use >= 1 && !mbar_wait_bounded(bar_empty + 8 * st, (use - 1) & 1u, kWaitLimitNs)) {
+                if (use >= 1 && !mbar_wait_bounded(bar_empty + 8 * st, (use - 1) & 1u, p.wait_ns)) {
                     abort = true;
                     break;
                 }
@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
         if (lane == 0) {
             const uint32_t first = sc > (uint32_t)NSX ? sc - NSX : 0u;
             for (uint32_t c = first; c < sc; ++c)
-                mbar_wait_bounded(bar_full + 8 * (c % NSX), (c / NSX) & 1u, kWaitLimitNs);
+                mbar_wait_bounded(bar_full + 8 * (c % NSX), (c / NSX) & 1u, p.wait_ns);
         }
     } else if (warp == C::W_QK) {
         // ===================================================== QK issue
@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
             if (item >= n_items) break;
             const PrefItem it = plan_prefill<GEN, C::BM, C::BN>(item, p);
             if (!it.seq_ok) continue;
-            if (!mbar_wait_bounded(bar_q8_full, ic & 1u, kWaitLimitNs)) {
+            if (!mbar_wait_bounded(bar_q8_full, ic & 1u, p.wait_ns)) {
                 abort = true;
                 break;
             }
@@ -290,8 +290,8 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
             for (int j = 0; j < it.T; ++j) {
                 const uint32_t s_ = sc + j, st = s_ % C::NSK, tcj = tc + j, b = tcj & 1u;
                 // K landed, and S buffer b is free: PV(tcj - 2) read the P it held
-                bool ok = mbar_wait_bounded(bar_k_full + 8 * st, (s_ / C::NSK) & 1u, kWaitLimitNs);
-                if (ok && tcj >= 2) ok = mbar_wait_bounded(bar_pv_done + 8 * b, ((tcj - 2) >> 1) & 1u, kWaitLimitNs);
+                bool ok = mbar_wait_bounded(bar_k_full + 8 * st, (s_ / C::NSK) & 1u, p.wait_ns);
+                if (ok && tcj >= 2) ok = mbar_wait_bounded(bar_pv_done + 8 * b, ((tcj - 2) >> 1) & 1u, p.wait_ns);
                 if (!__all_sync(0xffffffffu, ok)) {
                     abort = true;
                     break;
@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
                 // key rows 0 .. QK_VROWS-1 of V_j -> f16 buffer b (free: PV(tcj - 2) is done)
                 // while the softmax works on S_j
                 const uint32_t sv = s_ % C::NSV;
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar_v_full + 8 * sv, (s_ / C::NSV) & 1u, kWaitLimitNs))) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar_v_full + 8 * sv, (s_ / C::NSV) & 1u, p.wait_ns))) {
                     abort = true;
                     break;
                 }
@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
         // every MMA this thread issued is complete before TMEM is released
         if (lane == 0 && issued) {
             tc_commit(bar_final);
-            mbar_wait_bounded(bar_final, 0, kWaitLimitNs);
+            mbar_wait_bounded(bar_final, 0, p.wait_ns);
         }
         __syncwarp();
     } else if (warp == C::W_V) {
@@ -353,10 +353,10 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
             const int zlo = GEN ? it.klo : 0;   // keys below the tile's window may hold anything
             for (int j = 0; j < it.T; ++j) {
                 const uint32_t s_ = sc + j, st = s_ % C::NSV, tcj = tc + j, b = tcj & 1u;
-                bool ok = mbar_wait_bounded(bar_v_full + 8 * st, (s_ / C::NSV) & 1u, kWaitLimitNs);
+                bool ok = mbar_wait_bounded(bar_v_full + 8 * st, (s_ / C::NSV) & 1u, p.wait_ns);
                 // f16 buffer b was last read by PV(tcj - 2)
                 if (ok && tcj >= 2)
-                    ok = mbar_wait_bounded(bar_pv_done + 8 * b, ((tcj - 2) >> 1) & 1u, kWaitLimitNs);
+                    ok = mbar_wait_bounded(bar_pv_done + 8 * b, ((tcj - 2) >> 1) & 1u, p.wait_ns);
                 if (!__all_sync(0xffffffffu, ok)) {
                     abort = true;
                     break;
@@ -369,9 +369,9 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_v_empty + 8 * st);   // the staged V tile is read
                 // PV once P is written (and, at an item's first tile, O was read out)
-                ok = mbar_wait_bounded(bar_p_full + 8 * b, (tcj >> 1) & 1u, kWaitLimitNs);
-                if (ok) ok = mbar_wait_bounded(bar_v16_full + 8 * b, (tcj >> 1) & 1u, kWaitLimitNs);
-                if (ok && j == 0 && ic >= 1) ok = mbar_wait_bounded(bar_o_free, (ic - 1) & 1u, kWaitLimitNs);
+                ok = mbar_wait_bounded(bar_p_full + 8 * b, (tcj >> 1) & 1u, p.wait_ns);
+                if (ok) ok = mbar_wait_bounded(bar_v16_full + 8 * b, (tcj >> 1) & 1u, p.wait_ns);
+                if (ok && j == 0 && ic >= 1) ok = mbar_wait_bounded(bar_o_free, (ic - 1) & 1u, p.wait_ns);
                 if (!__all_sync(0xffffffffu, ok)) {
                     abort = true;
                     break;
@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
         }
         if (lane == 0 && issued) {
             tc_commit(bar_final + 8);
-            mbar_wait_bounded(bar_final + 8, 0, kWaitLimitNs);
+            mbar_wait_bounded(bar_final + 8, 0, p.wait_ns);
         }
         __syncwarp();
     } else {
@@ -420,7 +420,7 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
                 continue;
             }
             // ---- the row's query as two e4m3 terms (the previous item's QKs are done)
-            if (ic >= 1 && !__all_sync(0xffffffffu, mbar_wait_bounded(bar_q8_empty, (ic - 1) & 1u, kWaitLimitNs))) {
+            if (ic >= 1 && !__all_sync(0xffffffffu, mbar_wait_bounded(bar_q8_empty, (ic - 1) & 1u, p.wait_ns))) {
                 abort = true;
                 break;
             }
@@ -492,8 +492,8 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
                 const uint32_t s_ = sc + j, st = s_ % C::NSK;
                 // S_j landed, and the K stage's scales are visible (its K-full phase is
                 // complete: QK waited for it); the stage is released after the reads
-                bool ok = mbar_wait_bounded(bar_s_full + 8 * b, (tcj >> 1) & 1u, kWaitLimitNs);
-                if (ok) ok = mbar_wait_bounded(bar_k_full + 8 * st, (s_ / C::NSK) & 1u, kWaitLimitNs);
+                bool ok = mbar_wait_bounded(bar_s_full + 8 * b, (tcj >> 1) & 1u, p.wait_ns);
+                if (ok) ok = mbar_wait_bounded(bar_k_full + 8 * st, (s_ / C::NSK) & 1u, p.wait_ns);
                 if (!__all_sync(0xffffffffu, ok)) {
                     abort = true;
                     break;
@@ -543,7 +543,7 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
                 }
                 if (__any_sync(0xffffffffu, need)) {
                     const uint32_t tp = tcj - 1;   // the previous tile's PV
-                    const bool okw = mbar_wait_bounded(bar_pv_done + 8 * (tp & 1u), (tp >> 1) & 1u, kWaitLimitNs);
+                    const bool okw = mbar_wait_bounded(bar_pv_done + 8 * (tp & 1u), (tp >> 1) & 1u, p.wait_ns);
                     if (!__all_sync(0xffffffffu, okw)) {
                         abort = true;
                         break;
@@ -594,7 +594,7 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
             }
             // ---- epilogue: O / l -> bf16
             const uint32_t tcl = tc + it.T - 1;
-            if (!mbar_wait_bounded(bar_pv_done + 8 * (tcl & 1u), (tcl >> 1) & 1u, kWaitLimitNs)) abort = true;
+            if (!mbar_wait_bounded(bar_pv_done + 8 * (tcl & 1u), (tcl >> 1) & 1u, p.wait_ns)) abort = true;
             tc_fence_after();
             const float inv = (bad || l_run == 0.f) ? 0.f : 1.f / l_run;
 #pragma unroll

@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
             const PrefItem it = plan_prefill<GEN>(item, p);
             if (!it.seq_ok) continue;
             if (is_k) {
-                if (ic >= 1 && !mbar_wait_bounded(bar_q_empty, (ic - 1) & 1u, kWaitLimitNs)) {
+                if (ic >= 1 && !mbar_wait_bounded(bar_q_empty, (ic - 1) & 1u, p.wait_ns)) {
                     abort = true;
                     break;
                 }
@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
             int batch0 = -1 << 30, my_pg = 0;
             for (int j = 0; j < it.T; ++j) {
                 const uint32_t st = sc % (uint32_t)NSX, use = sc / (uint32_t)NSX;
-                if (use >= 1 && !mbar_wait_bounded(bar_empty + 8 * st, (use - 1) & 1u, kWaitLimitNs)) {
+                if (use >= 1 && !mbar_wait_bounded(bar_empty + 8 * st, (use - 1) & 1u, p.wait_ns)) {
                     abort = true;
                     break;
                 }
@@ -272,8 +272,8 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
         if (lane == 0) {
             const uint32_t first = sc > (uint32_t)NSX ? sc - NSX : 0u;
             for (uint32_t c = first; c < sc; ++c)
-                mbar_wait_bounded(bar_full + 8 * (c % NSX), (c / NSX) & 1u, kWaitLimitNs);
-            if (is_k && ic >= 1) mbar_wait_bounded(bar_q_full, (ic - 1) & 1u, kWaitLimitNs);
+                mbar_wait_bounded(bar_full + 8 * (c % NSX), (c / NSX) & 1u, p.wait_ns);
+            if (is_k && ic >= 1) mbar_wait_bounded(bar_q_full, (ic - 1) & 1u, p.wait_ns);
         }
     } else if (warp == C::W_QK) {
         // ===================================================== QK issue
@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
             if (item >= n_items) break;
             const PrefItem it = plan_prefill<GEN>(item, p);
             if (!it.seq_ok) continue;
-            if (!mbar_wait_bounded(bar_q_full, ic & 1u, kWaitLimitNs)) {
+            if (!mbar_wait_bounded(bar_q_full, ic & 1u, p.wait_ns)) {
                 abort = true;
                 break;
             }
@@ -293,8 +293,8 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
             for (int j = 0; j < it.T; ++j) {
                 const uint32_t s_ = sc + j, st = s_ % C::NSK, tcj = tc + j, b = tcj & 1u;
                 // K landed, and S buffer b is free: PV(tcj - 2) read the P it held
-                if (!mbar_wait_bounded(bar_k_full + 8 * st, (s_ / C::NSK) & 1u, kWaitLimitNs) ||
-                    (tcj >= 2 && !mbar_wait_bounded(bar_pv_done + 8 * b, ((tcj - 2) >> 1) & 1u, kWaitLimitNs))) {
+                if (!mbar_wait_bounded(bar_k_full + 8 * st, (s_ / C::NSK) & 1u, p.wait_ns) ||
+                    (tcj >= 2 && !mbar_wait_bounded(bar_pv_done + 8 * b, ((tcj - 2) >> 1) & 1u, p.wait_ns))) {
                     abort = true;
                     break;
                 }
@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
         // every MMA this thread issued is complete before TMEM is released
         if (lane == 0 && issued) {
             tc_commit(bar_final);
-            mbar_wait_bounded(bar_final, 0, kWaitLimitNs);
+            mbar_wait_bounded(bar_final, 0, p.wait_ns);
         }
         __syncwarp();
     } else if (warp == C::W_PV) {
@@ -346,9 +346,9 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
             for (int jj = 0; jj < it.T; ++jj) {
                 const uint32_t tcj = tc + jj, b = tcj & 1u;
                 const uint32_t s_ = sc + jj, st = s_ % C::NSV;
-                if (!mbar_wait_bounded(bar_p_full + 8 * b, (tcj >> 1) & 1u, kWaitLimitNs) ||
-                    !mbar_wait_bounded(bar_v_full + 8 * st, (s_ / C::NSV) & 1u, kWaitLimitNs) ||
-                    (jj == 0 && ic >= 1 && !mbar_wait_bounded(bar_o_free, (ic - 1) & 1u, kWaitLimitNs))) {
+                if (!mbar_wait_bounded(bar_p_full + 8 * b, (tcj >> 1) & 1u, p.wait_ns) ||
+                    !mbar_wait_bounded(bar_v_full + 8 * st, (s_ / C::NSV) & 1u, p.wait_ns) ||
+                    (jj == 0 && ic >= 1 && !mbar_wait_bounded(bar_o_free, (ic - 1) & 1u, p.wait_ns))) {
                     abort = true;
                     break;
                 }
@@ -390,7 +390,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
         }
         if (lane == 0 && issued) {
             tc_commit(bar_final + 8);
-            mbar_wait_bounded(bar_final + 8, 0, kWaitLimitNs);
+            mbar_wait_bounded(bar_final + 8, 0, p.wait_ns);
         }
         __syncwarp();
     } else {
@@ -432,7 +432,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
                 const uint32_t tcj = tc + j, b = tcj & 1u;
                 // (every exit from here is taken by the whole warp: the tcgen05
                 // loads and stores below are warp-collective)
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar_s_full + 8 * b, (tcj >> 1) & 1u, kWaitLimitNs))) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar_s_full + 8 * b, (tcj >> 1) & 1u, p.wait_ns))) {
                     abort = true;
                     break;
                 }
@@ -486,7 +486,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
                 if (__any_sync(0xffffffffu, need)) {
                     // PV of the previous tile must have landed before O is rescaled
                     const uint32_t tp = tcj - 1;   // the previous tile
-                    const bool ok = mbar_wait_bounded(bar_pv_done + 8 * (tp & 1u), (tp >> 1) & 1u, kWaitLimitNs);
+                    const bool ok = mbar_wait_bounded(bar_pv_done + 8 * (tp & 1u), (tp >> 1) & 1u, p.wait_ns);
                     if (!__all_sync(0xffffffffu, ok)) {
                         abort = true;
                         break;
@@ -539,7 +539,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
             }
             // ---- epilogue: O / l -> bf16
             const uint32_t tcl = tc + it.T - 1;
-            if (!mbar_wait_bounded(bar_pv_done + 8 * (tcl & 1u), (tcl >> 1) & 1u, kWaitLimitNs)) abort = true;
+            if (!mbar_wait_bounded(bar_pv_done + 8 * (tcl & 1u), (tcl >> 1) & 1u, p.wait_ns)) abort = true;
             tc_fence_after();
             const float inv = (bad || l_run == 0.f) ? 0.f : 1.f / l_run;
 #pragma unroll

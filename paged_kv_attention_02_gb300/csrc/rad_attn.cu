@@ -236,7 +236,8 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
                     int32_t head_dim, int32_t page_size, int32_t pages_per_seq, int32_t num_pages, float scale,
                     int32_t kv_dtype, const float* k_scales, const float* v_scales, int32_t window,
                     const int32_t* cu_seqlens, const uint32_t* tree_mask, int32_t total_rows, void* out,
-                    void* workspace, size_t workspace_bytes, uint32_t* err_word, rad_stream_t stream);
+                    void* workspace, size_t workspace_bytes, uint32_t* err_word, rad_stream_t stream,
+                    uint64_t wait_ns = rad::kWaitLimitNs, int fault = rad::kFaultNone);
 
 // Fields of a RadAttnPagedArgs that an older caller's struct_size leaves out read as zero.
 template <class T>
@@ -321,6 +322,23 @@ size_t rad_attn_paged_ex_workspace_bytes(const RadAttnPagedArgs* a) {
         .total_bytes;
 }
 
+int rad_attn_paged_fault_test(const RadAttnPagedArgs* a, uint64_t wait_limit_ns, int32_t fault,
+                              rad_stream_t stream) {
+    const int rc = check_ex_struct(a);
+    if (rc != RAD_OK) return rc;
+    if (wait_limit_ns != 0 && (wait_limit_ns < 1000000ull || wait_limit_ns > rad::kWaitLimitNs)) return RAD_E_ARG;
+    if (fault != RAD_FAULT_NONE && fault != RAD_FAULT_SKIP_FIRST_K_TILE) return RAD_E_ARG;
+    const int32_t window = ex_field(a, &RadAttnPagedArgs::window, offsetof(RadAttnPagedArgs, window));
+    const int32_t* cu = ex_field(a, &RadAttnPagedArgs::cu_seqlens, offsetof(RadAttnPagedArgs, cu_seqlens));
+    const uint32_t* tm = ex_field(a, &RadAttnPagedArgs::tree_mask, offsetof(RadAttnPagedArgs, tree_mask));
+    const int32_t total = ex_field(a, &RadAttnPagedArgs::total_rows, offsetof(RadAttnPagedArgs, total_rows));
+    return attn_paged_impl(a->q, a->k_pool, a->v_pool, a->page_table, a->seq_lens, a->groups, a->rows, a->n_head,
+                           a->n_head_kv, a->head_dim, a->page_size, a->pages_per_seq, a->num_pages, a->scale,
+                           a->kv_dtype, a->k_scales, a->v_scales, window, cu, tm, total, a->out, a->workspace,
+                           a->workspace_bytes, a->err_word, stream, wait_limit_ns ? wait_limit_ns : rad::kWaitLimitNs,
+                           fault == RAD_FAULT_SKIP_FIRST_K_TILE ? rad::kFaultSkipFirstKTile : rad::kFaultNone);
+}
+
 }  // extern "C"
 
 namespace {
@@ -330,7 +348,8 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
                     int32_t head_dim, int32_t page_size, int32_t pages_per_seq, int32_t num_pages, float scale,
                     int32_t kv_dtype, const float* k_scales, const float* v_scales, int32_t window,
                     const int32_t* cu_seqlens, const uint32_t* tree_mask, int32_t total_rows, void* out,
-                    void* workspace, size_t workspace_bytes, uint32_t* err_word, rad_stream_t stream) {
+                    void* workspace, size_t workspace_bytes, uint32_t* err_word, rad_stream_t stream,
+                    uint64_t wait_ns, int fault) {
     int rc = check_scalars(groups, rows, n_head, n_head_kv, head_dim, page_size, pages_per_seq, kv_dtype);
     if (rc != RAD_OK) return rc;
     if (num_pages <= 0 || (long long)num_pages * page_size > 0x7FFFFFFFll) return RAD_E_SHAPE;
@@ -352,6 +371,9 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
     if (tree_mask && window > 0) return RAD_E_ARG;    // tree rows take no sliding window
     if (pl.total_bytes > 0 && (!workspace || workspace_bytes < pl.total_bytes || !is_aligned(workspace, 256)))
         return RAD_E_WORKSPACE;
+    // an injected fault is honoured by the bf16 tcgen05 split kernel only
+    if (fault != rad::kFaultNone && (fault != rad::kFaultSkipFirstKTile || pl.family != rad::kFamSplitBf))
+        return RAD_E_ARG;
 
     int dev = 0, sms = 0;
     rc = device_info(&dev, &sms);
@@ -386,6 +408,8 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
     p.n_items = (int)pl.n_items;
     p.window = window;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.wait_ns = wait_ns;
+    p.fault = fault;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // decode-shaped sequences of a dual ragged call: the decode tile's own
     // tile list and partials

@@ -8,6 +8,7 @@
 // given inputs and outputs but no scratch buffer).  Neither may call cudaMalloc
 // per call: it would fail once the arena has reserved the device, or break the
 // one-time memory plan.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -24,20 +25,42 @@ constexpr int kMaxDevices = 64;
 // address: the device address comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[RAD_NOALLOC_SCRATCH_BYTES];
 
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
 std::mutex g_setup_mutex;
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+// Per device: the context the address was looked up in, and the address.  A
+// device reset (or a released and re-created primary context) loads the
+// module again, possibly elsewhere, so a changed context means a new lookup.
+CUcontext g_scratch_ctx[kMaxDevices] = {};
 void* g_scratch_addr[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device, looked up once
-// per device (with that device current).  Returns RAD_OK or RAD_E_CUDA.
+// Device address of the scratch array in the current device's current
+// context, looked up (with that device current) the first time and again
+// whenever the context has changed.  Returns RAD_OK or RAD_E_CUDA.
 int scratch_address(void** addr) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return RAD_E_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return RAD_E_DEVICE;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (g_scratch_addr[dev] == nullptr) {
+    if (g_ctx_get_current == nullptr) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return RAD_E_CUDA;
+        g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+    }
+    // no current context yet (the runtime has not touched the device): the
+    // lookup below makes the device's primary context current
+    CUcontext ctx = nullptr;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS) return RAD_E_CUDA;
+    if (ctx == nullptr || g_scratch_addr[dev] == nullptr || g_scratch_ctx[dev] != ctx) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return RAD_E_CUDA;
+        if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return RAD_E_CUDA;
         g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     *addr = g_scratch_addr[dev];
     return RAD_OK;

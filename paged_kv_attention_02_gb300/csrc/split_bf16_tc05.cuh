@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
                     }
                 }
                 const uint32_t st = sc % (uint32_t)NSX, use = sc / (uint32_t)NSX;
-                if (use >= 1 && !mbar_wait_bounded(bar_empty + 8 * st, (use - 1) & 1u, kWaitLimitNs)) {
+                if (use >= 1 && !mbar_wait_bounded(bar_empty + 8 * st, (use - 1) & 1u, p.wait_ns)) {
                     abort = true;
                     break;
                 }
@@ -243,9 +243,11 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
                         reinterpret_cast<uint32_t*>(smem + C::OFF_META + st * C::META_STRIDE)[16] =
                             bad_any ? kErrPage : 0u;
                 }
-                if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * st, (uint32_t)C::KV_TILE);
+                // (a test's injected fault: CTA 0 leaves its first K tile unissued)
+                const bool skip = is_k && p.fault == kFaultSkipFirstKTile && blockIdx.x == 0 && sc == 0;
+                if (lane == 0 && !skip) mbar_arrive_expect_tx(bar_full + 8 * st, (uint32_t)C::KV_TILE);
                 __syncwarp();
-                if (mine)
+                if (mine && !skip)
                     tma_load_3d(ring + st * C::KV_TILE + (uint32_t)(blk * C::BLK + pl * P * 128), tm,
                                 bar_full + 8 * st, blk * 64, it.kvh, live ? pg * P : oob_tok, pol_kv);
                 __syncwarp();
@@ -257,7 +259,7 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
         if (lane == 0) {
             const uint32_t first = sc > (uint32_t)NSX ? sc - NSX : 0u;
             for (uint32_t c = first; c < sc; ++c)
-                mbar_wait_bounded(bar_full + 8 * (c % NSX), (c / NSX) & 1u, kWaitLimitNs);
+                mbar_wait_bounded(bar_full + 8 * (c % NSX), (c / NSX) & 1u, p.wait_ns);
         }
         __syncwarp();
     } else if (warp == C::W_Q) {
@@ -276,7 +278,7 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i)
                 qv[i] = valid ? __ldg(reinterpret_cast<const uint4*>(qrow) + i) : make_uint4(0u, 0u, 0u, 0u);
-            if (ic >= 1 && !__all_sync(0xffffffffu, mbar_wait_bounded(bar_q_empty, (ic - 1) & 1u, kWaitLimitNs))) {
+            if (ic >= 1 && !__all_sync(0xffffffffu, mbar_wait_bounded(bar_q_empty, (ic - 1) & 1u, p.wait_ns))) {
                 abort = true;
                 break;
             }
@@ -308,7 +310,7 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
             const ItemPlan it = plan_item<C, WIN>(item, p);
             if (!real(it)) continue;
             const int T = it.n_stages;
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar_q_full, ic & 1u, kWaitLimitNs))) {
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar_q_full, ic & 1u, p.wait_ns))) {
                 abort = true;
                 break;
             }
@@ -316,8 +318,8 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
             for (int j = 0; j < T; ++j) {
                 const uint32_t tcj = tc + j, b = tcj & 1u, sk = tcj % C::NSK;
                 // K landed, and S/P buffer b is free: PV(tcj - 2) is done
-                bool ok = mbar_wait_bounded(bar_k_full + 8 * sk, (tcj / C::NSK) & 1u, kWaitLimitNs);
-                if (ok && tcj >= 2) ok = mbar_wait_bounded(bar_pv_done + 8 * b, ((tcj - 2) >> 1) & 1u, kWaitLimitNs);
+                bool ok = mbar_wait_bounded(bar_k_full + 8 * sk, (tcj / C::NSK) & 1u, p.wait_ns);
+                if (ok && tcj >= 2) ok = mbar_wait_bounded(bar_pv_done + 8 * b, ((tcj - 2) >> 1) & 1u, p.wait_ns);
                 if (!__all_sync(0xffffffffu, ok)) {
                     abort = true;
                     break;
@@ -347,7 +349,7 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
         // every MMA this thread issued is complete before TMEM is released
         if (lane == 0 && issued) {
             tc_commit(bar_final);
-            mbar_wait_bounded(bar_final, 0, kWaitLimitNs);
+            mbar_wait_bounded(bar_final, 0, p.wait_ns);
         }
         __syncwarp();
     } else if (warp == C::W_PV) {
@@ -364,10 +366,10 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
                 // P_j written, V_j landed, and at an item's first tile its O buffer read out
                 // (the item two before)
                 const uint32_t t_ob = t_o + 128 * (ic & 1u);
-                bool ok = mbar_wait_bounded(bar_p_full + 8 * b, (tcj >> 1) & 1u, kWaitLimitNs);
-                if (ok) ok = mbar_wait_bounded(bar_v_full + 8 * sv, (tcj / C::NSV) & 1u, kWaitLimitNs);
+                bool ok = mbar_wait_bounded(bar_p_full + 8 * b, (tcj >> 1) & 1u, p.wait_ns);
+                if (ok) ok = mbar_wait_bounded(bar_v_full + 8 * sv, (tcj / C::NSV) & 1u, p.wait_ns);
                 if (ok && j == 0 && ic >= 2)
-                    ok = mbar_wait_bounded(bar_o_free + 8 * (ic & 1u), ((ic - 2) >> 1) & 1u, kWaitLimitNs);
+                    ok = mbar_wait_bounded(bar_o_free + 8 * (ic & 1u), ((ic - 2) >> 1) & 1u, p.wait_ns);
                 if (!__all_sync(0xffffffffu, ok)) {
                     abort = true;
                     break;
@@ -410,7 +412,7 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
         }
         if (lane == 0 && issued) {
             tc_commit(bar_final + 8);
-            mbar_wait_bounded(bar_final + 8, 0, kWaitLimitNs);
+            mbar_wait_bounded(bar_final + 8, 0, p.wait_ns);
         }
         __syncwarp();
     } else if (warp >= C::W_EPI) {
@@ -429,8 +431,8 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
             if (!real(it)) continue;
             // the item's last PV done and the softmax warps' hand-off
             const uint32_t ob = ic & 1u;
-            bool ok = mbar_wait_bounded(bar_o_full + 8 * ob, (ic >> 1) & 1u, kWaitLimitNs);
-            if (ok) ok = mbar_wait_bounded(bar_ml_full + 8 * ob, (ic >> 1) & 1u, kWaitLimitNs);
+            bool ok = mbar_wait_bounded(bar_o_full + 8 * ob, (ic >> 1) & 1u, p.wait_ns);
+            if (ok) ok = mbar_wait_bounded(bar_ml_full + 8 * ob, (ic >> 1) & 1u, p.wait_ns);
             if (named_barrier_or(2, 128, !__all_sync(0xffffffffu, ok) || misc[1] != 0)) {   // all leave together
                 abort = true;
                 break;
@@ -604,8 +606,8 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
                 const uint32_t tcj = tc + j, b = tcj & 1u, sk = tcj % C::NSK;
                 // S_j landed, and the K stage's scales are visible (QK waited for its K-full
                 // phase); the stage is released after the reads
-                bool ok = mbar_wait_bounded(bar_s_full + 8 * b, (tcj >> 1) & 1u, kWaitLimitNs);
-                if (ok) ok = mbar_wait_bounded(bar_k_full + 8 * sk, (tcj / C::NSK) & 1u, kWaitLimitNs);
+                bool ok = mbar_wait_bounded(bar_s_full + 8 * b, (tcj >> 1) & 1u, p.wait_ns);
+                if (ok) ok = mbar_wait_bounded(bar_k_full + 8 * sk, (tcj / C::NSK) & 1u, p.wait_ns);
                 if (!__all_sync(0xffffffffu, ok)) {
                     abort = true;
                     break;
@@ -657,7 +659,7 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
                 }
                 if (__any_sync(0xffffffffu, need)) {
                     const uint32_t tp = tcj - 1;   // the previous tile's PV
-                    const bool okw = j == 0 || mbar_wait_bounded(bar_pv_done + 8 * (tp & 1u), (tp >> 1) & 1u, kWaitLimitNs);
+                    const bool okw = j == 0 || mbar_wait_bounded(bar_pv_done + 8 * (tp & 1u), (tp >> 1) & 1u, p.wait_ns);
                     if (!__all_sync(0xffffffffu, okw)) {
                         abort = true;
                         break;
@@ -724,7 +726,7 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
             // slot and O buffer are this item's)
             const uint32_t ob = ic & 1u;
             if (ic >= 2 &&
-                !__all_sync(0xffffffffu, mbar_wait_bounded(bar_o_free + 8 * ob, ((ic - 2) >> 1) & 1u, kWaitLimitNs))) {
+                !__all_sync(0xffffffffu, mbar_wait_bounded(bar_o_free + 8 * ob, ((ic - 2) >> 1) & 1u, p.wait_ns))) {
                 abort = true;
                 break;
             }

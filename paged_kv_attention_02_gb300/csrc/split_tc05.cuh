@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
                     }
                 }
                 const uint32_t st = sc % (uint32_t)NSX, use = sc / (uint32_t)NSX;
-                if (use >= 1 && !mbar_wait_bounded(bar_empty + 8 * st, (use - 1) & 1u, kWaitLimitNs)) {
+                if (use >= 1 && !mbar_wait_bounded(bar_empty + 8 * st, (use - 1) & 1u, p.wait_ns)) {
                     abort = true;
                     break;
                 }
@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
         if (lane == 0) {
             const uint32_t first = sc > (uint32_t)NSX ? sc - NSX : 0u;
             for (uint32_t c = first; c < sc; ++c)
-                mbar_wait_bounded(bar_full + 8 * (c % NSX), (c / NSX) & 1u, kWaitLimitNs);
+                mbar_wait_bounded(bar_full + 8 * (c % NSX), (c / NSX) & 1u, p.wait_ns);
         }
         __syncwarp();
     } else if (warp >= C::W_CONV) {
@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
             if (!real(it)) continue;
             // ---- this copy of the item's query rows as two e4m3 terms, once the
             // previous item's QKs are done and the softmax warps have read its 2^-k
-            if (ic >= 1 && !__all_sync(0xffffffffu, mbar_wait_bounded(bar_q8_empty, (ic - 1) & 1u, kWaitLimitNs))) {
+            if (ic >= 1 && !__all_sync(0xffffffffu, mbar_wait_bounded(bar_q8_empty, (ic - 1) & 1u, p.wait_ns))) {
                 abort = true;
                 break;
             }
@@ -374,9 +374,9 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
             // ---- this converter's rows of every V tile of the item
             for (int j = 0; j < it.n_stages; ++j) {
                 const uint32_t tcj = tc + j, b = tcj & 1u, sv = tcj % C::NSV;
-                bool ok = mbar_wait_bounded(bar_v_full + 8 * sv, (tcj / C::NSV) & 1u, kWaitLimitNs);
+                bool ok = mbar_wait_bounded(bar_v_full + 8 * sv, (tcj / C::NSV) & 1u, p.wait_ns);
                 // f16 buffer b was last read by PV(tcj - 2) (waited at every tile, in order)
-                if (ok && tcj >= 2) ok = mbar_wait_bounded(bar_pv_done + 8 * b, ((tcj - 2) >> 1) & 1u, kWaitLimitNs);
+                if (ok && tcj >= 2) ok = mbar_wait_bounded(bar_pv_done + 8 * b, ((tcj - 2) >> 1) & 1u, p.wait_ns);
                 if (!__all_sync(0xffffffffu, ok)) {
                     abort = true;
                     break;
@@ -404,7 +404,7 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
             const ItemPlan it = plan_item<C, WIN>(item, p);
             if (!real(it)) continue;
             const int T = it.n_stages;
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar_q8_full, ic & 1u, kWaitLimitNs))) {
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar_q8_full, ic & 1u, p.wait_ns))) {
                 abort = true;
                 break;
             }
@@ -412,8 +412,8 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
             for (int j = 0; j < T; ++j) {
                 const uint32_t tcj = tc + j, b = tcj & 1u, sk = tcj % C::NSK;
                 // K landed, and the S and P buffers b are free: PV(tcj - 2) is done
-                bool ok = mbar_wait_bounded(bar_k_full + 8 * sk, (tcj / C::NSK) & 1u, kWaitLimitNs);
-                if (ok && tcj >= 2) ok = mbar_wait_bounded(bar_pv_done + 8 * b, ((tcj - 2) >> 1) & 1u, kWaitLimitNs);
+                bool ok = mbar_wait_bounded(bar_k_full + 8 * sk, (tcj / C::NSK) & 1u, p.wait_ns);
+                if (ok && tcj >= 2) ok = mbar_wait_bounded(bar_pv_done + 8 * b, ((tcj - 2) >> 1) & 1u, p.wait_ns);
                 if (!__all_sync(0xffffffffu, ok)) {
                     abort = true;
                     break;
@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
         // every MMA this thread issued is complete before TMEM is released
         if (lane == 0 && issued) {
             tc_commit(bar_final);
-            mbar_wait_bounded(bar_final, 0, kWaitLimitNs);
+            mbar_wait_bounded(bar_final, 0, p.wait_ns);
         }
         __syncwarp();
     } else if (warp == C::W_PV) {
@@ -458,9 +458,9 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
             for (int j = 0; j < T; ++j) {
                 const uint32_t tcj = tc + j, b = tcj & 1u;
                 // P_j written, V_j converted, and at an item's first tile the previous item's O read out
-                bool ok = mbar_wait_bounded(bar_p_full + 8 * b, (tcj >> 1) & 1u, kWaitLimitNs);
-                if (ok) ok = mbar_wait_bounded(bar_v16_full + 8 * b, (tcj >> 1) & 1u, kWaitLimitNs);
-                if (ok && j == 0 && ic >= 1) ok = mbar_wait_bounded(bar_o_free, (ic - 1) & 1u, kWaitLimitNs);
+                bool ok = mbar_wait_bounded(bar_p_full + 8 * b, (tcj >> 1) & 1u, p.wait_ns);
+                if (ok) ok = mbar_wait_bounded(bar_v16_full + 8 * b, (tcj >> 1) & 1u, p.wait_ns);
+                if (ok && j == 0 && ic >= 1) ok = mbar_wait_bounded(bar_o_free, (ic - 1) & 1u, p.wait_ns);
                 if (!__all_sync(0xffffffffu, ok)) {
                     abort = true;
                     break;
@@ -483,7 +483,7 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
         }
         if (lane == 0 && issued) {
             tc_commit(bar_final + 8);
-            mbar_wait_bounded(bar_final + 8, 0, kWaitLimitNs);
+            mbar_wait_bounded(bar_final + 8, 0, p.wait_ns);
         }
         __syncwarp();
     } else {
@@ -561,7 +561,7 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
                 tmw = valid ? __ldg(p.tree_mask + it.qrow0 + tok) : 0u;
             }
             // the rows' 2^-k, from the converters' split of this item's query rows
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar_q8_full, ic & 1u, kWaitLimitNs))) abort = true;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar_q8_full, ic & 1u, p.wait_ns))) abort = true;
             if (named_barrier_or(1, 128, abort)) {   // all four warps leave together
                 abort = true;
                 break;
@@ -581,8 +581,8 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
                 const uint32_t tcj = tc + j, b = tcj & 1u, sk = tcj % C::NSK;
                 // S_j landed, and the K stage's scales are visible (QK waited for its K-full
                 // phase); the stage is released after the reads
-                bool ok = mbar_wait_bounded(bar_s_full + 8 * b, (tcj >> 1) & 1u, kWaitLimitNs);
-                if (ok) ok = mbar_wait_bounded(bar_k_full + 8 * sk, (tcj / C::NSK) & 1u, kWaitLimitNs);
+                bool ok = mbar_wait_bounded(bar_s_full + 8 * b, (tcj >> 1) & 1u, p.wait_ns);
+                if (ok) ok = mbar_wait_bounded(bar_k_full + 8 * sk, (tcj / C::NSK) & 1u, p.wait_ns);
                 if (!__all_sync(0xffffffffu, ok)) {
                     abort = true;
                     break;
@@ -638,7 +638,7 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
                 }
                 if (__any_sync(0xffffffffu, need)) {
                     const uint32_t tp = tcj - 1;   // the previous tile's PV
-                    const bool okw = j == 0 || mbar_wait_bounded(bar_pv_done + 8 * (tp & 1u), (tp >> 1) & 1u, kWaitLimitNs);
+                    const bool okw = j == 0 || mbar_wait_bounded(bar_pv_done + 8 * (tp & 1u), (tp >> 1) & 1u, p.wait_ns);
                     if (!__all_sync(0xffffffffu, okw)) {
                         abort = true;
                         break;
@@ -686,7 +686,7 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
             }
             // ---- epilogue: the four quarters' (max, sum, O) of row r, merged in warp order
             const uint32_t tcl = tc + T - 1;
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar_pv_done + 8 * (tcl & 1u), (tcl >> 1) & 1u, kWaitLimitNs)))
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar_pv_done + 8 * (tcl & 1u), (tcl >> 1) & 1u, p.wait_ns)))
                 abort = true;
             tc_fence_after();
             if (named_barrier_or(1, 128, abort)) {   // all four warps leave together

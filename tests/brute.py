@@ -20,7 +20,14 @@ definition with explicit positions:
 """
 import math
 
-from trees import path_of
+
+def _path(parents, r):
+    """Node r and its ancestors, walked up the parents list to the context."""
+    nodes = []
+    while r >= 0:
+        nodes.append(r)
+        r = parents[r]
+    return nodes
 
 
 def attend_sequence(q_rows, keys, values, scale, n_head_kv, window=0, parents=None):
@@ -38,7 +45,7 @@ def attend_sequence(q_rows, keys, values, scale, n_head_kv, window=0, parents=No
         first = max(0, position - window + 1) if window > 0 else 0
         visible = range(first, position + 1)
         if parents is not None:
-            visible = list(range(L - R)) + sorted(L - R + i for i in path_of(parents, r))
+            visible = list(range(L - R)) + sorted(L - R + i for i in _path(parents, r))
         row_out = []
         for h in range(H):
             kvh = h // group

@@ -136,16 +136,22 @@ def test_full_size_sampled_rows_match_oracle(full, name):
     c = w.cfg
     rng = np.random.default_rng(7)
     n = 48
-    sel = np.stack([rng.integers(0, w.groups, n), rng.integers(0, c.rows, n),
-                    rng.integers(0, c.n_head, n)], axis=1)
-    sel[0] = (int(np.argmax(w.seq_lens)), c.rows - 1, c.n_head - 1)     # the longest row
-    sel[1] = (int(np.argmin(w.seq_lens)), 0, 0)                         # the shortest
+    rand = np.stack([rng.integers(0, w.groups, n), rng.integers(0, c.rows, n),
+                     rng.integers(0, c.n_head, n)], axis=1)
+    # one row of every sequence (so every context length is checked once), and
+    # every head of the longest sequence's last row and of the shortest's first
+    each = np.stack([np.arange(w.groups), rng.integers(0, c.rows, w.groups),
+                     rng.integers(0, c.n_head, w.groups)], axis=1)
+    heads = np.arange(c.n_head)
+    longest = np.stack([np.full(c.n_head, int(np.argmax(w.seq_lens))), np.full(c.n_head, c.rows - 1), heads], axis=1)
+    shortest = np.stack([np.full(c.n_head, int(np.argmin(w.seq_lens))), np.zeros(c.n_head, int), heads], axis=1)
+    sel = np.concatenate([rand, each, longest, shortest]).astype(np.int64)
     ref = oracle_rows(w, sel)
     got = o[sel[:, 0], sel[:, 1], sel[:, 2]]
     assert_parity(got, ref.out, dw.fp8, name)
 
 
-@pytest.mark.parametrize("name", ["batched_decode", "spec_verify"])
+@pytest.mark.parametrize("name", ["batched_decode", "hybrid_decode", "spec_verify"])
 def test_full_size_rows_are_bit_identical_across_batch_compositions(full, name):
     w, dw = full(name)
     out, _ = dw.run()
@@ -171,6 +177,29 @@ def test_full_size_rows_are_bit_identical_across_batch_compositions(full, name):
     for i, g in enumerate(order):
         if g >= 0:
             assert np.array_equal(ob[i], base[g]), f"group {g} in a shuffled padded batch"
+
+
+def test_full_size_prefill_chunk_is_bit_identical_alone_and_batched(full):
+    # The 2048-row chunk over 8192 keys alone, and the same sequence as the
+    # second group of a two-group call whose first group is another chunk of
+    # 2048 rows (zero queries, the same pages, seq_len 2048): its rows must not
+    # change with the other group.
+    w, dw = full("prefill_chunk")
+    alone, err = dw.run()
+    assert err == 0
+    R = w.cfg.rows
+    q = torch.cat([torch.zeros_like(dw.q), dw.q])
+    table = torch.cat([dw.table, dw.table])
+    lens = torch.tensor([R, int(w.seq_lens[0])], dtype=torch.int32, device="cuda")
+    both, err = dw.run(q=q, table=table, lens=lens)
+    assert err == 0
+    assert np.array_equal(bits(both)[1], bits(alone)[0])
+    # and with the real sequence first, the padding group after it
+    q = torch.cat([dw.q, torch.zeros_like(dw.q)])
+    lens = torch.tensor([int(w.seq_lens[0]), R], dtype=torch.int32, device="cuda")
+    both, err = dw.run(q=q, table=table, lens=lens)
+    assert err == 0
+    assert np.array_equal(bits(both)[0], bits(alone)[0])
 
 
 @pytest.mark.parametrize("name", ["prefill", "prefill_fp8", "prefill_fp8_r1"])

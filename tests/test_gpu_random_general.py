@@ -16,7 +16,7 @@ import pytest
 from gpu_util import DevWorkload, assert_parity
 from paged_kv_attention_02_gb300 import workloads as wl
 from test_gpu_tree import SENTINEL, as_float, named_rows, oracle_general, ragged_q, run_general
-from trees import mask_words, random_parents
+from paged_kv_attention_02_gb300.workloads import mask_words, random_parents
 
 pytestmark = pytest.mark.gpu
 

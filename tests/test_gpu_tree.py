@@ -17,7 +17,7 @@ import oracle
 from gpu_util import DevWorkload, as_f64, assert_parity, bf16_tensor, bits
 from paged_kv_attention_02_gb300 import binding as b
 from paged_kv_attention_02_gb300 import workloads as wl
-from trees import chain, mask_words, random_parents
+from paged_kv_attention_02_gb300.workloads import chain, mask_words, random_parents
 
 pytestmark = pytest.mark.gpu
 

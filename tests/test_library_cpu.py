@@ -258,3 +258,32 @@ def test_compact_pool_keeps_the_call():
     c = oracle.attn_paged(small.q, small.k_pool, small.v_pool, small.page_table, small.seq_lens,
                           **small.call_args()).out
     assert np.array_equal(a, c)
+
+
+def _fault_args(**over):
+    """A RadAttnPagedArgs with fake, aligned device pointers (never touched:
+    every case below is refused by the host checks)."""
+    g = good_args(**over)
+    a = b.shape_args(g["groups"], g["rows"], g["n_head"], g["n_head_kv"], g["head_dim"], g["page_size"],
+                     g["pages_per_seq"], g["kv_dtype"])
+    a.cu_seqlens = a.tree_mask = None
+    a.q, a.k_pool, a.v_pool = g["q_ptr"], g["k_ptr"], g["v_ptr"]
+    a.page_table, a.seq_lens, a.out = g["table_ptr"], g["lens_ptr"], g["out_ptr"]
+    a.num_pages, a.scale = g["num_pages"], g["scale"]
+    a.k_scales, a.v_scales = (4096, 4096) if g["kv_dtype"] == b.RAD_KV_FP8_E4M3 else (None, None)
+    a.workspace, a.workspace_bytes = g["ws_ptr"], g["ws_bytes"]
+    return a
+
+
+@pytest.mark.parametrize("limit,fault,over", [
+    (5, b.RAD_FAULT_NONE, {}),                                       # a limit below 1 ms
+    (3_000_000_000, b.RAD_FAULT_NONE, {}),                           # above the 2 s default
+    (0, 7, {}),                                                      # an unknown fault
+    (0, b.RAD_FAULT_SKIP_FIRST_K_TILE, dict(kv_dtype=b.RAD_KV_FP8_E4M3)),   # e4m3 pools: not honoured
+    (0, b.RAD_FAULT_SKIP_FIRST_K_TILE, dict(head_dim=256)),          # head_dim 256: not honoured
+    (0, b.RAD_FAULT_SKIP_FIRST_K_TILE, dict(rows=300)),              # a prefill chunk: not honoured
+])
+def test_fault_test_hook_refuses_what_it_cannot_honour(limit, fault, over):
+    lib = b.load()
+    a = _fault_args(**over)
+    assert lib.rad_attn_paged_fault_test(ctypes.byref(a), limit, fault, None) == b.RAD_E_ARG

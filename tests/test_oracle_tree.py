@@ -19,7 +19,7 @@ import pytest
 import oracle
 from brute import attend_sequence
 from test_oracle import bf16_bits, bf16_values, e4m3_values, paged_from_logical, random_case, run_oracle
-from trees import mask_words, path_of, random_parents
+from paged_kv_attention_02_gb300.workloads import mask_words, path_of, random_parents
 
 
 def logical_kv(c, g, P, fp8):
