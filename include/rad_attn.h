@@ -120,8 +120,11 @@ enum {
  * (0 is possible).  A pure function of its arguments; no device access.
  * Returns 0 as well for shapes rad_attn_paged would refuse.  The workspace
  * holds per-split partial results ("kern manifest v7", $defs.Impl `scratch`:
- * implementation-private buffers) and is dead between calls; calls that may
- * run concurrently need separate workspaces.
+ * implementation-private buffers) and, for the tcgen05 split kernels, a work
+ * counter that the call zeroes with a 4-byte cudaMemsetAsync on its stream
+ * before the kernel (stream-ordered, so it is captured with the call in a CUDA
+ * graph).  It is dead between calls; calls that may run concurrently need
+ * separate workspaces.
  */
 size_t rad_attn_paged_workspace_bytes(int32_t groups, int32_t rows, int32_t n_head,
                                       int32_t n_head_kv, int32_t head_dim, int32_t page_size,
@@ -245,9 +248,9 @@ int rad_attn_paged_window(const void* q, const void* k_pool, const void* v_pool,
  *                small kernel that maps its query tiles into the workspace.
  *
  * Calls with cu_seqlens or tree_mask run on the same kernel family as a
- * uniform call of their shape when head_dim is 128 (the tcgen05 split kernels
- * for calls of at most 256 rows), else on the mma.sync tile kernels, so their
- * rows keep the uniform call's bits; their workspace need is
+ * uniform call of their shape when head_dim is 128 or the pools are bf16 (the
+ * tcgen05 split kernels for calls of at most 256 rows), else on the mma.sync
+ * tile kernels, so their rows keep the uniform call's bits; their workspace need is
  * rad_attn_paged_ex_workspace_bytes(args), which may differ from
  * rad_attn_paged_workspace_bytes() of the same shape.
  * Returns the status rad_attn_paged_window returns for the same arguments,
@@ -304,7 +307,7 @@ int rad_attn_paged_ex_describe(const RadAttnPagedArgs* args, char* buf, size_t b
  *                  roles (copies in flight drained, tensor memory freed) and
  *                  returns, leaving that CTA's rows unwritten.
  * The fault is honoured only by calls that run on the bf16 tcgen05 split
- * kernel (split calls with head_dim 128 over bf16 pools); any other call
+ * kernel (split calls over bf16 pools, either head_dim); any other call
  * with a fault, an unknown fault or a limit outside the range returns
  * RAD_E_ARG and launches nothing.  Nothing here is meant for production use.
  */

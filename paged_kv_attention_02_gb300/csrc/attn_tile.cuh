@@ -116,6 +116,7 @@ struct AttnParams {
     float scale_log2;      // scale * log2(e)
     uint64_t wait_ns;      // limit of each bounded wait (kWaitLimitNs unless a test lowers it)
     int fault;             // kFaultNone, or a test's injected fault
+    uint32_t* sched_ctr;   // tcgen05 split kernels: the shared item counter (zero at launch), or null
 };
 
 // First key that query row r of a call with `rows` rows over a sequence of

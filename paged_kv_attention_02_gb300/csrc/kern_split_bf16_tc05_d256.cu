@@ -1,0 +1,19 @@
+// Launcher of the tcgen05 split kernel for bf16 KV pools with head_dim 256
+// (decode and verify calls) and of the split combine after it.
+#include <cuda_runtime.h>
+
+#include "launch.cuh"
+#include "split_bf16_tc05.cuh"
+#include "tile_configs.cuh"
+
+namespace rad {
+
+cudaError_t launch_split_bf16_tc05_d256(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
+                                        cudaStream_t st, bool few) {
+    const cudaError_t e = few ? launch_split_bf16_form<true, 256>(tk, tv, p, sms, st)
+                              : launch_split_bf16_form<false, 256>(tk, tv, p, sms, st);
+    if (e != cudaSuccess || p.max_splits <= 1) return e;
+    return launch_combine<256>(p, st);
+}
+
+}  // namespace rad

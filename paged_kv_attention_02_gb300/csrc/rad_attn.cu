@@ -41,7 +41,7 @@ struct Plan {
     bool ragged;       // items and partial slots run over the call's query tiles (a tile map)
     rad::TileInfo tile;
     long long n_items;
-    size_t map_bytes, flags_bytes, ml_bytes, acc_bytes, total_bytes;
+    size_t sched_bytes, map_bytes, flags_bytes, ml_bytes, acc_bytes, total_bytes;
     // A ragged call whose family is the verify or wide tile runs its
     // decode-shaped sequences (at most the decode tile's rows per KV head) on
     // the decode tile instead, as a second tile list: `dec`.  The two tiles
@@ -82,8 +82,9 @@ bool use_prefill_tc(int32_t rows, int32_t ratio, int32_t head_dim, int32_t kv_dt
 }
 
 // `general`: a call with ragged rows (cu_seqlens) or tree masks.  Split calls
-// with head_dim 128 run on the tcgen05 split kernels whether ragged or not,
-// with or without tree masks; the others on the tile kernels.  `ragged_rows`
+// with head_dim 128 (both pool types) or with bf16 pools (both head dims) run
+// on the tcgen05 split kernels whether ragged or not, with or without tree
+// masks; the others on the tile kernels.  `ragged_rows`
 // >= 0 marks a ragged call: its work and workspace run
 // over the call's query tiles, bounded with the caller's total of rows when
 // it gives one (> 0), else with `rows` rows per sequence.
@@ -103,9 +104,10 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
         pl.family = rad::kFamSplitTC;
         pl.split_len = rad::kSplitLenTC;
     }
-    else if (pl.split_len > 0 && RAD_SPLIT_BF16_TC05 && head_dim == 128 && kv_dtype == RAD_KV_BF16) {
+    else if (pl.split_len > 0 && kv_dtype == RAD_KV_BF16 &&
+             (head_dim == 128 ? RAD_SPLIT_BF16_TC05 : RAD_SPLIT_BF16_TC05_D256)) {
         pl.family = rad::kFamSplitBf;
-        pl.split_len = rad::kSplitLenTC;
+        pl.split_len = head_dim == 128 ? rad::kSplitLenTC : rad::kSplitLenTC256;
     }
     else if (pl.split_len > 0)
         pl.family = pl.M <= 8 ? rad::kFamDecode : rad::kFamVerify;
@@ -118,7 +120,7 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
     else if (pl.family == rad::kFamSplitTC)
         pl.tile = rad::split_tc05_info(pl.M <= 8);
     else if (pl.family == rad::kFamSplitBf)
-        pl.tile = rad::split_bf16_tc05_info(pl.M <= 8);
+        pl.tile = rad::split_bf16_tc05_info(pl.M <= 8, head_dim);
     else
         pl.tile = tile_for(head_dim, kv_dtype, pl.family);
     pl.n_qtiles = (pl.M + pl.tile.QT - 1) / pl.tile.QT;
@@ -146,7 +148,9 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
         pl.ml_bytes = round_up((size_t)slots * pl.qtv * 2 * 4, 256);
         pl.acc_bytes = round_up((size_t)slots * pl.qtv * head_dim * 4, 256);
     }
-    pl.total_bytes = pl.map_bytes + pl.flags_bytes + pl.ml_bytes + pl.acc_bytes;
+    // the tcgen05 split kernels' shared item counter (zeroed before each launch that uses it)
+    if (pl.family == rad::kFamSplitBf) pl.sched_bytes = 256;
+    pl.total_bytes = pl.sched_bytes + pl.map_bytes + pl.flags_bytes + pl.ml_bytes + pl.acc_bytes;
     pl.dual = pl.ragged && (pl.family == rad::kFamVerify || pl.family == rad::kFamWide);
     if (pl.dual) {
         Plan::Part& d = pl.dec;
@@ -414,8 +418,12 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
     // decode-shaped sequences of a dual ragged call: the decode tile's own
     // tile list and partials
     AttnParams pd = p;
+    // a kernel with more items than CTAs takes them from a shared counter
+    const bool dynamic = RAD_SPLIT_DYNAMIC && pl.sched_bytes > 0 && pl.n_items > sms;
     if (pl.total_bytes > 0) {
         char* ws = static_cast<char*>(workspace);
+        if (dynamic) p.sched_ctr = reinterpret_cast<uint32_t*>(ws);
+        ws += pl.sched_bytes;
         if (pl.ragged) p.tile_map = reinterpret_cast<const int2*>(ws);
         ws += pl.map_bytes;
         if (pl.split_len > 0) {
@@ -441,6 +449,7 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
         }
     }
     cudaError_t e;
+    if (dynamic && cudaMemsetAsync(p.sched_ctr, 0, sizeof(uint32_t), st) != cudaSuccess) return RAD_E_CUDA;
     if (pl.ragged) {
         // the tile lists of the call's sequence classes, on the device
         rad::RaggedMaps m{};
@@ -486,7 +495,8 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
         CUtensorMap tk, tv;
         if (encode_bf16_map(&tk, k_pool, 3, kd, ks, kb) != RAD_OK || encode_bf16_map(&tv, v_pool, 3, kd, ks, kb) != RAD_OK)
             return RAD_E_CUDA;
-        e = rad::launch_split_bf16_tc05(tk, tv, p, sms, st, pl.M <= 8);
+        e = head_dim == 128 ? rad::launch_split_bf16_tc05(tk, tv, p, sms, st, pl.M <= 8)
+                            : rad::launch_split_bf16_tc05_d256(tk, tv, p, sms, st, pl.M <= 8);
     } else if (pl.family == rad::kFamPrefillTC) {
         rc = get_encoder();
         if (rc != RAD_OK) return rc;
@@ -540,10 +550,11 @@ int describe_call(int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_
         snprintf(buf, buf_len,
                  "%sattn_split_bf16_tc05 family=%s head_dim=%d kv=bf16 query_rows_per_kv_head=%d tile_rows=%d "
                  "keys_per_tile=%d stages=%d ctas_per_sm=1 warps=13 4 softmax (a quarter of each tile's keys "
-                 "each)+1 qk+1 pv+2 tma producers+1 query rows+4 epilogue (two O buffers) mma=tcgen05 (query rows as M, four copies; keys as "
+                 "each)+1 qk+1 pv+2 tma producers+1 query rows+4 epilogue (%s) mma=tcgen05 (query rows as M, four copies; keys as "
                  "N; QK kind::f16 bf16, PV kind::f16 with P from TMEM as bf16 hi+lo over S) "
                  "split_len=%d + attn_combine (split order)",
-                 pre, family_name(pl.family), head_dim, pl.M, t.QT, t.KS, t.NS, pl.split_len);
+                 pre, family_name(pl.family), head_dim, pl.M, t.QT, t.KS, t.NS,
+                 head_dim == 128 ? "two O buffers" : "one O buffer", pl.split_len);
         return RAD_OK;
     }
     if (pl.family == rad::kFamPrefillTC && kv_dtype == RAD_KV_FP8_E4M3) {

@@ -1,0 +1,106 @@
+// Work-item queue of a persistent CTA: a scheduler warp hands the CTA's work
+// items to every warp role through a small ring in shared memory.
+//
+// Items are taken from a counter shared by all CTAs (atomicAdd on a word of
+// the workspace, zeroed before the launch), so a CTA that finishes early takes
+// more: with a fixed stride over the items, the sequences' different lengths
+// leave some CTAs with far more key tiles than others.  The CTA's first item
+// is its block index; counter value c names item gridDim.x + c.  Without a
+// counter (AttnParams::sched_ctr null) the items are the fixed stride
+// blockIdx.x, blockIdx.x + gridDim.x, ...
+//
+// Only active items (plan_item's `active`) enter the ring; -1 ends it.  Which
+// CTA runs an item does not change the item's arithmetic, so every output bit
+// is the same either way.
+//
+// Barriers per ring slot: full (the scheduler's write), empty (every consumer
+// warp has read it) and taken (the first consumer, the K producer, has read
+// it).  The scheduler fetches entry m once entry m - kRingLead is taken, so
+// the CTA holds at most kRingLead items beyond the one its producer loads,
+// and once entry m - kRingSlots is empty.  All waits are bounded.
+#pragma once
+#include "attn_tile.cuh"
+
+namespace rad {
+
+constexpr int kRingSlots = 8;
+constexpr int kRingLead = 2;
+// int32 items[kRingSlots], then full, empty and taken barriers [kRingSlots] each
+constexpr int kRingBytes = kRingSlots * 4 + 3 * kRingSlots * 8;
+
+struct ItemRing {
+    volatile int* items;
+    uint32_t full, empty, taken;   // shared-memory addresses of the barrier arrays
+
+    // `at` / `at_addr`: kRingBytes of shared memory, 8-byte aligned
+    __device__ ItemRing(uint8_t* at, uint32_t at_addr)
+        : items(reinterpret_cast<volatile int*>(at)),
+          full(at_addr + kRingSlots * 4),
+          empty(at_addr + kRingSlots * 4 + kRingSlots * 8),
+          taken(at_addr + kRingSlots * 4 + 2 * kRingSlots * 8) {}
+
+    // One thread, before fence_mbarrier_init: `consumers` warps read every entry.
+    __device__ void init(uint32_t consumers) const {
+        for (int s = 0; s < kRingSlots; ++s) {
+            mbar_init(full + 8 * s, 1);
+            mbar_init(empty + 8 * s, consumers);
+            mbar_init(taken + 8 * s, 1);
+        }
+    }
+
+    // A consumer warp (all lanes): entry n of the ring into `item` (-1: no more).
+    // `first`: the warp is the K producer, whose reads pace the scheduler.
+    // Returns false on a time-out.
+    __device__ bool take(uint32_t n, int& item, uint64_t wait_ns, bool first) const {
+        const uint32_t s = n % kRingSlots;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(full + 8 * s, (n / kRingSlots) & 1u, wait_ns));
+        if (!ok) return false;
+        item = items[s];
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) {
+            mbar_arrive(empty + 8 * s);
+            if (first) mbar_arrive(taken + 8 * s);
+        }
+        return true;
+    }
+
+    // The scheduler: one thread.  Fills the ring until the items run out (or
+    // `abort_flag` is set), then writes -1.  Returns false on a time-out.
+    template <class C, bool WIN>
+    __device__ bool run(const AttnParams& p, const volatile uint32_t* abort_flag) const {
+        bool first = true;
+        unsigned next_static = blockIdx.x;
+        for (uint32_t m = 0;; ++m) {
+            if (m >= (uint32_t)kRingLead &&
+                !mbar_wait_bounded(taken + 8 * ((m - kRingLead) % kRingSlots),
+                                   ((m - kRingLead) / kRingSlots) & 1u, p.wait_ns))
+                return false;
+            if (m >= (uint32_t)kRingSlots &&
+                !mbar_wait_bounded(empty + 8 * (m % kRingSlots), (m / kRingSlots - 1) & 1u, p.wait_ns))
+                return false;
+            int item = -1;
+            while (!*abort_flag) {
+                unsigned cand;
+                if (!p.sched_ctr) {
+                    cand = next_static;
+                    next_static += gridDim.x;
+                } else if (first) {
+                    cand = blockIdx.x;
+                } else {
+                    cand = atomicAdd(p.sched_ctr, 1u) + gridDim.x;
+                }
+                first = false;
+                if (cand >= (unsigned)p.n_items) break;
+                if (plan_item<C, WIN>((int)cand, p).active) {
+                    item = (int)cand;
+                    break;
+                }
+            }
+            items[m % kRingSlots] = item;
+            mbar_arrive(full + 8 * (m % kRingSlots));
+            if (item < 0) return true;
+        }
+    }
+};
+
+}  // namespace rad

@@ -1,23 +1,26 @@
 // Split-call attention on the 5th-generation tensor cores (tcgen05, TMEM) for
-// bf16 KV pools with head_dim 128, the query rows on the MMA's M: the verify
-// call shape ("kern manifest v7", $defs.Batch) of the `attn_paged` op with
-// more than 8 query rows per KV head.
+// bf16 KV pools with head_dim 128 or 256, the query rows on the MMA's M: the
+// decode and verify call shapes ("kern manifest v7", $defs.Batch) of the
+// `attn_paged` op.
 //
 // The same item plan, partials and combine as attn_tile.cuh, and the same
 // structure as the e4m3 split kernel (split_tc05.cuh): the item's up to 32
 // query rows are copied into the four 32-lane quarters of M = 128, and softmax
-// warp w owns keys 32w .. 32w+31 of every 128-key tile, with its own running
-// max and sum; the four partials of a row are merged once per item, in warp
-// order.  With bf16 pools nothing is converted:
+// warp w owns keys KW*w .. KW*w+KW-1 of every BK-key tile (BK = 128, KW = 32
+// with head_dim 128; BK = 64, KW = 16 with head_dim 256, so a K or V tile is
+// 32 KB either way), with its own running max and sum; the four partials of a
+// row are merged once per item, in warp order.  With bf16 pools nothing is
+// converted:
 //   S  = Q K^T   kind::f16, bf16 A (Q, exact) and B (the staged K rows,
-//                K-major, two 64-column blocks), M 128, N 128, K = head_dim
+//                K-major, head_dim/64 64-column blocks), M 128, N BK,
+//                K = head_dim
 //   O += P V     kind::f16, A = P from TMEM as bf16 hi + lo (two MMAs, the
 //                pair carries p to ~16 bits), B = the staged V rows as the
-//                MN-major operand
-// P is written over S in TMEM (S buffer b's 128 columns hold P_hi in the
-// first 64 and P_lo in the last 64; in lane 32w + r only keys 32w .. 32w+31
-// are non-zero), so TMEM holds two O buffers (by item parity) and two S/P
-// buffers (by tile parity).
+//                MN-major operand, N = head_dim
+// P is written over S in TMEM (S buffer b's BK columns hold P_hi in the first
+// BK/2 and P_lo in the last BK/2; in lane 32w + r only warp w's keys are
+// non-zero), so TMEM holds two O buffers (by item parity) with head_dim 128, one
+// with head_dim 256 (256 columns), and two S/P buffers (by tile parity).
 //
 // Warp roles (one CTA per SM, persistent):
 //   warps 0-3   softmax (quarter w, thread = query row r); at an item's end
@@ -32,25 +35,29 @@
 //               the V rows outside it.
 //   warps 6, 7  K and V producers: page ids, one TMA box per page and 64-column
 //               block (page_size rows x 128 bytes of the KV head), issued by
-//               lanes 0 .. 2 * pages - 1; pages outside the item's range load
-//               zeros.
+//               lanes 0 .. (head_dim/64) * pages - 1; pages outside the item's
+//               range load zeros.
 //   warp 8      query rows: the item's rows, four copies, in the 128-byte
 //               swizzled K-major layout, once the previous item's QKs are done.
 //   warps 9-12  epilogue: warp 9 + i reads TMEM lane quarter (9 + i) & 3 of
 //               the item's O buffer, and the four merge the quarters of each row
 //               in warp order (a 16 KB scratch), then store the row or the
 //               split's partial; an item's merge overlaps the next item's tiles.
+//   warp 13     scheduler: takes the CTA's items from the counter shared by all
+//               CTAs and hands them to the other warps (sched.cuh).
 // PV of tile t completes a phase of pv_done[t & 1]; a thread that has seen
 // S(t) knows PV(t-2) is done (QK(t) waited for it), so no wait on pv_done is
 // two phases ahead of its barrier.  The O buffers' barriers (o_full, ml_full,
-// o_free) complete once per item of that parity, and each role waits on them
-// in order, the softmax for the epilogue two items back before it reuses that
-// hand-off slot.  Every wait is bounded; a time-out sets RAD_ERRW_TIMEOUT and
-// the roles unwind.
+// o_free) complete once per item of that buffer, and each role waits on them
+// in order: the PV warp and the softmax hand-off wait for the read-out of the
+// item NOB back (NOB = the O buffers), so no waiter falls two phases behind.
+// Every wait is bounded; a time-out sets RAD_ERRW_TIMEOUT and the roles
+// unwind.
 #pragma once
 #include <cuda.h>
 
 #include "attn_tile.cuh"
+#include "sched.cuh"
 #include "tc05.cuh"
 
 #ifndef RAD_SPLITBF_NSK
@@ -67,6 +74,19 @@
 #ifndef RAD_SPLITBF_FEW_NSV
 #define RAD_SPLITBF_FEW_NSV 3
 #endif
+// head_dim 256: the four query copies take 64 KB (the FEW form's 8 rows 4 KB).
+#ifndef RAD_SPLITBF256_NSK
+#define RAD_SPLITBF256_NSK 2
+#endif
+#ifndef RAD_SPLITBF256_NSV
+#define RAD_SPLITBF256_NSV 2
+#endif
+#ifndef RAD_SPLITBF256_FEW_NSK
+#define RAD_SPLITBF256_FEW_NSK 3
+#endif
+#ifndef RAD_SPLITBF256_FEW_NSV
+#define RAD_SPLITBF256_FEW_NSV 3
+#endif
 
 namespace rad {
 
@@ -76,16 +96,21 @@ namespace rad {
 // lane 32w + r holds row r % 8, the item's row r for r < 8, and the rows
 // beyond are masked as before.  Nothing else changes, so a row's bits are
 // those of the other form.
-template <bool FEW>
+template <bool FEW, int D_ = 128>
 struct SplitBf16Cfg {
-    static constexpr int D = 128;                   // head dim
-    static constexpr int BK = 128;                  // keys per tile
+    static constexpr int D = D_;                    // head dim: 128 or 256
+    static constexpr int BK = D == 128 ? 128 : 64;  // keys per tile (a K or V tile is 32 KB)
+    static constexpr int NBLK = D / 64;             // 64-column blocks of a row
+    static constexpr int KW = BK / 4;               // keys of a tile per softmax warp
+    static constexpr int NOB = D == 128 ? 2 : 1;    // O buffers in TMEM
     static constexpr int QT = 32;                   // (item planner) query rows per item
     static constexpr int KS = BK;                   // (item planner) keys per stage
-    static constexpr int NSK = FEW ? RAD_SPLITBF_FEW_NSK : RAD_SPLITBF_NSK;   // K stages (with the page-id flag)
-    static constexpr int NSV = FEW ? RAD_SPLITBF_FEW_NSV : RAD_SPLITBF_NSV;   // V stages
+    static constexpr int NSK = D == 128 ? (FEW ? RAD_SPLITBF_FEW_NSK : RAD_SPLITBF_NSK)
+                                        : (FEW ? RAD_SPLITBF256_FEW_NSK : RAD_SPLITBF256_NSK);   // K stages
+    static constexpr int NSV = D == 128 ? (FEW ? RAD_SPLITBF_FEW_NSV : RAD_SPLITBF_NSV)
+                                        : (FEW ? RAD_SPLITBF256_FEW_NSV : RAD_SPLITBF256_NSV);   // V stages
     static constexpr int BLK = BK * 128;            // one 64-column block of a K or V tile: [key][128 B]
-    static constexpr int KV_TILE = 2 * BLK;
+    static constexpr int KV_TILE = NBLK * BLK;
     static constexpr int Q_ROWS = FEW ? 8 : 128;    // query operand rows held: 8, or four copies of 32
     static constexpr int Q_BLK = Q_ROWS * 128;      // one 64-column block of them
     static constexpr uint32_t Q_SBO = FEW ? 0u : 1024u;   // the A descriptor's 8-row group stride
@@ -93,33 +118,53 @@ struct SplitBf16Cfg {
     static constexpr int META_STRIDE = 128;         // [16]: the tile's page-id flag
     static constexpr int SCR_BYTES = 4 * 32 * 128;  // the merge: [warp][row][32 floats], chunks swizzled
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + 2 * Q_BLK;    // 1 KB-aligned: 2 KB or 32 KB
+    static constexpr int OFF_K = OFF_Q + NBLK * Q_BLK;    // 1 KB-aligned
     static constexpr int OFF_V = OFF_K + NSK * KV_TILE;
     static constexpr int OFF_SCR = OFF_V + NSV * KV_TILE;
-    static constexpr int OFF_ML = OFF_SCR + SCR_BYTES;      // [O buffer][max, sum][quarter][32 rows]
-    static constexpr int OFF_FLAGS = OFF_ML + 2 * 2 * 4 * 32 * 4;   // [O buffer]: the item's error bits
+    static constexpr int OFF_ML = OFF_SCR + SCR_BYTES;      // [hand-off slot][max, sum][quarter][32 rows]
+    static constexpr int OFF_FLAGS = OFF_ML + 2 * 2 * 4 * 32 * 4;   // [hand-off slot]: the item's error bits
     static constexpr int OFF_META = OFF_FLAGS + 16;
     static constexpr int OFF_BARS = OFF_META + NSK * META_STRIDE;
     // q_full, q_empty, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[2], p_full[2],
     // pv_done[2], o_full[2], ml_full[2], o_free[2], final[2]
     static constexpr int NBARS = 2 + 2 * NSK + 2 * NSV + 2 + 2 + 2 + 2 + 2 + 2 + 2;
-    static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
+    static constexpr int OFF_RING = OFF_BARS + NBARS * 8;     // the item ring (sched.cuh)
+    static constexpr int OFF_MISC = OFF_RING + kRingBytes;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // 1 KB alignment of the swizzled tiles
-    static constexpr int NTHREADS = 13 * 32;
-    static constexpr int W_QK = 4, W_PV = 5, W_PROD_K = 6, W_PROD_V = 7, W_Q = 8, W_EPI = 9;
+    static constexpr int NTHREADS = 14 * 32;
+    static constexpr int W_QK = 4, W_PV = 5, W_PROD_K = 6, W_PROD_V = 7, W_Q = 8, W_EPI = 9, W_SCHED = 13;
+    static constexpr int RING_CONSUMERS = 13;                 // every warp but the scheduler
     static constexpr int K_EMPTY_ARRIVALS = 1 + 4;            // the QK commit + the softmax warps' flag reads
-    static constexpr uint32_t TMEM_COLS = 512;   // O_b [128b, ...), S/P_b [256 + 128b, ...)
+    static constexpr uint32_t TMEM_COLS = 512;   // O_b [D b, ...), S/P_b [NOB D + BK b, ...)
+    static_assert(D == 128 || D == 256, "head_dim 128 or 256");
+    static_assert(NOB * D + 2 * BK <= (int)TMEM_COLS, "tensor memory budget");
     static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && KV_TILE % 1024 == 0, "1 KB tiles");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
+// Loads and stores of N consecutive 32-bit TMEM columns of a warp's lanes.
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]) {
+    static_assert(N == 8 || N == 16 || N == 32, "8, 16 or 32 columns");
+    if constexpr (N == 32) tmem_ld32(taddr, r);
+    else if constexpr (N == 16) tmem_ld16(taddr, r);
+    else tmem_ld8(taddr, r);
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[N]) {
+    static_assert(N == 8 || N == 16 || N == 32, "8, 16 or 32 columns");
+    if constexpr (N == 32) tmem_st32(taddr, r);
+    else if constexpr (N == 16) tmem_st16(taddr, r);
+    else tmem_st8(taddr, r);
+}
+
 // MODE: kModeCausal, kModeWindow or kModeTree (draft-tree rows, uniform row
 // counts: bit i of a row's mask word lets it see the call's key i).
-template <int MODE, bool FEW>
-__global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
+template <int MODE, bool FEW, int D = 128>
+__global__ void __launch_bounds__(SplitBf16Cfg<FEW, D>::NTHREADS, 1)
     attn_split_bf16_tc05_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                                 const __grid_constant__ AttnParams p) {
-    using C = SplitBf16Cfg<FEW>;
+    using C = SplitBf16Cfg<FEW, D>;
     constexpr bool WIN = MODE == kModeWindow;
     constexpr bool TREE = MODE == kModeTree;
     extern __shared__ uint8_t smem_raw[];
@@ -136,11 +181,12 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
     const uint32_t bar_s_full = bar_v_empty + 8 * C::NSV;   // [2]
     const uint32_t bar_p_full = bar_s_full + 16;            // [2]
     const uint32_t bar_pv_done = bar_p_full + 16;           // [2], by tile parity
-    const uint32_t bar_o_full = bar_pv_done + 16;           // [2], by O buffer: the item's last PV done
-    const uint32_t bar_ml_full = bar_o_full + 16;           // [2], by O buffer: the softmax's hand-off
-    const uint32_t bar_o_free = bar_ml_full + 16;           // [2], by O buffer: read out by the epilogue
+    const uint32_t bar_o_full = bar_pv_done + 16;           // [NOB], by O buffer: the item's last PV done
+    const uint32_t bar_ml_full = bar_o_full + 16;           // [NOB], by O buffer: the softmax's hand-off
+    const uint32_t bar_o_free = bar_ml_full + 16;           // [NOB], by O buffer: read out by the epilogue
     const uint32_t bar_final = bar_o_free + 16;             // [2]: QK warp, PV warp
     volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);  // [0] tmem, [1] abort
+    const ItemRing iring(smem + C::OFF_RING, base + C::OFF_RING);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -170,6 +216,7 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
         reinterpret_cast<uint32_t*>(smem + C::OFF_FLAGS)[1] = 0u;
         mbar_init(bar_final, 1);
         mbar_init(bar_final + 8, 1);
+        iring.init(C::RING_CONSUMERS);
         misc[1] = 0;
         fence_mbarrier_init();
     }
@@ -181,14 +228,18 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
-    const uint32_t t_o = tmem;         // O buffer b (by item parity) at t_o + 128 b
-    const uint32_t t_s = tmem + 256;   // S/P buffer b (by tile parity) at t_s + 128 b
+    const uint32_t t_o = tmem;                   // O buffer b (item ic: b = ic % NOB) at t_o + D b
+    const uint32_t t_s = tmem + C::NOB * C::D;   // S/P buffer b (by tile parity) at t_s + BK b
     bool abort = false;
 
     // items that run the pipeline: active, a valid sequence length, keys to see
     const auto real = [&](const ItemPlan& it) { return it.active && it.seq_ok && it.n_stages > 0; };
 
-    if (warp == C::W_PROD_K || warp == C::W_PROD_V) {
+    if (warp == C::W_SCHED) {
+        // ===================================================== scheduler (lane 0)
+        if (lane == 0 && !iring.run<C, WIN>(p, misc + 1)) abort = true;
+        __syncwarp();
+    } else if (warp == C::W_PROD_K || warp == C::W_PROD_V) {
         // ===================================================== producers
         const bool is_k = warp == C::W_PROD_K;
         const int NSX = is_k ? C::NSK : C::NSV;
@@ -202,7 +253,13 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
         const int oob_tok = p.num_pages * P;   // a row past the pool: TMA fills the box with zeros
         uint32_t sc = 0;
         if (lane == 0) prefetch_tmap(tm);
-        for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
+        for (uint32_t n = 0; !abort; ++n) {
+            int item;
+            if (!iring.take(n, item, p.wait_ns, is_k)) {
+                abort = true;
+                break;
+            }
+            if (item < 0) break;
             const ItemPlan it = plan_item<C, WIN>(item, p);
             if (!real(it)) continue;
             const int page_hi = (it.k1 + P - 1) / P;
@@ -228,12 +285,12 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
                     abort = true;
                     break;
                 }
-                // lane i < 2 * ppt: page i % ppt of the tile, 64-column block i / ppt
+                // lane i < NBLK * ppt: page i % ppt of the tile, 64-column block i / ppt
                 const int pl = lane % ppt, blk = lane / ppt;
                 const int pi = pstart + pl;
                 const int srcl = (pstart - batch0 + pl) & 31;
                 const int pg = __shfl_sync(0xffffffffu, my_pg, srcl);
-                const bool mine = lane < 2 * ppt;
+                const bool mine = lane < C::NBLK * ppt;
                 const bool live = mine && (!WIN || pi >= page_lo) && pi < page_hi;
                 if (is_k) {
                     // the tile's page-id flag, released by the arrive below
@@ -265,7 +322,13 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
     } else if (warp == C::W_Q) {
         // ===================================================== query rows
         uint32_t ic = 0;
-        for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
+        for (uint32_t n = 0; !abort; ++n) {
+            int item;
+            if (!iring.take(n, item, p.wait_ns, false)) {
+                abort = true;
+                break;
+            }
+            if (item < 0) break;
             const ItemPlan it = plan_item<C, WIN>(item, p);
             if (!real(it)) continue;
             // lane r: query row r of the item (zeros past its rows), loaded before the
@@ -274,26 +337,39 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
             const bool valid = lane < it.m_end - it.m0;
             const int tok = m / p.ratio, hl = m - tok * p.ratio;
             const __nv_bfloat16* qrow = p.q + ((it.qrow0 + tok) * p.n_head + it.kvh * p.ratio + hl) * C::D;
-            uint4 qv[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                qv[i] = valid ? __ldg(reinterpret_cast<const uint4*>(qrow) + i) : make_uint4(0u, 0u, 0u, 0u);
-            if (ic >= 1 && !__all_sync(0xffffffffu, mbar_wait_bounded(bar_q_empty, (ic - 1) & 1u, p.wait_ns))) {
-                abort = true;
-                break;
-            }
-            // copy c at rows 32c + r of the M = 128 operand (FEW: rows 0-7 once);
-            // elements 8i .. 8i+7 in block i / 8, 16-byte chunk i % 8 (swizzled by
-            // the row)
-#pragma unroll
-            for (int c = 0; c < (FEW ? 1 : 4); ++c) {
-                const int qr = 32 * c + lane;
-                if (FEW && lane >= 8) break;
-                uint8_t* dst = smem + C::OFF_Q + qr * 128;
+            // the row in pieces of 16 x 16 bytes (128 columns); the first is loaded
+            // before the wait
+            bool wait_ok = true;
+#pragma unroll 1
+            for (int h = 0; h < C::D / 128; ++h) {
+                uint4 qv[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
-                    *reinterpret_cast<uint4*>(dst + (i >> 3) * C::Q_BLK + ((((uint32_t)i & 7u) ^ (uint32_t)(qr & 7)) << 4)) =
-                        qv[i];
+                    qv[i] = valid ? __ldg(reinterpret_cast<const uint4*>(qrow) + 16 * h + i) : make_uint4(0u, 0u, 0u, 0u);
+                if (h == 0 && ic >= 1 &&
+                    !__all_sync(0xffffffffu, mbar_wait_bounded(bar_q_empty, (ic - 1) & 1u, p.wait_ns))) {
+                    wait_ok = false;
+                    break;
+                }
+                // copy c at rows 32c + r of the M = 128 operand (FEW: rows 0-7 once);
+                // elements 8i .. 8i+7 in block i / 8, 16-byte chunk i % 8 (swizzled by
+                // the row)
+#pragma unroll
+                for (int c = 0; c < (FEW ? 1 : 4); ++c) {
+                    const int qr = 32 * c + lane;
+                    if (FEW && lane >= 8) break;
+                    uint8_t* dst = smem + C::OFF_Q + qr * 128;
+#pragma unroll
+                    for (int i0 = 0; i0 < 16; ++i0) {
+                        const int i = 16 * h + i0;
+                        *reinterpret_cast<uint4*>(dst + (i >> 3) * C::Q_BLK +
+                                                  ((((uint32_t)i & 7u) ^ (uint32_t)(qr & 7)) << 4)) = qv[i0];
+                    }
+                }
+            }
+            if (!wait_ok) {
+                abort = true;
+                break;
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -306,7 +382,13 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
         constexpr uint32_t idesc_qk = umma_idesc_bf16(128, C::BK, 0, 0);
         uint32_t tc = 0, ic = 0;
         bool issued = false;
-        for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
+        for (uint32_t n = 0; !abort; ++n) {
+            int item;
+            if (!iring.take(n, item, p.wait_ns, false)) {
+                abort = true;
+                break;
+            }
+            if (item < 0) break;
             const ItemPlan it = plan_item<C, WIN>(item, p);
             if (!real(it)) continue;
             const int T = it.n_stages;
@@ -330,7 +412,7 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
 #pragma unroll
                     for (int kk = 0; kk < C::D / 16; ++kk) {
                         const uint32_t off = (uint32_t)((kk >> 2) * C::BLK + (kk & 3) * 32);
-                        tc_mma_ss(t_s + 128 * b,
+                        tc_mma_ss(t_s + C::BK * b,
                                   umma_desc_sw128(base + C::OFF_Q + (uint32_t)((kk >> 2) * C::Q_BLK + (kk & 3) * 32), 16,
                                                   C::Q_SBO),
                                   umma_desc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
@@ -357,19 +439,26 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
         constexpr uint32_t idesc_pv = umma_idesc_bf16(128, C::D, 0, 1);
         uint32_t tc = 0, ic = 0;
         bool issued = false;
-        for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
+        for (uint32_t n = 0; !abort; ++n) {
+            int item;
+            if (!iring.take(n, item, p.wait_ns, false)) {
+                abort = true;
+                break;
+            }
+            if (item < 0) break;
             const ItemPlan it = plan_item<C, WIN>(item, p);
             if (!real(it)) continue;
             const int T = it.n_stages;
             for (int j = 0; j < T; ++j) {
                 const uint32_t tcj = tc + j, b = tcj & 1u, sv = tcj % C::NSV;
                 // P_j written, V_j landed, and at an item's first tile its O buffer read out
-                // (the item two before)
-                const uint32_t t_ob = t_o + 128 * (ic & 1u);
+                // (the item NOB before)
+                const uint32_t ob = ic % C::NOB;
+                const uint32_t t_ob = t_o + C::D * ob;
                 bool ok = mbar_wait_bounded(bar_p_full + 8 * b, (tcj >> 1) & 1u, p.wait_ns);
                 if (ok) ok = mbar_wait_bounded(bar_v_full + 8 * sv, (tcj / C::NSV) & 1u, p.wait_ns);
-                if (ok && j == 0 && ic >= 2)
-                    ok = mbar_wait_bounded(bar_o_free + 8 * (ic & 1u), ((ic - 2) >> 1) & 1u, p.wait_ns);
+                if (ok && j == 0 && ic >= (uint32_t)C::NOB)
+                    ok = mbar_wait_bounded(bar_o_free + 8 * ob, ((ic - C::NOB) / C::NOB) & 1u, p.wait_ns);
                 if (!__all_sync(0xffffffffu, ok)) {
                     abort = true;
                     break;
@@ -380,8 +469,9 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
                 const int zlo = it.klo - key0, zhi = it.k1 - key0;
                 if (zlo > 0 || zhi < C::BK) {
                     uint8_t* vt = smem + C::OFF_V + sv * C::KV_TILE;
-                    for (int idx = lane; idx < C::BK * 16; idx += 32) {
-                        const int row = idx >> 4, ch = idx & 15;
+                    constexpr int CPR = C::NBLK * 8;   // 16-byte chunks per row
+                    for (int idx = lane; idx < C::BK * CPR; idx += 32) {
+                        const int row = idx / CPR, ch = idx % CPR;
                         if (row < zlo || row >= zhi)
                             *reinterpret_cast<uint4*>(vt + (ch >> 3) * C::BLK + row * 128 + ((ch & 7) << 4)) =
                                 make_uint4(0u, 0u, 0u, 0u);
@@ -392,16 +482,16 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
                 tc_fence_after();
                 if (lane == 0) {
                     const uint32_t vb = base + C::OFF_V + sv * C::KV_TILE;
-                    const uint32_t tp = t_s + 128 * b;
+                    const uint32_t tp = t_s + C::BK * b;
 #pragma unroll
                     for (int kk = 0; kk < C::BK / 16; ++kk) {
                         const uint64_t bd = umma_desc_sw128(vb + kk * 16 * 128, C::BLK, 1024);
                         tc_mma_ts(t_ob, tp + kk * 8, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);   // P_hi
-                        tc_mma_ts(t_ob, tp + 64 + kk * 8, bd, idesc_pv, 1u);                      // P_lo
+                        tc_mma_ts(t_ob, tp + C::BK / 2 + kk * 8, bd, idesc_pv, 1u);               // P_lo
                     }
                     tc_commit(bar_pv_done + 8 * b);
                     tc_commit(bar_v_empty + 8 * sv);
-                    if (j == T - 1) tc_commit(bar_o_full + 8 * (ic & 1u));
+                    if (j == T - 1) tc_commit(bar_o_full + 8 * ob);
                     issued = true;
                 }
                 __syncwarp();
@@ -426,19 +516,25 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
         uint32_t* const flags = reinterpret_cast<uint32_t*>(smem + C::OFF_FLAGS);
         uint8_t* const scr = smem + C::OFF_SCR;
         uint32_t ic = 0;
-        for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
+        for (uint32_t n = 0; !abort; ++n) {
+            int item;
+            if (!iring.take(n, item, p.wait_ns, false)) {
+                abort = true;
+                break;
+            }
+            if (item < 0) break;
             const ItemPlan it = plan_item<C, WIN>(item, p);
             if (!real(it)) continue;
             // the item's last PV done and the softmax warps' hand-off
-            const uint32_t ob = ic & 1u;
-            bool ok = mbar_wait_bounded(bar_o_full + 8 * ob, (ic >> 1) & 1u, p.wait_ns);
-            if (ok) ok = mbar_wait_bounded(bar_ml_full + 8 * ob, (ic >> 1) & 1u, p.wait_ns);
+            const uint32_t ob = ic % C::NOB, hs = ic & 1u;   // O buffer, hand-off slot
+            bool ok = mbar_wait_bounded(bar_o_full + 8 * ob, (ic / C::NOB) & 1u, p.wait_ns);
+            if (ok) ok = mbar_wait_bounded(bar_ml_full + 8 * ob, (ic / C::NOB) & 1u, p.wait_ns);
             if (named_barrier_or(2, 128, !__all_sync(0xffffffffu, ok) || misc[1] != 0)) {   // all leave together
                 abort = true;
                 break;
             }
             tc_fence_after();
-            const float* const mlb = ml + ob * 256;
+            const float* const mlb = ml + hs * 256;
             const int nrows = it.m_end - it.m0;
             const int m = it.m0 + r;
             const bool valid = r < nrows;
@@ -446,7 +542,7 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
             const long long orow = (it.qrow0 + tok) * p.n_head + it.kvh * p.ratio + hl;   // q/out row
             const long long slot_idx = it.gq * p.max_splits + it.s;
             // ---- the four quarters' (max, sum, O) of row r, merged in warp order
-            const uint32_t item_bits = flags[ob];
+            const uint32_t item_bits = flags[hs];
             const bool page_bad = (item_bits & kErrPage) != 0;
             const bool mask_bad = TREE && (item_bits & kErrMask) != 0;
             const bool item_bad = page_bad || mask_bad;
@@ -465,25 +561,25 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
             const bool final_write = it.n_splits - it.s_first == 1;
             const float inv = L == 0.f ? 0.f : 1.f / L;
             float* pacc = p.part_acc + slot_idx * p.qtv * C::D;
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < C::D / 32; ++c) {
                 // quarter w's scaled O of row r, columns 32c .. 32c+31, 16-byte chunks
                 // swizzled by the row
                 uint32_t ov[32];
-                tmem_ld32(t_o + 128 * ob + lane_off + 32 * c, ov);
+                tmem_ld32(t_o + C::D * ob + lane_off + 32 * c, ov);
                 float4* mine = reinterpret_cast<float4*>(scr + (w * 32 + r) * 128);
 #pragma unroll
                 for (int e4 = 0; e4 < 8; ++e4)
                     mine[e4 ^ (r & 7)] = make_float4(__uint_as_float(ov[4 * e4]) * f_me, __uint_as_float(ov[4 * e4 + 1]) * f_me,
                                                      __uint_as_float(ov[4 * e4 + 2]) * f_me,
                                                      __uint_as_float(ov[4 * e4 + 3]) * f_me);
-                if (c == 3) {
+                if (c == C::D / 32 - 1) {
                     // O is read out: the next item's first PV may overwrite it
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar_o_free + 8 * ob);
                 }
                 named_barrier_sync(2, 128);
-                if (c == 0 && t == 0) flags[ob] = 0u;   // read by all: reset for the item two on
+                if (c == 0 && t == 0) flags[hs] = 0u;   // read by all: reset for the item two on
                 // row r, columns 32c + 8w .. 32c + 8w + 7: the four quarters summed in order
                 float a[8];
 #pragma unroll
@@ -532,14 +628,20 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
         }
     } else {
         // ===================================================== softmax (warps 0-3)
-        const int w = warp;                                     // quarter: keys 32w .. 32w+31 of a tile
+        const int w = warp;                                     // quarter: keys KW w .. KW w + KW-1 of a tile
         const int r = lane;                                     // query row r of the item
         const uint32_t lane_off = (uint32_t)(w * 32) << 16;     // this warp's TMEM lanes
         const int t = threadIdx.x;                              // 0 .. 127
         float* const ml = reinterpret_cast<float*>(smem + C::OFF_ML);
         uint32_t* const flags = reinterpret_cast<uint32_t*>(smem + C::OFF_FLAGS);
         uint32_t tc = 0, ic = 0;
-        for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
+        for (uint32_t n = 0; !abort; ++n) {
+            int item;
+            if (!iring.take(n, item, p.wait_ns, false)) {
+                abort = true;
+                break;
+            }
+            if (item < 0) break;
             const ItemPlan it = plan_item<C, WIN>(item, p);
             if (!it.active) continue;
             const int nrows = it.m_end - it.m0;
@@ -616,32 +718,33 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_k_empty + 8 * sk);
                 tc_fence_after();
-                uint32_t sv[32];
-                tmem_ld32(t_s + 128 * b + 32 * w + lane_off, sv);
+                constexpr int KW = C::KW;
+                uint32_t sv[KW];
+                tmem_ld_cols<KW>(t_s + C::BK * b + KW * w + lane_off, sv);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) sv[e] = __float_as_uint(__uint_as_float(sv[e]) * crow);
+                for (int e = 0; e < KW; ++e) sv[e] = __float_as_uint(__uint_as_float(sv[e]) * crow);
 #define X(e) __uint_as_float(sv[e])
-                const int key0 = it.k0 + j * C::BK + 32 * w;
+                const int key0 = it.k0 + j * C::BK + KW * w;
                 const int lim = nk - key0, lim_lo = nlo - key0;   // columns outside [lim_lo, lim) are masked
                 if (TREE) {
                     // key0 + e < n_full: a cached key; else the call's key i = key0 + e - n_full
                     const int ib = key0 - n_full;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
+                    for (int e = 0; e < KW; ++e) {
                         const int i = ib + e;
                         const bool vis = e < lim && e >= lim_lo && (i < 0 || ((tmw >> (i & 31)) & 1u));
                         if (!vis) sv[e] = __float_as_uint(-CUDART_INF_F);
                     }
-                } else if (lim < 32 || lim_lo > 0) {
+                } else if (lim < KW || lim_lo > 0) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
+                    for (int e = 0; e < KW; ++e)
                         if (e >= lim || e < lim_lo) sv[e] = __float_as_uint(-CUDART_INF_F);
                 }
                 float mx8[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) mx8[i] = X(i);
 #pragma unroll
-                for (int e = 8; e < 32; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], X(e));
+                for (int e = 8; e < KW; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], X(e));
                 const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                        fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
                 // lazy rescale of this quarter's O past 2^8, warp-wide (tcgen05.ld/st are
@@ -666,12 +769,12 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
                     }
                     tc_fence_after();
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
+                    for (int q = 0; q < C::D / 32; ++q) {
                         uint32_t ov[32];
-                        tmem_ld32(t_o + 128 * (ic & 1u) + lane_off + 32 * q, ov);
+                        tmem_ld32(t_o + C::D * (ic % C::NOB) + lane_off + 32 * q, ov);
 #pragma unroll
                         for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                        tmem_st32(t_o + 128 * (ic & 1u) + lane_off + 32 * q, ov);
+                        tmem_st32(t_o + C::D * (ic % C::NOB) + lane_off + 32 * q, ov);
                     }
                     tmem_wait_st();
                     if (need) {
@@ -681,9 +784,9 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
                 }
                 const float m_use = (m_run == -CUDART_INF_F) ? 0.f : m_run;
                 float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                uint32_t ph[16], plo[16];   // p as bf16 hi + lo
+                uint32_t ph[KW / 2], plo[KW / 2];   // p as bf16 hi + lo
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
+                for (int e = 0; e < KW / 2; ++e) {
                     const float p0 = exp2f(X(2 * e) - m_use), p1 = exp2f(X(2 * e + 1) - m_use);
                     ps8[e & 7] += p0 + p1;
                     const uint32_t hv = pack_bf16x2(p0, p1);
@@ -692,21 +795,21 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
                 }
 #undef X
                 {
-                    // P over S in this warp's lanes: P_hi in columns [0, 64), P_lo in
-                    // [64, 128); this quarter's keys at columns 16w .. 16w+15 of each,
-                    // zeros elsewhere (its S reads are complete)
-                    uint32_t z[16];
+                    // P over S in this warp's lanes: P_hi in columns [0, BK/2), P_lo in
+                    // [BK/2, BK); this quarter's keys at columns KW/2 w .. KW/2 w + KW/2-1
+                    // of each, zeros elsewhere (its S reads are complete)
+                    uint32_t z[KW / 2];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) z[e] = 0u;
-                    const uint32_t tp = t_s + 128 * b + lane_off;
+                    for (int e = 0; e < KW / 2; ++e) z[e] = 0u;
+                    const uint32_t tp = t_s + C::BK * b + lane_off;
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
                         if (h == w) {
-                            tmem_st16(tp + 16 * h, ph);
-                            tmem_st16(tp + 64 + 16 * h, plo);
+                            tmem_st_cols<KW / 2>(tp + (KW / 2) * h, ph);
+                            tmem_st_cols<KW / 2>(tp + C::BK / 2 + (KW / 2) * h, plo);
                         } else {
-                            tmem_st16(tp + 16 * h, z);
-                            tmem_st16(tp + 64 + 16 * h, z);
+                            tmem_st_cols<KW / 2>(tp + (KW / 2) * h, z);
+                            tmem_st_cols<KW / 2>(tp + C::BK / 2 + (KW / 2) * h, z);
                         }
                     }
                 }
@@ -722,18 +825,19 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
             }
             if (abort) break;
             // ---- hand-off: this quarter's (max, sum) of row r and the item's error bits
-            // go to the epilogue warps, once they have read out the item two before (its
-            // slot and O buffer are this item's)
-            const uint32_t ob = ic & 1u;
-            if (ic >= 2 &&
-                !__all_sync(0xffffffffu, mbar_wait_bounded(bar_o_free + 8 * ob, ((ic - 2) >> 1) & 1u, p.wait_ns))) {
+            // go to the epilogue warps, once they have read out the item NOB before (its
+            // O buffer is this item's; its hand-off slot was read before that)
+            const uint32_t ob = ic % C::NOB, hs = ic & 1u;
+            if (ic >= (uint32_t)C::NOB &&
+                !__all_sync(0xffffffffu,
+                            mbar_wait_bounded(bar_o_free + 8 * ob, ((ic - C::NOB) / C::NOB) & 1u, p.wait_ns))) {
                 abort = true;
                 break;
             }
-            ml[ob * 256 + w * 32 + r] = m_run;
-            ml[ob * 256 + 128 + w * 32 + r] = l_run;
+            ml[hs * 256 + w * 32 + r] = m_run;
+            ml[hs * 256 + 128 + w * 32 + r] = l_run;
             const uint32_t bad_w = __reduce_or_sync(0xffffffffu, bad);
-            if (lane == 0 && bad_w) atomicOr(flags + ob, bad_w);
+            if (lane == 0 && bad_w) atomicOr(flags + hs, bad_w);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_ml_full + 8 * ob);
             tc += T;
@@ -748,6 +852,29 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW>::NTHREADS, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == C::W_QK) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// Launch of one form: one CTA per SM (shared memory, TMEM), persistent over
+// the items; calls with a sliding window run the window build, calls with
+// tree masks the tree build, others the causal one.
+template <bool FEW, int D>
+cudaError_t launch_split_bf16_form(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
+                                   cudaStream_t st) {
+    using C = SplitBf16Cfg<FEW, D>;
+    auto kern = p.window > 0  ? attn_split_bf16_tc05_kernel<kModeWindow, FEW, D>
+                : p.tree_mask ? attn_split_bf16_tc05_kernel<kModeTree, FEW, D>
+                              : attn_split_bf16_tc05_kernel<kModeCausal, FEW, D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    long long grid = sms;
+    if (grid > p.n_items) grid = p.n_items;
+    if (grid < 1) grid = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(C::NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = st;
+    return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 
 }  // namespace rad

@@ -20,6 +20,10 @@ enum Family : int { kFamDecode = 0, kFamVerify = 1, kFamWide = 2, kFamPrefillTC 
 #ifndef RAD_SPLIT_BF16_TC05
 #define RAD_SPLIT_BF16_TC05 1
 #endif
+// The same for head_dim 256 with bf16 pools.
+#ifndef RAD_SPLIT_BF16_TC05_D256
+#define RAD_SPLIT_BF16_TC05_D256 1
+#endif
 
 // Keys per split for calls of up to kSplitMaxRows rows; longer calls (prefill
 // chunks) run one range per query tile.  A multiple of every tile's KS.
@@ -34,7 +38,17 @@ constexpr int kSplitLen = RAD_SPLIT_LEN;
 #define RAD_SPLITTC_LEN 2048
 #endif
 constexpr int kSplitLenTC = RAD_SPLITTC_LEN;
+// The same for the bf16 tcgen05 split kernel with head_dim 256.
+#ifndef RAD_SPLITTC_LEN_D256
+#define RAD_SPLITTC_LEN_D256 2048
+#endif
+constexpr int kSplitLenTC256 = RAD_SPLITTC_LEN_D256;
 constexpr int kSplitMaxRows = 256;
+// The tcgen05 split kernels take their items from a counter shared by all
+// CTAs (sched.cuh); 0 gives every CTA a fixed stride of items instead.
+#ifndef RAD_SPLIT_DYNAMIC
+#define RAD_SPLIT_DYNAMIC 1
+#endif
 
 // Tile shapes: WQ, NQW, WK, KS, NS, CTAs per SM (see TileCfg).  Each can be
 // overridden at compile time (-DRAD_TILE_...="...") for tuning sweeps.
@@ -157,7 +171,9 @@ cudaError_t launch_split_tc05(const CUtensorMap& tk, const CUtensorMap& tv, cons
 TileInfo split_tc05_info(bool few);
 cudaError_t launch_split_bf16_tc05(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
                                    cudaStream_t st, bool few);
-TileInfo split_bf16_tc05_info(bool few);
+cudaError_t launch_split_bf16_tc05_d256(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
+                                        cudaStream_t st, bool few);
+TileInfo split_bf16_tc05_info(bool few, int head_dim);
 // Ragged calls: the tile maps (one CTA), before the tile kernels.  map[1]
 // null: one class; else sequences with at most split_m query rows per KV head
 // go to map[0] (tiles of qt[0] rows), the rest to map[1].

@@ -93,9 +93,9 @@ def test_workspace_sizes():
     assert b.workspace_bytes(4, 1, 8, 2, 96, 16, 19) == 0
 
 
-def bf16_tc() -> bool:
-    """Whether the library was built with the bf16 tcgen05 split kernel (a compile-time switch)."""
-    return "split_bf16_tc05" in b.describe(8, 32, 8, 128, 16)
+def bf16_tc(head_dim: int = 128) -> bool:
+    """Whether the library was built with the bf16 tcgen05 split kernel for this head_dim (a compile-time switch)."""
+    return "split_bf16_tc05" in b.describe(8, 32, 8, head_dim, 16)
 
 
 def test_describe_names_the_kernel_choice():
@@ -108,8 +108,14 @@ def test_describe_names_the_kernel_choice():
     else:
         assert "family=decode" in b.describe(1, 32, 8, 128, 16)
         assert "family=verify" in b.describe(8, 32, 8, 128, 16)
-    assert "family=decode" in b.describe(1, 32, 8, 256, 16)
-    assert "family=verify" in b.describe(8, 32, 8, 256, 16)
+    # bf16 pools with head_dim 256: the same, on the kernel's head_dim-256 build
+    if bf16_tc(256):
+        assert "family=split_bf16_tc05 head_dim=256" in b.describe(1, 16, 2, 256, 32)
+        assert "keys_per_tile=64" in b.describe(1, 16, 2, 256, 32)
+        assert "family=split_bf16_tc05 head_dim=256" in b.describe(8, 32, 8, 256, 16)
+    else:
+        assert "family=decode" in b.describe(1, 32, 8, 256, 16)
+        assert "family=verify" in b.describe(8, 32, 8, 256, 16)
     assert "family=verify" in b.describe(8, 16, 2, 256, 32, b.RAD_KV_FP8_E4M3)
     # fp8 pools with head_dim 128: decode and verify shapes share the tcgen05 split kernel
     assert "family=split_tc05" in b.describe(8, 32, 8, 128, 16, b.RAD_KV_FP8_E4M3)
@@ -229,7 +235,8 @@ def test_ex_describe_names_the_kernels_of_ragged_and_tree_calls():
     assert tree.startswith("attn_split_bf16_tc05 family=split_bf16_tc05" if bf16_tc() else "attn_tile family=verify")
     assert "attn_combine" in tree
     tree256 = b.ex_describe(b.shape_args(64, 8, 32, 8, 256, 16, 1024, tree=True))
-    assert tree256.startswith("attn_tile family=verify") and "attn_combine" in tree256
+    assert tree256.startswith("attn_split_bf16_tc05 family=split_bf16_tc05" if bf16_tc(256)
+                              else "attn_tile family=verify") and "attn_combine" in tree256
     rag = b.ex_describe(shape(ragged=True))
     assert rag.startswith("ragged_tile_map + attn_split_tc05 family=split_tc05") and rag.count("attn_combine") == 1
     rag256 = b.ex_describe(b.shape_args(64, 8, 32, 8, 256, 16, 1024, b.RAD_KV_FP8_E4M3, ragged=True))
@@ -242,7 +249,10 @@ def test_ex_describe_names_the_kernels_of_ragged_and_tree_calls():
     assert dec.startswith("ragged_tile_map + attn_split_bf16_tc05 family=split_bf16_tc05" if bf16_tc()
                           else "ragged_tile_map + attn_tile family=decode")
     dec256 = b.ex_describe(b.shape_args(4, 2, 32, 8, 256, 16, 64, ragged=True))
-    assert dec256.startswith("ragged_tile_map + attn_tile family=decode") and dec256.count("attn_tile") == 1
+    if bf16_tc(256):
+        assert dec256.startswith("ragged_tile_map + attn_split_bf16_tc05 family=split_bf16_tc05")
+    else:
+        assert dec256.startswith("ragged_tile_map + attn_tile family=decode") and dec256.count("attn_tile") == 1
     assert b.describe(300, 32, 8, 128, 16).startswith("attn_prefill_tc05")
 
 
@@ -280,7 +290,7 @@ def _fault_args(**over):
     (3_000_000_000, b.RAD_FAULT_NONE, {}),                           # above the 2 s default
     (0, 7, {}),                                                      # an unknown fault
     (0, b.RAD_FAULT_SKIP_FIRST_K_TILE, dict(kv_dtype=b.RAD_KV_FP8_E4M3)),   # e4m3 pools: not honoured
-    (0, b.RAD_FAULT_SKIP_FIRST_K_TILE, dict(head_dim=256)),          # head_dim 256: not honoured
+    (0, b.RAD_FAULT_SKIP_FIRST_K_TILE, dict(head_dim=256, kv_dtype=b.RAD_KV_FP8_E4M3)),   # the tile kernel
     (0, b.RAD_FAULT_SKIP_FIRST_K_TILE, dict(rows=300)),              # a prefill chunk: not honoured
 ])
 def test_fault_test_hook_refuses_what_it_cannot_honour(limit, fault, over):
