@@ -15,9 +15,13 @@
 //
 // Barriers per ring slot: full (the scheduler's write), empty (every consumer
 // warp has read it) and taken (the first consumer, the K producer, has read
-// it).  The scheduler fetches entry m once entry m - kRingLead is taken, so
-// the CTA holds at most kRingLead items beyond the one its producer loads,
-// and once entry m - kRingSlots is empty.  All waits are bounded.
+// it).  A kernel with a scheduler warp (run) fetches entry m once entry
+// m - kRingLead is taken, so the CTA holds at most kRingLead items beyond the
+// one its producer loads; a kernel without one lets its K producer fetch and
+// publish each entry itself (fetch, publish) after issuing the previous
+// item's last tile, while its stages still hold tiles for the consumers.  An
+// entry is written once entry m - kRingSlots is empty.  All waits are
+// bounded.
 #pragma once
 #include "attn_tile.cuh"
 
@@ -25,8 +29,10 @@ namespace rad {
 
 constexpr int kRingSlots = 8;
 constexpr int kRingLead = 2;
-// int32 items[kRingSlots], then full, empty and taken barriers [kRingSlots] each
+// int32 items[kRingSlots], then full, empty and taken barriers [kRingSlots] each;
+// a ring filled by the K producer itself has no taken barriers
 constexpr int kRingBytes = kRingSlots * 4 + 3 * kRingSlots * 8;
+constexpr int kRingBytesNoTaken = kRingSlots * 4 + 2 * kRingSlots * 8;
 
 struct ItemRing {
     volatile int* items;
@@ -39,12 +45,13 @@ struct ItemRing {
           empty(at_addr + kRingSlots * 4 + kRingSlots * 8),
           taken(at_addr + kRingSlots * 4 + 2 * kRingSlots * 8) {}
 
-    // One thread, before fence_mbarrier_init: `consumers` warps read every entry.
-    __device__ void init(uint32_t consumers) const {
+    // One thread, before fence_mbarrier_init: `consumers` warps read every entry;
+    // `with_taken`: the ring has its taken barriers (kRingBytes).
+    __device__ void init(uint32_t consumers, bool with_taken) const {
         for (int s = 0; s < kRingSlots; ++s) {
             mbar_init(full + 8 * s, 1);
             mbar_init(empty + 8 * s, consumers);
-            mbar_init(taken + 8 * s, 1);
+            if (with_taken) mbar_init(taken + 8 * s, 1);
         }
     }
 
@@ -64,40 +71,59 @@ struct ItemRing {
         return true;
     }
 
-    // The scheduler: one thread.  Fills the ring until the items run out (or
-    // `abort_flag` is set), then writes -1.  Returns false on a time-out.
-    template <class C, bool WIN>
-    __device__ bool run(const AttnParams& p, const volatile uint32_t* abort_flag) const {
+    // Where a CTA's next item comes from: its first item, then the shared
+    // counter (or, without one, the fixed stride).
+    struct Cursor {
         bool first = true;
         unsigned next_static = blockIdx.x;
+    };
+
+    // One thread: the CTA's next active item, or -1 once the items run out
+    // (or `abort_flag` is set).
+    template <class C, bool WIN>
+    __device__ int fetch(const AttnParams& p, Cursor& cur, const volatile uint32_t* abort_flag) const {
+        while (!*abort_flag) {
+            unsigned cand;
+            if (!p.sched_ctr) {
+                cand = cur.next_static;
+                cur.next_static += gridDim.x;
+            } else if (cur.first) {
+                cand = blockIdx.x;
+            } else {
+                cand = atomicAdd(p.sched_ctr, 1u) + gridDim.x;
+            }
+            cur.first = false;
+            if (cand >= (unsigned)p.n_items) return -1;
+            if (plan_item<C, WIN>((int)cand, p).active) return (int)cand;
+        }
+        return -1;
+    }
+
+    // One thread: writes entry m once entry m - kRingSlots has been read by
+    // every consumer.  Returns false on a time-out.
+    __device__ bool publish(uint32_t m, int item, uint64_t wait_ns) const {
+        if (m >= (uint32_t)kRingSlots &&
+            !mbar_wait_bounded(empty + 8 * (m % kRingSlots), (m / kRingSlots - 1) & 1u, wait_ns))
+            return false;
+        items[m % kRingSlots] = item;
+        mbar_arrive(full + 8 * (m % kRingSlots));
+        return true;
+    }
+
+    // A scheduler warp's one thread: fills the ring, each entry once entry
+    // m - kRingLead has been taken by the first consumer, until the items run
+    // out (or `abort_flag` is set), then writes -1.  Returns false on a
+    // time-out.
+    template <class C, bool WIN>
+    __device__ bool run(const AttnParams& p, const volatile uint32_t* abort_flag) const {
+        Cursor cur;
         for (uint32_t m = 0;; ++m) {
             if (m >= (uint32_t)kRingLead &&
                 !mbar_wait_bounded(taken + 8 * ((m - kRingLead) % kRingSlots),
                                    ((m - kRingLead) / kRingSlots) & 1u, p.wait_ns))
                 return false;
-            if (m >= (uint32_t)kRingSlots &&
-                !mbar_wait_bounded(empty + 8 * (m % kRingSlots), (m / kRingSlots - 1) & 1u, p.wait_ns))
-                return false;
-            int item = -1;
-            while (!*abort_flag) {
-                unsigned cand;
-                if (!p.sched_ctr) {
-                    cand = next_static;
-                    next_static += gridDim.x;
-                } else if (first) {
-                    cand = blockIdx.x;
-                } else {
-                    cand = atomicAdd(p.sched_ctr, 1u) + gridDim.x;
-                }
-                first = false;
-                if (cand >= (unsigned)p.n_items) break;
-                if (plan_item<C, WIN>((int)cand, p).active) {
-                    item = (int)cand;
-                    break;
-                }
-            }
-            items[m % kRingSlots] = item;
-            mbar_arrive(full + 8 * (m % kRingSlots));
+            const int item = fetch<C, WIN>(p, cur, abort_flag);
+            if (!publish(m, item, p.wait_ns)) return false;
             if (item < 0) return true;
         }
     }

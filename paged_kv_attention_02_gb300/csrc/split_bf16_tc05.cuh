@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(SplitBf16Cfg<FEW, D>::NTHREADS, 1)
         reinterpret_cast<uint32_t*>(smem + C::OFF_FLAGS)[1] = 0u;
         mbar_init(bar_final, 1);
         mbar_init(bar_final + 8, 1);
-        iring.init(C::RING_CONSUMERS);
+        iring.init(C::RING_CONSUMERS, true);
         misc[1] = 0;
         fence_mbarrier_init();
     }

@@ -38,7 +38,10 @@
 //   warps 6, 7   K and V producers: page ids, the per-page K/V scales (into the
 //                K stage's meta block), one TMA box per page (page_size rows x
 //                128 bytes of the KV head, issued by lanes 0-7); pages outside
-//                the item's range load zeros.
+//                the item's range load zeros.  The K producer also takes the
+//                CTA's items from the counter shared by all CTAs and hands them
+//                to the other warps (sched.cuh), each after issuing the previous
+//                item's last tile.
 //   warps 8-11   converters, one per scheduler partition: converter c turns key
 //                rows 32c .. 32c+31 of every staged e4m3 V tile into f16 (a
 //                quarter-rate instruction: on the MMA or softmax warps it set
@@ -54,6 +57,7 @@
 #include <cuda.h>
 
 #include "attn_tile.cuh"
+#include "sched.cuh"
 #include "tc05.cuh"
 
 #ifndef RAD_SPLITTC_NSK
@@ -92,7 +96,7 @@ struct SplitTcCfg {
     static constexpr int V16_BYTES = 2 * ATOM;
     static constexpr int Q8_TERM = 128 * 128;       // one e4m3 term of the four copies of the rows
     static constexpr int MAXPG = BK / 16;           // pages per tile
-    static constexpr int META_STRIDE = 128;         // ks[8], vs[8], bad
+    static constexpr int META_STRIDE = 80;          // ks[8], vs[8], bad
     static constexpr int SCR_BYTES = 4 * 32 * 128;  // the merge: [warp][row][32 floats], chunks swizzled
     static constexpr int OFF_Q8 = 0;
     static constexpr int OFF_K = OFF_Q8 + 2 * Q8_TERM;
@@ -106,9 +110,11 @@ struct SplitTcCfg {
     // q8_full, q8_empty, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[2], p_full[2],
     // pv_done[2], v16_full[2], o_free, final[2]
     static constexpr int NBARS = 2 + 2 * NSK + 2 * NSV + 2 + 2 + 2 + 2 + 1 + 2;
-    static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
+    static constexpr int OFF_RING = OFF_BARS + NBARS * 8;     // the item ring (sched.cuh)
+    static constexpr int OFF_MISC = OFF_RING + kRingBytesNoTaken;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // 1 KB alignment of the swizzled tiles
     static constexpr int NTHREADS = 12 * 32;
+    static constexpr int RING_CONSUMERS = 11;                 // every warp but the K producer, which fills it
     static constexpr int W_QK = 4, W_PV = 5, W_PROD_K = 6, W_PROD_V = 7, W_CONV = 8;
     static constexpr int K_FULL_ARRIVALS = MAXPG;             // expect-tx arrive + 7 lanes' meta arrives
     static constexpr int K_EMPTY_ARRIVALS = 1 + 4;            // the QK commit + the softmax warps' scale reads
@@ -178,6 +184,7 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
     const uint32_t bar_final = bar_o_free + 8;              // [2]: QK warp, PV warp
     volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);  // [0] tmem, [1] abort
     float* const isq_s = reinterpret_cast<float*>(smem + C::OFF_ISQ);
+    const ItemRing iring(smem + C::OFF_RING, base + C::OFF_RING);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -202,6 +209,7 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
         mbar_init(bar_o_free, 4);
         mbar_init(bar_final, 1);
         mbar_init(bar_final + 8, 1);
+        iring.init(C::RING_CONSUMERS, false);
         misc[1] = 0;
         fence_mbarrier_init();
     }
@@ -235,7 +243,27 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
         const int oob_tok = p.num_pages * P;   // a row past the pool: TMA fills the box with zeros
         uint32_t sc = 0;
         if (lane == 0) prefetch_tmap(tm);
-        for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
+        ItemRing::Cursor cur;
+        for (uint32_t n = 0; !abort; ++n) {
+            int item = -1;
+            if (is_k) {
+                // the next item, fetched and handed out while the stages still
+                // hold the previous item's last tiles
+                bool ok = true;
+                if (lane == 0) {
+                    item = iring.fetch<C, WIN>(p, cur, misc + 1);
+                    ok = iring.publish(n, item, p.wait_ns);
+                }
+                item = __shfl_sync(0xffffffffu, item, 0);
+                if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                    abort = true;
+                    break;
+                }
+            } else if (!iring.take(n, item, p.wait_ns, false)) {
+                abort = true;
+                break;
+            }
+            if (item < 0) break;
             const ItemPlan it = plan_item<C, WIN>(item, p);
             if (!real(it)) continue;
             const int page_hi = (it.k1 + P - 1) / P;
@@ -309,7 +337,13 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
         // ===================================================== converters
         const int cv = warp - C::W_CONV;   // key rows 32cv .. 32cv+31 of every V tile; query-row copy cv
         uint32_t tc = 0, ic = 0;
-        for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
+        for (uint32_t n = 0; !abort; ++n) {
+            int item;
+            if (!iring.take(n, item, p.wait_ns, false)) {
+                abort = true;
+                break;
+            }
+            if (item < 0) break;
             const ItemPlan it = plan_item<C, WIN>(item, p);
             if (!real(it)) continue;
             // ---- this copy of the item's query rows as two e4m3 terms, once the
@@ -400,7 +434,13 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
         constexpr uint32_t idesc_qk = umma_idesc_e4m3(128, C::BK);
         uint32_t tc = 0, ic = 0;
         bool issued = false;
-        for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
+        for (uint32_t n = 0; !abort; ++n) {
+            int item;
+            if (!iring.take(n, item, p.wait_ns, false)) {
+                abort = true;
+                break;
+            }
+            if (item < 0) break;
             const ItemPlan it = plan_item<C, WIN>(item, p);
             if (!real(it)) continue;
             const int T = it.n_stages;
@@ -451,7 +491,13 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
         constexpr uint32_t idesc_pv = umma_idesc_f16(128, C::D, 0, 1);
         uint32_t tc = 0, ic = 0;
         bool issued = false;
-        for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
+        for (uint32_t n = 0; !abort; ++n) {
+            int item;
+            if (!iring.take(n, item, p.wait_ns, false)) {
+                abort = true;
+                break;
+            }
+            if (item < 0) break;
             const ItemPlan it = plan_item<C, WIN>(item, p);
             if (!real(it)) continue;
             const int T = it.n_stages;
@@ -504,7 +550,13 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
             tmem_wait_st();
         }
         uint32_t tc = 0, ic = 0;
-        for (int item = blockIdx.x; item < p.n_items && !abort; item += gridDim.x) {
+        for (uint32_t n = 0; !abort; ++n) {
+            int item;
+            if (!iring.take(n, item, p.wait_ns, false)) {
+                abort = true;
+                break;
+            }
+            if (item < 0) break;
             const ItemPlan it = plan_item<C, WIN>(item, p);
             if (!it.active) continue;
             const int nrows = it.m_end - it.m0;
