@@ -48,17 +48,36 @@ FALLBACK_HBM_GBS = 6800.0
 
 # DRAM traffic per launch of the dominant kernel plus the combine, from the
 # committed ncu captures (a capture of fewer sequences scaled by the KV bytes
-# where the workload is too large to capture), valid only while the kernel
-# sources hash to `src_sha256`.
+# where the workload is too large to capture), valid only while the sources
+# that kernel is built from hash to `src_sha256`.
+_BF16_SPLIT_SOURCES = ("split_bf16_tc05.cuh", "sched.cuh", "attn_tile.cuh", "tc05.cuh", "ptx.cuh", "combine.cuh",
+                       "launch.cuh", "tile_configs.cuh", "kern_split_bf16_tc05.cu", "kern_split_bf16_tc05_d256.cu",
+                       "rad_attn.cu")
+_E4M3_SPLIT_SOURCES = ("split_tc05.cuh", "sched.cuh", "attn_tile.cuh", "tc05.cuh", "ptx.cuh", "combine.cuh",
+                       "launch.cuh", "tile_configs.cuh", "kern_split_tc05.cu", "rad_attn.cu")
 NCU_TRAFFIC: dict[str, dict] = {
-    "batched_decode": {"bytes_per_launch": 4_499_500_000 + 20_200_000,
-                       "src_sha256": "d9c485962b741bef7061e794a1ade571092f6afaced02c5fea4373d38c12118b"},
+    "batched_decode": {"bytes_per_launch": 4_532_758_546, "sources": _BF16_SPLIT_SOURCES,
+                       "src_sha256": "2c31db0c9fd78129262051e538642ec38a6226436ba76032125a75807ead07c6",
+                       "capture": "64 sequences, scaled by the KV bytes (x 4.3412)"},
+    "hybrid_decode": {"bytes_per_launch": 2_295_206_334, "sources": _BF16_SPLIT_SOURCES,
+                      "src_sha256": "2c31db0c9fd78129262051e538642ec38a6226436ba76032125a75807ead07c6",
+                      "capture": "32 sequences, scaled by the KV bytes (x 3.8372)"},
+    "spec_verify": {"bytes_per_launch": 1_284_122_492, "sources": _E4M3_SPLIT_SOURCES,
+                    "src_sha256": "b49bacb64e8f9d7dd8026127aaf7c9be22f8458c49dfcacd40206f1615d820b0",
+                    "capture": "16 sequences, scaled by the KV bytes (x 4.4698)"},
+    "tiny_decode": {"bytes_per_launch": 678_400, "sources": _BF16_SPLIT_SOURCES,
+                    "src_sha256": "2c31db0c9fd78129262051e538642ec38a6226436ba76032125a75807ead07c6",
+                    "capture": "the whole workload"},
 }
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(names=None) -> str:
+    """sha256 over the named files of csrc/ (all of them by default), in name order."""
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "paged_kv_attention_02_gb300", "csrc", "*"))):
+    csrc = os.path.join(ROOT, "paged_kv_attention_02_gb300", "csrc")
+    paths = sorted(glob.glob(os.path.join(csrc, "*"))) if names is None else \
+        [os.path.join(csrc, n) for n in sorted(names)]
+    for p in paths:
         with open(p, "rb") as f:
             h.update(os.path.basename(p).encode())
             h.update(f.read())
@@ -449,7 +468,7 @@ def measure_device(st: Step, steps: int, warmup: int, world: int, sampler: Clock
 def roofline_of(w: wl.Workload, ms: float, desc: str) -> dict:
     nbytes = wl.kv_bytes(w) + wl.aux_bytes(w)
     tr = NCU_TRAFFIC.get(w.cfg.name)
-    traffic = tr["bytes_per_launch"] if tr and tr.get("src_sha256") == kernel_source_hash() else None
+    traffic = tr["bytes_per_launch"] if tr and tr.get("src_sha256") == kernel_source_hash(tr["sources"]) else None
     if "split_len=0" in desc:
         # a prefill chunk (no splits): bound by the tensor pipe, not by HBM
         tpeak, tpeak_src = tensor_peak()

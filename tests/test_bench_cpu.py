@@ -42,3 +42,15 @@ def test_roofline_peaks_come_from_the_measured_file():
         peaks = json.load(f)
     assert bench.hbm_peak() == (float(peaks["hbm_gbs"]), "measured")
     assert bench.tensor_peak() == (float(peaks["bf16_tflops"]), "measured")
+
+
+def test_traffic_figures_name_existing_kernel_sources():
+    # each recorded ncu traffic figure is tied to files that exist, and is
+    # reported only while they hash to the recorded value
+    csrc = os.path.join(bench.ROOT, "paged_kv_attention_02_gb300", "csrc")
+    for name, tr in bench.NCU_TRAFFIC.items():
+        assert name in wl.CONFIGS
+        assert tr["bytes_per_launch"] > 0 and len(tr["src_sha256"]) == 64
+        for f in tr["sources"]:
+            assert os.path.exists(os.path.join(csrc, f)), f
+    assert bench.kernel_source_hash(["ptx.cuh"]) != bench.kernel_source_hash(["tc05.cuh"])
