@@ -120,8 +120,9 @@ enum {
  * (0 is possible).  A pure function of its arguments; no device access.
  * Returns 0 as well for shapes rad_attn_paged would refuse.  The workspace
  * holds per-split partial results ("kern manifest v7", $defs.Impl `scratch`:
- * implementation-private buffers) and, for the tcgen05 split kernels, a work
- * counter that the call zeroes with a 4-byte cudaMemsetAsync on its stream
+ * implementation-private buffers) and, for the tcgen05 split kernels and the
+ * fp8 prefill kernel, a work counter that the call zeroes with a 4-byte
+ * cudaMemsetAsync on its stream
  * before the kernel (stream-ordered, so it is captured with the call in a CUDA
  * graph).  It is dead between calls; calls that may run concurrently need
  * separate workspaces.

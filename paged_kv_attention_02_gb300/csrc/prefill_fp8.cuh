@@ -6,8 +6,8 @@
 // Work items, masks and the item order are those of the bf16 tcgen05 prefill
 // kernel (prefill_tc05.cuh): (sequence g, KV head kvh, 128 query rows), keys
 // 0 .. kmax-1, causal per row, an optional sliding window.  The CTAs take the
-// items with a plain stride: the snake that the bf16 kernel uses measured 3%
-// slower here.
+// items, heavier query tiles first, from a counter shared by all CTAs
+// (sched.cuh), the K producer handing each CTA's items to its other warps.
 //
 //   S_j  = Q K_j^T     kind::f8f6f4, M 128 query rows, N 128 keys, K = head_dim:
 //                      K straight from the TMA-staged e4m3 rows; each query row
@@ -51,6 +51,7 @@
 #include <cuda.h>
 
 #include "prefill_tc05.cuh"
+#include "sched.cuh"
 #include "tc05.cuh"
 
 namespace rad {
@@ -76,7 +77,9 @@ struct PrefillFp8Cfg {
     // q8_full, q8_empty, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[2], p_full[2],
     // pv_done[2], v16_full[2], o_free, final[2]
     static constexpr int NBARS = 2 + 2 * NSK + 2 * NSV + 2 + 2 + 2 + 2 + 1 + 2;
-    static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
+    static constexpr int OFF_RING = OFF_BARS + NBARS * 8;     // the item ring (sched.cuh)
+    static constexpr int OFF_MISC = OFF_RING + kRingBytesNoTaken;
+    static constexpr int RING_CONSUMERS = 7;                 // every warp but the K producer, which fills it
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // 1 KB alignment of the swizzled tiles
     static constexpr int NTHREADS = 8 * 32;   // 8 warps: the softmax threads keep 255 registers
     static constexpr int W_QK = 4, W_V = 5, W_PROD_K = 6, W_PROD_V = 7;
@@ -150,6 +153,7 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
     const uint32_t bar_o_free = bar_v16_full + 16;
     const uint32_t bar_final = bar_o_free + 8;
     volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);  // [0] tmem, [1] abort
+    const ItemRing iring(smem + C::OFF_RING, base + C::OFF_RING);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -174,6 +178,7 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
         mbar_init(bar_o_free, 4);
         mbar_init(bar_final, 1);
         mbar_init(bar_final + 8, 1);
+        iring.init(C::RING_CONSUMERS, false);
         misc[1] = 0;
         fence_mbarrier_init();
     }
@@ -188,7 +193,6 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
     const uint32_t t_o = tmem;
     const uint32_t t_s = tmem + 128;   // S buffer b at t_s + BN*b
 
-    const int n_items = p.n_items;
     const int P = p.page_size;
     const int ppt = C::BN / P;       // pages per key tile (8 or 4)
     bool abort = false;
@@ -205,11 +209,34 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
         const int oob_tok = p.num_pages * P;
         uint32_t sc = 0;
         if (lane == 0) prefetch_tmap(tm);
-        for (int rd = 0; rd * (int)gridDim.x < n_items && !abort; ++rd) {
-            const int item = prefill_item_of<false>(rd, blockIdx.x, gridDim.x);
-            if (item >= n_items) break;
+        // The K producer fills the item ring (sched.cuh): entry n + 1 right after
+        // it issued entry n's last tile (at once for an invalid sequence).
+        ItemRing::Cursor cur;
+        int next = -1;
+        const auto publish_next = [&](uint32_t m) {
+            bool ok = true;
+            if (lane == 0) {
+                next = iring.fetch_if(p, cur, misc + 1, [](int) { return true; });
+                ok = iring.publish(m, next, p.wait_ns);
+            }
+            next = __shfl_sync(0xffffffffu, next, 0);
+            return __shfl_sync(0xffffffffu, ok, 0);
+        };
+        if (is_k && !publish_next(0)) abort = true;
+        for (uint32_t n = 0; !abort; ++n) {
+            int item = -1;
+            if (is_k) {
+                item = next;
+            } else if (!iring.take(n, item, p.wait_ns, false)) {
+                abort = true;
+                break;
+            }
+            if (item < 0) break;
             const PrefItem it = plan_prefill<GEN, C::BM, C::BN>(item, p);
-            if (!it.seq_ok) continue;
+            if (!it.seq_ok) {
+                if (is_k && !publish_next(n + 1)) abort = true;
+                continue;
+            }
             const int page_hi = (it.kmax + P - 1) / P;
             const int page_lo = GEN ? it.klo / P : 0;   // pages below hold no visible key: never read
             const int32_t* trow = p.page_table + (long long)it.g * p.pages_per_seq;
@@ -263,7 +290,14 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
                     if (lane == 0) tma_load_3d(dst + (uint32_t)(i * P * 128), tm, bar_full + 8 * st, 0, it.kvh, tok, pol);
                 }
                 ++sc;
+                // the next item, RAD_PREFILL_PUBLISH_LEAD tiles before this one's last
+                if (is_k && j == it.T - 1 - RAD_PREFILL_PUBLISH_LEAD && !publish_next(n + 1)) {
+                    abort = true;
+                    break;
+                }
             }
+            // the next item, if this one had too few tiles to hand it out earlier
+            if (is_k && !abort && it.T <= RAD_PREFILL_PUBLISH_LEAD && !publish_next(n + 1)) abort = true;
             if (misc[1]) abort = true;
         }
         // drain: nothing may still be landing in shared memory at exit
@@ -277,9 +311,13 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
         constexpr uint32_t idesc_qk = umma_idesc_e4m3(C::BM, C::BN);
         uint32_t sc = 0, tc = 0, ic = 0;
         bool issued = false;
-        for (int rd = 0; rd * (int)gridDim.x < n_items && !abort; ++rd) {
-            const int item = prefill_item_of<false>(rd, blockIdx.x, gridDim.x);
-            if (item >= n_items) break;
+        for (uint32_t n = 0; !abort; ++n) {
+            int item;
+            if (!iring.take(n, item, p.wait_ns, false)) {
+                abort = true;
+                break;
+            }
+            if (item < 0) break;
             const PrefItem it = plan_prefill<GEN, C::BM, C::BN>(item, p);
             if (!it.seq_ok) continue;
             if (!mbar_wait_bounded(bar_q8_full, ic & 1u, p.wait_ns)) {
@@ -345,9 +383,13 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
         constexpr uint32_t idesc_pv = umma_idesc_f16(C::BM, C::D, 0, 1);
         uint32_t sc = 0, tc = 0, ic = 0;
         bool issued = false;
-        for (int rd = 0; rd * (int)gridDim.x < n_items && !abort; ++rd) {
-            const int item = prefill_item_of<false>(rd, blockIdx.x, gridDim.x);
-            if (item >= n_items) break;
+        for (uint32_t n = 0; !abort; ++n) {
+            int item;
+            if (!iring.take(n, item, p.wait_ns, false)) {
+                abort = true;
+                break;
+            }
+            if (item < 0) break;
             const PrefItem it = plan_prefill<GEN, C::BM, C::BN>(item, p);
             if (!it.seq_ok) continue;
             const int zlo = GEN ? it.klo : 0;   // keys below the tile's window may hold anything
@@ -405,9 +447,13 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;      // this warp's TMEM lanes
         const int lp = (P == 16) ? 4 : 5;
         uint32_t sc = 0, tc = 0, ic = 0;
-        for (int rd = 0; rd * (int)gridDim.x < n_items && !abort; ++rd) {
-            const int item = prefill_item_of<false>(rd, blockIdx.x, gridDim.x);
-            if (item >= n_items) break;
+        for (uint32_t n = 0; !abort; ++n) {
+            int item;
+            if (!iring.take(n, item, p.wait_ns, false)) {
+                abort = true;
+                break;
+            }
+            if (item < 0) break;
             const PrefItem it = plan_prefill<GEN, C::BM, C::BN>(item, p);
             const int m = it.m0 + t;
             const bool valid = m < it.m_end;

@@ -148,8 +148,11 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
         pl.ml_bytes = round_up((size_t)slots * pl.qtv * 2 * 4, 256);
         pl.acc_bytes = round_up((size_t)slots * pl.qtv * head_dim * 4, 256);
     }
-    // the tcgen05 split kernels' shared item counter (zeroed before each launch that uses it)
-    if (pl.family == rad::kFamSplitBf || pl.family == rad::kFamSplitTC) pl.sched_bytes = 256;
+    // the tcgen05 kernels' shared item counter (zeroed before each launch that uses it); the
+    // bf16 prefill kernel deals its items in a fixed snake order instead
+    if (pl.family == rad::kFamSplitBf || pl.family == rad::kFamSplitTC ||
+        (pl.family == rad::kFamPrefillTC && kv_dtype == RAD_KV_FP8_E4M3))
+        pl.sched_bytes = 256;
     pl.total_bytes = pl.sched_bytes + pl.map_bytes + pl.flags_bytes + pl.ml_bytes + pl.acc_bytes;
     pl.dual = pl.ragged && (pl.family == rad::kFamVerify || pl.family == rad::kFamWide);
     if (pl.dual) {

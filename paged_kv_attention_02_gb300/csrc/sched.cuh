@@ -78,10 +78,11 @@ struct ItemRing {
         unsigned next_static = blockIdx.x;
     };
 
-    // One thread: the CTA's next active item, or -1 once the items run out
-    // (or `abort_flag` is set).
-    template <class C, bool WIN>
-    __device__ int fetch(const AttnParams& p, Cursor& cur, const volatile uint32_t* abort_flag) const {
+    // One thread: the CTA's next item for which keep(item) holds, or -1 once
+    // the items run out (or `abort_flag` is set).
+    template <class Keep>
+    __device__ int fetch_if(const AttnParams& p, Cursor& cur, const volatile uint32_t* abort_flag,
+                            const Keep& keep) const {
         while (!*abort_flag) {
             unsigned cand;
             if (!p.sched_ctr) {
@@ -94,9 +95,15 @@ struct ItemRing {
             }
             cur.first = false;
             if (cand >= (unsigned)p.n_items) return -1;
-            if (plan_item<C, WIN>((int)cand, p).active) return (int)cand;
+            if (keep((int)cand)) return (int)cand;
         }
         return -1;
+    }
+
+    // The split kernels: the CTA's next active item (plan_item's `active`).
+    template <class C, bool WIN>
+    __device__ int fetch(const AttnParams& p, Cursor& cur, const volatile uint32_t* abort_flag) const {
+        return fetch_if(p, cur, abort_flag, [&](int item) { return plan_item<C, WIN>(item, p).active; });
     }
 
     // One thread: writes entry m once entry m - kRingSlots has been read by

@@ -123,6 +123,11 @@ template <> struct Pick<256, true,  kFamWide>   { using T = TileCfg<256, true,  
 #define RAD_PREFILL_CTAS 1
 #endif
 constexpr int PrefillTileKeys = RAD_PREFILL_BN;
+// The prefill kernels' K producer hands out the CTA's next item this many key
+// tiles before it issues the current item's last one.
+#ifndef RAD_PREFILL_PUBLISH_LEAD
+#define RAD_PREFILL_PUBLISH_LEAD 0
+#endif
 
 // Split calls (decode and verify shapes) share one key schedule: two key
 // warps take alternate 16-key sub-tiles in key order, so a query row's

@@ -88,7 +88,9 @@ def test_workspace_sizes():
     max_splits = -(-512 * 16 // split_len)
     ws = b.workspace_bytes(256, 1, 32, 8, 128, 16, 512)
     assert ws >= 256 * 8 * max_splits * (4 * 130 * 4 + 4)
-    assert b.workspace_bytes(1, 2048, 32, 8, 128, 16, 512) == 0      # prefill: no split
+    assert b.workspace_bytes(1, 2048, 32, 8, 128, 16, 512) == 0      # bf16 prefill: no split
+    assert b.workspace_bytes(1, 2048, 32, 8, 128, 16, 512, b.RAD_KV_FP8_E4M3) == 256   # fp8: the item counter
+    assert b.workspace_bytes(1, 2048, 32, 8, 256, 16, 512) == 0      # head_dim-256 prefill (tile kernel): none
     assert b.workspace_bytes(0, 1, 32, 8, 128, 16, 512) == 0
     assert b.workspace_bytes(4, 1, 8, 2, 96, 16, 19) == 0
 
@@ -217,9 +219,10 @@ def test_ex_workspace_follows_the_kernel_the_call_takes():
     small.total_rows = -1
     assert ws(small) == 0
     assert int(b.load().rad_attn_paged_ex(ctypes.byref(small), None)) == b.RAD_E_ARG
-    # chunks past the split limit need no partials: a uniform call needs
-    # nothing, a ragged one its tile maps (4 x ceil(1200 / 64) tiles x 8 bytes
-    # for the wide tile, 4 x 8 bytes for the decode tile, each rounded to 256)
+    # chunks past the split limit need no partials: a uniform call over bf16
+    # pools needs nothing, a ragged one (on the tile kernels) its tile maps
+    # (4 x ceil(1200 / 64) tiles x 8 bytes for the wide tile, 4 x 8 bytes for
+    # the decode tile, each rounded to 256)
     assert b.workspace_bytes(4, 300, 32, 8, 128, 16, 64) == 0
     assert ws(_general_args(rows=300, cu=fake)) == 768 + 256
     bad = _general_args()
