@@ -82,9 +82,9 @@ bool use_prefill_tc(int32_t rows, int32_t ratio, int32_t head_dim, int32_t kv_dt
 }
 
 // `general`: a call with ragged rows (cu_seqlens) or tree masks.  Split calls
-// with head_dim 128 (both pool types) or with bf16 pools (both head dims) run
-// on the tcgen05 split kernels whether ragged or not, with or without tree
-// masks; the others on the tile kernels.  `ragged_rows`
+// (both head dims, both pool types) run on the tcgen05 split kernels whether
+// ragged or not, with or without tree masks; longer calls that the prefill
+// kernels do not take, on the tile kernels.  `ragged_rows`
 // >= 0 marks a ragged call: its work and workspace run
 // over the call's query tiles, bounded with the caller's total of rows when
 // it gives one (> 0), else with `rows` rows per sequence.
@@ -100,7 +100,7 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
     // it applies, else the wide tile.
     pl.split_len = rows <= rad::kSplitMaxRows ? rad::kSplitLen : 0;
     const bool ragged = ragged_rows >= 0;
-    if (pl.split_len > 0 && RAD_SPLIT_TC05 && head_dim == 128 && kv_dtype == RAD_KV_FP8_E4M3) {
+    if (pl.split_len > 0 && kv_dtype == RAD_KV_FP8_E4M3 && (head_dim == 128 ? RAD_SPLIT_TC05 : RAD_SPLIT_TC05_D256)) {
         pl.family = rad::kFamSplitTC;
         pl.split_len = rad::kSplitLenTC;
     }
@@ -118,7 +118,7 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
         pl.tile = rad::TileInfo{128, 0, 4, 0, 0, rad::PrefillTileKeys, RAD_PREFILL_NSK + RAD_PREFILL_NSV, 128, 256, 0,
                                 RAD_PREFILL_CTAS};
     else if (pl.family == rad::kFamSplitTC)
-        pl.tile = rad::split_tc05_info(pl.M <= 8);
+        pl.tile = rad::split_tc05_info(pl.M <= 8, head_dim);
     else if (pl.family == rad::kFamSplitBf)
         pl.tile = rad::split_bf16_tc05_info(pl.M <= 8, head_dim);
     else
@@ -476,17 +476,19 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
     if ((pl.family == rad::kFamPrefillTC && fp8) || pl.family == rad::kFamSplitTC) {
         rc = get_encoder();
         if (rc != RAD_OK) return rc;
-        // e4m3 pools viewed as [tokens][n_head_kv][128 bytes]: one box = one page of one KV head
+        // e4m3 pools viewed as [tokens][n_head_kv][head_dim bytes]: one box = one page of one
+        // KV head x 128 bytes (the 128-byte swizzle's span: two boxes a page at head_dim 256)
         const cuuint64_t kd[3] = {(cuuint64_t)head_dim, (cuuint64_t)n_head_kv,
                                   (cuuint64_t)num_pages * (cuuint64_t)page_size};
         const cuuint64_t ks[2] = {(cuuint64_t)head_dim, (cuuint64_t)n_head_kv * head_dim};
-        const cuuint32_t kb[3] = {(cuuint32_t)head_dim, 1, (cuuint32_t)page_size};
+        const cuuint32_t kb[3] = {128, 1, (cuuint32_t)page_size};
         CUtensorMap tk, tv;
         if (encode_map(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, k_pool, 3, kd, ks, kb) != RAD_OK ||
             encode_map(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, v_pool, 3, kd, ks, kb) != RAD_OK)
             return RAD_E_CUDA;
-        e = pl.family == rad::kFamSplitTC ? rad::launch_split_tc05(tk, tv, p, sms, st, pl.M <= 8)
-                                          : rad::launch_prefill_fp8(tk, tv, p, sms, st);
+        e = pl.family != rad::kFamSplitTC ? rad::launch_prefill_fp8(tk, tv, p, sms, st)
+            : head_dim == 128             ? rad::launch_split_tc05(tk, tv, p, sms, st, pl.M <= 8)
+                                          : rad::launch_split_tc05_d256(tk, tv, p, sms, st);
     } else if (pl.family == rad::kFamSplitBf) {
         rc = get_encoder();
         if (rc != RAD_OK) return rc;

@@ -142,22 +142,6 @@ struct SplitBf16Cfg {
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-// Loads and stores of N consecutive 32-bit TMEM columns of a warp's lanes.
-template <int N>
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]) {
-    static_assert(N == 8 || N == 16 || N == 32, "8, 16 or 32 columns");
-    if constexpr (N == 32) tmem_ld32(taddr, r);
-    else if constexpr (N == 16) tmem_ld16(taddr, r);
-    else tmem_ld8(taddr, r);
-}
-template <int N>
-__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[N]) {
-    static_assert(N == 8 || N == 16 || N == 32, "8, 16 or 32 columns");
-    if constexpr (N == 32) tmem_st32(taddr, r);
-    else if constexpr (N == 16) tmem_st16(taddr, r);
-    else tmem_st8(taddr, r);
-}
-
 // MODE: kModeCausal, kModeWindow or kModeTree (draft-tree rows, uniform row
 // counts: bit i of a row's mask word lets it see the call's key i).
 template <int MODE, bool FEW, int D = 128>

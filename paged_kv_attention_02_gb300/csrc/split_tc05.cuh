@@ -73,6 +73,13 @@
 #ifndef RAD_SPLITTC_NSV
 #define RAD_SPLITTC_NSV 3
 #endif
+// head_dim 256: the four query copies take 64 KB.
+#ifndef RAD_SPLITTC256_NSK
+#define RAD_SPLITTC256_NSK 3
+#endif
+#ifndef RAD_SPLITTC256_NSV
+#define RAD_SPLITTC256_NSV 2
+#endif
 
 namespace rad {
 
@@ -82,19 +89,25 @@ namespace rad {
 // other form.  (Holding a decode item's 8 rows once, with a zero 8-row group
 // stride in the QK descriptor as the bf16 kernel does, made this kernel's
 // decode slower.)
-template <bool FEW>
+template <bool FEW, int D_ = 128>
 struct SplitTcCfg {
-    static constexpr int D = 128;                   // head dim
-    static constexpr int BK = 128;                  // keys per tile
+    static constexpr int D = D_;                    // head dim: 128 or 256
+    static constexpr int BK = D == 128 ? 128 : 64;  // keys per tile (16 KB of e4m3 K rows either way)
+    static constexpr int NKB = D / 128;             // 128-byte column blocks of an e4m3 row
+    static constexpr int KW = BK / 4;               // keys of a tile per softmax warp
     static constexpr int QT = 32;                   // (item planner) query rows per item
     static constexpr int KS = BK;                   // (item planner) keys per stage
-    static constexpr int NSK = FEW ? RAD_SPLITTC_FEW_NSK : RAD_SPLITTC_NSK;   // K stages (with the page scales)
-    static constexpr int NSV = FEW ? RAD_SPLITTC_FEW_NSV : RAD_SPLITTC_NSV;   // V stages
-    static constexpr int ROW = 128;                 // bytes of one e4m3 key row
-    static constexpr int KV_TILE = BK * ROW;        // e4m3 K or V rows of one tile
+    static constexpr int NSK = D == 128 ? (FEW ? RAD_SPLITTC_FEW_NSK : RAD_SPLITTC_NSK)
+                                        : RAD_SPLITTC256_NSK;   // K stages (with the page scales)
+    static constexpr int NSV = D == 128 ? (FEW ? RAD_SPLITTC_FEW_NSV : RAD_SPLITTC_NSV)
+                                        : RAD_SPLITTC256_NSV;   // V stages
+    static constexpr int ROW = D;                   // bytes of one e4m3 key row
+    static constexpr int KBLK = BK * 128;           // one 128-byte column block of a K or V tile
+    static constexpr int KV_TILE = NKB * KBLK;      // e4m3 K or V rows of one tile
     static constexpr int ATOM = BK * 128;           // one 64-column block of the f16 V tile
-    static constexpr int V16_BYTES = 2 * ATOM;
-    static constexpr int Q8_TERM = 128 * 128;       // one e4m3 term of the four copies of the rows
+    static constexpr int V16_BYTES = (D / 64) * ATOM;
+    static constexpr int Q8_BLK = 128 * 128;        // one 128-byte column block of the four copies of the rows
+    static constexpr int Q8_TERM = NKB * Q8_BLK;    // one e4m3 term of the four copies
     static constexpr int MAXPG = BK / 16;           // pages per tile
     static constexpr int META_STRIDE = 80;          // ks[8], vs[8], bad
     static constexpr int SCR_BYTES = 4 * 32 * 128;  // the merge: [warp][row][32 floats], chunks swizzled
@@ -116,20 +129,25 @@ struct SplitTcCfg {
     static constexpr int NTHREADS = 12 * 32;
     static constexpr int RING_CONSUMERS = 11;                 // every warp but the K producer, which fills it
     static constexpr int W_QK = 4, W_PV = 5, W_PROD_K = 6, W_PROD_V = 7, W_CONV = 8;
-    static constexpr int K_FULL_ARRIVALS = MAXPG;             // expect-tx arrive + 7 lanes' meta arrives
+    static constexpr int K_FULL_ARRIVALS = MAXPG;             // expect-tx arrive + the other page lanes' meta arrives
     static constexpr int K_EMPTY_ARRIVALS = 1 + 4;            // the QK commit + the softmax warps' scale reads
-    static constexpr uint32_t TMEM_COLS = 512;   // O [0,128), S_b [128 + 128b, ...), P_b [384 + 64b, ...)
+    // O [0, D), S_b [D + BK b, ...), P_b [D + 2 BK + (BK/2) b, ...)
+    static constexpr uint32_t TMEM_COLS = 512;
+    static_assert(D == 128 || D == 256, "head_dim 128 or 256");
+    static_assert(D + 2 * BK + BK <= (int)TMEM_COLS, "tensor memory budget");
     static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && OFF_V16 % 1024 == 0 && KV_TILE % 1024 == 0,
                   "1 KB tiles");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-// Key row `row` of a staged e4m3 V tile -> the f16 MN-major tile PV reads
-// (128-byte swizzle, two 64-column blocks); `zero` writes zeros (keys outside
-// the item: P is 0 there, the staged row may hold anything).  The row's loads
-// come before its stores, which may alias them as far as the compiler knows.
+// One 128-code column block of key row `row` of a staged e4m3 V tile (`stage`:
+// the block's [key][128 B] rows) -> the f16 MN-major tile PV reads (128-byte
+// swizzle; `v16`: the block's pair of 64-column blocks, ATOM bytes apart);
+// `zero` writes zeros (keys outside the item: P is 0 there, the staged row
+// may hold anything).  The row's loads come before its stores, which may alias
+// them as far as the compiler knows.
+template <int ATOM>
 __device__ __forceinline__ void convert_v_row(const uint8_t* stage, uint8_t* v16, int row, bool zero) {
-    using C = SplitTcCfg<false>;   // the f16 tile's layout is the same in both forms
     const uint32_t sw = (uint32_t)(row & 7);
     const uint8_t* src = stage + row * 128;
     uint8_t* dst = v16 + row * 128;
@@ -149,7 +167,7 @@ __device__ __forceinline__ void convert_v_row(const uint8_t* stage, uint8_t* v16
         const uint32_t h5 = e4m3x2_to_f16x2((uint16_t)(v.z >> 16));
         const uint32_t h6 = e4m3x2_to_f16x2((uint16_t)(v.w & 0xFFFFu));
         const uint32_t h7 = e4m3x2_to_f16x2((uint16_t)(v.w >> 16));
-        uint8_t* blk = dst + (ch >> 2) * C::ATOM;
+        uint8_t* blk = dst + (ch >> 2) * ATOM;
         const uint32_t c2 = (uint32_t)((ch & 3) * 2);
         *reinterpret_cast<uint4*>(blk + ((c2 ^ sw) << 4)) = make_uint4(h0, h1, h2, h3);
         *reinterpret_cast<uint4*>(blk + (((c2 + 1) ^ sw) << 4)) = make_uint4(h4, h5, h6, h7);
@@ -158,11 +176,11 @@ __device__ __forceinline__ void convert_v_row(const uint8_t* stage, uint8_t* v16
 
 // MODE: kModeCausal, kModeWindow or kModeTree (draft-tree rows, uniform row
 // counts: bit i of a row's mask word lets it see the call's key i).
-template <int MODE, bool FEW>
-__global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
+template <int MODE, bool FEW, int D = 128>
+__global__ void __launch_bounds__(SplitTcCfg<FEW, D>::NTHREADS, 1)
     attn_split_tc05_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                                 const __grid_constant__ AttnParams p) {
-    using C = SplitTcCfg<FEW>;
+    using C = SplitTcCfg<FEW, D>;
     constexpr bool WIN = MODE == kModeWindow;
     constexpr bool TREE = MODE == kModeTree;
     extern __shared__ uint8_t smem_raw[];
@@ -222,8 +240,8 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
     tc_fence_after();
     const uint32_t tmem = misc[0];
     const uint32_t t_o = tmem;
-    const uint32_t t_s = tmem + 128;   // S buffer b at t_s + 128 b
-    const uint32_t t_p = tmem + 384;   // P buffer b at t_p + 64 b
+    const uint32_t t_s = tmem + C::D;                // S buffer b at t_s + BK b
+    const uint32_t t_p = tmem + C::D + 2 * C::BK;    // P buffer b at t_p + (BK/2) b
     bool abort = false;
 
     // items that run the pipeline: active, a valid sequence length, keys to see
@@ -300,7 +318,6 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
                 const int srcl = (pstart - batch0 + lane) & 31;
                 const int pg = __shfl_sync(0xffffffffu, my_pg, srcl);
                 const bool mine = lane < ppt;
-                const bool live = mine && (!WIN || pi >= page_lo) && pi < page_hi;
                 if (is_k) {
                     // each of lanes 0 .. MAXPG-1 releases its own meta entries with its arrive
                     const float ksl = __shfl_sync(0xffffffffu, my_ks, srcl);
@@ -315,12 +332,26 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
                     if (lane == 0) reinterpret_cast<uint32_t*>(meta)[16] = bad_any ? kErrPage : 0u;
                     if (lane > 0 && lane < C::MAXPG) mbar_arrive(bar_full + 8 * st);
                 }
-                // one 3-D box per page (P rows x 128 bytes of this KV head, 128-byte swizzle)
+                // one 3-D box per page and 128-byte column block (P rows x 128 bytes of this
+                // KV head, 128-byte swizzle), issued by lanes 0 .. NKB * ppt - 1: lane i
+                // loads page i % ppt, block i / ppt
                 if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * st, (uint32_t)C::KV_TILE);
                 __syncwarp();
-                if (mine)
-                    tma_load_3d(ring + st * C::KV_TILE + (uint32_t)(lane * P * C::ROW), tm, bar_full + 8 * st, 0,
-                                it.kvh, live ? pg * P : oob_tok, pol_kv);
+                if constexpr (C::NKB == 1) {
+                    const bool live = mine && (!WIN || pi >= page_lo) && pi < page_hi;
+                    if (mine)
+                        tma_load_3d(ring + st * C::KV_TILE + (uint32_t)(lane * P * 128), tm, bar_full + 8 * st, 0,
+                                    it.kvh, live ? pg * P : oob_tok, pol_kv);
+                } else {
+                    const int pl = lane % ppt, kb = lane / ppt;
+                    const int pib = pstart + pl;
+                    const int pgb = __shfl_sync(0xffffffffu, my_pg, (pstart - batch0 + pl) & 31);
+                    const bool boxl = lane < C::NKB * ppt;
+                    const bool liveb = boxl && (!WIN || pib >= page_lo) && pib < page_hi;
+                    if (boxl)
+                        tma_load_3d(ring + st * C::KV_TILE + (uint32_t)(kb * C::KBLK + pl * P * 128), tm,
+                                    bar_full + 8 * st, kb * 128, it.kvh, liveb ? pgb * P : oob_tok, pol_kv);
+                }
                 __syncwarp();
                 ++sc;
             }
@@ -335,7 +366,7 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
         __syncwarp();
     } else if (warp >= C::W_CONV) {
         // ===================================================== converters
-        const int cv = warp - C::W_CONV;   // key rows 32cv .. 32cv+31 of every V tile; query-row copy cv
+        const int cv = warp - C::W_CONV;   // (row, block) pairs 32cv .. 32cv+31 of every V tile; query-row copy cv
         uint32_t tc = 0, ic = 0;
         for (uint32_t n = 0; !abort; ++n) {
             int item;
@@ -358,48 +389,102 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
                 const bool valid = r < nrows;
                 const int m = it.m0 + r;
                 const int tok = m / p.ratio, hl = m - tok * p.ratio;
-                uint4 qv[16];
-                const __nv_bfloat16* qrow = p.q + ((it.qrow0 + tok) * p.n_head + it.kvh * p.ratio + hl) * C::D;
+                if constexpr (C::D == 128) {
+                    uint4 qv[16];
+                    const __nv_bfloat16* qrow = p.q + ((it.qrow0 + tok) * p.n_head + it.kvh * p.ratio + hl) * C::D;
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    qv[i] = valid ? __ldg(reinterpret_cast<const uint4*>(qrow) + i) : make_uint4(0u, 0u, 0u, 0u);
-                float amax = 0.f;
+                    for (int i = 0; i < 16; ++i)
+                        qv[i] = valid ? __ldg(reinterpret_cast<const uint4*>(qrow) + i) : make_uint4(0u, 0u, 0u, 0u);
+                    float amax = 0.f;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const uint32_t x[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
+                    for (int i = 0; i < 16; ++i) {
+                        const uint32_t x[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(x[e])), fabsf(bf16_hi(x[e]))));
-                }
-                // 2^k with amax * 2^k in [128, 256): k = 7 - floor(log2 amax), kept a normal float
-                const int ex = amax > 0.f ? (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 : 7;
-                const int kx = max(-126, min(127, 7 - ex));
-                const float sq = __uint_as_float((uint32_t)(kx + 127) << 23);
-                if (cv == 0) isq_s[(ic & 1u) * 32 + r] = __uint_as_float((uint32_t)(127 - kx) << 23);
-                const int qr = 32 * cv + r;   // this copy's row of the M = 128 operand
-                uint8_t* q8 = smem + C::OFF_Q8 + qr * 128;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    // elements 16i .. 16i+15: chunk i of each term's row
-                    uint32_t wt[2][4];
-                    const uint32_t words[8] = {qv[2 * i].x,     qv[2 * i].y,     qv[2 * i].z,     qv[2 * i].w,
-                                               qv[2 * i + 1].x, qv[2 * i + 1].y, qv[2 * i + 1].z, qv[2 * i + 1].w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const uint32_t x0 = words[2 * e], x1 = words[2 * e + 1];
-                        const float v0 = bf16_lo(x0) * sq, v1 = bf16_hi(x0) * sq;
-                        const float v2 = bf16_lo(x1) * sq, v3 = bf16_hi(x1) * sq;
-                        const uint32_t h01 = f32x2_to_e4m3x2(v0, v1), h23 = f32x2_to_e4m3x2(v2, v3);
-                        const float2 a01 = e4m3x2_to_f32x2(h01), a23 = e4m3x2_to_f32x2(h23);
-                        const uint32_t l01 = f32x2_to_e4m3x2(v0 - a01.x, v1 - a01.y);
-                        const uint32_t l23 = f32x2_to_e4m3x2(v2 - a23.x, v3 - a23.y);
-                        wt[0][e] = h01 | (h23 << 16);
-                        wt[1][e] = l01 | (l23 << 16);
+                        for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(x[e])), fabsf(bf16_hi(x[e]))));
                     }
-                    const uint32_t off = (((uint32_t)i ^ (uint32_t)(qr & 7)) << 4);
+                    // 2^k with amax * 2^k in [128, 256): k = 7 - floor(log2 amax), kept a normal float
+                    const int ex = amax > 0.f ? (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 : 7;
+                    const int kx = max(-126, min(127, 7 - ex));
+                    const float sq = __uint_as_float((uint32_t)(kx + 127) << 23);
+                    if (cv == 0) isq_s[(ic & 1u) * 32 + r] = __uint_as_float((uint32_t)(127 - kx) << 23);
+                    const int qr = 32 * cv + r;   // this copy's row of the M = 128 operand
+                    uint8_t* q8 = smem + C::OFF_Q8 + qr * 128;
 #pragma unroll
-                    for (int term = 0; term < 2; ++term)
-                        *reinterpret_cast<uint4*>(q8 + term * C::Q8_TERM + off) =
-                            make_uint4(wt[term][0], wt[term][1], wt[term][2], wt[term][3]);
+                    for (int i = 0; i < 8; ++i) {
+                        // elements 16i .. 16i+15: chunk i of each term's row
+                        uint32_t wt[2][4];
+                        const uint32_t words[8] = {qv[2 * i].x,     qv[2 * i].y,     qv[2 * i].z,     qv[2 * i].w,
+                                                   qv[2 * i + 1].x, qv[2 * i + 1].y, qv[2 * i + 1].z, qv[2 * i + 1].w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const uint32_t x0 = words[2 * e], x1 = words[2 * e + 1];
+                            const float v0 = bf16_lo(x0) * sq, v1 = bf16_hi(x0) * sq;
+                            const float v2 = bf16_lo(x1) * sq, v3 = bf16_hi(x1) * sq;
+                            const uint32_t h01 = f32x2_to_e4m3x2(v0, v1), h23 = f32x2_to_e4m3x2(v2, v3);
+                            const float2 a01 = e4m3x2_to_f32x2(h01), a23 = e4m3x2_to_f32x2(h23);
+                            const uint32_t l01 = f32x2_to_e4m3x2(v0 - a01.x, v1 - a01.y);
+                            const uint32_t l23 = f32x2_to_e4m3x2(v2 - a23.x, v3 - a23.y);
+                            wt[0][e] = h01 | (h23 << 16);
+                            wt[1][e] = l01 | (l23 << 16);
+                        }
+                        const uint32_t off = (((uint32_t)i ^ (uint32_t)(qr & 7)) << 4);
+#pragma unroll
+                        for (int term = 0; term < 2; ++term)
+                            *reinterpret_cast<uint4*>(q8 + term * C::Q8_TERM + off) =
+                                make_uint4(wt[term][0], wt[term][1], wt[term][2], wt[term][3]);
+                    }
+                } else {
+                    // a 512-byte row: two passes, a quarter of it at a time (few
+                    // registers; the second pass reads it from L1): its largest
+                    // magnitude, then the terms
+                    const uint4* qrow =
+                        reinterpret_cast<const uint4*>(p.q + ((it.qrow0 + tok) * p.n_head + it.kvh * p.ratio + hl) * C::D);
+                    float amax = 0.f;
+#pragma unroll
+                    for (int h = 0; h < C::D / 64; ++h) {
+                        uint4 qv[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) qv[i] = valid ? __ldg(qrow + 8 * h + i) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const uint32_t x[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(x[e])), fabsf(bf16_hi(x[e]))));
+                        }
+                    }
+                    // 2^k with amax * 2^k in [128, 256): k = 7 - floor(log2 amax), kept a normal float
+                    const int ex = amax > 0.f ? (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 : 7;
+                    const int kx = max(-126, min(127, 7 - ex));
+                    const float sq = __uint_as_float((uint32_t)(kx + 127) << 23);
+                    if (cv == 0) isq_s[(ic & 1u) * 32 + r] = __uint_as_float((uint32_t)(127 - kx) << 23);
+                    const int qr = 32 * cv + r;   // this copy's row of the M = 128 operand
+#pragma unroll 4
+                    for (int i = 0; i < C::D / 16; ++i) {
+                        // elements 16i .. 16i+15: chunk i % 8 of column block i / 8 of each term's row
+                        uint32_t wt[2][4];
+                        const uint4 qa = valid ? __ldg(qrow + 2 * i) : make_uint4(0u, 0u, 0u, 0u);
+                        const uint4 qb = valid ? __ldg(qrow + 2 * i + 1) : make_uint4(0u, 0u, 0u, 0u);
+                        const uint32_t words[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const uint32_t x0 = words[2 * e], x1 = words[2 * e + 1];
+                            const float v0 = bf16_lo(x0) * sq, v1 = bf16_hi(x0) * sq;
+                            const float v2 = bf16_lo(x1) * sq, v3 = bf16_hi(x1) * sq;
+                            const uint32_t h01 = f32x2_to_e4m3x2(v0, v1), h23 = f32x2_to_e4m3x2(v2, v3);
+                            const float2 a01 = e4m3x2_to_f32x2(h01), a23 = e4m3x2_to_f32x2(h23);
+                            const uint32_t l01 = f32x2_to_e4m3x2(v0 - a01.x, v1 - a01.y);
+                            const uint32_t l23 = f32x2_to_e4m3x2(v2 - a23.x, v3 - a23.y);
+                            wt[0][e] = h01 | (h23 << 16);
+                            wt[1][e] = l01 | (l23 << 16);
+                        }
+                        uint8_t* q8 = smem + C::OFF_Q8 + (i >> 3) * C::Q8_BLK + qr * 128 +
+                                      ((((uint32_t)i & 7u) ^ (uint32_t)(qr & 7)) << 4);
+#pragma unroll
+                        for (int term = 0; term < 2; ++term)
+                            *reinterpret_cast<uint4*>(q8 + term * C::Q8_TERM) =
+                                make_uint4(wt[term][0], wt[term][1], wt[term][2], wt[term][3]);
+                    }
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -415,9 +500,13 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
                     abort = true;
                     break;
                 }
-                const int row = 32 * cv + lane, key = it.k0 + j * C::BK + row;
-                convert_v_row(smem + C::OFF_V + sv * C::KV_TILE, smem + C::OFF_V16 + b * C::V16_BYTES, row,
-                                key < it.klo || key >= it.k1);
+                // (row, 128-code block) pairs 32cv .. 32cv+31 of the tile's BK x NKB
+                const int pr = 32 * cv + lane;
+                const int row = C::NKB == 1 ? pr : pr % C::BK, kb = C::NKB == 1 ? 0 : pr / C::BK;
+                const int key = it.k0 + j * C::BK + row;
+                convert_v_row<C::ATOM>(smem + C::OFF_V + sv * C::KV_TILE + kb * C::KBLK,
+                                       smem + C::OFF_V16 + b * C::V16_BYTES + 2 * kb * C::ATOM, row,
+                                       key < it.klo || key >= it.k1);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
@@ -465,9 +554,11 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
                     for (int term = 0; term < 2; ++term)
 #pragma unroll
                         for (int kk = 0; kk < C::D / 32; ++kk)
-                            tc_mma_ss_f8(t_s + 128 * b,
-                                         umma_desc_sw128(base + C::OFF_Q8 + term * C::Q8_TERM + kk * 32, 16, 1024),
-                                         umma_desc_sw128(kb + kk * 32, 16, 1024), idesc_qk,
+                            tc_mma_ss_f8(t_s + C::BK * b,
+                                         umma_desc_sw128(base + C::OFF_Q8 + term * C::Q8_TERM + (kk >> 2) * C::Q8_BLK +
+                                                             (kk & 3) * 32,
+                                                         16, 1024),
+                                         umma_desc_sw128(kb + (kk >> 2) * C::KBLK + (kk & 3) * 32, 16, 1024), idesc_qk,
                                          (term > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(bar_s_full + 8 * b);
                     tc_commit(bar_k_empty + 8 * sk);
@@ -516,7 +607,7 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
                     const uint32_t vb = base + C::OFF_V16 + b * C::V16_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < C::BK / 16; ++kk)
-                        tc_mma_ts(t_o, t_p + 64 * b + kk * 8, umma_desc_sw128(vb + kk * 16 * 128, C::ATOM, 1024),
+                        tc_mma_ts(t_o, t_p + (C::BK / 2) * b + kk * 8, umma_desc_sw128(vb + kk * 16 * 128, C::ATOM, 1024),
                                   idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(bar_pv_done + 8 * b);
                     issued = true;
@@ -546,7 +637,7 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
 #pragma unroll
             for (int e = 0; e < 32; ++e) z[e] = 0u;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_st32(t_p + lane_off + 32 * q, z);
+            for (int q = 0; q < C::BK / 32; ++q) tmem_st32(t_p + lane_off + 32 * q, z);
             tmem_wait_st();
         }
         uint32_t tc = 0, ic = 0;
@@ -640,39 +731,44 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
                     break;
                 }
                 const float* meta = reinterpret_cast<const float*>(smem + C::OFF_META + sk * C::META_STRIDE);
-                // this quarter's keys 32w .. 32w+31: pages (32w) >> lp and (32w + 16) >> lp
-                const float kf0 = crow * meta[(32 * w) >> lp], kf1 = crow * meta[(32 * w + 16) >> lp];
-                const float vf0 = meta[8 + ((32 * w) >> lp)], vf1 = meta[8 + ((32 * w + 16) >> lp)];
+                // this quarter's keys KW w .. KW w + KW-1, in runs of 16 within one page
+                constexpr int KW = C::KW;
+                float kf[KW / 16], vf[KW / 16];
+#pragma unroll
+                for (int g = 0; g < KW / 16; ++g) {
+                    kf[g] = crow * meta[(KW * w + 16 * g) >> lp];
+                    vf[g] = meta[8 + ((KW * w + 16 * g) >> lp)];
+                }
                 bad |= reinterpret_cast<const uint32_t*>(meta)[16];
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_k_empty + 8 * sk);
                 tc_fence_after();
-                uint32_t sv[32];
-                tmem_ld32(t_s + 128 * b + 32 * w + lane_off, sv);
+                uint32_t sv[KW];
+                tmem_ld_cols<KW>(t_s + C::BK * b + KW * w + lane_off, sv);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) sv[e] = __float_as_uint(__uint_as_float(sv[e]) * (e < 16 ? kf0 : kf1));
+                for (int e = 0; e < KW; ++e) sv[e] = __float_as_uint(__uint_as_float(sv[e]) * kf[e / 16]);
 #define X(e) __uint_as_float(sv[e])
-                const int key0 = it.k0 + j * C::BK + 32 * w;
+                const int key0 = it.k0 + j * C::BK + KW * w;
                 const int lim = nk - key0, lim_lo = nlo - key0;   // columns outside [lim_lo, lim) are masked
                 if (TREE) {
                     // key0 + e < n_full: a cached key; else the call's key i = key0 + e - n_full
                     const int ib = key0 - n_full;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
+                    for (int e = 0; e < KW; ++e) {
                         const int i = ib + e;
                         const bool vis = e < lim && e >= lim_lo && (i < 0 || ((tmw >> (i & 31)) & 1u));
                         if (!vis) sv[e] = __float_as_uint(-CUDART_INF_F);
                     }
-                } else if (lim < 32 || lim_lo > 0) {
+                } else if (lim < KW || lim_lo > 0) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
+                    for (int e = 0; e < KW; ++e)
                         if (e >= lim || e < lim_lo) sv[e] = __float_as_uint(-CUDART_INF_F);
                 }
                 float mx8[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) mx8[i] = X(i);
 #pragma unroll
-                for (int e = 8; e < 32; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], X(e));
+                for (int e = 8; e < KW; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], X(e));
                 const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                        fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
                 // lazy rescale of this quarter's O past 2^8, warp-wide (tcgen05.ld/st are
@@ -697,7 +793,7 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
                     }
                     tc_fence_after();
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
+                    for (int q = 0; q < C::D / 32; ++q) {
                         uint32_t ov[32];
                         tmem_ld32(t_o + lane_off + 32 * q, ov);
 #pragma unroll
@@ -712,16 +808,15 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
                 }
                 const float m_use = (m_run == -CUDART_INF_F) ? 0.f : m_run;
                 float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                uint32_t pk[16];
+                uint32_t pk[KW / 2];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
+                for (int e = 0; e < KW / 2; ++e) {
                     const float p0 = exp2f(X(2 * e) - m_use), p1 = exp2f(X(2 * e + 1) - m_use);
                     ps8[e & 7] += p0 + p1;
-                    const float vf = e < 8 ? vf0 : vf1;
-                    pk[e] = pack_f16x2(p0 * vf, p1 * vf);
+                    pk[e] = pack_f16x2(p0 * vf[e / 8], p1 * vf[e / 8]);
                 }
 #undef X
-                tmem_st16(t_p + 64 * b + 16 * w + lane_off, pk);
+                tmem_st_cols<KW / 2>(t_p + (C::BK / 2) * b + (KW / 2) * w + lane_off, pk);
                 l_run += ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
                 tmem_wait_st();
                 tc_fence_before();
@@ -765,7 +860,7 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
             const bool final_write = it.n_splits - it.s_first == 1;
             const float inv = L == 0.f ? 0.f : 1.f / L;
             float* pacc = p.part_acc + slot_idx * p.qtv * C::D;
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < C::D / 32; ++c) {
                 // quarter w's scaled O of row r, columns 32c .. 32c+31, 16-byte chunks
                 // swizzled by the row
                 uint32_t ov[32];
@@ -776,7 +871,7 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
                     mine[e4 ^ (r & 7)] = make_float4(__uint_as_float(ov[4 * e4]) * f_me, __uint_as_float(ov[4 * e4 + 1]) * f_me,
                                                      __uint_as_float(ov[4 * e4 + 2]) * f_me,
                                                      __uint_as_float(ov[4 * e4 + 3]) * f_me);
-                if (c == 3) {
+                if (c == C::D / 32 - 1) {
                     // O is read out: the next item's first PV may overwrite it
                     tc_fence_before();
                     __syncwarp();
@@ -839,6 +934,29 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW>::NTHREADS, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == C::W_QK) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// Launch of one form: one CTA per SM (shared memory, all of TMEM), persistent
+// over the items; calls with a sliding window run the window build, calls
+// with tree masks the tree build, others the causal one.
+template <bool FEW, int D>
+cudaError_t launch_split_tc05_form(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
+                                   cudaStream_t st) {
+    using C = SplitTcCfg<FEW, D>;
+    auto kern = p.window > 0  ? attn_split_tc05_kernel<kModeWindow, FEW, D>
+                : p.tree_mask ? attn_split_tc05_kernel<kModeTree, FEW, D>
+                              : attn_split_tc05_kernel<kModeCausal, FEW, D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    long long grid = sms;
+    if (grid > p.n_items) grid = p.n_items;
+    if (grid < 1) grid = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(C::NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = st;
+    return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 
 }  // namespace rad

@@ -20,9 +20,12 @@ enum Family : int { kFamDecode = 0, kFamVerify = 1, kFamWide = 2, kFamPrefillTC 
 #ifndef RAD_SPLIT_BF16_TC05
 #define RAD_SPLIT_BF16_TC05 1
 #endif
-// The same for head_dim 256 with bf16 pools.
+// The same for head_dim 256 with bf16 pools, and with fp8 pools.
 #ifndef RAD_SPLIT_BF16_TC05_D256
 #define RAD_SPLIT_BF16_TC05_D256 1
+#endif
+#ifndef RAD_SPLIT_TC05_D256
+#define RAD_SPLIT_TC05_D256 1
 #endif
 
 // Keys per split for calls of up to kSplitMaxRows rows; longer calls (prefill
@@ -173,7 +176,9 @@ cudaError_t launch_prefill_fp8(const CUtensorMap& tk, const CUtensorMap& tv, con
                                cudaStream_t st);
 cudaError_t launch_split_tc05(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
                               cudaStream_t st, bool few);
-TileInfo split_tc05_info(bool few);
+cudaError_t launch_split_tc05_d256(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
+                                   cudaStream_t st);
+TileInfo split_tc05_info(bool few, int head_dim);
 cudaError_t launch_split_bf16_tc05(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
                                    cudaStream_t st, bool few);
 cudaError_t launch_split_bf16_tc05_d256(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,

@@ -118,7 +118,9 @@ def test_describe_names_the_kernel_choice():
     else:
         assert "family=decode" in b.describe(1, 32, 8, 256, 16)
         assert "family=verify" in b.describe(8, 32, 8, 256, 16)
-    assert "family=verify" in b.describe(8, 16, 2, 256, 32, b.RAD_KV_FP8_E4M3)
+    # fp8 pools with head_dim 256: the e4m3 tcgen05 split kernel's head_dim-256 build
+    assert "family=split_tc05 head_dim=256" in b.describe(8, 16, 2, 256, 32, b.RAD_KV_FP8_E4M3)
+    assert "keys_per_tile=64" in b.describe(1, 16, 2, 256, 32, b.RAD_KV_FP8_E4M3)
     # fp8 pools with head_dim 128: decode and verify shapes share the tcgen05 split kernel
     assert "family=split_tc05" in b.describe(8, 32, 8, 128, 16, b.RAD_KV_FP8_E4M3)
     assert "family=split_tc05" in b.describe(1, 8, 8, 128, 16, b.RAD_KV_FP8_E4M3)
@@ -196,19 +198,13 @@ def test_ex_workspace_follows_the_kernel_the_call_takes():
     for hd, dt in ((128, b.RAD_KV_BF16), (256, b.RAD_KV_FP8_E4M3), (128, b.RAD_KV_FP8_E4M3)):
         a = _general_args(head_dim=hd, kv_dtype=dt)
         assert ws(a) == b.workspace_bytes(4, 8, 32, 8, hd, 16, 64, dt) > 0
-    # head_dim 128: uniform, tree and ragged calls run the tcgen05 split kernels;
-    # a ragged call adds its tile map (256 bytes here)
-    for dt in (b.RAD_KV_BF16, b.RAD_KV_FP8_E4M3) if bf16_tc() else (b.RAD_KV_FP8_E4M3,):
-        uniform = b.workspace_bytes(4, 8, 32, 8, 128, 16, 64, dt)
-        assert ws(_general_args(tree=fake, kv_dtype=dt)) == uniform
-        assert ws(_general_args(cu=fake, kv_dtype=dt)) == uniform + 256
-    # head_dim 256: a ragged call runs the verify tile plus, for its
-    # decode-shaped sequences, the decode tile: two tile maps and two sets of
-    # partials
-    fp8 = b.RAD_KV_FP8_E4M3
-    verify_part = ws(_general_args(tree=fake, head_dim=256, kv_dtype=fp8))
-    decode_part = b.workspace_bytes(4, 2, 32, 8, 256, 16, 64, fp8)   # the decode tile's partials: 8-row slots
-    assert ws(_general_args(cu=fake, head_dim=256, kv_dtype=fp8)) == verify_part + decode_part + 2 * 256
+    # uniform, tree and ragged split calls run the tcgen05 split kernels at both
+    # head dims and pool types; a ragged call adds its tile map (256 bytes here)
+    for hd in (128, 256):
+        for dt in (b.RAD_KV_BF16, b.RAD_KV_FP8_E4M3):
+            uniform = b.workspace_bytes(4, 8, 32, 8, hd, 16, 64, dt)
+            assert ws(_general_args(tree=fake, head_dim=hd, kv_dtype=dt)) == uniform
+            assert ws(_general_args(cu=fake, head_dim=hd, kv_dtype=dt)) == uniform + 256
     # the caller's row total bounds the tiles: 4 sequences of up to 256 rows
     # (ratio 4, 32-row tiles: 32 tiles each) holding 40 rows in all need at
     # most ceil(160 / 32) + 4 = 9 tiles instead of 128
@@ -243,8 +239,8 @@ def test_ex_describe_names_the_kernels_of_ragged_and_tree_calls():
     rag = b.ex_describe(shape(ragged=True))
     assert rag.startswith("ragged_tile_map + attn_split_tc05 family=split_tc05") and rag.count("attn_combine") == 1
     rag256 = b.ex_describe(b.shape_args(64, 8, 32, 8, 256, 16, 1024, b.RAD_KV_FP8_E4M3, ragged=True))
-    assert rag256.startswith("ragged_tile_map + attn_tile family=decode")
-    assert " + attn_tile family=verify" in rag256 and rag256.count("attn_combine") == 2
+    assert rag256.startswith("ragged_tile_map + attn_split_tc05 family=split_tc05 head_dim=256")
+    assert rag256.count("attn_combine") == 1
     chunk = b.ex_describe(b.shape_args(4, 300, 32, 8, 128, 16, 64, ragged=True))
     assert chunk.startswith("ragged_tile_map + attn_tile family=decode") and " + attn_tile family=wide" in chunk
     assert "attn_combine" not in chunk
@@ -293,7 +289,6 @@ def _fault_args(**over):
     (3_000_000_000, b.RAD_FAULT_NONE, {}),                           # above the 2 s default
     (0, 7, {}),                                                      # an unknown fault
     (0, b.RAD_FAULT_SKIP_FIRST_K_TILE, dict(kv_dtype=b.RAD_KV_FP8_E4M3)),   # e4m3 pools: not honoured
-    (0, b.RAD_FAULT_SKIP_FIRST_K_TILE, dict(head_dim=256, kv_dtype=b.RAD_KV_FP8_E4M3)),   # the tile kernel
     (0, b.RAD_FAULT_SKIP_FIRST_K_TILE, dict(rows=300)),              # a prefill chunk: not honoured
 ])
 def test_fault_test_hook_refuses_what_it_cannot_honour(limit, fault, over):
