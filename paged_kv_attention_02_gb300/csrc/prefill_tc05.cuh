@@ -50,10 +50,13 @@
 
 namespace rad {
 
-struct PrefillCfg {
-    static constexpr int D = 128;
+// D: head_dim 128 or 256.  At 256 a key tile holds 64 keys (a K or V tile is
+// 32 KB, as a 128-key tile is at 128) and the query tile takes 64 KB.
+template <int D_>
+struct PrefillCfgD {
+    static constexpr int D = D_;
     static constexpr int BM = 128;   // query rows per item
-    static constexpr int BN = RAD_PREFILL_BN;     // keys per tile (64 or 128)
+    static constexpr int BN = D == 128 ? RAD_PREFILL_BN : 64;   // keys per tile (64 or 128)
     static constexpr int NSK = RAD_PREFILL_NSK;   // K stages: a K tile is free once its QK is done
     static constexpr int NSV = RAD_PREFILL_NSV;   // V stages: a V tile is free once its PV is done
     static constexpr int CTAS = RAD_PREFILL_CTAS; // CTAs sharing an SM
@@ -72,15 +75,17 @@ struct PrefillCfg {
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
     static constexpr int NTHREADS = 8 * 32;   // 4 softmax, QK issue, PV issue, K (+Q) and V producers
     static constexpr int W_QK = 4, W_PV = 5, W_PROD_K = 6, W_PROD_V = 7;
-    // tensor memory: O in columns [0,128), S buffer b in [128 + b*BN, 128 + (b+1)*BN);
+    // tensor memory: O in columns [0,D), S buffer b in [D + b*BN, D + (b+1)*BN);
     // P of a tile is written over its S buffer as bf16 pairs: hi in the first
     // BN/2 columns, lo in the next BN/2
-    static constexpr uint32_t TMEM_COLS = 128 + 2 * BN <= 256 ? 256 : 512;
+    static constexpr uint32_t TMEM_COLS = D + 2 * BN <= 256 ? 256 : 512;
     static constexpr float RESCALE_LOG2 = 8.f;            // rescale O when the max grows past 2^8
     static_assert(BN == 64 || BN == 128, "key tile");
+    static_assert(D == 128 || D == 256, "head_dim 128 or 256");
     static_assert(CTAS * (SMEM_BYTES + 1024) <= 233472, "shared memory budget");
     static_assert(CTAS * TMEM_COLS <= 512, "tensor memory budget");
 };
+using PrefillCfg = PrefillCfgD<128>;
 
 struct PrefItem {
     int g, kvh, qt, L;
@@ -126,11 +131,11 @@ __device__ __forceinline__ PrefItem plan_prefill(int item, const AttnParams& p) 
     return it;
 }
 
-template <bool GEN>
-__global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
+template <bool GEN, int D = 128>
+__global__ void __launch_bounds__(PrefillCfgD<D>::NTHREADS, PrefillCfgD<D>::CTAS)
     attn_prefill_tc05_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ AttnParams p) {
-    using C = PrefillCfg;
+    using C = PrefillCfgD<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -190,7 +195,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
     tc_fence_after();
     const uint32_t tmem = misc[0];
     const uint32_t t_o = tmem;
-    const uint32_t t_s = tmem + 128;   // S buffer b at t_s + BN*b
+    const uint32_t t_s = tmem + C::D;   // S buffer b at t_s + BN*b
 
     const int n_items = p.n_items;
     bool abort = false;
@@ -215,7 +220,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
         for (int rd = 0; rd * (int)gridDim.x < n_items && !abort; ++rd) {
             const int item = prefill_item_of<true>(rd, blockIdx.x, gridDim.x);
             if (item >= n_items) break;
-            const PrefItem it = plan_prefill<GEN>(item, p);
+            const PrefItem it = plan_prefill<GEN, C::BM, C::BN>(item, p);
             if (!it.seq_ok) continue;
             if (is_k) {
                 if (ic >= 1 && !mbar_wait_bounded(bar_q_empty, (ic - 1) & 1u, p.wait_ns)) {
@@ -225,7 +230,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
                 if (lane == 0) {
                     mbar_arrive_expect_tx(bar_q_full, C::Q_BYTES);
 #pragma unroll
-                    for (int hb = 0; hb < 2; ++hb)
+                    for (int hb = 0; hb < C::D / 64; ++hb)
                         tma_load_4d(base + C::OFF_Q + hb * C::QHB_BYTES, &tm_q, bar_q_full, hb * 64, it.kvh * p.ratio,
                                     it.m0 / p.ratio, it.g, pol);
                 }
@@ -259,7 +264,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
                     const int tok = ((!GEN || pi >= page_lo) && pi < page_hi) ? pg * P : oob_tok;
                     if (lane == 0) {
 #pragma unroll
-                        for (int hb = 0; hb < 2; ++hb)
+                        for (int hb = 0; hb < C::D / 64; ++hb)
                             tma_load_3d(dst + hb * C::HB_BYTES + i * P * 128, tm, bar_full + 8 * st, hb * 64, it.kvh,
                                         tok, pol);
                     }
@@ -283,7 +288,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
         for (int rd = 0; rd * (int)gridDim.x < n_items && !abort; ++rd) {
             const int item = prefill_item_of<true>(rd, blockIdx.x, gridDim.x);
             if (item >= n_items) break;
-            const PrefItem it = plan_prefill<GEN>(item, p);
+            const PrefItem it = plan_prefill<GEN, C::BM, C::BN>(item, p);
             if (!it.seq_ok) continue;
             if (!mbar_wait_bounded(bar_q_full, ic & 1u, p.wait_ns)) {
                 abort = true;
@@ -336,7 +341,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
         for (int rd = 0; rd * (int)gridDim.x < n_items && !abort; ++rd) {
             const int item = prefill_item_of<true>(rd, blockIdx.x, gridDim.x);
             if (item >= n_items) break;
-            const PrefItem it = plan_prefill<GEN>(item, p);
+            const PrefItem it = plan_prefill<GEN, C::BM, C::BN>(item, p);
             if (!it.seq_ok) continue;
             // V rows to zero: slots past the sequence's end in its last page,
             // and slots of the first live page below the tile's first visible key
@@ -359,8 +364,9 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
                 const int h0 = max(head_lo, key0) - key0, h1 = min(head_hi, key0 + C::BN) - key0;
                 const int nz = max(z1 - z0, 0), nh = GEN ? max(h1 - h0, 0) : 0;
                 if (nz + nh > 0) {
-                    for (int idx = lane; idx < (nz + nh) * 16; idx += 32) {
-                        const int rr = idx / 16, c16 = idx % 16;
+                    constexpr int CPR = C::D / 8;   // 16-byte chunks of a row
+                    for (int idx = lane; idx < (nz + nh) * CPR; idx += 32) {
+                        const int rr = idx / CPR, c16 = idx % CPR;
                         const int row = rr < nz ? z0 + rr : h0 + (rr - nz);
                         const uint32_t a = vb + (c16 >> 3) * C::HB_BYTES + row * 128 + (((c16 & 7) ^ (row & 7)) << 4);
                         asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
@@ -402,7 +408,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
         for (int rd = 0; rd * (int)gridDim.x < n_items && !abort; ++rd) {
             const int item = prefill_item_of<true>(rd, blockIdx.x, gridDim.x);
             if (item >= n_items) break;
-            const PrefItem it = plan_prefill<GEN>(item, p);
+            const PrefItem it = plan_prefill<GEN, C::BM, C::BN>(item, p);
             const int m = it.m0 + t;
             const bool valid = m < it.m_end;
             const int r = m / p.ratio, hl = m - r * p.ratio;
@@ -493,7 +499,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
                     }
                     tc_fence_after();
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
+                    for (int q = 0; q < C::D / 32; ++q) {
                         uint32_t ov[32];
                         tmem_ld32(t_o + lane_off + 32 * q, ov);
 #pragma unroll
@@ -543,7 +549,7 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
             tc_fence_after();
             const float inv = (bad || l_run == 0.f) ? 0.f : 1.f / l_run;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < C::D / 32; ++q) {
                 uint32_t ov[32];
                 tmem_ld32(t_o + lane_off + 32 * q, ov);
                 if (valid) {
@@ -576,6 +582,27 @@ __global__ void __launch_bounds__(PrefillCfg::NTHREADS, PrefillCfg::CTAS)
     __syncthreads();
     tc_fence_after();
     if (warp == C::W_QK) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// The launch: one CTA per SM (shared memory, TMEM), persistent over the items;
+// the general build for a sliding window or a scale <= 0, else the lean one.
+template <int D>
+cudaError_t launch_prefill_tc05_dim(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                    const AttnParams& p, int sms, cudaStream_t st) {
+    using C = PrefillCfgD<D>;
+    auto kern = (p.window > 0 || p.scale_log2 <= 0.f) ? attn_prefill_tc05_kernel<true, D>
+                                                      : attn_prefill_tc05_kernel<false, D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    long long grid = (long long)sms * C::CTAS;
+    if (grid > p.n_items) grid = p.n_items;
+    if (grid < 1) grid = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(C::NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = st;
+    return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, p);
 }
 
 }  // namespace rad

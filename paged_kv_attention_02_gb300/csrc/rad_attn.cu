@@ -74,11 +74,12 @@ rad::TileInfo tile_for(int head_dim, int kv_dtype, int family) {
     return fp8 ? rad::tile_info<256, true>(family) : rad::tile_info<256, false>(family);
 }
 
-// Prefill chunks (no split) with head_dim 128 run on the tcgen05 prefill
-// kernels (bf16 and fp8 pools) when whole query heads tile their 128-row blocks.
+// Prefill chunks (no split) run on the tcgen05 prefill kernels when whole
+// query heads tile their 128-row blocks: head_dim 128 over bf16 and fp8 pools,
+// head_dim 256 over bf16 pools.
 bool use_prefill_tc(int32_t rows, int32_t ratio, int32_t head_dim, int32_t kv_dtype) {
-    (void)kv_dtype;
-    return rows > rad::kSplitMaxRows && head_dim == 128 && ratio <= 128 && 128 % ratio == 0;
+    const bool dim_ok = head_dim == 128 || (head_dim == 256 && kv_dtype == RAD_KV_BF16 && RAD_PREFILL_TC05_D256);
+    return rows > rad::kSplitMaxRows && dim_ok && ratio <= 128 && 128 % ratio == 0;
 }
 
 // `general`: a call with ragged rows (cu_seqlens) or tree masks.  Split calls
@@ -115,8 +116,9 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
         pl.family = !general && use_prefill_tc(rows, pl.ratio, head_dim, kv_dtype) ? rad::kFamPrefillTC
                                                                                    : rad::kFamWide;
     if (pl.family == rad::kFamPrefillTC)
-        pl.tile = rad::TileInfo{128, 0, 4, 0, 0, rad::PrefillTileKeys, RAD_PREFILL_NSK + RAD_PREFILL_NSV, 128, 256, 0,
-                                RAD_PREFILL_CTAS};
+        pl.tile = rad::TileInfo{head_dim, kv_dtype == RAD_KV_FP8_E4M3 ? 1 : 0, 4, 0, 0,
+                                kv_dtype == RAD_KV_FP8_E4M3 ? 128 : rad::prefill_tc05_tile_keys(head_dim),
+                                RAD_PREFILL_NSK + RAD_PREFILL_NSV, 128, 256, 0, RAD_PREFILL_CTAS};
     else if (pl.family == rad::kFamSplitTC)
         pl.tile = rad::split_tc05_info(pl.M <= 8, head_dim);
     else if (pl.family == rad::kFamSplitBf)
@@ -520,7 +522,8 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
         if (encode_bf16_map(&tq, q, 4, qd, qs, qb) != RAD_OK || encode_bf16_map(&tk, k_pool, 3, kd, ks, kb) != RAD_OK ||
             encode_bf16_map(&tv, v_pool, 3, kd, ks, kb) != RAD_OK)
             return RAD_E_CUDA;
-        e = rad::launch_prefill_tc05(tq, tk, tv, p, sms, st);
+        e = head_dim == 128 ? rad::launch_prefill_tc05(tq, tk, tv, p, sms, st)
+                            : rad::launch_prefill_tc05_d256(tq, tk, tv, p, sms, st);
     } else if (head_dim == 128)
         e = fp8 ? rad::launch_d128_fp8(pl.family, p, sms, st) : rad::launch_d128_bf16(pl.family, p, sms, st);
     else
@@ -577,7 +580,7 @@ int describe_call(int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_
                  "attn_prefill_tc05 family=%s head_dim=%d kv=bf16 query_rows_per_kv_head=%d tile_rows=128 "
                  "keys_per_tile=%d k_stages=%d v_stages=%d ctas_per_sm=%d warps=4 softmax+1 qk+1 pv+2 producers "
                  "mma=tcgen05.kind::f16 (S and O in TMEM, P bf16 hi+lo from TMEM) split_len=0",
-                 family_name(pl.family), head_dim, pl.M, rad::PrefillTileKeys, RAD_PREFILL_NSK, RAD_PREFILL_NSV,
+                 family_name(pl.family), head_dim, pl.M, pl.tile.KS, RAD_PREFILL_NSK, RAD_PREFILL_NSV,
                  pl.tile.minb);
         return RAD_OK;
     }

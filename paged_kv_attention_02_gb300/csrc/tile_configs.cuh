@@ -27,6 +27,11 @@ enum Family : int { kFamDecode = 0, kFamVerify = 1, kFamWide = 2, kFamPrefillTC 
 #ifndef RAD_SPLIT_TC05_D256
 #define RAD_SPLIT_TC05_D256 1
 #endif
+// Prefill chunks with head_dim 256 over bf16 pools run on the tcgen05 prefill
+// kernel's head_dim-256 build; 0 keeps them on the mma.sync wide tile.
+#ifndef RAD_PREFILL_TC05_D256
+#define RAD_PREFILL_TC05_D256 1
+#endif
 
 // Keys per split for calls of up to kSplitMaxRows rows; longer calls (prefill
 // chunks) run one range per query tile.  A multiple of every tile's KS.
@@ -172,6 +177,9 @@ cudaError_t launch_d256_bf16(int family, const AttnParams& p, int sms, cudaStrea
 cudaError_t launch_d256_fp8(int family, const AttnParams& p, int sms, cudaStream_t st);
 cudaError_t launch_prefill_tc05(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const AttnParams& p, int sms, cudaStream_t st);
+cudaError_t launch_prefill_tc05_d256(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                     const AttnParams& p, int sms, cudaStream_t st);
+int prefill_tc05_tile_keys(int head_dim);
 cudaError_t launch_prefill_fp8(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
                                cudaStream_t st);
 cudaError_t launch_split_tc05(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,

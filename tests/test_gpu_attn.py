@@ -51,6 +51,11 @@ MID = {
                                     "fixed:1800", pages_per_seq=60),
     "prefill_fp8_r1": wl.Config("prefill_fp8_r1", 2, 272, 4, 4, 128, 16, wl.KV_FP8_E4M3, 115,
                                 "fixed:272,2000", pages_per_seq=130),
+    # head_dim-256 bf16 prefill chunks: the tcgen05 prefill kernel's 64-key-tile build (ratios 8, 1)
+    "prefill_d256": wl.Config("prefill_d256", 2, 300, 16, 2, 256, 32, wl.KV_BF16, 118, "fixed:300,1500",
+                              pages_per_seq=60, meta=dict(head_dim=256, n_embd=3408)),
+    "prefill_d256_r1": wl.Config("prefill_d256_r1", 1, 272, 4, 4, 256, 16, wl.KV_BF16, 119, "fixed:900",
+                                 pages_per_seq=64),
 }
 
 
@@ -202,7 +207,7 @@ def test_full_size_prefill_chunk_is_bit_identical_alone_and_batched(full):
     assert np.array_equal(bits(both)[0], bits(alone)[0])
 
 
-@pytest.mark.parametrize("name", ["prefill", "prefill_fp8", "prefill_fp8_r1"])
+@pytest.mark.parametrize("name", ["prefill", "prefill_fp8", "prefill_fp8_r1", "prefill_d256"])
 def test_prefill_rows_bit_identical_alone_and_batched(mid, name):
     w, dw = mid(name)
     out, _ = dw.run()
@@ -306,7 +311,7 @@ def test_verify_bad_page_in_a_late_split_zeroes_every_row(mid):
     assert np.all(ob[4] == 0) and np.array_equal(ob[:4], gb[:4])
 
 
-@pytest.mark.parametrize("name", ["chunk_split", "prefill", "prefill_fp8_d256", "prefill_fp8"])
+@pytest.mark.parametrize("name", ["chunk_split", "prefill", "prefill_fp8_d256", "prefill_fp8", "prefill_d256"])
 def test_bad_last_page_zeroes_rows_of_every_query_tile(mid, name):
     # Calls with several query tiles per KV head: the early tiles never load
     # the last page, yet a bad id there zeroes every row of the group.
@@ -322,7 +327,7 @@ def test_bad_last_page_zeroes_rows_of_every_query_tile(mid, name):
     assert np.all(ob[g] == 0) and np.array_equal(ob[:g], gb[:g])
 
 
-@pytest.mark.parametrize("name", ["prefill", "dec128", "ver_fp8", "chunk_split", "prefill_fp8"])
+@pytest.mark.parametrize("name", ["prefill", "dec128", "ver_fp8", "chunk_split", "prefill_fp8", "prefill_d256"])
 @pytest.mark.parametrize("scale", [0.0, -0.07])
 def test_zero_and_negative_scales_match_oracle(mid, name, scale):
     # scale 0: every visible key weighs the same; scale < 0 reverses the order

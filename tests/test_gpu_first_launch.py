@@ -42,6 +42,8 @@ CASES = [
     ("tile_verify_d256", (4, 8, 16, 2, 256, 32, 0, 213, "fixed:8,700,2100,4000"), 130, 0),
     ("prefill_fp8_window", (3, 300, 8, 2, 128, 16, 1, 214, "fixed:300,1000,2500"), 160, 257),
     ("prefill_fp8_plain", (2, 384, 8, 2, 128, 16, 1, 215, "fixed:384,2000"), 160, 0),
+    ("prefill_d256_window", (2, 300, 16, 2, 256, 32, 0, 216, "fixed:300,1500"), 60, 257),
+    ("prefill_d256_plain", (1, 384, 16, 2, 256, 32, 0, 217, "fixed:2000"), 70, 0),
 ]
 
 

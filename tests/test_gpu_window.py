@@ -47,6 +47,8 @@ WIN = {
                                  pages_per_seq=60), 64),
     "prefill_fp8_d256_w100": (wl.Config("prefill_fp8_d256_w100", 1, 260, 4, 1, 256, 32, wl.KV_FP8_E4M3,
                                         211, "fixed:900", pages_per_seq=30), 100),
+    "prefill_d256_w100": (wl.Config("prefill_d256_w100", 2, 300, 16, 2, 256, 32, wl.KV_BF16, 216,
+                                    "fixed:300,1800", pages_per_seq=60), 100),
     "prefill_fp8_w257": (wl.Config("prefill_fp8_w257", 3, 300, 8, 2, 128, 16, wl.KV_FP8_E4M3, 212,
                                    "fixed:300,1000,2500", pages_per_seq=160), 257),
     "prefill_fp8_w64": (wl.Config("prefill_fp8_w64", 1, 520, 4, 1, 128, 32, wl.KV_FP8_E4M3, 213, "fixed:1800",
