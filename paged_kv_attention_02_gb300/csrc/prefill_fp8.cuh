@@ -56,17 +56,24 @@
 
 namespace rad {
 
-struct PrefillFp8Cfg {
-    static constexpr int D = 128;
+// D: head_dim 128 or 256.  At 256 a key tile holds 64 keys (16 KB of e4m3 K or
+// V rows, as a 128-key tile at 128) in two 128-byte column blocks, the query
+// terms take 64 KB, and each converting warp turns 32 rows of a tile into f16.
+template <int D_>
+struct PrefillFp8CfgD {
+    static constexpr int D = D_;
     static constexpr int BM = 128;                  // query rows per item
-    static constexpr int BN = 128;                  // keys per tile
-    static constexpr int NSK = RAD_PREFILL_FP8_NSK;   // K stages (with the tile's page scales)
-    static constexpr int NSV = RAD_PREFILL_FP8_NSV;   // V stages
-    static constexpr int QK_VROWS = 64;               // V rows the QK warp converts per tile (the V warp: the rest)
-    static constexpr int Q8_TERM = BM * 128;        // one e4m3 term of the query tile: [row][128 B]
-    static constexpr int KV_TILE = BN * 128;        // e4m3 K or V rows of one tile
+    static constexpr int BN = D == 128 ? 128 : 64;  // keys per tile
+    static constexpr int NKB = D / 128;             // 128-byte column blocks of an e4m3 row
+    static constexpr int NSK = D == 128 ? RAD_PREFILL_FP8_NSK : 3;   // K stages (with the tile's page scales)
+    static constexpr int NSV = D == 128 ? RAD_PREFILL_FP8_NSV : 3;   // V stages
+    static constexpr int QK_VROWS = BN / 2;         // V rows the QK warp converts per tile (the V warp: the rest)
+    static constexpr int Q8_BLK = BM * 128;         // one 128-byte column block of a query term: [row][128 B]
+    static constexpr int Q8_TERM = NKB * Q8_BLK;    // one e4m3 term of the query tile
+    static constexpr int KBLK = BN * 128;           // one 128-byte column block of a K or V tile
+    static constexpr int KV_TILE = NKB * KBLK;      // e4m3 K or V rows of one tile
     static constexpr int ATOM = BN * 128;           // one 64-column block of the f16 V tile
-    static constexpr int V16_BYTES = 2 * ATOM;
+    static constexpr int V16_BYTES = (D / 64) * ATOM;
     static constexpr int META_STRIDE = 64;          // ks[8], vs[8] of a tile's pages
     static constexpr int OFF_Q8 = 0;
     static constexpr int OFF_K = OFF_Q8 + 2 * Q8_TERM;
@@ -85,56 +92,64 @@ struct PrefillFp8Cfg {
     static constexpr int W_QK = 4, W_V = 5, W_PROD_K = 6, W_PROD_V = 7;
     // a K stage is free once QK read its K (a commit) and the softmax warps read its scales
     static constexpr int K_EMPTY_ARRIVALS = 1 + 4;
-    static constexpr uint32_t TMEM_COLS = 512;      // O in [0,128), S buffer b in [128 + 128 b, ...)
+    static constexpr uint32_t TMEM_COLS = 512;      // O in [0, D), S buffer b in [D + BN b, ...)
     static constexpr float RESCALE_LOG2 = 8.f;
+    static_assert(D == 128 || D == 256, "head_dim 128 or 256");
     static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && OFF_V16 % 1024 == 0 && KV_TILE % 1024 == 0, "1 KB tiles");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(QK_VROWS % 32 == 0 && QK_VROWS > 0 && QK_VROWS < BN, "both warps convert whole 32-row groups");
+    static_assert(D + 2 * BN <= (int)TMEM_COLS, "tensor memory budget");
 };
+using PrefillFp8Cfg = PrefillFp8CfgD<128>;
 
 // Key rows row0 + lane + 32 i (i < n) of a staged e4m3 V tile -> the f16
-// MN-major tile PV reads (128-byte swizzle, two 64-column blocks); keys outside
-// [zlo, L) become zeros.
+// MN-major tile PV reads (128-byte swizzle, 64-column blocks); keys outside
+// [zlo, L) become zeros.  Each 128-code column block of a row goes to its
+// pair of f16 blocks.
+template <class C>
 __device__ __forceinline__ void convert_v_rows(const uint8_t* stage, uint8_t* v16, int row0, int n, int key0, int zlo,
                                                int L, int lane) {
-    using C = PrefillFp8Cfg;
     const uint32_t sw = (uint32_t)(lane & 7);   // (row0 + lane + 32 i) & 7: row0 is a multiple of 32
 #pragma unroll 1
     for (int i = 0; i < n; ++i) {
         const int row = row0 + lane + 32 * i;
         const int key = key0 + row;
         const bool zero = key < zlo || key >= L;
-        const uint8_t* src = stage + row * 128;
-        uint8_t* dst = v16 + row * 128;
-        uint4 in[8];   // the row's loads first: stores below may alias them as far as the compiler knows
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-            in[ch] = zero ? make_uint4(0u, 0u, 0u, 0u) : *reinterpret_cast<const uint4*>(src + (((uint32_t)ch ^ sw) << 4));
+        for (int kb = 0; kb < C::NKB; ++kb) {
+            const uint8_t* src = stage + kb * C::KBLK + row * 128;
+            uint8_t* dst = v16 + 2 * kb * C::ATOM + row * 128;
+            uint4 in[8];   // the row's loads first: stores below may alias them as far as the compiler knows
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-            // codes 16ch .. 16ch+15 -> f16 chunks 2ch, 2ch+1 of the row, column block ch / 4
-            const uint4 v = in[ch];
-            const uint32_t h0 = e4m3x2_to_f16x2((uint16_t)(v.x & 0xFFFFu));
-            const uint32_t h1 = e4m3x2_to_f16x2((uint16_t)(v.x >> 16));
-            const uint32_t h2 = e4m3x2_to_f16x2((uint16_t)(v.y & 0xFFFFu));
-            const uint32_t h3 = e4m3x2_to_f16x2((uint16_t)(v.y >> 16));
-            const uint32_t h4 = e4m3x2_to_f16x2((uint16_t)(v.z & 0xFFFFu));
-            const uint32_t h5 = e4m3x2_to_f16x2((uint16_t)(v.z >> 16));
-            const uint32_t h6 = e4m3x2_to_f16x2((uint16_t)(v.w & 0xFFFFu));
-            const uint32_t h7 = e4m3x2_to_f16x2((uint16_t)(v.w >> 16));
-            uint8_t* blk = dst + (ch >> 2) * C::ATOM;
-            const uint32_t c2 = (uint32_t)((ch & 3) * 2);
-            *reinterpret_cast<uint4*>(blk + ((c2 ^ sw) << 4)) = make_uint4(h0, h1, h2, h3);
-            *reinterpret_cast<uint4*>(blk + (((c2 + 1) ^ sw) << 4)) = make_uint4(h4, h5, h6, h7);
+            for (int ch = 0; ch < 8; ++ch)
+                in[ch] = zero ? make_uint4(0u, 0u, 0u, 0u)
+                              : *reinterpret_cast<const uint4*>(src + (((uint32_t)ch ^ sw) << 4));
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                // codes 16ch .. 16ch+15 -> f16 chunks 2ch, 2ch+1 of the row, column block ch / 4
+                const uint4 v = in[ch];
+                const uint32_t h0 = e4m3x2_to_f16x2((uint16_t)(v.x & 0xFFFFu));
+                const uint32_t h1 = e4m3x2_to_f16x2((uint16_t)(v.x >> 16));
+                const uint32_t h2 = e4m3x2_to_f16x2((uint16_t)(v.y & 0xFFFFu));
+                const uint32_t h3 = e4m3x2_to_f16x2((uint16_t)(v.y >> 16));
+                const uint32_t h4 = e4m3x2_to_f16x2((uint16_t)(v.z & 0xFFFFu));
+                const uint32_t h5 = e4m3x2_to_f16x2((uint16_t)(v.z >> 16));
+                const uint32_t h6 = e4m3x2_to_f16x2((uint16_t)(v.w & 0xFFFFu));
+                const uint32_t h7 = e4m3x2_to_f16x2((uint16_t)(v.w >> 16));
+                uint8_t* blk = dst + (ch >> 2) * C::ATOM;
+                const uint32_t c2 = (uint32_t)((ch & 3) * 2);
+                *reinterpret_cast<uint4*>(blk + ((c2 ^ sw) << 4)) = make_uint4(h0, h1, h2, h3);
+                *reinterpret_cast<uint4*>(blk + (((c2 + 1) ^ sw) << 4)) = make_uint4(h4, h5, h6, h7);
+            }
         }
     }
 }
 
-template <bool GEN>
-__global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
+template <bool GEN, int D = 128>
+__global__ void __launch_bounds__(PrefillFp8CfgD<D>::NTHREADS, 1)
     attn_prefill_fp8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                             const __grid_constant__ AttnParams p) {
-    using C = PrefillFp8Cfg;
+    using C = PrefillFp8CfgD<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -191,7 +206,7 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
     tc_fence_after();
     const uint32_t tmem = misc[0];
     const uint32_t t_o = tmem;
-    const uint32_t t_s = tmem + 128;   // S buffer b at t_s + BN*b
+    const uint32_t t_s = tmem + C::D;   // S buffer b at t_s + BN*b
 
     const int P = p.page_size;
     const int ppt = C::BN / P;       // pages per key tile (8 or 4)
@@ -287,7 +302,12 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
                     const int pi = pstart + i;
                     const int pg = __shfl_sync(0xffffffffu, my_pg, (pi - batch0) & 31);
                     const int tok = ((!GEN || pi >= page_lo) && pi < page_hi) ? pg * P : oob_tok;
-                    if (lane == 0) tma_load_3d(dst + (uint32_t)(i * P * 128), tm, bar_full + 8 * st, 0, it.kvh, tok, pol);
+                    if (lane == 0) {
+#pragma unroll
+                        for (int kb = 0; kb < C::NKB; ++kb)
+                            tma_load_3d(dst + (uint32_t)(kb * C::KBLK + i * P * 128), tm, bar_full + 8 * st, kb * 128,
+                                        it.kvh, tok, pol);
+                    }
                 }
                 ++sc;
                 // the next item, RAD_PREFILL_PUBLISH_LEAD tiles before this one's last
@@ -342,8 +362,10 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
 #pragma unroll
                         for (int kk = 0; kk < C::D / 32; ++kk)
                             tc_mma_ss_f8(t_s + C::BN * b,
-                                         umma_desc_sw128(base + C::OFF_Q8 + term * C::Q8_TERM + kk * 32, 16, 1024),
-                                         umma_desc_sw128(kb + kk * 32, 16, 1024), idesc_qk,
+                                         umma_desc_sw128(base + C::OFF_Q8 + term * C::Q8_TERM + (kk >> 2) * C::Q8_BLK +
+                                                             (kk & 3) * 32,
+                                                         16, 1024),
+                                         umma_desc_sw128(kb + (kk >> 2) * C::KBLK + (kk & 3) * 32, 16, 1024), idesc_qk,
                                          (term > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(bar_s_full + 8 * b);
                     tc_commit(bar_k_empty + 8 * st);
@@ -358,7 +380,7 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
                     abort = true;
                     break;
                 }
-                convert_v_rows(smem + C::OFF_V + sv * C::KV_TILE, smem + C::OFF_V16 + b * C::V16_BYTES, 0,
+                convert_v_rows<C>(smem + C::OFF_V + sv * C::KV_TILE, smem + C::OFF_V16 + b * C::V16_BYTES, 0,
                                C::QK_VROWS / 32, (it.kt0 + j) * C::BN, GEN ? it.klo : 0, it.L, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -404,7 +426,7 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
                     break;
                 }
                 // key rows QK_VROWS .. 127 of the staged tile -> f16 (the QK warp converts the rows below)
-                convert_v_rows(smem + C::OFF_V + st * C::KV_TILE, smem + C::OFF_V16 + b * C::V16_BYTES, C::QK_VROWS,
+                convert_v_rows<C>(smem + C::OFF_V + st * C::KV_TILE, smem + C::OFF_V16 + b * C::V16_BYTES, C::QK_VROWS,
                                (C::BN - C::QK_VROWS) / 32,
                                (it.kt0 + j) * C::BN, zlo, it.L, lane);
                 fence_proxy_async_smem();
@@ -472,47 +494,61 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
             }
             float isq = 1.f;   // 2^-k: the row's logits scale back
             {
+                const uint4* qrow = reinterpret_cast<const uint4*>(
+                    p.q + (((long long)it.g * p.rows + r) * p.n_head + it.kvh * p.ratio + hl) * C::D);
+                // the row's largest magnitude, 128 elements at a time (head_dim 256: the
+                // second pass reads the row again, from L1)
                 uint4 qv[16];
-                const __nv_bfloat16* qrow = p.q + (((long long)it.g * p.rows + r) * p.n_head + it.kvh * p.ratio + hl) * C::D;
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    qv[i] = valid ? __ldg(reinterpret_cast<const uint4*>(qrow) + i) : make_uint4(0u, 0u, 0u, 0u);
                 float amax = 0.f;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const uint32_t x[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
+                for (int h = 0; h < C::D / 128; ++h) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(x[e])), fabsf(bf16_hi(x[e]))));
+                    for (int i = 0; i < 16; ++i) qv[i] = valid ? __ldg(qrow + 16 * h + i) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const uint32_t x[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(x[e])), fabsf(bf16_hi(x[e]))));
+                    }
                 }
                 // 2^k with amax * 2^k in [128, 256): k = 7 - floor(log2 amax), kept a normal float
                 const int ex = amax > 0.f ? (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 : 7;
                 const int kx = max(-126, min(127, 7 - ex));
                 const float sq = __uint_as_float((uint32_t)(kx + 127) << 23);
                 isq = __uint_as_float((uint32_t)(127 - kx) << 23);
-                uint8_t* q8 = smem + C::OFF_Q8 + t * 128;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    // elements 16i .. 16i+15: chunk i of each term's row
-                    uint32_t w[2][4];
-                    const uint32_t words[8] = {qv[2 * i].x,     qv[2 * i].y,     qv[2 * i].z,     qv[2 * i].w,
-                                               qv[2 * i + 1].x, qv[2 * i + 1].y, qv[2 * i + 1].z, qv[2 * i + 1].w};
+                for (int h = 0; h < C::D / 128; ++h) {
+                    if (C::D > 128) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const uint32_t x0 = words[2 * e], x1 = words[2 * e + 1];
-                        const float v0 = bf16_lo(x0) * sq, v1 = bf16_hi(x0) * sq;
-                        const float v2 = bf16_lo(x1) * sq, v3 = bf16_hi(x1) * sq;
-                        const uint32_t h01 = f32x2_to_e4m3x2(v0, v1), h23 = f32x2_to_e4m3x2(v2, v3);
-                        const float2 a01 = e4m3x2_to_f32x2(h01), a23 = e4m3x2_to_f32x2(h23);
-                        const uint32_t l01 = f32x2_to_e4m3x2(v0 - a01.x, v1 - a01.y);
-                        const uint32_t l23 = f32x2_to_e4m3x2(v2 - a23.x, v3 - a23.y);
-                        w[0][e] = h01 | (h23 << 16);
-                        w[1][e] = l01 | (l23 << 16);
+                        for (int i = 0; i < 16; ++i) qv[i] = valid ? __ldg(qrow + 16 * h + i) : make_uint4(0u, 0u, 0u, 0u);
                     }
-                    const uint32_t off = (((uint32_t)i ^ (uint32_t)(t & 7)) << 4);
+                    // column block h of each term: [row][128 B]
+                    uint8_t* q8 = smem + C::OFF_Q8 + h * C::Q8_BLK + t * 128;
 #pragma unroll
-                    for (int term = 0; term < 2; ++term)
-                        *reinterpret_cast<uint4*>(q8 + term * C::Q8_TERM + off) =
-                            make_uint4(w[term][0], w[term][1], w[term][2], w[term][3]);
+                    for (int i = 0; i < 8; ++i) {
+                        // elements 128h + 16i .. 128h + 16i+15: chunk i of the block's row
+                        uint32_t w[2][4];
+                        const uint32_t words[8] = {qv[2 * i].x,     qv[2 * i].y,     qv[2 * i].z,     qv[2 * i].w,
+                                                   qv[2 * i + 1].x, qv[2 * i + 1].y, qv[2 * i + 1].z, qv[2 * i + 1].w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const uint32_t x0 = words[2 * e], x1 = words[2 * e + 1];
+                            const float v0 = bf16_lo(x0) * sq, v1 = bf16_hi(x0) * sq;
+                            const float v2 = bf16_lo(x1) * sq, v3 = bf16_hi(x1) * sq;
+                            const uint32_t h01 = f32x2_to_e4m3x2(v0, v1), h23 = f32x2_to_e4m3x2(v2, v3);
+                            const float2 a01 = e4m3x2_to_f32x2(h01), a23 = e4m3x2_to_f32x2(h23);
+                            const uint32_t l01 = f32x2_to_e4m3x2(v0 - a01.x, v1 - a01.y);
+                            const uint32_t l23 = f32x2_to_e4m3x2(v2 - a23.x, v3 - a23.y);
+                            w[0][e] = h01 | (h23 << 16);
+                            w[1][e] = l01 | (l23 << 16);
+                        }
+                        const uint32_t off = (((uint32_t)i ^ (uint32_t)(t & 7)) << 4);
+#pragma unroll
+                        for (int term = 0; term < 2; ++term)
+                            *reinterpret_cast<uint4*>(q8 + term * C::Q8_TERM + off) =
+                                make_uint4(w[term][0], w[term][1], w[term][2], w[term][3]);
+                    }
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -545,9 +581,9 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
                     break;
                 }
                 const float* meta = reinterpret_cast<const float*>(smem + C::OFF_META + st * C::META_STRIDE);
-                float kf[8], vf[8];   // per 16-key block of the tile
+                float kf[C::BN / 16], vf[C::BN / 16];   // per 16-key block of the tile
 #pragma unroll
-                for (int q16 = 0; q16 < 8; ++q16) {
+                for (int q16 = 0; q16 < C::BN / 16; ++q16) {
                     kf[q16] = crow * meta[(q16 * 16) >> lp];
                     vf[q16] = meta[8 + ((q16 * 16) >> lp)];
                 }
@@ -556,7 +592,11 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
                 tc_fence_after();
                 const uint32_t sc_addr = t_s + C::BN * b + lane_off;
                 uint32_t sv[C::BN];
-                tmem_ld128(sc_addr, *reinterpret_cast<uint32_t(*)[128]>(sv));
+                if constexpr (C::BN == 128) {
+                    tmem_ld128(sc_addr, *reinterpret_cast<uint32_t(*)[128]>(sv));
+                } else {
+                    tmem_ld64(sc_addr, *reinterpret_cast<uint32_t(*)[64]>(sv));
+                }
                 // the logits in log2 units, in place
 #pragma unroll
                 for (int e = 0; e < C::BN; ++e) sv[e] = __float_as_uint(__uint_as_float(sv[e]) * kf[e >> 4]);
@@ -596,7 +636,7 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
                     }
                     tc_fence_after();
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
+                    for (int q = 0; q < C::D / 32; ++q) {
                         uint32_t ov[32];
                         tmem_ld32(t_o + lane_off + 32 * q, ov);
 #pragma unroll
@@ -612,7 +652,7 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
                 const float m_use = (m_run == -CUDART_INF_F) ? 0.f : m_run;
                 float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
+                for (int q = 0; q < C::BN / 64; ++q) {
                     uint32_t pk[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
@@ -644,7 +684,7 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
             tc_fence_after();
             const float inv = (bad || l_run == 0.f) ? 0.f : 1.f / l_run;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < C::D / 32; ++q) {
                 uint32_t ov[32];
                 tmem_ld32(t_o + lane_off + 32 * q, ov);
                 if (valid) {
@@ -678,6 +718,27 @@ __global__ void __launch_bounds__(PrefillFp8Cfg::NTHREADS, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == C::W_QK) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// The launch: one CTA per SM, persistent over the items; the window build for
+// a sliding window, else the lean one (a scale <= 0 needs nothing special
+// here: logits are scaled before their max).
+template <int D>
+cudaError_t launch_prefill_fp8_dim(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
+                                   cudaStream_t st) {
+    using C = PrefillFp8CfgD<D>;
+    auto kern = p.window > 0 ? attn_prefill_fp8_kernel<true, D> : attn_prefill_fp8_kernel<false, D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    long long grid = sms;
+    if (grid > p.n_items) grid = p.n_items;
+    if (grid < 1) grid = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(C::NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = st;
+    return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 
 }  // namespace rad

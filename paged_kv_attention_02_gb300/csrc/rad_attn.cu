@@ -75,10 +75,10 @@ rad::TileInfo tile_for(int head_dim, int kv_dtype, int family) {
 }
 
 // Prefill chunks (no split) run on the tcgen05 prefill kernels when whole
-// query heads tile their 128-row blocks: head_dim 128 over bf16 and fp8 pools,
-// head_dim 256 over bf16 pools.
+// query heads tile their 128-row blocks: head_dim 128 or 256, bf16 or fp8 pools.
 bool use_prefill_tc(int32_t rows, int32_t ratio, int32_t head_dim, int32_t kv_dtype) {
-    const bool dim_ok = head_dim == 128 || (head_dim == 256 && kv_dtype == RAD_KV_BF16 && RAD_PREFILL_TC05_D256);
+    const bool dim_ok = head_dim == 128 ||
+                        (head_dim == 256 && (kv_dtype == RAD_KV_BF16 ? RAD_PREFILL_TC05_D256 : RAD_PREFILL_FP8_D256));
     return rows > rad::kSplitMaxRows && dim_ok && ratio <= 128 && 128 % ratio == 0;
 }
 
@@ -117,7 +117,8 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
                                                                                    : rad::kFamWide;
     if (pl.family == rad::kFamPrefillTC)
         pl.tile = rad::TileInfo{head_dim, kv_dtype == RAD_KV_FP8_E4M3 ? 1 : 0, 4, 0, 0,
-                                kv_dtype == RAD_KV_FP8_E4M3 ? 128 : rad::prefill_tc05_tile_keys(head_dim),
+                                kv_dtype == RAD_KV_FP8_E4M3 ? rad::prefill_fp8_tile_keys(head_dim)
+                                                            : rad::prefill_tc05_tile_keys(head_dim),
                                 RAD_PREFILL_NSK + RAD_PREFILL_NSV, 128, 256, 0, RAD_PREFILL_CTAS};
     else if (pl.family == rad::kFamSplitTC)
         pl.tile = rad::split_tc05_info(pl.M <= 8, head_dim);
@@ -488,9 +489,12 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
         if (encode_map(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, k_pool, 3, kd, ks, kb) != RAD_OK ||
             encode_map(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, v_pool, 3, kd, ks, kb) != RAD_OK)
             return RAD_E_CUDA;
-        e = pl.family != rad::kFamSplitTC ? rad::launch_prefill_fp8(tk, tv, p, sms, st)
-            : head_dim == 128             ? rad::launch_split_tc05(tk, tv, p, sms, st, pl.M <= 8)
-                                          : rad::launch_split_tc05_d256(tk, tv, p, sms, st);
+        if (pl.family == rad::kFamSplitTC)
+            e = head_dim == 128 ? rad::launch_split_tc05(tk, tv, p, sms, st, pl.M <= 8)
+                                : rad::launch_split_tc05_d256(tk, tv, p, sms, st);
+        else
+            e = head_dim == 128 ? rad::launch_prefill_fp8(tk, tv, p, sms, st)
+                                : rad::launch_prefill_fp8_d256(tk, tv, p, sms, st);
     } else if (pl.family == rad::kFamSplitBf) {
         rc = get_encoder();
         if (rc != RAD_OK) return rc;
@@ -568,11 +572,12 @@ int describe_call(int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_
     if (pl.family == rad::kFamPrefillTC && kv_dtype == RAD_KV_FP8_E4M3) {
         snprintf(buf, buf_len,
                  "attn_prefill_tc05 family=%s head_dim=%d kv=fp8e4m3 query_rows_per_kv_head=%d tile_rows=128 "
-                 "keys_per_tile=128 k_stages=%d v_stages=%d ctas_per_sm=1 warps=4 softmax+1 qk (+ half the v "
+                 "keys_per_tile=%d k_stages=%d v_stages=%d ctas_per_sm=1 warps=4 softmax+1 qk (+ half the v "
                  "convert)+1 pv (+ half the v convert)+2 producers mma=tcgen05 (QK kind::f8f6f4 on the staged e4m3 "
                  "K with Q as two e4m3 terms, PV kind::f16 with V e4m3 -> f16 once per tile and P f16 from TMEM) "
                  "split_len=0",
-                 family_name(pl.family), head_dim, pl.M, RAD_PREFILL_FP8_NSK, RAD_PREFILL_FP8_NSV);
+                 family_name(pl.family), head_dim, pl.M, t.KS, head_dim == 128 ? RAD_PREFILL_FP8_NSK : 3,
+                 head_dim == 128 ? RAD_PREFILL_FP8_NSV : 3);
         return RAD_OK;
     }
     if (pl.family == rad::kFamPrefillTC) {

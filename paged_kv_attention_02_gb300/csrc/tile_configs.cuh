@@ -27,10 +27,13 @@ enum Family : int { kFamDecode = 0, kFamVerify = 1, kFamWide = 2, kFamPrefillTC 
 #ifndef RAD_SPLIT_TC05_D256
 #define RAD_SPLIT_TC05_D256 1
 #endif
-// Prefill chunks with head_dim 256 over bf16 pools run on the tcgen05 prefill
-// kernel's head_dim-256 build; 0 keeps them on the mma.sync wide tile.
+// Prefill chunks with head_dim 256 over bf16 (fp8) pools run on the tcgen05
+// prefill kernels' head_dim-256 builds; 0 keeps them on the mma.sync wide tile.
 #ifndef RAD_PREFILL_TC05_D256
 #define RAD_PREFILL_TC05_D256 1
+#endif
+#ifndef RAD_PREFILL_FP8_D256
+#define RAD_PREFILL_FP8_D256 1
 #endif
 
 // Keys per split for calls of up to kSplitMaxRows rows; longer calls (prefill
@@ -182,6 +185,9 @@ cudaError_t launch_prefill_tc05_d256(const CUtensorMap& tq, const CUtensorMap& t
 int prefill_tc05_tile_keys(int head_dim);
 cudaError_t launch_prefill_fp8(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
                                cudaStream_t st);
+cudaError_t launch_prefill_fp8_d256(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
+                                    cudaStream_t st);
+int prefill_fp8_tile_keys(int head_dim);
 cudaError_t launch_split_tc05(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
                               cudaStream_t st, bool few);
 cudaError_t launch_split_tc05_d256(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,

@@ -56,6 +56,11 @@ MID = {
                               pages_per_seq=60, meta=dict(head_dim=256, n_embd=3408)),
     "prefill_d256_r1": wl.Config("prefill_d256_r1", 1, 272, 4, 4, 256, 16, wl.KV_BF16, 119, "fixed:900",
                                  pages_per_seq=64),
+    # a GQA ratio (3) that does not tile the prefill kernels' 128-row blocks: the mma.sync wide tile
+    "prefill_fp8_d256_r3": wl.Config("prefill_fp8_d256_r3", 1, 260, 6, 2, 256, 32, wl.KV_FP8_E4M3, 120,
+                                     "fixed:900", pages_per_seq=30),
+    "prefill_fp8_d256_2g": wl.Config("prefill_fp8_d256_2g", 2, 300, 16, 2, 256, 32, wl.KV_FP8_E4M3, 121,
+                                     "fixed:300,1500", pages_per_seq=60),
 }
 
 
@@ -207,7 +212,7 @@ def test_full_size_prefill_chunk_is_bit_identical_alone_and_batched(full):
     assert np.array_equal(bits(both)[0], bits(alone)[0])
 
 
-@pytest.mark.parametrize("name", ["prefill", "prefill_fp8", "prefill_fp8_r1", "prefill_d256"])
+@pytest.mark.parametrize("name", ["prefill", "prefill_fp8", "prefill_fp8_r1", "prefill_d256", "prefill_fp8_d256_2g"])
 def test_prefill_rows_bit_identical_alone_and_batched(mid, name):
     w, dw = mid(name)
     out, _ = dw.run()
@@ -248,13 +253,14 @@ def test_verified_rows_equal_decode_rows_bit_for_bit(mid, name):
 # ------------------------------------------------------------------ errors never fault
 
 def test_q_beyond_f16_range_flags_only_the_fp8_wide_tile(mid):
-    """fp8 pools with head_dim 256 on the mma.sync wide tile (prefill chunks)
-    round q to f16: an element past its range raises RAD_ERRW_QRANGE (the other
-    rows still match the oracle).  The tcgen05 e4m3 kernels split q exactly
-    into two e4m3 terms with a per-row power-of-two scale and raise nothing,
-    at either head_dim."""
+    """fp8 pools with head_dim 256 on the mma.sync wide tile (prefill chunks
+    whose GQA ratio does not tile 128 rows) round q to f16: an element past its
+    range raises RAD_ERRW_QRANGE (the other rows still match the oracle).  The
+    tcgen05 e4m3 kernels split q exactly into two e4m3 terms with a per-row
+    power-of-two scale and raise nothing, at either head_dim."""
     big = 100352.0   # a bf16 value past the f16 maximum (65504)
-    for name, flagged in (("prefill_fp8_d256", True), ("dec_fp8_d256", False), ("dec_fp8_ratio1", False)):
+    for name, flagged in (("prefill_fp8_d256_r3", True), ("prefill_fp8_d256", False), ("dec_fp8_d256", False),
+                          ("dec_fp8_ratio1", False)):
         w, dw = mid(name)
         q = w.q.copy()
         q[0, 0, 0, 5] = np.array([big], dtype=np.float32).view(np.uint32)[0] >> 16   # bf16 bits
@@ -311,7 +317,8 @@ def test_verify_bad_page_in_a_late_split_zeroes_every_row(mid):
     assert np.all(ob[4] == 0) and np.array_equal(ob[:4], gb[:4])
 
 
-@pytest.mark.parametrize("name", ["chunk_split", "prefill", "prefill_fp8_d256", "prefill_fp8", "prefill_d256"])
+@pytest.mark.parametrize("name", ["chunk_split", "prefill", "prefill_fp8_d256", "prefill_fp8", "prefill_d256",
+                                  "prefill_fp8_d256_r3"])
 def test_bad_last_page_zeroes_rows_of_every_query_tile(mid, name):
     # Calls with several query tiles per KV head: the early tiles never load
     # the last page, yet a bad id there zeroes every row of the group.

@@ -44,6 +44,8 @@ CASES = [
     ("prefill_fp8_plain", (2, 384, 8, 2, 128, 16, 1, 215, "fixed:384,2000"), 160, 0),
     ("prefill_d256_window", (2, 300, 16, 2, 256, 32, 0, 216, "fixed:300,1500"), 60, 257),
     ("prefill_d256_plain", (1, 384, 16, 2, 256, 32, 0, 217, "fixed:2000"), 70, 0),
+    ("prefill_fp8_d256_window", (2, 300, 16, 2, 256, 32, 1, 218, "fixed:300,1500"), 60, 257),
+    ("prefill_fp8_d256_plain", (1, 384, 16, 2, 256, 32, 1, 219, "fixed:2000"), 70, 0),
 ]
 
 
