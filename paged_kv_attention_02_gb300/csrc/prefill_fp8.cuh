@@ -487,11 +487,8 @@ __global__ void __launch_bounds__(PrefillFp8CfgD<D>::NTHREADS, 1)
                 if (t == 0 && p.err_word) atomicOr(p.err_word, kErrSeqLen);
                 continue;
             }
-            // ---- the row's query as two e4m3 terms (the previous item's QKs are done)
-            if (ic >= 1 && !__all_sync(0xffffffffu, mbar_wait_bounded(bar_q8_empty, (ic - 1) & 1u, p.wait_ns))) {
-                abort = true;
-                break;
-            }
+            // ---- the row's query as two e4m3 terms, written once the previous item's
+            // QKs are done (the row is loaded and its scale found before that wait)
             float isq = 1.f;   // 2^-k: the row's logits scale back
             {
                 const uint4* qrow = reinterpret_cast<const uint4*>(
@@ -517,6 +514,11 @@ __global__ void __launch_bounds__(PrefillFp8CfgD<D>::NTHREADS, 1)
                 const int kx = max(-126, min(127, 7 - ex));
                 const float sq = __uint_as_float((uint32_t)(kx + 127) << 23);
                 isq = __uint_as_float((uint32_t)(127 - kx) << 23);
+                if (ic >= 1 &&
+                    !__all_sync(0xffffffffu, mbar_wait_bounded(bar_q8_empty, (ic - 1) & 1u, p.wait_ns))) {
+                    abort = true;
+                    break;
+                }
 #pragma unroll
                 for (int h = 0; h < C::D / 128; ++h) {
                     if (C::D > 128) {

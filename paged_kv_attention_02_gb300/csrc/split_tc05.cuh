@@ -378,11 +378,11 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW, D>::NTHREADS, 1)
             const ItemPlan it = plan_item<C, WIN>(item, p);
             if (!real(it)) continue;
             // ---- this copy of the item's query rows as two e4m3 terms, once the
-            // previous item's QKs are done and the softmax warps have read its 2^-k
-            if (ic >= 1 && !__all_sync(0xffffffffu, mbar_wait_bounded(bar_q8_empty, (ic - 1) & 1u, p.wait_ns))) {
-                abort = true;
-                break;
-            }
+            // previous item's QKs are done and the softmax warps have read its 2^-k;
+            // the rows are loaded (and their scale found) before that wait
+            const auto q8_free = [&]() {
+                return ic == 0 || __all_sync(0xffffffffu, mbar_wait_bounded(bar_q8_empty, (ic - 1) & 1u, p.wait_ns));
+            };
             {
                 const int r = lane;
                 const int nrows = it.m_end - it.m0;
@@ -406,6 +406,10 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW, D>::NTHREADS, 1)
                     const int ex = amax > 0.f ? (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 : 7;
                     const int kx = max(-126, min(127, 7 - ex));
                     const float sq = __uint_as_float((uint32_t)(kx + 127) << 23);
+                    if (!q8_free()) {
+                        abort = true;
+                        break;
+                    }
                     if (cv == 0) isq_s[(ic & 1u) * 32 + r] = __uint_as_float((uint32_t)(127 - kx) << 23);
                     const int qr = 32 * cv + r;   // this copy's row of the M = 128 operand
                     uint8_t* q8 = smem + C::OFF_Q8 + qr * 128;
@@ -457,6 +461,10 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW, D>::NTHREADS, 1)
                     const int ex = amax > 0.f ? (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 : 7;
                     const int kx = max(-126, min(127, 7 - ex));
                     const float sq = __uint_as_float((uint32_t)(kx + 127) << 23);
+                    if (!q8_free()) {
+                        abort = true;
+                        break;
+                    }
                     if (cv == 0) isq_s[(ic & 1u) * 32 + r] = __uint_as_float((uint32_t)(127 - kx) << 23);
                     const int qr = 32 * cv + r;   // this copy's row of the M = 128 operand
 #pragma unroll 4
