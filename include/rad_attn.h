@@ -101,10 +101,13 @@ enum { RAD_KV_BF16 = 0, RAD_KV_FP8_E4M3 = 1 };
 enum {
     RAD_ERRW_SEQLEN = 1u,  /* seq_lens[g] < rows or > pages_per_seq*page_size */
     RAD_ERRW_PAGE = 2u,    /* a page id the group needs is outside [0, num_pages) */
-    RAD_ERRW_QRANGE = 4u,  /* fp8 pools with head_dim 256: a q element beyond
-                              the f16 range (|q| > 65504) -- that row's output
-                              is not meaningful (head_dim 128 carries q exactly
-                              and never raises it) */
+    RAD_ERRW_QRANGE = 4u,  /* fp8 pools with head_dim 256, calls of more than
+                              256 rows whose n_head/n_head_kv does not divide
+                              128 (the mma.sync wide tile, which rounds q to
+                              f16): a q element beyond the f16 range
+                              (|q| > 65504) -- that row's output is not
+                              meaningful.  Every other call carries q exactly
+                              and never raises it. */
     RAD_ERRW_TIMEOUT = 8u, /* an internal wait ran past its time limit (2 s
                               by default); the kernel unwinds and returns,
                               the affected outputs are not meaningful, and
