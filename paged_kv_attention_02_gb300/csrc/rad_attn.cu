@@ -526,8 +526,9 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
         if (encode_bf16_map(&tq, q, 4, qd, qs, qb) != RAD_OK || encode_bf16_map(&tk, k_pool, 3, kd, ks, kb) != RAD_OK ||
             encode_bf16_map(&tv, v_pool, 3, kd, ks, kb) != RAD_OK)
             return RAD_E_CUDA;
-        e = head_dim == 128 ? rad::launch_prefill_tc05(tq, tk, tv, p, sms, st)
-                            : rad::launch_prefill_tc05_d256(tq, tk, tv, p, sms, st);
+        e = head_dim == 256  ? rad::launch_prefill_tc05_d256(tq, tk, tv, p, sms, st)
+            : RAD_PREFILL_PAIR ? rad::launch_prefill_tc05_pair(tq, tk, tv, p, sms, st)
+                               : rad::launch_prefill_tc05(tq, tk, tv, p, sms, st);
     } else if (head_dim == 128)
         e = fp8 ? rad::launch_d128_fp8(pl.family, p, sms, st) : rad::launch_d128_bf16(pl.family, p, sms, st);
     else

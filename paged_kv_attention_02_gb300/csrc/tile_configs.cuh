@@ -35,6 +35,11 @@ enum Family : int { kFamDecode = 0, kFamVerify = 1, kFamWide = 2, kFamPrefillTC 
 #ifndef RAD_PREFILL_FP8_D256
 #define RAD_PREFILL_FP8_D256 1
 #endif
+// Prefill chunks with head_dim 128 over bf16 pools run two query tiles per
+// work item (prefill_pair.cuh); 0 keeps one tile per item (prefill_tc05.cuh).
+#ifndef RAD_PREFILL_PAIR
+#define RAD_PREFILL_PAIR 1
+#endif
 
 // Keys per split for calls of up to kSplitMaxRows rows; longer calls (prefill
 // chunks) run one range per query tile.  A multiple of every tile's KS.
@@ -181,6 +186,8 @@ cudaError_t launch_d256_fp8(int family, const AttnParams& p, int sms, cudaStream
 cudaError_t launch_prefill_tc05(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const AttnParams& p, int sms, cudaStream_t st);
 cudaError_t launch_prefill_tc05_d256(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                     const AttnParams& p, int sms, cudaStream_t st);
+cudaError_t launch_prefill_tc05_pair(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                      const AttnParams& p, int sms, cudaStream_t st);
 int prefill_tc05_tile_keys(int head_dim);
 cudaError_t launch_prefill_fp8(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p, int sms,
