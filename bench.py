@@ -51,23 +51,41 @@ FALLBACK_HBM_GBS = 6800.0
 # where the workload is too large to capture), valid only while the sources
 # that kernel is built from hash to `src_sha256`.
 _BF16_SPLIT_SOURCES = ("split_bf16_tc05.cuh", "sched.cuh", "attn_tile.cuh", "tc05.cuh", "ptx.cuh", "combine.cuh",
-                       "launch.cuh", "tile_configs.cuh", "kern_split_bf16_tc05.cu", "kern_split_bf16_tc05_d256.cu",
-                       "rad_attn.cu")
+                       "launch.cuh", "tile_configs.cuh", "kern_split_bf16_tc05.cu", "kern_split_bf16_tc05_d256.cu")
 _E4M3_SPLIT_SOURCES = ("split_tc05.cuh", "sched.cuh", "attn_tile.cuh", "tc05.cuh", "ptx.cuh", "combine.cuh",
-                       "launch.cuh", "tile_configs.cuh", "kern_split_tc05.cu", "rad_attn.cu")
+                       "launch.cuh", "tile_configs.cuh", "kern_split_tc05.cu", "kern_split_tc05_d256.cu")
+_BF16_PREFILL_SOURCES = ("prefill_pair.cuh", "prefill_tc05.cuh", "attn_tile.cuh", "tc05.cuh", "ptx.cuh",
+                         "tile_configs.cuh", "kern_prefill_pair.cu", "kern_prefill_tc05_d256.cu")
+_FP8_PREFILL_SOURCES = ("prefill_fp8.cuh", "prefill_tc05.cuh", "sched.cuh", "attn_tile.cuh", "tc05.cuh", "ptx.cuh",
+                        "tile_configs.cuh", "kern_prefill_fp8.cu", "kern_prefill_fp8_d256.cu")
 NCU_TRAFFIC: dict[str, dict] = {
-    "batched_decode": {"bytes_per_launch": 4_532_758_546, "sources": _BF16_SPLIT_SOURCES,
-                       "src_sha256": "2c31db0c9fd78129262051e538642ec38a6226436ba76032125a75807ead07c6",
+    "batched_decode": {"bytes_per_launch": 4532795290, "sources": _BF16_SPLIT_SOURCES,
+                       "src_sha256": "224e20c9b2dad8286499e5e3a742a7ea437eacaac58f3fa39ac90e2aedaeff23",
                        "capture": "64 sequences, scaled by the KV bytes (x 4.3412)"},
-    "hybrid_decode": {"bytes_per_launch": 2_295_206_334, "sources": _BF16_SPLIT_SOURCES,
-                      "src_sha256": "2c31db0c9fd78129262051e538642ec38a6226436ba76032125a75807ead07c6",
+    "hybrid_decode": {"bytes_per_launch": 2295690616, "sources": _BF16_SPLIT_SOURCES,
+                      "src_sha256": "224e20c9b2dad8286499e5e3a742a7ea437eacaac58f3fa39ac90e2aedaeff23",
                       "capture": "32 sequences, scaled by the KV bytes (x 3.8372)"},
-    "spec_verify": {"bytes_per_launch": 1_284_122_492, "sources": _E4M3_SPLIT_SOURCES,
-                    "src_sha256": "b49bacb64e8f9d7dd8026127aaf7c9be22f8458c49dfcacd40206f1615d820b0",
+    "spec_verify": {"bytes_per_launch": 1285175227, "sources": _E4M3_SPLIT_SOURCES,
+                    "src_sha256": "7cfc926fed6d08a076e9a8dd716cb947355428c8e2ad1734bbf9d240b04ed115",
                     "capture": "16 sequences, scaled by the KV bytes (x 4.4698)"},
-    "tiny_decode": {"bytes_per_launch": 678_400, "sources": _BF16_SPLIT_SOURCES,
-                    "src_sha256": "2c31db0c9fd78129262051e538642ec38a6226436ba76032125a75807ead07c6",
+    "tiny_decode": {"bytes_per_launch": 678656, "sources": _BF16_SPLIT_SOURCES,
+                    "src_sha256": "224e20c9b2dad8286499e5e3a742a7ea437eacaac58f3fa39ac90e2aedaeff23",
                     "capture": "the whole workload"},
+    "prefill_chunk": {"bytes_per_launch": 51_253_760, "sources": _BF16_PREFILL_SOURCES,
+                      "src_sha256": "d5a859414136e9823fed8ae8529778c4de4b24099bb8216af0ff07bb87867ba4",
+                      "capture": "the whole workload (K/V re-reads served by L2)"},
+    "prefill_chunk_fp8": {"bytes_per_launch": 33_652_224, "sources": _FP8_PREFILL_SOURCES,
+                          "src_sha256": "a2647dcfd673425fe562b68198f2508c5172df1e97f6b2370a96a91b54f86dc5",
+                          "capture": "the whole workload (K/V re-reads served by L2)"},
+    "prefill_chunk_d256": {"bytes_per_launch": 33_628_928, "sources": _BF16_PREFILL_SOURCES,
+                           "src_sha256": "d5a859414136e9823fed8ae8529778c4de4b24099bb8216af0ff07bb87867ba4",
+                           "capture": "the whole workload (K/V re-reads served by L2)"},
+    "prefill_chunk_d256_fp8": {"bytes_per_launch": 25_282_048, "sources": _FP8_PREFILL_SOURCES,
+                               "src_sha256": "a2647dcfd673425fe562b68198f2508c5172df1e97f6b2370a96a91b54f86dc5",
+                               "capture": "the whole workload (K/V re-reads served by L2)"},
+    "hybrid_decode_fp8": {"bytes_per_launch": 1368119845, "sources": _E4M3_SPLIT_SOURCES,
+                          "src_sha256": "7cfc926fed6d08a076e9a8dd716cb947355428c8e2ad1734bbf9d240b04ed115",
+                          "capture": "32 sequences, scaled by the KV bytes (x 4.1277)"},
 }
 
 

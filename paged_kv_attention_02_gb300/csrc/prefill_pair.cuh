@@ -3,7 +3,8 @@
 //
 // The arithmetic of a row is that of prefill_tc05.cuh (S = Q K^T in TMEM, a
 // lazily rescaled running max in log2 units, P written back over S as bf16
-// hi + lo, O += P V in TMEM, O / l at the end), over 64-key tiles.  What
+// hi + lo, O += P V in TMEM, O / l at the end), over 64-key tiles (RAD_PAIR_BN;
+// the 128-key build, one S buffer per query tile, measured slower).  What
 // changes is the work item: (sequence g, KV head kvh, query tiles 2qp and
 // 2qp + 1), so every K and V tile that lands in shared memory serves 256
 // query rows.  Per 128 query rows and key that halves the TMA page boxes (two
@@ -12,12 +13,14 @@
 // per query tile (the per-tile softmax on four warps bounded it as well).
 //
 // Tensor memory (512 columns): O_k at 128 k, and S/P buffers b of query tile
-// k at 256 + 128 k + 64 b (k, b in {0, 1}).
+// k at 256 + 128 k + BN b (k in {0, 1}; b < NSB: two buffers of 64 keys, or
+// one of 128).
 //
 // Warp roles (one CTA per SM, persistent over items, heavier items first):
 //   warps 0-3   softmax of query tile 0 (thread t: its row t, TMEM lane t)
 //   warp 4      QK: per key tile j, once K_j landed, issues S_0 = Q_0 K_j^T into
-//               S buffer (0, j & 1) once PV_0(j-2) is done, then S_1 likewise
+//               S buffer (0, j mod NSB) once PV_0(j-NSB) is done, then S_1
+//               likewise
 //   warp 5      PV: per key tile j, once V_j landed, issues O_0 += P_0 V_j once
 //               P_0(j) is written, then O_1; it first zeroes V rows past the
 //               sequence's end (and below the item's first visible key in the
@@ -27,8 +30,8 @@
 //   warp 7      V producer: the same for V
 //   warps 8-11  softmax of query tile 1
 // Waits on the per-tile barriers follow prefill_tc05.cuh (PV of tile t
-// completes a phase of pv_done[k][t & 1]; a thread that has seen S_k(t)
-// knows PV_k(t-2) is done).  Every wait is bounded; on a time-out the CTA sets
+// completes a phase of pv_done[k][t mod NSB]; a thread that has seen S_k(t)
+// knows PV_k(t-NSB) is done).  Every wait is bounded; on a time-out the CTA sets
 // RAD_ERRW_TIMEOUT and unwinds, waiting (bounded) for its copies and MMAs
 // before freeing TMEM.
 #pragma once
@@ -40,12 +43,16 @@
 
 namespace rad {
 
+#ifndef RAD_PAIR_BN
+#define RAD_PAIR_BN 64
+#endif
 struct PrefPairCfg {
     static constexpr int D = 128;
     static constexpr int BM = 128;                  // query rows per query tile
-    static constexpr int BN = 64;                   // keys per tile
-    static constexpr int NSK = 4;                   // K stages
-    static constexpr int NSV = 4;                   // V stages
+    static constexpr int BN = RAD_PAIR_BN;          // keys per tile
+    static constexpr int NSB = BN == 64 ? 2 : 1;    // S/P buffers per query tile
+    static constexpr int NSK = BN == 64 ? 4 : 2;    // K stages
+    static constexpr int NSV = BN == 64 ? 4 : 2;    // V stages
     static constexpr int HB_BYTES = BN * 128;       // one 64-column block of a K/V tile: [key][128 B]
     static constexpr int QHB_BYTES = BM * 128;      // one 64-column block of a query tile
     static constexpr int TILE_BYTES = BN * D * 2;   // K or V tile
@@ -173,7 +180,7 @@ __global__ void __launch_bounds__(PrefPairCfg::NTHREADS, 1)
     tc_fence_after();
     const uint32_t tmem = misc[0];
     const auto t_o = [&](int k) { return tmem + 128u * (uint32_t)k; };
-    const auto t_s = [&](int k, uint32_t b) { return tmem + 256u + 128u * (uint32_t)k + 64u * b; };
+    const auto t_s = [&](int k, uint32_t b) { return tmem + 256u + 128u * (uint32_t)k + (uint32_t)C::BN * b; };
 
     const int n_items = p.n_items;
     bool abort = false;
@@ -278,16 +285,16 @@ __global__ void __launch_bounds__(PrefPairCfg::NTHREADS, 1)
             }
             tc_fence_after();
             for (int j = 0; j < pi.T; ++j) {
-                const uint32_t s_ = sc + j, st = s_ % C::NSK, tcj = tc + j, b = tcj & 1u;
+                const uint32_t s_ = sc + j, st = s_ % C::NSK, tcj = tc + j, b = tcj % C::NSB;
                 if (!mbar_wait_bounded(bar_k_full + 8 * st, (s_ / C::NSK) & 1u, p.wait_ns)) {
                     abort = true;
                     break;
                 }
                 const uint32_t kb = base + C::OFF_K + st * C::TILE_BYTES;
                 for (int k = 0; k < 2 && !abort; ++k) {
-                    // S buffer (k, b) is free: PV_k(tcj - 2) read the P it held
-                    if (tcj >= 2 &&
-                        !mbar_wait_bounded(bar_pv_done + 8 * (2 * k + b), ((tcj - 2) >> 1) & 1u, p.wait_ns)) {
+                    // S buffer (k, b) is free: PV_k(tcj - NSB) read the P it held
+                    if (tcj >= (uint32_t)C::NSB &&
+                        !mbar_wait_bounded(bar_pv_done + 8 * (2 * k + b), ((tcj - C::NSB) / C::NSB) & 1u, p.wait_ns)) {
                         abort = true;
                         break;
                     }
@@ -340,7 +347,7 @@ __global__ void __launch_bounds__(PrefPairCfg::NTHREADS, 1)
             const int zero_lo = pi.L, zero_hi = ((pi.L + P - 1) / P) * P;
             const int head_lo = (pi.q[0].klo / P) * P, head_hi = pi.q[0].klo;
             for (int jj = 0; jj < pi.T; ++jj) {
-                const uint32_t tcj = tc + jj, b = tcj & 1u;
+                const uint32_t tcj = tc + jj, b = tcj % C::NSB;
                 const uint32_t s_ = sc + jj, st = s_ % C::NSV;
                 if (!mbar_wait_bounded(bar_v_full + 8 * st, (s_ / C::NSV) & 1u, p.wait_ns)) {
                     abort = true;
@@ -364,7 +371,7 @@ __global__ void __launch_bounds__(PrefPairCfg::NTHREADS, 1)
                 }
                 for (int k = 0; k < 2 && !abort; ++k) {
                     // P_k(j) written, and at an item's first tile O_k read out
-                    bool ok = mbar_wait_bounded(bar_p_full + 8 * (2 * k + b), (tcj >> 1) & 1u, p.wait_ns);
+                    bool ok = mbar_wait_bounded(bar_p_full + 8 * (2 * k + b), (tcj / C::NSB) & 1u, p.wait_ns);
                     if (ok && jj == 0 && ic >= 1) ok = mbar_wait_bounded(bar_o_free + 8 * k, (ic - 1) & 1u, p.wait_ns);
                     if (!__all_sync(0xffffffffu, ok)) {
                         abort = true;
@@ -437,18 +444,22 @@ __global__ void __launch_bounds__(PrefPairCfg::NTHREADS, 1)
             const int nlo = (GEN && valid) ? first_visible_key(it.L, p.rows, r, p.window) : 0;   // row sees nlo .. nk-1
             float m_run = -CUDART_INF_F, l_run = 0.f;
             for (int j = 0; j < pi.T; ++j) {
-                const uint32_t tcj = tc + j, b = tcj & 1u;
+                const uint32_t tcj = tc + j, b = tcj % C::NSB;
                 // (every exit from here is taken by the whole warp: the tcgen05
                 // loads and stores below are warp-collective)
                 if (!__all_sync(0xffffffffu,
-                                mbar_wait_bounded(bar_s_full + 8 * (2 * k + b), (tcj >> 1) & 1u, p.wait_ns))) {
+                                mbar_wait_bounded(bar_s_full + 8 * (2 * k + b), (tcj / C::NSB) & 1u, p.wait_ns))) {
                     abort = true;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t sc_ = t_s(k, b) + lane_off;
                 uint32_t sv[C::BN];
-                tmem_ld64(sc_, sv);
+                if constexpr (C::BN == 128) {
+                    tmem_ld128(sc_, *reinterpret_cast<uint32_t(*)[128]>(sv));
+                } else {
+                    tmem_ld64(sc_, *reinterpret_cast<uint32_t(*)[64]>(sv));
+                }
                 // Logits are scaled by c after the max; a scale <= 0 would turn
                 // that order around (and -inf * 0 into NaN), so then the tile is
                 // scaled first and c taken as 1.
@@ -490,8 +501,8 @@ __global__ void __launch_bounds__(PrefPairCfg::NTHREADS, 1)
                 if (__any_sync(0xffffffffu, need)) {
                     // PV of the previous tile must have landed before O is rescaled
                     const uint32_t tp = tcj - 1;
-                    const bool ok = j == 0 ||
-                                    mbar_wait_bounded(bar_pv_done + 8 * (2 * k + (tp & 1u)), (tp >> 1) & 1u, p.wait_ns);
+                    const bool ok = j == 0 || mbar_wait_bounded(bar_pv_done + 8 * (2 * k + tp % C::NSB),
+                                                                 (tp / C::NSB) & 1u, p.wait_ns);
                     if (!__all_sync(0xffffffffu, ok)) {
                         abort = true;
                         break;
@@ -544,7 +555,8 @@ __global__ void __launch_bounds__(PrefPairCfg::NTHREADS, 1)
             }
             // ---- epilogue: O / l -> bf16
             const uint32_t tcl = tc + pi.T - 1;
-            if (!mbar_wait_bounded(bar_pv_done + 8 * (2 * k + (tcl & 1u)), (tcl >> 1) & 1u, p.wait_ns)) abort = true;
+            if (!mbar_wait_bounded(bar_pv_done + 8 * (2 * k + tcl % C::NSB), (tcl / C::NSB) & 1u, p.wait_ns))
+                abort = true;
             tc_fence_after();
             const float inv = (bad || l_run == 0.f) ? 0.f : 1.f / l_run;
 #pragma unroll

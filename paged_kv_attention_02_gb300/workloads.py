@@ -112,6 +112,17 @@ CONFIGS: dict[str, Config] = {
     "mixed_step": Config("mixed_step", 121, 256, 32, 8, 128, 16, KV_BF16, 6, "uniform:512,8192",
                          pages_per_seq=512, q_lens="96x1,24x8,1x256",
                          meta=dict(n_head=32, n_head_kv=8, head_dim=128, n_embd=4096)),
+    # The hybrid model's shapes at head_dim 256 (read from its metadata): its
+    # decode over an fp8 cache, and a prefill chunk over bf16 and fp8 caches.
+    "hybrid_decode_fp8": Config("hybrid_decode_fp8", 128, 1, 16, 2, 256, 32, KV_FP8_E4M3, 8,
+                                "loguniform:1024,32768", pages_per_seq=1024,
+                                meta=dict(n_head=16, n_head_kv=2, head_dim=256, n_embd=3408)),
+    "prefill_chunk_d256": Config("prefill_chunk_d256", 1, 2048, 16, 2, 256, 32, KV_BF16, 9, "fixed:8192",
+                                 pages_per_seq=256, pool_pages=256,
+                                 meta=dict(n_head=16, n_head_kv=2, head_dim=256, n_embd=3408)),
+    "prefill_chunk_d256_fp8": Config("prefill_chunk_d256_fp8", 1, 2048, 16, 2, 256, 32, KV_FP8_E4M3, 10,
+                                     "fixed:8192", pages_per_seq=256, pool_pages=256,
+                                     meta=dict(n_head=16, n_head_kv=2, head_dim=256, n_embd=3408)),
 }
 
 
