@@ -45,9 +45,9 @@
 //   warps 8-11   converters, one per scheduler partition: converter c turns key
 //                rows 32c .. 32c+31 of every staged e4m3 V tile into f16 (a
 //                quarter-rate instruction: on the MMA or softmax warps it set
-//                the pace), and at each item's start splits its copy of the
-//                query rows into the two e4m3 terms (overlapping the previous
-//                item's last tiles and merge).
+//                the pace), and at each item's start splits a quarter of every
+//                query row into the two e4m3 terms, written to the row's four
+//                copies (overlapping the previous item's last tiles and merge).
 // PV of tile t completes a phase of pv_done[t & 1]; a thread that has seen
 // S(t) knows PV(t-2) is done (QK(t) waited for it), so no wait on pv_done is
 // two phases ahead of its barrier (see prefill_tc05.cuh); the converters wait
@@ -366,7 +366,7 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW, D>::NTHREADS, 1)
         __syncwarp();
     } else if (warp >= C::W_CONV) {
         // ===================================================== converters
-        const int cv = warp - C::W_CONV;   // (row, block) pairs 32cv .. 32cv+31 of every V tile; query-row copy cv
+        const int cv = warp - C::W_CONV;   // (row, block) pairs 32cv .. 32cv+31 of every V tile; query-row quarter cv
         uint32_t tc = 0, ic = 0;
         for (uint32_t n = 0; !abort; ++n) {
             int item;
@@ -377,9 +377,10 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW, D>::NTHREADS, 1)
             if (item < 0) break;
             const ItemPlan it = plan_item<C, WIN>(item, p);
             if (!real(it)) continue;
-            // ---- this copy of the item's query rows as two e4m3 terms, once the
-            // previous item's QKs are done and the softmax warps have read its 2^-k;
-            // the rows are loaded (and their scale found) before that wait
+            // ---- the item's query rows as two e4m3 terms (this converter a quarter of
+            // every row, into all four copies), once the previous item's QKs are done and
+            // the softmax warps have read its 2^-k; each row's scale is found before that
+            // wait
             const auto q8_free = [&]() {
                 return ic == 0 || __all_sync(0xffffffffu, mbar_wait_bounded(bar_q8_empty, (ic - 1) & 1u, p.wait_ns));
             };
@@ -389,110 +390,62 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW, D>::NTHREADS, 1)
                 const bool valid = r < nrows;
                 const int m = it.m0 + r;
                 const int tok = m / p.ratio, hl = m - tok * p.ratio;
-                if constexpr (C::D == 128) {
-                    uint4 qv[16];
-                    const __nv_bfloat16* qrow = p.q + ((it.qrow0 + tok) * p.n_head + it.kvh * p.ratio + hl) * C::D;
+                // the row's largest magnitude, 128 bytes at a time
+                const uint4* qrow =
+                    reinterpret_cast<const uint4*>(p.q + ((it.qrow0 + tok) * p.n_head + it.kvh * p.ratio + hl) * C::D);
+                float amax = 0.f;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        qv[i] = valid ? __ldg(reinterpret_cast<const uint4*>(qrow) + i) : make_uint4(0u, 0u, 0u, 0u);
-                    float amax = 0.f;
+                for (int h = 0; h < C::D / 64; ++h) {
+                    uint4 qv[8];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
+                    for (int i = 0; i < 8; ++i) qv[i] = valid ? __ldg(qrow + 8 * h + i) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
                         const uint32_t x[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(x[e])), fabsf(bf16_hi(x[e]))));
                     }
-                    // 2^k with amax * 2^k in [128, 256): k = 7 - floor(log2 amax), kept a normal float
-                    const int ex = amax > 0.f ? (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 : 7;
-                    const int kx = max(-126, min(127, 7 - ex));
-                    const float sq = __uint_as_float((uint32_t)(kx + 127) << 23);
-                    if (!q8_free()) {
-                        abort = true;
-                        break;
+                }
+                // 2^k with amax * 2^k in [128, 256): k = 7 - floor(log2 amax), kept a normal float
+                const int ex = amax > 0.f ? (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 : 7;
+                const int kx = max(-126, min(127, 7 - ex));
+                const float sq = __uint_as_float((uint32_t)(kx + 127) << 23);
+                if (!q8_free()) {
+                    abort = true;
+                    break;
+                }
+                if (cv == 0) isq_s[(ic & 1u) * 32 + r] = __uint_as_float((uint32_t)(127 - kx) << 23);
+                // this converter's quarter of the row (16-element chunks CH cv .. CH cv + CH-1,
+                // read again from L1) as the two terms, written to all four copies of the row
+                constexpr int CH = C::D / 64;
+#pragma unroll
+                for (int ii = 0; ii < CH; ++ii) {
+                    const int i = CH * cv + ii;   // chunk i % 8 of column block i / 8 of each term's row
+                    uint32_t wt[2][4];
+                    const uint4 qa = valid ? __ldg(qrow + 2 * i) : make_uint4(0u, 0u, 0u, 0u);
+                    const uint4 qb = valid ? __ldg(qrow + 2 * i + 1) : make_uint4(0u, 0u, 0u, 0u);
+                    const uint32_t words[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const uint32_t x0 = words[2 * e], x1 = words[2 * e + 1];
+                        const float v0 = bf16_lo(x0) * sq, v1 = bf16_hi(x0) * sq;
+                        const float v2 = bf16_lo(x1) * sq, v3 = bf16_hi(x1) * sq;
+                        const uint32_t h01 = f32x2_to_e4m3x2(v0, v1), h23 = f32x2_to_e4m3x2(v2, v3);
+                        const float2 a01 = e4m3x2_to_f32x2(h01), a23 = e4m3x2_to_f32x2(h23);
+                        const uint32_t l01 = f32x2_to_e4m3x2(v0 - a01.x, v1 - a01.y);
+                        const uint32_t l23 = f32x2_to_e4m3x2(v2 - a23.x, v3 - a23.y);
+                        wt[0][e] = h01 | (h23 << 16);
+                        wt[1][e] = l01 | (l23 << 16);
                     }
-                    if (cv == 0) isq_s[(ic & 1u) * 32 + r] = __uint_as_float((uint32_t)(127 - kx) << 23);
-                    const int qr = 32 * cv + r;   // this copy's row of the M = 128 operand
-                    uint8_t* q8 = smem + C::OFF_Q8 + qr * 128;
+                    // row 32 copy + r of the M = 128 operand; (32 copy + r) & 7 = r & 7
+                    uint8_t* q8 = smem + C::OFF_Q8 + (i >> 3) * C::Q8_BLK + r * 128 +
+                                  ((((uint32_t)i & 7u) ^ (uint32_t)(r & 7)) << 4);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        // elements 16i .. 16i+15: chunk i of each term's row
-                        uint32_t wt[2][4];
-                        const uint32_t words[8] = {qv[2 * i].x,     qv[2 * i].y,     qv[2 * i].z,     qv[2 * i].w,
-                                                   qv[2 * i + 1].x, qv[2 * i + 1].y, qv[2 * i + 1].z, qv[2 * i + 1].w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const uint32_t x0 = words[2 * e], x1 = words[2 * e + 1];
-                            const float v0 = bf16_lo(x0) * sq, v1 = bf16_hi(x0) * sq;
-                            const float v2 = bf16_lo(x1) * sq, v3 = bf16_hi(x1) * sq;
-                            const uint32_t h01 = f32x2_to_e4m3x2(v0, v1), h23 = f32x2_to_e4m3x2(v2, v3);
-                            const float2 a01 = e4m3x2_to_f32x2(h01), a23 = e4m3x2_to_f32x2(h23);
-                            const uint32_t l01 = f32x2_to_e4m3x2(v0 - a01.x, v1 - a01.y);
-                            const uint32_t l23 = f32x2_to_e4m3x2(v2 - a23.x, v3 - a23.y);
-                            wt[0][e] = h01 | (h23 << 16);
-                            wt[1][e] = l01 | (l23 << 16);
-                        }
-                        const uint32_t off = (((uint32_t)i ^ (uint32_t)(qr & 7)) << 4);
+                    for (int copy = 0; copy < 4; ++copy)
 #pragma unroll
                         for (int term = 0; term < 2; ++term)
-                            *reinterpret_cast<uint4*>(q8 + term * C::Q8_TERM + off) =
+                            *reinterpret_cast<uint4*>(q8 + copy * 32 * 128 + term * C::Q8_TERM) =
                                 make_uint4(wt[term][0], wt[term][1], wt[term][2], wt[term][3]);
-                    }
-                } else {
-                    // a 512-byte row: two passes, a quarter of it at a time (few
-                    // registers; the second pass reads it from L1): its largest
-                    // magnitude, then the terms
-                    const uint4* qrow =
-                        reinterpret_cast<const uint4*>(p.q + ((it.qrow0 + tok) * p.n_head + it.kvh * p.ratio + hl) * C::D);
-                    float amax = 0.f;
-#pragma unroll
-                    for (int h = 0; h < C::D / 64; ++h) {
-                        uint4 qv[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) qv[i] = valid ? __ldg(qrow + 8 * h + i) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const uint32_t x[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(x[e])), fabsf(bf16_hi(x[e]))));
-                        }
-                    }
-                    // 2^k with amax * 2^k in [128, 256): k = 7 - floor(log2 amax), kept a normal float
-                    const int ex = amax > 0.f ? (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 : 7;
-                    const int kx = max(-126, min(127, 7 - ex));
-                    const float sq = __uint_as_float((uint32_t)(kx + 127) << 23);
-                    if (!q8_free()) {
-                        abort = true;
-                        break;
-                    }
-                    if (cv == 0) isq_s[(ic & 1u) * 32 + r] = __uint_as_float((uint32_t)(127 - kx) << 23);
-                    const int qr = 32 * cv + r;   // this copy's row of the M = 128 operand
-#pragma unroll 4
-                    for (int i = 0; i < C::D / 16; ++i) {
-                        // elements 16i .. 16i+15: chunk i % 8 of column block i / 8 of each term's row
-                        uint32_t wt[2][4];
-                        const uint4 qa = valid ? __ldg(qrow + 2 * i) : make_uint4(0u, 0u, 0u, 0u);
-                        const uint4 qb = valid ? __ldg(qrow + 2 * i + 1) : make_uint4(0u, 0u, 0u, 0u);
-                        const uint32_t words[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const uint32_t x0 = words[2 * e], x1 = words[2 * e + 1];
-                            const float v0 = bf16_lo(x0) * sq, v1 = bf16_hi(x0) * sq;
-                            const float v2 = bf16_lo(x1) * sq, v3 = bf16_hi(x1) * sq;
-                            const uint32_t h01 = f32x2_to_e4m3x2(v0, v1), h23 = f32x2_to_e4m3x2(v2, v3);
-                            const float2 a01 = e4m3x2_to_f32x2(h01), a23 = e4m3x2_to_f32x2(h23);
-                            const uint32_t l01 = f32x2_to_e4m3x2(v0 - a01.x, v1 - a01.y);
-                            const uint32_t l23 = f32x2_to_e4m3x2(v2 - a23.x, v3 - a23.y);
-                            wt[0][e] = h01 | (h23 << 16);
-                            wt[1][e] = l01 | (l23 << 16);
-                        }
-                        uint8_t* q8 = smem + C::OFF_Q8 + (i >> 3) * C::Q8_BLK + qr * 128 +
-                                      ((((uint32_t)i & 7u) ^ (uint32_t)(qr & 7)) << 4);
-#pragma unroll
-                        for (int term = 0; term < 2; ++term)
-                            *reinterpret_cast<uint4*>(q8 + term * C::Q8_TERM) =
-                                make_uint4(wt[term][0], wt[term][1], wt[term][2], wt[term][3]);
-                    }
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
