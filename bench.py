@@ -65,8 +65,8 @@ NCU_TRAFFIC: dict[str, dict] = {
     "hybrid_decode": {"bytes_per_launch": 2295690616, "sources": _BF16_SPLIT_SOURCES,
                       "src_sha256": "224e20c9b2dad8286499e5e3a742a7ea437eacaac58f3fa39ac90e2aedaeff23",
                       "capture": "32 sequences, scaled by the KV bytes (x 3.8372)"},
-    "spec_verify": {"bytes_per_launch": 1285175227, "sources": _E4M3_SPLIT_SOURCES,
-                    "src_sha256": "7cfc926fed6d08a076e9a8dd716cb947355428c8e2ad1734bbf9d240b04ed115",
+    "spec_verify": {"bytes_per_launch": 1285582563, "sources": _E4M3_SPLIT_SOURCES,
+                    "src_sha256": "6efb78392a018e884c7b403466417507c8bad63a6e725958a688aef358a97c7f",
                     "capture": "16 sequences, scaled by the KV bytes (x 4.4698)"},
     "tiny_decode": {"bytes_per_launch": 678656, "sources": _BF16_SPLIT_SOURCES,
                     "src_sha256": "224e20c9b2dad8286499e5e3a742a7ea437eacaac58f3fa39ac90e2aedaeff23",
@@ -83,8 +83,8 @@ NCU_TRAFFIC: dict[str, dict] = {
     "prefill_chunk_d256_fp8": {"bytes_per_launch": 25_282_048, "sources": _FP8_PREFILL_SOURCES,
                                "src_sha256": "a2647dcfd673425fe562b68198f2508c5172df1e97f6b2370a96a91b54f86dc5",
                                "capture": "the whole workload (K/V re-reads served by L2)"},
-    "hybrid_decode_fp8": {"bytes_per_launch": 1368119845, "sources": _E4M3_SPLIT_SOURCES,
-                          "src_sha256": "7cfc926fed6d08a076e9a8dd716cb947355428c8e2ad1734bbf9d240b04ed115",
+    "hybrid_decode_fp8": {"bytes_per_launch": 1368660256, "sources": _E4M3_SPLIT_SOURCES,
+                          "src_sha256": "6efb78392a018e884c7b403466417507c8bad63a6e725958a688aef358a97c7f",
                           "capture": "32 sequences, scaled by the KV bytes (x 4.1277)"},
 }
 
