@@ -47,7 +47,12 @@
 //                quarter-rate instruction: on the MMA or softmax warps it set
 //                the pace), and at each item's start splits a quarter of every
 //                query row into the two e4m3 terms, written to the row's four
-//                copies (overlapping the previous item's last tiles and merge).
+//                copies (overlapping the previous item's last tiles and merge);
+//                each loads only its quarter of the rows, the row's scale coming
+//                from the four quarters' largest exponents, exchanged through
+//                shared memory.  At the start they pull the call's query rows
+//                into L2: behind the K/V stream a row load from HBM at an item
+//                boundary took ~3 us.
 // PV of tile t completes a phase of pv_done[t & 1]; a thread that has seen
 // S(t) knows PV(t-2) is done (QK(t) waited for it), so no wait on pv_done is
 // two phases ahead of its barrier (see prefill_tc05.cuh); the converters wait
@@ -79,6 +84,11 @@
 #endif
 #ifndef RAD_SPLITTC256_NSV
 #define RAD_SPLITTC256_NSV 2
+#endif
+
+// The converters pull the call's query rows into L2 at the start (uniform calls).
+#ifndef RAD_SPLITTC_Q_L2
+#define RAD_SPLITTC_Q_L2 1
 #endif
 
 namespace rad {
@@ -117,12 +127,14 @@ struct SplitTcCfg {
     static constexpr int OFF_V16 = OFF_V + NSV * KV_TILE;
     static constexpr int OFF_SCR = OFF_V16 + 2 * V16_BYTES;
     static constexpr int OFF_ML = OFF_SCR + SCR_BYTES;      // [2][4][32]: the quarters' row max, sum
-    static constexpr int OFF_ISQ = OFF_ML + 2 * 4 * 32 * 4;  // [2][32]: each row's 2^-k, by item parity
-    static constexpr int OFF_META = OFF_ISQ + 2 * 32 * 4;
+    // [2][4][32] bytes, by item parity: the exponent field of each row's largest magnitude
+    // within each quarter of its elements (the row's scale 2^k follows from their max)
+    static constexpr int OFF_QEXP = OFF_ML + 2 * 4 * 32 * 4;
+    static constexpr int OFF_META = OFF_QEXP + 2 * 4 * 32;
     static constexpr int OFF_BARS = OFF_META + NSK * META_STRIDE;
     // q8_full, q8_empty, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[2], p_full[2],
     // pv_done[2], v16_full[2], o_free, final[2]
-    static constexpr int NBARS = 2 + 2 * NSK + 2 * NSV + 2 + 2 + 2 + 2 + 1 + 2;
+    static constexpr int NBARS = 2 + 2 * NSK + 2 * NSV + 2 + 2 + 2 + 2 + 1 + 2 + 2;
     static constexpr int OFF_RING = OFF_BARS + NBARS * 8;     // the item ring (sched.cuh)
     static constexpr int OFF_MISC = OFF_RING + kRingBytesNoTaken;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // 1 KB alignment of the swizzled tiles
@@ -174,6 +186,15 @@ __device__ __forceinline__ void convert_v_row(const uint8_t* stage, uint8_t* v16
     }
 }
 
+// k of a query row's scale 2^k: the largest magnitude a of the row times 2^k lies
+// in [128, 256), k = 7 - floor(log2 a) kept to a normal float's range; from the
+// exponent fields of the row's four quarter maxima (`qexp`: [quarter][32 rows]).
+// (An all-zero row gets k = 127: every product with it is 0 whatever k is.)
+__device__ __forceinline__ int row_scale_exp(const uint8_t* qexp, int r) {
+    const int e = max(max((int)qexp[r], (int)qexp[32 + r]), max((int)qexp[64 + r], (int)qexp[96 + r]));
+    return max(-126, min(127, 7 - (e - 127)));
+}
+
 // MODE: kModeCausal, kModeWindow or kModeTree (draft-tree rows, uniform row
 // counts: bit i of a row's mask word lets it see the call's key i).
 template <int MODE, bool FEW, int D = 128>
@@ -200,8 +221,8 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW, D>::NTHREADS, 1)
     const uint32_t bar_v16_full = bar_pv_done + 16;         // [2], by tile parity: the converters' rows
     const uint32_t bar_o_free = bar_v16_full + 16;
     const uint32_t bar_final = bar_o_free + 8;              // [2]: QK warp, PV warp
+    const uint32_t bar_amax = bar_final + 16;               // [2], by item parity: the converters' quarter maxima
     volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);  // [0] tmem, [1] abort
-    float* const isq_s = reinterpret_cast<float*>(smem + C::OFF_ISQ);
     const ItemRing iring(smem + C::OFF_RING, base + C::OFF_RING);
 
     const int warp = threadIdx.x >> 5;
@@ -227,6 +248,8 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW, D>::NTHREADS, 1)
         mbar_init(bar_o_free, 4);
         mbar_init(bar_final, 1);
         mbar_init(bar_final + 8, 1);
+        mbar_init(bar_amax, 4);
+        mbar_init(bar_amax + 8, 4);
         iring.init(C::RING_CONSUMERS, false);
         misc[1] = 0;
         fence_mbarrier_init();
@@ -367,6 +390,15 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW, D>::NTHREADS, 1)
     } else if (warp >= C::W_CONV) {
         // ===================================================== converters
         const int cv = warp - C::W_CONV;   // (row, block) pairs 32cv .. 32cv+31 of every V tile; query-row quarter cv
+        if (RAD_SPLITTC_Q_L2 && !p.cu_seqlens) {
+            // The call's query rows (a few MB) into L2, a slice per CTA: they are read again
+            // at every item boundary, where a load from HBM behind the K/V stream took ~3 us
+            const size_t qbytes = (size_t)p.groups * p.rows * p.n_head * C::D * 2;
+            const size_t per = ((qbytes + gridDim.x - 1) / gridDim.x + 127) & ~(size_t)127;
+            const size_t lo = per * blockIdx.x, hi = min(qbytes, lo + per);
+            for (size_t off = lo + 128 * (size_t)(cv * 32 + lane); off < hi; off += 128 * 128)
+                prefetch_l2(reinterpret_cast<const char*>(p.q) + off);
+        }
         uint32_t tc = 0, ic = 0;
         for (uint32_t n = 0; !abort; ++n) {
             int item;
@@ -390,40 +422,42 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW, D>::NTHREADS, 1)
                 const bool valid = r < nrows;
                 const int m = it.m0 + r;
                 const int tok = m / p.ratio, hl = m - tok * p.ratio;
-                // the row's largest magnitude, 128 bytes at a time
+                // this converter's quarter of the row (16-element chunks CH cv .. CH cv + CH-1),
+                // its largest magnitude shared with the other converters: the row's scale
+                constexpr int CH = C::D / 64;
                 const uint4* qrow =
                     reinterpret_cast<const uint4*>(p.q + ((it.qrow0 + tok) * p.n_head + it.kvh * p.ratio + hl) * C::D);
-                float amax = 0.f;
+                uint4 qq[2 * CH];
 #pragma unroll
-                for (int h = 0; h < C::D / 64; ++h) {
-                    uint4 qv[8];
+                for (int i = 0; i < 2 * CH; ++i)
+                    qq[i] = valid ? __ldg(qrow + 2 * CH * cv + i) : make_uint4(0u, 0u, 0u, 0u);
+                float amq = 0.f;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) qv[i] = valid ? __ldg(qrow + 8 * h + i) : make_uint4(0u, 0u, 0u, 0u);
+                for (int i = 0; i < 2 * CH; ++i) {
+                    const uint32_t x[4] = {qq[i].x, qq[i].y, qq[i].z, qq[i].w};
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const uint32_t x[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(x[e])), fabsf(bf16_hi(x[e]))));
-                    }
+                    for (int e = 0; e < 4; ++e) amq = fmaxf(amq, fmaxf(fabsf(bf16_lo(x[e])), fabsf(bf16_hi(x[e]))));
                 }
-                // 2^k with amax * 2^k in [128, 256): k = 7 - floor(log2 amax), kept a normal float
-                const int ex = amax > 0.f ? (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 : 7;
-                const int kx = max(-126, min(127, 7 - ex));
+                uint8_t* const qexp = smem + C::OFF_QEXP + (ic & 1u) * 128;
+                qexp[cv * 32 + r] = (uint8_t)((__float_as_uint(amq) >> 23) & 0xFFu);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_amax + 8 * (ic & 1u));
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar_amax + 8 * (ic & 1u), (ic >> 1) & 1u, p.wait_ns))) {
+                    abort = true;
+                    break;
+                }
+                const int kx = row_scale_exp(qexp, r);
                 const float sq = __uint_as_float((uint32_t)(kx + 127) << 23);
                 if (!q8_free()) {
                     abort = true;
                     break;
                 }
-                if (cv == 0) isq_s[(ic & 1u) * 32 + r] = __uint_as_float((uint32_t)(127 - kx) << 23);
-                // this converter's quarter of the row (16-element chunks CH cv .. CH cv + CH-1,
-                // read again from L1) as the two terms, written to all four copies of the row
-                constexpr int CH = C::D / 64;
+                // the quarter as the two terms, written to all four copies of the row
 #pragma unroll
                 for (int ii = 0; ii < CH; ++ii) {
                     const int i = CH * cv + ii;   // chunk i % 8 of column block i / 8 of each term's row
                     uint32_t wt[2][4];
-                    const uint4 qa = valid ? __ldg(qrow + 2 * i) : make_uint4(0u, 0u, 0u, 0u);
-                    const uint4 qb = valid ? __ldg(qrow + 2 * i + 1) : make_uint4(0u, 0u, 0u, 0u);
+                    const uint4 qa = qq[2 * ii], qb = qq[2 * ii + 1];
                     const uint32_t words[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -670,7 +704,7 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW, D>::NTHREADS, 1)
                 abort = true;
                 break;
             }
-            const float isq = isq_s[(ic & 1u) * 32 + r];
+            const float isq = __uint_as_float((uint32_t)(127 - row_scale_exp(smem + C::OFF_QEXP + (ic & 1u) * 128, r)) << 23);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_q8_empty);
             // keys row r sees: [nlo, nk) (tree rows: every cached key, of the call's
