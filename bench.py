@@ -60,31 +60,31 @@ _FP8_PREFILL_SOURCES = ("prefill_fp8.cuh", "prefill_tc05.cuh", "sched.cuh", "att
                         "tile_configs.cuh", "kern_prefill_fp8.cu", "kern_prefill_fp8_d256.cu")
 NCU_TRAFFIC: dict[str, dict] = {
     "batched_decode": {"bytes_per_launch": 4532795290, "sources": _BF16_SPLIT_SOURCES,
-                       "src_sha256": "224e20c9b2dad8286499e5e3a742a7ea437eacaac58f3fa39ac90e2aedaeff23",
+                       "src_sha256": "613e2a936b7fbed949d3215a752984e620ebfa2269b8cbd7539766a41fe2efb1",
                        "capture": "64 sequences, scaled by the KV bytes (x 4.3412)"},
     "hybrid_decode": {"bytes_per_launch": 2295690616, "sources": _BF16_SPLIT_SOURCES,
-                      "src_sha256": "224e20c9b2dad8286499e5e3a742a7ea437eacaac58f3fa39ac90e2aedaeff23",
+                      "src_sha256": "613e2a936b7fbed949d3215a752984e620ebfa2269b8cbd7539766a41fe2efb1",
                       "capture": "32 sequences, scaled by the KV bytes (x 3.8372)"},
-    "spec_verify": {"bytes_per_launch": 1285582563, "sources": _E4M3_SPLIT_SOURCES,
-                    "src_sha256": "6efb78392a018e884c7b403466417507c8bad63a6e725958a688aef358a97c7f",
+    "spec_verify": {"bytes_per_launch": 1283237957, "sources": _E4M3_SPLIT_SOURCES,
+                    "src_sha256": "ef63e82755f88ef77c19bfdbede2d880d85ac6089b46ad88f887033ed40e908a",
                     "capture": "16 sequences, scaled by the KV bytes (x 4.4698)"},
     "tiny_decode": {"bytes_per_launch": 678656, "sources": _BF16_SPLIT_SOURCES,
-                    "src_sha256": "224e20c9b2dad8286499e5e3a742a7ea437eacaac58f3fa39ac90e2aedaeff23",
+                    "src_sha256": "613e2a936b7fbed949d3215a752984e620ebfa2269b8cbd7539766a41fe2efb1",
                     "capture": "the whole workload"},
     "prefill_chunk": {"bytes_per_launch": 51_253_760, "sources": _BF16_PREFILL_SOURCES,
-                      "src_sha256": "d5a859414136e9823fed8ae8529778c4de4b24099bb8216af0ff07bb87867ba4",
+                      "src_sha256": "1d08e58e0778e0a94127011784ab4cb29b0cbde5aa523759409ab50cd11fcd32",
                       "capture": "the whole workload (K/V re-reads served by L2)"},
     "prefill_chunk_fp8": {"bytes_per_launch": 33_652_224, "sources": _FP8_PREFILL_SOURCES,
-                          "src_sha256": "a2647dcfd673425fe562b68198f2508c5172df1e97f6b2370a96a91b54f86dc5",
+                          "src_sha256": "a156c0785f16213876ce426663d8b22d314f583c5f96fabb9fa45adc75b6c9a8",
                           "capture": "the whole workload (K/V re-reads served by L2)"},
     "prefill_chunk_d256": {"bytes_per_launch": 33_628_928, "sources": _BF16_PREFILL_SOURCES,
-                           "src_sha256": "d5a859414136e9823fed8ae8529778c4de4b24099bb8216af0ff07bb87867ba4",
+                           "src_sha256": "1d08e58e0778e0a94127011784ab4cb29b0cbde5aa523759409ab50cd11fcd32",
                            "capture": "the whole workload (K/V re-reads served by L2)"},
     "prefill_chunk_d256_fp8": {"bytes_per_launch": 25_282_048, "sources": _FP8_PREFILL_SOURCES,
-                               "src_sha256": "a2647dcfd673425fe562b68198f2508c5172df1e97f6b2370a96a91b54f86dc5",
+                               "src_sha256": "a156c0785f16213876ce426663d8b22d314f583c5f96fabb9fa45adc75b6c9a8",
                                "capture": "the whole workload (K/V re-reads served by L2)"},
-    "hybrid_decode_fp8": {"bytes_per_launch": 1368660256, "sources": _E4M3_SPLIT_SOURCES,
-                          "src_sha256": "6efb78392a018e884c7b403466417507c8bad63a6e725958a688aef358a97c7f",
+    "hybrid_decode_fp8": {"bytes_per_launch": 1368382346, "sources": _E4M3_SPLIT_SOURCES,
+                          "src_sha256": "ef63e82755f88ef77c19bfdbede2d880d85ac6089b46ad88f887033ed40e908a",
                           "capture": "32 sequences, scaled by the KV bytes (x 4.1277)"},
 }
 
