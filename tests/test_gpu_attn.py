@@ -276,6 +276,46 @@ def test_q_beyond_f16_range_flags_only_the_fp8_wide_tile(mid):
             assert np.all(np.isfinite(as_f64(out)))
 
 
+def _bf16_bits(x):
+    """float array -> bf16 bit patterns (round to nearest even)."""
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("name", ["ver_fp8", "ver_fp8_d256", "dec_fp8_ratio1", "dec_fp8_d256", "prefill_fp8"])
+def test_fp8_query_row_scales_at_the_extremes(mid, name):
+    """The e4m3 kernels split each query row q into two e4m3 terms of q 2^k,
+    k from the row's largest magnitude (the split kernels gather it from four
+    quarters of the row).  Rows of zeros, of bf16 subnormals, of huge values,
+    and rows whose largest element sits alone in the last quarter must match
+    the oracle like any other."""
+    import copy
+    w, dw = mid(name)
+    c = w.cfg
+    D = c.meta.get("head_dim", c.head_dim)
+    q = w.q.copy()
+    rng = np.random.default_rng(7)
+    picks = [(0, t) for t in range(4)] if c.rows >= 4 else [(g, 0) for g in range(min(4, w.groups))]
+    kinds = ["zero", "subnormal", "huge", "lone_max"]
+    for (g, t), kind in zip(picks, kinds):
+        for h in range(c.n_head):
+            if kind == "zero":
+                row = np.zeros(D)
+            elif kind == "subnormal":
+                row = rng.standard_normal(D) * 1e-39        # below bf16's smallest normal (1.2e-38)
+            elif kind == "huge":
+                row = rng.standard_normal(D) * 1e20
+            else:
+                row = rng.standard_normal(D) * 1e-3
+                row[D - 3] = 3e3                              # the last quarter's element dominates
+            q[g, t, h] = _bf16_bits(row)
+    w2 = copy.copy(w)
+    w2.q = q
+    qd = torch.from_numpy(np.ascontiguousarray(q).view(np.int16)).view(torch.bfloat16).cuda()
+    out, err = dw.run(q=qd)
+    assert err == 0
+    assert_parity(as_f64(out), oracle_rows(w2).out, True, name)
+
+
 def test_bad_inputs_flag_errors_and_zero_only_their_group(mid):
     w, dw = mid("dec128")
     good, _ = dw.run()
