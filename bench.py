@@ -72,13 +72,13 @@ NCU_TRAFFIC: dict[str, dict] = {
                     "src_sha256": "613e2a936b7fbed949d3215a752984e620ebfa2269b8cbd7539766a41fe2efb1",
                     "capture": "the whole workload"},
     "prefill_chunk": {"bytes_per_launch": 51_253_760, "sources": _BF16_PREFILL_SOURCES,
-                      "src_sha256": "1d08e58e0778e0a94127011784ab4cb29b0cbde5aa523759409ab50cd11fcd32",
+                      "src_sha256": "caaa9c35e3038fd1573ac57bdca7d958863bd67805bf7c76c17ba5350cb0d313",
                       "capture": "the whole workload (K/V re-reads served by L2)"},
     "prefill_chunk_fp8": {"bytes_per_launch": 33_652_224, "sources": _FP8_PREFILL_SOURCES,
                           "src_sha256": "a156c0785f16213876ce426663d8b22d314f583c5f96fabb9fa45adc75b6c9a8",
                           "capture": "the whole workload (K/V re-reads served by L2)"},
     "prefill_chunk_d256": {"bytes_per_launch": 33_628_928, "sources": _BF16_PREFILL_SOURCES,
-                           "src_sha256": "1d08e58e0778e0a94127011784ab4cb29b0cbde5aa523759409ab50cd11fcd32",
+                           "src_sha256": "caaa9c35e3038fd1573ac57bdca7d958863bd67805bf7c76c17ba5350cb0d313",
                            "capture": "the whole workload (K/V re-reads served by L2)"},
     "prefill_chunk_d256_fp8": {"bytes_per_launch": 25_282_048, "sources": _FP8_PREFILL_SOURCES,
                                "src_sha256": "a156c0785f16213876ce426663d8b22d314f583c5f96fabb9fa45adc75b6c9a8",

@@ -3,8 +3,8 @@
 //
 // The arithmetic of a row is that of prefill_tc05.cuh (S = Q K^T in TMEM, a
 // lazily rescaled running max in log2 units, P written back over S as bf16
-// hi + lo, O += P V in TMEM, O / l at the end), over 64-key tiles (RAD_PAIR_BN;
-// the 128-key build, one S buffer per query tile, measured slower).  What
+// hi + lo, O += P V in TMEM, O / l at the end), over 64-key tiles (128-key tiles
+// with one S buffer per query tile measured slower).  What
 // changes is the work item: (sequence g, KV head kvh, query tiles 2qp and
 // 2qp + 1), so every K and V tile that lands in shared memory serves 256
 // query rows.  Per 128 query rows and key that halves the TMA page boxes (two
@@ -43,16 +43,13 @@
 
 namespace rad {
 
-#ifndef RAD_PAIR_BN
-#define RAD_PAIR_BN 64
-#endif
 struct PrefPairCfg {
     static constexpr int D = 128;
     static constexpr int BM = 128;                  // query rows per query tile
-    static constexpr int BN = RAD_PAIR_BN;          // keys per tile
-    static constexpr int NSB = BN == 64 ? 2 : 1;    // S/P buffers per query tile
-    static constexpr int NSK = BN == 64 ? 4 : 2;    // K stages
-    static constexpr int NSV = BN == 64 ? 4 : 2;    // V stages
+    static constexpr int BN = 64;                   // keys per tile
+    static constexpr int NSB = 2;                   // S/P buffers per query tile
+    static constexpr int NSK = 4;                   // K stages
+    static constexpr int NSV = 4;                   // V stages
     static constexpr int HB_BYTES = BN * 128;       // one 64-column block of a K/V tile: [key][128 B]
     static constexpr int QHB_BYTES = BM * 128;      // one 64-column block of a query tile
     static constexpr int TILE_BYTES = BN * D * 2;   // K or V tile
@@ -455,11 +452,7 @@ __global__ void __launch_bounds__(PrefPairCfg::NTHREADS, 1)
                 tc_fence_after();
                 const uint32_t sc_ = t_s(k, b) + lane_off;
                 uint32_t sv[C::BN];
-                if constexpr (C::BN == 128) {
-                    tmem_ld128(sc_, *reinterpret_cast<uint32_t(*)[128]>(sv));
-                } else {
-                    tmem_ld64(sc_, *reinterpret_cast<uint32_t(*)[64]>(sv));
-                }
+                tmem_ld64(sc_, sv);
                 // Logits are scaled by c after the max; a scale <= 0 would turn
                 // that order around (and -inf * 0 into NaN), so then the tile is
                 // scaled first and c taken as 1.
