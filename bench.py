@@ -60,31 +60,31 @@ _FP8_PREFILL_SOURCES = ("prefill_fp8.cuh", "prefill_tc05.cuh", "sched.cuh", "att
                         "tile_configs.cuh", "kern_prefill_fp8.cu", "kern_prefill_fp8_d256.cu")
 NCU_TRAFFIC: dict[str, dict] = {
     "batched_decode": {"bytes_per_launch": 4532795290, "sources": _BF16_SPLIT_SOURCES,
-                       "src_sha256": "613e2a936b7fbed949d3215a752984e620ebfa2269b8cbd7539766a41fe2efb1",
+                       "src_sha256": "2f6061c7dc82c704d296e83cd176089b119329574b2828aa02f7b09f7cf29957",
                        "capture": "64 sequences, scaled by the KV bytes (x 4.3412)"},
     "hybrid_decode": {"bytes_per_launch": 2295690616, "sources": _BF16_SPLIT_SOURCES,
-                      "src_sha256": "613e2a936b7fbed949d3215a752984e620ebfa2269b8cbd7539766a41fe2efb1",
+                      "src_sha256": "2f6061c7dc82c704d296e83cd176089b119329574b2828aa02f7b09f7cf29957",
                       "capture": "32 sequences, scaled by the KV bytes (x 3.8372)"},
-    "spec_verify": {"bytes_per_launch": 1283237957, "sources": _E4M3_SPLIT_SOURCES,
-                    "src_sha256": "ef63e82755f88ef77c19bfdbede2d880d85ac6089b46ad88f887033ed40e908a",
+    "spec_verify": {"bytes_per_launch": 1257676136, "sources": _E4M3_SPLIT_SOURCES,
+                    "src_sha256": "87aa2f5fb68f6b960c7b91c73cc8e99284244909b0be2db89c4d02736d25f430",
                     "capture": "16 sequences, scaled by the KV bytes (x 4.4698)"},
     "tiny_decode": {"bytes_per_launch": 678656, "sources": _BF16_SPLIT_SOURCES,
-                    "src_sha256": "613e2a936b7fbed949d3215a752984e620ebfa2269b8cbd7539766a41fe2efb1",
+                    "src_sha256": "2f6061c7dc82c704d296e83cd176089b119329574b2828aa02f7b09f7cf29957",
                     "capture": "the whole workload"},
     "prefill_chunk": {"bytes_per_launch": 51_253_760, "sources": _BF16_PREFILL_SOURCES,
-                      "src_sha256": "caaa9c35e3038fd1573ac57bdca7d958863bd67805bf7c76c17ba5350cb0d313",
+                      "src_sha256": "3e65bd4c84f1bcda581e9df5f504243f65e08d9fb7545d79b1c3e7189279f967",
                       "capture": "the whole workload (K/V re-reads served by L2)"},
     "prefill_chunk_fp8": {"bytes_per_launch": 33_652_224, "sources": _FP8_PREFILL_SOURCES,
-                          "src_sha256": "a156c0785f16213876ce426663d8b22d314f583c5f96fabb9fa45adc75b6c9a8",
+                          "src_sha256": "91969330d3e5a1f06cb0f12de2a7ff367c10331433416f468f4766f39a6be35a",
                           "capture": "the whole workload (K/V re-reads served by L2)"},
     "prefill_chunk_d256": {"bytes_per_launch": 33_628_928, "sources": _BF16_PREFILL_SOURCES,
-                           "src_sha256": "caaa9c35e3038fd1573ac57bdca7d958863bd67805bf7c76c17ba5350cb0d313",
+                           "src_sha256": "3e65bd4c84f1bcda581e9df5f504243f65e08d9fb7545d79b1c3e7189279f967",
                            "capture": "the whole workload (K/V re-reads served by L2)"},
     "prefill_chunk_d256_fp8": {"bytes_per_launch": 25_282_048, "sources": _FP8_PREFILL_SOURCES,
-                               "src_sha256": "a156c0785f16213876ce426663d8b22d314f583c5f96fabb9fa45adc75b6c9a8",
+                               "src_sha256": "91969330d3e5a1f06cb0f12de2a7ff367c10331433416f468f4766f39a6be35a",
                                "capture": "the whole workload (K/V re-reads served by L2)"},
     "hybrid_decode_fp8": {"bytes_per_launch": 1368382346, "sources": _E4M3_SPLIT_SOURCES,
-                          "src_sha256": "ef63e82755f88ef77c19bfdbede2d880d85ac6089b46ad88f887033ed40e908a",
+                          "src_sha256": "87aa2f5fb68f6b960c7b91c73cc8e99284244909b0be2db89c4d02736d25f430",
                           "capture": "32 sequences, scaled by the KV bytes (x 4.1277)"},
 }
 

@@ -103,12 +103,12 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
     const bool ragged = ragged_rows >= 0;
     if (pl.split_len > 0 && kv_dtype == RAD_KV_FP8_E4M3 && (head_dim == 128 ? RAD_SPLIT_TC05 : RAD_SPLIT_TC05_D256)) {
         pl.family = rad::kFamSplitTC;
-        pl.split_len = rad::kSplitLenTC;
+        pl.split_len = head_dim == 128 ? rad::kSplitLenTC : rad::kSplitLenTC_E4M3_256;
     }
     else if (pl.split_len > 0 && kv_dtype == RAD_KV_BF16 &&
              (head_dim == 128 ? RAD_SPLIT_BF16_TC05 : RAD_SPLIT_BF16_TC05_D256)) {
         pl.family = rad::kFamSplitBf;
-        pl.split_len = head_dim == 128 ? rad::kSplitLenTC : rad::kSplitLenTC256;
+        pl.split_len = head_dim == 128 ? rad::kSplitLenBf : rad::kSplitLenTC256;
     }
     else if (pl.split_len > 0)
         pl.family = pl.M <= 8 ? rad::kFamDecode : rad::kFamVerify;

@@ -47,16 +47,25 @@ enum Family : int { kFamDecode = 0, kFamVerify = 1, kFamWide = 2, kFamPrefillTC 
 #define RAD_SPLIT_LEN 1024
 #endif
 constexpr int kSplitLen = RAD_SPLIT_LEN;
-// The tcgen05 split kernel's splits (fp8 head_dim-128 split calls): each work
-// item pays a fixed cost (query-row split, epilogue, the wait for its last PV)
-// that longer splits spread over more key tiles.
+// Keys per split of the tcgen05 split kernels: each work item pays a fixed cost
+// (query rows, the merge of its four quarters, the wait for its last PV) that
+// longer splits spread over more key tiles, and fewer, longer items spread
+// less evenly over the SMs.  One length per kernel family and head_dim: a row's
+// bits depend on it, so decode and verify calls of one family share it.
 #ifndef RAD_SPLITTC_LEN
-#define RAD_SPLITTC_LEN 2048
+#define RAD_SPLITTC_LEN 4096   // e4m3 pools, head_dim 128
 #endif
 constexpr int kSplitLenTC = RAD_SPLITTC_LEN;
-// The same for the bf16 tcgen05 split kernel with head_dim 256.
+#ifndef RAD_SPLITTC_LEN_E4M3_D256
+#define RAD_SPLITTC_LEN_E4M3_D256 2048   // e4m3 pools, head_dim 256
+#endif
+constexpr int kSplitLenTC_E4M3_256 = RAD_SPLITTC_LEN_E4M3_D256;
+#ifndef RAD_SPLITBF_LEN
+#define RAD_SPLITBF_LEN 2048   // bf16 pools, head_dim 128
+#endif
+constexpr int kSplitLenBf = RAD_SPLITBF_LEN;
 #ifndef RAD_SPLITTC_LEN_D256
-#define RAD_SPLITTC_LEN_D256 2048
+#define RAD_SPLITTC_LEN_D256 2048   // bf16 pools, head_dim 256
 #endif
 constexpr int kSplitLenTC256 = RAD_SPLITTC_LEN_D256;
 constexpr int kSplitMaxRows = 256;

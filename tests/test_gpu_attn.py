@@ -25,11 +25,11 @@ MID = {
                               "fixed:40,900,1700", pages_per_seq=60),
     "ver_fp8": wl.Config("ver_fp8", 5, 8, 32, 8, 128, 16, wl.KV_FP8_E4M3, 105, "fixed:8,9,520,1000,2050",
                          pages_per_seq=130),
-    # the tcgen05 split kernel's 2048-key splits: lengths on both sides of 1, 2 and 3 splits
+    # the e4m3 tcgen05 split kernel's 4096-key splits: lengths on both sides of 1, 2 and 3 splits
     "ver_fp8_splits": wl.Config("ver_fp8_splits", 6, 8, 32, 8, 128, 16, wl.KV_FP8_E4M3, 116,
-                                "fixed:2047,2048,2049,4095,4097,6145", pages_per_seq=390),
+                                "fixed:4095,4096,4097,8191,8193,12289", pages_per_seq=770),
     "dec_fp8_splits": wl.Config("dec_fp8_splits", 5, 1, 32, 8, 128, 32, wl.KV_FP8_E4M3, 117,
-                                "fixed:2047,2048,2049,4096,4097", pages_per_seq=130),
+                                "fixed:4095,4096,4097,8192,8193", pages_per_seq=260),
     "ver_bf16": wl.Config("ver_bf16", 4, 8, 8, 2, 128, 16, wl.KV_BF16, 106, "fixed:8,100,513,1100",
                           pages_per_seq=70),
     "ver_wide_d256": wl.Config("ver_wide_d256", 3, 8, 16, 2, 256, 32, wl.KV_BF16, 107, "fixed:8,600,1500",
@@ -96,13 +96,13 @@ def test_tiny_decode_matches_oracle_everywhere():
 # ------------------------------------------------------------------ contexts past one combine chunk
 
 # The combine kernel stages a row's partials 128 splits at a time: these contexts
-# have more splits than that (1024-key splits on the tile kernel, 2048 on the
-# tcgen05 split kernel), so rows merge across chunk boundaries.
+# have more splits than that (2048-key splits on the bf16 tcgen05 split kernel,
+# 4096 on the e4m3 one), so rows merge across chunk boundaries.
 LONG = {
-    "long_dec_bf16": wl.Config("long_dec_bf16", 2, 1, 8, 2, 128, 16, wl.KV_BF16, 121, "fixed:140000,1000",
-                               pages_per_seq=8760),
-    "long_ver_fp8": wl.Config("long_ver_fp8", 1, 8, 8, 2, 128, 32, wl.KV_FP8_E4M3, 122, "fixed:270000",
-                              pages_per_seq=8440),
+    "long_dec_bf16": wl.Config("long_dec_bf16", 2, 1, 8, 2, 128, 16, wl.KV_BF16, 121, "fixed:270000,1000",
+                               pages_per_seq=16880),
+    "long_ver_fp8": wl.Config("long_ver_fp8", 1, 8, 8, 2, 128, 32, wl.KV_FP8_E4M3, 122, "fixed:530000",
+                              pages_per_seq=16570),
 }
 
 

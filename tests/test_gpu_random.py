@@ -43,7 +43,7 @@ def random_config(i: int) -> wl.Config:
         if kind < 0.2:
             L = rows                                        # nothing cached
         elif kind < 0.5:
-            L = r.choice([1023, 1024, 1025, 2047, 2048, 2049]) + rows
+            L = r.choice([1023, 1024, 1025, 2047, 2048, 2049, 4095, 4096, 4097]) + rows
         else:
             L = rows + r.randint(1, 3000 if rows < 40 else 2000)
         lens.append(max(L, rows))

@@ -61,9 +61,9 @@ TREES = {
                      True),
     "t32_d128_fp8_r8": (cfg("t32_d128_fp8_r8", 3, 32, 64, 8, 128, 16, wl.KV_FP8_E4M3, 316, "fixed:32,800,3000", 190),
                         False),
-    # the tcgen05 split kernel's 2048-key split boundaries
+    # the e4m3 tcgen05 split kernel's 4096-key split boundaries
     "t8_d128_fp8_splits": (cfg("t8_d128_fp8_splits", 4, 8, 32, 8, 128, 16, wl.KV_FP8_E4M3, 317,
-                               "fixed:2048,2052,4096,4103", 260), True),
+                               "fixed:4096,4100,8192,8199", 520), True),
 }
 
 

@@ -30,9 +30,9 @@ WIN = {
     "ver_fp8_w513": (wl.Config("ver_fp8_w513", 5, 8, 32, 8, 128, 16, wl.KV_FP8_E4M3, 205,
                                "fixed:8,9,600,2100,4000", pages_per_seq=260), 513),
     # head_dim-128 fp8 decode (the tcgen05 split kernel, 16 query rows): windows across its
-    # 2048-key splits, and one narrower than a 32-slot page
+    # 4096-key splits, and one narrower than a 32-slot page
     "dec_fp8_w1000": (wl.Config("dec_fp8_w1000", 6, 1, 32, 8, 128, 16, wl.KV_FP8_E4M3, 214,
-                                "fixed:1,15,1000,2047,2049,6000", pages_per_seq=380), 1000),
+                                "fixed:1,15,1000,4095,4097,9000", pages_per_seq=570), 1000),
     "dec_fp8_p32_w20": (wl.Config("dec_fp8_p32_w20", 4, 1, 16, 4, 128, 32, wl.KV_FP8_E4M3, 215,
                                   "fixed:3,21,2100,4200", pages_per_seq=140), 20),
     "ver_bf16_w4": (wl.Config("ver_bf16_w4", 3, 8, 8, 2, 128, 16, wl.KV_BF16, 206, "fixed:8,30,1500",
