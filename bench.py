@@ -60,16 +60,16 @@ _FP8_PREFILL_SOURCES = ("prefill_fp8.cuh", "prefill_tc05.cuh", "sched.cuh", "att
                         "tile_configs.cuh", "kern_prefill_fp8.cu", "kern_prefill_fp8_d256.cu")
 NCU_TRAFFIC: dict[str, dict] = {
     "batched_decode": {"bytes_per_launch": 4532795290, "sources": _BF16_SPLIT_SOURCES,
-                       "src_sha256": "2f6061c7dc82c704d296e83cd176089b119329574b2828aa02f7b09f7cf29957",
+                       "src_sha256": "2591a1ef194cda6ae803afc73ec243c3d1c532def3f65fd852c6150f82c128ae",
                        "capture": "64 sequences, scaled by the KV bytes (x 4.3412)"},
     "hybrid_decode": {"bytes_per_launch": 2295690616, "sources": _BF16_SPLIT_SOURCES,
-                      "src_sha256": "2f6061c7dc82c704d296e83cd176089b119329574b2828aa02f7b09f7cf29957",
+                      "src_sha256": "2591a1ef194cda6ae803afc73ec243c3d1c532def3f65fd852c6150f82c128ae",
                       "capture": "32 sequences, scaled by the KV bytes (x 3.8372)"},
     "spec_verify": {"bytes_per_launch": 1257676136, "sources": _E4M3_SPLIT_SOURCES,
-                    "src_sha256": "87aa2f5fb68f6b960c7b91c73cc8e99284244909b0be2db89c4d02736d25f430",
+                    "src_sha256": "4c0f6fcfcee9aed2bd0d861f40ef316a867b5057ada75049bb9b58e176c66674",
                     "capture": "16 sequences, scaled by the KV bytes (x 4.4698)"},
     "tiny_decode": {"bytes_per_launch": 678656, "sources": _BF16_SPLIT_SOURCES,
-                    "src_sha256": "2f6061c7dc82c704d296e83cd176089b119329574b2828aa02f7b09f7cf29957",
+                    "src_sha256": "2591a1ef194cda6ae803afc73ec243c3d1c532def3f65fd852c6150f82c128ae",
                     "capture": "the whole workload"},
     "prefill_chunk": {"bytes_per_launch": 51_253_760, "sources": _BF16_PREFILL_SOURCES,
                       "src_sha256": "3e65bd4c84f1bcda581e9df5f504243f65e08d9fb7545d79b1c3e7189279f967",
@@ -84,7 +84,7 @@ NCU_TRAFFIC: dict[str, dict] = {
                                "src_sha256": "91969330d3e5a1f06cb0f12de2a7ff367c10331433416f468f4766f39a6be35a",
                                "capture": "the whole workload (K/V re-reads served by L2)"},
     "hybrid_decode_fp8": {"bytes_per_launch": 1368382346, "sources": _E4M3_SPLIT_SOURCES,
-                          "src_sha256": "87aa2f5fb68f6b960c7b91c73cc8e99284244909b0be2db89c4d02736d25f430",
+                          "src_sha256": "4c0f6fcfcee9aed2bd0d861f40ef316a867b5057ada75049bb9b58e176c66674",
                           "capture": "32 sequences, scaled by the KV bytes (x 4.1277)"},
 }
 

@@ -745,8 +745,9 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW, D>::NTHREADS, 1)
 #define X(e) __uint_as_float(sv[e])
                 const int key0 = it.k0 + j * C::BK + KW * w;
                 const int lim = nk - key0, lim_lo = nlo - key0;   // columns outside [lim_lo, lim) are masked
-                if (TREE) {
+                if (TREE && key0 + KW > n_full) {
                     // key0 + e < n_full: a cached key; else the call's key i = key0 + e - n_full
+                    // (a tile of cached keys only takes the plain test below: i < 0 there)
                     const int ib = key0 - n_full;
 #pragma unroll
                     for (int e = 0; e < KW; ++e) {
