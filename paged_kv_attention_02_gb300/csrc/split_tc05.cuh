@@ -32,8 +32,8 @@
 //                warp-wide), write p x page V scale as f16 to TMEM; per item,
 //                merge the four quarters' (max, sum, O) of each row and store
 //                the row or the split's partial.
-//   warp 4       QK: once K_j landed and PV_{j-2} is done (S, P and f16 V
-//                buffers j & 1 free), lane 0 issues QK_j (2 terms x 4 K-steps).
+//   warp 4       QK: once K_j landed and PV_{j-NSP} is done (S/P buffer
+//                j % NSP free), lane 0 issues QK_j (2 terms x 4 K-steps).
 //   warp 5       PV: once P_j is written and V_j converted, lane 0 issues PV_j.
 //   warps 6, 7   K and V producers: page ids, the per-page K/V scales (into the
 //                K stage's meta block), one TMA box per page (page_size rows x
@@ -53,10 +53,15 @@
 //                shared memory.  At the start they pull the call's query rows
 //                into L2: behind the K/V stream a row load from HBM at an item
 //                boundary took ~3 us.
-// PV of tile t completes a phase of pv_done[t & 1]; a thread that has seen
-// S(t) knows PV(t-2) is done (QK(t) waited for it), so no wait on pv_done is
-// two phases ahead of its barrier (see prefill_tc05.cuh); the converters wait
-// for PV(t-2) at every tile, in order.  Every wait is bounded; a time-out sets
+// TMEM holds O and NSP S/P buffers: the decode form two S buffers and two P
+// buffers of their own (a quarter's lanes zero outside its columns for good),
+// the verify form three S buffers with P written over the first half of its S
+// (zeros over the other quarters' columns at every tile).  PV of tile t
+// completes a phase of pv_done[t % NSP]; a thread that has seen S(t) knows
+// PV(t-NSP) is done (QK(t) waited for it), and every wait on pv_done is for a
+// PV whose barrier cannot complete again before the waiter itself has acted
+// (see prefill_tc05.cuh); the converters wait for PV(t-NV16) at every tile, in
+// order, before they write f16 buffer t % NV16.  Every wait is bounded; a time-out sets
 // RAD_ERRW_TIMEOUT and the roles unwind.
 #pragma once
 #include <cuda.h>
@@ -77,6 +82,15 @@
 #endif
 #ifndef RAD_SPLITTC_NSV
 #define RAD_SPLITTC_NSV 3
+#endif
+// S/P buffers in TMEM (QK of tile t waits for PV of tile t - NSP) and f16 V
+// buffers (the converters' rows of tile t wait for PV of tile t - NV16) of the
+// head_dim-128 verify form; the decode form keeps two and two.
+#ifndef RAD_SPLITTC_NSP
+#define RAD_SPLITTC_NSP 3
+#endif
+#ifndef RAD_SPLITTC_NV16
+#define RAD_SPLITTC_NV16 2
 #endif
 // head_dim 256: the four query copies take 64 KB.
 #ifndef RAD_SPLITTC256_NSK
@@ -111,6 +125,10 @@ struct SplitTcCfg {
                                         : RAD_SPLITTC256_NSK;   // K stages (with the page scales)
     static constexpr int NSV = D == 128 ? (FEW ? RAD_SPLITTC_FEW_NSV : RAD_SPLITTC_NSV)
                                         : RAD_SPLITTC256_NSV;   // V stages
+    static constexpr int NSP = FEW ? 2 : RAD_SPLITTC_NSP;   // S/P buffers in TMEM
+    static constexpr bool P_OVER_S = NSP > 2;       // three S buffers leave no columns for P buffers of its own
+    static constexpr int P_STRIDE = P_OVER_S ? BK : BK / 2;   // TMEM columns from P buffer b to b + 1
+    static constexpr int NV16 = (FEW || D != 128) ? 2 : RAD_SPLITTC_NV16;   // f16 V buffers
     static constexpr int ROW = D;                   // bytes of one e4m3 key row
     static constexpr int KBLK = BK * 128;           // one 128-byte column block of a K or V tile
     static constexpr int KV_TILE = NKB * KBLK;      // e4m3 K or V rows of one tile
@@ -125,16 +143,16 @@ struct SplitTcCfg {
     static constexpr int OFF_K = OFF_Q8 + 2 * Q8_TERM;
     static constexpr int OFF_V = OFF_K + NSK * KV_TILE;
     static constexpr int OFF_V16 = OFF_V + NSV * KV_TILE;
-    static constexpr int OFF_SCR = OFF_V16 + 2 * V16_BYTES;
+    static constexpr int OFF_SCR = OFF_V16 + NV16 * V16_BYTES;
     static constexpr int OFF_ML = OFF_SCR + SCR_BYTES;      // [2][4][32]: the quarters' row max, sum
     // [2][4][32] bytes, by item parity: the exponent field of each row's largest magnitude
     // within each quarter of its elements (the row's scale 2^k follows from their max)
     static constexpr int OFF_QEXP = OFF_ML + 2 * 4 * 32 * 4;
     static constexpr int OFF_META = OFF_QEXP + 2 * 4 * 32;
     static constexpr int OFF_BARS = OFF_META + NSK * META_STRIDE;
-    // q8_full, q8_empty, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[2], p_full[2],
-    // pv_done[2], v16_full[2], o_free, final[2]
-    static constexpr int NBARS = 2 + 2 * NSK + 2 * NSV + 2 + 2 + 2 + 2 + 1 + 2 + 2;
+    // q8_full, q8_empty, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[NSP], p_full[NSP],
+    // pv_done[NSP], v16_full[NV16], o_free, final[2], amax[2]
+    static constexpr int NBARS = 2 + 2 * NSK + 2 * NSV + 3 * NSP + NV16 + 1 + 2 + 2;
     static constexpr int OFF_RING = OFF_BARS + NBARS * 8;     // the item ring (sched.cuh)
     static constexpr int OFF_MISC = OFF_RING + kRingBytesNoTaken;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // 1 KB alignment of the swizzled tiles
@@ -143,10 +161,14 @@ struct SplitTcCfg {
     static constexpr int W_QK = 4, W_PV = 5, W_PROD_K = 6, W_PROD_V = 7, W_CONV = 8;
     static constexpr int K_FULL_ARRIVALS = MAXPG;             // expect-tx arrive + the other page lanes' meta arrives
     static constexpr int K_EMPTY_ARRIVALS = 1 + 4;            // the QK commit + the softmax warps' scale reads
-    // O [0, D), S_b [D + BK b, ...), P_b [D + 2 BK + (BK/2) b, ...)
+    // O [0, D), S_b [D + BK b, ...), P_b (f16 pairs) [D + NSP BK + (BK/2) b, ...) or, with three
+    // S buffers, over the first BK/2 columns of S_b
     static constexpr uint32_t TMEM_COLS = 512;
     static_assert(D == 128 || D == 256, "head_dim 128 or 256");
-    static_assert(D + 2 * BK + BK <= (int)TMEM_COLS, "tensor memory budget");
+    static_assert(D + NSP * BK + (P_OVER_S ? 0 : NSP * (BK / 2)) <= (int)TMEM_COLS, "tensor memory budget");
+    // the converters wait on pv_done for PV(t - NV16) before their rows of tile t; that barrier's
+    // next phase is PV(t - NV16 + NSP), which must need those rows too: NSP >= NV16
+    static_assert(NSP >= NV16, "f16 V buffers");
     static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && OFF_V16 % 1024 == 0 && KV_TILE % 1024 == 0,
                   "1 KB tiles");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -215,11 +237,11 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW, D>::NTHREADS, 1)
     const uint32_t bar_k_empty = bar_k_full + 8 * C::NSK;
     const uint32_t bar_v_full = bar_k_empty + 8 * C::NSK;
     const uint32_t bar_v_empty = bar_v_full + 8 * C::NSV;
-    const uint32_t bar_s_full = bar_v_empty + 8 * C::NSV;   // [2]
-    const uint32_t bar_p_full = bar_s_full + 16;            // [2]
-    const uint32_t bar_pv_done = bar_p_full + 16;           // [2], by tile parity
-    const uint32_t bar_v16_full = bar_pv_done + 16;         // [2], by tile parity: the converters' rows
-    const uint32_t bar_o_free = bar_v16_full + 16;
+    const uint32_t bar_s_full = bar_v_empty + 8 * C::NSV;   // [NSP], by tile % NSP
+    const uint32_t bar_p_full = bar_s_full + 8 * C::NSP;    // [NSP]
+    const uint32_t bar_pv_done = bar_p_full + 8 * C::NSP;   // [NSP]
+    const uint32_t bar_v16_full = bar_pv_done + 8 * C::NSP; // [NV16], by tile % NV16: the converters' rows
+    const uint32_t bar_o_free = bar_v16_full + 8 * C::NV16;
     const uint32_t bar_final = bar_o_free + 8;              // [2]: QK warp, PV warp
     const uint32_t bar_amax = bar_final + 16;               // [2], by item parity: the converters' quarter maxima
     volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC);  // [0] tmem, [1] abort
@@ -239,12 +261,12 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW, D>::NTHREADS, 1)
             mbar_init(bar_v_full + 8 * i, 1);
             mbar_init(bar_v_empty + 8 * i, 4);   // the converters
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < C::NSP; ++i) {
             mbar_init(bar_s_full + 8 * i, 1);
             mbar_init(bar_p_full + 8 * i, 4);
             mbar_init(bar_pv_done + 8 * i, 1);
-            mbar_init(bar_v16_full + 8 * i, 4);
         }
+        for (int i = 0; i < C::NV16; ++i) mbar_init(bar_v16_full + 8 * i, 4);
         mbar_init(bar_o_free, 4);
         mbar_init(bar_final, 1);
         mbar_init(bar_final + 8, 1);
@@ -264,7 +286,7 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW, D>::NTHREADS, 1)
     const uint32_t tmem = misc[0];
     const uint32_t t_o = tmem;
     const uint32_t t_s = tmem + C::D;                // S buffer b at t_s + BK b
-    const uint32_t t_p = tmem + C::D + 2 * C::BK;    // P buffer b at t_p + (BK/2) b
+    const uint32_t t_p = C::P_OVER_S ? t_s : tmem + C::D + C::NSP * C::BK;   // P buffer b at t_p + P_STRIDE b
     bool abort = false;
 
     // items that run the pipeline: active, a valid sequence length, keys to see
@@ -487,10 +509,13 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW, D>::NTHREADS, 1)
             }
             // ---- this converter's rows of every V tile of the item
             for (int j = 0; j < it.n_stages; ++j) {
-                const uint32_t tcj = tc + j, b = tcj & 1u, sv = tcj % C::NSV;
+                const uint32_t tcj = tc + j, b = tcj % C::NV16, sv = tcj % C::NSV;
                 bool ok = mbar_wait_bounded(bar_v_full + 8 * sv, (tcj / C::NSV) & 1u, p.wait_ns);
-                // f16 buffer b was last read by PV(tcj - 2) (waited at every tile, in order)
-                if (ok && tcj >= 2) ok = mbar_wait_bounded(bar_pv_done + 8 * b, ((tcj - 2) >> 1) & 1u, p.wait_ns);
+                // f16 buffer b was last read by PV(tcj - NV16) (waited at every tile, in order; the
+                // barrier's next phase needs PV(tcj - NV16 + NSP), after this warp's rows of tile tcj)
+                if (ok && tcj >= (uint32_t)C::NV16)
+                    ok = mbar_wait_bounded(bar_pv_done + 8 * ((tcj - C::NV16) % C::NSP), ((tcj - C::NV16) / C::NSP) & 1u,
+                                           p.wait_ns);
                 if (!__all_sync(0xffffffffu, ok)) {
                     abort = true;
                     break;
@@ -534,10 +559,11 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW, D>::NTHREADS, 1)
             }
             tc_fence_after();
             for (int j = 0; j < T; ++j) {
-                const uint32_t tcj = tc + j, b = tcj & 1u, sk = tcj % C::NSK;
-                // K landed, and the S and P buffers b are free: PV(tcj - 2) is done
+                const uint32_t tcj = tc + j, b = tcj % C::NSP, sk = tcj % C::NSK;
+                // K landed, and S/P buffer b is free: PV(tcj - NSP) is done
                 bool ok = mbar_wait_bounded(bar_k_full + 8 * sk, (tcj / C::NSK) & 1u, p.wait_ns);
-                if (ok && tcj >= 2) ok = mbar_wait_bounded(bar_pv_done + 8 * b, ((tcj - 2) >> 1) & 1u, p.wait_ns);
+                if (ok && tcj >= (uint32_t)C::NSP)
+                    ok = mbar_wait_bounded(bar_pv_done + 8 * b, (tcj / C::NSP - 1) & 1u, p.wait_ns);
                 if (!__all_sync(0xffffffffu, ok)) {
                     abort = true;
                     break;
@@ -588,10 +614,10 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW, D>::NTHREADS, 1)
             if (!real(it)) continue;
             const int T = it.n_stages;
             for (int j = 0; j < T; ++j) {
-                const uint32_t tcj = tc + j, b = tcj & 1u;
+                const uint32_t tcj = tc + j, b = tcj % C::NSP, b16 = tcj % C::NV16;
                 // P_j written, V_j converted, and at an item's first tile the previous item's O read out
-                bool ok = mbar_wait_bounded(bar_p_full + 8 * b, (tcj >> 1) & 1u, p.wait_ns);
-                if (ok) ok = mbar_wait_bounded(bar_v16_full + 8 * b, (tcj >> 1) & 1u, p.wait_ns);
+                bool ok = mbar_wait_bounded(bar_p_full + 8 * b, (tcj / C::NSP) & 1u, p.wait_ns);
+                if (ok) ok = mbar_wait_bounded(bar_v16_full + 8 * b16, (tcj / C::NV16) & 1u, p.wait_ns);
                 if (ok && j == 0 && ic >= 1) ok = mbar_wait_bounded(bar_o_free, (ic - 1) & 1u, p.wait_ns);
                 if (!__all_sync(0xffffffffu, ok)) {
                     abort = true;
@@ -599,10 +625,10 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW, D>::NTHREADS, 1)
                 }
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t vb = base + C::OFF_V16 + b * C::V16_BYTES;
+                    const uint32_t vb = base + C::OFF_V16 + b16 * C::V16_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < C::BK / 16; ++kk)
-                        tc_mma_ts(t_o, t_p + (C::BK / 2) * b + kk * 8, umma_desc_sw128(vb + kk * 16 * 128, C::ATOM, 1024),
+                        tc_mma_ts(t_o, t_p + C::P_STRIDE * b + kk * 8, umma_desc_sw128(vb + kk * 16 * 128, C::ATOM, 1024),
                                   idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(bar_pv_done + 8 * b);
                     issued = true;
@@ -626,13 +652,13 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW, D>::NTHREADS, 1)
         const int t = threadIdx.x;                              // 0 .. 127
         float* const ml = reinterpret_cast<float*>(smem + C::OFF_ML);
         uint8_t* const scr = smem + C::OFF_SCR;
-        // this quarter's lanes of both P buffers hold zeros outside its own 16 columns
-        {
+        if constexpr (!C::P_OVER_S) {
+            // this quarter's lanes of the P buffers hold zeros outside its own columns for good
             uint32_t z[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) z[e] = 0u;
 #pragma unroll
-            for (int q = 0; q < C::BK / 32; ++q) tmem_st32(t_p + lane_off + 32 * q, z);
+            for (int q = 0; q < C::NSP * C::BK / 64; ++q) tmem_st32(t_p + lane_off + 32 * q, z);
             tmem_wait_st();
         }
         uint32_t tc = 0, ic = 0;
@@ -716,10 +742,10 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW, D>::NTHREADS, 1)
             const int lp = (p.page_size == 16) ? 4 : 5;
             float m_run = -CUDART_INF_F, l_run = 0.f;
             for (int j = 0; j < T; ++j) {
-                const uint32_t tcj = tc + j, b = tcj & 1u, sk = tcj % C::NSK;
+                const uint32_t tcj = tc + j, b = tcj % C::NSP, sk = tcj % C::NSK;
                 // S_j landed, and the K stage's scales are visible (QK waited for its K-full
                 // phase); the stage is released after the reads
-                bool ok = mbar_wait_bounded(bar_s_full + 8 * b, (tcj >> 1) & 1u, p.wait_ns);
+                bool ok = mbar_wait_bounded(bar_s_full + 8 * b, (tcj / C::NSP) & 1u, p.wait_ns);
                 if (ok) ok = mbar_wait_bounded(bar_k_full + 8 * sk, (tcj / C::NSK) & 1u, p.wait_ns);
                 if (!__all_sync(0xffffffffu, ok)) {
                     abort = true;
@@ -782,7 +808,8 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW, D>::NTHREADS, 1)
                 }
                 if (__any_sync(0xffffffffu, need)) {
                     const uint32_t tp = tcj - 1;   // the previous tile's PV
-                    const bool okw = j == 0 || mbar_wait_bounded(bar_pv_done + 8 * (tp & 1u), (tp >> 1) & 1u, p.wait_ns);
+                    const bool okw =
+                        j == 0 || mbar_wait_bounded(bar_pv_done + 8 * (tp % C::NSP), (tp / C::NSP) & 1u, p.wait_ns);
                     if (!__all_sync(0xffffffffu, okw)) {
                         abort = true;
                         break;
@@ -812,7 +839,22 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW, D>::NTHREADS, 1)
                     pk[e] = pack_f16x2(p0 * vf[e / 8], p1 * vf[e / 8]);
                 }
 #undef X
-                tmem_st_cols<KW / 2>(t_p + (C::BK / 2) * b + (KW / 2) * w + lane_off, pk);
+                // this quarter's KW/2 columns of P buffer b; over S, zeros over the other
+                // quarters' columns too (in these lanes PV must see only this quarter's keys,
+                // and the S values there are not this warp's)
+                const uint32_t pb = t_p + C::P_STRIDE * b + lane_off;
+                if constexpr (C::P_OVER_S) {
+                    uint32_t zk[KW / 2];
+#pragma unroll
+                    for (int e = 0; e < KW / 2; ++e) zk[e] = 0u;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if (q == w) tmem_st_cols<KW / 2>(pb + (KW / 2) * q, pk);
+                        else tmem_st_cols<KW / 2>(pb + (KW / 2) * q, zk);
+                    }
+                } else {
+                    tmem_st_cols<KW / 2>(pb + (KW / 2) * w, pk);
+                }
                 l_run += ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
                 tmem_wait_st();
                 tc_fence_before();
@@ -829,7 +871,7 @@ __global__ void __launch_bounds__(SplitTcCfg<FEW, D>::NTHREADS, 1)
             }
             // ---- epilogue: the four quarters' (max, sum, O) of row r, merged in warp order
             const uint32_t tcl = tc + T - 1;
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar_pv_done + 8 * (tcl & 1u), (tcl >> 1) & 1u, p.wait_ns)))
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar_pv_done + 8 * (tcl % C::NSP), (tcl / C::NSP) & 1u, p.wait_ns)))
                 abort = true;
             tc_fence_after();
             if (named_barrier_or(1, 128, abort)) {   // all four warps leave together
