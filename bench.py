@@ -65,8 +65,8 @@ NCU_TRAFFIC: dict[str, dict] = {
     "hybrid_decode": {"bytes_per_launch": 2295690616, "sources": _BF16_SPLIT_SOURCES,
                       "src_sha256": "2591a1ef194cda6ae803afc73ec243c3d1c532def3f65fd852c6150f82c128ae",
                       "capture": "32 sequences, scaled by the KV bytes (x 3.8372)"},
-    "spec_verify": {"bytes_per_launch": 1257676136, "sources": _E4M3_SPLIT_SOURCES,
-                    "src_sha256": "4c0f6fcfcee9aed2bd0d861f40ef316a867b5057ada75049bb9b58e176c66674",
+    "spec_verify": {"bytes_per_launch": 1258556079, "sources": _E4M3_SPLIT_SOURCES,
+                    "src_sha256": "a59cd6e2290df41d6aad337ae09b6d415e4a20c4ccc9f34f9184817e546dec52",
                     "capture": "16 sequences, scaled by the KV bytes (x 4.4698)"},
     "tiny_decode": {"bytes_per_launch": 678656, "sources": _BF16_SPLIT_SOURCES,
                     "src_sha256": "2591a1ef194cda6ae803afc73ec243c3d1c532def3f65fd852c6150f82c128ae",
@@ -84,7 +84,7 @@ NCU_TRAFFIC: dict[str, dict] = {
                                "src_sha256": "91969330d3e5a1f06cb0f12de2a7ff367c10331433416f468f4766f39a6be35a",
                                "capture": "the whole workload (K/V re-reads served by L2)"},
     "hybrid_decode_fp8": {"bytes_per_launch": 1368382346, "sources": _E4M3_SPLIT_SOURCES,
-                          "src_sha256": "4c0f6fcfcee9aed2bd0d861f40ef316a867b5057ada75049bb9b58e176c66674",
+                          "src_sha256": "a59cd6e2290df41d6aad337ae09b6d415e4a20c4ccc9f34f9184817e546dec52",
                           "capture": "32 sequences, scaled by the KV bytes (x 4.1277)"},
 }
 
