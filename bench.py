@@ -46,10 +46,11 @@ METRIC = "paged-decode KV GB/s and seq-tokens/s (fraction of GB300 HBM peak) at 
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM traffic per launch of the dominant kernel plus the combine, from the
-# committed ncu captures (a capture of fewer sequences scaled by the KV bytes
-# where the workload is too large to capture), valid only while the sources
-# that kernel is built from hash to `src_sha256`.
+# DRAM traffic per launch of the dominant kernel plus the combine (and the
+# item-order kernel where the call runs one), from the committed ncu captures
+# (a capture of fewer sequences scaled by the KV bytes where the workload is
+# too large to capture), valid only while the sources that kernel is built
+# from hash to `src_sha256`.
 _BF16_SPLIT_SOURCES = ("split_bf16_tc05.cuh", "sched.cuh", "attn_tile.cuh", "tc05.cuh", "ptx.cuh", "combine.cuh",
                        "launch.cuh", "tile_configs.cuh", "kern_split_bf16_tc05.cu", "kern_split_bf16_tc05_d256.cu")
 _E4M3_SPLIT_SOURCES = ("split_tc05.cuh", "sched.cuh", "attn_tile.cuh", "tc05.cuh", "ptx.cuh", "combine.cuh",
@@ -59,32 +60,32 @@ _BF16_PREFILL_SOURCES = ("prefill_pair.cuh", "prefill_tc05.cuh", "attn_tile.cuh"
 _FP8_PREFILL_SOURCES = ("prefill_fp8.cuh", "prefill_tc05.cuh", "sched.cuh", "attn_tile.cuh", "tc05.cuh", "ptx.cuh",
                         "tile_configs.cuh", "kern_prefill_fp8.cu", "kern_prefill_fp8_d256.cu")
 NCU_TRAFFIC: dict[str, dict] = {
-    "batched_decode": {"bytes_per_launch": 4532795290, "sources": _BF16_SPLIT_SOURCES,
-                       "src_sha256": "2591a1ef194cda6ae803afc73ec243c3d1c532def3f65fd852c6150f82c128ae",
+    "batched_decode": {"bytes_per_launch": 4522011744, "sources": _BF16_SPLIT_SOURCES,
+                       "src_sha256": "e90b9726308599e2c550ac2673f8ca8c6b4376b66744c06b9fee0ad47c61cac3",
                        "capture": "64 sequences, scaled by the KV bytes (x 4.3412)"},
-    "hybrid_decode": {"bytes_per_launch": 2295690616, "sources": _BF16_SPLIT_SOURCES,
-                      "src_sha256": "2591a1ef194cda6ae803afc73ec243c3d1c532def3f65fd852c6150f82c128ae",
+    "hybrid_decode": {"bytes_per_launch": 2284209889, "sources": _BF16_SPLIT_SOURCES,
+                      "src_sha256": "e90b9726308599e2c550ac2673f8ca8c6b4376b66744c06b9fee0ad47c61cac3",
                       "capture": "32 sequences, scaled by the KV bytes (x 3.8372)"},
-    "spec_verify": {"bytes_per_launch": 1258556079, "sources": _E4M3_SPLIT_SOURCES,
-                    "src_sha256": "a59cd6e2290df41d6aad337ae09b6d415e4a20c4ccc9f34f9184817e546dec52",
+    "spec_verify": {"bytes_per_launch": 1246796429, "sources": _E4M3_SPLIT_SOURCES,
+                    "src_sha256": "e16553d6d950ffcc996177c15ec91ee9327eb36a0f8b973fefee5c28be3c952c",
                     "capture": "16 sequences, scaled by the KV bytes (x 4.4698)"},
-    "tiny_decode": {"bytes_per_launch": 678656, "sources": _BF16_SPLIT_SOURCES,
-                    "src_sha256": "2591a1ef194cda6ae803afc73ec243c3d1c532def3f65fd852c6150f82c128ae",
+    "tiny_decode": {"bytes_per_launch": 679168, "sources": _BF16_SPLIT_SOURCES,
+                    "src_sha256": "e90b9726308599e2c550ac2673f8ca8c6b4376b66744c06b9fee0ad47c61cac3",
                     "capture": "the whole workload"},
     "prefill_chunk": {"bytes_per_launch": 51_253_760, "sources": _BF16_PREFILL_SOURCES,
-                      "src_sha256": "3e65bd4c84f1bcda581e9df5f504243f65e08d9fb7545d79b1c3e7189279f967",
+                      "src_sha256": "c8486b490e146bf5cc9cf675cb49b485f11b6a5be0116df2fb05e21946855e8f",
                       "capture": "the whole workload (K/V re-reads served by L2)"},
     "prefill_chunk_fp8": {"bytes_per_launch": 33_652_224, "sources": _FP8_PREFILL_SOURCES,
-                          "src_sha256": "91969330d3e5a1f06cb0f12de2a7ff367c10331433416f468f4766f39a6be35a",
+                          "src_sha256": "c0bb9bae586e70b64535be04a707278e26fb960bdfe460cb0aadd4b4776e1afb",
                           "capture": "the whole workload (K/V re-reads served by L2)"},
     "prefill_chunk_d256": {"bytes_per_launch": 33_628_928, "sources": _BF16_PREFILL_SOURCES,
-                           "src_sha256": "3e65bd4c84f1bcda581e9df5f504243f65e08d9fb7545d79b1c3e7189279f967",
+                           "src_sha256": "c8486b490e146bf5cc9cf675cb49b485f11b6a5be0116df2fb05e21946855e8f",
                            "capture": "the whole workload (K/V re-reads served by L2)"},
     "prefill_chunk_d256_fp8": {"bytes_per_launch": 25_282_048, "sources": _FP8_PREFILL_SOURCES,
-                               "src_sha256": "91969330d3e5a1f06cb0f12de2a7ff367c10331433416f468f4766f39a6be35a",
+                               "src_sha256": "c0bb9bae586e70b64535be04a707278e26fb960bdfe460cb0aadd4b4776e1afb",
                                "capture": "the whole workload (K/V re-reads served by L2)"},
-    "hybrid_decode_fp8": {"bytes_per_launch": 1368382346, "sources": _E4M3_SPLIT_SOURCES,
-                          "src_sha256": "a59cd6e2290df41d6aad337ae09b6d415e4a20c4ccc9f34f9184817e546dec52",
+    "hybrid_decode_fp8": {"bytes_per_launch": 1355983132, "sources": _E4M3_SPLIT_SOURCES,
+                          "src_sha256": "e16553d6d950ffcc996177c15ec91ee9327eb36a0f8b973fefee5c28be3c952c",
                           "capture": "32 sequences, scaled by the KV bytes (x 4.1277)"},
 }
 

@@ -85,6 +85,10 @@ constexpr int kFaultSkipFirstKTile = 1;
 #endif
 constexpr float kLazyRescaleLog2 = RAD_LAZY_RESCALE_LOG2;
 
+// The most sequences of a call whose split items are sorted heaviest first
+// (sched.cuh: their lengths are staged in shared memory).
+constexpr int kOrderMaxGroups = 8192;
+
 struct AttnParams {
     const __nv_bfloat16* q;
     const uint8_t* k_pool;
@@ -117,6 +121,8 @@ struct AttnParams {
     uint64_t wait_ns;      // limit of each bounded wait (kWaitLimitNs unless a test lowers it)
     int fault;             // kFaultNone, or a test's injected fault
     uint32_t* sched_ctr;   // tcgen05 split kernels: the shared item counter (zero at launch), or null
+    int32_t* item_order;   // tcgen05 split kernels: (split, sequence) pairs heaviest first (sched.cuh), or null
+                           // (uniform calls of at most kOrderMaxGroups sequences)
 };
 
 // First key that query row r of a call with `rows` rows over a sequence of

@@ -156,6 +156,9 @@ Plan make_plan(int32_t groups, int32_t rows, int32_t n_head, int32_t n_head_kv, 
     if (pl.family == rad::kFamSplitBf || pl.family == rad::kFamSplitTC ||
         (pl.family == rad::kFamPrefillTC && kv_dtype == RAD_KV_FP8_E4M3))
         pl.sched_bytes = 256;
+    // the split kernels' items heaviest first: one int32 an item after the counter
+    if (RAD_ITEM_ORDER && (pl.family == rad::kFamSplitBf || pl.family == rad::kFamSplitTC))
+        pl.sched_bytes += round_up((size_t)pl.n_items * 4, 256);
     pl.total_bytes = pl.sched_bytes + pl.map_bytes + pl.flags_bytes + pl.ml_bytes + pl.acc_bytes;
     pl.dual = pl.ragged && (pl.family == rad::kFamVerify || pl.family == rad::kFamWide);
     if (pl.dual) {
@@ -426,9 +429,19 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
     AttnParams pd = p;
     // a kernel with more items than CTAs takes them from a shared counter
     const bool dynamic = RAD_SPLIT_DYNAMIC && pl.sched_bytes > 0 && pl.n_items > sms;
+    // ... heaviest first, sorted by an order kernel that also zeroes the counter
+    // (uniform calls: the order kernel weighs items by the sequence lengths alone).  Measured
+    // same box: the e4m3 kernel gains at both head dims (64 x 8 verify -3 %, 24-sequence decode
+    // -10 %) and so does the head_dim-256 bf16 build (-3 %), whose one O buffer makes item
+    // boundaries dear; the head_dim-128 bf16 build, with two O buffers, lost ~2 %.  With at
+    // most two items per CTA there is no tail to even out, and the order kernel only costs.
+    const bool ordered = dynamic && RAD_ITEM_ORDER && !pl.ragged && !cu_seqlens &&
+                         groups <= rad::kOrderMaxGroups && pl.n_items > 2LL * sms &&
+                         (pl.family == rad::kFamSplitTC || (pl.family == rad::kFamSplitBf && head_dim == 256));
     if (pl.total_bytes > 0) {
         char* ws = static_cast<char*>(workspace);
         if (dynamic) p.sched_ctr = reinterpret_cast<uint32_t*>(ws);
+        if (ordered) p.item_order = reinterpret_cast<int32_t*>(ws + 256);
         ws += pl.sched_bytes;
         if (pl.ragged) p.tile_map = reinterpret_cast<const int2*>(ws);
         ws += pl.map_bytes;
@@ -455,7 +468,7 @@ int attn_paged_impl(const void* q, const void* k_pool, const void* v_pool, const
         }
     }
     cudaError_t e;
-    if (dynamic && cudaMemsetAsync(p.sched_ctr, 0, sizeof(uint32_t), st) != cudaSuccess) return RAD_E_CUDA;
+    if (dynamic && !ordered && cudaMemsetAsync(p.sched_ctr, 0, sizeof(uint32_t), st) != cudaSuccess) return RAD_E_CUDA;
     if (pl.ragged) {
         // the tile lists of the call's sequence classes, on the device
         rad::RaggedMaps m{};

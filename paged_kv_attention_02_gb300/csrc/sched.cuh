@@ -13,6 +13,15 @@
 // CTA runs an item does not change the item's arithmetic, so every output bit
 // is the same either way.
 //
+// The split kernels of uniform calls take their items heaviest first:
+// item_order_kernel, run just before them, sorts the (split, sequence) pairs
+// by the keys of the split (most first) into AttnParams::item_order, and the
+// fetch maps position c to item c % (KV heads x query tiles) of pair
+// item_order[c / (KV heads x query tiles)] (skipping inactive ones as before).
+// Taken in split order instead, the last items handed out were random-length
+// last splits of the longest sequences, and the CTAs that drew long ones set
+// the kernel's end.
+//
 // Barriers per ring slot: full (the scheduler's write), empty (every consumer
 // warp has read it) and taken (the first consumer, the K producer, has read
 // it).  A kernel with a scheduler warp (run) fetches entry m once entry
@@ -95,6 +104,14 @@ struct ItemRing {
             }
             cur.first = false;
             if (cand >= (unsigned)p.n_items) return -1;
+            if (p.item_order) {
+                // position cand: item j of the k-th heaviest (split, sequence) pair
+                const unsigned per_g = (unsigned)(p.n_head_kv * p.n_qtiles);
+                const unsigned k = cand / per_g, j = cand - k * per_g;
+                const unsigned pr = (unsigned)__ldg(p.item_order + k);
+                const unsigned sp = pr / (unsigned)p.groups, g = pr - sp * (unsigned)p.groups;
+                cand = sp * (unsigned)p.groups * per_g + g * per_g + j;
+            }
             if (keep((int)cand)) return (int)cand;
         }
         return -1;
@@ -135,5 +152,75 @@ struct ItemRing {
         }
     }
 };
+
+constexpr int kOrderThreads = 1024;
+constexpr int kOrderBuckets = 64;   // by key tiles: 0 .. 62, and 63 or more
+
+// One CTA, in the stream just before a split kernel of a uniform call (no row
+// offsets, no tile map): zeroes the shared item counter and sorts the call's
+// (split s, sequence g) pairs heaviest first into p.item_order, as pair ids
+// s * groups + g.  A pair's weight is the keys of its split: min(split_len,
+// L - s split_len) for a sequence of L keys (0 past its last split), in
+// buckets of KS keys; pairs of one bucket come in no particular order.  The
+// fetch hands out each pair's items (its KV heads and query tiles) one after
+// another, as the split order did, so items reading the same pages still run
+// side by side; it still skips inactive items, so the set of items run is the
+// same in any order.  The lengths are staged in shared memory and each warp
+// makes one shared atomic per bucket its pairs fall in.
+template <class C>
+__global__ void __launch_bounds__(kOrderThreads) item_order_kernel(const __grid_constant__ AttnParams p) {
+    __shared__ uint32_t at[kOrderBuckets];   // counts, then each bucket's next position
+    __shared__ int lens[kOrderMaxGroups];
+    const int tid = threadIdx.x, lane = tid & 31;
+    if (tid < kOrderBuckets) at[tid] = 0u;
+    for (int g = tid; g < p.groups; g += kOrderThreads) lens[g] = __ldg(p.seq_lens + g);
+    __syncthreads();
+    const int n_pairs = p.max_splits * p.groups;
+    // bucket 0 holds the heaviest pairs; -1: past the last pair
+    const auto bucket_of = [&](int pr) {
+        if (pr >= n_pairs) return -1;
+        const int sp = pr / p.groups, g = pr - sp * p.groups;
+        const int keys = min(p.split_len, max(0, lens[g] - sp * p.split_len));
+        return kOrderBuckets - 1 - min((keys + C::KS - 1) / C::KS, kOrderBuckets - 1);
+    };
+    for (int i0 = 0; i0 < n_pairs; i0 += kOrderThreads) {
+        const int b = bucket_of(i0 + tid);
+        const unsigned peers = __match_any_sync(0xffffffffu, b);
+        if (b >= 0 && lane == __ffs(peers) - 1) atomicAdd(&at[b], (uint32_t)__popc(peers));
+    }
+    __syncthreads();
+    if (tid == 0) {
+        uint32_t sum = 0;
+        for (int b = 0; b < kOrderBuckets; ++b) {
+            const uint32_t n = at[b];
+            at[b] = sum;
+            sum += n;
+        }
+        p.sched_ctr[0] = 0u;
+    }
+    __syncthreads();
+    for (int i0 = 0; i0 < n_pairs; i0 += kOrderThreads) {
+        const int pr = i0 + tid;
+        const int b = bucket_of(pr);
+        const unsigned peers = __match_any_sync(0xffffffffu, b);
+        const int leader = __ffs(peers) - 1;
+        uint32_t pos = 0;
+        if (b >= 0 && lane == leader) pos = atomicAdd(&at[b], (uint32_t)__popc(peers));
+        pos = __shfl_sync(0xffffffffu, pos, leader);
+        if (b >= 0) p.item_order[pos + __popc(peers & ((1u << lane) - 1u))] = pr;
+    }
+}
+
+// The order kernel of a split kernel's launch (C: its config, for KS).
+template <class C>
+cudaError_t launch_item_order(const AttnParams& p, cudaStream_t st) {
+    if (!p.item_order) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, 1);
+    cfg.blockDim = dim3(kOrderThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    return cudaLaunchKernelEx(&cfg, item_order_kernel<C>, p);
+}
 
 }  // namespace rad

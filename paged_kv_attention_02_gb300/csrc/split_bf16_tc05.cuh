@@ -849,7 +849,9 @@ cudaError_t launch_split_bf16_form(const CUtensorMap& tk, const CUtensorMap& tv,
     auto kern = p.window > 0  ? attn_split_bf16_tc05_kernel<kModeWindow, FEW, D>
                 : p.tree_mask ? attn_split_bf16_tc05_kernel<kModeTree, FEW, D>
                               : attn_split_bf16_tc05_kernel<kModeCausal, FEW, D>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    cudaError_t e = launch_item_order<C>(p, st);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     long long grid = sms;
     if (grid > p.n_items) grid = p.n_items;

@@ -53,16 +53,17 @@
 //                shared memory.  At the start they pull the call's query rows
 //                into L2: behind the K/V stream a row load from HBM at an item
 //                boundary took ~3 us.
-// TMEM holds O and NSP S/P buffers: the decode form two S buffers and two P
-// buffers of their own (a quarter's lanes zero outside its columns for good),
-// the verify form three S buffers with P written over the first half of its S
-// (zeros over the other quarters' columns at every tile).  PV of tile t
-// completes a phase of pv_done[t % NSP]; a thread that has seen S(t) knows
-// PV(t-NSP) is done (QK(t) waited for it), and every wait on pv_done is for a
-// PV whose barrier cannot complete again before the waiter itself has acted
-// (see prefill_tc05.cuh); the converters wait for PV(t-NV16) at every tile, in
-// order, before they write f16 buffer t % NV16.  Every wait is bounded; a time-out sets
-// RAD_ERRW_TIMEOUT and the roles unwind.
+// TMEM holds O and NSP S/P buffers: the decode form and the head_dim-256 build
+// two S buffers and two P buffers of their own (a quarter's lanes zero outside
+// its columns for good), the head_dim-128 verify form three S buffers with P
+// written over the first half of its S (zeros over the other quarters' columns
+// at every tile).  PV of tile t completes a phase of pv_done[t % NSP]; a thread
+// that has seen S(t) knows PV(t-NSP) is done (QK(t) waited for it), and every
+// wait on pv_done is for a PV whose barrier cannot complete again before the
+// waiter itself has acted (see prefill_tc05.cuh); the converters wait for
+// PV(t-NV16) at every tile, in order, before they write f16 buffer t % NV16.
+// Every wait is bounded; a time-out sets RAD_ERRW_TIMEOUT and the roles
+// unwind.
 #pragma once
 #include <cuda.h>
 
@@ -85,7 +86,8 @@
 #endif
 // S/P buffers in TMEM (QK of tile t waits for PV of tile t - NSP) and f16 V
 // buffers (the converters' rows of tile t wait for PV of tile t - NV16) of the
-// head_dim-128 verify form; the decode form keeps two and two.
+// head_dim-128 verify form; the decode form and the head_dim-256 build (one
+// form for decode and verify calls) keep two and two.
 #ifndef RAD_SPLITTC_NSP
 #define RAD_SPLITTC_NSP 3
 #endif
@@ -125,7 +127,7 @@ struct SplitTcCfg {
                                         : RAD_SPLITTC256_NSK;   // K stages (with the page scales)
     static constexpr int NSV = D == 128 ? (FEW ? RAD_SPLITTC_FEW_NSV : RAD_SPLITTC_NSV)
                                         : RAD_SPLITTC256_NSV;   // V stages
-    static constexpr int NSP = FEW ? 2 : RAD_SPLITTC_NSP;   // S/P buffers in TMEM
+    static constexpr int NSP = (FEW || D != 128) ? 2 : RAD_SPLITTC_NSP;   // S/P buffers in TMEM
     static constexpr bool P_OVER_S = NSP > 2;       // three S buffers leave no columns for P buffers of its own
     static constexpr int P_STRIDE = P_OVER_S ? BK : BK / 2;   // TMEM columns from P buffer b to b + 1
     static constexpr int NV16 = (FEW || D != 128) ? 2 : RAD_SPLITTC_NV16;   // f16 V buffers
@@ -984,7 +986,9 @@ cudaError_t launch_split_tc05_form(const CUtensorMap& tk, const CUtensorMap& tv,
     auto kern = p.window > 0  ? attn_split_tc05_kernel<kModeWindow, FEW, D>
                 : p.tree_mask ? attn_split_tc05_kernel<kModeTree, FEW, D>
                               : attn_split_tc05_kernel<kModeCausal, FEW, D>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    cudaError_t e = launch_item_order<C>(p, st);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     long long grid = sms;
     if (grid > p.n_items) grid = p.n_items;

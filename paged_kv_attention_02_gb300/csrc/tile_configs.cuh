@@ -74,6 +74,11 @@ constexpr int kSplitMaxRows = 256;
 #ifndef RAD_SPLIT_DYNAMIC
 #define RAD_SPLIT_DYNAMIC 1
 #endif
+// ... heaviest first (an order kernel sorts the items by key tiles before
+// the split kernel runs); 0 hands them out in split order.
+#ifndef RAD_ITEM_ORDER
+#define RAD_ITEM_ORDER 1
+#endif
 
 // Tile shapes: WQ, NQW, WK, KS, NS, CTAs per SM (see TileCfg).  Each can be
 // overridden at compile time (-DRAD_TILE_...="...") for tuning sweeps.
