@@ -644,14 +644,23 @@ def describe(w) -> str:
 def launches_per_step(w) -> int:
     """Kernels one call launches: the attention kernel, plus the split combine
     when a sequence of the call's capacity can span more than one split, plus
-    the tile map of a ragged call."""
+    the tile map of a ragged call, plus the item-order kernel of a split call
+    that runs one (a uniform call with more than two items per SM)."""
+    import torch
     c = w.cfg
     desc = describe(w)
     kernels = (desc.count("attn_tile family") + desc.count("attn_split_tc05 ") + desc.count("attn_split_bf16_tc05 ")
                + desc.count("attn_prefill_tc05 "))
     split_len = int(desc.split("split_len=")[1].split()[0])
     combines = desc.count("attn_combine") if split_len > 0 and w.pages_per_seq * c.page_size > split_len else 0
-    return kernels + combines + int("ragged_tile_map" in desc)
+    order = 0
+    if "item_order" in desc:
+        m = c.rows * (c.n_head // c.n_head_kv)
+        qt = int(desc.split("tile_rows=")[1].split()[0])
+        n_items = w.groups * c.n_head_kv * (-(-m // qt)) * (-(-(w.pages_per_seq * c.page_size) // split_len))
+        sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 152
+        order = int(n_items > 2 * sms)
+    return kernels + combines + order + int("ragged_tile_map" in desc)
 
 
 def main():

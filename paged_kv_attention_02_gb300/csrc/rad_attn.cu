@@ -568,8 +568,9 @@ int describe_call(int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_
                  "each)+1 qk+1 pv+2 tma producers+4 v converters mma=tcgen05 (query rows as M, four copies; keys "
                  "as N; QK kind::f8f6f4 on the staged e4m3 K with Q as two e4m3 terms, PV kind::f16 with P from "
                  "TMEM and V e4m3 -> f16 once per tile) "
-                 "split_len=%d + attn_combine (split order)",
-                 pre, family_name(pl.family), head_dim, pl.M, t.QT, t.KS, t.NS, pl.split_len);
+                 "split_len=%d + attn_combine (split order)%s",
+                 pre, family_name(pl.family), head_dim, pl.M, t.QT, t.KS, t.NS, pl.split_len,
+                 ragged ? "" : "; uniform calls of more than two items per CTA first run item_order (one CTA)");
         return RAD_OK;
     }
     if (pl.family == rad::kFamSplitBf) {
@@ -578,9 +579,12 @@ int describe_call(int32_t rows, int32_t n_head, int32_t n_head_kv, int32_t head_
                  "keys_per_tile=%d stages=%d ctas_per_sm=1 warps=13 4 softmax (a quarter of each tile's keys "
                  "each)+1 qk+1 pv+2 tma producers+1 query rows+4 epilogue (%s) mma=tcgen05 (query rows as M, four copies; keys as "
                  "N; QK kind::f16 bf16, PV kind::f16 with P from TMEM as bf16 hi+lo over S) "
-                 "split_len=%d + attn_combine (split order)",
+                 "split_len=%d + attn_combine (split order)%s",
                  pre, family_name(pl.family), head_dim, pl.M, t.QT, t.KS, t.NS,
-                 head_dim == 128 ? "two O buffers" : "one O buffer", pl.split_len);
+                 head_dim == 128 ? "two O buffers" : "one O buffer", pl.split_len,
+                 (head_dim == 256 && !ragged)
+                     ? "; uniform calls of more than two items per CTA first run item_order (one CTA)"
+                     : "");
         return RAD_OK;
     }
     if (pl.family == rad::kFamPrefillTC && kv_dtype == RAD_KV_FP8_E4M3) {
