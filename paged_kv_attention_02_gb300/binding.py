@@ -120,7 +120,7 @@ def workspace_bytes(groups, rows, n_head, n_head_kv, head_dim, page_size, pages_
 
 
 def describe(rows, n_head, n_head_kv, head_dim, page_size, kv_dtype=RAD_KV_BF16) -> str:
-    buf = ctypes.create_string_buffer(512)
+    buf = ctypes.create_string_buffer(2048)
     rc = load().rad_attn_paged_describe(rows, n_head, n_head_kv, head_dim, page_size, kv_dtype, buf,
                                         len(buf))
     if rc != RAD_OK:

@@ -61,6 +61,14 @@ MID = {
                                      "fixed:900", pages_per_seq=30),
     "prefill_fp8_d256_2g": wl.Config("prefill_fp8_d256_2g", 2, 300, 16, 2, 256, 32, wl.KV_FP8_E4M3, 121,
                                      "fixed:300,1500", pages_per_seq=60),
+    # uniform split calls with more than two items per SM: the e4m3 kernel and the head_dim-256
+    # bf16 build take their items heaviest first (an order kernel sorts them before the launch)
+    "ver_fp8_ordered": wl.Config("ver_fp8_ordered", 16, 8, 32, 8, 128, 16, wl.KV_FP8_E4M3, 122,
+                                 "uniform:8,6000", pages_per_seq=600),
+    "dec_d256_ordered": wl.Config("dec_d256_ordered", 48, 1, 16, 2, 256, 32, wl.KV_BF16, 123,
+                                  "loguniform:1,12000", pages_per_seq=400, meta=dict(head_dim=256, n_embd=3408)),
+    "dec_fp8_d256_ordered": wl.Config("dec_fp8_d256_ordered", 48, 1, 16, 2, 256, 32, wl.KV_FP8_E4M3, 124,
+                                      "loguniform:1,12000", pages_per_seq=400),
 }
 
 
@@ -218,6 +226,23 @@ def test_prefill_rows_bit_identical_alone_and_batched(mid, name):
     out, _ = dw.run()
     o1, _ = dw.run(q=dw.q[1:2], table=dw.table[1:2], lens=dw.lens[1:2])
     assert np.array_equal(bits(o1)[0], bits(out)[1])
+
+
+@pytest.mark.parametrize("name", ["ver_fp8_ordered", "dec_d256_ordered", "dec_fp8_d256_ordered"])
+def test_heaviest_first_rows_equal_split_order_rows(mid, name):
+    # the full call (more than two items per SM) takes its items heaviest first; two of its
+    # sequences alone (a handful of items) take them in split order: same bits
+    w, dw = mid(name)
+    desc = b.describe(w.cfg.rows, w.cfg.n_head, w.cfg.n_head_kv, w.cfg.meta.get("head_dim", w.cfg.head_dim),
+                      w.cfg.page_size, w.cfg.kv_dtype)
+    assert "item_order" in desc
+    out, err = dw.run()
+    assert err == 0
+    base = bits(out)
+    for g in (int(np.argmax(w.seq_lens)), int(np.argmin(w.seq_lens))):
+        o, err = dw.run(q=dw.q[g:g + 1], table=dw.table[g:g + 1], lens=dw.lens[g:g + 1])
+        assert err == 0
+        assert np.array_equal(bits(o)[0], base[g]), f"group {g} alone"
 
 
 def test_repeated_calls_are_bit_identical(mid):
