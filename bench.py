@@ -61,31 +61,31 @@ _FP8_PREFILL_SOURCES = ("prefill_fp8.cuh", "prefill_tc05.cuh", "sched.cuh", "att
                         "tile_configs.cuh", "kern_prefill_fp8.cu", "kern_prefill_fp8_d256.cu")
 NCU_TRAFFIC: dict[str, dict] = {
     "batched_decode": {"bytes_per_launch": 4522011744, "sources": _BF16_SPLIT_SOURCES,
-                       "src_sha256": "e90b9726308599e2c550ac2673f8ca8c6b4376b66744c06b9fee0ad47c61cac3",
+                       "src_sha256": "8bed5860df4e7fd28ba80b09164f9fc677126ba6cd8fe4255139580dad95172c",
                        "capture": "64 sequences, scaled by the KV bytes (x 4.3412)"},
     "hybrid_decode": {"bytes_per_launch": 2284209889, "sources": _BF16_SPLIT_SOURCES,
-                      "src_sha256": "e90b9726308599e2c550ac2673f8ca8c6b4376b66744c06b9fee0ad47c61cac3",
+                      "src_sha256": "8bed5860df4e7fd28ba80b09164f9fc677126ba6cd8fe4255139580dad95172c",
                       "capture": "32 sequences, scaled by the KV bytes (x 3.8372)"},
     "spec_verify": {"bytes_per_launch": 1246796429, "sources": _E4M3_SPLIT_SOURCES,
-                    "src_sha256": "e16553d6d950ffcc996177c15ec91ee9327eb36a0f8b973fefee5c28be3c952c",
+                    "src_sha256": "905400cfdeb263ce7ff3e9ed8df80ba87a68170b8ccfcd213d85a184c767a7d2",
                     "capture": "16 sequences, scaled by the KV bytes (x 4.4698)"},
     "tiny_decode": {"bytes_per_launch": 679168, "sources": _BF16_SPLIT_SOURCES,
-                    "src_sha256": "e90b9726308599e2c550ac2673f8ca8c6b4376b66744c06b9fee0ad47c61cac3",
+                    "src_sha256": "8bed5860df4e7fd28ba80b09164f9fc677126ba6cd8fe4255139580dad95172c",
                     "capture": "the whole workload"},
     "prefill_chunk": {"bytes_per_launch": 51_253_760, "sources": _BF16_PREFILL_SOURCES,
                       "src_sha256": "c8486b490e146bf5cc9cf675cb49b485f11b6a5be0116df2fb05e21946855e8f",
                       "capture": "the whole workload (K/V re-reads served by L2)"},
     "prefill_chunk_fp8": {"bytes_per_launch": 33_652_224, "sources": _FP8_PREFILL_SOURCES,
-                          "src_sha256": "c0bb9bae586e70b64535be04a707278e26fb960bdfe460cb0aadd4b4776e1afb",
+                          "src_sha256": "bfdae5aaa1f5c0033858df83a8b67ba4fb4a94e94246b34d21d02d9d53ea2373",
                           "capture": "the whole workload (K/V re-reads served by L2)"},
     "prefill_chunk_d256": {"bytes_per_launch": 33_628_928, "sources": _BF16_PREFILL_SOURCES,
                            "src_sha256": "c8486b490e146bf5cc9cf675cb49b485f11b6a5be0116df2fb05e21946855e8f",
                            "capture": "the whole workload (K/V re-reads served by L2)"},
     "prefill_chunk_d256_fp8": {"bytes_per_launch": 25_282_048, "sources": _FP8_PREFILL_SOURCES,
-                               "src_sha256": "c0bb9bae586e70b64535be04a707278e26fb960bdfe460cb0aadd4b4776e1afb",
+                               "src_sha256": "bfdae5aaa1f5c0033858df83a8b67ba4fb4a94e94246b34d21d02d9d53ea2373",
                                "capture": "the whole workload (K/V re-reads served by L2)"},
     "hybrid_decode_fp8": {"bytes_per_launch": 1355983132, "sources": _E4M3_SPLIT_SOURCES,
-                          "src_sha256": "e16553d6d950ffcc996177c15ec91ee9327eb36a0f8b973fefee5c28be3c952c",
+                          "src_sha256": "905400cfdeb263ce7ff3e9ed8df80ba87a68170b8ccfcd213d85a184c767a7d2",
                           "capture": "32 sequences, scaled by the KV bytes (x 4.1277)"},
 }
 

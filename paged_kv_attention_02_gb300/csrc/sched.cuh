@@ -13,7 +13,9 @@
 // CTA runs an item does not change the item's arithmetic, so every output bit
 // is the same either way.
 //
-// The split kernels of uniform calls take their items heaviest first:
+// The e4m3 split kernel and the head_dim-256 bf16 build take the items of a
+// uniform call with more than two items per SM heaviest first (the host
+// decides; the head_dim-128 bf16 build measured slower so):
 // item_order_kernel, run just before them, sorts the (split, sequence) pairs
 // by the keys of the split (most first) into AttnParams::item_order, and the
 // fetch maps position c to item c % (KV heads x query tiles) of pair
