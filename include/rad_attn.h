@@ -124,11 +124,12 @@ enum {
  * Returns 0 as well for shapes rad_attn_paged would refuse.  The workspace
  * holds per-split partial results ("kern manifest v7", $defs.Impl `scratch`:
  * implementation-private buffers) and, for the tcgen05 split kernels and the
- * fp8 prefill kernel, a work counter that the call zeroes with a 4-byte
- * cudaMemsetAsync on its stream
- * before the kernel (stream-ordered, so it is captured with the call in a CUDA
- * graph).  It is dead between calls; calls that may run concurrently need
- * separate workspaces.
+ * fp8 prefill kernel, a work counter that the call zeroes on its stream before
+ * the kernel: a 4-byte cudaMemsetAsync, or, where the split kernel takes its
+ * items heaviest first, a one-CTA kernel that also writes the item order (one
+ * int32 an item, after the counter).  Both are stream-ordered, so they are
+ * captured with the call in a CUDA graph.  It is dead between calls; calls
+ * that may run concurrently need separate workspaces.
  */
 size_t rad_attn_paged_workspace_bytes(int32_t groups, int32_t rows, int32_t n_head,
                                       int32_t n_head_kv, int32_t head_dim, int32_t page_size,
