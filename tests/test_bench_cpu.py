@@ -54,3 +54,20 @@ def test_traffic_figures_name_existing_kernel_sources():
         for f in tr["sources"]:
             assert os.path.exists(os.path.join(csrc, f)), f
     assert bench.kernel_source_hash(["ptx.cuh"]) != bench.kernel_source_hash(["tc05.cuh"])
+
+
+def test_launches_per_step_counts_every_kernel_of_a_call():
+    # shape-only stand-ins (the real workloads hold GBs): the split kernel, its combine
+    # when a sequence can span splits, the order kernel of a sorted call, the tile map of
+    # a ragged one
+    def shape(name):
+        c = wl.CONFIGS[name]
+        return SimpleNamespace(cfg=c, groups=c.groups, pages_per_seq=c.pages_per_seq,
+                               ragged=c.q_lens is not None, tree_mask=object() if c.tree else None)
+    assert bench.launches_per_step(shape("tiny_decode")) == 1      # one split per sequence
+    assert bench.launches_per_step(shape("batched_decode")) == 2   # split order: kernel + combine
+    assert bench.launches_per_step(shape("spec_verify")) == 3      # + the order kernel
+    assert bench.launches_per_step(shape("tree_verify")) == 3
+    assert bench.launches_per_step(shape("hybrid_decode_fp8")) == 3
+    assert bench.launches_per_step(shape("mixed_step")) == 3       # tile map + kernel + combine
+    assert bench.launches_per_step(shape("prefill_chunk")) == 1

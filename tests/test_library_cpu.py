@@ -129,6 +129,18 @@ def test_describe_names_the_kernel_choice():
         b.describe(1, 32, 8, 96, 16)
 
 
+def test_describe_names_the_item_order_kernel_where_it_runs():
+    # uniform calls on the e4m3 split kernel (both head dims) and on the head_dim-256 bf16
+    # build sort their items heaviest first when they have more than two a CTA; the
+    # head_dim-128 bf16 build and ragged calls keep split order
+    assert "item_order" in b.describe(8, 32, 8, 128, 16, b.RAD_KV_FP8_E4M3)
+    assert "item_order" in b.describe(1, 16, 2, 256, 32, b.RAD_KV_FP8_E4M3)
+    if bf16_tc(256):
+        assert "item_order" in b.describe(1, 16, 2, 256, 32)
+    assert "item_order" not in b.describe(1, 32, 8, 128, 16)
+    assert "item_order" not in b.ex_describe(b.shape_args(4, 8, 32, 8, 128, 16, 64, b.RAD_KV_FP8_E4M3, ragged=True))
+
+
 def test_args_struct_matches_the_c_layout(tmp_path):
     """The binding's RadAttnPagedArgs mirror has the header's size and offsets."""
     fields = [f for f, _ in b.RadAttnPagedArgs._fields_]
